@@ -1,0 +1,321 @@
+"""Plain fp64 CPU oracle for the Focus inference hot path.
+
+TEST INFRASTRUCTURE ONLY.  Only the test suite, the package smoke check and
+the benchmark's CPU-baseline leg may import this module.  The product path
+(the CUDA library and its Python binding) never imports or calls it and shares
+no code with it.
+
+Sources (page titles and sections):
+  [FocusJA] "Focus: Learning Which Attention Pairs Matter" (gist.science, ja),
+            section 2.1 (architecture: centroids, local + group-gated far
+            attention), section 2.2 (inference: hard top-k assignment, far pairs
+            of different groups skipped, pair count O(n^2/K + n*w)),
+            section 3.3 (local window + in-group causal decomposition).
+  [FocusKO] "Why Attend to Everything? Focus is the Key" (gist.science, ko),
+            section 2.1 (exact softmax preserved), section 2.3 (hard top-k
+            assignment at inference, two FlashAttention calls).
+
+What the oracle computes (fp64 throughout, no blocking or fusion):
+  assign       p = W_a h (no bias), s_k = p . c_k, g = argmax_k s_k with the
+               lowest index winning ties.  The decision is taken on the scores
+               rounded to fp32 (the precision the hot path fixes for the
+               scores); the exact fp64 margin between the best and runner-up
+               score is returned as well.
+  build_index  counting sort of tokens by (group, position) per (batch,
+               assignment): counts, offsets, perm, rank, farlen, and the
+               group-pass work list for a tile height BM.
+  keep mask    pair (i, j) kept iff j <= i and (i - j < w or g_i == g_j).
+  attention    exact softmax over the kept pairs only, S = scale * Q K^T.
+
+Readings where the pages are silent (each listed in the design notes):
+  similarity = dot product; no projection bias; window strictly i - j < w;
+  scale = 1/sqrt(d) by default; GQA head map kv = floor(h * H_kv / H);
+  each kept pair counted once (union of the local and the group rule).
+
+Parity pins: every function here is checked by tests/test_oracle_pins.py
+against closed forms, brute force, special cases and invariants.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+__all__ = [
+    "assign", "build_index", "work_items", "lpt_order", "keep_mask_rows", "keep_mask",
+    "kept_counts", "attention", "attention_rows", "attention_masked_rows",
+    "dense_causal", "lse_merge", "attention_bruteforce", "attention_weights_rows",
+    "kv_head", "assignment_of_head",
+]
+
+
+# ---------------------------------------------------------------- helpers ---
+
+def kv_head(h: int, H: int, H_kv: int) -> int:
+    """Key/value head used by query head h: contiguous groups of H/H_kv heads."""
+    return (h * H_kv) // H
+
+
+def assignment_of_head(h: int, H: int, H_kv: int, A: int) -> int:
+    """Assignment index a used by query head h (A == 1: shared; A == H_kv: per kv head)."""
+    return 0 if A == 1 else kv_head(h, H, H_kv)
+
+
+def _f64(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+# ----------------------------------------------------------------- assign ---
+
+def assign(h, W, C, chunk: int = 4096):
+    """Nearest-centroid group ids.  [FocusJA] 2.1 (centroids, projection,
+    similarity), 2.2 and [FocusKO] 2.3 (hard assignment at inference).
+
+    h [B, n, D], W [A, d_g, D], C [A, K, d_g]  ->  gid [B, A, n] int32,
+    margin [B, A, n] fp64 (best minus runner-up score; +inf when K == 1).
+    """
+    h = np.asarray(h)
+    W = _f64(W)
+    C = _f64(C)
+    B, n, D = h.shape
+    A, d_g, D2 = W.shape
+    K = C.shape[1]
+    assert D2 == D and C.shape == (A, K, d_g)
+    gid = np.empty((B, A, n), dtype=np.int32)
+    margin = np.empty((B, A, n), dtype=np.float64)
+    for b in range(B):
+        for s in range(0, n, chunk):
+            hb = _f64(h[b, s:s + chunk])                  # [m, D]
+            for a in range(A):
+                p = hb @ W[a].T                           # projection, [m, d_g]
+                sc = p @ C[a].T                           # scores, [m, K]
+                sc32 = sc.astype(np.float32)              # decision precision
+                gid[b, a, s:s + chunk] = np.argmax(sc32, axis=1)   # first max wins
+                if K > 1:
+                    top2 = np.sort(sc, axis=1)[:, -2:]
+                    margin[b, a, s:s + chunk] = top2[:, 1] - top2[:, 0]
+                else:
+                    margin[b, a, s:s + chunk] = np.inf
+    return gid, margin
+
+
+# ------------------------------------------------------------------ index ---
+
+def build_index(gid, K: int, w: int):
+    """Group-sorted token index per (batch, assignment).  [FocusJA] 2.2 (far
+    pairs of different groups are skipped, so each group's tokens are gathered
+    together); the sort key is (group, position).
+
+    Returns a dict of arrays, each with leading dims [B, A]:
+      counts [K], offsets [K+1] (exclusive scan), perm [n] (sorted slot ->
+      position), rank [n] (position -> slot), farlen_tok [n] (per position),
+      farlen_slot [n] (per slot), where farlen of token i is the number of
+      tokens j of the same group with j <= i - w.
+    """
+    gid = np.asarray(gid)
+    B, A, n = gid.shape
+    counts = np.zeros((B, A, K), np.int32)
+    offsets = np.zeros((B, A, K + 1), np.int32)
+    perm = np.zeros((B, A, n), np.int32)
+    rank = np.zeros((B, A, n), np.int32)
+    far_tok = np.zeros((B, A, n), np.int32)
+    far_slot = np.zeros((B, A, n), np.int32)
+    for b in range(B):
+        for a in range(A):
+            g = gid[b, a].astype(np.int64)
+            assert g.min() >= 0 and g.max() < K, "group id out of range"
+            counts[b, a] = np.bincount(g, minlength=K)
+            offsets[b, a, 1:] = np.cumsum(counts[b, a])
+            p = np.argsort(g, kind="stable")              # by group, then position
+            perm[b, a] = p
+            rank[b, a, p] = np.arange(n)
+            for k in range(K):
+                members = p[offsets[b, a, k]:offsets[b, a, k + 1]]   # increasing positions
+                if len(members) == 0:
+                    continue
+                # members j with j <= i - w  ==  count of members < i - w + 1
+                fl = np.searchsorted(members, members - w + 1, side="left")
+                far_tok[b, a, members] = fl
+                far_slot[b, a, offsets[b, a, k]:offsets[b, a, k + 1]] = fl
+    return dict(counts=counts, offsets=offsets, perm=perm, rank=rank,
+                farlen_tok=far_tok, farlen_slot=far_slot)
+
+
+def work_items(index: dict, BM: int):
+    """Group-pass work list in canonical order (b, a, g, row0).
+
+    One candidate tile per BM sorted slots of each group; a tile is emitted only
+    when its last row has at least one far key (farlen is non-decreasing inside
+    a group, so that row has the most).  Each item is
+    (b, a, g, row0, rows, keys, key0): rows = sorted slots row0..row0+rows-1,
+    keys = farlen of the tile's last row, key0 = offsets[g] (first key slot).
+    """
+    counts, offsets, fs = index["counts"], index["offsets"], index["farlen_slot"]
+    B, A, K = counts.shape
+    out = []
+    for b in range(B):
+        for a in range(A):
+            for g in range(K):
+                c = int(counts[b, a, g])
+                o = int(offsets[b, a, g])
+                for t in range(0, c, BM):
+                    rows = min(BM, c - t)
+                    keys = int(fs[b, a, o + t + rows - 1])
+                    if keys > 0:
+                        out.append((b, a, g, o + t, rows, keys, o))
+    return np.array(out, dtype=np.int32).reshape(-1, 7)
+
+
+def lpt_order(items: np.ndarray, BN: int):
+    """Longest-first schedule: item indices sorted by ceil(keys/BN) descending,
+    ties by canonical index ascending."""
+    tiles = (items[:, 5].astype(np.int64) + BN - 1) // BN
+    return np.lexsort((np.arange(len(items)), -tiles)).astype(np.int32)
+
+
+# ------------------------------------------------------------------- mask ---
+
+def keep_mask_rows(g, w: int, rows):
+    """Keep rule for query rows `rows` against all keys.  [FocusJA] 2.1 and
+    [FocusKO] 2.1: local window at full resolution, far pairs only inside a
+    group; causal.  M[r, j] = (j <= i) and ((i - j < w) or (g_i == g_j)), i = rows[r].
+    """
+    g = np.asarray(g)
+    rows = np.asarray(rows, dtype=np.int64)
+    j = np.arange(len(g))[None, :]
+    i = rows[:, None]
+    return (j <= i) & (((i - j) < w) | (g[rows][:, None] == g[None, :]))
+
+
+def keep_mask(g, w: int):
+    return keep_mask_rows(g, w, np.arange(len(g)))
+
+
+def kept_counts(index: dict, w: int):
+    """Kept pairs per query token: min(i+1, w) window keys plus farlen far keys.
+    [FocusJA] 2.2 (pair count O(n^2/K + n*w))."""
+    n = index["perm"].shape[-1]
+    win = np.minimum(np.arange(n) + 1, w)
+    return win[None, None, :] + index["farlen_tok"]
+
+
+# -------------------------------------------------------------- attention ---
+
+def attention_masked_rows(Q, K, V, M, rows, scale):
+    """Exact softmax attention of query rows `rows` of one head over mask M.
+
+    Q [n, d], K/V [n, d], M [len(rows), n] bool.  Returns O [len(rows), d] and
+    the natural-log LSE [len(rows)]; rows with an empty kept set give O = 0 and
+    LSE = -inf.  [FocusKO] 2.1: softmax exactly as in the pretrained model,
+    restricted to the kept pairs.
+    """
+    q = _f64(Q)[np.asarray(rows)]
+    S = (q @ _f64(K).T) * float(scale)
+    S = np.where(M, S, -np.inf)
+    m = S.max(axis=1, keepdims=True)
+    empty = ~np.isfinite(m[:, 0])
+    m_safe = np.where(np.isfinite(m), m, 0.0)
+    P = np.exp(S - m_safe)
+    P[~M] = 0.0
+    l = P.sum(axis=1, keepdims=True)
+    l_safe = np.where(l > 0, l, 1.0)
+    O = (P @ _f64(V)) / l_safe
+    lse = (m_safe + np.log(l_safe))[:, 0]
+    O[empty] = 0.0
+    lse[empty] = -np.inf
+    return O, lse
+
+
+def attention_weights_rows(Q, K, M, rows, scale):
+    """Softmax weights P [len(rows), n] of query rows over mask M (for invariants)."""
+    q = _f64(Q)[np.asarray(rows)]
+    S = np.where(M, (q @ _f64(K).T) * float(scale), -np.inf)
+    m = S.max(axis=1, keepdims=True)
+    P = np.exp(S - m)
+    P[~M] = 0.0
+    return P / P.sum(axis=1, keepdims=True)
+
+
+def attention_rows(Q, K, V, gid, w: int, scale: float, rows, A: int, row_block: int = 1024):
+    """Focus attention for selected query rows of every (b, h).
+
+    Q [B,H,n,d], K/V [B,H_kv,n,d], gid [B,A,n], rows: index array into n.
+    Returns O [B,H,len(rows),d] and LSE [B,H,len(rows)] in fp64.
+    """
+    B, H, n, d = Q.shape
+    H_kv = K.shape[1]
+    rows = np.asarray(rows, dtype=np.int64)
+    O = np.empty((B, H, len(rows), d))
+    L = np.empty((B, H, len(rows)))
+    for b in range(B):
+        for hq in range(H):
+            kv = kv_head(hq, H, H_kv)
+            a = assignment_of_head(hq, H, H_kv, A)
+            Kf, Vf = _f64(K[b, kv]), _f64(V[b, kv])
+            for s in range(0, len(rows), row_block):
+                r = rows[s:s + row_block]
+                M = keep_mask_rows(gid[b, a], w, r)
+                O[b, hq, s:s + row_block], L[b, hq, s:s + row_block] = \
+                    attention_masked_rows(Q[b, hq], Kf, Vf, M, r, scale)
+    return O, L
+
+
+def attention(Q, K, V, gid, w: int, scale: float, A: int):
+    """Focus attention over all rows: O [B,H,n,d], LSE [B,H,n] (fp64)."""
+    return attention_rows(Q, K, V, gid, w, scale, np.arange(Q.shape[2]), A)
+
+
+def dense_causal(Q, K, V, scale: float):
+    """Ordinary causal attention (every j <= i kept) over all rows."""
+    B, H, n, d = Q.shape
+    gid = np.zeros((B, 1, n), np.int32)
+    return attention(Q, K, V, gid, n, scale, 1)
+
+
+def lse_merge(O1, L1, O2, L2):
+    """Merge two softmax partials over disjoint key sets into one.
+
+    O = (e^{L1} O1 + e^{L2} O2) / (e^{L1} + e^{L2}), with the larger LSE shifted
+    out; an empty partial (LSE = -inf) contributes nothing.  [FocusKO] 2.3 and
+    [FocusJA] 3.3: the pattern splits into a local-window call and an in-group
+    call whose results combine into the exact softmax over the union.
+    """
+    O1, O2 = _f64(O1), _f64(O2)
+    L1, L2 = _f64(L1), _f64(L2)
+    m = np.maximum(L1, L2)
+    m_safe = np.where(np.isfinite(m), m, 0.0)
+    e1 = np.where(np.isfinite(L1), np.exp(L1 - m_safe), 0.0)
+    e2 = np.where(np.isfinite(L2), np.exp(L2 - m_safe), 0.0)
+    den = e1 + e2
+    den_safe = np.where(den > 0, den, 1.0)
+    O = (e1[..., None] * O1 + e2[..., None] * O2) / den_safe[..., None]
+    L = np.where(den > 0, m_safe + np.log(den_safe), -np.inf)
+    return O, L
+
+
+# ------------------------------------------------------------ brute force ---
+
+def attention_bruteforce(q, k, v, g, w: int, scale: float):
+    """Scalar-loop reference for one head at small n (n <= 64).
+
+    The kept set of row i is built as the union of its window list
+    {max(0, i-w+1), ..., i} and the list of earlier members of its own group,
+    a construction independent of the n x n mask; sums use math.fsum.
+    Returns O [n][d] and LSE [n] as Python lists.
+    """
+    n, d = len(q), len(q[0])
+    members = {}
+    for j in range(n):
+        members.setdefault(int(g[j]), []).append(j)
+    O, L = [], []
+    for i in range(n):
+        kept = set(range(max(0, i - w + 1), i + 1))
+        kept.update(j for j in members[int(g[i])] if j <= i)
+        kept = sorted(kept)
+        s = [math.fsum(float(q[i][c]) * float(k[j][c]) for c in range(d)) * scale for j in kept]
+        mx = max(s)
+        e = [math.exp(x - mx) for x in s]
+        z = math.fsum(e)
+        O.append([math.fsum(e[t] * float(v[j][c]) for t, j in enumerate(kept)) / z for c in range(d)])
+        L.append(mx + math.log(z))
+    return O, L

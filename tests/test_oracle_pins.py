@@ -1,0 +1,365 @@
+"""Pins for the fp64 oracle: checks against things other than the oracle itself.
+
+Each test ties one oracle function to a hand-worked example, a closed form, a
+special case that reduces to a textbook routine, brute force on tiny inputs or
+an invariant the method fixes, so that a dropped term, a wrong sign or index
+or a transposed operand in the oracle fails at least one of them.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.focus_ref as ref
+from learned_group_sparse_focus_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _parse_golden(name):
+    out = {"kept": {}, "item": [], "O": {}}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            key, val = line.split(":", 1)
+            vals = val.split()
+            if key.startswith("kept "):
+                out["kept"][int(key.split()[1])] = [int(v) for v in vals]
+            elif key == "item":
+                out["item"].append([int(v) for v in vals])
+            elif key.startswith("O") and key[1:].isdigit():
+                out["O"][int(key[1:])] = [float(v) for v in vals]
+            else:
+                out[key] = [float(v) if "." in v else int(v) for v in vals]
+    return out
+
+
+# ------------------------------------------------------------ golden case ---
+
+def test_golden_keep_rule_index_and_softmax():
+    gd = _parse_golden("keep_rule_n8.txt")
+    n, w, K = gd["n"][0], gd["w"][0], gd["K"][0]
+    g = np.array(gd["groups"], np.int32)
+    M = ref.keep_mask(g, w)
+    for i in range(n):
+        assert list(np.nonzero(M[i])[0]) == gd["kept"][i], i
+    idx = ref.build_index(g[None, None, :], K, w)
+    for key in ("counts", "offsets", "perm", "rank", "farlen_tok", "farlen_slot"):
+        assert idx[key][0, 0].tolist() == gd[key], key
+    items = ref.work_items(idx, gd["BM"][0])
+    assert items.tolist() == gd["item"]
+    assert ref.lpt_order(items, gd["BN"][0]).tolist() == gd["lpt"]
+    kc = ref.kept_counts(idx, w)[0, 0]
+    assert kc.tolist() == gd["lse_count"]
+    # exact softmax with all-zero scores
+    Q = np.zeros((1, 1, n, 2))
+    Kt = np.random.default_rng(0).standard_normal((1, 1, n, 2))
+    V = np.stack([np.arange(n, dtype=np.float64), np.ones(n)], axis=1)[None, None]
+    O, L = ref.attention(Q, Kt, V, g[None, None, :], w, 0.7, 1)
+    for i in range(n):
+        np.testing.assert_allclose(O[0, 0, i], gd["O"][i], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(L[0, 0], np.log(np.array(gd["lse_count"], float)), atol=1e-14)
+
+
+# ----------------------------------------------------------------- assign ---
+
+def test_assign_closed_form_signed_basis_and_ties():
+    # W = I, C = signed basis vectors: the score of centroid k is a signed
+    # coordinate of h, so the group is the largest signed coordinate; the
+    # duplicate of e0 (index 4) never wins over index 0.
+    d = 4
+    W = np.eye(d)[None]
+    C = np.array([[1, 0, 0, 0], [0, 1, 0, 0], [-1, 0, 0, 0], [0, 0, 1, 0], [1, 0, 0, 0]], float)[None]
+    h = np.array([[[3, -1, 0.5, 2], [-2, 1, 0, 0], [0.1, 0.2, 0.3, 0], [-1, -1, -1, -1]]], float)
+    gid, margin = ref.assign(h, W, C)
+    # scores: row0 [3,-1,-3,.5,3] -> 0 (tie with 4); row1 [-2,1,2,0,-2] -> 2;
+    # row2 [.1,.2,-.1,.3,.1] -> 3; row3 [-1,-1,1,-1,-1] -> 2
+    assert gid[0, 0].tolist() == [0, 2, 3, 2]
+    np.testing.assert_allclose(margin[0, 0], [0.0, 1.0, 0.1, 2.0], atol=1e-15)
+
+
+def test_assign_bruteforce_loops():
+    rng = np.random.default_rng(1)
+    B, n, D, A, dg, K = 2, 9, 7, 2, 5, 6
+    h = rng.standard_normal((B, n, D))
+    W = rng.standard_normal((A, dg, D))
+    C = rng.standard_normal((A, K, dg))
+    gid, margin = ref.assign(h, W, C)
+    for b in range(B):
+        for a in range(A):
+            for i in range(n):
+                p = [math.fsum(W[a, r, c] * h[b, i, c] for c in range(D)) for r in range(dg)]
+                s = [math.fsum(p[r] * C[a, k, r] for r in range(dg)) for k in range(K)]
+                best = 0
+                for k in range(1, K):
+                    if s[k] > s[best]:
+                        best = k
+                assert gid[b, a, i] == best
+                srt = sorted(s)
+                assert abs(margin[b, a, i] - (srt[-1] - srt[-2])) < 1e-12
+
+
+def test_assign_centroid_permutation_relabels():
+    rng = np.random.default_rng(2)
+    h = rng.standard_normal((1, 200, 16))
+    W = rng.standard_normal((1, 8, 16))
+    C = rng.standard_normal((1, 10, 8))
+    pi = rng.permutation(10)
+    g1, _ = ref.assign(h, W, C)
+    g2, _ = ref.assign(h, W, C[:, pi])     # centroid k of the new set is old pi[k]
+    assert np.array_equal(pi[g2], g1)
+
+
+def test_assign_depends_on_projection_not_raw_h():
+    # with a projection that zeroes all but one hidden coordinate, only that
+    # coordinate decides: transposing W would break this.
+    h = np.array([[[5.0, -3.0, 0.0], [-5.0, 3.0, 0.0]]])
+    W = np.array([[[0.0, 1.0, 0.0], [0.0, 0.0, 0.0]]])        # d_g=2, D=3: p = (h1, 0)
+    C = np.array([[[1.0, 0.0], [-1.0, 0.0]]])
+    gid, _ = ref.assign(h, W, C)
+    assert gid[0, 0].tolist() == [1, 0]
+
+
+# ------------------------------------------------------------------ index ---
+
+@pytest.mark.parametrize("kind,K,n,w", [
+    ("uniform", 5, 300, 7), ("zipf", 16, 512, 33), ("one", 1, 100, 10),
+    ("blocks", 8, 256, 4), ("distinct", 64, 64, 1), ("uniform", 3, 50, 0),
+    ("uniform", 40, 90, 200),
+])
+def test_index_invariants_and_bruteforce(kind, K, n, w):
+    g = synth.draw_group_ids(7, 2, 2, n, K, kind)
+    idx = ref.build_index(g, K, w)
+    for b in range(2):
+        for a in range(2):
+            gg = g[b, a]
+            perm, rank = idx["perm"][b, a], idx["rank"][b, a]
+            assert idx["counts"][b, a].sum() == n
+            assert sorted(perm.tolist()) == list(range(n))
+            assert np.array_equal(rank[perm], np.arange(n))
+            assert np.all(np.diff(gg[perm]) >= 0)
+            for k in range(K):
+                o0, o1 = idx["offsets"][b, a, k], idx["offsets"][b, a, k + 1]
+                assert o1 - o0 == np.sum(gg == k)
+                assert np.all(np.diff(perm[o0:o1]) > 0)
+            for i in range(n):
+                bf = sum(1 for j in range(n) if gg[j] == gg[i] and j <= i - w)
+                assert idx["farlen_tok"][b, a, i] == bf
+                assert idx["farlen_slot"][b, a, rank[i]] == bf
+
+
+@pytest.mark.parametrize("K,n,w", [(4, 200, 9), (13, 333, 1), (2, 64, 64), (30, 257, 16)])
+def test_kept_count_three_ways(K, n, w):
+    g = synth.draw_group_ids(11, 1, 1, n, K, "uniform")
+    idx = ref.build_index(g, K, w)
+    total = int(ref.kept_counts(idx, w).sum())
+    pop = int(ref.keep_mask(g[0, 0], w).sum())
+    # inclusion-exclusion: window pairs + same-group causal pairs - same-group window pairs
+    win = sum(min(i + 1, w) for i in range(n))
+    cnt = np.bincount(g[0, 0], minlength=K)
+    same = int(sum(c * (c + 1) // 2 for c in cnt))
+    overlap = sum(1 for i in range(n) for j in range(max(0, i - w + 1), i + 1) if g[0, 0, i] == g[0, 0, j])
+    assert total == pop == win + same - overlap
+
+
+def test_work_items_cover_exactly_far_rows():
+    g = synth.draw_group_ids(5, 2, 3, 700, 9, "zipf")
+    w, BM = 40, 32
+    idx = ref.build_index(g, 9, w)
+    items = ref.work_items(idx, BM)
+    cover = np.zeros((2, 3, 700), int)
+    prev = None
+    for b, a, k, row0, rows, keys, key0 in items:
+        key = (b, a, k, row0)
+        assert prev is None or key > prev
+        prev = key
+        assert 1 <= rows <= BM and key0 == idx["offsets"][b, a, k]
+        assert row0 + rows <= idx["offsets"][b, a, k + 1]
+        fs = idx["farlen_slot"][b, a, row0:row0 + rows]
+        assert keys == fs.max() > 0
+        assert keys <= row0 + rows - key0 - 1 + 1
+        cover[b, a, row0:row0 + rows] += 1
+    far = idx["farlen_slot"] > 0
+    assert np.all(cover[far] == 1) and cover.max() <= 1
+    order = ref.lpt_order(items, 64)
+    assert sorted(order.tolist()) == list(range(len(items)))
+    tiles = (items[order, 5] + 63) // 64
+    assert np.all(np.diff(tiles) <= 0)
+
+
+# -------------------------------------------------------------- attention ---
+
+def _sdpa_causal(Q, K, V, scale):
+    H, Hkv = Q.shape[1], K.shape[1]
+    Kt = torch.from_numpy(np.repeat(K, H // Hkv, axis=1))
+    Vt = torch.from_numpy(np.repeat(V, H // Hkv, axis=1))
+    return torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(Q), Kt, Vt, is_causal=True, scale=scale).numpy()
+
+
+@pytest.mark.parametrize("mode", ["K1", "wide_window"])
+def test_reduces_to_dense_causal_sdpa(mode):
+    rng = np.random.default_rng(3)
+    B, H, Hkv, n, d = 2, 4, 2, 97, 16
+    Q = rng.standard_normal((B, H, n, d))
+    K = rng.standard_normal((B, Hkv, n, d))
+    V = rng.standard_normal((B, Hkv, n, d))
+    if mode == "K1":
+        g, w = np.zeros((B, 1, n), np.int32), 5
+    else:
+        g, w = synth.draw_group_ids(1, B, 1, n, 7, "uniform"), n
+    O, L = ref.attention(Q, K, V, g, w, 0.3, 1)
+    np.testing.assert_allclose(O, _sdpa_causal(Q, K, V, 0.3), atol=1e-12)
+    O2, _ = ref.dense_causal(Q, K, V, 0.3)
+    np.testing.assert_allclose(O2, O, atol=1e-13)
+
+
+def test_distinct_groups_window_one_is_identity_on_v():
+    rng = np.random.default_rng(4)
+    n, d = 64, 8
+    Q, K, V = (rng.standard_normal((1, 1, n, d)) for _ in range(3))
+    g = synth.draw_group_ids(2, 1, 1, n, n, "distinct")
+    O, L = ref.attention(Q, K, V, g, 1, 0.5, 1)
+    assert np.array_equal(O[0, 0], V[0, 0])
+    np.testing.assert_allclose(L[0, 0], 0.5 * np.sum(Q[0, 0] * K[0, 0], axis=1), atol=1e-14)
+
+
+def test_group_relabelling_leaves_output_unchanged():
+    rng = np.random.default_rng(5)
+    n, d, K = 150, 12, 6
+    Q, Kt, V = (rng.standard_normal((1, 2, n, d)) for _ in range(3))
+    g = synth.draw_group_ids(3, 1, 1, n, K, "uniform")
+    pi = rng.permutation(K)
+    O1, L1 = ref.attention(Q, Kt, V, g, 10, 0.4, 1)
+    O2, L2 = ref.attention(Q, Kt, V, pi[g].astype(np.int32), 10, 0.4, 1)
+    np.testing.assert_allclose(O1, O2, atol=1e-12)
+    np.testing.assert_allclose(L1, L2, atol=1e-12)
+
+
+def test_weights_sum_to_one_and_vanish_off_mask():
+    rng = np.random.default_rng(6)
+    n, d = 120, 10
+    Q, K = rng.standard_normal((n, d)), rng.standard_normal((n, d))
+    g = synth.draw_group_ids(4, 1, 1, n, 5, "uniform")[0, 0]
+    M = ref.keep_mask(g, 9)
+    P = ref.attention_weights_rows(Q, K, M, np.arange(n), 0.3)
+    np.testing.assert_allclose(P.sum(axis=1), 1.0, atol=1e-12)
+    assert np.all(P[~M] == 0) and np.all(P[M] > 0)
+
+
+@pytest.mark.parametrize("n,w,K,kind", [(64, 4, 3, "uniform"), (40, 1, 40, "distinct"),
+                                        (33, 0, 5, "uniform"), (50, 64, 2, "uniform"),
+                                        (64, 8, 1, "one"), (17, 3, 4, "blocks")])
+def test_bruteforce_small(n, w, K, kind):
+    rng = np.random.default_rng(n * 100 + w)
+    d = 6
+    Q, Kt, V = (rng.standard_normal((1, 1, n, d)) for _ in range(3))
+    g = synth.draw_group_ids(n + w, 1, 1, n, K, kind)
+    O, L = ref.attention(Q, Kt, V, g, w, 0.45, 1)
+    Ob, Lb = ref.attention_bruteforce(Q[0, 0], Kt[0, 0], V[0, 0], g[0, 0], w, 0.45)
+    np.testing.assert_allclose(O[0, 0], np.array(Ob), atol=1e-12)
+    np.testing.assert_allclose(L[0, 0], np.array(Lb), atol=1e-12)
+
+
+def test_local_plus_far_merge_equals_union():
+    # The two-call decomposition: window-only and far-only (j <= i - w, same
+    # group) partials merged by log-sum-exp equal one softmax over the union.
+    rng = np.random.default_rng(8)
+    n, d, w = 200, 8, 13
+    Q, K, V = (rng.standard_normal((n, d)) for _ in range(3))
+    g = synth.draw_group_ids(9, 1, 1, n, 4, "uniform")[0, 0]
+    i = np.arange(n)[:, None]
+    j = np.arange(n)[None, :]
+    local = (j <= i) & (i - j < w)
+    far = (j <= i - w) & (g[:, None] == g[None, :])
+    assert not np.any(local & far)
+    rows = np.arange(n)
+    O1, L1 = ref.attention_masked_rows(Q, K, V, local, rows, 0.35)
+    O2, L2 = ref.attention_masked_rows(Q, K, V, far, rows, 0.35)
+    Om, Lm = ref.lse_merge(O1, L1, O2, L2)
+    Ou, Lu = ref.attention_masked_rows(Q, K, V, ref.keep_mask(g, w), rows, 0.35)
+    np.testing.assert_allclose(Om, Ou, atol=1e-12)
+    np.testing.assert_allclose(Lm, Lu, atol=1e-12)
+    assert np.any(~np.isfinite(L2))     # some rows have no far keys: merge must skip them
+
+
+def test_window_zero_equals_window_one():
+    g = synth.draw_group_ids(12, 1, 1, 80, 6, "uniform")[0, 0]
+    assert np.array_equal(ref.keep_mask(g, 0), ref.keep_mask(g, 1))
+
+
+def test_gqa_head_map_and_assignment_per_kv_head():
+    rng = np.random.default_rng(10)
+    B, H, Hkv, n, d = 1, 6, 3, 40, 4
+    Q = rng.standard_normal((B, H, n, d))
+    K = rng.standard_normal((B, Hkv, n, d))
+    V = rng.standard_normal((B, Hkv, n, d))
+    g = synth.draw_group_ids(13, B, Hkv, n, 4, "uniform")
+    O, _ = ref.attention(Q, K, V, g, 5, 0.5, Hkv)
+    K2, V2 = K.copy(), V.copy()
+    K2[:, 2] += 3.0
+    V2[:, 2] -= 1.0
+    g2 = g.copy()
+    g2[:, 2] = (g2[:, 2] + 1) % 4 * 0       # change kv head 2's assignment only
+    O2, _ = ref.attention(Q, K2, V2, g2, 5, 0.5, Hkv)
+    np.testing.assert_array_equal(O[:, :4], O2[:, :4])           # heads 0..3 -> kv 0, 1
+    assert not np.allclose(O[:, 4:], O2[:, 4:])
+    # each query head equals single-head attention with its own kv head and ids
+    for hq in range(H):
+        kv = hq * Hkv // H
+        Os, _ = ref.attention(Q[:, hq:hq + 1], K[:, kv:kv + 1], V[:, kv:kv + 1],
+                              g[:, kv:kv + 1], 5, 0.5, 1)
+        np.testing.assert_array_equal(Os[:, 0], O[:, hq])
+
+
+def test_scale_enters_as_product_with_q():
+    rng = np.random.default_rng(11)
+    Q, K, V = (rng.standard_normal((1, 1, 60, 8)) for _ in range(3))
+    g = synth.draw_group_ids(14, 1, 1, 60, 3, "uniform")
+    O1, _ = ref.attention(Q, K, V, g, 7, 0.25, 1)
+    O2, _ = ref.attention(Q * 0.25, K, V, g, 7, 1.0, 1)
+    np.testing.assert_allclose(O1, O2, atol=1e-13)
+
+
+def test_row_sampling_matches_full():
+    rng = np.random.default_rng(12)
+    B, H, n, d = 1, 2, 300, 8
+    Q, K, V = (rng.standard_normal((B, H, n, d)) for _ in range(3))
+    g = synth.draw_group_ids(15, B, 1, n, 5, "zipf")
+    O, L = ref.attention(Q, K, V, g, 17, 0.3, 1)
+    rows = np.array([0, 5, 77, 299, 150])
+    Os, Ls = ref.attention_rows(Q, K, V, g, 17, 0.3, rows, 1, row_block=2)
+    np.testing.assert_allclose(Os, O[:, :, rows], atol=1e-14)   # BLAS blocking only
+    np.testing.assert_allclose(Ls, L[:, :, rows], atol=1e-14)
+
+
+# ------------------------------------------------ planted oracle mistakes ---
+
+def test_pins_catch_planted_mistakes(monkeypatch):
+    """Each plausible slip in the keep rule breaks the hand-worked example."""
+    gd = _parse_golden("keep_rule_n8.txt")
+    g = np.array(gd["groups"], np.int32)
+    good = ref.keep_mask_rows
+
+    def off_by_one(gg, w, rows):          # window read as i - j <= w
+        return good(gg, w + 1, rows)
+
+    def no_causal(gg, w, rows):           # future same-group keys leak in
+        rows = np.asarray(rows)
+        jj = np.arange(len(gg))[None, :]
+        ii = rows[:, None]
+        return (((ii - jj) < w) & (jj <= ii)) | (gg[rows][:, None] == gg[None, :])
+
+    def no_group(gg, w, rows):            # far term dropped
+        rows = np.asarray(rows)
+        jj = np.arange(len(gg))[None, :]
+        ii = rows[:, None]
+        return (jj <= ii) & ((ii - jj) < w)
+
+    for bad in (off_by_one, no_causal, no_group):
+        M = bad(g, gd["w"][0], np.arange(gd["n"][0]))
+        assert any(list(np.nonzero(M[i])[0]) != gd["kept"][i] for i in range(gd["n"][0])), bad.__name__
