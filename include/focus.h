@@ -1,0 +1,197 @@
+/*
+ * focus.h -- C ABI of the Focus attention hot path on one NVIDIA GB300 (sm_103a).
+ *
+ * Focus keeps, for causal attention, only the token pairs that matter:
+ * pairs inside a local window, and far pairs whose two tokens fall in the
+ * same learned group; every other pair is skipped, and softmax stays exact
+ * over the kept pairs.  Sources (page titles and sections):
+ *   "Focus: Learning Which Attention Pairs Matter", section 2.1 (centroids,
+ *     projection, local + group-gated far attention), section 2.2 (hard
+ *     top-k assignment at inference; far pairs of different groups skipped;
+ *     pair count O(n^2/K + n*w)), section 3.3 (local-window + in-group causal
+ *     decomposition).
+ *   "Why Attend to Everything? Focus is the Key", section 2.1 (exact softmax
+ *     preserved), section 2.3 (hard assignment, two FlashAttention calls).
+ *
+ * The hot path is three calls, issued in order on one stream:
+ *   focus_assign        hidden states -> group id per token (top-1 centroid)
+ *   focus_build_index   group ids -> (group, position) sorted index + work list
+ *   focus_attention_fwd Q, K, V, index -> O over the kept pairs only
+ *
+ * Conventions shared by every call
+ *   - All tensor pointers are DEVICE pointers to row-major contiguous arrays,
+ *     16-byte aligned, owned by the caller.  The library allocates nothing,
+ *     keeps no state beyond a per-process cache of kernel attributes, and
+ *     never synchronises except in focus_check_errors.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - `ws` is caller-owned device scratch of at least focus_workspace_bytes(p)
+ *     bytes, 256-byte aligned.  It holds the device error word, the index and
+ *     attention temporaries; one workspace serves one stream at a time.
+ *   - Argument errors are reported synchronously as a status with nothing
+ *     launched.  Launch failures give FOCUS_ERR_CUDA.  Errors found on the
+ *     device (a group id outside [0, K), a bounded wait that ran out) set bits
+ *     of the device error word and are reported by focus_check_errors.  No
+ *     call traps, asserts, aborts or throws across this boundary.
+ *
+ * Shapes (notation of the pages plus standard attention names)
+ *   B batch, H query heads, H_kv key/value heads (H % H_kv == 0),
+ *   n tokens, d head dim, D hidden size, d_g projection dim, K centroids,
+ *   A independent assignments (1: one group id per token shared by all heads;
+ *   H_kv: one per key/value head), w local window (pair kept when i - j < w;
+ *   w = 0 keeps the same pairs as w = 1 because a token always shares its own
+ *   group), scale softmax scale (1/sqrt(d) in the usual setting).
+ *   Query head h reads key/value head kv = h * H_kv / H (integer division) and
+ *   assignment a = (A == 1 ? 0 : kv).
+ */
+#ifndef FOCUS_H_
+#define FOCUS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FOCUS_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define FOCUS_API __attribute__((visibility("default")))
+#else
+#define FOCUS_API
+#endif
+
+/* Query rows per group-pass work item; the work list is built for this height. */
+#define FOCUS_TILE_M 128
+/* Keys per attention tile; the longest-first schedule counts cost in these. */
+#define FOCUS_TILE_N 128
+/* Largest supported number of centroids K. */
+#define FOCUS_MAX_K 4096
+/* Largest supported sequence length n. */
+#define FOCUS_MAX_N (1 << 20)
+
+typedef enum {
+  FOCUS_OK = 0,
+  FOCUS_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad shape or value   */
+  FOCUS_ERR_UNSUPPORTED = 2,   /* valid request with no kernel (dtype, d, ...)  */
+  FOCUS_ERR_WORKSPACE = 3,     /* ws_bytes < focus_workspace_bytes(p)           */
+  FOCUS_ERR_CUDA = 4,          /* a CUDA runtime/launch call failed             */
+  FOCUS_ERR_TIMEOUT = 5,       /* device: a bounded wait ran out                */
+  FOCUS_ERR_BAD_GROUP_ID = 6   /* device: a group id outside [0, K)             */
+} focus_status_t;
+
+typedef enum { FOCUS_F32 = 0, FOCUS_BF16 = 1 } focus_dtype_t;
+
+/* Problem description; every call takes the same struct. */
+typedef struct {
+  int32_t B, H, H_kv, n, d, D, d_g, K, A, w;
+  float scale;
+  int32_t dtype; /* focus_dtype_t: element type of h, W, C, Q, K, V and O */
+} focus_params_t;
+
+/* One group-pass work item: query rows = sorted slots row0 .. row0+rows-1 of
+ * assignment (b, a), all in group g; keys = the first `keys` slots of that
+ * group, starting at slot key0 (= offsets[g]). */
+typedef struct {
+  int32_t b, a, g, row0, rows, keys, key0, pad;
+} focus_item_t;
+
+/* Device pointers into the workspace, filled by focus_build_index.
+ * Arrays are indexed [(b * A + a) * len + i]. */
+typedef struct {
+  int32_t* counts;       /* [B*A][K]   tokens per group                         */
+  int32_t* offsets;      /* [B*A][K+1] exclusive scan of counts                 */
+  int32_t* perm;         /* [B*A][n]   sorted slot -> token position            */
+  int32_t* rank;         /* [B*A][n]   token position -> sorted slot            */
+  int32_t* farlen_tok;   /* [B*A][n]   per position: same-group tokens j<=i-w   */
+  int32_t* farlen_slot;  /* [B*A][n]   the same, per sorted slot                */
+  focus_item_t* items;   /* [max_items] work list, canonical (b, a, g, row0)    */
+  int32_t* order;        /* [max_items] longest-first schedule over items       */
+  int32_t* n_items;      /* [1]        number of valid entries in items/order   */
+  int32_t max_items;     /* host-side capacity of items/order                   */
+  int32_t w_eff;         /* window the index was built for (max(w, 1))          */
+} focus_index_t;
+
+/* Bytes of device workspace the calls below need for problem p (0 if p is
+ * invalid).  Pure host arithmetic. */
+FOCUS_API size_t focus_workspace_bytes(const focus_params_t* p);
+
+/* Clears the device error word at the start of ws (an async memset on
+ * `stream`).  Call once after allocating a workspace, before the first call
+ * that uses it; focus_check_errors clears the word again after each report. */
+FOCUS_API focus_status_t focus_workspace_init(void* ws, void* stream);
+
+/* Group assignment ("Focus: Learning Which Attention Pairs Matter" 2.1, 2.2;
+ * "Why Attend to Everything?" 2.3).  For each token i of batch b and each
+ * assignment a: p = W[a] h[b,i] (no bias, accumulated and kept in fp32),
+ * s_k = p . C[a,k] in fp32, gid[b,a,i] = argmax_k s_k, lowest k on ties.
+ *   h   [B, n, D]      dtype          W [A, d_g, D] dtype     C [A, K, d_g] dtype
+ *   gid [B, A, n]      int32 output
+ * bf16 runs the projection on the tensor cores (fp32 accumulate) and needs
+ * D % 8 == 0, d_g in {32, 64, 128} and A*d_g <= 512; f32 runs it in fp32 on the
+ * CUDA cores and needs d_g in {16, 32, 64, 128}.  Other shapes give
+ * FOCUS_ERR_UNSUPPORTED. */
+FOCUS_API focus_status_t focus_assign(const focus_params_t* p, const void* h, const void* W,
+                            const void* C, int32_t* gid, void* ws, size_t ws_bytes,
+                            void* stream);
+
+/* Group-sorted index ("Focus: Learning Which Attention Pairs Matter" 2.2: far
+ * pairs of different groups are skipped, so each group's tokens are gathered).
+ * Stable counting sort of tokens by (group, position) per (b, a), farlen per
+ * token, and the group-pass work list in canonical order plus a longest-first
+ * order.  gid [B, A, n] int32 device input.  *idx_out (host struct) receives
+ * device pointers into ws; they stay valid while ws is not reused by another
+ * focus_build_index.  A gid outside [0, K) is clamped for safety and flagged
+ * as FOCUS_ERR_BAD_GROUP_ID in the device error word. */
+FOCUS_API focus_status_t focus_build_index(const focus_params_t* p, const int32_t* gid,
+                                 focus_index_t* idx_out, void* ws, size_t ws_bytes,
+                                 void* stream);
+
+/* Focus attention over the kept pairs ("Focus: Learning Which Attention Pairs
+ * Matter" 2.1, 2.2, 3.3; "Why Attend to Everything?" 2.1, 2.3).  Row i of head h
+ * attends to key j iff j <= i and (i - j < w or g_i == g_j), with
+ * softmax(scale * q_i . k_j) exact over that set.
+ *   Q [B, H, n, d], K/V [B, H_kv, n, d] dtype, O [B, H, n, d] dtype output,
+ *   lse_opt [B, H, n] fp32 natural-log sum-exp of the scaled scores, or NULL.
+ * idx must come from focus_build_index with the same p and ws.  d in {64, 128}.
+ * The call runs a group pass (far same-group keys, rows in sorted order) and a
+ * local pass (window keys, natural order) that merges both partial softmaxes. */
+FOCUS_API focus_status_t focus_attention_fwd(const focus_params_t* p, const void* Q, const void* K,
+                                   const void* V, const focus_index_t* idx, void* O,
+                                   float* lse_opt, void* ws, size_t ws_bytes, void* stream);
+
+/* Ordinary causal attention (every j <= i kept) with the same kernels and
+ * layouts as the local pass: the dense comparator for the speedup figure.
+ * Ignores p->w, p->K, p->A.  Same tensors and rules as focus_attention_fwd. */
+FOCUS_API focus_status_t focus_dense_causal_fwd(const focus_params_t* p, const void* Q, const void* K,
+                                      const void* V, void* O, float* lse_opt, void* ws,
+                                      size_t ws_bytes, void* stream);
+
+/* The whole layer from HOST buffers: copies h, W, C, Q, K, V from host memory
+ * (pinned for overlap) into the caller's device buffers with one
+ * cudaMemcpyAsync each, runs assign -> index -> attention on `stream`, and
+ * copies O back to host memory.  d_* are device buffers of the sizes above;
+ * d_gid is [B, A, n] int32.  Returns after enqueueing; synchronise the stream
+ * (or call focus_check_errors) before reading host_O. */
+FOCUS_API focus_status_t focus_layer_fwd_host(const focus_params_t* p,
+                                    const void* host_h, const void* host_W, const void* host_C,
+                                    const void* host_Q, const void* host_K, const void* host_V,
+                                    void* host_O,
+                                    void* d_h, void* d_W, void* d_C, void* d_Q, void* d_K,
+                                    void* d_V, void* d_O, int32_t* d_gid,
+                                    void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, reads and clears the device error word in ws.
+ * Returns FOCUS_OK, FOCUS_ERR_BAD_GROUP_ID, FOCUS_ERR_TIMEOUT or FOCUS_ERR_CUDA. */
+FOCUS_API focus_status_t focus_check_errors(void* ws, void* stream);
+
+/* Static description of a status code. */
+FOCUS_API const char* focus_status_string(focus_status_t s);
+
+/* FOCUS_ABI_VERSION of the loaded library. */
+FOCUS_API int32_t focus_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FOCUS_H_ */

@@ -1,0 +1,370 @@
+// Host side of the Focus C ABI: argument checks, workspace layout, TMA
+// descriptors and the launch sequence of each call.  See include/focus.h for
+// the contract of every entry point.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "kernels.h"
+
+namespace focus {
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t elt_size(int dtype) { return dtype == FOCUS_BF16 ? 2 : 4; }
+
+// Byte offsets of every region inside the workspace.
+struct Layout {
+  size_t err, segcnt, counts, offsets, tile_base, perm, rank, far_tok, far_slot, items, cost,
+      order, n_items, Ks, Vs, O_far, lse_far, total;
+  int nseg, max_items;
+};
+
+bool params_ok(const focus_params_t* p) {
+  if (!p) return false;
+  if (p->B < 1 || p->H < 1 || p->H_kv < 1 || p->H % p->H_kv != 0) return false;
+  if (p->n < 1 || p->n > FOCUS_MAX_N) return false;
+  if (p->d < 1 || p->D < 1 || p->d_g < 1) return false;
+  if (p->K < 1 || p->K > FOCUS_MAX_K) return false;
+  if (!(p->A == 1 || p->A == p->H_kv)) return false;
+  if (p->w < 0) return false;
+  if (!(std::isfinite(p->scale) && p->scale > 0.f)) return false;
+  if (p->dtype != FOCUS_F32 && p->dtype != FOCUS_BF16) return false;
+  if (static_cast<long long>(p->B) * p->A > 4096) return false;
+  return true;
+}
+
+Layout layout_of(const focus_params_t* p) {
+  Layout L{};
+  const size_t P = static_cast<size_t>(p->B) * p->A;
+  const size_t n = p->n, K = p->K;
+  L.nseg = static_cast<int>((n + kIndexSeg - 1) / kIndexSeg);
+  L.max_items = static_cast<int>(P * ((n + kTileM - 1) / kTileM + (K < n ? K : n)));
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align_up(o + bytes);
+    return at;
+  };
+  L.err = take(kAlign);
+  L.segcnt = take(P * L.nseg * K * 4);
+  L.counts = take(P * K * 4);
+  L.offsets = take(P * (K + 1) * 4);
+  L.tile_base = take(P * (K + 1) * 4);
+  L.perm = take(P * n * 4);
+  L.rank = take(P * n * 4);
+  L.far_tok = take(P * n * 4);
+  L.far_slot = take(P * n * 4);
+  L.items = take(static_cast<size_t>(L.max_items) * sizeof(focus_item_t));
+  L.cost = take(static_cast<size_t>(L.max_items) * 4);
+  L.order = take(static_cast<size_t>(L.max_items) * 4);
+  L.n_items = take(4);
+  const size_t es = elt_size(p->dtype);
+  const size_t kvb = static_cast<size_t>(p->B) * p->H_kv * n * p->d * es;
+  L.Ks = take(p->dtype == FOCUS_BF16 ? kvb : 0);
+  L.Vs = take(p->dtype == FOCUS_BF16 ? kvb : 0);
+  L.O_far = take(static_cast<size_t>(p->B) * p->H * n * p->d * es);
+  L.lse_far = take(static_cast<size_t>(p->B) * p->H * n * 4);
+  L.total = o;
+  return L;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+// ----------------------------------------------------- per-device set-up ---
+std::mutex g_mu;
+bool g_ready[64] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+focus_status_t ensure_setup() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FOCUS_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return FOCUS_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  if (!g_ready[dev]) {
+    if (setup_index_kernels() != cudaSuccess) return FOCUS_ERR_CUDA;
+    if (setup_assign_kernels() != cudaSuccess) return FOCUS_ERR_CUDA;
+    if (setup_attn_kernels() != cudaSuccess) return FOCUS_ERR_CUDA;
+    g_ready[dev] = true;
+  }
+  return FOCUS_OK;
+}
+
+// bf16 tensor map over rows of `inner` elements: dims {inner, rows[, planes]}
+// (rank 2 or 3, matching the TMA instruction that reads it), box
+// {64, box_rows[, 1]}, 128-byte swizzle, zero fill out of bounds.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t planes,
+              uint32_t box_rows, int rank) {
+  cuuint64_t dims[3] = {inner, rows, planes};
+  cuuint64_t strides[2] = {inner * 2, inner * rows * 2};
+  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
+                              const_cast<void*>(base), dims, strides, box, es,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+focus_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? FOCUS_OK : FOCUS_ERR_CUDA; }
+
+focus_status_t check_ws(const focus_params_t* p, void* ws, size_t ws_bytes) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return FOCUS_ERR_INVALID_ARG;
+  if (ws_bytes < layout_of(p).total) return FOCUS_ERR_WORKSPACE;
+  return FOCUS_OK;
+}
+
+AttnArgs attn_args(const focus_params_t* p, const void* Q, const void* K, const void* V, void* O,
+                   float* lse, void* ws, const Layout& L) {
+  AttnArgs a{};
+  a.Q = Q;
+  a.O = O;
+  a.lse = lse;
+  a.O_far = at<void>(ws, L.O_far);
+  a.lse_far = at<float>(ws, L.lse_far);
+  a.Kg = K;
+  a.Vg = V;
+  a.B = p->B;
+  a.H = p->H;
+  a.H_kv = p->H_kv;
+  a.n = p->n;
+  a.A = p->A;
+  a.w = p->w > 1 ? p->w : 1;
+  a.scale_log2 = p->scale * 1.4426950408889634f;
+  a.err = at<int>(ws, L.err);
+  return a;
+}
+
+}  // namespace
+}  // namespace focus
+
+using namespace focus;
+
+extern "C" {
+
+int32_t focus_abi_version(void) { return FOCUS_ABI_VERSION; }
+
+const char* focus_status_string(focus_status_t s) {
+  switch (s) {
+    case FOCUS_OK: return "ok";
+    case FOCUS_ERR_INVALID_ARG: return "invalid argument";
+    case FOCUS_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case FOCUS_ERR_WORKSPACE: return "workspace too small";
+    case FOCUS_ERR_CUDA: return "CUDA error";
+    case FOCUS_ERR_TIMEOUT: return "device wait timed out";
+    case FOCUS_ERR_BAD_GROUP_ID: return "group id outside [0, K)";
+  }
+  return "unknown status";
+}
+
+size_t focus_workspace_bytes(const focus_params_t* p) {
+  if (!params_ok(p)) return 0;
+  return layout_of(p).total;
+}
+
+focus_status_t focus_workspace_init(void* ws, void* stream) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return FOCUS_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(ws, 0, kAlign, static_cast<cudaStream_t>(stream)));
+}
+
+focus_status_t focus_assign(const focus_params_t* p, const void* h, const void* W, const void* C,
+                            int32_t* gid, void* ws, size_t ws_bytes, void* stream) {
+  if (!params_ok(p)) return FOCUS_ERR_INVALID_ARG;
+  if (!h || !W || !C || !gid || !aligned16(h) || !aligned16(W) || !aligned16(C) || !aligned16(gid))
+    return FOCUS_ERR_INVALID_ARG;
+  if (focus_status_t s = check_ws(p, ws, ws_bytes)) return s;
+  if (focus_status_t s = ensure_setup()) return s;
+  const Layout L = layout_of(p);
+  AssignLaunch al{h, W, C, gid, p->B, p->n, p->D, p->d_g, p->K, p->A, at<int>(ws, L.err)};
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (p->dtype == FOCUS_F32) {
+    if (!(p->d_g == 16 || p->d_g == 32 || p->d_g == 64 || p->d_g == 128)) return FOCUS_ERR_UNSUPPORTED;
+    return cuda_status(launch_assign_f32(al, st));
+  }
+  if (!(p->d_g == 32 || p->d_g == 64 || p->d_g == 128)) return FOCUS_ERR_UNSUPPORTED;
+  if (p->A * p->d_g > 512 || p->D % 8 != 0) return FOCUS_ERR_UNSUPPORTED;
+  const int ncol = p->A * p->d_g;
+  CUtensorMap tm_h, tm_w;
+  if (!make_map(&tm_h, h, p->D, static_cast<uint64_t>(p->B) * p->n, 1, 128, 2) ||
+      !make_map(&tm_w, W, p->D, ncol, 1, ncol < 256 ? ncol : 256, 2))
+    return FOCUS_ERR_CUDA;
+  return cuda_status(launch_assign_bf16(al, &tm_h, &tm_w, st));
+}
+
+focus_status_t focus_build_index(const focus_params_t* p, const int32_t* gid,
+                                 focus_index_t* idx_out, void* ws, size_t ws_bytes, void* stream) {
+  if (!params_ok(p) || !gid || !idx_out || !aligned16(gid)) return FOCUS_ERR_INVALID_ARG;
+  if (focus_status_t s = check_ws(p, ws, ws_bytes)) return s;
+  if (focus_status_t s = ensure_setup()) return s;
+  const Layout L = layout_of(p);
+  IndexLaunch il{};
+  il.gid = gid;
+  il.P = p->B * p->A;
+  il.A = p->A;
+  il.n = p->n;
+  il.K = p->K;
+  il.w_eff = p->w > 1 ? p->w : 1;
+  il.segcnt = at<int32_t>(ws, L.segcnt);
+  il.counts = at<int32_t>(ws, L.counts);
+  il.offsets = at<int32_t>(ws, L.offsets);
+  il.tile_base = at<int32_t>(ws, L.tile_base);
+  il.perm = at<int32_t>(ws, L.perm);
+  il.rank = at<int32_t>(ws, L.rank);
+  il.farlen_tok = at<int32_t>(ws, L.far_tok);
+  il.farlen_slot = at<int32_t>(ws, L.far_slot);
+  il.items = at<focus_item_t>(ws, L.items);
+  il.cost = at<int32_t>(ws, L.cost);
+  il.order = at<int32_t>(ws, L.order);
+  il.n_items = at<int32_t>(ws, L.n_items);
+  il.max_items = L.max_items;
+  il.err = at<int>(ws, L.err);
+  const focus_status_t s = cuda_status(launch_build_index(il, static_cast<cudaStream_t>(stream)));
+  if (s != FOCUS_OK) return s;
+  idx_out->counts = il.counts;
+  idx_out->offsets = il.offsets;
+  idx_out->perm = il.perm;
+  idx_out->rank = il.rank;
+  idx_out->farlen_tok = il.farlen_tok;
+  idx_out->farlen_slot = il.farlen_slot;
+  idx_out->items = il.items;
+  idx_out->order = il.order;
+  idx_out->n_items = il.n_items;
+  idx_out->max_items = il.max_items;
+  idx_out->w_eff = il.w_eff;
+  return FOCUS_OK;
+}
+
+static focus_status_t attention_common(const focus_params_t* p, const void* Q, const void* K,
+                                       const void* V, void* O, float* lse, void* ws,
+                                       size_t ws_bytes) {
+  if (!params_ok(p)) return FOCUS_ERR_INVALID_ARG;
+  if (!Q || !K || !V || !O || !aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) ||
+      (lse && !aligned16(lse)))
+    return FOCUS_ERR_INVALID_ARG;
+  if (!(p->d == 64 || p->d == 128)) return FOCUS_ERR_UNSUPPORTED;
+  if (focus_status_t s = check_ws(p, ws, ws_bytes)) return s;
+  return ensure_setup();
+}
+
+focus_status_t focus_attention_fwd(const focus_params_t* p, const void* Q, const void* K,
+                                   const void* V, const focus_index_t* idx, void* O, float* lse_opt,
+                                   void* ws, size_t ws_bytes, void* stream) {
+  if (!idx || !idx->perm || !idx->farlen_tok || !idx->farlen_slot || !idx->items || !idx->order ||
+      !idx->n_items)
+    return FOCUS_ERR_INVALID_ARG;
+  if (params_ok(p) && (idx->max_items != layout_of(p).max_items || idx->w_eff != (p->w > 1 ? p->w : 1)))
+    return FOCUS_ERR_INVALID_ARG;
+  if (focus_status_t s = attention_common(p, Q, K, V, O, lse_opt, ws, ws_bytes)) return s;
+  const Layout L = layout_of(p);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  AttnArgs a = attn_args(p, Q, K, V, O, lse_opt, ws, L);
+  a.perm = idx->perm;
+  a.farlen_tok = idx->farlen_tok;
+  a.farlen_slot = idx->farlen_slot;
+  a.items = idx->items;
+  a.order = idx->order;
+  a.n_items = idx->n_items;
+  if (p->dtype == FOCUS_F32) {
+    cudaError_t e = launch_attn_simt_f32(a, p->d, kModeGroup, L.max_items, st);
+    if (e == cudaSuccess) e = launch_attn_simt_f32(a, p->d, kModeLocal, 0, st);
+    return cuda_status(e);
+  }
+  void* Ks = at<void>(ws, L.Ks);
+  void* Vs = at<void>(ws, L.Vs);
+  cudaError_t e = launch_permute_kv_bf16(K, V, Ks, Vs, idx->perm, p->B, p->H_kv, p->n, p->d, p->A, st);
+  if (e != cudaSuccess) return FOCUS_ERR_CUDA;
+  CUtensorMap tk, tv, tks, tvs;
+  const uint64_t planes = static_cast<uint64_t>(p->B) * p->H_kv;
+  if (!make_map(&tk, K, p->d, p->n, planes, 128, 3) || !make_map(&tv, V, p->d, p->n, planes, 128, 3) ||
+      !make_map(&tks, Ks, p->d, p->n, planes, 128, 3) || !make_map(&tvs, Vs, p->d, p->n, planes, 128, 3))
+    return FOCUS_ERR_CUDA;
+  e = launch_attn_tc_bf16(a, &tks, &tvs, p->d, kModeGroup, L.max_items, st);
+  if (e == cudaSuccess) e = launch_attn_tc_bf16(a, &tk, &tv, p->d, kModeLocal, 0, st);
+  return cuda_status(e);
+}
+
+focus_status_t focus_dense_causal_fwd(const focus_params_t* p, const void* Q, const void* K,
+                                      const void* V, void* O, float* lse_opt, void* ws,
+                                      size_t ws_bytes, void* stream) {
+  if (focus_status_t s = attention_common(p, Q, K, V, O, lse_opt, ws, ws_bytes)) return s;
+  const Layout L = layout_of(p);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  AttnArgs a = attn_args(p, Q, K, V, O, lse_opt, ws, L);
+  a.w = p->n;
+  if (p->dtype == FOCUS_F32) return cuda_status(launch_attn_simt_f32(a, p->d, kModeDense, 0, st));
+  CUtensorMap tk, tv;
+  const uint64_t planes = static_cast<uint64_t>(p->B) * p->H_kv;
+  if (!make_map(&tk, K, p->d, p->n, planes, 128, 3) || !make_map(&tv, V, p->d, p->n, planes, 128, 3))
+    return FOCUS_ERR_CUDA;
+  return cuda_status(launch_attn_tc_bf16(a, &tk, &tv, p->d, kModeDense, 0, st));
+}
+
+focus_status_t focus_layer_fwd_host(const focus_params_t* p, const void* host_h,
+                                    const void* host_W, const void* host_C, const void* host_Q,
+                                    const void* host_K, const void* host_V, void* host_O,
+                                    void* d_h, void* d_W, void* d_C, void* d_Q, void* d_K,
+                                    void* d_V, void* d_O, int32_t* d_gid, void* ws,
+                                    size_t ws_bytes, void* stream) {
+  if (!params_ok(p)) return FOCUS_ERR_INVALID_ARG;
+  if (!host_h || !host_W || !host_C || !host_Q || !host_K || !host_V || !host_O)
+    return FOCUS_ERR_INVALID_ARG;
+  const size_t es = elt_size(p->dtype);
+  const size_t nb = static_cast<size_t>(p->B) * p->n;
+  const size_t bytes_h = nb * p->D * es;
+  const size_t bytes_W = static_cast<size_t>(p->A) * p->d_g * p->D * es;
+  const size_t bytes_C = static_cast<size_t>(p->A) * p->K * p->d_g * es;
+  const size_t bytes_Q = nb * p->H * p->d * es;
+  const size_t bytes_KV = nb * p->H_kv * p->d * es;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const struct { void* dst; const void* src; size_t n; } up[] = {
+      {d_h, host_h, bytes_h}, {d_W, host_W, bytes_W}, {d_C, host_C, bytes_C},
+      {d_Q, host_Q, bytes_Q}, {d_K, host_K, bytes_KV}, {d_V, host_V, bytes_KV}};
+  for (const auto& c : up) {
+    if (!c.dst) return FOCUS_ERR_INVALID_ARG;
+    if (cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return FOCUS_ERR_CUDA;
+  }
+  focus_status_t s = focus_assign(p, d_h, d_W, d_C, d_gid, ws, ws_bytes, stream);
+  if (s) return s;
+  focus_index_t idx{};
+  s = focus_build_index(p, d_gid, &idx, ws, ws_bytes, stream);
+  if (s) return s;
+  s = focus_attention_fwd(p, d_Q, d_K, d_V, &idx, d_O, nullptr, ws, ws_bytes, stream);
+  if (s) return s;
+  return cuda_status(cudaMemcpyAsync(host_O, d_O, bytes_Q, cudaMemcpyDeviceToHost, st));
+}
+
+focus_status_t focus_check_errors(void* ws, void* stream) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return FOCUS_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FOCUS_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FOCUS_ERR_CUDA;
+  if (word == 0) return FOCUS_OK;
+  if (cudaMemset(ws, 0, sizeof(int)) != cudaSuccess) return FOCUS_ERR_CUDA;
+  if (word & kErrTimeout) return FOCUS_ERR_TIMEOUT;
+  if (word & kErrBadGroup) return FOCUS_ERR_BAD_GROUP_ID;
+  return FOCUS_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,264 @@
+// focus_assign kernels: nearest-centroid group ids.
+//
+// "Focus: Learning Which Attention Pairs Matter", section 2.1: each hidden
+// state h_i is projected and compared with K learnable centroids; section 2.2
+// and "Why Attend to Everything? Focus is the Key", section 2.3: at inference
+// the assignment is hard (top-1 here).  Per token and assignment a:
+//   p = W_a h (fp32 accumulate, kept in fp32), s_k = p . c_k (fp32),
+//   g = argmax_k s_k, lowest k on ties.
+//
+// bf16: the projection is a [128 tokens x A*d_g] tile of h W^T on the
+// tcgen05 tensor cores (TMA-fed 4..6-stage pipeline, fp32 accumulator in
+// TMEM); the epilogue reads each token's row of p from TMEM and scores the
+// centroids with fp32 FMAs, so p is never rounded below fp32.
+// fp32: one thread per token on the CUDA cores.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace focus {
+namespace {
+
+// ------------------------------------------------------------------ fp32 ---
+template <int DG>
+__global__ void __launch_bounds__(128) assign_f32_kernel(const float* __restrict__ h,
+                                                         const float* __restrict__ W,
+                                                         const float* __restrict__ C,
+                                                         int32_t* __restrict__ gid, int B, int n,
+                                                         int D, int K, int A) {
+  const int tok = blockIdx.x * blockDim.x + threadIdx.x;
+  if (tok >= B * n) return;
+  const int b = tok / n, i = tok % n;
+  const float* hr = h + static_cast<size_t>(tok) * D;
+  for (int a = 0; a < A; ++a) {
+    float p[DG];
+#pragma unroll
+    for (int r = 0; r < DG; ++r) p[r] = 0.f;
+    const float* Wa = W + static_cast<size_t>(a) * DG * D;
+    for (int c = 0; c < D; ++c) {
+      const float x = hr[c];
+#pragma unroll
+      for (int r = 0; r < DG; ++r) p[r] = fmaf(__ldg(Wa + static_cast<size_t>(r) * D + c), x, p[r]);
+    }
+    const float* Ca = C + static_cast<size_t>(a) * K * DG;
+    int best = 0;
+    float bs = -INFINITY;
+    for (int k = 0; k < K; ++k) {
+      float s = 0.f;
+#pragma unroll
+      for (int r = 0; r < DG; ++r) s = fmaf(p[r], __ldg(Ca + static_cast<size_t>(k) * DG + r), s);
+      if (s > bs || k == 0) {
+        bs = s;
+        best = k;
+      }
+    }
+    gid[(static_cast<size_t>(b) * A + a) * n + i] = best;
+  }
+}
+
+// ------------------------------------------------------------ bf16 tcgen05 ---
+constexpr int kBM = 128;          // tokens per CTA
+constexpr int kBK = 64;           // hidden elements per stage (one 128 B swizzle row)
+
+template <int NALLOC>
+struct AssignCfg {
+  static constexpr int kStageA = kBM * kBK * 2;            // 16 KB
+  static constexpr int kStageB = NALLOC * kBK * 2;         // <= 64 KB
+  static constexpr int kStage = kStageA + kStageB;
+  static constexpr int kStages = (196 * 1024 / kStage) > 6 ? 6 : (196 * 1024 / kStage);
+  static constexpr int kSmem = kStages * kStage + 1024 /*align*/ + 256 /*barriers*/;
+};
+
+template <int NALLOC>
+__global__ void __launch_bounds__(128, 1) assign_tc_kernel(
+    const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
+    const __nv_bfloat16* __restrict__ C, int32_t* __restrict__ gid, int B, int n, int D, int d_g,
+    int K, int A, int* err) {
+  using Cfg = AssignCfg<NALLOC>;
+  constexpr int S = Cfg::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * Cfg::kStage);
+  uint64_t* empty = full + S;
+  uint64_t* done = empty + S;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = warp_id(), lane = lane_id();
+  const int ncol = A * d_g;
+  const int m0 = blockIdx.x * kBM;
+  const int nk = (D + kBK - 1) / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(done, 1);
+    *abort = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tm_h);
+    prefetch_tmap(&tm_w);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, NALLOC);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // producer: h tile [128 x 64] and W tile [ncol x 64] per stage; W rows come
+    // in boxes of wbox rows (the tensor map's box height)
+    const int wbox = ncol < 256 ? ncol : 256;
+    const int wloads = (ncol + wbox - 1) / wbox;
+    const uint32_t bytes = Cfg::kStageA + wloads * wbox * kBK * 2;
+    int issued = 0;
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % S, u = kb / S;
+      if (u > 0 && !mbar_wait(&empty[s], (u - 1) & 1, abort, err)) break;
+      uint8_t* sa = smem + s * Cfg::kStage;
+      uint8_t* sb = sa + Cfg::kStageA;
+      mbar_expect_tx(&full[s], bytes);
+      tma_load_2d(sa, &tm_h, &full[s], kb * kBK, m0);
+      for (int l = 0; l < wloads; ++l) tma_load_2d(sb + l * wbox * 128, &tm_w, &full[s], kb * kBK, l * wbox);
+      ++issued;
+    }
+    if (*abort) {
+      // let copies already in flight land before the CTA exits
+      for (int kb = max(0, issued - S); kb < issued; ++kb) {
+        if (!mbar_wait(&full[kb % S], (kb / S) & 1, abort, err)) {
+          // the abort flag is already up; a bounded wait on the timer remains
+          const unsigned long long t0 = global_ns();
+          while (!mbar_try_wait(&full[kb % S], (kb / S) & 1) && global_ns() - t0 < kWaitTimeoutNs) {}
+        }
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // MMA issuer: D[128 x ncol] += h_tile * W_tile^T, N split in <= 256 chunks
+    bool ok = true;
+    for (int kb = 0; kb < nk && ok; ++kb) {
+      const int s = kb % S, u = kb / S;
+      if (!mbar_wait(&full[s], u & 1, abort, err)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t sa = smem_u32(smem + s * Cfg::kStage);
+      const uint32_t sb = sa + Cfg::kStageA;
+#pragma unroll
+      for (int kk = 0; kk < kBK / 16; ++kk) {
+        const uint64_t ad = sw128_desc(sa + kk * 32, 16, 1024);
+        for (int c0 = 0; c0 < ncol; c0 += 256) {
+          const int nn = min(256, ncol - c0);
+          const uint64_t bd = sw128_desc(sb + c0 * 128 + kk * 32, 16, 1024);
+          mma_ss(tmem + c0, ad, bd, idesc_bf16_f32(128, nn, false, false), (kb | kk) != 0);
+        }
+      }
+      mma_commit(&empty[s]);
+    }
+    mma_commit(done);
+  }
+  __syncwarp();
+
+  // epilogue (all 4 warps): warp w owns TMEM lanes 32w..32w+31 = tokens m0+32w+lane
+  const bool got = mbar_wait(done, 0, abort, err);
+  tc_fence_after();
+  __syncthreads();   // pipeline smem is free from here on: reuse it for centroids
+  float* Cs = reinterpret_cast<float*>(smem);
+  const int kc = (S * Cfg::kStage) / (d_g * 4);   // centroids per shared-memory chunk
+  const int row = warp * 32 + lane;
+  const int tok = m0 + row;
+  for (int a = 0; a < A; ++a) {
+    float p[128];
+#pragma unroll
+    for (int c = 0; c < 128; c += 32) {
+      if (c < d_g) {
+        uint32_t r[32];
+        tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + a * d_g + c, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) p[c + j] = __uint_as_float(r[j]);
+      }
+    }
+    int best = 0;
+    float bs = -INFINITY;
+    for (int k0 = 0; k0 < K; k0 += kc) {
+      const int kn = min(kc, K - k0);
+      __syncthreads();
+      for (int e = threadIdx.x; e < kn * d_g; e += blockDim.x)
+        Cs[e] = __bfloat162float(C[(static_cast<size_t>(a) * K + k0) * d_g + e]);
+      __syncthreads();
+      for (int k = 0; k < kn; ++k) {
+        const float* ck = Cs + k * d_g;
+        float s = 0.f;
+#pragma unroll
+        for (int j = 0; j < 128; ++j)
+          if (j < d_g) s = fmaf(p[j], ck[j], s);
+        if (s > bs || k0 + k == 0) {
+          bs = s;
+          best = k0 + k;
+        }
+      }
+    }
+    if (got && !*abort && tok < B * n) {
+      const int b = tok / n, i = tok % n;
+      gid[(static_cast<size_t>(b) * A + a) * n + i] = best;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, NALLOC);
+  }
+}
+
+template <int NALLOC>
+cudaError_t launch_tc(const AssignLaunch& L, const CUtensorMap* tm_h, const CUtensorMap* tm_w,
+                      cudaStream_t st) {
+  const int grid = (L.B * L.n + kBM - 1) / kBM;
+  assign_tc_kernel<NALLOC><<<grid, 128, AssignCfg<NALLOC>::kSmem, st>>>(
+      *tm_h, *tm_w, static_cast<const __nv_bfloat16*>(L.C), L.gid, L.B, L.n, L.D, L.d_g, L.K,
+      L.A, L.err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_assign_f32(const AssignLaunch& L, cudaStream_t st) {
+  const int grid = (L.B * L.n + 127) / 128;
+  const float* h = static_cast<const float*>(L.h);
+  const float* W = static_cast<const float*>(L.W);
+  const float* C = static_cast<const float*>(L.C);
+  switch (L.d_g) {
+    case 16: assign_f32_kernel<16><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.B, L.n, L.D, L.K, L.A); break;
+    case 32: assign_f32_kernel<32><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.B, L.n, L.D, L.K, L.A); break;
+    case 64: assign_f32_kernel<64><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.B, L.n, L.D, L.K, L.A); break;
+    case 128: assign_f32_kernel<128><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.B, L.n, L.D, L.K, L.A); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_assign_bf16(const AssignLaunch& L, const CUtensorMap* tm_h,
+                               const CUtensorMap* tm_w, cudaStream_t st) {
+  const int ncol = L.A * L.d_g;
+  if (ncol <= 32) return launch_tc<32>(L, tm_h, tm_w, st);
+  if (ncol <= 64) return launch_tc<64>(L, tm_h, tm_w, st);
+  if (ncol <= 128) return launch_tc<128>(L, tm_h, tm_w, st);
+  if (ncol <= 256) return launch_tc<256>(L, tm_h, tm_w, st);
+  if (ncol <= 512) return launch_tc<512>(L, tm_h, tm_w, st);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t setup_assign_kernels() {
+  cudaError_t e;
+#define FOCUS_SET_SMEM(N)                                                                   \
+  e = cudaFuncSetAttribute(assign_tc_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                           AssignCfg<N>::kSmem);                                            \
+  if (e != cudaSuccess) return e;
+  FOCUS_SET_SMEM(32)
+  FOCUS_SET_SMEM(64)
+  FOCUS_SET_SMEM(128)
+  FOCUS_SET_SMEM(256)
+  FOCUS_SET_SMEM(512)
+#undef FOCUS_SET_SMEM
+  return cudaSuccess;
+}
+
+}  // namespace focus

@@ -1,0 +1,366 @@
+// focus_build_index kernels: the group-sorted token index.
+//
+// "Focus: Learning Which Attention Pairs Matter", section 2.2: at inference
+// every token goes to one group and far pairs of different groups are skipped,
+// so the far part of attention only ever pairs tokens of one group.  Sorting
+// tokens by (group, position) turns each group into a contiguous run of
+// sorted slots, which the group pass then walks as dense tiles.
+//
+// Five small launches per call, all integer work:
+//   count    per (segment, group) histogram of ids          grid (nseg, P)
+//   scan     group counts, offsets, per-segment bases,
+//            per-group tile bases                           grid (P)
+//   scatter  stable placement: perm (slot -> position) and
+//            rank (position -> slot); warp match + popc     grid (nseg, P)
+//   farlen   per slot: same-group tokens at or before
+//            position - w (binary search in the group run)  grid (n/256, P)
+//   items    work list in canonical order, compacted, and
+//            a longest-first schedule (stable counting sort) grid (1)
+// P = B * A independent problems.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace focus {
+
+namespace {
+
+__device__ __forceinline__ int clamp_gid(int g, int K, int* err) {
+  if (static_cast<unsigned>(g) >= static_cast<unsigned>(K)) {
+    atomicOr(err, kErrBadGroup);
+    g = g < 0 ? 0 : K - 1;
+  }
+  return g;
+}
+
+// Exclusive scan of one value per thread over a 1024-thread block.
+__device__ int block_excl_scan(int v, int* warp_sums, int* total) {
+  const int lane = lane_id(), warp = warp_id();
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int s = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    warp_sums[lane] = s;
+  }
+  __syncthreads();
+  int excl = x - v + (warp > 0 ? warp_sums[warp - 1] : 0);
+  *total = warp_sums[31];
+  __syncthreads();
+  return excl;
+}
+
+// In-place exclusive scan of L <= 4 * 1024 ints in shared memory; returns the total.
+__device__ int block_scan_smem(int* a, int L, int* warp_sums) {
+  constexpr int kPer = 4;
+  const int t = threadIdx.x;
+  int v[kPer];
+  int s = 0;
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    int idx = t * kPer + k;
+    v[k] = idx < L ? a[idx] : 0;
+    s += v[k];
+  }
+  int total;
+  int run = block_excl_scan(s, warp_sums, &total);
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    int idx = t * kPer + k;
+    if (idx < L) a[idx] = run;
+    run += v[k];
+  }
+  __syncthreads();
+  return total;
+}
+
+__device__ __forceinline__ int upper_bound_minus1(const int* a, int len, int v) {
+  // largest i in [0, len) with a[i] <= v, given a[0] <= v < a[len]
+  int lo = 0, hi = len;
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (a[mid] <= v) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(256) index_count_kernel(const int32_t* __restrict__ gid, int n,
+                                                          int K, int nseg,
+                                                          int32_t* __restrict__ segcnt, int* err) {
+  extern __shared__ int hist[];
+  const int p = blockIdx.y, seg = blockIdx.x;
+  for (int g = threadIdx.x; g < K; g += blockDim.x) hist[g] = 0;
+  __syncthreads();
+  const int32_t* gp = gid + static_cast<size_t>(p) * n;
+  const int start = seg * kIndexSeg, end = min(n, start + kIndexSeg);
+  for (int i = start + threadIdx.x; i < end; i += blockDim.x) {
+    atomicAdd(&hist[clamp_gid(__ldg(gp + i), K, err)], 1);
+  }
+  __syncthreads();
+  int32_t* out = segcnt + (static_cast<size_t>(p) * nseg + seg) * K;
+  for (int g = threadIdx.x; g < K; g += blockDim.x) out[g] = hist[g];
+}
+
+__global__ void __launch_bounds__(1024) index_scan_kernel(int n, int K, int nseg,
+                                                          int32_t* __restrict__ segcnt,
+                                                          int32_t* __restrict__ counts,
+                                                          int32_t* __restrict__ offsets,
+                                                          int32_t* __restrict__ tile_base) {
+  extern __shared__ int sm[];
+  int* cnt = sm;              // K
+  int* tiles = sm + K;        // K
+  __shared__ int warp_sums[32];
+  const int p = blockIdx.x;
+  int32_t* sc = segcnt + static_cast<size_t>(p) * nseg * K;
+  for (int g = threadIdx.x; g < K; g += blockDim.x) {
+    int s = 0;
+    for (int seg = 0; seg < nseg; ++seg) s += sc[static_cast<size_t>(seg) * K + g];
+    cnt[g] = s;
+    counts[static_cast<size_t>(p) * K + g] = s;
+    tiles[g] = (s + kTileM - 1) / kTileM;
+  }
+  __syncthreads();
+  int total = block_scan_smem(cnt, K, warp_sums);      // cnt -> offsets
+  int ttot = block_scan_smem(tiles, K, warp_sums);     // tiles -> tile bases
+  int32_t* off = offsets + static_cast<size_t>(p) * (K + 1);
+  int32_t* tb = tile_base + static_cast<size_t>(p) * (K + 1);
+  for (int g = threadIdx.x; g < K; g += blockDim.x) {
+    off[g] = cnt[g];
+    tb[g] = tiles[g];
+    int run = cnt[g];
+    for (int seg = 0; seg < nseg; ++seg) {
+      int32_t* c = sc + static_cast<size_t>(seg) * K + g;
+      int v = *c;
+      *c = run;
+      run += v;
+    }
+  }
+  if (threadIdx.x == 0) {
+    off[K] = total;
+    tb[K] = ttot;
+  }
+  (void)n;
+}
+
+__global__ void __launch_bounds__(256) index_scatter_kernel(const int32_t* __restrict__ gid, int n,
+                                                            int K, int nseg,
+                                                            const int32_t* __restrict__ segbase,
+                                                            int32_t* __restrict__ perm,
+                                                            int32_t* __restrict__ rank, int* err) {
+  extern __shared__ int sm[];
+  int* base = sm;                                                  // K
+  uint16_t* wc = reinterpret_cast<uint16_t*>(sm + K);              // [8][K]
+  const int p = blockIdx.y, seg = blockIdx.x;
+  const int lane = lane_id(), warp = warp_id();
+  const int32_t* gp = gid + static_cast<size_t>(p) * n;
+  const int32_t* sb = segbase + (static_cast<size_t>(p) * nseg + seg) * K;
+  for (int g = threadIdx.x; g < K; g += blockDim.x) base[g] = sb[g];
+  for (int e = threadIdx.x; e < 8 * K; e += blockDim.x) wc[e] = 0;
+  __syncthreads();
+  const unsigned lt = (1u << lane) - 1u;
+  const int wbeg = seg * kIndexSeg + warp * (kIndexSeg / 8);
+  // per-warp group counts over this warp's 128 tokens
+  for (int c = 0; c < kIndexSeg / 8; c += 32) {
+    const int i = wbeg + c + lane;
+    const bool valid = i < n;
+    const int g = valid ? clamp_gid(__ldg(gp + i), K, err) : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, g);
+    if (valid && lane == __ffs(peers) - 1) wc[warp * K + g] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  for (int g = threadIdx.x; g < K; g += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < 8; ++w) {
+      int v = wc[w * K + g];
+      wc[w * K + g] = static_cast<uint16_t>(run);
+      run += v;
+    }
+  }
+  __syncthreads();
+  int32_t* pp = perm + static_cast<size_t>(p) * n;
+  int32_t* rp = rank + static_cast<size_t>(p) * n;
+  for (int c = 0; c < kIndexSeg / 8; c += 32) {
+    const int i = wbeg + c + lane;
+    const bool valid = i < n;
+    const int g = valid ? clamp_gid(__ldg(gp + i), K, err) : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, g);
+    if (valid) {
+      const int slot = base[g] + wc[warp * K + g] + __popc(peers & lt);
+      pp[slot] = i;
+      rp[i] = slot;
+    }
+    __syncwarp();
+    if (valid && lane == __ffs(peers) - 1) wc[warp * K + g] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+__global__ void __launch_bounds__(256) index_farlen_kernel(int n, int K, int w_eff,
+                                                           const int32_t* __restrict__ offsets,
+                                                           const int32_t* __restrict__ perm,
+                                                           int32_t* __restrict__ farlen_tok,
+                                                           int32_t* __restrict__ farlen_slot) {
+  extern __shared__ int offs[];  // K + 1
+  const int p = blockIdx.y;
+  const int32_t* op = offsets + static_cast<size_t>(p) * (K + 1);
+  for (int g = threadIdx.x; g <= K; g += blockDim.x) offs[g] = op[g];
+  __syncthreads();
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= n) return;
+  const int32_t* pp = perm + static_cast<size_t>(p) * n;
+  const int pos = pp[s];
+  const int g = upper_bound_minus1(offs, K, s);
+  // members of g at slots [offs[g], s) have positions < pos; count those
+  // with position <= pos - w_eff, i.e. < target
+  const int target = pos - w_eff + 1;
+  int lo = offs[g], hi = s;   // first slot in [lo, hi) whose position >= target
+  while (lo < hi) {
+    int mid = (lo + hi) >> 1;
+    if (__ldg(pp + mid) < target) lo = mid + 1; else hi = mid;
+  }
+  const int fl = lo - offs[g];
+  farlen_slot[static_cast<size_t>(p) * n + s] = fl;
+  farlen_tok[static_cast<size_t>(p) * n + pos] = fl;
+}
+
+__global__ void __launch_bounds__(1024) index_items_kernel(
+    int P, int A, int n, int K, const int32_t* __restrict__ counts,
+    const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_base,
+    const int32_t* __restrict__ farlen_slot, focus_item_t* __restrict__ items,
+    int32_t* __restrict__ cost, int32_t* __restrict__ order, int32_t* __restrict__ n_items,
+    int max_items, int* err) {
+  extern __shared__ int sm[];
+  int* pbase = sm;                 // P + 1
+  int* hist = sm + P + 1;          // nb + 1
+  __shared__ int warp_sums[32];
+  const int nb = (n + kTileN - 1) / kTileN + 1;   // cost buckets 0..nb-1
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int p = 0; p < P; ++p) {
+      pbase[p] = run;
+      run += tile_base[static_cast<size_t>(p) * (K + 1) + K];
+    }
+    pbase[P] = run;
+  }
+  for (int c = threadIdx.x; c < nb; c += blockDim.x) hist[c] = 0;
+  __syncthreads();
+  const int total = pbase[P];
+  int out = 0;
+  for (int c0 = 0; c0 < total; c0 += blockDim.x) {
+    const int c = c0 + threadIdx.x;
+    int flag = 0;
+    focus_item_t it{};
+    if (c < total) {
+      const int p = upper_bound_minus1(pbase, P, c);
+      const int t = c - pbase[p];
+      const int32_t* tb = tile_base + static_cast<size_t>(p) * (K + 1);
+      // group of candidate tile t: largest g with tb[g] <= t (tb[K] > t)
+      int lo = 0, hi = K;
+      while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if (__ldg(tb + mid) <= t) lo = mid; else hi = mid;
+      }
+      const int g = lo;
+      const int tt = t - tb[g];
+      const int off = offsets[static_cast<size_t>(p) * (K + 1) + g];
+      const int cnt = counts[static_cast<size_t>(p) * K + g];
+      it.b = p / A;
+      it.a = p % A;
+      it.g = g;
+      it.row0 = off + tt * kTileM;
+      it.rows = min(kTileM, cnt - tt * kTileM);
+      it.key0 = off;
+      if (it.rows <= 0) {
+        atomicOr(err, kErrInternal);
+      } else {
+        it.keys = farlen_slot[static_cast<size_t>(p) * n + it.row0 + it.rows - 1];
+        flag = it.keys > 0;
+      }
+    }
+    int tot;
+    const int pos = block_excl_scan(flag, warp_sums, &tot);
+    if (flag && out + pos < max_items) {
+      items[out + pos] = it;
+      const int cb = (it.keys + kTileN - 1) / kTileN;
+      cost[out + pos] = cb;
+      atomicAdd(&hist[cb], 1);
+    }
+    out += tot;
+  }
+  if (out > max_items) {
+    if (threadIdx.x == 0) atomicOr(err, kErrInternal);
+    out = max_items;
+  }
+  __syncthreads();
+  // start of each cost bucket in descending-cost order
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int cb = nb - 1; cb >= 0; --cb) {
+      int v = hist[cb];
+      hist[cb] = run;
+      run += v;
+    }
+    *n_items = out;
+  }
+  __syncthreads();
+  if (warp_id() == 0) {
+    const int lane = lane_id();
+    const unsigned lt = (1u << lane) - 1u;
+    for (int c0 = 0; c0 < out; c0 += 32) {
+      const int c = c0 + lane;
+      const int cb = c < out ? cost[c] : -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, cb);
+      if (c < out) order[hist[cb] + __popc(peers & lt)] = c;
+      __syncwarp();
+      if (c < out && lane == __ffs(peers) - 1) hist[cb] += __popc(peers);
+      __syncwarp();
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_build_index(const IndexLaunch& L, cudaStream_t st) {
+  const int P = L.P;
+  const int nseg = (L.n + kIndexSeg - 1) / kIndexSeg;
+  const size_t sm_count = static_cast<size_t>(L.K) * sizeof(int);
+  index_count_kernel<<<dim3(nseg, P), 256, sm_count, st>>>(L.gid, L.n, L.K, nseg, L.segcnt, L.err);
+  const size_t sm_scan = 2 * static_cast<size_t>(L.K) * sizeof(int);
+  index_scan_kernel<<<P, 1024, sm_scan, st>>>(L.n, L.K, nseg, L.segcnt, L.counts, L.offsets,
+                                              L.tile_base);
+  const size_t sm_scatter = static_cast<size_t>(L.K) * sizeof(int) + 8 * static_cast<size_t>(L.K) * 2;
+  index_scatter_kernel<<<dim3(nseg, P), 256, sm_scatter, st>>>(L.gid, L.n, L.K, nseg, L.segcnt,
+                                                                L.perm, L.rank, L.err);
+  const size_t sm_far = static_cast<size_t>(L.K + 1) * sizeof(int);
+  index_farlen_kernel<<<dim3((L.n + 255) / 256, P), 256, sm_far, st>>>(
+      L.n, L.K, L.w_eff, L.offsets, L.perm, L.farlen_tok, L.farlen_slot);
+  const int nb = (L.n + kTileN - 1) / kTileN + 1;
+  const size_t sm_items = static_cast<size_t>(P + 1 + nb) * sizeof(int);
+  index_items_kernel<<<1, 1024, sm_items, st>>>(P, L.A, L.n, L.K, L.counts, L.offsets,
+                                                L.tile_base, L.farlen_slot, L.items, L.cost,
+                                                L.order, L.n_items, L.max_items, L.err);
+  return cudaGetLastError();
+}
+
+cudaError_t setup_index_kernels() {
+  // dynamic shared memory above 48 KB for the largest K and n
+  cudaError_t e = cudaFuncSetAttribute(index_scatter_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kMaxK * 4 + 8 * kMaxK * 2);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(index_items_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           160 * 1024);
+  return e;
+}
+
+}  // namespace focus

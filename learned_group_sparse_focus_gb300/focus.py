@@ -1,0 +1,210 @@
+"""Python binding of libfocus.so (the Focus C ABI declared in include/focus.h).
+
+Argument marshalling only: every step of the hot path runs in the library's
+CUDA kernels.  PyTorch provides device memory and streams.  If the compiled
+library is missing, importing this module raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libfocus.so")
+
+F32, BF16 = 0, 1
+TILE_M = 128
+TILE_N = 128
+
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace too small",
+          4: "CUDA error", 5: "device wait timed out", 6: "group id outside [0, K)"}
+
+
+class FocusError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)} ({status})")
+        self.status = status
+
+
+class Params(ctypes.Structure):
+    _fields_ = [(k, ctypes.c_int32) for k in ("B", "H", "H_kv", "n", "d", "D", "d_g", "K", "A", "w")] + \
+               [("scale", ctypes.c_float), ("dtype", ctypes.c_int32)]
+
+
+class Item(ctypes.Structure):
+    _fields_ = [(k, ctypes.c_int32) for k in ("b", "a", "g", "row0", "rows", "keys", "key0", "pad")]
+
+
+class Index(ctypes.Structure):
+    _fields_ = [("counts", ctypes.c_void_p), ("offsets", ctypes.c_void_p), ("perm", ctypes.c_void_p),
+                ("rank", ctypes.c_void_p), ("farlen_tok", ctypes.c_void_p),
+                ("farlen_slot", ctypes.c_void_p), ("items", ctypes.c_void_p),
+                ("order", ctypes.c_void_p), ("n_items", ctypes.c_void_p),
+                ("max_items", ctypes.c_int32), ("w_eff", ctypes.c_int32)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libfocus.so not built ({LIB_PATH}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, P = ctypes.c_void_p, ctypes.POINTER(Params)
+    sig = {
+        "focus_abi_version": ([], ctypes.c_int32),
+        "focus_status_string": ([ctypes.c_int], ctypes.c_char_p),
+        "focus_workspace_bytes": ([P], ctypes.c_size_t),
+        "focus_workspace_init": ([vp, vp], ctypes.c_int),
+        "focus_assign": ([P, vp, vp, vp, vp, vp, ctypes.c_size_t, vp], ctypes.c_int),
+        "focus_build_index": ([P, vp, ctypes.POINTER(Index), vp, ctypes.c_size_t, vp], ctypes.c_int),
+        "focus_attention_fwd": ([P, vp, vp, vp, ctypes.POINTER(Index), vp, vp, vp, ctypes.c_size_t, vp],
+                                ctypes.c_int),
+        "focus_dense_causal_fwd": ([P, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp], ctypes.c_int),
+        "focus_layer_fwd_host": ([P] + [vp] * 7 + [vp] * 8 + [vp, ctypes.c_size_t, vp], ctypes.c_int),
+        "focus_check_errors": ([vp, vp], ctypes.c_int),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    return lib
+
+
+_lib = _load()
+
+EXPORTED = ("focus_abi_version", "focus_status_string", "focus_workspace_bytes",
+            "focus_workspace_init", "focus_assign", "focus_build_index", "focus_attention_fwd",
+            "focus_dense_causal_fwd", "focus_layer_fwd_host", "focus_check_errors")
+
+
+def lib():
+    return _lib
+
+
+def make_params(B, H, H_kv, n, d, D, d_g, K, A, w, scale=None, dtype=BF16) -> Params:
+    if scale is None:
+        scale = 1.0 / (d ** 0.5)
+    if isinstance(dtype, str):
+        dtype = BF16 if dtype == "bf16" else F32
+    return Params(B, H, H_kv, n, d, D, d_g, K, A, w, float(scale), int(dtype))
+
+
+def params_from_workload(wl, **override) -> Params:
+    f = dict(B=wl.B, H=wl.H, H_kv=wl.H_kv, n=wl.n, d=wl.d, D=wl.D, d_g=wl.d_g, K=wl.K, A=wl.A,
+             w=wl.w, scale=wl.scale, dtype=wl.dtype)
+    f.update(override)
+    return make_params(**f)
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, torch.Tensor):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+        return t.data_ptr()
+    return int(t)
+
+
+def _stream(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _check(fn: str, st: int):
+    if st != 0:
+        raise FocusError(fn, st)
+
+
+def focus_workspace_bytes(p: Params) -> int:
+    return int(_lib.focus_workspace_bytes(ctypes.byref(p)))
+
+
+def alloc_workspace(p: Params, device="cuda", stream=None) -> torch.Tensor:
+    """Caller-owned workspace (a uint8 device tensor), error word cleared."""
+    nbytes = focus_workspace_bytes(p)
+    if nbytes == 0:
+        raise FocusError("focus_workspace_bytes", 1)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    focus_workspace_init(ws, stream)
+    return ws
+
+
+def focus_workspace_init(ws, stream=None):
+    _check("focus_workspace_init", _lib.focus_workspace_init(_ptr(ws), _stream(stream)))
+
+
+def focus_assign(p: Params, h, W, C, gid, ws, stream=None):
+    _check("focus_assign", _lib.focus_assign(ctypes.byref(p), _ptr(h), _ptr(W), _ptr(C), _ptr(gid),
+                                             _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def focus_build_index(p: Params, gid, ws, stream=None) -> Index:
+    idx = Index()
+    _check("focus_build_index", _lib.focus_build_index(ctypes.byref(p), _ptr(gid), ctypes.byref(idx),
+                                                       _ptr(ws), ws.numel(), _stream(stream)))
+    return idx
+
+
+def focus_attention_fwd(p: Params, Q, K, V, idx: Index, O, lse, ws, stream=None):
+    _check("focus_attention_fwd",
+           _lib.focus_attention_fwd(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), ctypes.byref(idx),
+                                    _ptr(O), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def focus_dense_causal_fwd(p: Params, Q, K, V, O, lse, ws, stream=None):
+    _check("focus_dense_causal_fwd",
+           _lib.focus_dense_causal_fwd(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(lse),
+                                       _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def focus_layer_fwd_host(p: Params, host: dict, dev: dict, ws, stream=None):
+    """host: pinned CPU tensors h, W, C, Q, K, V, O; dev: device tensors of the same
+    names plus gid.  Enqueues H2D copies, the three steps and the D2H copy of O."""
+    _check("focus_layer_fwd_host", _lib.focus_layer_fwd_host(
+        ctypes.byref(p), *[_ptr(host[k]) for k in ("h", "W", "C", "Q", "K", "V", "O")],
+        *[_ptr(dev[k]) for k in ("h", "W", "C", "Q", "K", "V", "O", "gid")],
+        _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def focus_check_errors(ws, stream=None) -> int:
+    """Synchronise the stream; return (and clear) the device error status."""
+    return int(_lib.focus_check_errors(_ptr(ws), _stream(stream)))
+
+
+# ------------------------------------------------------------ index views ---
+
+def index_views(p: Params, idx: Index, ws: torch.Tensor) -> dict:
+    """Torch views (no copy) of the index arrays living inside the workspace."""
+    base = ws.data_ptr()
+    P, n, K = p.B * p.A, p.n, p.K
+
+    def view(ptr, count, dtype=torch.int32, shape=None):
+        off = ptr - base
+        t = ws[off:off + count * 4].view(dtype)
+        return t.view(*shape) if shape else t
+
+    out = dict(counts=view(idx.counts, P * K, shape=(p.B, p.A, K)),
+               offsets=view(idx.offsets, P * (K + 1), shape=(p.B, p.A, K + 1)),
+               perm=view(idx.perm, P * n, shape=(p.B, p.A, n)),
+               rank=view(idx.rank, P * n, shape=(p.B, p.A, n)),
+               farlen_tok=view(idx.farlen_tok, P * n, shape=(p.B, p.A, n)),
+               farlen_slot=view(idx.farlen_slot, P * n, shape=(p.B, p.A, n)),
+               n_items=view(idx.n_items, 1))
+    m = idx.max_items
+    out["items"] = view(idx.items, m * 8, shape=(m, 8))
+    out["order"] = view(idx.order, m)
+    return out
+
+
+def run_layer(p: Params, h, W, C, Q, K, V, ws, stream=None, want_lse=False):
+    """assign -> index -> attention on device tensors; returns (O, gid, idx, lse)."""
+    dev = Q.device
+    gid = torch.empty((p.B, p.A, p.n), dtype=torch.int32, device=dev)
+    focus_assign(p, h, W, C, gid, ws, stream)
+    idx = focus_build_index(p, gid, ws, stream)
+    O = torch.empty_like(Q)
+    lse = torch.empty((p.B, p.H, p.n), dtype=torch.float32, device=dev) if want_lse else None
+    focus_attention_fwd(p, Q, K, V, idx, O, lse, ws, stream)
+    return O, gid, idx, lse

@@ -1,0 +1,96 @@
+"""The C-ABI library builds, loads and exports every declared entry point, and
+rejects bad arguments synchronously (host-only checks; no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def fz():
+    from learned_group_sparse_focus_gb300 import _build
+    if not os.path.exists(_build.LIB):
+        _build.build()
+    from learned_group_sparse_focus_gb300 import focus
+    return focus
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "focus.h")).read()
+    return re.findall(r"FOCUS_API\s+[\w\s\*]+?\b(focus_\w+)\s*\(", src)
+
+
+def test_header_declares_the_hot_path():
+    names = set(_declared())
+    assert {"focus_assign", "focus_build_index", "focus_attention_fwd",
+            "focus_dense_causal_fwd", "focus_workspace_bytes", "focus_check_errors"} <= names
+
+
+def test_every_declared_symbol_is_exported(fz):
+    lib = ctypes.CDLL(fz.LIB_PATH)
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert set(fz.EXPORTED) == set(_declared())
+    assert lib.focus_abi_version() == 1
+
+
+def test_struct_layouts_match_header(fz):
+    assert ctypes.sizeof(fz.Params) == 12 * 4
+    assert ctypes.sizeof(fz.Item) == 8 * 4
+    assert ctypes.sizeof(fz.Index) == 9 * 8 + 2 * 4
+
+
+def test_status_strings(fz):
+    lib = fz.lib()
+    for s in range(7):
+        assert lib.focus_status_string(s)
+    assert lib.focus_status_string(3) == b"workspace too small"
+
+
+def test_workspace_size_is_host_arithmetic(fz):
+    p = fz.make_params(B=1, H=32, H_kv=8, n=32768, d=128, D=4096, d_g=64, K=64, A=1, w=512)
+    nb = fz.focus_workspace_bytes(p)
+    # at least the group partial (O_far bf16 + LSE) and the sorted K/V copies
+    assert nb >= 32 * 32768 * 128 * 2 + 32 * 32768 * 4 + 2 * 8 * 32768 * 128 * 2
+    assert nb % 256 == 0
+    bad = fz.make_params(B=1, H=3, H_kv=2, n=10, d=64, D=8, d_g=32, K=2, A=1, w=1)
+    assert fz.focus_workspace_bytes(bad) == 0
+
+
+@pytest.mark.parametrize("field,value", [
+    ("H_kv", 5), ("n", 0), ("K", 0), ("K", 5000), ("A", 3), ("w", -1), ("scale", 0.0),
+    ("dtype", 7), ("n", (1 << 20) + 1),
+])
+def test_invalid_params_rejected_before_any_launch(fz, field, value):
+    kw = dict(B=1, H=4, H_kv=2, n=64, d=64, D=64, d_g=32, K=4, A=1, w=8)
+    p = fz.make_params(**kw)
+    setattr(p, field, value)
+    lib = fz.lib()
+    fake = ctypes.c_void_p(1 << 20)
+    st = lib.focus_assign(ctypes.byref(p), fake, fake, fake, fake, fake, 1 << 30, None)
+    assert st == 1
+    idx = fz.Index()
+    assert lib.focus_build_index(ctypes.byref(p), fake, ctypes.byref(idx), fake, 1 << 30, None) == 1
+
+
+def test_null_misaligned_and_small_workspace(fz):
+    lib = fz.lib()
+    p = fz.make_params(B=1, H=4, H_kv=2, n=64, d=64, D=64, d_g=32, K=4, A=1, w=8)
+    ok = ctypes.c_void_p(1 << 20)
+    mis = ctypes.c_void_p((1 << 20) + 8)
+    need = fz.focus_workspace_bytes(p)
+    assert lib.focus_assign(ctypes.byref(p), None, ok, ok, ok, ok, need, None) == 1
+    assert lib.focus_assign(ctypes.byref(p), mis, ok, ok, ok, ok, need, None) == 1
+    assert lib.focus_assign(ctypes.byref(p), ok, ok, ok, ok, ok, need - 256, None) == 3
+    assert lib.focus_assign(ctypes.byref(p), ok, ok, ok, ok, mis, need, None) == 1
+    idx = fz.Index()
+    assert lib.focus_build_index(ctypes.byref(p), ok, None, ok, need, None) == 1
+    assert lib.focus_attention_fwd(ctypes.byref(p), ok, ok, ok, None, ok, None, ok, need, None) == 1
+    assert lib.focus_dense_causal_fwd(ctypes.byref(p), ok, ok, ok, ok, None, ok, need - 256, None) == 3
+    p.d = 96
+    assert lib.focus_dense_causal_fwd(ctypes.byref(p), ok, ok, ok, ok, None, ok, need, None) == 2
+    assert lib.focus_workspace_init(mis, None) == 1
+    del idx
