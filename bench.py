@@ -1,0 +1,415 @@
+#!/usr/bin/env python
+"""Benchmark of the Focus attention hot path on GB300 (one JSON line).
+
+A step is one whole layer of the hot path on one batch of synthetic input:
+focus_assign -> focus_build_index -> focus_attention_fwd, all through the C
+ABI, for every head of the layer.  The default workload is the 32K-token GQA
+layer (B=1, 32 query / 8 KV heads, n=32768, d=128, hidden 4096, K=64, w=512).
+
+value        kept-pair TFLOP/s over the whole layer: 4*d FLOPs per kept
+             (query, key) pair per head, kept pairs counted exactly from the
+             index, divided by the device time of the step.
+e2e          the same metric through focus_layer_fwd_host: host->device copies
+             of h, W, C, Q, K, V from pinned memory, the three steps, and the
+             device->host copy of O, all inside the timed region.
+roofline     the dominant attention kernel's achieved TFLOP/s (its algorithmic
+             FLOPs per launch over its CUDA-event duration) against the measured
+             sustained bf16 tensor peak.
+cpu_baseline the fp64 oracle timed on the host cores on a bounded row sample.
+
+--impl reference times the oracle alone (the comparison arm of this build).
+Under torchrun (N > 1) every rank runs its own replica of the workload (weak
+scaling); there is no data-path collective.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "kept-pair TFLOP/s (% of bf16 TC peak), ms/layer at n=32K, speedup vs dense"
+UNIT = "TFLOP/s"
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20      # larger than the 129 MB L2
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.dev = device_index
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.3)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in (self.out or "").splitlines():
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def traffic_record(kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source
+    is unchanged since it was captured; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "learned_group_sparse_focus_gb300", "csrc", rec["source"])
+    try:
+        sha = hashlib.sha1(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    return rec if sha == rec.get("source_sha1") else None
+
+
+# ------------------------------------------------------------ oracle arm ---
+
+def oracle_sample(wl, x, rows_per_head: int, heads, seed: int):
+    """Time the oracle on a bounded sample: full assignment and index for the
+    batch, attention for `rows_per_head` seeded rows of each head in `heads`.
+    Returns (kept-pair FLOPs of the sample, seconds, description)."""
+    import oracle.focus_ref as ref
+    t0 = time.perf_counter()
+    gid, _ = ref.assign(x["h"], x["W"], x["C"])
+    idx = ref.build_index(gid, wl.K, max(wl.w, 1))
+    t1 = time.perf_counter()
+    rng = np.random.default_rng(seed)
+    kept = ref.kept_counts(idx, max(wl.w, 1))
+    flops = 0
+    t_attn = 0.0
+    for hq in heads:
+        kv = ref.kv_head(hq, wl.H, wl.H_kv)
+        a = ref.assignment_of_head(hq, wl.H, wl.H_kv, wl.A)
+        rows = np.sort(rng.choice(wl.n, size=min(rows_per_head, wl.n), replace=False))
+        s = time.perf_counter()
+        ref.attention_rows(x["Q"][:, hq:hq + 1], x["K"][:, kv:kv + 1], x["V"][:, kv:kv + 1],
+                           gid[:, a:a + 1], wl.w, wl.scale, rows, 1, row_block=256)
+        t_attn += time.perf_counter() - s
+        flops += 4 * wl.d * int(kept[:, a, rows].sum())
+    frac = len(heads) * rows_per_head / (wl.H * wl.n)
+    secs = (t1 - t0) * frac + t_attn
+    desc = (f"oracle fp64: assign + index over all {wl.B * wl.n} tokens (time prorated by the "
+            f"sampled fraction {frac:.2e}) and attention for {rows_per_head} seeded rows of heads "
+            f"{list(heads)}")
+    return flops, secs, desc
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, wl, world, rank):
+    if rank != 0:
+        return
+    from learned_group_sparse_focus_gb300 import synth
+    x = synth.draw(wl)
+    heads = [0, wl.H - 1]
+    for s in range(args.warmup):
+        oracle_sample(wl, x, 64, heads[:1], seed=s)
+    tot_f, tot_s, desc = 0, 0.0, ""
+    for s in range(args.steps):
+        f, sec, desc = oracle_sample(wl, x, args.ref_rows, heads, seed=1000 + s)
+        tot_f += f
+        tot_s += sec
+    v = tot_f / tot_s / 1e12
+    ms = tot_s / args.steps * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, **{k: getattr(wl, k) for k in ("B", "H", "H_kv", "n", "d", "D", "K", "w", "A")}},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                         "sample": desc + f"; per step, {args.steps} steps"},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------- GPU arm ---
+
+def run_ours(args, wl, world, rank, local):
+    import torch
+    from learned_group_sparse_focus_gb300 import synth
+    from learned_group_sparse_focus_gb300 import focus as fz
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    x = synth.draw(wl)
+
+    def dev(a):
+        if wl.dtype == "bf16":
+            return torch.from_numpy(synth.bf16_bits(a)).view(torch.bfloat16).cuda()
+        return torch.from_numpy(a).cuda()
+
+    d = {k: dev(x[k]) for k in ("h", "W", "C", "Q", "K", "V")}
+    p = fz.params_from_workload(wl)
+    ws = fz.alloc_workspace(p)
+    gid = torch.empty((wl.B, wl.A, wl.n), dtype=torch.int32, device="cuda")
+    O = torch.empty_like(d["Q"])
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    # one untimed pass: kept-pair counts come from the index itself
+    fz.focus_assign(p, d["h"], d["W"], d["C"], gid, ws)
+    idx = fz.focus_build_index(p, gid, ws)
+    fz.focus_attention_fwd(p, d["Q"], d["K"], d["V"], idx, O, None, ws)
+    st = fz.focus_check_errors(ws)
+    if st != 0:
+        raise RuntimeError(f"device error status {st}")
+    far = fz.index_views(p, idx, ws)["farlen_tok"].to(torch.int64).cpu().numpy()   # [B, A, n]
+    n_items = int(fz.index_views(p, idx, ws)["n_items"].item())
+    win_per_head = int(np.minimum(np.arange(wl.n) + 1, max(wl.w, 1)).sum())
+    far_pairs = 0
+    for hq in range(wl.H):
+        a = 0 if wl.A == 1 else (hq * wl.H_kv) // wl.H
+        far_pairs += int(far[:, a, :].sum())
+    win_pairs = win_per_head * wl.B * wl.H
+    kept = win_pairs + far_pairs
+    f_attn, f_group, f_local = 4 * wl.d * kept, 4 * wl.d * far_pairs, 4 * wl.d * win_pairs
+
+    def step(evs):
+        flush.zero_()
+        evs[0].record()
+        fz.focus_assign(p, d["h"], d["W"], d["C"], gid, ws)
+        evs[1].record()
+        ix = fz.focus_build_index(p, gid, ws)
+        evs[2].record()
+        fz.focus_attention_fwd_timed(p, d["Q"], d["K"], d["V"], ix, O, None, ws, evs[3:7])
+
+    def new_events(k):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(k)]
+        for row in evs:            # events are created lazily: record each once
+            for e in row:
+                e.record()
+        return evs
+
+    warm = new_events(1)[0]
+    for _ in range(args.warmup):
+        step(warm)
+    evs = new_events(args.steps)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(int(os.environ.get("FOCUS_NVSMI_INDEX", local))) as clk:
+        wall0 = time.perf_counter()
+        for s in range(args.steps):
+            step(evs[s])
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    st = fz.focus_check_errors(ws)
+    if st != 0:
+        raise RuntimeError(f"device error status {st}")
+
+    def mean_ms(i, j):
+        return statistics.mean(evs[s][i].elapsed_time(evs[s][j]) for s in range(args.steps))
+
+    t_step = mean_ms(0, 6)
+    t = {"assign": mean_ms(0, 1), "index": mean_ms(1, 2), "permute_kv": mean_ms(3, 4),
+         "group_pass": mean_ms(4, 5), "local_pass": mean_ms(5, 6)}
+    t_attn = mean_ms(3, 6)
+    if dist is not None:
+        tt = torch.tensor([t_step, t_attn], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_step, t_attn = tt.tolist()
+
+    # dense causal comparator on the same shape
+    for _ in range(3):
+        fz.focus_dense_causal_fwd(p, d["Q"], d["K"], d["V"], O, None, ws)
+    dn = max(3, min(args.steps, 10))
+    dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(dn)]
+    for a0, a1 in dev_ev:
+        flush.zero_()
+        a0.record()
+        fz.focus_dense_causal_fwd(p, d["Q"], d["K"], d["V"], O, None, ws)
+        a1.record()
+    torch.cuda.synchronize()
+    t_dense = statistics.mean(a0.elapsed_time(a1) for a0, a1 in dev_ev)
+
+    # end to end through the host-buffer entry point
+    host = {k: d[k].cpu().pin_memory() for k in ("h", "W", "C", "Q", "K", "V")}
+    host["O"] = torch.empty(O.shape, dtype=O.dtype).pin_memory()
+    dbuf = {k: torch.empty_like(d[k]) for k in ("h", "W", "C", "Q", "K", "V")}
+    dbuf["O"] = torch.empty_like(O)
+    dbuf["gid"] = torch.empty_like(gid)
+    h2d = sum(host[k].numel() * host[k].element_size() for k in ("h", "W", "C", "Q", "K", "V"))
+    d2h = host["O"].numel() * host["O"].element_size()
+    for _ in range(2):
+        fz.focus_layer_fwd_host(p, host, dbuf, ws)
+    en = max(3, min(args.steps, 10))
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(en)]
+    for a0, a1 in e2e_ev:
+        flush.zero_()
+        a0.record()
+        fz.focus_layer_fwd_host(p, host, dbuf, ws)
+        a1.record()
+    torch.cuda.synchronize()
+    t_e2e = statistics.mean(a0.elapsed_time(a1) for a0, a1 in e2e_ev)
+    st = fz.focus_check_errors(ws)
+    if st != 0:
+        raise RuntimeError(f"device error status {st}")
+    if not torch.equal(host["O"].cuda(), O):
+        # dense comparator overwrote O; recompute the device result for the check
+        fz.focus_attention_fwd(p, d["Q"], d["K"], d["V"], fz.focus_build_index(p, gid, ws), O, None, ws)
+        torch.cuda.synchronize()
+        if not torch.equal(host["O"].cuda(), O):
+            raise RuntimeError("host-buffer path and device path disagree")
+
+    peaks, peak_kind = load_peaks()
+    peak_tc = float(peaks["bf16_tflops_sustained"])
+    peak_hbm = float(peaks["hbm_gbs"])
+    dom = "group_pass" if t["group_pass"] >= t["local_pass"] else "local_pass"
+    dom_flops = f_group if dom == "group_pass" else f_local
+    achieved = dom_flops / (t[dom] * 1e-3) / 1e12
+    tr = traffic_record("attn_tc_" + dom)
+    value = world * f_attn / (t_step * 1e-3) / 1e12
+    es = 2 if wl.dtype == "bf16" else 4
+    assign_bytes = (wl.B * wl.n * wl.D + wl.A * wl.d_g * wl.D + wl.A * wl.K * wl.d_g) * es + wl.B * wl.A * wl.n * 4
+    kv_bytes = 2 * wl.B * wl.H_kv * wl.n * wl.d * es
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded N(0,1) Q/K/V/h, Zipf-planted groups)",
+        "config": {"workload": wl.name, **{k: getattr(wl, k) for k in ("B", "H", "H_kv", "n", "d", "D", "d_g", "K", "w", "A")},
+                   "kept_pairs": kept, "kept_density_vs_causal": kept / (wl.B * wl.H * wl.n * (wl.n + 1) / 2),
+                   "work_items": n_items, "l2": "flushed (256 MB write) before every timed step; flush not timed",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "pct_of_bf16_peak": 100.0 * (f_attn / (t_step * 1e-3) / 1e12) / float(peaks["bf16_tflops"]),
+        "attention_tflops": f_attn / (t_attn * 1e-3) / 1e12,
+        "ms_breakdown": t, "ms_attention": t_attn, "ms_dense_causal": t_dense,
+        "speedup_vs_dense": t_dense / t_step, "speedup_vs_dense_attention_only": t_dense / t_attn,
+        "roofline": {"bound": "tensor", "kernel": "attn_tc_" + dom, "achieved": achieved, "peak": peak_tc,
+                     "unit": "TFLOP/s", "frac": achieved / peak_tc,
+                     "traffic": tr["bytes_per_launch"] if tr else None,
+                     "peak_source": f"{peak_kind} bf16_tflops_sustained"},
+        "kernels": {
+            "assign": {"ms": t["assign"], "GB/s": assign_bytes / (t["assign"] * 1e-3) / 1e9,
+                       "hbm_frac": assign_bytes / (t["assign"] * 1e-3) / 1e9 / peak_hbm},
+            "permute_kv": {"ms": t["permute_kv"], "GB/s": 2 * kv_bytes / (t["permute_kv"] * 1e-3) / 1e9},
+            "group_pass": {"ms": t["group_pass"], "TFLOP/s": f_group / (t["group_pass"] * 1e-3) / 1e12},
+            "local_pass": {"ms": t["local_pass"], "TFLOP/s": f_local / (t["local_pass"] * 1e-3) / 1e12},
+            "index": {"ms": t["index"]},
+        },
+        "e2e": {"value": world * f_attn / (t_e2e * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": t_e2e,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "call": "focus_layer_fwd_host (pinned host buffers)"},
+        "gpu_launches": 9 * args.steps,
+        "wall_s_timed_region": wall,
+    }
+    if rank == 0:
+        line["clocks"] = clk.summary()
+        if world == 1 and not args.no_cpu_baseline:
+            f, sec, desc = oracle_sample(wl, x, args.cpu_rows, [0, wl.H - 1], seed=7)
+            line["cpu_baseline"] = {"value": f / sec / 1e12, "unit": UNIT, "cores": cpu_cores(),
+                                    "kind": "oracle", "sample": desc, "seconds": sec}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gqa_32k")
+    ap.add_argument("--cpu-rows", type=int, default=1024)
+    ap.add_argument("--ref-rows", type=int, default=256)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    from learned_group_sparse_focus_gb300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, wl, world, rank)
+    else:
+        run_ours(args, wl, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -160,6 +160,17 @@ FOCUS_API focus_status_t focus_attention_fwd(const focus_params_t* p, const void
                                    const void* V, const focus_index_t* idx, void* O,
                                    float* lse_opt, void* ws, size_t ws_bytes, void* stream);
 
+/* focus_attention_fwd that also records four caller-created CUDA events
+ * (cudaEvent_t, passed as void*) on `stream`: events[0] before the K/V sort
+ * copy, events[1] before the group pass, events[2] before the local pass and
+ * events[3] after it, so a caller can time each kernel.  events == NULL is
+ * exactly focus_attention_fwd.  Same arguments and errors otherwise. */
+FOCUS_API focus_status_t focus_attention_fwd_timed(const focus_params_t* p, const void* Q,
+                                                   const void* K, const void* V,
+                                                   const focus_index_t* idx, void* O,
+                                                   float* lse_opt, void* ws, size_t ws_bytes,
+                                                   void* stream, void* const* events);
+
 /* Ordinary causal attention (every j <= i kept) with the same kernels and
  * layouts as the local pass: the dense comparator for the speedup figure.
  * Ignores p->w, p->K, p->A.  Same tensors and rules as focus_attention_fwd. */

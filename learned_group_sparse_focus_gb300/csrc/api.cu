@@ -266,9 +266,10 @@ static focus_status_t attention_common(const focus_params_t* p, const void* Q, c
   return ensure_setup();
 }
 
-focus_status_t focus_attention_fwd(const focus_params_t* p, const void* Q, const void* K,
-                                   const void* V, const focus_index_t* idx, void* O, float* lse_opt,
-                                   void* ws, size_t ws_bytes, void* stream) {
+focus_status_t focus_attention_fwd_timed(const focus_params_t* p, const void* Q, const void* K,
+                                         const void* V, const focus_index_t* idx, void* O,
+                                         float* lse_opt, void* ws, size_t ws_bytes, void* stream,
+                                         void* const* events) {
   if (!idx || !idx->perm || !idx->farlen_tok || !idx->farlen_slot || !idx->items || !idx->order ||
       !idx->n_items)
     return FOCUS_ERR_INVALID_ARG;
@@ -284,14 +285,23 @@ focus_status_t focus_attention_fwd(const focus_params_t* p, const void* Q, const
   a.items = idx->items;
   a.order = idx->order;
   a.n_items = idx->n_items;
+  auto mark = [&](int i) {
+    return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) : cudaSuccess;
+  };
   if (p->dtype == FOCUS_F32) {
-    cudaError_t e = launch_attn_simt_f32(a, p->d, kModeGroup, L.max_items, st);
+    cudaError_t e = mark(0);
+    if (e == cudaSuccess) e = mark(1);
+    if (e == cudaSuccess) e = launch_attn_simt_f32(a, p->d, kModeGroup, L.max_items, st);
+    if (e == cudaSuccess) e = mark(2);
     if (e == cudaSuccess) e = launch_attn_simt_f32(a, p->d, kModeLocal, 0, st);
+    if (e == cudaSuccess) e = mark(3);
     return cuda_status(e);
   }
   void* Ks = at<void>(ws, L.Ks);
   void* Vs = at<void>(ws, L.Vs);
-  cudaError_t e = launch_permute_kv_bf16(K, V, Ks, Vs, idx->perm, p->B, p->H_kv, p->n, p->d, p->A, st);
+  cudaError_t e = mark(0);
+  if (e == cudaSuccess) e = launch_permute_kv_bf16(K, V, Ks, Vs, idx->perm, p->B, p->H_kv, p->n, p->d, p->A, st);
+  if (e == cudaSuccess) e = mark(1);
   if (e != cudaSuccess) return FOCUS_ERR_CUDA;
   CUtensorMap tk, tv, tks, tvs;
   const uint64_t planes = static_cast<uint64_t>(p->B) * p->H_kv;
@@ -299,9 +309,18 @@ focus_status_t focus_attention_fwd(const focus_params_t* p, const void* Q, const
       !make_map(&tks, Ks, p->d, p->n, planes, 128, 3) || !make_map(&tvs, Vs, p->d, p->n, planes, 128, 3))
     return FOCUS_ERR_CUDA;
   e = launch_attn_tc_bf16(a, &tks, &tvs, p->d, kModeGroup, L.max_items, st);
+  if (e == cudaSuccess) e = mark(2);
   if (e == cudaSuccess) e = launch_attn_tc_bf16(a, &tk, &tv, p->d, kModeLocal, 0, st);
+  if (e == cudaSuccess) e = mark(3);
   return cuda_status(e);
 }
+
+focus_status_t focus_attention_fwd(const focus_params_t* p, const void* Q, const void* K,
+                                   const void* V, const focus_index_t* idx, void* O, float* lse_opt,
+                                   void* ws, size_t ws_bytes, void* stream) {
+  return focus_attention_fwd_timed(p, Q, K, V, idx, O, lse_opt, ws, ws_bytes, stream, nullptr);
+}
+
 
 focus_status_t focus_dense_causal_fwd(const focus_params_t* p, const void* Q, const void* K,
                                       const void* V, void* O, float* lse_opt, void* ws,

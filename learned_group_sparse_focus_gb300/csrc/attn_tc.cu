@@ -124,8 +124,10 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
   uint64_t* v_empty = bars + 7;
   uint64_t* s_full = bars + 9;
   uint64_t* p_ready = bars + 11;
-  uint64_t* o_done = bars + 13;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+  uint64_t* o_done = bars + 13;    // one phase per PV product (waited only while
+                                   // at most one phase behind: see the rescale)
+  uint64_t* o_final = bars + 14;   // single phase: every PV product is done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = warp_id(), lane = lane_id();
@@ -140,6 +142,7 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
       mbar_init(&p_ready[s], 128);
     }
     mbar_init(o_done, 1);
+    mbar_init(o_final, 1);
     *abort = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_k);
@@ -219,7 +222,7 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
         mma_commit(&k_empty[st]);
         if (t > 0 && !issue_pv(t - 1)) { ok = false; break; }
       }
-      if (ok) issue_pv(nt - 1);
+      if (ok && issue_pv(nt - 1)) mma_commit(o_final);
     }
   } else {
     // ------------------------------------------------------- softmax ---
@@ -329,7 +332,9 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
     }
 
     // ------------------------------------------------------ epilogue ---
-    if (ok) ok = warp_wait(o_done, (nt - 1) & 1, abort, a.err);
+    // o_done may trail by two phases here, so its parity cannot tell whether
+    // the last product landed; o_final has exactly one phase.
+    if (ok) ok = warp_wait(o_final, 0, abort, a.err);
     tc_fence_after();
     if (ok) {
       constexpr float kLn2 = 0.6931471805599453f;

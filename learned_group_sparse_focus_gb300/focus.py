@@ -60,6 +60,8 @@ def _load():
         "focus_build_index": ([P, vp, ctypes.POINTER(Index), vp, ctypes.c_size_t, vp], ctypes.c_int),
         "focus_attention_fwd": ([P, vp, vp, vp, ctypes.POINTER(Index), vp, vp, vp, ctypes.c_size_t, vp],
                                 ctypes.c_int),
+        "focus_attention_fwd_timed": ([P, vp, vp, vp, ctypes.POINTER(Index), vp, vp, vp, ctypes.c_size_t,
+                                       vp, ctypes.POINTER(ctypes.c_void_p)], ctypes.c_int),
         "focus_dense_causal_fwd": ([P, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp], ctypes.c_int),
         "focus_layer_fwd_host": ([P] + [vp] * 7 + [vp] * 8 + [vp, ctypes.c_size_t, vp], ctypes.c_int),
         "focus_check_errors": ([vp, vp], ctypes.c_int),
@@ -75,7 +77,7 @@ _lib = _load()
 
 EXPORTED = ("focus_abi_version", "focus_status_string", "focus_workspace_bytes",
             "focus_workspace_init", "focus_assign", "focus_build_index", "focus_attention_fwd",
-            "focus_dense_causal_fwd", "focus_layer_fwd_host", "focus_check_errors")
+            "focus_attention_fwd_timed", "focus_dense_causal_fwd", "focus_layer_fwd_host", "focus_check_errors")
 
 
 def lib():
@@ -151,6 +153,14 @@ def focus_attention_fwd(p: Params, Q, K, V, idx: Index, O, lse, ws, stream=None)
     _check("focus_attention_fwd",
            _lib.focus_attention_fwd(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), ctypes.byref(idx),
                                     _ptr(O), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def focus_attention_fwd_timed(p: Params, Q, K, V, idx: Index, O, lse, ws, events, stream=None):
+    """events: four recorded-once torch.cuda.Event objects (see include/focus.h)."""
+    arr = (ctypes.c_void_p * 4)(*[e.cuda_event for e in events])
+    _check("focus_attention_fwd_timed",
+           _lib.focus_attention_fwd_timed(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), ctypes.byref(idx),
+                                          _ptr(O), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream), arr))
 
 
 def focus_dense_causal_fwd(p: Params, Q, K, V, O, lse, ws, stream=None):

@@ -186,6 +186,34 @@ def test_attention_all_rows(fz, dtype, B, H, H_kv, A, n, d, K, w, kind):
     _attn_case(fz, dtype, B, H, H_kv, A, n, d, K, w, kind, seed=n + w + K)
 
 
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("bf16", 64), ("f32", 128)])
+def test_attention_long_groups_deterministic(fz, dtype, d):
+    """Two big groups: group-pass items walk up to ~16 key tiles, so the tile
+    pipeline cycles its barriers many times; three runs must agree bit for bit
+    and match the oracle on every row."""
+    import torch
+    B, H, H_kv, A, n, K, w = 1, 4, 2, 1, 4096, 2, 64
+    rng = np.random.default_rng(77)
+    store = (lambda a: synth.round_bf16(a)) if dtype == "bf16" else (lambda a: a)
+    Q = store(rng.standard_normal((B, H, n, d)).astype(np.float32))
+    Kt = store(rng.standard_normal((B, H_kv, n, d)).astype(np.float32))
+    V = store(rng.standard_normal((B, H_kv, n, d)).astype(np.float32))
+    g = synth.draw_group_ids(77, B, A, n, K, "uniform")
+    p = fz.make_params(B=B, H=H, H_kv=H_kv, n=n, d=d, D=64, d_g=32, K=K, A=A, w=w, dtype=dtype)
+    ws = _ws(fz, p)
+    Qd, Kd, Vd = to_dev(Q, dtype), to_dev(Kt, dtype), to_dev(V, dtype)
+    idx = fz.focus_build_index(p, torch.from_numpy(g).cuda(), ws)
+    outs = []
+    for _ in range(3):
+        O = torch.full_like(Qd, float("nan"))
+        fz.focus_attention_fwd(p, Qd, Kd, Vd, idx, O, None, ws)
+        outs.append(O)
+    assert fz.focus_check_errors(ws) == 0
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    want_O, _ = ref.attention(Q, Kt, V, g, w, p.scale, A)
+    assert_close(to_host(outs[0]), want_O, dtype, "O")
+
+
 @pytest.mark.parametrize("dtype,n,d,H,H_kv", [("bf16", 700, 128, 4, 2), ("bf16", 129, 64, 2, 2),
                                               ("f32", 300, 64, 2, 1)])
 def test_dense_causal_all_rows(fz, dtype, n, d, H, H_kv):
@@ -214,6 +242,10 @@ def test_workload_full_size(fz, name):
     O, gid, idx, lse = fz.run_layer(p, dev["h"], dev["W"], dev["C"], dev["Q"], dev["K"], dev["V"],
                                     ws, want_lse=True)
     assert fz.focus_check_errors(ws) == 0
+    O2 = torch.empty_like(O)
+    fz.focus_attention_fwd(p, dev["Q"], dev["K"], dev["V"], idx, O2, None, ws)
+    assert fz.focus_check_errors(ws) == 0
+    assert torch.equal(O, O2), "attention is not deterministic"
     g = gid.cpu().numpy()
     assert np.array_equal(g, x["gid_ref"]), "group ids"
     got_idx = _index_np(fz, p, idx, ws)
