@@ -85,6 +85,7 @@ T* at(void* ws, size_t off) {
 // ----------------------------------------------------- per-device set-up ---
 std::mutex g_mu;
 bool g_ready[64] = {};
+int g_sms[64] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 focus_status_t ensure_setup() {
@@ -101,6 +102,9 @@ focus_status_t ensure_setup() {
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
   if (!g_ready[dev]) {
+    if (cudaDeviceGetAttribute(&g_sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        g_sms[dev] < 1)
+      return FOCUS_ERR_CUDA;
     if (setup_index_kernels() != cudaSuccess) return FOCUS_ERR_CUDA;
     if (setup_assign_kernels() != cudaSuccess) return FOCUS_ERR_CUDA;
     if (setup_attn_kernels() != cudaSuccess) return FOCUS_ERR_CUDA;
@@ -127,6 +131,13 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, u
 }
 
 focus_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? FOCUS_OK : FOCUS_ERR_CUDA; }
+
+// SMs of the current device (valid after ensure_setup).
+int sm_count() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return (dev >= 0 && dev < 64 && g_sms[dev] > 0) ? g_sms[dev] : 1;
+}
 
 focus_status_t check_ws(const focus_params_t* p, void* ws, size_t ws_bytes) {
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return FOCUS_ERR_INVALID_ARG;
@@ -303,14 +314,17 @@ focus_status_t focus_attention_fwd_timed(const focus_params_t* p, const void* Q,
   if (e == cudaSuccess) e = launch_permute_kv_bf16(K, V, Ks, Vs, idx->perm, p->B, p->H_kv, p->n, p->d, p->A, st);
   if (e == cudaSuccess) e = mark(1);
   if (e != cudaSuccess) return FOCUS_ERR_CUDA;
-  CUtensorMap tk, tv, tks, tvs;
+  CUtensorMap tq, tk, tv, tks, tvs;
   const uint64_t planes = static_cast<uint64_t>(p->B) * p->H_kv;
-  if (!make_map(&tk, K, p->d, p->n, planes, 128, 3) || !make_map(&tv, V, p->d, p->n, planes, 128, 3) ||
+  const uint64_t qplanes = static_cast<uint64_t>(p->B) * p->H;
+  if (!make_map(&tq, Q, p->d, p->n, qplanes, 128, 3) ||
+      !make_map(&tk, K, p->d, p->n, planes, 128, 3) || !make_map(&tv, V, p->d, p->n, planes, 128, 3) ||
       !make_map(&tks, Ks, p->d, p->n, planes, 128, 3) || !make_map(&tvs, Vs, p->d, p->n, planes, 128, 3))
     return FOCUS_ERR_CUDA;
-  e = launch_attn_tc_bf16(a, &tks, &tvs, p->d, kModeGroup, L.max_items, st);
+  const int sms = sm_count();
+  e = launch_attn_tc_bf16(a, &tq, &tks, &tvs, p->d, kModeGroup, L.max_items, sms, st);
   if (e == cudaSuccess) e = mark(2);
-  if (e == cudaSuccess) e = launch_attn_tc_bf16(a, &tk, &tv, p->d, kModeLocal, 0, st);
+  if (e == cudaSuccess) e = launch_attn_tc_bf16(a, &tq, &tk, &tv, p->d, kModeLocal, 0, sms, st);
   if (e == cudaSuccess) e = mark(3);
   return cuda_status(e);
 }
@@ -331,11 +345,13 @@ focus_status_t focus_dense_causal_fwd(const focus_params_t* p, const void* Q, co
   AttnArgs a = attn_args(p, Q, K, V, O, lse_opt, ws, L);
   a.w = p->n;
   if (p->dtype == FOCUS_F32) return cuda_status(launch_attn_simt_f32(a, p->d, kModeDense, 0, st));
-  CUtensorMap tk, tv;
+  CUtensorMap tq, tk, tv;
   const uint64_t planes = static_cast<uint64_t>(p->B) * p->H_kv;
-  if (!make_map(&tk, K, p->d, p->n, planes, 128, 3) || !make_map(&tv, V, p->d, p->n, planes, 128, 3))
+  const uint64_t qplanes = static_cast<uint64_t>(p->B) * p->H;
+  if (!make_map(&tq, Q, p->d, p->n, qplanes, 128, 3) ||
+      !make_map(&tk, K, p->d, p->n, planes, 128, 3) || !make_map(&tv, V, p->d, p->n, planes, 128, 3))
     return FOCUS_ERR_CUDA;
-  return cuda_status(launch_attn_tc_bf16(a, &tk, &tv, p->d, kModeDense, 0, st));
+  return cuda_status(launch_attn_tc_bf16(a, &tq, &tk, &tv, p->d, kModeDense, 0, sm_count(), st));
 }
 
 focus_status_t focus_layer_fwd_host(const focus_params_t* p, const void* host_h,

@@ -9,7 +9,7 @@
 
 namespace focus {
 
-constexpr int kTileM = FOCUS_TILE_M;   // query rows per attention tile / work item
+constexpr int kTileM = FOCUS_TILE_M;   // query rows per group-pass work item
 constexpr int kTileN = FOCUS_TILE_N;   // keys per attention tile
 constexpr int kMaxK = FOCUS_MAX_K;
 constexpr int kIndexSeg = 1024;        // tokens per counting-sort segment
@@ -88,9 +88,9 @@ cudaError_t launch_attn_simt_f32(const AttnArgs& a, int d, int mode, int max_ite
 cudaError_t launch_permute_kv_bf16(const void* K, const void* V, void* Ks, void* Vs,
                                    const int32_t* perm, int B, int H_kv, int n, int d, int A,
                                    cudaStream_t st);
-cudaError_t launch_attn_tc_bf16(const AttnArgs& a, const CUtensorMap* tm_k,
-                                const CUtensorMap* tm_v, int d, int mode, int max_items,
-                                cudaStream_t st);
+cudaError_t launch_attn_tc_bf16(const AttnArgs& a, const CUtensorMap* tm_q,
+                                const CUtensorMap* tm_k, const CUtensorMap* tm_v, int d, int mode,
+                                int max_items, int num_sms, cudaStream_t st);
 cudaError_t setup_attn_kernels();
 
 }  // namespace focus
