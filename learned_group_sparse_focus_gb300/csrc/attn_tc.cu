@@ -48,6 +48,10 @@ constexpr int kHalf = 128;                   // query rows per half
 constexpr int kUnitRows = 2 * kHalf;
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
 constexpr int kThreads = 384;
+// K and V tiles share one ring of 32 KB slots (K(t) then V(t)), five deep:
+// the loader runs about 2.5 tiles ahead of the MMAs, enough to cover a TMA
+// round trip while every SM streams keys at once.
+constexpr int kKvSlots = 5;
 // Register split (setmaxnreg).  The kernel launches at 168 registers per
 // thread (384 x 168 = 64512, the cap for 12 warps).  Warpgroup 2 (loads, MMA,
 // two idle warps) gives registers back down to 88 and the two softmax
@@ -61,9 +65,8 @@ struct AttnCfg {
   static constexpr int kChunk = 128 * 128;   // 64 columns x 128 rows, one swizzle slab
   static constexpr int kTile = 128 * D * 2;  // one 128-row Q/K/V tile
   static constexpr int kQ = 0;               // two halves
-  static constexpr int kK = kQ + 2 * kTile;  // two stages
-  static constexpr int kV = kK + 2 * kTile;  // two stages
-  static constexpr int kBar = kV + 2 * kTile;
+  static constexpr int kRing = kQ + 2 * kTile;           // K/V slots
+  static constexpr int kBar = kRing + kKvSlots * kTile;
   static constexpr int kSmem = kBar + 512 + 1024;
   static constexpr uint32_t kTmemCols = 512;
 };
@@ -188,20 +191,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + Cfg::kQ;
-  uint8_t* sK = smem + Cfg::kK;
-  uint8_t* sV = smem + Cfg::kV;
+  uint8_t* sKV = smem + Cfg::kRing;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBar);
   uint64_t* q_full = bars + 0;     // [2] per half
   uint64_t* q_empty = bars + 2;    // [2]
-  uint64_t* k_full = bars + 4;     // [2] per stage
-  uint64_t* k_empty = bars + 6;
-  uint64_t* v_full = bars + 8;
-  uint64_t* v_empty = bars + 10;
-  uint64_t* s_full = bars + 12;    // [2] per half
-  uint64_t* p_ready = bars + 14;   // [2]
-  uint64_t* o_final = bars + 16;   // [2]
-  uint64_t* o_free = bars + 18;    // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
+  uint64_t* kv_full = bars + 4;    // [kKvSlots]
+  uint64_t* kv_empty = bars + 4 + kKvSlots;
+  uint64_t* s_full = bars + 4 + 2 * kKvSlots;    // [2] per half
+  uint64_t* p_ready = s_full + 2;  // [2]
+  uint64_t* o_final = s_full + 4;  // [2]
+  uint64_t* o_free = s_full + 6;   // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 8);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = warp_id(), lane = lane_id();
@@ -210,14 +210,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int x = 0; x < 2; ++x) {
       mbar_init(&q_full[x], MODE == kModeGroup ? 32 : 1);
       mbar_init(&q_empty[x], 1);
-      mbar_init(&k_full[x], 1);
-      mbar_init(&k_empty[x], 1);
-      mbar_init(&v_full[x], 1);
-      mbar_init(&v_empty[x], 1);
       mbar_init(&s_full[x], 1);
       mbar_init(&p_ready[x], 128);
       mbar_init(&o_final[x], 1);
       mbar_init(&o_free[x], 128);
+    }
+    for (int k = 0; k < kKvSlots; ++k) {
+      mbar_init(&kv_full[k], 1);
+      mbar_init(&kv_empty[k], 1);
     }
     *abort = 0;
     fence_mbar_init();
@@ -235,7 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
     if (warp == 8) {
     // ---------------------------------------------------------- loads ---
-    int c = 0;                 // K/V tiles issued
+    int c = 0;                 // K/V tiles walked
+    int issued = 0;            // K/V loads issued (lane 0)
     int qn[2] = {0, 0};        // Q loads issued per half
     bool ok = true;
     const __nv_bfloat16* Qg = static_cast<const __nv_bfloat16*>(a.Q);
@@ -272,19 +273,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       if (lane == 0) {
-        for (int t = U.T0; t <= U.T1; ++t, ++c) {
-          const int st = c & 1, use = c >> 1;
+        // load L = 2c (K of tile c) and 2c+1 (V of tile c) into slot L % kKvSlots
+        for (int t = U.T0; t <= U.T1 && ok; ++t, ++c) {
           const int y = U.ybase + t * kBN;
-          if (use > 0 && !mbar_wait(&k_empty[st], (use - 1) & 1, abort, a.err)) { ok = false; break; }
-          mbar_expect_tx(&k_full[st], Cfg::kTile);
 #pragma unroll
-          for (int ch = 0; ch < kChunks; ++ch)
-            tma_load_3d(sK + st * Cfg::kTile + ch * Cfg::kChunk, &tm_k, &k_full[st], ch * 64, y, U.zkv);
-          if (use > 0 && !mbar_wait(&v_empty[st], (use - 1) & 1, abort, a.err)) { ok = false; ++c; break; }
-          mbar_expect_tx(&v_full[st], Cfg::kTile);
+          for (int kv = 0; kv < 2; ++kv) {
+            const int L = 2 * c + kv, sl = L % kKvSlots, use = L / kKvSlots;
+            if (use > 0 && !mbar_wait(&kv_empty[sl], (use - 1) & 1, abort, a.err)) { ok = false; break; }
+            mbar_expect_tx(&kv_full[sl], Cfg::kTile);
 #pragma unroll
-          for (int ch = 0; ch < kChunks; ++ch)
-            tma_load_3d(sV + st * Cfg::kTile + ch * Cfg::kChunk, &tm_v, &v_full[st], ch * 64, y, U.zkv);
+            for (int ch = 0; ch < kChunks; ++ch)
+              tma_load_3d(sKV + sl * Cfg::kTile + ch * Cfg::kChunk, kv ? &tm_v : &tm_k, &kv_full[sl],
+                          ch * 64, y, U.zkv);
+            ++issued;
+          }
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort;
@@ -292,11 +294,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (*abort && lane == 0) {
       // drain: TMA copies already issued must land before the CTA exits
-      for (int k = max(0, c - 2); k < c; ++k) {
+      for (int L = max(0, issued - kKvSlots); L < issued; ++L) {
         const unsigned long long t0 = global_ns();
-        while (!mbar_try_wait(&k_full[k & 1], (k >> 1) & 1) && global_ns() - t0 < kWaitTimeoutNs) {}
-        const unsigned long long t1 = global_ns();
-        while (!mbar_try_wait(&v_full[k & 1], (k >> 1) & 1) && global_ns() - t1 < kWaitTimeoutNs) {}
+        while (!mbar_try_wait(&kv_full[L % kKvSlots], (L / kKvSlots) & 1) &&
+               global_ns() - t0 < kWaitTimeoutNs) {}
       }
       if (MODE != kModeGroup) {
         for (int x = 0; x < 2; ++x) {
@@ -311,17 +312,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, kBN, false, false);
       constexpr uint32_t idPV = idesc_bf16_f32(128, D, false, true);
-      const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), v0 = smem_u32(sV);
+      const uint32_t q0 = smem_u32(sQ), r0 = smem_u32(sKV);
       int c = 0;                   // K/V tiles consumed
       int qn[2] = {0, 0};          // units per half
       int pv[2] = {0, 0};          // PV products issued per half
       bool ok = true;
+      // descriptor low words: Q halves and ring slots as K-major operands
+      // (LBO unused), ring slots as MN-major V operands (LBO = one 64-column slab)
+      constexpr uint32_t dhi = sw128_desc_hi();
+      const uint32_t qlo = sw128_desc_lo(q0, 16), klo = sw128_desc_lo(r0, 16);
+      const uint32_t vlo = sw128_desc_lo(r0, Cfg::kChunk);
       auto issue_s = [&](int x, int st) {
+        const uint32_t a0 = qlo + x * (Cfg::kTile >> 4), b0 = klo + st * (Cfg::kTile >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * Cfg::kChunk + (kk & 3) * 32;
-          mma_ss(tmem + 128 * x, sw128_desc(q0 + x * Cfg::kTile + off, 16, 1024),
-                 sw128_desc(k0 + st * Cfg::kTile + off, 16, 1024), idS, kk > 0);
+          const uint32_t off = ((kk >> 2) * Cfg::kChunk + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + 128 * x, desc_join(a0 + off, dhi), desc_join(b0 + off, dhi), idS, kk > 0);
         }
         mma_commit(&s_full[x]);
       };
@@ -335,20 +341,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         // first key tile: S products only
-        if (!mbar_wait(&k_full[c & 1], (c >> 1) & 1, abort, a.err)) break;
+        if (!mbar_wait(&kv_full[(2 * c) % kKvSlots], ((2 * c) / kKvSlots) & 1, abort, a.err)) break;
         tc_fence_after();
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
           if (!active_at(U, x, U.T0)) continue;
-          issue_s(x, c & 1);
+          issue_s(x, (2 * c) % kKvSlots);
           if (U.T0 == U.t1[x]) mma_commit(&q_empty[x]);
         }
-        mma_commit(&k_empty[c & 1]);
+        mma_commit(&kv_empty[(2 * c) % kKvSlots]);
         for (int t = U.T0; t <= U.T1 && ok; ++t, ++c) {
-          const int st = c & 1, stn = (c + 1) & 1;
+          const int st = (2 * c + 1) % kKvSlots;          // V of this tile
+          const int stn = (2 * c + 2) % kKvSlots;         // K of the next tile
           const bool next = t < U.T1;
-          if (!mbar_wait(&v_full[st], (c >> 1) & 1, abort, a.err)) { ok = false; break; }
-          if (next && !mbar_wait(&k_full[stn], ((c + 1) >> 1) & 1, abort, a.err)) { ok = false; break; }
+          if (!mbar_wait(&kv_full[st], ((2 * c + 1) / kKvSlots) & 1, abort, a.err)) { ok = false; break; }
+          if (next && !mbar_wait(&kv_full[stn], ((2 * c + 2) / kKvSlots) & 1, abort, a.err)) { ok = false; break; }
 #pragma unroll
           for (int x = 0; x < 2; ++x) {
             if (!ok) continue;
@@ -356,11 +363,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (first[x] && qn[x] > 0 && !mbar_wait(&o_free[x], (qn[x] - 1) & 1, abort, a.err)) { ok = false; continue; }
               if (!mbar_wait(&p_ready[x], pv[x] & 1, abort, a.err)) { ok = false; continue; }
               tc_fence_after();
-              const uint32_t vb = v0 + st * Cfg::kTile;
+              const uint32_t vb = vlo + st * (Cfg::kTile >> 4);
 #pragma unroll
               for (int kk = 0; kk < kBN / 16; ++kk)
                 mma_ts(tmem + 256 + 128 * x, tmem + 128 * x + kk * 8,
-                       sw128_desc(vb + kk * 16 * 128, Cfg::kChunk, 1024), idPV, (!first[x]) || kk > 0);
+                       desc_join(vb + kk * ((16 * 128) >> 4), dhi), idPV, (!first[x]) || kk > 0);
               ++pv[x];
               first[x] = false;
               if (t == U.t1[x]) mma_commit(&o_final[x]);
@@ -372,8 +379,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (!ok) break;
-          mma_commit(&v_empty[st]);
-          if (next) mma_commit(&k_empty[stn]);
+          mma_commit(&kv_empty[st]);
+          if (next) mma_commit(&kv_empty[stn]);
         }
 #pragma unroll
         for (int x = 0; x < 2; ++x)

@@ -53,12 +53,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking probe of the same condition (no suspend hint).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+
 // Wait for phase `parity` of `bar` to complete, giving up after
 // kWaitTimeoutNs or as soon as another role of the CTA raised `abort`.
 // On giving up it raises `abort`, sets the timeout bit and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           int* err) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -148,6 +158,23 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo_byte
   d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
   d |= (uint64_t)1 << 46;   // descriptor version for this architecture
   d |= (uint64_t)2 << 61;   // 128-byte swizzle
+  return d;
+}
+
+// The same descriptor split in halves.  Every descriptor these kernels build
+// shares the upper word (SBO = 1024, version, 128-byte swizzle); the lower word
+// is start>>4 | LBO>>4 << 16, and moving the start by a multiple of 16 bytes is
+// one 32-bit add on it (shared-memory addresses stay below 2^18, so start>>4
+// never leaves its 14-bit field).
+__host__ __device__ constexpr uint32_t sw128_desc_hi() {
+  return (1024u >> 4) | (1u << 14) | (2u << 29);
+}
+__device__ __forceinline__ uint32_t sw128_desc_lo(uint32_t saddr, uint32_t lbo_bytes) {
+  return ((saddr >> 4) & 0x3FFFu) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+__device__ __forceinline__ uint64_t desc_join(uint32_t lo, uint32_t hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
   return d;
 }
 
