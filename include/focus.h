@@ -61,9 +61,8 @@ extern "C" {
 #define FOCUS_API
 #endif
 
-/* Query rows per group-pass work item (two 128-row halves that share every
- * key tile); the work list is built for this height. */
-#define FOCUS_TILE_M 256
+/* Query rows per group-pass work item; the work list is built for this height. */
+#define FOCUS_TILE_M 128
 /* Keys per attention tile; the longest-first schedule counts cost in these. */
 #define FOCUS_TILE_N 128
 /* Largest supported number of centroids K. */

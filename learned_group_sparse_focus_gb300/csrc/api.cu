@@ -314,17 +314,19 @@ focus_status_t focus_attention_fwd_timed(const focus_params_t* p, const void* Q,
   if (e == cudaSuccess) e = launch_permute_kv_bf16(K, V, Ks, Vs, idx->perm, p->B, p->H_kv, p->n, p->d, p->A, st);
   if (e == cudaSuccess) e = mark(1);
   if (e != cudaSuccess) return FOCUS_ERR_CUDA;
-  CUtensorMap tq, tk, tv, tks, tvs;
+  CUtensorMap tq, tk, tv, tks, tvs, to, tof;
   const uint64_t planes = static_cast<uint64_t>(p->B) * p->H_kv;
   const uint64_t qplanes = static_cast<uint64_t>(p->B) * p->H;
   if (!make_map(&tq, Q, p->d, p->n, qplanes, 128, 3) ||
       !make_map(&tk, K, p->d, p->n, planes, 128, 3) || !make_map(&tv, V, p->d, p->n, planes, 128, 3) ||
-      !make_map(&tks, Ks, p->d, p->n, planes, 128, 3) || !make_map(&tvs, Vs, p->d, p->n, planes, 128, 3))
+      !make_map(&tks, Ks, p->d, p->n, planes, 128, 3) || !make_map(&tvs, Vs, p->d, p->n, planes, 128, 3) ||
+      !make_map(&to, O, p->d, p->n, qplanes, 128, 3) ||
+      !make_map(&tof, a.O_far, p->d, p->n, qplanes, 128, 3))
     return FOCUS_ERR_CUDA;
   const int sms = sm_count();
-  e = launch_attn_tc_bf16(a, &tq, &tks, &tvs, p->d, kModeGroup, L.max_items, sms, st);
+  e = launch_attn_tc_bf16(a, &tq, &tks, &tvs, &to, &tof, p->d, kModeGroup, L.max_items, sms, st);
   if (e == cudaSuccess) e = mark(2);
-  if (e == cudaSuccess) e = launch_attn_tc_bf16(a, &tq, &tk, &tv, p->d, kModeLocal, 0, sms, st);
+  if (e == cudaSuccess) e = launch_attn_tc_bf16(a, &tq, &tk, &tv, &to, &tof, p->d, kModeLocal, 0, sms, st);
   if (e == cudaSuccess) e = mark(3);
   return cuda_status(e);
 }
@@ -345,13 +347,14 @@ focus_status_t focus_dense_causal_fwd(const focus_params_t* p, const void* Q, co
   AttnArgs a = attn_args(p, Q, K, V, O, lse_opt, ws, L);
   a.w = p->n;
   if (p->dtype == FOCUS_F32) return cuda_status(launch_attn_simt_f32(a, p->d, kModeDense, 0, st));
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   const uint64_t planes = static_cast<uint64_t>(p->B) * p->H_kv;
   const uint64_t qplanes = static_cast<uint64_t>(p->B) * p->H;
   if (!make_map(&tq, Q, p->d, p->n, qplanes, 128, 3) ||
-      !make_map(&tk, K, p->d, p->n, planes, 128, 3) || !make_map(&tv, V, p->d, p->n, planes, 128, 3))
+      !make_map(&tk, K, p->d, p->n, planes, 128, 3) || !make_map(&tv, V, p->d, p->n, planes, 128, 3) ||
+      !make_map(&to, O, p->d, p->n, qplanes, 128, 3))
     return FOCUS_ERR_CUDA;
-  return cuda_status(launch_attn_tc_bf16(a, &tq, &tk, &tv, p->d, kModeDense, 0, sm_count(), st));
+  return cuda_status(launch_attn_tc_bf16(a, &tq, &tk, &tv, &to, &to, p->d, kModeDense, 0, sm_count(), st));
 }
 
 focus_status_t focus_layer_fwd_host(const focus_params_t* p, const void* host_h,

@@ -88,8 +88,11 @@ cudaError_t launch_attn_simt_f32(const AttnArgs& a, int d, int mode, int max_ite
 cudaError_t launch_permute_kv_bf16(const void* K, const void* V, void* Ks, void* Vs,
                                    const int32_t* perm, int B, int H_kv, int n, int d, int A,
                                    cudaStream_t st);
+// tm_o / tm_of: O and the group partial O_far as {d, n, B*H} tiles (local and
+// dense passes store O, and the local pass loads O_far, through them).
 cudaError_t launch_attn_tc_bf16(const AttnArgs& a, const CUtensorMap* tm_q,
-                                const CUtensorMap* tm_k, const CUtensorMap* tm_v, int d, int mode,
+                                const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                const CUtensorMap* tm_o, const CUtensorMap* tm_of, int d, int mode,
                                 int max_items, int num_sms, cudaStream_t st);
 cudaError_t setup_attn_kernels();
 

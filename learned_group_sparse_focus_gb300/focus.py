@@ -16,7 +16,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_lib", "libfocus.so")
 
 F32, BF16 = 0, 1
-TILE_M = 256
+TILE_M = 128
 TILE_N = 128
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace too small",
