@@ -64,12 +64,15 @@ struct AssignCfg {
   static constexpr int kStageA = kBM * kBK * 2;            // 16 KB
   static constexpr int kStageB = NALLOC * kBK * 2;         // <= 64 KB
   static constexpr int kStage = kStageA + kStageB;
-  static constexpr int kStages = (196 * 1024 / kStage) > 6 ? 6 : (196 * 1024 / kStage);
+  // narrow projections: four stages and two CTAs per SM, so a whole layer's
+  // tiles run in one wave and both CTAs' loads are in flight together
+  static constexpr int kStages = NALLOC <= 128 ? 4 : ((196 * 1024 / kStage) > 6 ? 6 : (196 * 1024 / kStage));
   static constexpr int kSmem = kStages * kStage + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int kMinBlocks = kSmem <= 112 * 1024 ? 2 : 1;
 };
 
 template <int NALLOC>
-__global__ void __launch_bounds__(128, 1) assign_tc_kernel(
+__global__ void __launch_bounds__(128, AssignCfg<NALLOC>::kMinBlocks) assign_tc_kernel(
     const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
     const __nv_bfloat16* __restrict__ C, int32_t* __restrict__ gid, int B, int n, int D, int d_g,
     int K, int A, int* err) {
@@ -183,7 +186,33 @@ __global__ void __launch_bounds__(128, 1) assign_tc_kernel(
       for (int e = threadIdx.x; e < kn * d_g; e += blockDim.x)
         Cs[e] = __bfloat162float(C[(static_cast<size_t>(a) * K + k0) * d_g + e]);
       __syncthreads();
-      for (int k = 0; k < kn; ++k) {
+      int k = 0;
+      // four centroids per pass: independent FMA chains, 16-byte broadcast reads;
+      // each score still sums j = 0, 1, ... in order
+      for (; k + 4 <= kn; k += 4) {
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < 128; j += 4) {
+          if (j < d_g) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float4 c4 = *reinterpret_cast<const float4*>(Cs + (k + q) * d_g + j);
+              sc[q] = fmaf(p[j], c4.x, sc[q]);
+              sc[q] = fmaf(p[j + 1], c4.y, sc[q]);
+              sc[q] = fmaf(p[j + 2], c4.z, sc[q]);
+              sc[q] = fmaf(p[j + 3], c4.w, sc[q]);
+            }
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (sc[q] > bs || k0 + k + q == 0) {
+            bs = sc[q];
+            best = k0 + k + q;
+          }
+        }
+      }
+      for (; k < kn; ++k) {
         const float* ck = Cs + k * d_g;
         float s = 0.f;
 #pragma unroll
