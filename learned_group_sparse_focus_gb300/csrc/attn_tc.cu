@@ -63,9 +63,10 @@ struct AttnCfg {
   static constexpr int kTile = 128 * D * 2;  // one 128-row Q/K/V tile
   static constexpr int kQ = 0;               // staged Q tile
   static constexpr int kRing = kQ + kTile;   // K/V slots
-  static constexpr int kOst = kRing + kKvSlots * kTile;   // O tile staging (local, dense)
-  static constexpr int kBar = kOst + kTile;
-  static constexpr int kSmem = kBar + 512 + 1024;
+  static constexpr int kOst = kRing + kKvSlots * kTile;   // O tile staging
+  static constexpr int kBar = kOst + kTile;                 // barriers (< 256 B)
+  static constexpr int kRows = kBar + 256;                  // group pass: row -> token (+1), 0 = skip
+  static constexpr int kSmem = kRows + 128 * 4 + 1024;
   static constexpr uint32_t kS = 0;          // two S buffers of 128 columns
   static constexpr uint32_t kO = 256;        // O: d columns
   static constexpr uint32_t kQt = 384;       // Q: d/2 columns of bf16 pairs
@@ -136,6 +137,16 @@ __device__ __forceinline__ void decode_unit(const AttnArgs& a, int u, Unit& U) {
   U.zq = U.b * a.H + U.h;
 }
 
+// Unit walked by this CTA in round k, or -1 past the end.  Rounds alternate
+// direction (0..G-1, then G-1..0, ...), so over a longest-first unit list
+// every CTA gets a balanced mix of long and short units.
+__device__ __forceinline__ int snake_unit(int k, int n_units) {
+  const int G = gridDim.x, base = k * G;
+  if (base >= n_units) return -1;
+  const int u = base + ((k & 1) ? G - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x));
+  return u < n_units ? u : -2;
+}
+
 // What the epilogue of a unit needs once its tile loop is over.  In the local
 // pass the row's far flag and group LSE are read when the unit starts (and its
 // group O row is prefetched into L2), so their latency hides behind the tiles.
@@ -174,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* kv_empty = bars + 14 + kKvSlots;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14 + 2 * kKvSlots);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* row_tok = reinterpret_cast<int*>(smem + Cfg::kRows);
 
   const int warp = warp_id(), lane = lane_id();
   const int n_units = unit_count<MODE>(a);
@@ -215,7 +227,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int qn = 0;                // Q tiles staged
     bool ok = true;
     const __nv_bfloat16* Qg = static_cast<const __nv_bfloat16*>(a.Q);
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+    for (int k = 0; ok; ++k) {
+      const int u = snake_unit(k, n_units);
+      if (u == -1) break;
+      if (u < 0) continue;
       Unit U;
       decode_unit<MODE>(a, u, U);
       if (qn > 0 && !warp_wait(q_free, (qn - 1) & 1, abort, a.err)) break;
@@ -304,7 +319,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int c = 0;        // K/V tiles walked
       int un = 0;       // units walked
       bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      for (int k = 0; ok; ++k) {
+        const int u = snake_unit(k, n_units);
+        if (u == -1) break;
+        if (u < 0) continue;
         Unit U;
         decode_unit<MODE>(a, u, U);
         const int nt = U.t1 - U.t0 + 1;
@@ -383,10 +401,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         lse2 = mm + log2f(den);
       }
       if (MODE == kModeGroup) {
-        // rows are scattered by perm: each thread stores its own row
+        // rows are scattered by perm: stage the tile in shared memory, then
+        // each warp writes two whole 256-byte rows per store instruction
         const bool write = s.valid && s.l > 0.f;
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.O_far);
-        const size_t orow = (qrow + (s.valid ? s.pos : 0)) * D;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t ou[32];
@@ -396,19 +413,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(o_free);
           }
-          if (write) {
 #pragma unroll
-            for (int cc = 0; cc < 32; cc += 8) {
-              uint4 o4;
-              o4.x = pack_bf16x2(__uint_as_float(ou[cc + 0]) * c1, __uint_as_float(ou[cc + 1]) * c1);
-              o4.y = pack_bf16x2(__uint_as_float(ou[cc + 2]) * c1, __uint_as_float(ou[cc + 3]) * c1);
-              o4.z = pack_bf16x2(__uint_as_float(ou[cc + 4]) * c1, __uint_as_float(ou[cc + 5]) * c1);
-              o4.w = pack_bf16x2(__uint_as_float(ou[cc + 6]) * c1, __uint_as_float(ou[cc + 7]) * c1);
-              *reinterpret_cast<uint4*>(dst + orow + c0 + cc) = o4;
+          for (int cc = 0; cc < 32; cc += 8) {
+            const int v = (c0 + cc) >> 3;
+            uint4 o4;
+            o4.x = pack_bf16x2(__uint_as_float(ou[cc + 0]) * c1, __uint_as_float(ou[cc + 1]) * c1);
+            o4.y = pack_bf16x2(__uint_as_float(ou[cc + 2]) * c1, __uint_as_float(ou[cc + 3]) * c1);
+            o4.z = pack_bf16x2(__uint_as_float(ou[cc + 4]) * c1, __uint_as_float(ou[cc + 5]) * c1);
+            o4.w = pack_bf16x2(__uint_as_float(ou[cc + 6]) * c1, __uint_as_float(ou[cc + 7]) * c1);
+            *reinterpret_cast<uint4*>(sO + (v >> 3) * Cfg::kChunk + r * 128 + (((v & 7) ^ (r & 7)) << 4)) = o4;
+          }
+        }
+        row_tok[r] = write ? s.pos + 1 : 0;
+        if (write) a.lse_far[qrow + s.pos] = lse2 * kLn2;
+        named_barrier(1, 128);
+        {
+          __nv_bfloat16* Of = static_cast<__nv_bfloat16*>(a.O_far);
+          constexpr int kVec = D / 8;               // 16-byte pieces per row
+          constexpr int kRowsPerStore = 32 / kVec;  // rows one warp store covers
+#pragma unroll 4
+          for (int rr = 0; rr < 32; rr += kRowsPerStore) {
+            const int row = warp * 32 + rr + lane / kVec;
+            const int v = lane % kVec;
+            const int tok = row_tok[row];
+            if (tok > 0) {
+              const uint4 o4 = *reinterpret_cast<const uint4*>(sO + (v >> 3) * Cfg::kChunk + row * 128 +
+                                                             (((v & 7) ^ (row & 7)) << 4));
+              *reinterpret_cast<uint4*>(Of + (qrow + tok - 1) * D + v * 8) = o4;
             }
           }
         }
-        if (write) a.lse_far[qrow + s.pos] = lse2 * kLn2;
+        named_barrier(1, 128);   // the stage is free for the next unit
         return true;
       }
       // local and dense: the tile goes through the shared-memory stage (same
@@ -463,7 +498,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
 
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+    for (int k = 0; ok; ++k) {
+      const int u = snake_unit(k, n_units);
+      if (u == -1) break;
+      if (u < 0) continue;
       Unit U;
       decode_unit<MODE>(a, u, U);
       // 1. this unit's Q row: staged tile -> registers -> TMEM.  The previous
