@@ -273,6 +273,8 @@ static focus_status_t attention_common(const focus_params_t* p, const void* Q, c
       (lse && !aligned16(lse)))
     return FOCUS_ERR_INVALID_ARG;
   if (!(p->d == 64 || p->d == 128)) return FOCUS_ERR_UNSUPPORTED;
+  // tensor-map row coordinates are 32-bit
+  if (static_cast<long long>(p->B) * p->H * p->n >= (1LL << 31)) return FOCUS_ERR_UNSUPPORTED;
   if (focus_status_t s = check_ws(p, ws, ws_bytes)) return s;
   return ensure_setup();
 }
@@ -324,7 +326,10 @@ focus_status_t focus_attention_fwd_timed(const focus_params_t* p, const void* Q,
       !make_map(&tof, a.O_far, p->d, p->n, qplanes, 128, 3))
     return FOCUS_ERR_CUDA;
   const int sms = sm_count();
-  e = launch_attn_tc_bf16(a, &tq, &tks, &tvs, &to, &tof, p->d, kModeGroup, L.max_items, sms, st);
+  // group pass: Q rows are gathered through perm from a 2-D view with one-row boxes
+  CUtensorMap tqg;
+  if (!make_map(&tqg, Q, p->d, qplanes * p->n, 1, 1, 2)) return FOCUS_ERR_CUDA;
+  e = launch_attn_tc_bf16(a, &tqg, &tks, &tvs, &to, &tof, p->d, kModeGroup, L.max_items, sms, st);
   if (e == cudaSuccess) e = mark(2);
   if (e == cudaSuccess) e = launch_attn_tc_bf16(a, &tq, &tk, &tv, &to, &tof, p->d, kModeLocal, 0, sms, st);
   if (e == cudaSuccess) e = mark(3);

@@ -35,7 +35,7 @@
 //               and dense passes it builds the O tile in shared memory (merged
 //               with the group partial the load warp staged there) and writes
 //               it with one TMA store
-//   warp 4      loads: Q tile into shared memory (TMA, or a cp.async row gather
+//   warp 4      loads: Q tile into shared memory (TMA, or a TMA row gather
 //               through perm in group mode), K/V tiles (TMA, 5-slot ring) and,
 //               in the local pass, the unit's group-partial O tile
 //   warp 5      TMEM owner; issues O += P(t) V(t) once P(t) is written
@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = warp_id(), lane = lane_id();
   const int n_units = unit_count<MODE>(a);
   if (threadIdx.x == 0) {
-    mbar_init(q_full, MODE == kModeGroup ? 32 : 1);
+    mbar_init(q_full, 1);
     mbar_init(q_free, 128);
     mbar_init(q_ready, 128);
     mbar_init(o_done, 1);
@@ -235,20 +235,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       decode_unit<MODE>(a, u, U);
       if (qn > 0 && !warp_wait(q_free, (qn - 1) & 1, abort, a.err)) break;
       if (MODE == kModeGroup) {
-        // gather 128 rows through perm, four rows per lane, zero past the item
-        for (int k = 0; k < kBM / 32; ++k) {
-          const int r = lane + 32 * k;
-          const bool valid = r < U.nrows;
-          const int pos = valid ? a.perm[static_cast<size_t>(U.prob) * a.n + U.row0 + r] : 0;
-          const __nv_bfloat16* src = Qg + (static_cast<size_t>(U.zq) * a.n + pos) * D;
+        // TMA row gather through perm: lane l fetches tile rows 4l..4l+3 of every
+        // 64-column slab (tm_q is a 2-D {d, B*H*n} view with one-row boxes);
+        // rows past the item repeat its first row, whose scores are all masked
+        if (lane == 0) mbar_expect_tx(q_full, Cfg::kTile);
+        __syncwarp();
+        const int32_t* pp = a.perm + static_cast<size_t>(U.prob) * a.n + U.row0;
+        const int first = pp[0];
+        int rows[4];
 #pragma unroll
-          for (int v = 0; v < D / 8; ++v)
-            cp_async_16(sQ + (v >> 3) * Cfg::kChunk + r * 128 + (((v & 7) ^ (r & 7)) << 4), src + v * 8,
-                        valid ? 16u : 0u);
+        for (int j = 0; j < 4; ++j) {
+          const int rr = 4 * lane + j;
+          rows[j] = U.zq * a.n + (rr < U.nrows ? pp[rr] : first);
         }
-        cp_async_wait_all();
-        fence_proxy_async_smem();
-        mbar_arrive(q_full);
+#pragma unroll
+        for (int ch = 0; ch < kChunks; ++ch)
+          tma_gather4(sQ + ch * Cfg::kChunk + 4 * lane * 128, &tm_q, q_full, ch * 64, rows[0], rows[1],
+                      rows[2], rows[3]);
       } else if (lane == 0) {
         mbar_expect_tx(q_full, Cfg::kTile);
 #pragma unroll
@@ -294,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (!mbar_try_wait(&kv_full[L % kKvSlots], (L / kKvSlots) & 1) &&
                global_ns() - t0 < kWaitTimeoutNs) {}
       }
-      if (MODE != kModeGroup && qn > 0) {
+      if (qn > 0) {
         const unsigned long long t0 = global_ns();
         while (!mbar_try_wait(q_full, (qn - 1) & 1) && global_ns() - t0 < kWaitTimeoutNs) {}
       }
@@ -426,24 +429,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         row_tok[r] = write ? s.pos + 1 : 0;
         if (write) a.lse_far[qrow + s.pos] = lse2 * kLn2;
-        named_barrier(1, 128);
+        __syncwarp();   // a warp stages and stores only its own 32 rows
         {
           __nv_bfloat16* Of = static_cast<__nv_bfloat16*>(a.O_far);
           constexpr int kVec = D / 8;               // 16-byte pieces per row
           constexpr int kRowsPerStore = 32 / kVec;  // rows one warp store covers
+          constexpr int kIters = 32 / kRowsPerStore;
+          const int v = lane % kVec;
 #pragma unroll 4
-          for (int rr = 0; rr < 32; rr += kRowsPerStore) {
-            const int row = warp * 32 + rr + lane / kVec;
-            const int v = lane % kVec;
-            const int tok = row_tok[row];
-            if (tok > 0) {
-              const uint4 o4 = *reinterpret_cast<const uint4*>(sO + (v >> 3) * Cfg::kChunk + row * 128 +
-                                                             (((v & 7) ^ (row & 7)) << 4));
-              *reinterpret_cast<uint4*>(Of + (qrow + tok - 1) * D + v * 8) = o4;
-            }
+          for (int it = 0; it < kIters; ++it) {
+            const int row = warp * 32 + it * kRowsPerStore + lane / kVec;
+            const int tk = row_tok[row];
+            if (tk > 0)
+              *reinterpret_cast<uint4*>(Of + (qrow + tk - 1) * D + v * 8) = *reinterpret_cast<const uint4*>(
+                  sO + (v >> 3) * Cfg::kChunk + row * 128 + (((v & 7) ^ (row & 7)) << 4));
           }
         }
-        named_barrier(1, 128);   // the stage is free for the next unit
+        __syncwarp();   // the warp's rows of the stage may be rewritten
         return true;
       }
       // local and dense: the tile goes through the shared-memory stage (same
