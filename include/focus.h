@@ -147,6 +147,40 @@ FOCUS_API focus_status_t focus_build_index(const focus_params_t* p, const int32_
                                  focus_index_t* idx_out, void* ws, size_t ws_bytes,
                                  void* stream);
 
+/* Bytes of the fixed device scratch behind focus_build_index_static. */
+#define FOCUS_INDEX_STATIC_SCRATCH_BYTES (1u << 20)
+
+/* focus_build_index with no workspace and no allocation.  The papers have no
+ * counterpart: this is a deployment entry point for callers that cannot
+ * allocate device memory when they build the index (a process whose device
+ * footprint is fixed at start-up, or one that wants the index without the
+ * attention workspace).  Same operation and bit-identical outputs as
+ * focus_build_index ("Focus: Learning Which Attention Pairs Matter" 2.2).
+ *   gid  [B, A, n] int32 device input, 16-byte aligned.
+ *   idx  host struct, in/out.  On entry counts, offsets, perm, rank,
+ *        farlen_tok, farlen_slot, items, order and n_items are caller-owned
+ *        device buffers (16-byte aligned) sized as documented for
+ *        focus_index_t, and max_items is the capacity of items and order,
+ *        at least B*A*(ceil(n / FOCUS_TILE_M) + min(K, n)).  On return
+ *        max_items holds that bound and w_eff the window, so the index can be
+ *        passed to focus_attention_fwd like one from focus_build_index.
+ *   err  device int32 error word, 256-byte aligned (focus_check_errors(err,
+ *        stream) reads and clears it).  It must hold 0 before the first call;
+ *        kernels only OR bits into it (FOCUS_ERR_BAD_GROUP_ID as in
+ *        focus_build_index).
+ * The sort's scratch (per-segment histograms, tile bases, item costs:
+ * 4*(B*A*ceil(n/1024)*K + B*A*(K+1) + max_items) bytes plus alignment) comes
+ * from one fixed device array of FOCUS_INDEX_STATIC_SCRATCH_BYTES per device;
+ * a larger problem returns FOCUS_ERR_WORKSPACE before anything is launched.
+ * Nothing in that array has to start at zero.  All calls on a device share it,
+ * so calls whose kernels may overlap (other streams, other host threads) race:
+ * order them, e.g. on one stream.  The first call on each device looks up the
+ * array's address and sets kernel attributes; make that call before capturing
+ * a stream.  Returns FOCUS_ERR_INVALID_ARG for a bad p, pointer or capacity. */
+FOCUS_API focus_status_t focus_build_index_static(const focus_params_t* p, const int32_t* gid,
+                                                  focus_index_t* idx, int32_t* err,
+                                                  void* stream);
+
 /* Focus attention over the kept pairs ("Focus: Learning Which Attention Pairs
  * Matter" 2.1, 2.2, 3.3; "Why Attend to Everything?" 2.1, 2.3).  Row i of head h
  * attends to key j iff j <= i and (i - j < w or g_i == g_j), with

@@ -65,6 +65,7 @@ def _load():
         "focus_dense_causal_fwd": ([P, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp], ctypes.c_int),
         "focus_layer_fwd_host": ([P] + [vp] * 7 + [vp] * 8 + [vp, ctypes.c_size_t, vp], ctypes.c_int),
         "focus_check_errors": ([vp, vp], ctypes.c_int),
+        "focus_build_index_static": ([P, vp, ctypes.POINTER(Index), vp, vp], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -77,7 +78,8 @@ _lib = _load()
 
 EXPORTED = ("focus_abi_version", "focus_status_string", "focus_workspace_bytes",
             "focus_workspace_init", "focus_assign", "focus_build_index", "focus_attention_fwd",
-            "focus_attention_fwd_timed", "focus_dense_causal_fwd", "focus_layer_fwd_host", "focus_check_errors")
+            "focus_attention_fwd_timed", "focus_dense_causal_fwd", "focus_layer_fwd_host", "focus_check_errors",
+            "focus_build_index_static")
 
 
 def lib():
@@ -181,6 +183,32 @@ def focus_layer_fwd_host(p: Params, host: dict, dev: dict, ws, stream=None):
 def focus_check_errors(ws, stream=None) -> int:
     """Synchronise the stream; return (and clear) the device error status."""
     return int(_lib.focus_check_errors(_ptr(ws), _stream(stream)))
+
+
+def index_buffers(p: Params, device="cuda") -> dict:
+    """Caller-owned output buffers for focus_build_index_static, sized as the
+    index arrays of focus_build_index, plus a zeroed 256-byte error word."""
+    P, n, K = p.B * p.A, p.n, p.K
+    m = P * ((n + TILE_M - 1) // TILE_M + min(K, n))
+    z = lambda *shape: torch.empty(shape, dtype=torch.int32, device=device)
+    return dict(counts=z(p.B, p.A, K), offsets=z(p.B, p.A, K + 1), perm=z(p.B, p.A, n),
+                rank=z(p.B, p.A, n), farlen_tok=z(p.B, p.A, n), farlen_slot=z(p.B, p.A, n),
+                items=z(m, 8), order=z(m), n_items=z(1),
+                err=torch.zeros(64, dtype=torch.int32, device=device))
+
+
+def focus_build_index_static(p: Params, gid, bufs: dict, stream=None) -> Index:
+    """focus_build_index into the caller-owned buffers of index_buffers(); the
+    sort's scratch is the library's fixed device array (no workspace)."""
+    idx = Index()
+    for name in ("counts", "offsets", "perm", "rank", "farlen_tok", "farlen_slot", "items", "order",
+                 "n_items"):
+        setattr(idx, name, _ptr(bufs[name]))
+    idx.max_items = bufs["order"].numel()
+    _check("focus_build_index_static",
+           _lib.focus_build_index_static(ctypes.byref(p), _ptr(gid), ctypes.byref(idx), _ptr(bufs["err"]),
+                                         _stream(stream)))
+    return idx
 
 
 # ------------------------------------------------------------ index views ---
