@@ -25,22 +25,26 @@
 // softmax has read it: the S product of a later tile runs while the softmax
 // works, and only O += P V waits for P.
 //
-// Warp roles (224 threads), one CTA per SM looping over units:
-//   warps 0-3   softmax, one query row per thread: copy the staged Q row into
-//               TMEM, then per key tile read S from TMEM, apply the keep rule
-//               to boundary tiles, online max/sum in fp32 (exp2 domain), write
-//               P, rescale O only when the running max grows by more than 2^8;
-//               the epilogue of a unit runs after the next unit's Q is in TMEM,
-//               so the next unit's first S products overlap it; in the local
-//               and dense passes it builds the O tile in shared memory (merged
-//               with the group partial the load warp staged there) and writes
-//               it with one TMA store
-//   warp 4      loads: Q tile into shared memory (TMA, or a TMA row gather
+// Warp roles (384 threads), one CTA per SM looping over units:
+//   warps 0-7   softmax, two warps per query row (warps w and w + 4 share TMEM
+//               lane quadrant w, each takes half of every row's columns): copy
+//               the staged Q half-row into TMEM, then per key tile read the
+//               half S row from TMEM, apply the keep rule to boundary tiles,
+//               agree on the row max with the partner through shared memory,
+//               exp2 and sum in fp32, write the half P row, rescale the half O
+//               row only when the running max grows by more than 2^8; the
+//               epilogue of a unit runs after the next unit's Q is in TMEM, so
+//               the next unit's first S products overlap it; in the local and
+//               dense passes it builds the O tile in shared memory (merged with
+//               the group partial the load warp staged there) and writes it
+//               with one TMA store
+//   warp 8      loads: Q tile into shared memory (TMA, or a TMA row gather
 //               through perm in group mode), K/V tiles (TMA, 5-slot ring) and,
 //               in the local pass, the unit's group-partial O tile
-//   warp 5      TMEM owner; issues O += P(t) V(t) once P(t) is written
-//   warp 6      issues S(t) = Q K(t)^T once the softmax has read S(t-2),
+//   warp 9      TMEM owner; issues O += P(t) V(t) once P(t) is written
+//   warp 10     issues S(t) = Q K(t)^T once the softmax has read S(t-2),
 //               the previous content of the same buffer
+//   warp 11     idle (completes warpgroup 2 for the register split)
 // Every wait is bounded; on timeout the CTA raises an error bit, drains its
 // copies, frees TMEM and exits.
 #include "common.cuh"
@@ -52,7 +56,19 @@ namespace {
 constexpr int kBN = 128;                     // keys per tile
 constexpr int kBM = 128;                     // query rows per unit
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
-constexpr int kThreads = 224;
+constexpr int kSoftmaxWarps = 8;            // two per TMEM lane quadrant
+constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
+constexpr int kWarpLoad = kSoftmaxWarps;     // TMA loads
+constexpr int kWarpPV = kSoftmaxWarps + 1;   // TMEM owner, O += P V issuer
+constexpr int kWarpS = kSoftmaxWarps + 2;    // S = Q K^T issuer
+constexpr int kThreads = 32 * (kSoftmaxWarps + 4);   // warp 11 idles (whole warpgroups)
+// Register split (setmaxnreg).  The kernel launches at 168 registers per thread
+// (384 x 168 = 64512, the cap for 12 warps).  Warpgroup 2 gives registers back
+// down to 88 and the two softmax warpgroups take them up to 208:
+// 128 * 88 + 256 * 208 = 64512, and each SM sub-partition then holds
+// 208 + 208 + 88 = 504 registers per lane (<= 512).
+constexpr int kRegsLow = 88;
+constexpr int kRegsHigh = 208;
 // K and V tiles share one ring of slots, K(t) then V(t): the loader runs about
 // two and a half tiles ahead of the MMAs.
 constexpr int kKvSlots = 5;
@@ -65,8 +81,8 @@ struct AttnCfg {
   static constexpr int kRing = kQ + kTile;   // K/V slots
   static constexpr int kOst = kRing + kKvSlots * kTile;   // O tile staging
   static constexpr int kBar = kOst + kTile;                 // barriers (< 256 B)
-  static constexpr int kRows = kBar + 256;                  // group pass: row -> token (+1), 0 = skip
-  static constexpr int kSmem = kRows + 128 * 4 + 1024;
+  static constexpr int kXch = kBar + 256;                   // row max / sum exchange: [2][2][128] fp32
+  static constexpr int kSmem = kXch + 2 * 2 * 128 * 4;
   static constexpr uint32_t kS = 0;          // two S buffers of 128 columns
   static constexpr uint32_t kO = 256;        // O: d columns
   static constexpr uint32_t kQt = 384;       // Q: d/2 columns of bf16 pairs
@@ -164,44 +180,54 @@ __global__ void __launch_bounds__(kThreads, 1)
   using Cfg = AttnCfg<D>;
   constexpr int kChunks = D / 64;
 
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // The layout uses the whole 227 KB, with no room to realign: the dynamic
+  // shared memory base must already sit on a 1024-byte boundary (the 128-byte
+  // swizzle atoms), which it does when the kernel declares no static shared
+  // memory.  Checked, not assumed: a misaligned base only raises an error.
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(a.err, kErrInternal);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   uint8_t* sQ = smem + Cfg::kQ;
   uint8_t* sKV = smem + Cfg::kRing;
   uint8_t* sO = smem + Cfg::kOst;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBar);
   uint64_t* q_full = bars + 0;        // staged Q tile landed in shared memory
-  uint64_t* q_free = bars + 1;        // staged Q copied out (128 arrivals)
-  uint64_t* q_ready = bars + 2;       // Q in TMEM (128 arrivals)
+  uint64_t* q_free = bars + 1;        // staged Q copied out (softmax threads)
+  uint64_t* q_ready = bars + 2;       // Q in TMEM (softmax threads)
   uint64_t* o_done = bars + 3;        // one phase per PV product
   uint64_t* o_final = bars + 4;       // one phase per unit: its last PV landed
-  uint64_t* o_free = bars + 5;        // one phase per unit: O read out (128)
+  uint64_t* o_free = bars + 5;        // one phase per unit: O read out (softmax threads)
   uint64_t* s_full = bars + 6;        // [2] per S buffer
-  uint64_t* p_ready = bars + 8;       // [2] per S buffer (128 arrivals)
-  uint64_t* s_free = bars + 10;       // [2] per S buffer: the softmax has read it (128)
+  uint64_t* p_ready = bars + 8;       // [2] per S buffer (softmax threads)
+  uint64_t* s_free = bars + 10;       // [2] per S buffer: the softmax has read it
   uint64_t* ofar_full = bars + 12;    // local: the unit's group-partial tile is staged
   uint64_t* ost_free = bars + 13;     // local: the O stage was stored out (1 arrival)
   uint64_t* kv_full = bars + 14;      // [kKvSlots]
   uint64_t* kv_empty = bars + 14 + kKvSlots;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14 + 2 * kKvSlots);
+  uint64_t* ost_full = bars + 14 + 2 * kKvSlots;   // local/dense: the O stage is written (softmax threads)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15 + 2 * kKvSlots);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* row_tok = reinterpret_cast<int*>(smem + Cfg::kRows);
+  float* xch = reinterpret_cast<float*>(smem + Cfg::kXch);
 
   const int warp = warp_id(), lane = lane_id();
   const int n_units = unit_count<MODE>(a);
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    mbar_init(q_free, 128);
-    mbar_init(q_ready, 128);
+    mbar_init(q_free, kSoftmaxThreads);
+    mbar_init(q_ready, kSoftmaxThreads);
     mbar_init(o_done, 1);
     mbar_init(o_final, 1);
-    mbar_init(o_free, 128);
+    mbar_init(o_free, kSoftmaxThreads);
     mbar_init(ofar_full, 1);
     mbar_init(ost_free, 1);
+    mbar_init(ost_full, kSoftmaxThreads);
     for (int x = 0; x < 2; ++x) {
       mbar_init(&s_full[x], 1);
-      mbar_init(&p_ready[x], 128);
-      mbar_init(&s_free[x], 128);
+      mbar_init(&p_ready[x], kSoftmaxThreads);
+      mbar_init(&s_free[x], kSoftmaxThreads);
     }
     for (int k = 0; k < kKvSlots; ++k) {
       mbar_init(&kv_full[k], 1);
@@ -215,210 +241,247 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (MODE != kModeGroup) prefetch_tmap(&tm_o);
     if (MODE == kModeLocal) prefetch_tmap(&tm_of);
   }
-  if (warp == 5) tmem_alloc(tmem_slot, Cfg::kTmemCols);
+  if (warp == kWarpPV) tmem_alloc(tmem_slot, Cfg::kTmemCols);
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
-    // ---------------------------------------------------------- loads ---
-    int c = 0;                 // K/V tiles walked
-    int issued = 0;            // K/V loads issued (lane 0)
-    int qn = 0;                // Q tiles staged
-    bool ok = true;
-    const __nv_bfloat16* Qg = static_cast<const __nv_bfloat16*>(a.Q);
-    for (int k = 0; ok; ++k) {
-      const int u = snake_unit(k, n_units);
-      if (u == -1) break;
-      if (u < 0) continue;
-      Unit U;
-      decode_unit<MODE>(a, u, U);
-      if (qn > 0 && !warp_wait(q_free, (qn - 1) & 1, abort, a.err)) break;
-      if (MODE == kModeGroup) {
-        // TMA row gather through perm: lane l fetches tile rows 4l..4l+3 of every
-        // 64-column slab (tm_q is a 2-D {d, B*H*n} view with one-row boxes);
-        // rows past the item repeat its first row, whose scores are all masked
-        if (lane == 0) mbar_expect_tx(q_full, Cfg::kTile);
-        __syncwarp();
-        const int32_t* pp = a.perm + static_cast<size_t>(U.prob) * a.n + U.row0;
-        const int first = pp[0];
-        int rows[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int rr = 4 * lane + j;
-          rows[j] = U.zq * a.n + (rr < U.nrows ? pp[rr] : first);
-        }
-#pragma unroll
-        for (int ch = 0; ch < kChunks; ++ch)
-          tma_gather4(sQ + ch * Cfg::kChunk + 4 * lane * 128, &tm_q, q_full, ch * 64, rows[0], rows[1],
-                      rows[2], rows[3]);
-      } else if (lane == 0) {
-        mbar_expect_tx(q_full, Cfg::kTile);
-#pragma unroll
-        for (int ch = 0; ch < kChunks; ++ch)
-          tma_load_3d(sQ + ch * Cfg::kChunk, &tm_q, q_full, ch * 64, U.row0, U.zq);
-      }
-      ++qn;
-      if (lane == 0) {
-        // load L = 2c (K of tile c) and 2c+1 (V of tile c) into slot L % kKvSlots
-        for (int t = U.t0; t <= U.t1 && ok; ++t, ++c) {
-          const int y = U.ybase + t * kBN;
-#pragma unroll
-          for (int kv = 0; kv < 2; ++kv) {
-            const int L = 2 * c + kv, sl = L % kKvSlots, use = L / kKvSlots;
-            if (use > 0 && !mbar_wait(&kv_empty[sl], (use - 1) & 1, abort, a.err)) { ok = false; break; }
-            mbar_expect_tx(&kv_full[sl], Cfg::kTile);
-#pragma unroll
-            for (int ch = 0; ch < kChunks; ++ch)
-              tma_load_3d(sKV + sl * Cfg::kTile + ch * Cfg::kChunk, kv ? &tm_v : &tm_k, &kv_full[sl],
-                          ch * 64, y, U.zkv);
-            ++issued;
-          }
-        }
-        if (MODE == kModeLocal && ok) {
-          // the unit's group-partial tile into the O stage, once the previous
-          // unit's O has been stored out of it
-          if (qn > 1 && !mbar_wait(ost_free, (qn - 2) & 1, abort, a.err)) ok = false;
-          if (ok) {
-            mbar_expect_tx(ofar_full, Cfg::kTile);
-#pragma unroll
-            for (int ch = 0; ch < kChunks; ++ch)
-              tma_load_3d(sO + ch * Cfg::kChunk, &tm_of, ofar_full, ch * 64, U.row0, U.zq);
-          }
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort;
-      c = __shfl_sync(0xffffffffu, c, 0);
-    }
-    if (*abort && lane == 0) {
-      // drain: TMA copies already issued must land before the CTA exits
-      for (int L = max(0, issued - kKvSlots); L < issued; ++L) {
-        const unsigned long long t0 = global_ns();
-        while (!mbar_try_wait(&kv_full[L % kKvSlots], (L / kKvSlots) & 1) &&
-               global_ns() - t0 < kWaitTimeoutNs) {}
-      }
-      if (qn > 0) {
-        const unsigned long long t0 = global_ns();
-        while (!mbar_try_wait(q_full, (qn - 1) & 1) && global_ns() - t0 < kWaitTimeoutNs) {}
-      }
-      if (MODE == kModeLocal && qn > 0) {
-        const unsigned long long t0 = global_ns();
-        while (!mbar_try_wait(ofar_full, (qn - 1) & 1) && global_ns() - t0 < kWaitTimeoutNs) {}
-      }
-    }
-  } else if (warp == 5 || warp == 6) {
-    // ----------------------------------------------------------- MMAs ---
-    // Two issuing threads: warp 6 issues the S products, warp 5 the PV
-    // products.  The two chains share no TMEM (S buffers and Q vs P and O), so
-    // neither waits on the other's barriers and the tensor pipe sees both.
-    if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, kBN, false, false);
-      constexpr uint32_t idPV = idesc_bf16_f32(128, D, false, true);
-      constexpr uint32_t dhi = sw128_desc_hi();
-      const uint32_t r0 = smem_u32(sKV);
-      const uint32_t klo = sw128_desc_lo(r0, 16);            // K slots, K-major
-      const uint32_t vlo = sw128_desc_lo(r0, Cfg::kChunk);   // V slots, MN-major
-      int g = 0;        // tiles (S buffers) walked
-      int c = 0;        // K/V tiles walked
-      int un = 0;       // units walked
+  if (warp >= kSoftmaxWarps) {
+    // warpgroup 2 (loads, the two MMA issuers, one idle warp) hands registers
+    // to the softmax warpgroups
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+    if (warp == kWarpLoad) {
+      // ---------------------------------------------------------- loads ---
+      int c = 0;                 // K/V tiles walked
+      int issued = 0;            // K/V loads issued (lane 0)
+      int qn = 0;                // Q tiles staged
       bool ok = true;
+      const __nv_bfloat16* Qg = static_cast<const __nv_bfloat16*>(a.Q);
       for (int k = 0; ok; ++k) {
         const int u = snake_unit(k, n_units);
         if (u == -1) break;
         if (u < 0) continue;
         Unit U;
         decode_unit<MODE>(a, u, U);
-        const int nt = U.t1 - U.t0 + 1;
-        if (warp == 6) {
-          // S(gg) = Q K^T into S buffer gg&1.  The first two tiles of a unit reuse
-          // buffers the softmax finished with before it published this unit's Q.
-          if (!mbar_wait(q_ready, un & 1, abort, a.err)) break;
-          for (int i = 0; i < nt; ++i) {
-            const int gg = g + i, cc = c + i;
-            if (i >= 2 && !mbar_wait(&s_free[gg & 1], ((gg - 2) >> 1) & 1, abort, a.err)) { ok = false; break; }
-            const int sl = (2 * cc) % kKvSlots;
-            if (!mbar_wait(&kv_full[sl], ((2 * cc) / kKvSlots) & 1, abort, a.err)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t b0 = klo + sl * (Cfg::kTile >> 4);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = ((kk >> 2) * Cfg::kChunk + (kk & 3) * 32) >> 4;
-              mma_ts(tmem + Cfg::kS + 128 * (gg & 1), tmem + Cfg::kQt + kk * 8, desc_join(b0 + off, dhi),
-                     idS, kk > 0);
-            }
-            mma_commit(&s_full[gg & 1]);
-            mma_commit(&kv_empty[sl]);
+        if (qn > 0 && !warp_wait(q_free, (qn - 1) & 1, abort, a.err)) break;
+        if (MODE == kModeGroup) {
+          // TMA row gather through perm: lane l fetches tile rows 4l..4l+3 of every
+          // 64-column slab (tm_q is a 2-D {d, B*H*n} view with one-row boxes);
+          // rows past the item repeat its first row, whose scores are all masked
+          if (lane == 0) mbar_expect_tx(q_full, Cfg::kTile);
+          __syncwarp();
+          const int32_t* pp = a.perm + static_cast<size_t>(U.prob) * a.n + U.row0;
+          const int first = pp[0];
+          int rows[4];
+  #pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int rr = 4 * lane + j;
+            rows[j] = U.zq * a.n + (rr < U.nrows ? pp[rr] : first);
           }
-        } else {
-          // O += P(gg) V(gg)
-          for (int i = 0; i < nt; ++i) {
-            const int gg = g + i, cc = c + i;
-            if (!mbar_wait(&p_ready[gg & 1], (gg >> 1) & 1, abort, a.err)) { ok = false; break; }
-            if (i == 0 && un > 0 && !mbar_wait(o_free, (un - 1) & 1, abort, a.err)) { ok = false; break; }
-            const int sl = (2 * cc + 1) % kKvSlots;
-            if (!mbar_wait(&kv_full[sl], ((2 * cc + 1) / kKvSlots) & 1, abort, a.err)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t vb = vlo + sl * (Cfg::kTile >> 4);
-#pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk)
-              mma_ts(tmem + Cfg::kO, tmem + Cfg::kP + kk * 8, desc_join(vb + kk * ((16 * 128) >> 4), dhi),
-                     idPV, i > 0 || kk > 0);
-            mma_commit(o_done);
-            mma_commit(&kv_empty[sl]);
-            if (i == nt - 1) mma_commit(o_final);
+  #pragma unroll
+          for (int ch = 0; ch < kChunks; ++ch)
+            tma_gather4(sQ + ch * Cfg::kChunk + 4 * lane * 128, &tm_q, q_full, ch * 64, rows[0], rows[1],
+                        rows[2], rows[3]);
+        } else if (lane == 0) {
+          mbar_expect_tx(q_full, Cfg::kTile);
+  #pragma unroll
+          for (int ch = 0; ch < kChunks; ++ch)
+            tma_load_3d(sQ + ch * Cfg::kChunk, &tm_q, q_full, ch * 64, U.row0, U.zq);
+        }
+        ++qn;
+        if (lane == 0) {
+          // load L = 2c (K of tile c) and 2c+1 (V of tile c) into slot L % kKvSlots
+          for (int t = U.t0; t <= U.t1 && ok; ++t, ++c) {
+            const int y = U.ybase + t * kBN;
+  #pragma unroll
+            for (int kv = 0; kv < 2; ++kv) {
+              const int L = 2 * c + kv, sl = L % kKvSlots, use = L / kKvSlots;
+              if (use > 0 && !mbar_wait(&kv_empty[sl], (use - 1) & 1, abort, a.err)) { ok = false; break; }
+              mbar_expect_tx(&kv_full[sl], Cfg::kTile);
+  #pragma unroll
+              for (int ch = 0; ch < kChunks; ++ch)
+                tma_load_3d(sKV + sl * Cfg::kTile + ch * Cfg::kChunk, kv ? &tm_v : &tm_k, &kv_full[sl],
+                            ch * 64, y, U.zkv);
+              ++issued;
+            }
+          }
+          if (MODE == kModeLocal && ok) {
+            // the unit's group-partial tile into the O stage, once the previous
+            // unit's O has been stored out of it
+            if (qn > 1 && !mbar_wait(ost_free, (qn - 2) & 1, abort, a.err)) ok = false;
+            if (ok) {
+              mbar_expect_tx(ofar_full, Cfg::kTile);
+  #pragma unroll
+              for (int ch = 0; ch < kChunks; ++ch)
+                tma_load_3d(sO + ch * Cfg::kChunk, &tm_of, ofar_full, ch * 64, U.row0, U.zq);
+            }
           }
         }
-        g += nt;
-        c += nt;
-        ++un;
+        ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort;
+        c = __shfl_sync(0xffffffffu, c, 0);
+      }
+      if (*abort && lane == 0) {
+        // drain: TMA copies already issued must land before the CTA exits
+        for (int L = max(0, issued - kKvSlots); L < issued; ++L) {
+          const unsigned long long t0 = global_ns();
+          while (!mbar_try_wait(&kv_full[L % kKvSlots], (L / kKvSlots) & 1) &&
+                 global_ns() - t0 < kWaitTimeoutNs) {}
+        }
+        if (qn > 0) {
+          const unsigned long long t0 = global_ns();
+          while (!mbar_try_wait(q_full, (qn - 1) & 1) && global_ns() - t0 < kWaitTimeoutNs) {}
+        }
+        if (MODE == kModeLocal && qn > 0) {
+          const unsigned long long t0 = global_ns();
+          while (!mbar_try_wait(ofar_full, (qn - 1) & 1) && global_ns() - t0 < kWaitTimeoutNs) {}
+        }
+      }
+    } else if (warp == kWarpPV || warp == kWarpS) {
+      // ----------------------------------------------------------- MMAs ---
+      // Two issuing threads: one warp issues the S products, the other the PV
+      // products.  The two chains share no TMEM (S buffers and Q vs P and O), so
+      // neither waits on the other's barriers and the tensor pipe sees both.
+      if (lane == 0) {
+        constexpr uint32_t idS = idesc_bf16_f32(128, kBN, false, false);
+        constexpr uint32_t idPV = idesc_bf16_f32(128, D, false, true);
+        constexpr uint32_t dhi = sw128_desc_hi();
+        const uint32_t r0 = smem_u32(sKV);
+        const uint32_t klo = sw128_desc_lo(r0, 16);            // K slots, K-major
+        const uint32_t vlo = sw128_desc_lo(r0, Cfg::kChunk);   // V slots, MN-major
+        int g = 0;        // tiles (S buffers) walked
+        int c = 0;        // K/V tiles walked
+        int un = 0;       // units walked
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+          const int u = snake_unit(k, n_units);
+          if (u == -1) break;
+          if (u < 0) continue;
+          Unit U;
+          decode_unit<MODE>(a, u, U);
+          const int nt = U.t1 - U.t0 + 1;
+          if (warp == kWarpS) {
+            // S(gg) = Q K^T into S buffer gg&1.  The first two tiles of a unit reuse
+            // buffers the softmax finished with before it published this unit's Q.
+            if (!mbar_wait(q_ready, un & 1, abort, a.err)) break;
+            for (int i = 0; i < nt; ++i) {
+              const int gg = g + i, cc = c + i;
+              if (i >= 2 && !mbar_wait(&s_free[gg & 1], ((gg - 2) >> 1) & 1, abort, a.err)) { ok = false; break; }
+              const int sl = (2 * cc) % kKvSlots;
+              if (!mbar_wait(&kv_full[sl], ((2 * cc) / kKvSlots) & 1, abort, a.err)) { ok = false; break; }
+              tc_fence_after();
+              const uint32_t b0 = klo + sl * (Cfg::kTile >> 4);
+  #pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = ((kk >> 2) * Cfg::kChunk + (kk & 3) * 32) >> 4;
+                mma_ts(tmem + Cfg::kS + 128 * (gg & 1), tmem + Cfg::kQt + kk * 8, desc_join(b0 + off, dhi),
+                       idS, kk > 0);
+              }
+              mma_commit(&s_full[gg & 1]);
+              mma_commit(&kv_empty[sl]);
+            }
+          } else {
+            // O += P(gg) V(gg)
+            for (int i = 0; i < nt; ++i) {
+              const int gg = g + i, cc = c + i;
+              if (!mbar_wait(&p_ready[gg & 1], (gg >> 1) & 1, abort, a.err)) { ok = false; break; }
+              if (i == 0 && un > 0 && !mbar_wait(o_free, (un - 1) & 1, abort, a.err)) { ok = false; break; }
+              const int sl = (2 * cc + 1) % kKvSlots;
+              if (!mbar_wait(&kv_full[sl], ((2 * cc + 1) / kKvSlots) & 1, abort, a.err)) { ok = false; break; }
+              tc_fence_after();
+              const uint32_t vb = vlo + sl * (Cfg::kTile >> 4);
+  #pragma unroll
+              for (int kk = 0; kk < kBN / 16; ++kk)
+                mma_ts(tmem + Cfg::kO, tmem + Cfg::kP + kk * 8, desc_join(vb + kk * ((16 * 128) >> 4), dhi),
+                       idPV, i > 0 || kk > 0);
+              mma_commit(o_done);
+              mma_commit(&kv_empty[sl]);
+              if (i == nt - 1) mma_commit(o_final);
+            }
+          }
+          g += nt;
+          c += nt;
+          ++un;
+        }
       }
     }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
     // -------------------------------------------------------- softmax ---
-    const int r = warp * 32 + lane;       // query row within the tile = TMEM lane
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t tO = tmem + lane_base + Cfg::kO;
+    // Two warps per TMEM lane quadrant: warps w and w + 4 read the same 32 rows
+    // and split every row's columns in half.  The halves agree on the row max
+    // through a shared-memory exchange each tile and add their row sums at the
+    // end, so both apply identical scaling to their columns.
+    const int quad = warp & 3, hf = warp >> 2;
+    const int r = quad * 32 + lane;        // query row within the tile = TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    constexpr int kHalfS = kBN / 2;        // S columns per half
+    constexpr int kHalfD = D / 2;          // O columns per half
+    const uint32_t tO = tmem + lane_base + Cfg::kO + hf * kHalfD;
     const float sl2 = a.scale_log2;
     constexpr float kLn2 = 0.6931471805599453f;
     constexpr float kLog2e = 1.4426950408889634f;
-    int g = 0, un = 0;
+    int g = 0, un = 0, xc = 0;
     bool ok = true;
     RowState prev{};
     bool have_prev = false;
 
-    // normalise (and, in the local pass, merge) O of the finished unit
+    // The two warps of a quadrant meet at named barrier 1 + quad.  Once the CTA
+    // is aborting nobody enters it any more, and a warp that leaves the unit
+    // loop early arrives there once on its way out, so a partner already
+    // waiting is released: the barrier never waits for a warp that has gone.
+    auto pair_sync = [&]() -> bool {
+      if (__any_sync(0xffffffffu, *abort != 0)) return false;
+      named_barrier(1 + quad, 64);
+      return true;
+    };
+    // The partner half's value for this row.  Exchange k writes slot k & 1; the
+    // partner reads it before it reaches exchange k + 1, so the slot is free
+    // again by exchange k + 2.
+    auto exchange = [&](float v, float& o) -> bool {
+      float* slot = xch + (xc & 1) * 256;
+      slot[hf * 128 + r] = v;
+      if (!pair_sync()) return false;
+      o = slot[(hf ^ 1) * 128 + r];
+      ++xc;
+      return true;
+    };
+
+    // normalise (and, in the local pass, merge) this half of O of the finished unit
     auto epilogue = [&](const RowState& s, int unit_index) -> bool {
+      float l_other;
+      if (!exchange(s.l, l_other)) return false;
+      const float l = s.l + l_other;
       if (!warp_wait(o_final, unit_index & 1, abort, a.err)) return false;
       tc_fence_after();
       const size_t qrow = static_cast<size_t>(s.zq) * a.n;
-      float c1 = s.l > 0.f ? 1.f / s.l : 0.f, c2 = 0.f;
-      float lse2 = s.m + log2f(s.l);
+      float c1 = l > 0.f ? 1.f / l : 0.f, c2 = 0.f;
+      float lse2 = s.m + log2f(l);
       const bool far = MODE == kModeLocal && s.valid && s.far;
       if (far) {
         const float lf2 = s.lse_far * kLog2e;
         const float mm = fmaxf(lse2, lf2);
         const float e1 = ex2f(lse2 - mm), e2 = ex2f(lf2 - mm);
         const float den = e1 + e2;
-        c1 = e1 / (s.l * den);
+        c1 = e1 / (l * den);
         c2 = e2 / den;
         lse2 = mm + log2f(den);
       }
       if (MODE == kModeGroup) {
         // rows are scattered by perm: stage the tile in shared memory, then
-        // each warp writes two whole 256-byte rows per store instruction
-        const bool write = s.valid && s.l > 0.f;
+        // each warp writes 16 whole rows of its quadrant, 512 bytes per store
+        const bool write = s.valid && l > 0.f;
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = 0; c0 < kHalfD; c0 += 32) {
           uint32_t ou[32];
           tmem_ld32(tO + c0, ou);
           tmem_wait_ld();
-          if (c0 + 32 == D) {
+          if (c0 + 32 == kHalfD) {
             tc_fence_before();
             mbar_arrive(o_free);
           }
 #pragma unroll
           for (int cc = 0; cc < 32; cc += 8) {
-            const int v = (c0 + cc) >> 3;
+            const int v = (hf * kHalfD + c0 + cc) >> 3;
             uint4 o4;
             o4.x = pack_bf16x2(__uint_as_float(ou[cc + 0]) * c1, __uint_as_float(ou[cc + 1]) * c1);
             o4.y = pack_bf16x2(__uint_as_float(ou[cc + 2]) * c1, __uint_as_float(ou[cc + 3]) * c1);
@@ -427,25 +490,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(sO + (v >> 3) * Cfg::kChunk + r * 128 + (((v & 7) ^ (r & 7)) << 4)) = o4;
           }
         }
-        row_tok[r] = write ? s.pos + 1 : 0;
-        if (write) a.lse_far[qrow + s.pos] = lse2 * kLn2;
-        __syncwarp();   // a warp stages and stores only its own 32 rows
+        if (write && hf == 0) a.lse_far[qrow + s.pos] = lse2 * kLn2;
+        const int tok = write ? s.pos + 1 : 0;   // both halves hold the same rows
+        if (!pair_sync()) return false;          // both halves of the rows are staged
         {
           __nv_bfloat16* Of = static_cast<__nv_bfloat16*>(a.O_far);
           constexpr int kVec = D / 8;               // 16-byte pieces per row
           constexpr int kRowsPerStore = 32 / kVec;  // rows one warp store covers
-          constexpr int kIters = 32 / kRowsPerStore;
+          constexpr int kIters = 16 / kRowsPerStore;
           const int v = lane % kVec;
 #pragma unroll 4
           for (int it = 0; it < kIters; ++it) {
-            const int row = warp * 32 + it * kRowsPerStore + lane / kVec;
-            const int tk = row_tok[row];
+            const int j = hf * 16 + it * kRowsPerStore + lane / kVec;   // row within the quadrant
+            const int tk = __shfl_sync(0xffffffffu, tok, j);
+            const int row = quad * 32 + j;
             if (tk > 0)
               *reinterpret_cast<uint4*>(Of + (qrow + tk - 1) * D + v * 8) = *reinterpret_cast<const uint4*>(
                   sO + (v >> 3) * Cfg::kChunk + row * 128 + (((v & 7) ^ (row & 7)) << 4));
           }
         }
-        __syncwarp();   // the warp's rows of the stage may be rewritten
+        // the quadrant's stage rows are rewritten only after the next unit's
+        // tile exchanges, which both warps reach after these stores
         return true;
       }
       // local and dense: the tile goes through the shared-memory stage (same
@@ -453,17 +518,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // in the local pass the stage already holds the group partial of the rows
       if (MODE == kModeLocal && !warp_wait(ofar_full, unit_index & 1, abort, a.err)) return false;
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = 0; c0 < kHalfD; c0 += 32) {
         uint32_t ou[32];
         tmem_ld32(tO + c0, ou);
         tmem_wait_ld();
-        if (c0 + 32 == D) {
+        if (c0 + 32 == kHalfD) {
           tc_fence_before();
           mbar_arrive(o_free);
         }
 #pragma unroll
         for (int cc = 0; cc < 32; cc += 8) {
-          const int v = (c0 + cc) >> 3;
+          const int v = (hf * kHalfD + c0 + cc) >> 3;
           uint4* slot = reinterpret_cast<uint4*>(sO + (v >> 3) * Cfg::kChunk + r * 128 + (((v & 7) ^ (r & 7)) << 4));
           float f[8];
 #pragma unroll
@@ -486,17 +551,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           *slot = o4;
         }
       }
+      // every softmax thread's part is in the stage (and visible to the async
+      // proxy) once ost_full completes; one thread then stores the tile.  The
+      // next unit's arrivals need that thread's P, so a phase is never lapped.
       fence_proxy_async_smem();
-      named_barrier(1, 128);
+      mbar_arrive(ost_full);
+      bool stored = true;
       if (threadIdx.x == 0) {
-        // rows past n fall outside the tensor map and are not written
+        stored = mbar_wait(ost_full, unit_index & 1, abort, a.err);
+        if (stored) {
+          // rows past n fall outside the tensor map and are not written
 #pragma unroll
-        for (int ch = 0; ch < kChunks; ++ch) tma_store_3d(&tm_o, sO + ch * Cfg::kChunk, ch * 64, s.row0, s.zq);
-        tma_store_commit();
-        tma_store_wait_read();
-        if (MODE == kModeLocal) mbar_arrive(ost_free);
+          for (int ch = 0; ch < kChunks; ++ch)
+            tma_store_3d(&tm_o, sO + ch * Cfg::kChunk, ch * 64, s.row0, s.zq);
+          tma_store_commit();
+          tma_store_wait_read();
+          if (MODE == kModeLocal) mbar_arrive(ost_free);
+        }
       }
-      if (s.valid && a.lse) a.lse[qrow + s.pos] = lse2 * kLn2;
+      if (!__all_sync(0xffffffffu, stored)) return false;
+      if (hf == 0 && s.valid && a.lse) a.lse[qrow + s.pos] = lse2 * kLn2;
       return true;
     };
 
@@ -506,24 +580,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (u < 0) continue;
       Unit U;
       decode_unit<MODE>(a, u, U);
-      // 1. this unit's Q row: staged tile -> registers -> TMEM.  The previous
-      //    unit's S products, the only readers of TMEM Q, have all landed.
+      // 1. this half of the unit's Q row: staged tile -> registers -> TMEM.  The
+      //    previous unit's S products, the only readers of TMEM Q, have all landed.
       if (!warp_wait(q_full, un & 1, abort, a.err)) { ok = false; break; }
       {
-        uint32_t qu[D / 2];
+        uint32_t qu[kHalfD / 2];
 #pragma unroll
-        for (int v = 0; v < D / 8; ++v) {
+        for (int i = 0; i < kHalfD / 8; ++i) {
+          const int v = hf * (kHalfD / 8) + i;
           const uint4 q4 = *reinterpret_cast<const uint4*>(sQ + (v >> 3) * Cfg::kChunk + r * 128 +
                                                           (((v & 7) ^ (r & 7)) << 4));
-          qu[4 * v + 0] = q4.x;
-          qu[4 * v + 1] = q4.y;
-          qu[4 * v + 2] = q4.z;
-          qu[4 * v + 3] = q4.w;
+          qu[4 * i + 0] = q4.x;
+          qu[4 * i + 1] = q4.y;
+          qu[4 * i + 2] = q4.z;
+          qu[4 * i + 3] = q4.w;
         }
         mbar_arrive(q_free);
-#pragma unroll
-        for (int cc = 0; cc < D / 2; cc += 32)
-          tmem_st32(tmem + lane_base + Cfg::kQt + cc, *reinterpret_cast<uint32_t(*)[32]>(&qu[cc]));
+        const uint32_t tq = tmem + lane_base + Cfg::kQt + hf * (kHalfD / 2);
+        if constexpr (kHalfD / 2 == 32) tmem_st32(tq, qu);
+        else tmem_st16(tq, qu);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(q_ready);
@@ -560,8 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const size_t qi = static_cast<size_t>(U.zq) * a.n + st.pos;
             st.lse_far = a.lse_far[qi];
             const char* row = reinterpret_cast<const char*>(static_cast<const __nv_bfloat16*>(a.O_far) + qi * D);
-#pragma unroll
-            for (int b = 0; b < D * 2; b += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + b));
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(row + hf * D));
           }
         }
       }
@@ -569,34 +643,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nt = U.t1 - U.t0 + 1;
       for (int i = 0; i < nt; ++i) {
         const int gg = g + i;
-        const int j0 = (U.t0 + i) * kBN;
-        const uint32_t tS = tmem + lane_base + Cfg::kS + 128 * (gg & 1);
+        const int j0 = (U.t0 + i) * kBN + hf * kHalfS;    // first key of this half
+        const uint32_t tS = tmem + lane_base + Cfg::kS + 128 * (gg & 1) + hf * kHalfS;
         if (!warp_wait(&s_full[gg & 1], (gg >> 1) & 1, abort, a.err)) { ok = false; break; }
         tc_fence_after();
-        // S row: four 32-column loads in flight, one wait
-        uint32_t su[kBN];
-#pragma unroll
-        for (int cc = 0; cc < kBN; cc += 32)
-          tmem_ld32(tS + cc, *reinterpret_cast<uint32_t(*)[32]>(&su[cc]));
+        // this half of the S row: two 32-column loads in flight, one wait
+        uint32_t su[kHalfS];
+        tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&su[0]));
+        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&su[32]));
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&s_free[gg & 1]);     // S(gg+2) may now overwrite this buffer
-        const bool full = j0 >= lo && j0 + kBN - 1 <= hi;
+        const bool full = j0 >= lo && j0 + kHalfS - 1 <= hi;
         if (!full) {
 #pragma unroll
-          for (int cc = 0; cc < kBN; ++cc)
+          for (int cc = 0; cc < kHalfS; ++cc)
             if (j0 + cc < lo || j0 + cc > hi) su[cc] = __float_as_uint(-INFINITY);
         }
-        // row max: eight independent chains, then a tree
+        // half-row max: eight independent chains, a tree, then the partner's half
         float m8[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) m8[j] = __uint_as_float(su[j]);
 #pragma unroll
-        for (int cc = 8; cc < kBN; cc += 8)
+        for (int cc = 8; cc < kHalfS; cc += 8)
 #pragma unroll
           for (int j = 0; j < 8; ++j) m8[j] = fmaxf(m8[j], __uint_as_float(su[cc + j]));
-        const float mt = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+        const float mh = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                                fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        float mo;
+        if (!exchange(mh, mo)) { ok = false; break; }
+        const float mt = fmaxf(mh, mo);
         const float m_new = fmaxf(m_run, mt * sl2);
         const bool need = m_run != -INFINITY && m_new > m_run + kRescaleThreshold;
         if (m_run == -INFINITY) m_run = m_new;      // nothing accumulated yet for this row
@@ -610,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float alpha = need ? ex2f(m_run - m_new) : 1.f;
           uint32_t rr[32];
 #pragma unroll
-          for (int cc = 0; cc < D; cc += 32) {
+          for (int cc = 0; cc < kHalfD; cc += 32) {
             tmem_ld32(tO + cc, rr);
             tmem_wait_ld();
 #pragma unroll
@@ -625,26 +701,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mu = m_run == -INFINITY ? 0.f : m_run;
         // p = 2^(s*scale*log2e - m): scale-and-shift in packed pairs, exp2 per
         // element, four packed partial sums; P is written as bf16 pairs into
-        // the P buffer once PV(gg-1) has finished reading it
+        // this half of the P buffer once PV(gg-1) has finished reading it
         const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(-mu, -mu);
         uint64_t acc[4] = {0, 0, 0, 0};
-        uint32_t pk[64];
+        uint32_t pk[kHalfS / 2];
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-#pragma unroll
-          for (int cc = 0; cc < 64; cc += 2) {
-            const int col = 64 * h2 + cc;
-            float t0, t1;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(su[col]), __uint_as_float(su[col + 1])), sc2, nm2), t0, t1);
-            const float p0 = ex2f(t0), p1 = ex2f(t1);
-            acc[(cc >> 1) & 3] = f2_add(acc[(cc >> 1) & 3], f2_pack(p0, p1));
-            pk[32 * h2 + cc / 2] = pack_bf16x2(p0, p1);
-          }
+        for (int cc = 0; cc < kHalfS; cc += 2) {
+          float t0, t1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(su[cc]), __uint_as_float(su[cc + 1])), sc2, nm2), t0, t1);
+          const float p0 = ex2f(t0), p1 = ex2f(t1);
+          acc[(cc >> 1) & 3] = f2_add(acc[(cc >> 1) & 3], f2_pack(p0, p1));
+          pk[cc / 2] = pack_bf16x2(p0, p1);
         }
         if (pv_prev && !warp_wait(o_done, (gg - 1) & 1, abort, a.err)) { ok = false; break; }
         tc_fence_after();
-        tmem_st32(tmem + lane_base + Cfg::kP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-        tmem_st32(tmem + lane_base + Cfg::kP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        tmem_st32(tmem + lane_base + Cfg::kP + hf * (kHalfS / 2), pk);
         {
           const uint64_t s2 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
           float s0, s1;
@@ -663,13 +734,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       have_prev = true;
       ++un;
     }
-    if (ok && have_prev) epilogue(prev, un - 1);
+    if (ok && have_prev) ok = epilogue(prev, un - 1);
+    if (!ok) named_barrier_arrive(1 + quad, 64);   // release a partner waiting at the pair barrier
   }
 
-  __syncwarp();          // lanes of warps 4-6 reconverge before the CTA barrier
+  __syncwarp();          // lanes of the load and MMA warps reconverge before the CTA barrier
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kWarpPV) {
     tc_fence_after();
     tmem_dealloc(tmem, Cfg::kTmemCols);
   }

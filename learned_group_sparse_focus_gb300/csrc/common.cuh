@@ -120,6 +120,11 @@ __device__ __forceinline__ void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Count this warp in at a named barrier without waiting for it.
+__device__ __forceinline__ void named_barrier_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Row gather: four rows (r0..r3) of `box_cols` elements each from a 2-D tensor
 // map whose box is one row high; they land one after another at smem_dst.
 __device__ __forceinline__ void tma_gather4(void* smem_dst, const void* tmap, uint64_t* bar, int col,
