@@ -38,13 +38,14 @@
 //               dense passes it builds the O tile in shared memory (merged with
 //               the group partial the load warp staged there) and writes it
 //               with one TMA store
-//   warp 8      loads: Q tile into shared memory (TMA, or a TMA row gather
-//               through perm in group mode), K/V tiles (TMA, 5-slot ring) and,
-//               in the local pass, the unit's group-partial O tile
+//   warp 8      Q and K tiles into one 4-slot ring, in the order the S
+//               products use them (TMA; a TMA row gather through perm for the
+//               group pass's Q)
 //   warp 9      TMEM owner; issues O += P(t) V(t) once P(t) is written
 //   warp 10     issues S(t) = Q K(t)^T once the softmax has read S(t-2),
 //               the previous content of the same buffer
-//   warp 11     idle (completes warpgroup 2 for the register split)
+//   warp 11     V tiles into a 2-slot ring and, in the local pass, the unit's
+//               group-partial O tile into the O stage
 // Every wait is bounded; on timeout the CTA raises an error bit, drains its
 // copies, frees TMEM and exits.
 #include "common.cuh"
@@ -61,7 +62,8 @@ constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
 constexpr int kWarpLoad = kSoftmaxWarps;     // TMA loads
 constexpr int kWarpPV = kSoftmaxWarps + 1;   // TMEM owner, O += P V issuer
 constexpr int kWarpS = kSoftmaxWarps + 2;    // S = Q K^T issuer
-constexpr int kThreads = 32 * (kSoftmaxWarps + 4);   // warp 11 idles (whole warpgroups)
+constexpr int kWarpLoadV = kSoftmaxWarps + 3;  // V tiles (and the group partial)
+constexpr int kThreads = 32 * (kSoftmaxWarps + 4);
 // Register split (setmaxnreg).  The kernel launches at 168 registers per thread
 // (384 x 168 = 64512, the cap for 12 warps).  Warpgroup 2 gives registers back
 // down to 88 and the two softmax warpgroups take them up to 208:
@@ -69,17 +71,21 @@ constexpr int kThreads = 32 * (kSoftmaxWarps + 4);   // warp 11 idles (whole war
 // 208 + 208 + 88 = 504 registers per lane (<= 512).
 constexpr int kRegsLow = 88;
 constexpr int kRegsHigh = 208;
-// K and V tiles share one ring of slots, K(t) then V(t): the loader runs about
-// two and a half tiles ahead of the MMAs.
-constexpr int kKvSlots = 5;
+// Two rings of tile slots.  Q and K tiles share one, in the order the S issuer
+// consumes them (a unit's Q, then its K tiles): a K slot is free once its S
+// product is done, early in the tile's life.  V tiles have their own ring,
+// whose slots stay busy until O += P V, late in the tile's life, so a slow V
+// never holds up the next K.
+constexpr int kQkSlots = 4;
+constexpr int kVSlots = 2;
 
 template <int D>
 struct AttnCfg {
   static constexpr int kChunk = 128 * 128;   // 64 columns x 128 rows, one swizzle slab
   static constexpr int kTile = 128 * D * 2;  // one 128-row Q/K/V tile
-  static constexpr int kQ = 0;               // staged Q tile
-  static constexpr int kRing = kQ + kTile;   // K/V slots
-  static constexpr int kOst = kRing + kKvSlots * kTile;   // O tile staging
+  static constexpr int kQK = 0;                           // Q/K ring
+  static constexpr int kV = kQK + kQkSlots * kTile;       // V ring
+  static constexpr int kOst = kV + kVSlots * kTile;       // O tile staging
   static constexpr int kBar = kOst + kTile;                 // barriers (< 256 B)
   static constexpr int kXch = kBar + 256;                   // row max / sum exchange: [2][2][128] fp32
   static constexpr int kSmem = kXch + 2 * 2 * 128 * 4;
@@ -190,33 +196,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   uint8_t* smem = smem_raw;
-  uint8_t* sQ = smem + Cfg::kQ;
-  uint8_t* sKV = smem + Cfg::kRing;
+  uint8_t* sQK = smem + Cfg::kQK;
+  uint8_t* sV = smem + Cfg::kV;
   uint8_t* sO = smem + Cfg::kOst;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBar);
-  uint64_t* q_full = bars + 0;        // staged Q tile landed in shared memory
-  uint64_t* q_free = bars + 1;        // staged Q copied out (softmax threads)
-  uint64_t* q_ready = bars + 2;       // Q in TMEM (softmax threads)
-  uint64_t* o_done = bars + 3;        // one phase per PV product
-  uint64_t* o_final = bars + 4;       // one phase per unit: its last PV landed
-  uint64_t* o_free = bars + 5;        // one phase per unit: O read out (softmax threads)
-  uint64_t* s_full = bars + 6;        // [2] per S buffer
-  uint64_t* p_ready = bars + 8;       // [2] per S buffer (softmax threads)
-  uint64_t* s_free = bars + 10;       // [2] per S buffer: the softmax has read it
-  uint64_t* ofar_full = bars + 12;    // local: the unit's group-partial tile is staged
-  uint64_t* ost_free = bars + 13;     // local: the O stage was stored out (1 arrival)
-  uint64_t* kv_full = bars + 14;      // [kKvSlots]
-  uint64_t* kv_empty = bars + 14 + kKvSlots;
-  uint64_t* ost_full = bars + 14 + 2 * kKvSlots;   // local/dense: the O stage is written (softmax threads)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15 + 2 * kKvSlots);
+  uint64_t* q_ready = bars + 0;       // Q in TMEM (softmax threads)
+  uint64_t* o_done = bars + 1;        // one phase per PV product
+  uint64_t* o_final = bars + 2;       // one phase per unit: its last PV landed
+  uint64_t* o_free = bars + 3;        // one phase per unit: O read out (softmax threads)
+  uint64_t* s_full = bars + 4;        // [2] per S buffer
+  uint64_t* p_ready = bars + 6;       // [2] per S buffer (softmax threads)
+  uint64_t* s_free = bars + 8;        // [2] per S buffer: the softmax has read it
+  uint64_t* ofar_full = bars + 10;    // local: the unit's group-partial tile is staged
+  uint64_t* ost_free = bars + 11;     // local: the O stage was stored out (1 arrival)
+  uint64_t* ost_full = bars + 12;     // local/dense: the O stage is written (softmax threads)
+  uint64_t* qk_full = bars + 13;      // [kQkSlots]
+  uint64_t* qk_empty = bars + 13 + kQkSlots;
+  uint64_t* v_full = bars + 13 + 2 * kQkSlots;              // [kVSlots]
+  uint64_t* v_empty = bars + 13 + 2 * kQkSlots + kVSlots;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13 + 2 * kQkSlots + 2 * kVSlots);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* xch = reinterpret_cast<float*>(smem + Cfg::kXch);
 
   const int warp = warp_id(), lane = lane_id();
   const int n_units = unit_count<MODE>(a);
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_free, kSoftmaxThreads);
     mbar_init(q_ready, kSoftmaxThreads);
     mbar_init(o_done, 1);
     mbar_init(o_final, 1);
@@ -229,9 +233,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&p_ready[x], kSoftmaxThreads);
       mbar_init(&s_free[x], kSoftmaxThreads);
     }
-    for (int k = 0; k < kKvSlots; ++k) {
-      mbar_init(&kv_full[k], 1);
-      mbar_init(&kv_empty[k], 1);
+    for (int k = 0; k < kQkSlots; ++k) {
+      mbar_init(&qk_full[k], 1);
+      mbar_init(&qk_empty[k], 1);
+    }
+    for (int k = 0; k < kVSlots; ++k) {
+      mbar_init(&v_full[k], 1);
+      mbar_init(&v_empty[k], 1);
     }
     *abort = 0;
     fence_mbar_init();
@@ -247,93 +255,120 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp >= kSoftmaxWarps) {
-    // warpgroup 2 (loads, the two MMA issuers, one idle warp) hands registers
+    // warpgroup 2 (the two load warps and the two MMA issuers) hands registers
     // to the softmax warpgroups
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
     if (warp == kWarpLoad) {
-      // ---------------------------------------------------------- loads ---
-      int c = 0;                 // K/V tiles walked
-      int issued = 0;            // K/V loads issued (lane 0)
-      int qn = 0;                // Q tiles staged
+      // -------------------------------------------------- Q and K loads ---
+      int cq = 0;                // Q/K ring entries issued
       bool ok = true;
-      const __nv_bfloat16* Qg = static_cast<const __nv_bfloat16*>(a.Q);
       for (int k = 0; ok; ++k) {
         const int u = snake_unit(k, n_units);
         if (u == -1) break;
         if (u < 0) continue;
         Unit U;
         decode_unit<MODE>(a, u, U);
-        if (qn > 0 && !warp_wait(q_free, (qn - 1) & 1, abort, a.err)) break;
-        if (MODE == kModeGroup) {
-          // TMA row gather through perm: lane l fetches tile rows 4l..4l+3 of every
-          // 64-column slab (tm_q is a 2-D {d, B*H*n} view with one-row boxes);
-          // rows past the item repeat its first row, whose scores are all masked
-          if (lane == 0) mbar_expect_tx(q_full, Cfg::kTile);
-          __syncwarp();
-          const int32_t* pp = a.perm + static_cast<size_t>(U.prob) * a.n + U.row0;
-          const int first = pp[0];
-          int rows[4];
-  #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int rr = 4 * lane + j;
-            rows[j] = U.zq * a.n + (rr < U.nrows ? pp[rr] : first);
-          }
-  #pragma unroll
-          for (int ch = 0; ch < kChunks; ++ch)
-            tma_gather4(sQ + ch * Cfg::kChunk + 4 * lane * 128, &tm_q, q_full, ch * 64, rows[0], rows[1],
-                        rows[2], rows[3]);
-        } else if (lane == 0) {
-          mbar_expect_tx(q_full, Cfg::kTile);
-  #pragma unroll
-          for (int ch = 0; ch < kChunks; ++ch)
-            tma_load_3d(sQ + ch * Cfg::kChunk, &tm_q, q_full, ch * 64, U.row0, U.zq);
-        }
-        ++qn;
-        if (lane == 0) {
-          // load L = 2c (K of tile c) and 2c+1 (V of tile c) into slot L % kKvSlots
-          for (int t = U.t0; t <= U.t1 && ok; ++t, ++c) {
-            const int y = U.ybase + t * kBN;
-  #pragma unroll
-            for (int kv = 0; kv < 2; ++kv) {
-              const int L = 2 * c + kv, sl = L % kKvSlots, use = L / kKvSlots;
-              if (use > 0 && !mbar_wait(&kv_empty[sl], (use - 1) & 1, abort, a.err)) { ok = false; break; }
-              mbar_expect_tx(&kv_full[sl], Cfg::kTile);
-  #pragma unroll
-              for (int ch = 0; ch < kChunks; ++ch)
-                tma_load_3d(sKV + sl * Cfg::kTile + ch * Cfg::kChunk, kv ? &tm_v : &tm_k, &kv_full[sl],
-                            ch * 64, y, U.zkv);
-              ++issued;
+        {
+          // the unit's Q tile
+          const int sl = cq % kQkSlots, use = cq / kQkSlots;
+          if (use > 0 && !warp_wait(&qk_empty[sl], (use - 1) & 1, abort, a.err)) break;
+          uint8_t* dst = sQK + sl * Cfg::kTile;
+          if (MODE == kModeGroup) {
+            // TMA row gather through perm: lane l fetches tile rows 4l..4l+3 of every
+            // 64-column slab (tm_q is a 2-D {d, B*H*n} view with one-row boxes);
+            // rows past the item repeat its first row, whose scores are all masked
+            if (lane == 0) mbar_expect_tx(&qk_full[sl], Cfg::kTile);
+            __syncwarp();
+            const int32_t* pp = a.perm + static_cast<size_t>(U.prob) * a.n + U.row0;
+            const int first = pp[0];
+            int rows[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int rr = 4 * lane + j;
+              rows[j] = U.zq * a.n + (rr < U.nrows ? pp[rr] : first);
             }
+#pragma unroll
+            for (int ch = 0; ch < kChunks; ++ch)
+              tma_gather4(dst + ch * Cfg::kChunk + 4 * lane * 128, &tm_q, &qk_full[sl], ch * 64, rows[0],
+                          rows[1], rows[2], rows[3]);
+          } else if (lane == 0) {
+            mbar_expect_tx(&qk_full[sl], Cfg::kTile);
+#pragma unroll
+            for (int ch = 0; ch < kChunks; ++ch)
+              tma_load_3d(dst + ch * Cfg::kChunk, &tm_q, &qk_full[sl], ch * 64, U.row0, U.zq);
+          }
+          ++cq;
+        }
+        if (lane == 0) {
+          for (int t = U.t0; t <= U.t1; ++t, ++cq) {
+            const int sl = cq % kQkSlots, use = cq / kQkSlots;
+            if (use > 0 && !mbar_wait(&qk_empty[sl], (use - 1) & 1, abort, a.err)) { ok = false; break; }
+            mbar_expect_tx(&qk_full[sl], Cfg::kTile);
+#pragma unroll
+            for (int ch = 0; ch < kChunks; ++ch)
+              tma_load_3d(sQK + sl * Cfg::kTile + ch * Cfg::kChunk, &tm_k, &qk_full[sl], ch * 64,
+                          U.ybase + t * kBN, U.zkv);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort;
+        cq = __shfl_sync(0xffffffffu, cq, 0);
+      }
+      if (*abort && lane == 0) {
+        // drain: TMA copies already issued must land before the CTA exits
+        for (int L = max(0, cq - kQkSlots); L < cq; ++L) {
+          const unsigned long long t0 = global_ns();
+          while (!mbar_try_wait(&qk_full[L % kQkSlots], (L / kQkSlots) & 1) &&
+                 global_ns() - t0 < kWaitTimeoutNs) {}
+        }
+      }
+    } else if (warp == kWarpLoadV) {
+      // ------------------------------------------- V loads, group partial ---
+      if (lane == 0) {
+        int cv = 0;              // V ring entries issued
+        int un = 0;              // units walked
+        int ofn = 0;             // group-partial tiles issued
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+          const int u = snake_unit(k, n_units);
+          if (u == -1) break;
+          if (u < 0) continue;
+          Unit U;
+          decode_unit<MODE>(a, u, U);
+          for (int t = U.t0; t <= U.t1; ++t, ++cv) {
+            const int sl = cv % kVSlots, use = cv / kVSlots;
+            if (use > 0 && !mbar_wait(&v_empty[sl], (use - 1) & 1, abort, a.err)) { ok = false; break; }
+            mbar_expect_tx(&v_full[sl], Cfg::kTile);
+#pragma unroll
+            for (int ch = 0; ch < kChunks; ++ch)
+              tma_load_3d(sV + sl * Cfg::kTile + ch * Cfg::kChunk, &tm_v, &v_full[sl], ch * 64,
+                          U.ybase + t * kBN, U.zkv);
           }
           if (MODE == kModeLocal && ok) {
             // the unit's group-partial tile into the O stage, once the previous
             // unit's O has been stored out of it
-            if (qn > 1 && !mbar_wait(ost_free, (qn - 2) & 1, abort, a.err)) ok = false;
+            if (un > 0 && !mbar_wait(ost_free, (un - 1) & 1, abort, a.err)) ok = false;
             if (ok) {
               mbar_expect_tx(ofar_full, Cfg::kTile);
-  #pragma unroll
+#pragma unroll
               for (int ch = 0; ch < kChunks; ++ch)
                 tma_load_3d(sO + ch * Cfg::kChunk, &tm_of, ofar_full, ch * 64, U.row0, U.zq);
+              ++ofn;
             }
           }
+          ++un;
+          ok = ok && !*abort;
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort;
-        c = __shfl_sync(0xffffffffu, c, 0);
-      }
-      if (*abort && lane == 0) {
-        // drain: TMA copies already issued must land before the CTA exits
-        for (int L = max(0, issued - kKvSlots); L < issued; ++L) {
-          const unsigned long long t0 = global_ns();
-          while (!mbar_try_wait(&kv_full[L % kKvSlots], (L / kKvSlots) & 1) &&
-                 global_ns() - t0 < kWaitTimeoutNs) {}
-        }
-        if (qn > 0) {
-          const unsigned long long t0 = global_ns();
-          while (!mbar_try_wait(q_full, (qn - 1) & 1) && global_ns() - t0 < kWaitTimeoutNs) {}
-        }
-        if (MODE == kModeLocal && qn > 0) {
-          const unsigned long long t0 = global_ns();
-          while (!mbar_try_wait(ofar_full, (qn - 1) & 1) && global_ns() - t0 < kWaitTimeoutNs) {}
+        if (*abort) {
+          // drain: TMA copies already issued must land before the CTA exits
+          for (int L = max(0, cv - kVSlots); L < cv; ++L) {
+            const unsigned long long t0 = global_ns();
+            while (!mbar_try_wait(&v_full[L % kVSlots], (L / kVSlots) & 1) &&
+                   global_ns() - t0 < kWaitTimeoutNs) {}
+          }
+          if (ofn > 0) {
+            const unsigned long long t0 = global_ns();
+            while (!mbar_try_wait(ofar_full, (ofn - 1) & 1) && global_ns() - t0 < kWaitTimeoutNs) {}
+          }
         }
       }
     } else if (warp == kWarpPV || warp == kWarpS) {
@@ -345,11 +380,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t idS = idesc_bf16_f32(128, kBN, false, false);
         constexpr uint32_t idPV = idesc_bf16_f32(128, D, false, true);
         constexpr uint32_t dhi = sw128_desc_hi();
-        const uint32_t r0 = smem_u32(sKV);
-        const uint32_t klo = sw128_desc_lo(r0, 16);            // K slots, K-major
-        const uint32_t vlo = sw128_desc_lo(r0, Cfg::kChunk);   // V slots, MN-major
+        const uint32_t klo = sw128_desc_lo(smem_u32(sQK), 16);          // K slots, K-major
+        const uint32_t vlo = sw128_desc_lo(smem_u32(sV), Cfg::kChunk);  // V slots, MN-major
         int g = 0;        // tiles (S buffers) walked
-        int c = 0;        // K/V tiles walked
+        int cq = 0;       // Q/K ring entries walked
+        int cv = 0;       // V ring entries walked
         int un = 0;       // units walked
         bool ok = true;
         for (int k = 0; ok; ++k) {
@@ -360,46 +395,50 @@ __global__ void __launch_bounds__(kThreads, 1)
           decode_unit<MODE>(a, u, U);
           const int nt = U.t1 - U.t0 + 1;
           if (warp == kWarpS) {
+            // the unit's Q entry: the softmax copies it into TMEM; once it has,
+            // the slot goes back to the loader
+            const int qsl = cq % kQkSlots;
+            ++cq;
+            if (!mbar_wait(q_ready, un & 1, abort, a.err)) break;
+            mbar_arrive(&qk_empty[qsl]);
             // S(gg) = Q K^T into S buffer gg&1.  The first two tiles of a unit reuse
             // buffers the softmax finished with before it published this unit's Q.
-            if (!mbar_wait(q_ready, un & 1, abort, a.err)) break;
-            for (int i = 0; i < nt; ++i) {
-              const int gg = g + i, cc = c + i;
+            for (int i = 0; i < nt; ++i, ++cq) {
+              const int gg = g + i;
               if (i >= 2 && !mbar_wait(&s_free[gg & 1], ((gg - 2) >> 1) & 1, abort, a.err)) { ok = false; break; }
-              const int sl = (2 * cc) % kKvSlots;
-              if (!mbar_wait(&kv_full[sl], ((2 * cc) / kKvSlots) & 1, abort, a.err)) { ok = false; break; }
+              const int sl = cq % kQkSlots;
+              if (!mbar_wait(&qk_full[sl], (cq / kQkSlots) & 1, abort, a.err)) { ok = false; break; }
               tc_fence_after();
               const uint32_t b0 = klo + sl * (Cfg::kTile >> 4);
-  #pragma unroll
+#pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = ((kk >> 2) * Cfg::kChunk + (kk & 3) * 32) >> 4;
                 mma_ts(tmem + Cfg::kS + 128 * (gg & 1), tmem + Cfg::kQt + kk * 8, desc_join(b0 + off, dhi),
                        idS, kk > 0);
               }
               mma_commit(&s_full[gg & 1]);
-              mma_commit(&kv_empty[sl]);
+              mma_commit(&qk_empty[sl]);
             }
           } else {
             // O += P(gg) V(gg)
-            for (int i = 0; i < nt; ++i) {
-              const int gg = g + i, cc = c + i;
+            for (int i = 0; i < nt; ++i, ++cv) {
+              const int gg = g + i;
               if (!mbar_wait(&p_ready[gg & 1], (gg >> 1) & 1, abort, a.err)) { ok = false; break; }
               if (i == 0 && un > 0 && !mbar_wait(o_free, (un - 1) & 1, abort, a.err)) { ok = false; break; }
-              const int sl = (2 * cc + 1) % kKvSlots;
-              if (!mbar_wait(&kv_full[sl], ((2 * cc + 1) / kKvSlots) & 1, abort, a.err)) { ok = false; break; }
+              const int sl = cv % kVSlots;
+              if (!mbar_wait(&v_full[sl], (cv / kVSlots) & 1, abort, a.err)) { ok = false; break; }
               tc_fence_after();
               const uint32_t vb = vlo + sl * (Cfg::kTile >> 4);
-  #pragma unroll
+#pragma unroll
               for (int kk = 0; kk < kBN / 16; ++kk)
                 mma_ts(tmem + Cfg::kO, tmem + Cfg::kP + kk * 8, desc_join(vb + kk * ((16 * 128) >> 4), dhi),
                        idPV, i > 0 || kk > 0);
               mma_commit(o_done);
-              mma_commit(&kv_empty[sl]);
+              mma_commit(&v_empty[sl]);
               if (i == nt - 1) mma_commit(o_final);
             }
           }
           g += nt;
-          c += nt;
           ++un;
         }
       }
@@ -582,8 +621,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       decode_unit<MODE>(a, u, U);
       // 1. this half of the unit's Q row: staged tile -> registers -> TMEM.  The
       //    previous unit's S products, the only readers of TMEM Q, have all landed.
-      if (!warp_wait(q_full, un & 1, abort, a.err)) { ok = false; break; }
+      // the unit's Q sits in the Q/K ring after un earlier Q tiles and g K tiles
+      const int qe = un + g;
+      if (!warp_wait(&qk_full[qe % kQkSlots], (qe / kQkSlots) & 1, abort, a.err)) { ok = false; break; }
       {
+        const uint8_t* sQ = sQK + (qe % kQkSlots) * Cfg::kTile;
         uint32_t qu[kHalfD / 2];
 #pragma unroll
         for (int i = 0; i < kHalfD / 8; ++i) {
@@ -595,7 +637,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           qu[4 * i + 2] = q4.z;
           qu[4 * i + 3] = q4.w;
         }
-        mbar_arrive(q_free);
         const uint32_t tq = tmem + lane_base + Cfg::kQt + hf * (kHalfD / 2);
         if constexpr (kHalfD / 2 == 32) tmem_st32(tq, qu);
         else tmem_st16(tq, qu);
