@@ -38,13 +38,13 @@
 //               dense passes it builds the O tile in shared memory (merged with
 //               the group partial the load warp staged there) and writes it
 //               with one TMA store
-//   warp 8      Q and K tiles into one 4-slot ring, in the order the S
+//   warp 8      Q and K tiles into one 3-slot ring, in the order the S
 //               products use them (TMA; a TMA row gather through perm for the
 //               group pass's Q)
 //   warp 9      TMEM owner; issues O += P(t) V(t) once P(t) is written
 //   warp 10     issues S(t) = Q K(t)^T once the softmax has read S(t-2),
 //               the previous content of the same buffer
-//   warp 11     V tiles into a 2-slot ring and, in the local pass, the unit's
+//   warp 11     V tiles into a 3-slot ring and, in the local pass, the unit's
 //               group-partial O tile into the O stage
 // Every wait is bounded; on timeout the CTA raises an error bit, drains its
 // copies, frees TMEM and exits.
@@ -71,28 +71,29 @@ constexpr int kThreads = 32 * (kSoftmaxWarps + 4);
 // 208 + 208 + 88 = 504 registers per lane (<= 512).
 constexpr int kRegsLow = 88;
 constexpr int kRegsHigh = 208;
-// Two rings of tile slots.  Q and K tiles share one, in the order the S issuer
-// consumes them (a unit's Q, then its K tiles): a K slot is free once its S
-// product is done, early in the tile's life.  V tiles have their own ring,
-// whose slots stay busy until O += P V, late in the tile's life, so a slow V
-// never holds up the next K.
-constexpr int kQkSlots = 4;
+// Three rings of tile slots.  Q tiles (one per unit, read by every S product
+// of the unit) get two slots, so the next unit's Q lands while this unit runs.
+// K slots are free once their S product is done, early in a tile's life; V
+// slots only once O += P V is, late in it.  Separate rings keep a slow V from
+// holding up the next K.
+constexpr int kQSlots = 2;
+constexpr int kKSlots = 2;
 constexpr int kVSlots = 2;
 
 template <int D>
 struct AttnCfg {
   static constexpr int kChunk = 128 * 128;   // 64 columns x 128 rows, one swizzle slab
   static constexpr int kTile = 128 * D * 2;  // one 128-row Q/K/V tile
-  static constexpr int kQK = 0;                           // Q/K ring
-  static constexpr int kV = kQK + kQkSlots * kTile;       // V ring
+  static constexpr int kQ = 0;                            // Q ring
+  static constexpr int kK = kQ + kQSlots * kTile;         // K ring
+  static constexpr int kV = kK + kKSlots * kTile;         // V ring
   static constexpr int kOst = kV + kVSlots * kTile;       // O tile staging
   static constexpr int kBar = kOst + kTile;                 // barriers (< 256 B)
   static constexpr int kXch = kBar + 256;                   // row max / sum exchange: [2][2][128] fp32
   static constexpr int kSmem = kXch + 2 * 2 * 128 * 4;
   static constexpr uint32_t kS = 0;          // two S buffers of 128 columns
   static constexpr uint32_t kO = 256;        // O: d columns
-  static constexpr uint32_t kQt = 384;       // Q: d/2 columns of bf16 pairs
-  static constexpr uint32_t kP = 384 + D / 2;  // P: 64 columns of bf16 pairs
+  static constexpr uint32_t kP = 384;        // P double buffer: 2 x 64 columns of bf16 pairs
   static constexpr uint32_t kTmemCols = 512;
 };
 
@@ -100,6 +101,21 @@ __device__ __forceinline__ float ex2f(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// One arrival per warp: the lanes' earlier work (TMEM reads and writes, shared
+// memory stores, each already fenced by its own lane) is ordered before lane
+// 0's arrival by the warp barrier.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+}
+
+// warp-uniform bounded wait for a load warp (sleeping between probes)
+__device__ __forceinline__ bool warp_wait_nap(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                              int* err) {
+  const bool ok = mbar_wait_nap(bar, parity, abort, err);
+  return __all_sync(0xffffffffu, ok);
 }
 
 // warp-uniform bounded wait (every lane waits; the verdict is shared)
@@ -196,46 +212,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   uint8_t* smem = smem_raw;
-  uint8_t* sQK = smem + Cfg::kQK;
+  uint8_t* sQ = smem + Cfg::kQ;
+  uint8_t* sK = smem + Cfg::kK;
   uint8_t* sV = smem + Cfg::kV;
   uint8_t* sO = smem + Cfg::kOst;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBar);
-  uint64_t* q_ready = bars + 0;       // Q in TMEM (softmax threads)
-  uint64_t* o_done = bars + 1;        // one phase per PV product
+  uint64_t* pv_done = bars + 0;       // [2] per P buffer: O += P V of that buffer done
   uint64_t* o_final = bars + 2;       // one phase per unit: its last PV landed
-  uint64_t* o_free = bars + 3;        // one phase per unit: O read out (softmax threads)
+  uint64_t* o_free = bars + 3;        // one phase per unit: O read out (softmax warps)
   uint64_t* s_full = bars + 4;        // [2] per S buffer
-  uint64_t* p_ready = bars + 6;       // [2] per S buffer (softmax threads)
+  uint64_t* p_ready = bars + 6;       // [2] per S buffer (softmax warps)
   uint64_t* s_free = bars + 8;        // [2] per S buffer: the softmax has read it
   uint64_t* ofar_full = bars + 10;    // local: the unit's group-partial tile is staged
   uint64_t* ost_free = bars + 11;     // local: the O stage was stored out (1 arrival)
-  uint64_t* ost_full = bars + 12;     // local/dense: the O stage is written (softmax threads)
-  uint64_t* qk_full = bars + 13;      // [kQkSlots]
-  uint64_t* qk_empty = bars + 13 + kQkSlots;
-  uint64_t* v_full = bars + 13 + 2 * kQkSlots;              // [kVSlots]
-  uint64_t* v_empty = bars + 13 + 2 * kQkSlots + kVSlots;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13 + 2 * kQkSlots + 2 * kVSlots);
+  uint64_t* ost_full = bars + 12;     // local/dense: the O stage is written (softmax warps)
+  uint64_t* q_full = bars + 13;       // [kQSlots]
+  uint64_t* q_empty = q_full + kQSlots;
+  uint64_t* k_full = q_empty + kQSlots;   // [kKSlots]
+  uint64_t* k_empty = k_full + kKSlots;
+  uint64_t* v_full = k_empty + kKSlots;   // [kVSlots]
+  uint64_t* v_empty = v_full + kVSlots;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(v_empty + kVSlots);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* xch = reinterpret_cast<float*>(smem + Cfg::kXch);
 
   const int warp = warp_id(), lane = lane_id();
   const int n_units = unit_count<MODE>(a);
   if (threadIdx.x == 0) {
-    mbar_init(q_ready, kSoftmaxThreads);
-    mbar_init(o_done, 1);
+    mbar_init(&pv_done[0], 1);
+    mbar_init(&pv_done[1], 1);
     mbar_init(o_final, 1);
-    mbar_init(o_free, kSoftmaxThreads);
+    mbar_init(o_free, kSoftmaxWarps);
     mbar_init(ofar_full, 1);
     mbar_init(ost_free, 1);
-    mbar_init(ost_full, kSoftmaxThreads);
+    mbar_init(ost_full, kSoftmaxWarps);
     for (int x = 0; x < 2; ++x) {
       mbar_init(&s_full[x], 1);
-      mbar_init(&p_ready[x], kSoftmaxThreads);
-      mbar_init(&s_free[x], kSoftmaxThreads);
+      mbar_init(&p_ready[x], kSoftmaxWarps);
+      mbar_init(&s_free[x], kSoftmaxWarps);
     }
-    for (int k = 0; k < kQkSlots; ++k) {
-      mbar_init(&qk_full[k], 1);
-      mbar_init(&qk_empty[k], 1);
+    for (int k = 0; k < kQSlots; ++k) {
+      mbar_init(&q_full[k], 1);
+      mbar_init(&q_empty[k], 1);
+    }
+    for (int k = 0; k < kKSlots; ++k) {
+      mbar_init(&k_full[k], 1);
+      mbar_init(&k_empty[k], 1);
     }
     for (int k = 0; k < kVSlots; ++k) {
       mbar_init(&v_full[k], 1);
@@ -260,7 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
     if (warp == kWarpLoad) {
       // -------------------------------------------------- Q and K loads ---
-      int cq = 0;                // Q/K ring entries issued
+      int qn = 0;                // Q tiles issued
+      int ck = 0;                // K tiles issued
       bool ok = true;
       for (int k = 0; ok; ++k) {
         const int u = snake_unit(k, n_units);
@@ -270,14 +293,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         decode_unit<MODE>(a, u, U);
         {
           // the unit's Q tile
-          const int sl = cq % kQkSlots, use = cq / kQkSlots;
-          if (use > 0 && !warp_wait(&qk_empty[sl], (use - 1) & 1, abort, a.err)) break;
-          uint8_t* dst = sQK + sl * Cfg::kTile;
+          const int sl = qn % kQSlots, use = qn / kQSlots;
+          if (use > 0 && !warp_wait_nap(&q_empty[sl], (use - 1) & 1, abort, a.err)) break;
+          uint8_t* dst = sQ + sl * Cfg::kTile;
           if (MODE == kModeGroup) {
             // TMA row gather through perm: lane l fetches tile rows 4l..4l+3 of every
             // 64-column slab (tm_q is a 2-D {d, B*H*n} view with one-row boxes);
             // rows past the item repeat its first row, whose scores are all masked
-            if (lane == 0) mbar_expect_tx(&qk_full[sl], Cfg::kTile);
+            if (lane == 0) mbar_expect_tx(&q_full[sl], Cfg::kTile);
             __syncwarp();
             const int32_t* pp = a.perm + static_cast<size_t>(U.prob) * a.n + U.row0;
             const int first = pp[0];
@@ -289,35 +312,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 #pragma unroll
             for (int ch = 0; ch < kChunks; ++ch)
-              tma_gather4(dst + ch * Cfg::kChunk + 4 * lane * 128, &tm_q, &qk_full[sl], ch * 64, rows[0],
+              tma_gather4(dst + ch * Cfg::kChunk + 4 * lane * 128, &tm_q, &q_full[sl], ch * 64, rows[0],
                           rows[1], rows[2], rows[3]);
           } else if (lane == 0) {
-            mbar_expect_tx(&qk_full[sl], Cfg::kTile);
+            mbar_expect_tx(&q_full[sl], Cfg::kTile);
 #pragma unroll
             for (int ch = 0; ch < kChunks; ++ch)
-              tma_load_3d(dst + ch * Cfg::kChunk, &tm_q, &qk_full[sl], ch * 64, U.row0, U.zq);
+              tma_load_3d(dst + ch * Cfg::kChunk, &tm_q, &q_full[sl], ch * 64, U.row0, U.zq);
           }
-          ++cq;
+          ++qn;
         }
         if (lane == 0) {
-          for (int t = U.t0; t <= U.t1; ++t, ++cq) {
-            const int sl = cq % kQkSlots, use = cq / kQkSlots;
-            if (use > 0 && !mbar_wait(&qk_empty[sl], (use - 1) & 1, abort, a.err)) { ok = false; break; }
-            mbar_expect_tx(&qk_full[sl], Cfg::kTile);
+          for (int t = U.t0; t <= U.t1; ++t, ++ck) {
+            const int sl = ck % kKSlots, use = ck / kKSlots;
+            if (use > 0 && !mbar_wait_nap(&k_empty[sl], (use - 1) & 1, abort, a.err)) { ok = false; break; }
+            mbar_expect_tx(&k_full[sl], Cfg::kTile);
 #pragma unroll
             for (int ch = 0; ch < kChunks; ++ch)
-              tma_load_3d(sQK + sl * Cfg::kTile + ch * Cfg::kChunk, &tm_k, &qk_full[sl], ch * 64,
+              tma_load_3d(sK + sl * Cfg::kTile + ch * Cfg::kChunk, &tm_k, &k_full[sl], ch * 64,
                           U.ybase + t * kBN, U.zkv);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort;
-        cq = __shfl_sync(0xffffffffu, cq, 0);
+        ck = __shfl_sync(0xffffffffu, ck, 0);
       }
       if (*abort && lane == 0) {
         // drain: TMA copies already issued must land before the CTA exits
-        for (int L = max(0, cq - kQkSlots); L < cq; ++L) {
+        for (int L = max(0, ck - kKSlots); L < ck; ++L) {
           const unsigned long long t0 = global_ns();
-          while (!mbar_try_wait(&qk_full[L % kQkSlots], (L / kQkSlots) & 1) &&
+          while (!mbar_try_wait(&k_full[L % kKSlots], (L / kKSlots) & 1) &&
+                 global_ns() - t0 < kWaitTimeoutNs) {}
+        }
+        for (int L = max(0, qn - kQSlots); L < qn; ++L) {
+          const unsigned long long t0 = global_ns();
+          while (!mbar_try_wait(&q_full[L % kQSlots], (L / kQSlots) & 1) &&
                  global_ns() - t0 < kWaitTimeoutNs) {}
         }
       }
@@ -336,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           decode_unit<MODE>(a, u, U);
           for (int t = U.t0; t <= U.t1; ++t, ++cv) {
             const int sl = cv % kVSlots, use = cv / kVSlots;
-            if (use > 0 && !mbar_wait(&v_empty[sl], (use - 1) & 1, abort, a.err)) { ok = false; break; }
+            if (use > 0 && !mbar_wait_nap(&v_empty[sl], (use - 1) & 1, abort, a.err)) { ok = false; break; }
             mbar_expect_tx(&v_full[sl], Cfg::kTile);
 #pragma unroll
             for (int ch = 0; ch < kChunks; ++ch)
@@ -346,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (MODE == kModeLocal && ok) {
             // the unit's group-partial tile into the O stage, once the previous
             // unit's O has been stored out of it
-            if (un > 0 && !mbar_wait(ost_free, (un - 1) & 1, abort, a.err)) ok = false;
+            if (un > 0 && !mbar_wait_nap(ost_free, (un - 1) & 1, abort, a.err)) ok = false;
             if (ok) {
               mbar_expect_tx(ofar_full, Cfg::kTile);
 #pragma unroll
@@ -380,10 +408,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t idS = idesc_bf16_f32(128, kBN, false, false);
         constexpr uint32_t idPV = idesc_bf16_f32(128, D, false, true);
         constexpr uint32_t dhi = sw128_desc_hi();
-        const uint32_t klo = sw128_desc_lo(smem_u32(sQK), 16);          // K slots, K-major
+        const uint32_t klo = sw128_desc_lo(smem_u32(sK), 16);           // K slots, K-major
         const uint32_t vlo = sw128_desc_lo(smem_u32(sV), Cfg::kChunk);  // V slots, MN-major
         int g = 0;        // tiles (S buffers) walked
-        int cq = 0;       // Q/K ring entries walked
+        int ck = 0;       // K ring entries walked
         int cv = 0;       // V ring entries walked
         int un = 0;       // units walked
         bool ok = true;
@@ -395,45 +423,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           decode_unit<MODE>(a, u, U);
           const int nt = U.t1 - U.t0 + 1;
           if (warp == kWarpS) {
-            // the unit's Q entry: the softmax copies it into TMEM; once it has,
-            // the slot goes back to the loader
-            const int qsl = cq % kQkSlots;
-            ++cq;
-            if (!mbar_wait(q_ready, un & 1, abort, a.err)) break;
-            mbar_arrive(&qk_empty[qsl]);
-            // S(gg) = Q K^T into S buffer gg&1.  The first two tiles of a unit reuse
-            // buffers the softmax finished with before it published this unit's Q.
-            for (int i = 0; i < nt; ++i, ++cq) {
+            // S(gg) = Q K^T into S buffer gg&1 once the softmax has read S(gg-2),
+            // the previous content of that buffer; the unit's Q slot is released
+            // after its last S product
+            const int qsl = un % kQSlots;
+            if (!mbar_wait_nap(&q_full[qsl], (un / kQSlots) & 1, abort, a.err)) break;
+            const uint32_t q0 = sw128_desc_lo(smem_u32(sQ + qsl * Cfg::kTile), 16);
+            for (int i = 0; i < nt; ++i, ++ck) {
               const int gg = g + i;
-              if (i >= 2 && !mbar_wait(&s_free[gg & 1], ((gg - 2) >> 1) & 1, abort, a.err)) { ok = false; break; }
-              const int sl = cq % kQkSlots;
-              if (!mbar_wait(&qk_full[sl], (cq / kQkSlots) & 1, abort, a.err)) { ok = false; break; }
+              if (gg >= 2 && !mbar_wait_nap(&s_free[gg & 1], ((gg - 2) >> 1) & 1, abort, a.err)) { ok = false; break; }
+              const int sl = ck % kKSlots;
+              if (!mbar_wait_nap(&k_full[sl], (ck / kKSlots) & 1, abort, a.err)) { ok = false; break; }
               tc_fence_after();
               const uint32_t b0 = klo + sl * (Cfg::kTile >> 4);
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = ((kk >> 2) * Cfg::kChunk + (kk & 3) * 32) >> 4;
-                mma_ts(tmem + Cfg::kS + 128 * (gg & 1), tmem + Cfg::kQt + kk * 8, desc_join(b0 + off, dhi),
+                mma_ss(tmem + Cfg::kS + 128 * (gg & 1), desc_join(q0 + off, dhi), desc_join(b0 + off, dhi),
                        idS, kk > 0);
               }
               mma_commit(&s_full[gg & 1]);
-              mma_commit(&qk_empty[sl]);
+              mma_commit(&k_empty[sl]);
             }
+            if (!ok) break;
+            mma_commit(&q_empty[qsl]);
           } else {
             // O += P(gg) V(gg)
             for (int i = 0; i < nt; ++i, ++cv) {
               const int gg = g + i;
-              if (!mbar_wait(&p_ready[gg & 1], (gg >> 1) & 1, abort, a.err)) { ok = false; break; }
-              if (i == 0 && un > 0 && !mbar_wait(o_free, (un - 1) & 1, abort, a.err)) { ok = false; break; }
               const int sl = cv % kVSlots;
-              if (!mbar_wait(&v_full[sl], (cv / kVSlots) & 1, abort, a.err)) { ok = false; break; }
+              if (!mbar_wait_nap(&v_full[sl], (cv / kVSlots) & 1, abort, a.err)) { ok = false; break; }
+              if (i == 0 && un > 0 && !mbar_wait_nap(o_free, (un - 1) & 1, abort, a.err)) { ok = false; break; }
+              if (!mbar_wait_nap(&p_ready[gg & 1], (gg >> 1) & 1, abort, a.err)) { ok = false; break; }
               tc_fence_after();
               const uint32_t vb = vlo + sl * (Cfg::kTile >> 4);
 #pragma unroll
               for (int kk = 0; kk < kBN / 16; ++kk)
-                mma_ts(tmem + Cfg::kO, tmem + Cfg::kP + kk * 8, desc_join(vb + kk * ((16 * 128) >> 4), dhi),
-                       idPV, i > 0 || kk > 0);
-              mma_commit(o_done);
+                mma_ts(tmem + Cfg::kO, tmem + Cfg::kP + 64 * (gg & 1) + kk * 8,
+                       desc_join(vb + kk * ((16 * 128) >> 4), dhi), idPV, i > 0 || kk > 0);
+              mma_commit(&pv_done[gg & 1]);
               mma_commit(&v_empty[sl]);
               if (i == nt - 1) mma_commit(o_final);
             }
@@ -516,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
           if (c0 + 32 == kHalfD) {
             tc_fence_before();
-            mbar_arrive(o_free);
+            warp_arrive(o_free, lane);
           }
 #pragma unroll
           for (int cc = 0; cc < 32; cc += 8) {
@@ -563,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         if (c0 + 32 == kHalfD) {
           tc_fence_before();
-          mbar_arrive(o_free);
+          warp_arrive(o_free, lane);
         }
 #pragma unroll
         for (int cc = 0; cc < 32; cc += 8) {
@@ -594,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // proxy) once ost_full completes; one thread then stores the tile.  The
       // next unit's arrivals need that thread's P, so a phase is never lapped.
       fence_proxy_async_smem();
-      mbar_arrive(ost_full);
+      warp_arrive(ost_full, lane);
       bool stored = true;
       if (threadIdx.x == 0) {
         stored = mbar_wait(ost_full, unit_index & 1, abort, a.err);
@@ -621,35 +649,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       decode_unit<MODE>(a, u, U);
       // 1. this half of the unit's Q row: staged tile -> registers -> TMEM.  The
       //    previous unit's S products, the only readers of TMEM Q, have all landed.
-      // the unit's Q sits in the Q/K ring after un earlier Q tiles and g K tiles
-      const int qe = un + g;
-      if (!warp_wait(&qk_full[qe % kQkSlots], (qe / kQkSlots) & 1, abort, a.err)) { ok = false; break; }
-      {
-        const uint8_t* sQ = sQK + (qe % kQkSlots) * Cfg::kTile;
-        uint32_t qu[kHalfD / 2];
-#pragma unroll
-        for (int i = 0; i < kHalfD / 8; ++i) {
-          const int v = hf * (kHalfD / 8) + i;
-          const uint4 q4 = *reinterpret_cast<const uint4*>(sQ + (v >> 3) * Cfg::kChunk + r * 128 +
-                                                          (((v & 7) ^ (r & 7)) << 4));
-          qu[4 * i + 0] = q4.x;
-          qu[4 * i + 1] = q4.y;
-          qu[4 * i + 2] = q4.z;
-          qu[4 * i + 3] = q4.w;
-        }
-        const uint32_t tq = tmem + lane_base + Cfg::kQt + hf * (kHalfD / 2);
-        if constexpr (kHalfD / 2 == 32) tmem_st32(tq, qu);
-        else tmem_st16(tq, qu);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(q_ready);
-      }
-      // 2. the previous unit's epilogue overlaps this unit's first S products
+      // 1. the previous unit's epilogue overlaps this unit's first S products
       if (have_prev) {
         if (!epilogue(prev, un - 1)) { ok = false; break; }
         have_prev = false;
       }
-      // 3. this unit's key tiles
+      // 2. this unit's key tiles
       RowState st{};
       st.valid = r < U.nrows;
       st.prob = U.prob;
@@ -694,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&su[32]));
         tmem_wait_ld();
         tc_fence_before();
-        mbar_arrive(&s_free[gg & 1]);     // S(gg+2) may now overwrite this buffer
+        warp_arrive(&s_free[gg & 1], lane);     // S(gg+2) may now overwrite this buffer
         const bool full = j0 >= lo && j0 + kHalfS - 1 <= hi;
         if (!full) {
 #pragma unroll
@@ -717,12 +722,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float m_new = fmaxf(m_run, mt * sl2);
         const bool need = m_run != -INFINITY && m_new > m_run + kRescaleThreshold;
         if (m_run == -INFINITY) m_run = m_new;      // nothing accumulated yet for this row
-        // PV(gg-1) must be done before O is rescaled or P is overwritten.  This
-        // thread waited for PV(gg-2) before writing P(gg-1), and PV(gg) needs
-        // P(gg), so o_done is at most one phase behind: its parity is exact.
+        // O may be rescaled once PV(gg-1) is done.  P buffer b holds P(gg) for
+        // gg = b, b+2, ...; this thread waited for PV(gg-3) before writing
+        // P(gg-1), so pv_done[(gg-1)&1] is at most one phase behind.
         const bool pv_prev = i > 0;
         if (pv_prev && __any_sync(0xffffffffu, need)) {
-          if (!warp_wait(o_done, (gg - 1) & 1, abort, a.err)) { ok = false; break; }
+          if (!warp_wait(&pv_done[(gg - 1) & 1], ((gg - 1) >> 1) & 1, abort, a.err)) { ok = false; break; }
           tc_fence_after();
           const float alpha = need ? ex2f(m_run - m_new) : 1.f;
           uint32_t rr[32];
@@ -742,7 +747,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mu = m_run == -INFINITY ? 0.f : m_run;
         // p = 2^(s*scale*log2e - m): scale-and-shift in packed pairs, exp2 per
         // element, four packed partial sums; P is written as bf16 pairs into
-        // this half of the P buffer once PV(gg-1) has finished reading it
+        // this half of P buffer gg&1 once PV(gg-2) has finished reading it
         const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(-mu, -mu);
         uint64_t acc[4] = {0, 0, 0, 0};
         uint32_t pk[kHalfS / 2];
@@ -754,9 +759,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc[(cc >> 1) & 3] = f2_add(acc[(cc >> 1) & 3], f2_pack(p0, p1));
           pk[cc / 2] = pack_bf16x2(p0, p1);
         }
-        if (pv_prev && !warp_wait(o_done, (gg - 1) & 1, abort, a.err)) { ok = false; break; }
+        if (gg >= 2 && !warp_wait(&pv_done[gg & 1], ((gg - 2) >> 1) & 1, abort, a.err)) { ok = false; break; }
         tc_fence_after();
-        tmem_st32(tmem + lane_base + Cfg::kP + hf * (kHalfS / 2), pk);
+        tmem_st32(tmem + lane_base + Cfg::kP + 64 * (gg & 1) + hf * (kHalfS / 2), pk);
         {
           const uint64_t s2 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
           float s0, s1;
@@ -765,7 +770,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&p_ready[gg & 1]);
+        warp_arrive(&p_ready[gg & 1], lane);
       }
       if (!ok) break;
       g += nt;

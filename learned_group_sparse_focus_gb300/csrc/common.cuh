@@ -15,6 +15,10 @@ namespace focus {
 
 // One second: no wait in these kernels legitimately lasts this long.
 constexpr unsigned long long kWaitTimeoutNs = 1000000000ull;
+// Longest a single mbarrier try_wait may sleep before the loop checks again.
+constexpr uint32_t kWaitSleepNs = 2000;
+// Sleep between probes of a polling issuer thread.
+constexpr uint32_t kNapNs = 32;
 
 __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;
@@ -53,6 +57,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the warp may sleep up to `ns` nanoseconds
+// for the phase instead of returning at once, so a waiting warp does not take
+// issue slots from the warps sharing its SM sub-partition.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(ns) : "memory");
+  return ok != 0;
+}
+
 // Non-blocking probe of the same condition (no suspend hint).
 __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
@@ -71,8 +87,29 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   if (mbar_test_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
     if ((it & 63u) == 0) {
+      if (*abort) return false;
+      if (global_ns() - t0 > kWaitTimeoutNs) {
+        *abort = 1;
+        atomicOr(err, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// The same bounded wait for a lone issuing thread (a load or MMA warp): it
+// polls with a short sleep between probes, so while it waits it leaves the
+// issue slots of its SM sub-partition to the compute warps there.
+__device__ __forceinline__ bool mbar_wait_nap(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                              int* err) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(kNapNs);
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((it & 255u) == 0) {
       if (*abort) return false;
       if (global_ns() - t0 > kWaitTimeoutNs) {
         *abort = 1;
