@@ -17,35 +17,36 @@
 //          partial by log-sum-exp when the row has far keys; writes O.
 //   dense  128 consecutive tokens, every j <= i (the comparator).
 //
-// Both products read their A operand from TMEM: S = Q K^T takes Q from TMEM
-// and K from shared memory, O += P V takes P from TMEM and V from shared
-// memory.  TMEM (512 columns for d = 128): S double buffer (2 x 128), O (d
-// columns), Q (d/2 columns of bf16 pairs) and P (64 columns of bf16 pairs).
-// P has a buffer of its own, so S(t+2) may overwrite S(t) as soon as the
-// softmax has read it: the S product of a later tile runs while the softmax
-// works, and only O += P V waits for P.
+// S = Q K^T reads Q and K from shared memory; O += P V reads P from TMEM and
+// V from shared memory.  TMEM (512 columns for d = 128): S double buffer
+// (2 x 128), O (d columns) and a P double buffer (2 x 64 columns of bf16
+// pairs).  S(t+2) may overwrite S(t) as soon as the softmax has read it, and
+// P(t) goes to its own buffer once O += P(t-2) V is done, so the S product of
+// a later tile runs while the softmax works and the softmax never waits for
+// the PV product of the tile before.
 //
 // Warp roles (384 threads), one CTA per SM looping over units:
 //   warps 0-7   softmax, two warps per query row (warps w and w + 4 share TMEM
-//               lane quadrant w, each takes half of every row's columns): copy
-//               the staged Q half-row into TMEM, then per key tile read the
-//               half S row from TMEM, apply the keep rule to boundary tiles,
-//               agree on the row max with the partner through shared memory,
-//               exp2 and sum in fp32, write the half P row, rescale the half O
-//               row only when the running max grows by more than 2^8; the
-//               epilogue of a unit runs after the next unit's Q is in TMEM, so
-//               the next unit's first S products overlap it; in the local and
-//               dense passes it builds the O tile in shared memory (merged with
-//               the group partial the load warp staged there) and writes it
-//               with one TMA store
-//   warp 8      Q and K tiles into one 3-slot ring, in the order the S
-//               products use them (TMA; a TMA row gather through perm for the
-//               group pass's Q)
+//               lane quadrant w, each takes half of every row's columns): per
+//               key tile read the half S row from TMEM, apply the keep rule to
+//               boundary tiles, agree on the row max with the partner through
+//               shared memory, exp2 and sum in fp32, write the half P row,
+//               rescale the half O row only when the running max grows by
+//               more than 2^8; the epilogue of a unit runs at the start of the
+//               next one, so the next unit's first S products overlap it; in
+//               the local and dense passes it builds the O tile in shared
+//               memory (merged with the group partial the V load warp staged
+//               there) and writes it with one TMA store
+//   warp 8      Q tiles into a 2-slot ring and K tiles into a 2-slot ring
+//               (TMA; a TMA row gather through perm for the group pass's Q)
 //   warp 9      TMEM owner; issues O += P(t) V(t) once P(t) is written
 //   warp 10     issues S(t) = Q K(t)^T once the softmax has read S(t-2),
 //               the previous content of the same buffer
-//   warp 11     V tiles into a 3-slot ring and, in the local pass, the unit's
+//   warp 11     V tiles into a 2-slot ring and, in the local pass, the unit's
 //               group-partial O tile into the O stage
+// The load and MMA warps wait by polling with short sleeps: an issuing thread
+// that spins, or a tcgen05.mma queued behind a busy tensor pipe, slows the
+// softmax warps that share its SM sub-partition.
 // Every wait is bounded; on timeout the CTA raises an error bit, drains its
 // copies, frees TMEM and exits.
 #include "common.cuh"
