@@ -213,11 +213,16 @@ FOCUS_API focus_status_t focus_dense_causal_fwd(const focus_params_t* p, const v
                                       size_t ws_bytes, void* stream);
 
 /* The whole layer from HOST buffers: copies h, W, C, Q, K, V from host memory
- * (pinned for overlap) into the caller's device buffers with one
- * cudaMemcpyAsync each, runs assign -> index -> attention on `stream`, and
- * copies O back to host memory.  d_* are device buffers of the sizes above;
+ * (pinned, for the copies to overlap) into the caller's device buffers, runs
+ * assign -> index -> attention on `stream`, and copies O back to host memory.
+ * When B = 1 and A = 1, Q/K/V and O move in KV-head chunks on two
+ * library-owned streams (created once per device): each chunk's attention
+ * starts when its inputs have landed and its O returns while later chunks
+ * compute.  Everything is ordered after the caller's earlier work on `stream`
+ * and completes on `stream`.  d_* are device buffers of the sizes above;
  * d_gid is [B, A, n] int32.  Returns after enqueueing; synchronise the stream
- * (or call focus_check_errors) before reading host_O. */
+ * (or call focus_check_errors) before reading host_O.  Calls on one device
+ * share the internal streams: do not overlap two calls. */
 FOCUS_API focus_status_t focus_layer_fwd_host(const focus_params_t* p,
                                     const void* host_h, const void* host_W, const void* host_C,
                                     const void* host_Q, const void* host_K, const void* host_V,

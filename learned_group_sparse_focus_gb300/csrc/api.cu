@@ -166,6 +166,35 @@ AttnArgs attn_args(const focus_params_t* p, const void* Q, const void* K, const 
   return a;
 }
 
+// Streams and events focus_layer_fwd_host uses to overlap its copies with
+// compute, created once per device (the library allocates no memory for them).
+constexpr int kMaxChunks = 8;
+struct HostPipe {
+  cudaStream_t copy_in = nullptr, copy_out = nullptr;
+  cudaEvent_t start = nullptr, inputs = nullptr, done = nullptr;
+  cudaEvent_t chunk_in[kMaxChunks] = {}, chunk_out[kMaxChunks] = {};
+  bool ready = false;
+};
+HostPipe g_pipe[64];
+
+focus_status_t pipe_setup(HostPipe** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FOCUS_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  HostPipe& hp = g_pipe[dev];
+  if (!hp.ready) {
+    auto ev = [](cudaEvent_t* e) { return cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess; };
+    bool ok = cudaStreamCreateWithFlags(&hp.copy_in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&hp.copy_out, cudaStreamNonBlocking) == cudaSuccess &&
+              ev(&hp.start) && ev(&hp.inputs) && ev(&hp.done);
+    for (int c = 0; ok && c < kMaxChunks; ++c) ok = ev(&hp.chunk_in[c]) && ev(&hp.chunk_out[c]);
+    if (!ok) return FOCUS_ERR_CUDA;
+    hp.ready = true;
+  }
+  *out = &hp;
+  return FOCUS_OK;
+}
+
 }  // namespace
 }  // namespace focus
 
@@ -371,6 +400,10 @@ focus_status_t focus_layer_fwd_host(const focus_params_t* p, const void* host_h,
   if (!params_ok(p)) return FOCUS_ERR_INVALID_ARG;
   if (!host_h || !host_W || !host_C || !host_Q || !host_K || !host_V || !host_O)
     return FOCUS_ERR_INVALID_ARG;
+  if (!d_h || !d_W || !d_C || !d_Q || !d_K || !d_V || !d_O || !d_gid) return FOCUS_ERR_INVALID_ARG;
+  if (focus_status_t s = ensure_setup()) return s;
+  HostPipe* pp = nullptr;
+  if (focus_status_t s = pipe_setup(&pp)) return s;
   const size_t es = elt_size(p->dtype);
   const size_t nb = static_cast<size_t>(p->B) * p->n;
   const size_t bytes_h = nb * p->D * es;
@@ -378,23 +411,59 @@ focus_status_t focus_layer_fwd_host(const focus_params_t* p, const void* host_h,
   const size_t bytes_C = static_cast<size_t>(p->A) * p->K * p->d_g * es;
   const size_t bytes_Q = nb * p->H * p->d * es;
   const size_t bytes_KV = nb * p->H_kv * p->d * es;
+  // Q/K/V (and O) move in KV-head chunks so each chunk's attention starts as
+  // soon as its inputs land and its O goes back while later chunks compute.
+  // Head slices are contiguous when B = 1, and with A = 1 every chunk shares
+  // the one index; otherwise the layer runs as one chunk.
+  int chunks = 1;
+  if (p->B == 1 && p->A == 1)
+    for (int c = kMaxChunks; c > 1; --c)
+      if (p->H_kv % c == 0) { chunks = c; break; }
+  focus_params_t pc = *p;
+  pc.H = p->H / chunks;
+  pc.H_kv = p->H_kv / chunks;
+  const size_t cq = bytes_Q / chunks, ckv = bytes_KV / chunks;
+  auto ptr = [](const void* b, size_t off) { return static_cast<const char*>(b) + off; };
+  auto mptr = [](void* b, size_t off) { return static_cast<char*>(b) + off; };
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // host -> device, all on the copy-in stream, ordered after the caller's work
+  if (cudaEventRecord(pp->start, st) != cudaSuccess || cudaStreamWaitEvent(pp->copy_in, pp->start, 0) != cudaSuccess)
+    return FOCUS_ERR_CUDA;
   const struct { void* dst; const void* src; size_t n; } up[] = {
-      {d_h, host_h, bytes_h}, {d_W, host_W, bytes_W}, {d_C, host_C, bytes_C},
-      {d_Q, host_Q, bytes_Q}, {d_K, host_K, bytes_KV}, {d_V, host_V, bytes_KV}};
-  for (const auto& c : up) {
-    if (!c.dst) return FOCUS_ERR_INVALID_ARG;
-    if (cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, st) != cudaSuccess)
+      {d_h, host_h, bytes_h}, {d_W, host_W, bytes_W}, {d_C, host_C, bytes_C}};
+  for (const auto& c : up)
+    if (cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, pp->copy_in) != cudaSuccess)
+      return FOCUS_ERR_CUDA;
+  if (cudaEventRecord(pp->inputs, pp->copy_in) != cudaSuccess) return FOCUS_ERR_CUDA;
+  for (int c = 0; c < chunks; ++c) {
+    if (cudaMemcpyAsync(mptr(d_Q, c * cq), ptr(host_Q, c * cq), cq, cudaMemcpyHostToDevice, pp->copy_in) != cudaSuccess ||
+        cudaMemcpyAsync(mptr(d_K, c * ckv), ptr(host_K, c * ckv), ckv, cudaMemcpyHostToDevice, pp->copy_in) != cudaSuccess ||
+        cudaMemcpyAsync(mptr(d_V, c * ckv), ptr(host_V, c * ckv), ckv, cudaMemcpyHostToDevice, pp->copy_in) != cudaSuccess ||
+        cudaEventRecord(pp->chunk_in[c], pp->copy_in) != cudaSuccess)
       return FOCUS_ERR_CUDA;
   }
+  // assign and index once h, W, C are in
+  if (cudaStreamWaitEvent(st, pp->inputs, 0) != cudaSuccess) return FOCUS_ERR_CUDA;
   focus_status_t s = focus_assign(p, d_h, d_W, d_C, d_gid, ws, ws_bytes, stream);
   if (s) return s;
   focus_index_t idx{};
   s = focus_build_index(p, d_gid, &idx, ws, ws_bytes, stream);
   if (s) return s;
-  s = focus_attention_fwd(p, d_Q, d_K, d_V, &idx, d_O, nullptr, ws, ws_bytes, stream);
-  if (s) return s;
-  return cuda_status(cudaMemcpyAsync(host_O, d_O, bytes_Q, cudaMemcpyDeviceToHost, st));
+  // attention per chunk on the caller's stream, O back on the copy-out stream
+  for (int c = 0; c < chunks; ++c) {
+    if (cudaStreamWaitEvent(st, pp->chunk_in[c], 0) != cudaSuccess) return FOCUS_ERR_CUDA;
+    s = focus_attention_fwd(&pc, mptr(d_Q, c * cq), mptr(d_K, c * ckv), mptr(d_V, c * ckv), &idx,
+                            mptr(d_O, c * cq), nullptr, ws, ws_bytes, stream);
+    if (s) return s;
+    if (cudaEventRecord(pp->chunk_out[c], st) != cudaSuccess ||
+        cudaStreamWaitEvent(pp->copy_out, pp->chunk_out[c], 0) != cudaSuccess ||
+        cudaMemcpyAsync(mptr(host_O, c * cq), mptr(d_O, c * cq), cq, cudaMemcpyDeviceToHost, pp->copy_out) != cudaSuccess)
+      return FOCUS_ERR_CUDA;
+  }
+  // the caller's stream completes after the last copy back
+  if (cudaEventRecord(pp->done, pp->copy_out) != cudaSuccess || cudaStreamWaitEvent(st, pp->done, 0) != cudaSuccess)
+    return FOCUS_ERR_CUDA;
+  return FOCUS_OK;
 }
 
 focus_status_t focus_check_errors(void* ws, void* stream) {

@@ -59,7 +59,6 @@ constexpr int kBN = 128;                     // keys per tile
 constexpr int kBM = 128;                     // query rows per unit
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
 constexpr int kSoftmaxWarps = 8;            // two per TMEM lane quadrant
-constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
 constexpr int kWarpLoad = kSoftmaxWarps;     // TMA loads
 constexpr int kWarpPV = kSoftmaxWarps + 1;   // TMEM owner, O += P V issuer
 constexpr int kWarpS = kSoftmaxWarps + 2;    // S = Q K^T issuer
