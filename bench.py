@@ -381,7 +381,8 @@ def run_ours(args, wl, world, rank, local):
     if rank == 0:
         line["clocks"] = clk.summary()
         if world == 1 and not args.no_cpu_baseline:
-            f, sec, desc = oracle_sample(wl, x, args.cpu_rows, [0, wl.H - 1], seed=7)
+            heads = sorted({0, wl.H // 3, (2 * wl.H) // 3, wl.H - 1})
+            f, sec, desc = oracle_sample(wl, x, args.cpu_rows, heads, seed=7)
             line["cpu_baseline"] = {"value": f / sec / 1e12, "unit": UNIT, "cores": cpu_cores(),
                                     "kind": "oracle", "sample": desc, "seconds": sec}
         print(json.dumps(line), flush=True)
@@ -396,8 +397,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gqa_32k")
-    ap.add_argument("--cpu-rows", type=int, default=1024)
-    ap.add_argument("--ref-rows", type=int, default=256)
+    ap.add_argument("--cpu-rows", type=int, default=6144)
+    ap.add_argument("--ref-rows", type=int, default=1024)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
