@@ -36,14 +36,15 @@
 //               next one, so the next unit's first S products overlap it; in
 //               the local and dense passes it builds the O tile in shared
 //               memory (merged with the group partial the V load warp staged
-//               there) and writes it with one TMA store
+//               there) for the V load warp to store
 //   warp 8      Q tiles into a 2-slot ring and K tiles into a 2-slot ring
 //               (TMA; a TMA row gather through perm for the group pass's Q)
 //   warp 9      TMEM owner; issues O += P(t) V(t) once P(t) is written
 //   warp 10     issues S(t) = Q K(t)^T once the softmax has read S(t-2),
 //               the previous content of the same buffer
-//   warp 11     V tiles into a 2-slot ring and, in the local pass, the unit's
-//               group-partial O tile into the O stage
+//   warp 11     V tiles into a 2-slot ring; in the local and dense passes it
+//               also stores each unit's O tile from the stage with TMA and
+//               then (local) loads the next unit's group-partial tile into it
 // The load and MMA warps wait by polling with short sleeps: an issuing thread
 // that spins, or a tcgen05.mma queued behind a busy tensor pipe, slows the
 // softmax warps that share its SM sub-partition.
@@ -224,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_ready = bars + 6;       // [2] per S buffer (softmax warps)
   uint64_t* s_free = bars + 8;        // [2] per S buffer: the softmax has read it
   uint64_t* ofar_full = bars + 10;    // local: the unit's group-partial tile is staged
-  uint64_t* ost_free = bars + 11;     // local: the O stage was stored out (1 arrival)
+  uint64_t* ost_free = bars + 11;     // dense: the O stage was stored out (1 arrival)
   uint64_t* ost_full = bars + 12;     // local/dense: the O stage is written (softmax warps)
   uint64_t* q_full = bars + 13;       // [kQSlots]
   uint64_t* q_empty = q_full + kQSlots;
@@ -350,19 +351,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else if (warp == kWarpLoadV) {
-      // ------------------------------------------- V loads, group partial ---
+      // ------------------------- V loads; O stage out and group partial in ---
+      // In the local and dense passes this thread also owns the O stage: once
+      // the softmax warps have written a unit's O tile there (ost_full) it
+      // stores the tile with TMA and, when the copy has read the stage, loads
+      // the next unit's group partial into it (local) or releases it (dense).
       if (lane == 0) {
         int cv = 0;              // V ring entries issued
         int un = 0;              // units walked
         int ofn = 0;             // group-partial tiles issued
         bool ok = true;
+        int prow0 = 0, pzq = 0;  // the previous unit's tile
+        auto store_prev = [&]() -> bool {
+          if (!mbar_wait_nap(ost_full, (un - 1) & 1, abort, a.err)) return false;
+          // rows past n fall outside the tensor map and are not written
+#pragma unroll
+          for (int ch = 0; ch < kChunks; ++ch) tma_store_3d(&tm_o, sO + ch * Cfg::kChunk, ch * 64, prow0, pzq);
+          tma_store_commit();
+          tma_store_wait_read();
+          if (MODE == kModeDense) mbar_arrive(ost_free);
+          return true;
+        };
         for (int k = 0; ok; ++k) {
           const int u = snake_unit(k, n_units);
           if (u == -1) break;
           if (u < 0) continue;
           Unit U;
           decode_unit<MODE>(a, u, U);
-          for (int t = U.t0; t <= U.t1; ++t, ++cv) {
+          for (int t = U.t0, i = 0; t <= U.t1; ++t, ++cv, ++i) {
             const int sl = cv % kVSlots, use = cv / kVSlots;
             if (use > 0 && !mbar_wait_nap(&v_empty[sl], (use - 1) & 1, abort, a.err)) { ok = false; break; }
             mbar_expect_tx(&v_full[sl], Cfg::kTile);
@@ -370,24 +386,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int ch = 0; ch < kChunks; ++ch)
               tma_load_3d(sV + sl * Cfg::kTile + ch * Cfg::kChunk, &tm_v, &v_full[sl], ch * 64,
                           U.ybase + t * kBN, U.zkv);
-          }
-          if (MODE == kModeLocal && ok) {
-            // the unit's group-partial tile into the O stage, once the previous
-            // unit's O has been stored out of it
-            if (un > 0 && !mbar_wait_nap(ost_free, (un - 1) & 1, abort, a.err)) ok = false;
-            if (ok) {
-              mbar_expect_tx(ofar_full, Cfg::kTile);
+            // after this unit's first V tiles: the previous unit's O, whose
+            // epilogue runs at the start of this unit, then this unit's partial
+            if (MODE != kModeGroup && i == min(1, U.t1 - U.t0)) {
+              if (un > 0 && !store_prev()) { ok = false; break; }
+              if (MODE == kModeLocal) {
+                mbar_expect_tx(ofar_full, Cfg::kTile);
 #pragma unroll
-              for (int ch = 0; ch < kChunks; ++ch)
-                tma_load_3d(sO + ch * Cfg::kChunk, &tm_of, ofar_full, ch * 64, U.row0, U.zq);
-              ++ofn;
+                for (int ch = 0; ch < kChunks; ++ch)
+                  tma_load_3d(sO + ch * Cfg::kChunk, &tm_of, ofar_full, ch * 64, U.row0, U.zq);
+                ++ofn;
+              }
             }
           }
+          prow0 = U.row0;
+          pzq = U.zq;
           ++un;
           ok = ok && !*abort;
         }
-        if (*abort) {
-          // drain: TMA copies already issued must land before the CTA exits
+        if (MODE != kModeGroup && ok && un > 0) {
+          ok = store_prev();
+          tma_store_wait_all();
+        }
+        if (*abort || !ok) {
+          // drain: copies already issued must land before the CTA exits
+          tma_store_wait_all();
           for (int L = max(0, cv - kVSlots); L < cv; ++L) {
             const unsigned long long t0 = global_ns();
             while (!mbar_try_wait(&v_full[L % kVSlots], (L / kVSlots) & 1) &&
@@ -582,8 +605,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // local and dense: the tile goes through the shared-memory stage (same
       // 128 B-swizzled layout as the TMA boxes) and leaves with one TMA store;
-      // in the local pass the stage already holds the group partial of the rows
+      // in the local pass the stage already holds the group partial of the
+      // rows.  The stage is free once the V load warp has stored the previous
+      // unit's tile out of it: in the local pass that is implied by the group
+      // partial it loads there afterwards; in the dense pass it is signalled.
       if (MODE == kModeLocal && !warp_wait(ofar_full, unit_index & 1, abort, a.err)) return false;
+      if (MODE == kModeDense && unit_index > 0 &&
+          !warp_wait(ost_free, (unit_index - 1) & 1, abort, a.err))
+        return false;
 #pragma unroll
       for (int c0 = 0; c0 < kHalfD; c0 += 32) {
         uint32_t ou[32];
@@ -618,25 +647,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           *slot = o4;
         }
       }
-      // every softmax thread's part is in the stage (and visible to the async
-      // proxy) once ost_full completes; one thread then stores the tile.  The
-      // next unit's arrivals need that thread's P, so a phase is never lapped.
+      // the tile is in the stage (and visible to the async proxy) once all
+      // eight warps have arrived; the V load warp stores it
       fence_proxy_async_smem();
       warp_arrive(ost_full, lane);
-      bool stored = true;
-      if (threadIdx.x == 0) {
-        stored = mbar_wait(ost_full, unit_index & 1, abort, a.err);
-        if (stored) {
-          // rows past n fall outside the tensor map and are not written
-#pragma unroll
-          for (int ch = 0; ch < kChunks; ++ch)
-            tma_store_3d(&tm_o, sO + ch * Cfg::kChunk, ch * 64, s.row0, s.zq);
-          tma_store_commit();
-          tma_store_wait_read();
-          if (MODE == kModeLocal) mbar_arrive(ost_free);
-        }
-      }
-      if (!__all_sync(0xffffffffu, stored)) return false;
       if (hf == 0 && s.valid && a.lse) a.lse[qrow + s.pos] = lse2 * kLn2;
       return true;
     };
@@ -647,8 +661,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (u < 0) continue;
       Unit U;
       decode_unit<MODE>(a, u, U);
-      // 1. this half of the unit's Q row: staged tile -> registers -> TMEM.  The
-      //    previous unit's S products, the only readers of TMEM Q, have all landed.
       // 1. the previous unit's epilogue overlaps this unit's first S products
       if (have_prev) {
         if (!epilogue(prev, un - 1)) { ok = false; break; }
