@@ -71,7 +71,9 @@ Layout layout_of(const focus_params_t* p) {
   const size_t kvb = static_cast<size_t>(p->B) * p->H_kv * n * p->d * es;
   L.Ks = take(p->dtype == FOCUS_BF16 ? kvb : 0);
   L.Vs = take(p->dtype == FOCUS_BF16 ? kvb : 0);
-  L.O_far = take(static_cast<size_t>(p->B) * p->H * n * p->d * es);
+  // + one tile of rows that the group pass's row scatter sends rows past an
+  // item's end to (never read)
+  L.O_far = take((static_cast<size_t>(p->B) * p->H * n + kTileM) * p->d * es);
   L.lse_far = take(static_cast<size_t>(p->B) * p->H * n * 4);
   L.total = o;
   return L;
@@ -303,7 +305,7 @@ static focus_status_t attention_common(const focus_params_t* p, const void* Q, c
     return FOCUS_ERR_INVALID_ARG;
   if (!(p->d == 64 || p->d == 128)) return FOCUS_ERR_UNSUPPORTED;
   // tensor-map row coordinates are 32-bit
-  if (static_cast<long long>(p->B) * p->H * p->n >= (1LL << 31)) return FOCUS_ERR_UNSUPPORTED;
+  if (static_cast<long long>(p->B) * p->H * p->n + kTileM >= (1LL << 31)) return FOCUS_ERR_UNSUPPORTED;
   if (focus_status_t s = check_ws(p, ws, ws_bytes)) return s;
   return ensure_setup();
 }
@@ -356,9 +358,13 @@ focus_status_t focus_attention_fwd_timed(const focus_params_t* p, const void* Q,
     return FOCUS_ERR_CUDA;
   const int sms = sm_count();
   // group pass: Q rows are gathered through perm from a 2-D view with one-row boxes
-  CUtensorMap tqg;
-  if (!make_map(&tqg, Q, p->d, qplanes * p->n, 1, 1, 2)) return FOCUS_ERR_CUDA;
-  e = launch_attn_tc_bf16(a, &tqg, &tks, &tvs, &to, &tof, p->d, kModeGroup, L.max_items, sms, st);
+  // group pass: Q rows are gathered through perm, and O_far rows scattered
+  // back to token positions, through 2-D views with one-row boxes
+  CUtensorMap tqg, tofs;
+  if (!make_map(&tqg, Q, p->d, qplanes * p->n, 1, 1, 2) ||
+      !make_map(&tofs, a.O_far, p->d, qplanes * p->n + kTileM, 1, 1, 2))
+    return FOCUS_ERR_CUDA;
+  e = launch_attn_tc_bf16(a, &tqg, &tks, &tvs, &tofs, &tof, p->d, kModeGroup, L.max_items, sms, st);
   if (e == cudaSuccess) e = mark(2);
   if (e == cudaSuccess) e = launch_attn_tc_bf16(a, &tq, &tk, &tv, &to, &tof, p->d, kModeLocal, 0, sms, st);
   if (e == cudaSuccess) e = mark(3);

@@ -33,18 +33,19 @@
 //               shared memory, exp2 and sum in fp32, write the half P row,
 //               rescale the half O row only when the running max grows by
 //               more than 2^8; the epilogue of a unit runs at the start of the
-//               next one, so the next unit's first S products overlap it; in
-//               the local and dense passes it builds the O tile in shared
-//               memory (merged with the group partial the V load warp staged
-//               there) for the V load warp to store
+//               next one, so the next unit's first S products overlap it: it
+//               builds the O tile in shared memory (in the local pass merged
+//               with the group partial the V load warp staged there) for the V
+//               load warp to store
 //   warp 8      Q tiles into a 2-slot ring and K tiles into a 2-slot ring
 //               (TMA; a TMA row gather through perm for the group pass's Q)
 //   warp 9      TMEM owner; issues O += P(t) V(t) once P(t) is written
 //   warp 10     issues S(t) = Q K(t)^T once the softmax has read S(t-2),
 //               the previous content of the same buffer
-//   warp 11     V tiles into a 2-slot ring; in the local and dense passes it
-//               also stores each unit's O tile from the stage with TMA and
-//               then (local) loads the next unit's group-partial tile into it
+//   warp 11     V tiles into a 2-slot ring; it also stores each unit's O tile
+//               from the stage with TMA (a tile::scatter4 row scatter to the
+//               token positions in the group pass) and then (local) loads the
+//               next unit's group-partial tile into the stage
 // The load and MMA warps wait by polling with short sleeps: an issuing thread
 // that spins, or a tcgen05.mma queued behind a busy tensor pipe, slows the
 // softmax warps that share its SM sub-partition.
@@ -91,7 +92,8 @@ struct AttnCfg {
   static constexpr int kOst = kV + kVSlots * kTile;       // O tile staging
   static constexpr int kBar = kOst + kTile;                 // barriers (< 256 B)
   static constexpr int kXch = kBar + 256;                   // row max / sum exchange: [2][2][128] fp32
-  static constexpr int kSmem = kXch + 2 * 2 * 128 * 4;
+  static constexpr int kRowTok = kXch + 2 * 2 * 128 * 4;    // group pass: O_far row of each tile row
+  static constexpr int kSmem = kRowTok + 128 * 4;
   static constexpr uint32_t kS = 0;          // two S buffers of 128 columns
   static constexpr uint32_t kO = 256;        // O: d columns
   static constexpr uint32_t kP = 384;        // P double buffer: 2 x 64 columns of bf16 pairs
@@ -225,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_ready = bars + 6;       // [2] per S buffer (softmax warps)
   uint64_t* s_free = bars + 8;        // [2] per S buffer: the softmax has read it
   uint64_t* ofar_full = bars + 10;    // local: the unit's group-partial tile is staged
-  uint64_t* ost_free = bars + 11;     // dense: the O stage was stored out (1 arrival)
+  uint64_t* ost_free = bars + 11;     // group, dense: the O stage was stored out (1 arrival)
   uint64_t* ost_full = bars + 12;     // local/dense: the O stage is written (softmax warps)
   uint64_t* q_full = bars + 13;       // [kQSlots]
   uint64_t* q_empty = q_full + kQSlots;
@@ -236,6 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(v_empty + kVSlots);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* xch = reinterpret_cast<float*>(smem + Cfg::kXch);
+  int* row_tok = reinterpret_cast<int*>(smem + Cfg::kRowTok);
 
   const int warp = warp_id(), lane = lane_id();
   const int n_units = unit_count<MODE>(a);
@@ -269,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
-    if (MODE != kModeGroup) prefetch_tmap(&tm_o);
+    prefetch_tmap(&tm_o);
     if (MODE == kModeLocal) prefetch_tmap(&tm_of);
   }
   if (warp == kWarpPV) tmem_alloc(tmem_slot, Cfg::kTmemCols);
@@ -352,10 +355,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (warp == kWarpLoadV) {
       // ------------------------- V loads; O stage out and group partial in ---
-      // In the local and dense passes this thread also owns the O stage: once
-      // the softmax warps have written a unit's O tile there (ost_full) it
-      // stores the tile with TMA and, when the copy has read the stage, loads
-      // the next unit's group partial into it (local) or releases it (dense).
+      // This thread also owns the O stage: once the softmax warps have written
+      // a unit's O tile there (ost_full) it stores the tile with TMA (in the
+      // group pass scattered row by row to the token positions) and, when the
+      // copy has read the stage, loads the next unit's group partial into it
+      // (local) or releases it (group, dense).
       if (lane == 0) {
         int cv = 0;              // V ring entries issued
         int un = 0;              // units walked
@@ -364,12 +368,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         int prow0 = 0, pzq = 0;  // the previous unit's tile
         auto store_prev = [&]() -> bool {
           if (!mbar_wait_nap(ost_full, (un - 1) & 1, abort, a.err)) return false;
-          // rows past n fall outside the tensor map and are not written
+          if (MODE == kModeGroup) {
+            // four rows per scatter, one 64-column slab at a time
+#pragma unroll 4
+            for (int q4 = 0; q4 < 32; ++q4) {
+              const int4 rt = *reinterpret_cast<const int4*>(row_tok + 4 * q4);
 #pragma unroll
-          for (int ch = 0; ch < kChunks; ++ch) tma_store_3d(&tm_o, sO + ch * Cfg::kChunk, ch * 64, prow0, pzq);
+              for (int ch = 0; ch < kChunks; ++ch)
+                tma_scatter4(&tm_o, sO + ch * Cfg::kChunk + 4 * q4 * 128, ch * 64, rt.x, rt.y, rt.z, rt.w);
+            }
+          } else {
+            // rows past n fall outside the tensor map and are not written
+#pragma unroll
+            for (int ch = 0; ch < kChunks; ++ch) tma_store_3d(&tm_o, sO + ch * Cfg::kChunk, ch * 64, prow0, pzq);
+          }
           tma_store_commit();
           tma_store_wait_read();
-          if (MODE == kModeDense) mbar_arrive(ost_free);
+          if (MODE != kModeLocal) mbar_arrive(ost_free);
           return true;
         };
         for (int k = 0; ok; ++k) {
@@ -388,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           U.ybase + t * kBN, U.zkv);
             // after this unit's first V tiles: the previous unit's O, whose
             // epilogue runs at the start of this unit, then this unit's partial
-            if (MODE != kModeGroup && i == min(1, U.t1 - U.t0)) {
+            if (i == min(1, U.t1 - U.t0)) {
               if (un > 0 && !store_prev()) { ok = false; break; }
               if (MODE == kModeLocal) {
                 mbar_expect_tx(ofar_full, Cfg::kTile);
@@ -404,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++un;
           ok = ok && !*abort;
         }
-        if (MODE != kModeGroup && ok && un > 0) {
+        if (ok && un > 0) {
           ok = store_prev();
           tma_store_wait_all();
         }
@@ -557,8 +572,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         lse2 = mm + log2f(den);
       }
       if (MODE == kModeGroup) {
-        // rows are scattered by perm: stage the tile in shared memory, then
-        // each warp writes 16 whole rows of its quadrant, 512 bytes per store
+        // rows are scattered by perm: the tile is staged in shared memory with
+        // each row's O_far row index (rows past the item go to the spare rows
+        // after the last plane), and the V load warp scatters it with TMA once
+        // it has read the previous unit's tile out of the stage
+        if (unit_index > 0 && !warp_wait(ost_free, (unit_index - 1) & 1, abort, a.err)) return false;
         const bool write = s.valid && l > 0.f;
 #pragma unroll
         for (int c0 = 0; c0 < kHalfD; c0 += 32) {
@@ -580,27 +598,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(sO + (v >> 3) * Cfg::kChunk + r * 128 + (((v & 7) ^ (r & 7)) << 4)) = o4;
           }
         }
-        if (write && hf == 0) a.lse_far[qrow + s.pos] = lse2 * kLn2;
-        const int tok = write ? s.pos + 1 : 0;   // both halves hold the same rows
-        if (!pair_sync()) return false;          // both halves of the rows are staged
-        {
-          __nv_bfloat16* Of = static_cast<__nv_bfloat16*>(a.O_far);
-          constexpr int kVec = D / 8;               // 16-byte pieces per row
-          constexpr int kRowsPerStore = 32 / kVec;  // rows one warp store covers
-          constexpr int kIters = 16 / kRowsPerStore;
-          const int v = lane % kVec;
-#pragma unroll 4
-          for (int it = 0; it < kIters; ++it) {
-            const int j = hf * 16 + it * kRowsPerStore + lane / kVec;   // row within the quadrant
-            const int tk = __shfl_sync(0xffffffffu, tok, j);
-            const int row = quad * 32 + j;
-            if (tk > 0)
-              *reinterpret_cast<uint4*>(Of + (qrow + tk - 1) * D + v * 8) = *reinterpret_cast<const uint4*>(
-                  sO + (v >> 3) * Cfg::kChunk + row * 128 + (((v & 7) ^ (row & 7)) << 4));
-          }
+        if (hf == 0) {
+          row_tok[r] = s.valid ? s.zq * a.n + s.pos : a.B * a.H * a.n + r;
+          if (write) a.lse_far[qrow + s.pos] = lse2 * kLn2;
         }
-        // the quadrant's stage rows are rewritten only after the next unit's
-        // tile exchanges, which both warps reach after these stores
+        fence_proxy_async_smem();
+        warp_arrive(ost_full, lane);
         return true;
       }
       // local and dense: the tile goes through the shared-memory stage (same

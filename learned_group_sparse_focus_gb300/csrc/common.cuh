@@ -145,6 +145,17 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, const void* smem_
       "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];"
       ::"l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(smem_src)) : "memory");
 }
+// Row scatter: four 128-byte rows that sit one after another at smem_src go
+// to rows r0..r3 (column `col`) of a 2-D tensor map whose box is one row high.
+__device__ __forceinline__ void tma_scatter4(const void* tmap, const void* smem_src, int col, int r0, int r1,
+                                             int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile::scatter4.bulk_group"
+      " [%0, {%1, %2, %3, %4, %5}], [%6];"
+      ::"l"(tmap), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(smem_src))
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_store_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
