@@ -53,6 +53,22 @@ def load_peaks():
         return dict(FALLBACK), "fallback"
 
 
+def max_over_ranks(vals, dist=None, device="cpu"):
+    """Each entry's largest value over the ranks: a replica job takes as long
+    as its slowest rank.  With no process group the values come back as is."""
+    if dist is None:
+        return [float(v) for v in vals]
+    import torch
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_tflops(world: int, flops_per_rank: float, ms: float) -> float:
+    """Whole-job throughput: every rank processes its own replica."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -290,10 +306,6 @@ def run_ours(args, wl, world, rank, local):
     t = {"assign": mean_ms(0, 1), "index": mean_ms(1, 2), "permute_kv": mean_ms(3, 4),
          "group_pass": mean_ms(4, 5), "local_pass": mean_ms(5, 6)}
     t_attn = mean_ms(3, 6)
-    if dist is not None:
-        tt = torch.tensor([t_step, t_attn], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_step, t_attn = tt.tolist()
 
     # dense causal comparator on the same shape
     for _ in range(3):
@@ -337,6 +349,11 @@ def run_ours(args, wl, world, rank, local):
         if not torch.equal(host["O"].cuda(), O):
             raise RuntimeError("host-buffer path and device path disagree")
 
+    names = list(t)
+    red = max_over_ranks([t_step, t_attn, t_dense, t_e2e] + [t[k] for k in names], dist, "cuda")
+    t_step, t_attn, t_dense, t_e2e = red[:4]
+    t = dict(zip(names, red[4:]))
+
     peaks, peak_kind = load_peaks()
     peak_tc = float(peaks["bf16_tflops_sustained"])
     peak_hbm = float(peaks["hbm_gbs"])
@@ -344,7 +361,7 @@ def run_ours(args, wl, world, rank, local):
     dom_flops = f_group if dom == "group_pass" else f_local
     achieved = dom_flops / (t[dom] * 1e-3) / 1e12
     tr = traffic_record("attn_tc_" + dom)
-    value = world * f_attn / (t_step * 1e-3) / 1e12
+    value = job_tflops(world, f_attn, t_step)
     es = 2 if wl.dtype == "bf16" else 4
     assign_bytes = (wl.B * wl.n * wl.D + wl.A * wl.d_g * wl.D + wl.A * wl.K * wl.d_g) * es + wl.B * wl.A * wl.n * 4
     kv_bytes = 2 * wl.B * wl.H_kv * wl.n * wl.d * es
@@ -372,7 +389,7 @@ def run_ours(args, wl, world, rank, local):
             "local_pass": {"ms": t["local_pass"], "TFLOP/s": f_local / (t["local_pass"] * 1e-3) / 1e12},
             "index": {"ms": t["index"]},
         },
-        "e2e": {"value": world * f_attn / (t_e2e * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": t_e2e,
+        "e2e": {"value": job_tflops(world, f_attn, t_e2e), "unit": UNIT, "ms_per_step": t_e2e,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "call": "focus_layer_fwd_host (pinned host buffers)"},
         "gpu_launches": 9 * args.steps,

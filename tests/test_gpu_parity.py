@@ -270,9 +270,16 @@ def test_workload_full_size(fz, name):
                          f"{name} head {hq}")
 
 
-def test_layer_from_host_buffers_matches_device_path(fz):
+@pytest.mark.parametrize("shape", [
+    dict(n=2048, H=8, H_kv=2, D=512),           # two KV-head chunks
+    dict(n=1024, H=16, H_kv=8, D=512),          # eight chunks
+    dict(B=2, n=1024, H=8, H_kv=2, D=512),      # B = 2: one chunk
+])
+def test_layer_from_host_buffers_matches_device_path(fz, shape):
+    """focus_layer_fwd_host (copies overlapped with compute in KV-head chunks
+    when B = 1 and A = 1) gives the device path's O bit for bit."""
     import torch
-    wl = synth.workload("gqa_32k", n=2048, H=8, H_kv=2, D=512)
+    wl = synth.workload("gqa_32k", **shape)
     x = margin_filtered(wl)
     p = fz.params_from_workload(wl)
     ws = _ws(fz, p)
