@@ -100,6 +100,8 @@ struct AttnCfg {
   static constexpr uint32_t kTmemCols = 512;
 };
 
+static_assert(AttnCfg<128>::kSmem <= 227 * 1024, "attention shared memory above the 227 KB per CTA");
+
 __device__ __forceinline__ float ex2f(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
