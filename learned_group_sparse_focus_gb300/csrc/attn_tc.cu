@@ -101,6 +101,14 @@ struct AttnCfg {
 };
 
 static_assert(AttnCfg<128>::kSmem <= 227 * 1024, "attention shared memory above the 227 KB per CTA");
+static_assert(kBN / 2 % 16 == 0, "the half-row max walks 16 columns per step");
+
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 
 __device__ __forceinline__ float ex2f(float x) {
   float y;
@@ -723,16 +731,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int cc = 0; cc < kHalfS; ++cc)
             if (j0 + cc < lo || j0 + cc > hi) su[cc] = __float_as_uint(-INFINITY);
         }
-        // half-row max: eight independent chains, a tree, then the partner's half
+        // half-row max: eight independent chains of three-input maxima, a
+        // tree, then the partner's half
         float m8[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) m8[j] = __uint_as_float(su[j]);
+        for (int j = 0; j < 8; ++j) m8[j] = fmaxf(__uint_as_float(su[j]), __uint_as_float(su[8 + j]));
 #pragma unroll
-        for (int cc = 8; cc < kHalfS; cc += 8)
+        for (int cc = 16; cc < kHalfS; cc += 16)
 #pragma unroll
-          for (int j = 0; j < 8; ++j) m8[j] = fmaxf(m8[j], __uint_as_float(su[cc + j]));
-        const float mh = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+          for (int j = 0; j < 8; ++j)
+            m8[j] = fmax3(m8[j], __uint_as_float(su[cc + j]), __uint_as_float(su[cc + 8 + j]));
+        const float mh = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
         float mo;
         if (!exchange(mh, mo)) { ok = false; break; }
         const float mt = fmaxf(mh, mo);
