@@ -293,3 +293,46 @@ def test_layer_from_host_buffers_matches_device_path(fz, shape):
     fz.focus_layer_fwd_host(p, host, dbuf, ws)
     assert fz.focus_check_errors(ws) == 0
     assert torch.equal(host["O"], O_dev.cpu())
+
+
+def test_attention_at_the_largest_supported_length(fz):
+    """n = FOCUS_MAX_N (2^20 tokens, the pages' 1M-token setting): 16 uniform
+    groups of ~65K tokens give group-pass units of up to ~512 key tiles.
+    Index bit-exact; O and LSE on sampled rows (window start, first far row of
+    each group, the smallest groups' rows, random rows); a bitwise re-run."""
+    import torch
+    B, H, H_kv, A, n, d, K, w = 1, 2, 1, 1, 1 << 20, 64, 16, 1024
+    rng = np.random.default_rng(2024)
+    Q = synth.round_bf16(rng.standard_normal((B, H, n, d), dtype=np.float32))
+    Kt = synth.round_bf16(rng.standard_normal((B, H_kv, n, d), dtype=np.float32))
+    V = synth.round_bf16(rng.standard_normal((B, H_kv, n, d), dtype=np.float32))
+    g = synth.draw_group_ids(2024, B, A, n, K, "uniform")
+    p = fz.make_params(B=B, H=H, H_kv=H_kv, n=n, d=d, D=64, d_g=32, K=K, A=A, w=w)
+    ws = _ws(fz, p)
+    Qd, Kd, Vd = to_dev(Q, "bf16"), to_dev(Kt, "bf16"), to_dev(V, "bf16")
+    idx = fz.focus_build_index(p, torch.from_numpy(g).cuda(), ws)
+    O = torch.empty_like(Qd)
+    lse = torch.empty((B, H, n), dtype=torch.float32, device="cuda")
+    fz.focus_attention_fwd(p, Qd, Kd, Vd, idx, O, lse, ws)
+    O2 = torch.empty_like(Qd)
+    fz.focus_attention_fwd(p, Qd, Kd, Vd, idx, O2, None, ws)
+    assert fz.focus_check_errors(ws) == 0
+    assert torch.equal(O, O2), "attention is not deterministic"
+    want_idx = ref.build_index(g, K, w)
+    items = ref.work_items(want_idx, fz.TILE_M)
+    _check_index(_index_np(fz, p, idx, ws), want_idx, items, ref.lpt_order(items, fz.TILE_N))
+    # the oracle scores every row against all 2^20 keys: keep the sample small
+    perm, offs, fs = want_idx["perm"][0, 0], want_idx["offsets"][0, 0], want_idx["farlen_slot"][0, 0]
+    first_far = []
+    for gi in range(K):
+        seg = np.arange(offs[gi], offs[gi + 1])
+        far = seg[fs[seg] > 0]
+        if len(far):
+            first_far.append(int(perm[far[0]]))
+    rows = np.array(sorted(set(range(64)) | set(range(w - 8, w + 8)) | set(first_far) | {n - 1} |
+                           set(int(v) for v in rng.integers(0, n, 32))), dtype=np.int64)
+    for hq in range(H):
+        Oh, Lh = ref.attention_rows(Q[:, hq:hq + 1], Kt, V, g, w, p.scale, rows, 1, row_block=64)
+        sel = torch.from_numpy(rows).cuda()
+        assert_close(to_host(O[0, hq, sel]), Oh[0, 0], "bf16", f"n=2^20 head {hq}")
+        assert_lse_close(lse[0, hq, sel].cpu().numpy(), Lh[0, 0], "bf16", f"n=2^20 head {hq}")
