@@ -26,11 +26,20 @@ What the oracle computes (fp64 throughout, no blocking or fusion):
                group-pass work list for a tile height BM.
   keep mask    pair (i, j) kept iff j <= i and (i - j < w or g_i == g_j).
   attention    exact softmax over the kept pairs only, S = scale * Q K^T.
+  top-k        the hard top-k variant ([FocusJA] 2.2, 3.3; [FocusKO] 2.3,
+               whose experiment uses K=4, k=2): each token belongs to its k
+               best groups, and a far pair is kept when the two tokens' group
+               sets intersect.  assign_topk,
+               build_index_topk (memberships sorted by (group, position)),
+               keep_mask_rows_topk and attention_rows_topk are the same
+               definitions written for k memberships.
 
 Readings where the pages are silent (each listed in the design notes):
   similarity = dot product; no projection bias; window strictly i - j < w;
   scale = 1/sqrt(d) by default; GQA head map kv = floor(h * H_kv / H);
-  each kept pair counted once (union of the local and the group rule).
+  each kept pair counted once (union of the local and the group rule);
+  top-k: the k best fp32 scores, lower index first among equal scores, and a
+  pair whose tokens share several groups is still one kept pair.
 
 Parity pins: every function here is checked by tests/test_oracle_pins.py
 against closed forms, brute force, special cases and invariants.
@@ -46,6 +55,8 @@ __all__ = [
     "kept_counts", "attention", "attention_rows", "attention_masked_rows",
     "dense_causal", "lse_merge", "attention_bruteforce", "attention_weights_rows",
     "kv_head", "assignment_of_head",
+    "assign_topk", "build_index_topk", "keep_mask_rows_topk", "attention_rows_topk",
+    "attention_bruteforce_topk",
 ]
 
 
@@ -318,4 +329,143 @@ def attention_bruteforce(q, k, v, g, w: int, scale: float):
         z = math.fsum(e)
         O.append([math.fsum(e[t] * float(v[j][c]) for t, j in enumerate(kept)) / z for c in range(d)])
         L.append(mx + math.log(z))
+    return O, L
+
+
+# ------------------------------------------------------------------ top-k ---
+
+def assign_topk(h, W, C, k: int, chunk: int = 4096):
+    """The k nearest centroids per token, best first.  [FocusJA] 2.2, 3.3 and
+    [FocusKO] 2.3 (hard top-k membership at inference).
+
+    h [B, n, D], W [A, d_g, D], C [A, K, d_g]  ->  gid [B, A, n, k] int32 (rank
+    order; among equal fp32 scores the lower index ranks first), margin
+    [B, A, n] fp64: the smallest gap between consecutive ranks 1..k+1 (the
+    gaps that decide the set and its order; +inf where there is none).
+    """
+    h = np.asarray(h)
+    W = _f64(W)
+    C = _f64(C)
+    B, n, D = h.shape
+    A, d_g, _ = W.shape
+    K = C.shape[1]
+    assert 1 <= k <= K
+    gid = np.empty((B, A, n, k), dtype=np.int32)
+    margin = np.full((B, A, n), np.inf)
+    for b in range(B):
+        for s in range(0, n, chunk):
+            hb = _f64(h[b, s:s + chunk])
+            for a in range(A):
+                sc = (hb @ W[a].T) @ C[a].T                      # [m, K] scores
+                sc32 = sc.astype(np.float32)
+                order = np.argsort(-sc32, axis=1, kind="stable")  # best first, ties by index
+                gid[b, a, s:s + chunk] = order[:, :k]
+                srt = np.take_along_axis(sc, order, axis=1)
+                last = min(k + 1, K)
+                if last > 1:
+                    margin[b, a, s:s + chunk] = np.min(srt[:, :last - 1] - srt[:, 1:last], axis=1)
+    return gid, margin
+
+
+def build_index_topk(gid, K: int, w: int):
+    """Membership index for top-k groups per (batch, assignment).  [FocusJA]
+    2.2: a token sits in each of its k groups, so each group's member list
+    holds every token with that group among its k.
+
+    gid [B, A, n, k].  Entry e = i * k + c is token i's c-th membership.
+    Returns arrays with leading dims [B, A]: counts [K], offsets [K+1],
+    perm [n*k] (sorted slot -> entry; slots of a group in increasing
+    position), rank [n*k] (entry -> slot), farlen_entry [n*k] and farlen_slot
+    [n*k] (members of the entry's group at positions j <= i - w), other [n*k]
+    (k = 2: the group of the slot's token other than the slot's own; -1 for
+    k = 1).  For k = 1 these are exactly build_index's arrays.
+    """
+    gid = np.asarray(gid)
+    B, A, n, k = gid.shape
+    m = n * k
+    counts = np.zeros((B, A, K), np.int32)
+    offsets = np.zeros((B, A, K + 1), np.int32)
+    perm = np.zeros((B, A, m), np.int32)
+    rank = np.zeros((B, A, m), np.int32)
+    far_e = np.zeros((B, A, m), np.int32)
+    far_s = np.zeros((B, A, m), np.int32)
+    other = np.full((B, A, m), -1, np.int32)
+    for b in range(B):
+        for a in range(A):
+            ge = gid[b, a].reshape(m).astype(np.int64)        # group of each entry
+            assert ge.min() >= 0 and ge.max() < K, "group id out of range"
+            for i in range(n):
+                assert len(set(gid[b, a, i].tolist())) == k, "a token's k groups must differ"
+            counts[b, a] = np.bincount(ge, minlength=K)
+            offsets[b, a, 1:] = np.cumsum(counts[b, a])
+            p = np.argsort(ge, kind="stable")                 # by group, then entry = (position, choice)
+            perm[b, a] = p
+            rank[b, a, p] = np.arange(m)
+            pos = p // k
+            for g in range(K):
+                lo, hi = offsets[b, a, g], offsets[b, a, g + 1]
+                if hi == lo:
+                    continue
+                members = pos[lo:hi]                          # increasing positions
+                fl = np.searchsorted(members, members - w + 1, side="left")
+                far_s[b, a, lo:hi] = fl
+                far_e[b, a, p[lo:hi]] = fl
+            if k == 2:
+                other[b, a] = ge[p ^ 1]                       # the token's other membership
+    return dict(counts=counts, offsets=offsets, perm=perm, rank=rank,
+                farlen_entry=far_e, farlen_slot=far_s, other=other)
+
+
+def keep_mask_rows_topk(G, w: int, rows):
+    """Top-k keep rule for query rows `rows`: j <= i and (i - j < w or the
+    group sets of i and j intersect).  G [n, k]."""
+    G = np.asarray(G)
+    rows = np.asarray(rows, dtype=np.int64)
+    n, k = G.shape
+    j = np.arange(n)[None, :]
+    i = rows[:, None]
+    shared = np.zeros((len(rows), n), dtype=bool)
+    for c in range(k):
+        for c2 in range(k):
+            shared |= G[rows, c][:, None] == G[None, :, c2]
+    return (j <= i) & (((i - j) < w) | shared)
+
+
+def attention_rows_topk(Q, K, V, gid, w: int, scale: float, rows, A: int, row_block: int = 256):
+    """Top-k Focus attention for selected query rows of every (b, h):
+    Q [B,H,n,d], K/V [B,H_kv,n,d], gid [B,A,n,k].  O [B,H,R,d], LSE [B,H,R]."""
+    B, H, n, d = Q.shape
+    H_kv = K.shape[1]
+    rows = np.asarray(rows, dtype=np.int64)
+    O = np.empty((B, H, len(rows), d))
+    L = np.empty((B, H, len(rows)))
+    for b in range(B):
+        for hq in range(H):
+            kv = kv_head(hq, H, H_kv)
+            a = assignment_of_head(hq, H, H_kv, A)
+            Kf, Vf = _f64(K[b, kv]), _f64(V[b, kv])
+            for s in range(0, len(rows), row_block):
+                r = rows[s:s + row_block]
+                M = keep_mask_rows_topk(gid[b, a], w, r)
+                O[b, hq, s:s + row_block], L[b, hq, s:s + row_block] = \
+                    attention_masked_rows(Q[b, hq], Kf, Vf, M, r, scale)
+    return O, L
+
+
+def attention_bruteforce_topk(q, k, v, G, w: int, scale: float):
+    """Scalar loops for one head: kept set per row from the window and set
+    intersection, math.fsum softmax.  q, k, v [n, d], G [n, kk] -> O, LSE."""
+    n, d = q.shape
+    O = np.zeros((n, d))
+    L = np.zeros(n)
+    for i in range(n):
+        gi = set(int(x) for x in G[i])
+        kept = [j for j in range(i + 1) if i - j < w or gi & set(int(x) for x in G[j])]
+        s = [scale * math.fsum(float(q[i, t]) * float(k[j, t]) for t in range(d)) for j in kept]
+        mx = max(s)
+        e = [math.exp(x - mx) for x in s]
+        tot = math.fsum(e)
+        for t in range(d):
+            O[i, t] = math.fsum(e[r] * float(v[kept[r], t]) for r in range(len(kept))) / tot
+        L[i] = mx + math.log(tot)
     return O, L

@@ -337,6 +337,194 @@ def test_row_sampling_matches_full():
     np.testing.assert_allclose(Ls, L[:, :, rows], atol=1e-14)
 
 
+# ------------------------------------------------------------------ top-k ---
+
+def _golden_top2():
+    gd = _parse_golden("keep_rule_top2_n8.txt")
+    n = gd["n"][0]
+    G = np.array([gd["groups %d" % i] for i in range(n)], np.int32)
+    return gd, G
+
+
+def test_golden_top2_keep_rule_index_and_softmax():
+    gd, G = _golden_top2()
+    n, w, K = gd["n"][0], gd["w"][0], gd["K"][0]
+    M = ref.keep_mask_rows_topk(G, w, np.arange(n))
+    for i in range(n):
+        assert list(np.nonzero(M[i])[0]) == gd["kept"][i], i
+    idx = ref.build_index_topk(G[None, None], K, w)
+    for key in ("counts", "offsets", "perm", "rank", "farlen_slot", "farlen_entry", "other"):
+        assert idx[key][0, 0].tolist() == gd[key], key
+    far_total = int(idx["farlen_slot"].sum())
+    assert far_total == gd["far_total"][0]
+    ii, jj = np.nonzero(M)
+    assert int(np.sum(ii - jj >= w)) == gd["far_kept"][0] == far_total - gd["far_both"][0]
+    Q = np.zeros((1, 1, n, 2))
+    Kt = np.random.default_rng(0).standard_normal((1, 1, n, 2))
+    V = np.stack([np.arange(n, dtype=np.float64), np.ones(n)], axis=1)[None, None]
+    O, L = ref.attention_rows_topk(Q, Kt, V, G[None, None], w, 0.7, np.arange(n), 1)
+    for i in range(n):
+        np.testing.assert_allclose(O[0, 0, i], gd["O"][i], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(L[0, 0], np.log(np.array(gd["lse_count"], float)), atol=1e-14)
+
+
+def test_assign_topk_closed_form_order_and_ties():
+    # W = I, C = scaled basis / duplicates: the scores are known coordinates.
+    W = np.eye(4)[None]
+    C = np.array([[1, 0, 0, 0], [0, 1, 0, 0], [0, 0, 1, 0], [0, 1, 0, 0], [0, 0, 0, 1]], float)[None]
+    h = np.array([[[4, 3, 2, 1],       # scores [4,3,2,3,1]: top2 0, then 1 (tie 1/3 -> 1)
+                   [1, 2, 3, 4],       # [1,2,3,2,4]: 4, 2
+                   [0, 5, 5, 0],       # [0,5,5,5,0]: 1, 2 (three-way tie -> lowest two)
+                   [-1, -2, -3, -4]]], float)  # [-1,-2,-3,-2,-4]: 0, 1
+    gid, margin = ref.assign_topk(h, W, C, 2)
+    assert gid[0, 0].tolist() == [[0, 1], [4, 2], [1, 2], [0, 1]]
+    # smallest gap among ranks 1-2 and 2-3
+    np.testing.assert_allclose(margin[0, 0], [0.0, 1.0, 0.0, 0.0], atol=1e-15)
+    gid3, _ = ref.assign_topk(h, W, C, 3)
+    assert gid3[0, 0].tolist() == [[0, 1, 3], [4, 2, 1], [1, 2, 3], [0, 1, 3]]
+
+
+def test_assign_topk_bruteforce_and_k1_is_assign():
+    rng = np.random.default_rng(21)
+    B, n, D, A, dg, K = 2, 11, 6, 2, 4, 5
+    h = rng.standard_normal((B, n, D))
+    W = rng.standard_normal((A, dg, D))
+    C = rng.standard_normal((A, K, dg))
+    gid, margin = ref.assign_topk(h, W, C, 2)
+    for b in range(B):
+        for a in range(A):
+            for i in range(n):
+                p = [math.fsum(W[a, r, c] * h[b, i, c] for c in range(D)) for r in range(dg)]
+                s = [math.fsum(p[r] * C[a, k, r] for r in range(dg)) for k in range(K)]
+                first = max(range(K), key=lambda k: (s[k], -k))
+                second = max((k for k in range(K) if k != first), key=lambda k: (s[k], -k))
+                assert gid[b, a, i].tolist() == [first, second]
+                srt = sorted(s, reverse=True)
+                assert abs(margin[b, a, i] - min(srt[0] - srt[1], srt[1] - srt[2])) < 1e-12
+    g1, m1 = ref.assign(h, W, C)
+    gk, mk = ref.assign_topk(h, W, C, 1)
+    assert np.array_equal(gk[..., 0], g1)
+    np.testing.assert_allclose(mk, m1, atol=1e-12)
+
+
+@pytest.mark.parametrize("K,n,w", [(4, 200, 9), (7, 301, 1), (2, 64, 64), (16, 257, 16)])
+def test_index_topk_bruteforce_and_k1_is_index(K, n, w):
+    rng = np.random.default_rng(K * 1000 + n)
+    G = np.stack([rng.permutation(K)[:2] for _ in range(n)]).astype(np.int32)
+    idx = ref.build_index_topk(G[None, None], K, w)
+    slot = 0
+    for g in range(K):
+        members = [(i, c) for i in range(n) for c in range(2) if G[i, c] == g]
+        assert idx["counts"][0, 0, g] == len(members)
+        assert idx["offsets"][0, 0, g] == slot
+        for t, (i, c) in enumerate(members):
+            s = slot + t
+            assert idx["perm"][0, 0, s] == 2 * i + c
+            assert idx["rank"][0, 0, 2 * i + c] == s
+            far = sum(1 for (j, _) in members if j <= i - w)
+            assert idx["farlen_slot"][0, 0, s] == far
+            assert idx["farlen_entry"][0, 0, 2 * i + c] == far
+            assert idx["other"][0, 0, s] == G[i, 1 - c]
+        slot += len(members)
+    assert slot == 2 * n
+    g1 = synth.draw_group_ids(K + n, 1, 1, n, K, "uniform")
+    a = ref.build_index(g1, K, w)
+    b = ref.build_index_topk(g1[..., None], K, w)
+    for key, key2 in (("counts", "counts"), ("offsets", "offsets"), ("perm", "perm"), ("rank", "rank"),
+                      ("farlen_tok", "farlen_entry"), ("farlen_slot", "farlen_slot")):
+        assert np.array_equal(a[key], b[key2]), key
+    assert np.all(b["other"] == -1)
+
+
+@pytest.mark.parametrize("K,n,w", [(4, 160, 5), (6, 211, 12), (3, 90, 1)])
+def test_topk_far_count_once_per_pair(K, n, w):
+    # Far pairs kept by the mask = per-group far pairs (sum of farlen) minus
+    # the pairs whose tokens share both groups, which every group list of the
+    # two holds.  Also: keeping a shared-both pair only in the group that is
+    # not larger than the slot's other group counts every far pair once.
+    rng = np.random.default_rng(n + w)
+    G = np.stack([rng.permutation(K)[:2] for _ in range(n)]).astype(np.int32)
+    M = ref.keep_mask_rows_topk(G, w, np.arange(n))
+    ii, jj = np.nonzero(M)
+    far_kept = int(np.sum(ii - jj >= w))
+    S = [frozenset(r.tolist()) for r in G]
+    both = sum(1 for i in range(n) for j in range(max(0, i - w + 1)) if S[i] == S[j])
+    idx = ref.build_index_topk(G[None, None], K, w)
+    assert far_kept == int(idx["farlen_slot"].sum()) - both
+    perm, other, off = idx["perm"][0, 0], idx["other"][0, 0], idx["offsets"][0, 0]
+    dedup = 0
+    for g in range(K):
+        for s in range(off[g], off[g + 1]):
+            for t in range(off[g], off[g] + idx["farlen_slot"][0, 0, s]):
+                if not (other[t] == other[s] and other[s] < g):
+                    dedup += 1
+    assert dedup == far_kept
+
+
+def test_topk_reduces_to_dense_and_to_top1():
+    rng = np.random.default_rng(22)
+    B, H, Hkv, n, d = 1, 4, 2, 83, 8
+    Q = rng.standard_normal((B, H, n, d))
+    Kt = rng.standard_normal((B, Hkv, n, d))
+    V = rng.standard_normal((B, Hkv, n, d))
+    rows = np.arange(n)
+    # K = 2, k = 2: every token is in both groups -> dense causal
+    G = np.stack([rng.permutation(2) for _ in range(n)]).astype(np.int32)[None, None]
+    O, L = ref.attention_rows_topk(Q, Kt, V, G, 3, 0.3, rows, 1)
+    np.testing.assert_allclose(O, _sdpa_causal(Q, Kt, V, 0.3), atol=1e-12)
+    # window >= n -> dense causal whatever the groups
+    G = np.stack([rng.permutation(9)[:2] for _ in range(n)]).astype(np.int32)[None, None]
+    O, L = ref.attention_rows_topk(Q, Kt, V, G, n, 0.3, rows, 1)
+    np.testing.assert_allclose(O, _sdpa_causal(Q, Kt, V, 0.3), atol=1e-12)
+    # k = 1 is the top-1 path
+    g = synth.draw_group_ids(5, B, 2, n, 6, "uniform")
+    O1, L1 = ref.attention_rows(Q, Kt, V, g, 7, 0.3, rows, 2)
+    O2, L2 = ref.attention_rows_topk(Q, Kt, V, g[..., None], 7, 0.3, rows, 2)
+    np.testing.assert_allclose(O2, O1, atol=1e-13)
+    np.testing.assert_allclose(L2, L1, atol=1e-13)
+
+
+@pytest.mark.parametrize("n,w,K", [(40, 3, 4), (33, 1, 6), (25, 30, 3), (48, 6, 5)])
+def test_topk_bruteforce_small(n, w, K):
+    rng = np.random.default_rng(n * 31 + w)
+    d = 5
+    Q, Kt, V = (rng.standard_normal((1, 1, n, d)) for _ in range(3))
+    G = np.stack([rng.permutation(K)[:2] for _ in range(n)]).astype(np.int32)
+    O, L = ref.attention_rows_topk(Q, Kt, V, G[None, None], w, 0.45, np.arange(n), 1)
+    Ob, Lb = ref.attention_bruteforce_topk(Q[0, 0], Kt[0, 0], V[0, 0], G, w, 0.45)
+    np.testing.assert_allclose(O[0, 0], Ob, atol=1e-12)
+    np.testing.assert_allclose(L[0, 0], Lb, atol=1e-12)
+
+
+def test_topk_pins_catch_planted_mistakes():
+    """Plausible slips in the top-k rule each break the hand-worked example."""
+    gd, G = _golden_top2()
+    n, w = gd["n"][0], gd["w"][0]
+    rows = np.arange(n)
+
+    def first_only(GG, ww, rr):            # membership read as the first choice alone
+        return ref.keep_mask_rows(GG[:, 0], ww, rr)
+
+    def both_equal(GG, ww, rr):            # sets must be equal, not just meet
+        S = np.sort(GG, axis=1)
+        jj = np.arange(len(GG))[None, :]
+        ii = np.asarray(rr)[:, None]
+        same = np.all(S[rr][:, None, :] == S[None, :, :], axis=2)
+        return (jj <= ii) & (((ii - jj) < ww) | same)
+
+    def same_rank(GG, ww, rr):             # choices compared rank by rank only
+        jj = np.arange(len(GG))[None, :]
+        ii = np.asarray(rr)[:, None]
+        sh = np.zeros((len(rr), len(GG)), bool)
+        for c in range(GG.shape[1]):
+            sh |= GG[rr, c][:, None] == GG[None, :, c]
+        return (jj <= ii) & (((ii - jj) < ww) | sh)
+
+    for bad in (first_only, both_equal, same_rank):
+        M = bad(G, w, rows)
+        assert any(list(np.nonzero(M[i])[0]) != gd["kept"][i] for i in range(n)), bad.__name__
+
+
 # ------------------------------------------------ planted oracle mistakes ---
 
 def test_pins_catch_planted_mistakes(monkeypatch):
