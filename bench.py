@@ -17,6 +17,11 @@ roofline     the dominant attention kernel's achieved TFLOP/s (its algorithmic
              sustained bf16 tensor peak.
 cpu_baseline the fp64 oracle timed on the host cores on a bounded row sample.
 
+--topk 2 runs the top-2 membership layer instead (focus_assign_topk ->
+focus_build_index_topk -> focus_attention_topk_fwd; each token in its two
+best groups, a far pair kept when the tokens' group sets meet), by default
+with the pages' K = 4 (--K).  Kept pairs are counted once.
+
 --impl reference times the oracle alone (the comparison arm of this build).
 Under torchrun (N > 1) every rank runs its own replica of the workload (weak
 scaling); there is no data-path collective.
@@ -176,6 +181,36 @@ def oracle_sample(wl, x, rows_per_head: int, heads, seed: int):
     frac = len(heads) * rows_per_head / (wl.H * wl.n)
     secs = (t1 - t0) * frac + t_attn
     desc = (f"oracle fp64: assign + index over all {wl.B * wl.n} tokens (time prorated by the "
+            f"sampled fraction {frac:.2e}) and attention for {rows_per_head} seeded rows of heads "
+            f"{list(heads)}")
+    return flops, secs, desc
+
+
+def oracle_sample_topk(wl, x, rows_per_head: int, heads, seed: int, k: int):
+    """oracle_sample for top-k membership (assign_topk, build_index_topk,
+    attention_rows_topk).  Returns (kept-pair FLOPs of the sample, seconds,
+    description)."""
+    import oracle.focus_ref as ref
+    t0 = time.perf_counter()
+    gid, _ = ref.assign_topk(x["h"], x["W"], x["C"], k)
+    ref.build_index_topk(gid, wl.K, max(wl.w, 1))
+    t1 = time.perf_counter()
+    rng = np.random.default_rng(seed)
+    flops = 0
+    t_attn = 0.0
+    for hq in heads:
+        kv = ref.kv_head(hq, wl.H, wl.H_kv)
+        a = ref.assignment_of_head(hq, wl.H, wl.H_kv, wl.A)
+        rows = np.sort(rng.choice(wl.n, size=min(rows_per_head, wl.n), replace=False))
+        s = time.perf_counter()
+        ref.attention_rows_topk(x["Q"][:, hq:hq + 1], x["K"][:, kv:kv + 1], x["V"][:, kv:kv + 1],
+                                gid[:, a:a + 1], wl.w, wl.scale, rows, 1, row_block=128)
+        t_attn += time.perf_counter() - s
+        for b in range(wl.B):
+            flops += 4 * wl.d * int(ref.keep_mask_rows_topk(gid[b, a], max(wl.w, 1), rows).sum())
+    frac = len(heads) * rows_per_head / (wl.H * wl.n)
+    secs = (t1 - t0) * frac + t_attn
+    desc = (f"oracle fp64, top-{k}: assign + index over all {wl.B * wl.n} tokens (time prorated by the "
             f"sampled fraction {frac:.2e}) and attention for {rows_per_head} seeded rows of heads "
             f"{list(heads)}")
     return flops, secs, desc
@@ -407,6 +442,179 @@ def run_ours(args, wl, world, rank, local):
         dist.destroy_process_group()
 
 
+def run_ours_topk(args, wl, world, rank, local):
+    """The top-k layer: same timing rules as run_ours (L2 flushed before each
+    timed step, CUDA events on the launching stream, clocks sampled)."""
+    import torch
+    from learned_group_sparse_focus_gb300 import synth
+    from learned_group_sparse_focus_gb300 import focus as fz
+
+    k = args.topk
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    x = synth.draw(wl)
+
+    def dev(a):
+        if wl.dtype == "bf16":
+            return torch.from_numpy(synth.bf16_bits(a)).view(torch.bfloat16).cuda()
+        return torch.from_numpy(a).cuda()
+
+    names = ("h", "W", "C", "Q", "K", "V")
+    d = {n_: dev(x[n_]) for n_ in names}
+    p = fz.params_from_workload(wl)
+    ws = fz.alloc_workspace_topk(p, k)
+    gid = torch.empty((wl.B, wl.A, wl.n, k), dtype=torch.int32, device="cuda")
+    O = torch.empty_like(d["Q"])
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    fz.focus_assign_topk(p, k, d["h"], d["W"], d["C"], gid, ws)
+    idx = fz.focus_build_index_topk(p, k, gid, ws)
+    fz.focus_attention_topk_fwd(p, d["Q"], d["K"], d["V"], idx, O, None, ws)
+    st = fz.focus_check_errors(ws)
+    if st != 0:
+        raise RuntimeError(f"device error status {st}")
+    # far pairs per assignment: entry far keys (a key sharing both groups
+    # counted twice) minus pair far keys (those keys once more)
+    ent = fz.index_views(p, idx.entry, ws, n=wl.n * k)
+    far_e = ent["farlen_tok"].to(torch.int64).sum(dim=2).cpu().numpy()       # [B, A]
+    if k == 2:
+        pv = fz.index_views(p, idx.pair, ws, K=wl.K * (wl.K - 1) // 2)
+        far_p = pv["farlen_tok"].to(torch.int64).sum(dim=2).cpu().numpy()
+    else:
+        far_p = np.zeros_like(far_e)
+    heads_of = [0 if wl.A == 1 else (hq * wl.H_kv) // wl.H for hq in range(wl.H)]
+    far_pairs = sum(int(far_e[:, a].sum() - far_p[:, a].sum()) for a in heads_of)
+    ent_pairs = sum(int(far_e[:, a].sum()) for a in heads_of)
+    pair_pairs = sum(int(far_p[:, a].sum()) for a in heads_of)
+    win_pairs = int(np.minimum(np.arange(wl.n) + 1, max(wl.w, 1)).sum()) * wl.B * wl.H
+    kept = win_pairs + far_pairs
+    f_attn = 4 * wl.d * kept
+
+    def step(evs):
+        flush.zero_()
+        evs[0].record()
+        fz.focus_assign_topk(p, k, d["h"], d["W"], d["C"], gid, ws)
+        evs[1].record()
+        ix = fz.focus_build_index_topk(p, k, gid, ws)
+        evs[2].record()
+        fz.focus_attention_topk_fwd_timed(p, d["Q"], d["K"], d["V"], ix, O, None, ws, evs[3:8])
+
+    def new_events(cnt):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(cnt)]
+        for row in evs:
+            for e in row:
+                e.record()
+        return evs
+
+    warm = new_events(1)[0]
+    for _ in range(args.warmup):
+        step(warm)
+    evs = new_events(args.steps)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(int(os.environ.get("FOCUS_NVSMI_INDEX", local))) as clk:
+        for s_ in range(args.steps):
+            step(evs[s_])
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+    st = fz.focus_check_errors(ws)
+    if st != 0:
+        raise RuntimeError(f"device error status {st}")
+
+    def mean_ms(i, j):
+        return statistics.mean(evs[s_][i].elapsed_time(evs[s_][j]) for s_ in range(args.steps))
+
+    t = {"assign": mean_ms(0, 1), "index": mean_ms(1, 2), "permute_kv": mean_ms(3, 4),
+         "entry_group_pass": mean_ms(4, 5), "pair_pass_and_merge": mean_ms(5, 6),
+         "local_pass": mean_ms(6, 7)}
+    t_step = mean_ms(0, 7)
+
+    # dense comparator
+    dws = fz.alloc_workspace(p)
+    for _ in range(3):
+        fz.focus_dense_causal_fwd(p, d["Q"], d["K"], d["V"], O, None, dws)
+    dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(5)]
+    for a0, a1 in dev_ev:
+        flush.zero_()
+        a0.record()
+        fz.focus_dense_causal_fwd(p, d["Q"], d["K"], d["V"], O, None, dws)
+        a1.record()
+    torch.cuda.synchronize()
+    t_dense = statistics.mean(a0.elapsed_time(a1) for a0, a1 in dev_ev)
+    del dws
+
+    # end to end: pinned host inputs in, the three calls, O back to pinned host
+    host = {n_: d[n_].cpu().pin_memory() for n_ in names}
+    hO = torch.empty(O.shape, dtype=O.dtype).pin_memory()
+    h2d = sum(host[n_].numel() * host[n_].element_size() for n_ in names)
+    d2h = hO.numel() * hO.element_size()
+
+    def e2e_step():
+        for n_ in names:
+            d[n_].copy_(host[n_], non_blocking=True)
+        fz.focus_assign_topk(p, k, d["h"], d["W"], d["C"], gid, ws)
+        ix = fz.focus_build_index_topk(p, k, gid, ws)
+        fz.focus_attention_topk_fwd(p, d["Q"], d["K"], d["V"], ix, O, None, ws)
+        hO.copy_(O, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(5)]
+    for a0, a1 in e2e_ev:
+        flush.zero_()
+        a0.record()
+        e2e_step()
+        a1.record()
+    torch.cuda.synchronize()
+    t_e2e = statistics.mean(a0.elapsed_time(a1) for a0, a1 in e2e_ev)
+
+    keys = list(t)
+    red = max_over_ranks([t_step, t_dense, t_e2e] + [t[kk] for kk in keys], dist, "cuda")
+    t_step, t_dense, t_e2e = red[:3]
+    t = dict(zip(keys, red[3:]))
+    peaks, peak_kind = load_peaks()
+    peak_tc = float(peaks["bf16_tflops_sustained"])
+    f_ent = 4 * wl.d * ent_pairs
+    achieved = f_ent / (t["entry_group_pass"] * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": job_tflops(world, f_attn, t_step), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": f"synthetic (seeded N(0,1) Q/K/V/h, {wl.groups} hidden states), top-{k} membership",
+        "config": {"workload": wl.name, "topk": k,
+                   **{kk: getattr(wl, kk) for kk in ("B", "H", "H_kv", "n", "d", "D", "d_g", "K", "w", "A")},
+                   "kept_pairs": kept, "kept_density_vs_causal": kept / (wl.B * wl.H * wl.n * (wl.n + 1) / 2),
+                   "far_pairs_entry_pass": ent_pairs, "far_pairs_pair_pass": pair_pairs,
+                   "l2": "flushed (256 MB write) before every timed step; flush not timed",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "ms_breakdown": t, "ms_dense_causal": t_dense, "speedup_vs_dense": t_dense / t_step,
+        "roofline": {"bound": "tensor", "kernel": "attn_tc_group_pass (entries)", "achieved": achieved,
+                     "peak": peak_tc, "unit": "TFLOP/s", "frac": achieved / peak_tc, "traffic": None,
+                     "peak_source": f"{peak_kind} bf16_tflops_sustained"},
+        "e2e": {"value": job_tflops(world, f_attn, t_e2e), "unit": UNIT, "ms_per_step": t_e2e,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "call": "pinned host copies + focus_assign_topk, focus_build_index_topk, focus_attention_topk_fwd"},
+        "gpu_launches": (1 + (12 if k == 2 else 5) + (6 if k == 2 else 3)) * args.steps,
+    }
+    if rank == 0:
+        line["clocks"] = clk.summary()
+        if world == 1 and not args.no_cpu_baseline:
+            heads = sorted({0, wl.H - 1})
+            f, sec, desc = oracle_sample_topk(wl, x, max(64, args.cpu_rows // 8), heads, seed=7, k=k)
+            line["cpu_baseline"] = {"value": f / sec / 1e12, "unit": UNIT, "cores": cpu_cores(),
+                                    "kind": "oracle", "sample": desc, "seconds": sec}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -417,14 +625,20 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=6144)
     ap.add_argument("--ref-rows", type=int, default=1024)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--topk", type=int, default=1, choices=[1, 2],
+                    help="groups per token; 2 runs the top-2 membership layer")
+    ap.add_argument("--K", type=int, default=None, help="centroids (default: 4 with --topk 2)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     from learned_group_sparse_focus_gb300 import synth
-    wl = synth.WORKLOADS[args.workload]
+    K = args.K if args.K is not None else (4 if args.topk == 2 else None)
+    wl = synth.WORKLOADS[args.workload] if K is None else synth.workload(args.workload, K=K)
     world, rank, local = dist_env()
     if args.impl == "reference":
         run_reference(args, wl, world, rank)
+    elif args.topk > 1:
+        run_ours_topk(args, wl, world, rank, local)
     else:
         run_ours(args, wl, world, rank, local)
 

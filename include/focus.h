@@ -53,7 +53,7 @@
 extern "C" {
 #endif
 
-#define FOCUS_ABI_VERSION 1
+#define FOCUS_ABI_VERSION 2   /* 2: adds the top-k membership calls */
 
 #if defined(__GNUC__)
 #define FOCUS_API __attribute__((visibility("default")))
@@ -230,6 +230,88 @@ FOCUS_API focus_status_t focus_layer_fwd_host(const focus_params_t* p,
                                     void* d_h, void* d_W, void* d_C, void* d_Q, void* d_K,
                                     void* d_V, void* d_O, int32_t* d_gid,
                                     void* ws, size_t ws_bytes, void* stream);
+
+/* ----------------------------------------------------- top-k membership ---
+ * "Focus: Learning Which Attention Pairs Matter" 2.2 (each token is
+ * hard-assigned to its top-k groups at inference) and 3.3; "Why Attend to
+ * Everything? Focus is the Key" 2.3 (K = 4, k = 2 in its experiment).  With k
+ * groups per token, row i attends to key j iff j <= i and (i - j < w or the
+ * group sets of i and j intersect); softmax is exact over that set and a key
+ * that shares several groups with the query still counts once.  k is 1 or 2;
+ * k = 1 is the top-1 operation above.  Memberships are "entries": entry
+ * e = i * k + c is token i's c-th best group.
+ *
+ * Index layout for k memberships, all device pointers into ws, arrays
+ * indexed [(b * A + a) * len + x]:
+ *   entry      focus_index_t over the n*k entries: counts/offsets per group,
+ *              perm (sorted slot -> entry e), rank (entry -> slot),
+ *              farlen_tok (per ENTRY: members of that entry's group at token
+ *              positions j <= i - w), farlen_slot (the same per slot), and the
+ *              group-pass work list; every length n there reads n*k.
+ *   pair       k = 2 only: focus_index_t over tokens sorted by their group
+ *              pair {a, b} (K (K - 1) / 2 pair ids, numbered (0,1), (0,2), ...,
+ *              (0,K-1), (1,2), ...).  Its far members are the far keys that
+ *              share BOTH groups with the query, which the entry pass counts
+ *              twice; the attention call subtracts them once.
+ *   pair_gid   k = 2: [B*A][n] pair id per token.
+ *   far_tok    [B*A][n] 1 if token i has any far key, else 0.
+ * k = 2 needs K (K - 1) / 2 <= FOCUS_MAX_K (K <= 91), else
+ * FOCUS_ERR_UNSUPPORTED. */
+typedef struct {
+  focus_index_t entry;
+  focus_index_t pair;
+  int32_t* pair_gid;
+  int32_t* far_tok;
+  int32_t k;
+  int32_t pad;
+} focus_index_topk_t;
+
+/* Bytes of device workspace the top-k calls need for problem p and k (0 if p
+ * or k is invalid or unsupported).  Pure host arithmetic.  The layout differs
+ * from focus_workspace_bytes'; a top-k workspace serves only top-k calls. */
+FOCUS_API size_t focus_workspace_bytes_topk(const focus_params_t* p, int32_t k);
+
+/* Top-k assignment: as focus_assign, with the k best centroids per token.
+ *   gid [B, A, n, k] int32 output: gid[b,a,i,0] the best centroid, [.., 1] the
+ *   runner-up; among equal fp32 scores the lower index ranks first.
+ * Shapes, dtypes and errors as focus_assign; ws is a top-k workspace. */
+FOCUS_API focus_status_t focus_assign_topk(const focus_params_t* p, int32_t k, const void* h,
+                                           const void* W, const void* C, int32_t* gid, void* ws,
+                                           size_t ws_bytes, void* stream);
+
+/* Top-k index: the entry index (stable counting sort of the n*k entries by
+ * (group, entry), i.e. by (group, position)), farlen per entry and slot and
+ * the work list; for k = 2 also the pair ids, the pair index and far_tok.
+ * gid [B, A, n, k] int32 device input; a token's k ids must differ.  A gid
+ * outside [0, K), or two equal ids of one token, is clamped or refiled for
+ * safety and flagged as FOCUS_ERR_BAD_GROUP_ID in the device error word.
+ * *idx_out (host struct) receives device pointers into ws, valid until ws is
+ * reused by another index build. */
+FOCUS_API focus_status_t focus_build_index_topk(const focus_params_t* p, int32_t k,
+                                                const int32_t* gid, focus_index_topk_t* idx_out,
+                                                void* ws, size_t ws_bytes, void* stream);
+
+/* Top-k Focus attention over the kept pairs.  Tensors, d, lse_opt and errors
+ * as focus_attention_fwd; idx from focus_build_index_topk with the same p and
+ * ws.  Runs: the group pass over entries (one partial per entry), for k = 2 a
+ * group pass over pair ids and a merge that combines each token's two entry
+ * partials minus its pair partial by log-sum-exp, then the local pass that
+ * merges the far partial with the window keys. */
+FOCUS_API focus_status_t focus_attention_topk_fwd(const focus_params_t* p, const void* Q,
+                                                  const void* K, const void* V,
+                                                  const focus_index_topk_t* idx, void* O,
+                                                  float* lse_opt, void* ws, size_t ws_bytes,
+                                                  void* stream);
+
+/* focus_attention_topk_fwd recording five caller-created CUDA events on
+ * `stream` (NULL = none): events[0] before the entry K/V sort copy, [1] before
+ * the entry group pass, [2] after it, [3] before the local pass (after the
+ * pair pass and the merge), [4] after the local pass. */
+FOCUS_API focus_status_t focus_attention_topk_fwd_timed(const focus_params_t* p, const void* Q,
+                                                        const void* K, const void* V,
+                                                        const focus_index_topk_t* idx, void* O,
+                                                        float* lse_opt, void* ws, size_t ws_bytes,
+                                                        void* stream, void* const* events);
 
 /* Synchronises `stream`, reads and clears the device error word in ws.
  * Returns FOCUS_OK, FOCUS_ERR_BAD_GROUP_ID, FOCUS_ERR_TIMEOUT or FOCUS_ERR_CUDA. */

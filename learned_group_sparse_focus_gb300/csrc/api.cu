@@ -163,9 +163,152 @@ AttnArgs attn_args(const focus_params_t* p, const void* Q, const void* K, const 
   a.n = p->n;
   a.A = p->A;
   a.w = p->w > 1 ? p->w : 1;
+  a.m = p->n;
+  a.kshift = 0;
   a.scale_log2 = p->scale * 1.4426950408889634f;
   a.err = at<int>(ws, L.err);
   return a;
+}
+
+// ----------------------------------------------- top-k workspace layout ---
+// One index (regions of a counting sort over m items into K groups).
+struct IndexRegions {
+  size_t segcnt, counts, offsets, tile_base, perm, rank, far_tok, far_slot, items, cost, order,
+      n_items;
+  int nseg, max_items;
+};
+
+struct LayoutTopk {
+  size_t err, pair_gid, far_any, Ks, Vs, O_e, lse_e, O_p, lse_p, O_far, lse_far, total;
+  IndexRegions ent, pair;
+  int k, m, Kp;
+};
+
+int pair_count(int K) { return K * (K - 1) / 2; }
+
+bool topk_ok(const focus_params_t* p, int k) {
+  if (!params_ok(p) || !(k == 1 || k == 2)) return false;
+  if (k == 2 && (p->K < 2 || pair_count(p->K) > FOCUS_MAX_K)) return false;
+  return true;
+}
+
+LayoutTopk layout_topk(const focus_params_t* p, int k) {
+  LayoutTopk L{};
+  const size_t P = static_cast<size_t>(p->B) * p->A;
+  const size_t n = p->n;
+  L.k = k;
+  L.m = p->n * k;
+  L.Kp = k == 2 ? pair_count(p->K) : 0;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align_up(o + bytes);
+    return at;
+  };
+  auto take_index = [&](IndexRegions& R, size_t m, size_t K) {
+    R.nseg = static_cast<int>((m + kIndexSeg - 1) / kIndexSeg);
+    R.max_items = static_cast<int>(P * ((m + kTileM - 1) / kTileM + (K < m ? K : m)));
+    R.segcnt = take(P * R.nseg * K * 4);
+    R.counts = take(P * K * 4);
+    R.offsets = take(P * (K + 1) * 4);
+    R.tile_base = take(P * (K + 1) * 4);
+    R.perm = take(P * m * 4);
+    R.rank = take(P * m * 4);
+    R.far_tok = take(P * m * 4);
+    R.far_slot = take(P * m * 4);
+    R.items = take(static_cast<size_t>(R.max_items) * sizeof(focus_item_t));
+    R.cost = take(static_cast<size_t>(R.max_items) * 4);
+    R.order = take(static_cast<size_t>(R.max_items) * 4);
+    R.n_items = take(4);
+  };
+  L.err = take(kAlign);
+  take_index(L.ent, static_cast<size_t>(L.m), p->K);
+  if (k == 2) {
+    take_index(L.pair, n, L.Kp);
+    L.pair_gid = take(P * n * 4);
+    L.far_any = take(P * n * 4);
+  }
+  const size_t es = elt_size(p->dtype);
+  const size_t qplanes = static_cast<size_t>(p->B) * p->H;
+  const size_t kvb = static_cast<size_t>(p->B) * p->H_kv * L.m * p->d * es;
+  L.Ks = take(p->dtype == FOCUS_BF16 ? kvb : 0);
+  L.Vs = take(p->dtype == FOCUS_BF16 ? kvb : 0);
+  if (k == 2) {
+    // entry and pair partials, each with the spare tile of rows the row
+    // scatter sends rows past an item's end to
+    L.O_e = take((qplanes * L.m + kTileM) * p->d * es);
+    L.lse_e = take(qplanes * L.m * 4);
+    L.O_p = take((qplanes * n + kTileM) * p->d * es);
+    L.lse_p = take(qplanes * n * 4);
+  }
+  L.O_far = take((qplanes * n + kTileM) * p->d * es);
+  L.lse_far = take(qplanes * n * 4);
+  L.total = o;
+  return L;
+}
+
+focus_status_t check_ws_topk(const focus_params_t* p, int k, void* ws, size_t ws_bytes) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return FOCUS_ERR_INVALID_ARG;
+  if (ws_bytes < layout_topk(p, k).total) return FOCUS_ERR_WORKSPACE;
+  return FOCUS_OK;
+}
+
+IndexLaunch index_launch(void* ws, const IndexRegions& R, const int32_t* gid, int P, int A, int n,
+                         int K, int w_eff, int kshift, int* err) {
+  IndexLaunch il{};
+  il.gid = gid;
+  il.P = P;
+  il.A = A;
+  il.n = n;
+  il.K = K;
+  il.w_eff = w_eff;
+  il.kshift = kshift;
+  il.segcnt = at<int32_t>(ws, R.segcnt);
+  il.counts = at<int32_t>(ws, R.counts);
+  il.offsets = at<int32_t>(ws, R.offsets);
+  il.tile_base = at<int32_t>(ws, R.tile_base);
+  il.perm = at<int32_t>(ws, R.perm);
+  il.rank = at<int32_t>(ws, R.rank);
+  il.farlen_tok = at<int32_t>(ws, R.far_tok);
+  il.farlen_slot = at<int32_t>(ws, R.far_slot);
+  il.items = at<focus_item_t>(ws, R.items);
+  il.cost = at<int32_t>(ws, R.cost);
+  il.order = at<int32_t>(ws, R.order);
+  il.n_items = at<int32_t>(ws, R.n_items);
+  il.max_items = R.max_items;
+  il.err = err;
+  return il;
+}
+
+void index_out(const IndexLaunch& il, focus_index_t* out) {
+  out->counts = il.counts;
+  out->offsets = il.offsets;
+  out->perm = il.perm;
+  out->rank = il.rank;
+  out->farlen_tok = il.farlen_tok;
+  out->farlen_slot = il.farlen_slot;
+  out->items = il.items;
+  out->order = il.order;
+  out->n_items = il.n_items;
+  out->max_items = il.max_items;
+  out->w_eff = il.w_eff;
+}
+
+bool index_ok(const focus_index_t& x) {
+  return x.perm && x.farlen_tok && x.farlen_slot && x.items && x.order && x.n_items;
+}
+
+// Group-pass arguments for one index (entries or pairs).
+void group_args(AttnArgs& a, const focus_index_t& x, int m, int kshift, void* O_part, float* lse_part) {
+  a.perm = x.perm;
+  a.farlen_slot = x.farlen_slot;
+  a.items = x.items;
+  a.order = x.order;
+  a.n_items = x.n_items;
+  a.m = m;
+  a.kshift = kshift;
+  a.O_far = O_part;
+  a.lse_far = lse_part;
 }
 
 // Streams and events focus_layer_fwd_host uses to overlap its copies with
@@ -229,15 +372,10 @@ focus_status_t focus_workspace_init(void* ws, void* stream) {
   return cuda_status(cudaMemsetAsync(ws, 0, kAlign, static_cast<cudaStream_t>(stream)));
 }
 
-focus_status_t focus_assign(const focus_params_t* p, const void* h, const void* W, const void* C,
-                            int32_t* gid, void* ws, size_t ws_bytes, void* stream) {
-  if (!params_ok(p)) return FOCUS_ERR_INVALID_ARG;
-  if (!h || !W || !C || !gid || !aligned16(h) || !aligned16(W) || !aligned16(C) || !aligned16(gid))
-    return FOCUS_ERR_INVALID_ARG;
-  if (focus_status_t s = check_ws(p, ws, ws_bytes)) return s;
+static focus_status_t assign_impl(const focus_params_t* p, int k, const void* h, const void* W,
+                                  const void* C, int32_t* gid, int* err, void* stream) {
   if (focus_status_t s = ensure_setup()) return s;
-  const Layout L = layout_of(p);
-  AssignLaunch al{h, W, C, gid, p->B, p->n, p->D, p->d_g, p->K, p->A, at<int>(ws, L.err)};
+  AssignLaunch al{h, W, C, gid, p->B, p->n, p->D, p->d_g, p->K, p->A, k, err};
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (p->dtype == FOCUS_F32) {
     if (!(p->d_g == 16 || p->d_g == 32 || p->d_g == 64 || p->d_g == 128)) return FOCUS_ERR_UNSUPPORTED;
@@ -251,6 +389,15 @@ focus_status_t focus_assign(const focus_params_t* p, const void* h, const void* 
       !make_map(&tm_w, W, p->D, ncol, 1, ncol < 256 ? ncol : 256, 2))
     return FOCUS_ERR_CUDA;
   return cuda_status(launch_assign_bf16(al, &tm_h, &tm_w, st));
+}
+
+focus_status_t focus_assign(const focus_params_t* p, const void* h, const void* W, const void* C,
+                            int32_t* gid, void* ws, size_t ws_bytes, void* stream) {
+  if (!params_ok(p)) return FOCUS_ERR_INVALID_ARG;
+  if (!h || !W || !C || !gid || !aligned16(h) || !aligned16(W) || !aligned16(C) || !aligned16(gid))
+    return FOCUS_ERR_INVALID_ARG;
+  if (focus_status_t s = check_ws(p, ws, ws_bytes)) return s;
+  return assign_impl(p, 1, h, W, C, gid, at<int>(ws, layout_of(p).err), stream);
 }
 
 focus_status_t focus_build_index(const focus_params_t* p, const int32_t* gid,
@@ -344,7 +491,7 @@ focus_status_t focus_attention_fwd_timed(const focus_params_t* p, const void* Q,
   void* Ks = at<void>(ws, L.Ks);
   void* Vs = at<void>(ws, L.Vs);
   cudaError_t e = mark(0);
-  if (e == cudaSuccess) e = launch_permute_kv_bf16(K, V, Ks, Vs, idx->perm, p->B, p->H_kv, p->n, p->d, p->A, st);
+  if (e == cudaSuccess) e = launch_permute_kv_bf16(K, V, Ks, Vs, idx->perm, p->B, p->H_kv, p->n, p->n, 0, p->d, p->A, st);
   if (e == cudaSuccess) e = mark(1);
   if (e != cudaSuccess) return FOCUS_ERR_CUDA;
   CUtensorMap tq, tk, tv, tks, tvs, to, tof;
@@ -470,6 +617,162 @@ focus_status_t focus_layer_fwd_host(const focus_params_t* p, const void* host_h,
   if (cudaEventRecord(pp->done, pp->copy_out) != cudaSuccess || cudaStreamWaitEvent(st, pp->done, 0) != cudaSuccess)
     return FOCUS_ERR_CUDA;
   return FOCUS_OK;
+}
+
+// ------------------------------------------------------ top-k membership ---
+
+size_t focus_workspace_bytes_topk(const focus_params_t* p, int32_t k) {
+  if (!topk_ok(p, k)) return 0;
+  return layout_topk(p, k).total;
+}
+
+focus_status_t focus_assign_topk(const focus_params_t* p, int32_t k, const void* h, const void* W,
+                                 const void* C, int32_t* gid, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  if (!topk_ok(p, k)) return params_ok(p) && (k == 1 || k == 2) ? FOCUS_ERR_UNSUPPORTED : FOCUS_ERR_INVALID_ARG;
+  if (!h || !W || !C || !gid || !aligned16(h) || !aligned16(W) || !aligned16(C) || !aligned16(gid))
+    return FOCUS_ERR_INVALID_ARG;
+  if (focus_status_t s = check_ws_topk(p, k, ws, ws_bytes)) return s;
+  return assign_impl(p, k, h, W, C, gid, at<int>(ws, layout_topk(p, k).err), stream);
+}
+
+focus_status_t focus_build_index_topk(const focus_params_t* p, int32_t k, const int32_t* gid,
+                                      focus_index_topk_t* idx_out, void* ws, size_t ws_bytes,
+                                      void* stream) {
+  if (!topk_ok(p, k)) return params_ok(p) && (k == 1 || k == 2) ? FOCUS_ERR_UNSUPPORTED : FOCUS_ERR_INVALID_ARG;
+  if (!gid || !idx_out || !aligned16(gid)) return FOCUS_ERR_INVALID_ARG;
+  if (focus_status_t s = check_ws_topk(p, k, ws, ws_bytes)) return s;
+  if (focus_status_t s = ensure_setup()) return s;
+  const LayoutTopk L = layout_topk(p, k);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int P = p->B * p->A, w_eff = p->w > 1 ? p->w : 1;
+  int* err = at<int>(ws, L.err);
+  const IndexLaunch ie = index_launch(ws, L.ent, gid, P, p->A, L.m, p->K, w_eff, k == 2 ? 1 : 0, err);
+  if (launch_build_index(ie, st) != cudaSuccess) return FOCUS_ERR_CUDA;
+  focus_index_topk_t out{};
+  index_out(ie, &out.entry);
+  out.k = k;
+  if (k == 2) {
+    int32_t* pg = at<int32_t>(ws, L.pair_gid);
+    int32_t* fa = at<int32_t>(ws, L.far_any);
+    if (launch_pair_ids(gid, P, p->n, p->K, pg, err, st) != cudaSuccess) return FOCUS_ERR_CUDA;
+    const IndexLaunch ip = index_launch(ws, L.pair, pg, P, p->A, p->n, L.Kp, w_eff, 0, err);
+    if (launch_build_index(ip, st) != cudaSuccess) return FOCUS_ERR_CUDA;
+    if (launch_far_any(ie.farlen_tok, P, p->n, fa, st) != cudaSuccess) return FOCUS_ERR_CUDA;
+    index_out(ip, &out.pair);
+    out.pair_gid = pg;
+    out.far_tok = fa;
+  } else {
+    out.far_tok = ie.farlen_tok;    // one entry per token: its farlen is the flag
+  }
+  *idx_out = out;
+  return FOCUS_OK;
+}
+
+focus_status_t focus_attention_topk_fwd_timed(const focus_params_t* p, const void* Q, const void* K,
+                                              const void* V, const focus_index_topk_t* idx,
+                                              void* O, float* lse_opt, void* ws, size_t ws_bytes,
+                                              void* stream, void* const* events) {
+  if (!idx || !(idx->k == 1 || idx->k == 2)) return FOCUS_ERR_INVALID_ARG;
+  const int k = idx->k;
+  if (!topk_ok(p, k)) return params_ok(p) ? FOCUS_ERR_UNSUPPORTED : FOCUS_ERR_INVALID_ARG;
+  const LayoutTopk L = layout_topk(p, k);
+  const int w_eff = p->w > 1 ? p->w : 1;
+  if (!index_ok(idx->entry) || !idx->far_tok || idx->entry.max_items != L.ent.max_items ||
+      idx->entry.w_eff != w_eff)
+    return FOCUS_ERR_INVALID_ARG;
+  if (k == 2 && (!index_ok(idx->pair) || idx->pair.max_items != L.pair.max_items || idx->pair.w_eff != w_eff))
+    return FOCUS_ERR_INVALID_ARG;
+  if (!Q || !K || !V || !O || !aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) ||
+      (lse_opt && !aligned16(lse_opt)))
+    return FOCUS_ERR_INVALID_ARG;
+  if (!(p->d == 64 || p->d == 128)) return FOCUS_ERR_UNSUPPORTED;
+  const uint64_t qplanes = static_cast<uint64_t>(p->B) * p->H;
+  const uint64_t planes = static_cast<uint64_t>(p->B) * p->H_kv;
+  // tensor-map rows and the row scatter's targets are 32-bit
+  if (static_cast<long long>(qplanes) * L.m + kTileM >= (1LL << 31)) return FOCUS_ERR_UNSUPPORTED;
+  if (focus_status_t s = check_ws_topk(p, k, ws, ws_bytes)) return s;
+  if (focus_status_t s = ensure_setup()) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  auto mark = [&](int i) {
+    return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) : cudaSuccess;
+  };
+  Layout none{};
+  none.err = L.err;
+  none.O_far = L.O_far;
+  none.lse_far = L.lse_far;
+  const AttnArgs base = attn_args(p, Q, K, V, O, lse_opt, ws, none);
+  void* O_far = at<void>(ws, L.O_far);
+  float* lse_far = at<float>(ws, L.lse_far);
+  void* O_e = k == 2 ? at<void>(ws, L.O_e) : O_far;
+  float* lse_e = k == 2 ? at<float>(ws, L.lse_e) : lse_far;
+  void* O_p = at<void>(ws, L.O_p);
+  float* lse_p = at<float>(ws, L.lse_p);
+  AttnArgs ge = base;
+  group_args(ge, idx->entry, L.m, k == 2 ? 1 : 0, O_e, lse_e);
+  AttnArgs gp = base;
+  if (k == 2) group_args(gp, idx->pair, p->n, 0, O_p, lse_p);
+  AttnArgs lo = base;
+  lo.farlen_tok = idx->far_tok;
+  MergeLaunch ml{O_e, lse_e, O_p, lse_p, idx->entry.farlen_tok, idx->pair.farlen_tok, O_far, lse_far,
+                 p->B, p->H, p->H_kv, p->A, p->n, p->d};
+  cudaError_t e = mark(0);
+  if (p->dtype == FOCUS_F32) {
+    if (e == cudaSuccess) e = mark(1);
+    if (e == cudaSuccess) e = launch_attn_simt_f32(ge, p->d, kModeGroup, L.ent.max_items, st);
+    if (e == cudaSuccess) e = mark(2);
+    if (k == 2) {
+      if (e == cudaSuccess) e = launch_attn_simt_f32(gp, p->d, kModeGroup, L.pair.max_items, st);
+      if (e == cudaSuccess) e = launch_topk_merge(ml, p->dtype, st);
+    }
+    if (e == cudaSuccess) e = mark(3);
+    if (e == cudaSuccess) e = launch_attn_simt_f32(lo, p->d, kModeLocal, 0, st);
+    if (e == cudaSuccess) e = mark(4);
+    return cuda_status(e);
+  }
+  void* Ks = at<void>(ws, L.Ks);
+  void* Vs = at<void>(ws, L.Vs);
+  const int sms = sm_count();
+  if (e == cudaSuccess)
+    e = launch_permute_kv_bf16(K, V, Ks, Vs, idx->entry.perm, p->B, p->H_kv, p->n, L.m, ge.kshift, p->d, p->A, st);
+  if (e == cudaSuccess) e = mark(1);
+  if (e != cudaSuccess) return FOCUS_ERR_CUDA;
+  // entry pass: Q rows gathered by token, partial rows scattered by entry
+  CUtensorMap tqg, tks, tvs, tofs;
+  if (!make_map(&tqg, Q, p->d, qplanes * p->n, 1, 1, 2) ||
+      !make_map(&tks, Ks, p->d, L.m, planes, 128, 3) || !make_map(&tvs, Vs, p->d, L.m, planes, 128, 3) ||
+      !make_map(&tofs, O_e, p->d, qplanes * L.m + kTileM, 1, 1, 2))
+    return FOCUS_ERR_CUDA;
+  e = launch_attn_tc_bf16(ge, &tqg, &tks, &tvs, &tofs, &tofs, p->d, kModeGroup, L.ent.max_items, sms, st);
+  if (e == cudaSuccess) e = mark(2);
+  if (e == cudaSuccess && k == 2) {
+    // pair pass over the same K/V buffers, re-sorted by pair (the entry pass
+    // is done with them: same stream)
+    CUtensorMap pks, pvs, pofs;
+    e = launch_permute_kv_bf16(K, V, Ks, Vs, idx->pair.perm, p->B, p->H_kv, p->n, p->n, 0, p->d, p->A, st);
+    if (e != cudaSuccess) return FOCUS_ERR_CUDA;
+    if (!make_map(&pks, Ks, p->d, p->n, planes, 128, 3) || !make_map(&pvs, Vs, p->d, p->n, planes, 128, 3) ||
+        !make_map(&pofs, O_p, p->d, qplanes * p->n + kTileM, 1, 1, 2))
+      return FOCUS_ERR_CUDA;
+    e = launch_attn_tc_bf16(gp, &tqg, &pks, &pvs, &pofs, &pofs, p->d, kModeGroup, L.pair.max_items, sms, st);
+    if (e == cudaSuccess) e = launch_topk_merge(ml, p->dtype, st);
+  }
+  if (e == cudaSuccess) e = mark(3);
+  if (e != cudaSuccess) return FOCUS_ERR_CUDA;
+  CUtensorMap tq, tk, tv, to, tof;
+  if (!make_map(&tq, Q, p->d, p->n, qplanes, 128, 3) ||
+      !make_map(&tk, K, p->d, p->n, planes, 128, 3) || !make_map(&tv, V, p->d, p->n, planes, 128, 3) ||
+      !make_map(&to, O, p->d, p->n, qplanes, 128, 3) || !make_map(&tof, O_far, p->d, p->n, qplanes, 128, 3))
+    return FOCUS_ERR_CUDA;
+  e = launch_attn_tc_bf16(lo, &tq, &tk, &tv, &to, &tof, p->d, kModeLocal, 0, sms, st);
+  if (e == cudaSuccess) e = mark(4);
+  return cuda_status(e);
+}
+
+focus_status_t focus_attention_topk_fwd(const focus_params_t* p, const void* Q, const void* K,
+                                        const void* V, const focus_index_topk_t* idx, void* O,
+                                        float* lse_opt, void* ws, size_t ws_bytes, void* stream) {
+  return focus_attention_topk_fwd_timed(p, Q, K, V, idx, O, lse_opt, ws, ws_bytes, stream, nullptr);
 }
 
 focus_status_t focus_check_errors(void* ws, void* stream) {

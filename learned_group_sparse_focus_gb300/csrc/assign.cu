@@ -3,9 +3,10 @@
 // "Focus: Learning Which Attention Pairs Matter", section 2.1: each hidden
 // state h_i is projected and compared with K learnable centroids; section 2.2
 // and "Why Attend to Everything? Focus is the Key", section 2.3: at inference
-// the assignment is hard (top-1 here).  Per token and assignment a:
+// the assignment is hard: each token goes to its top-k centroids (k = 1 or 2).
+// Per token and assignment a:
 //   p = W_a h (fp32 accumulate, kept in fp32), s_k = p . c_k (fp32),
-//   g = argmax_k s_k, lowest k on ties.
+//   g = the k largest s_k, best first, the lower k first among equal scores.
 //
 // bf16: the projection is a [128 tokens x A*d_g] tile of h W^T on the
 // tcgen05 tensor cores (TMA-fed 4..6-stage pipeline, fp32 accumulator in
@@ -18,13 +19,32 @@
 namespace focus {
 namespace {
 
+// Running best and runner-up over centroids scanned in increasing k: a later
+// centroid displaces one only with a strictly larger score, so the lower index
+// wins ties (and a NaN score never displaces anything but the empty start).
+struct Top2 {
+  int b1 = -1, b2 = -1;
+  float s1 = -INFINITY, s2 = -INFINITY;
+  __device__ __forceinline__ void push(int k, float s) {
+    if (b1 < 0 || s > s1) {
+      b2 = b1;
+      s2 = s1;
+      b1 = k;
+      s1 = s;
+    } else if (b2 < 0 || s > s2) {
+      b2 = k;
+      s2 = s;
+    }
+  }
+};
+
 // ------------------------------------------------------------------ fp32 ---
 template <int DG>
 __global__ void __launch_bounds__(128) assign_f32_kernel(const float* __restrict__ h,
                                                          const float* __restrict__ W,
                                                          const float* __restrict__ C,
                                                          int32_t* __restrict__ gid, int B, int n,
-                                                         int D, int K, int A) {
+                                                         int D, int K, int A, int topk) {
   const int tok = blockIdx.x * blockDim.x + threadIdx.x;
   if (tok >= B * n) return;
   const int b = tok / n, i = tok % n;
@@ -40,18 +60,16 @@ __global__ void __launch_bounds__(128) assign_f32_kernel(const float* __restrict
       for (int r = 0; r < DG; ++r) p[r] = fmaf(__ldg(Wa + static_cast<size_t>(r) * D + c), x, p[r]);
     }
     const float* Ca = C + static_cast<size_t>(a) * K * DG;
-    int best = 0;
-    float bs = -INFINITY;
+    Top2 t;
     for (int k = 0; k < K; ++k) {
       float s = 0.f;
 #pragma unroll
       for (int r = 0; r < DG; ++r) s = fmaf(p[r], __ldg(Ca + static_cast<size_t>(k) * DG + r), s);
-      if (s > bs || k == 0) {
-        bs = s;
-        best = k;
-      }
+      t.push(k, s);
     }
-    gid[(static_cast<size_t>(b) * A + a) * n + i] = best;
+    int32_t* out = gid + ((static_cast<size_t>(b) * A + a) * n + i) * topk;
+    out[0] = t.b1;
+    if (topk == 2) out[1] = t.b2;
   }
 }
 
@@ -75,7 +93,7 @@ template <int NALLOC>
 __global__ void __launch_bounds__(128, AssignCfg<NALLOC>::kMinBlocks) assign_tc_kernel(
     const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
     const __nv_bfloat16* __restrict__ C, int32_t* __restrict__ gid, int B, int n, int D, int d_g,
-    int K, int A, int* err) {
+    int K, int A, int topk, int* err) {
   using Cfg = AssignCfg<NALLOC>;
   constexpr int S = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -178,8 +196,7 @@ __global__ void __launch_bounds__(128, AssignCfg<NALLOC>::kMinBlocks) assign_tc_
         for (int j = 0; j < 32; ++j) p[c + j] = __uint_as_float(r[j]);
       }
     }
-    int best = 0;
-    float bs = -INFINITY;
+    Top2 t;
     for (int k0 = 0; k0 < K; k0 += kc) {
       const int kn = min(kc, K - k0);
       __syncthreads();
@@ -205,12 +222,7 @@ __global__ void __launch_bounds__(128, AssignCfg<NALLOC>::kMinBlocks) assign_tc_
           }
         }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (sc[q] > bs || k0 + k + q == 0) {
-            bs = sc[q];
-            best = k0 + k + q;
-          }
-        }
+        for (int q = 0; q < 4; ++q) t.push(k0 + k + q, sc[q]);
       }
       for (; k < kn; ++k) {
         const float* ck = Cs + k * d_g;
@@ -218,15 +230,14 @@ __global__ void __launch_bounds__(128, AssignCfg<NALLOC>::kMinBlocks) assign_tc_
 #pragma unroll
         for (int j = 0; j < 128; ++j)
           if (j < d_g) s = fmaf(p[j], ck[j], s);
-        if (s > bs || k0 + k == 0) {
-          bs = s;
-          best = k0 + k;
-        }
+        t.push(k0 + k, s);
       }
     }
     if (got && !*abort && tok < B * n) {
       const int b = tok / n, i = tok % n;
-      gid[(static_cast<size_t>(b) * A + a) * n + i] = best;
+      int32_t* out = gid + ((static_cast<size_t>(b) * A + a) * n + i) * topk;
+      out[0] = t.b1;
+      if (topk == 2) out[1] = t.b2;
     }
   }
   tc_fence_before();
@@ -243,7 +254,7 @@ cudaError_t launch_tc(const AssignLaunch& L, const CUtensorMap* tm_h, const CUte
   const int grid = (L.B * L.n + kBM - 1) / kBM;
   assign_tc_kernel<NALLOC><<<grid, 128, AssignCfg<NALLOC>::kSmem, st>>>(
       *tm_h, *tm_w, static_cast<const __nv_bfloat16*>(L.C), L.gid, L.B, L.n, L.D, L.d_g, L.K,
-      L.A, L.err);
+      L.A, L.topk, L.err);
   return cudaGetLastError();
 }
 
@@ -255,10 +266,10 @@ cudaError_t launch_assign_f32(const AssignLaunch& L, cudaStream_t st) {
   const float* W = static_cast<const float*>(L.W);
   const float* C = static_cast<const float*>(L.C);
   switch (L.d_g) {
-    case 16: assign_f32_kernel<16><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.B, L.n, L.D, L.K, L.A); break;
-    case 32: assign_f32_kernel<32><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.B, L.n, L.D, L.K, L.A); break;
-    case 64: assign_f32_kernel<64><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.B, L.n, L.D, L.K, L.A); break;
-    case 128: assign_f32_kernel<128><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.B, L.n, L.D, L.K, L.A); break;
+    case 16: assign_f32_kernel<16><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.B, L.n, L.D, L.K, L.A, L.topk); break;
+    case 32: assign_f32_kernel<32><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.B, L.n, L.D, L.K, L.A, L.topk); break;
+    case 64: assign_f32_kernel<64><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.B, L.n, L.D, L.K, L.A, L.topk); break;
+    case 128: assign_f32_kernel<128><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.B, L.n, L.D, L.K, L.A, L.topk); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

@@ -6,7 +6,8 @@
 // window part and an in-group causal part):
 //   group pass  rows of one group in sorted order, keys = earlier members of
 //               the group with j <= i - w; writes a normalised partial O and
-//               its LSE at each row's token position.
+//               its LSE at each row's item (token position, or the top-k
+//               entry i * k + c of token i).
 //   local pass  natural-order rows, keys j in [i - w + 1, i]; merges the
 //               group partial (when the row has far keys) by log-sum-exp and
 //               writes O.  The dense comparator is the local pass with every
@@ -43,6 +44,7 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
 
   int b, h, kv, asg;
   int row_pos;            // token position of this thread's row (-1: none)
+  int row_item = -1;      // group pass: the row's sorted item (O_far row)
   int lo, hi;             // kept key interval for this row (positions or slots)
   int key_begin, key_end; // key range the CTA walks
   const int32_t* perm_p = nullptr;
@@ -64,17 +66,18 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
     h = a.A == 1 ? y : it.a * (a.H / a.H_kv) + y;
     kv = (h * a.H_kv) / a.H;
     const int p = b * a.A + asg;
-    perm_p = a.perm + static_cast<size_t>(p) * a.n;
+    perm_p = a.perm + static_cast<size_t>(p) * a.m;
     key0 = it.key0;
     const int rr = sub * kRows + r;
     const int last = min(it.rows, sub * kRows + kRows) - 1;
     key_begin = 0;
-    key_end = a.farlen_slot[static_cast<size_t>(p) * a.n + it.row0 + last];
+    key_end = a.farlen_slot[static_cast<size_t>(p) * a.m + it.row0 + last];
     if (rr < it.rows) {
       slot = it.row0 + rr;
-      row_pos = perm_p[slot];
+      row_item = perm_p[slot];
+      row_pos = row_item >> a.kshift;
       lo = 0;
-      hi = a.farlen_slot[static_cast<size_t>(p) * a.n + slot] - 1;
+      hi = a.farlen_slot[static_cast<size_t>(p) * a.m + slot] - 1;
     } else {
       row_pos = -1;
       lo = 1;
@@ -119,7 +122,7 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
     __syncthreads();
     if (tid < kKeys) {
       const int t = t0 + tid;
-      key_pos[tid] = t < key_end ? (MODE == kModeGroup ? perm_p[key0 + t] : t) : -1;
+      key_pos[tid] = t < key_end ? (MODE == kModeGroup ? perm_p[key0 + t] >> a.kshift : t) : -1;
     }
     __syncthreads();
     for (int e = tid; e < kKeys * D / 4; e += blockDim.x) {
@@ -169,11 +172,12 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
   constexpr float kLn2 = 0.6931471805599453f;
   if (MODE == kModeGroup) {
     if (l > 0.f) {
-      float* Of = static_cast<float*>(a.O_far);
+      const size_t frow = (static_cast<size_t>(b) * a.H + h) * a.m + row_item;
+      float* Of = static_cast<float*>(a.O_far) + frow * D + part * DT;
       const float inv = 1.f / l;
 #pragma unroll
-      for (int e = 0; e < DT; ++e) Of[orow + e] = acc[e] * inv;
-      if (part == 0) a.lse_far[qrow + row_pos] = (m + log2f(l)) * kLn2;
+      for (int e = 0; e < DT; ++e) Of[e] = acc[e] * inv;
+      if (part == 0) a.lse_far[frow] = (m + log2f(l)) * kLn2;
     }
     return;
   }

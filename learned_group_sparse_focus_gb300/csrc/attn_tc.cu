@@ -12,7 +12,8 @@
 //          earlier members at or before i - w (slot < farlen of the row), read
 //          from K/V pre-permuted into sorted order so each key tile is one
 //          dense TMA box.  Writes the normalised partial O and its LSE at each
-//          row's token position.
+//          row's item (its token position, or with top-k membership its entry
+//          i * k + c, whose query is token i).
 //   local  128 consecutive tokens, keys j in [i - w + 1, i]; merges the group
 //          partial by log-sum-exp when the row has far keys; writes O.
 //   dense  128 consecutive tokens, every j <= i (the comparator).
@@ -316,13 +317,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // rows past the item repeat its first row, whose scores are all masked
             if (lane == 0) mbar_expect_tx(&q_full[sl], Cfg::kTile);
             __syncwarp();
-            const int32_t* pp = a.perm + static_cast<size_t>(U.prob) * a.n + U.row0;
-            const int first = pp[0];
+            const int32_t* pp = a.perm + static_cast<size_t>(U.prob) * a.m + U.row0;
+            const int first = pp[0] >> a.kshift;
             int rows[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const int rr = 4 * lane + j;
-              rows[j] = U.zq * a.n + (rr < U.nrows ? pp[rr] : first);
+              rows[j] = U.zq * a.n + (rr < U.nrows ? pp[rr] >> a.kshift : first);
             }
 #pragma unroll
             for (int ch = 0; ch < kChunks; ++ch)
@@ -609,8 +610,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (hf == 0) {
-          row_tok[r] = s.valid ? s.zq * a.n + s.pos : a.B * a.H * a.n + r;
-          if (write) a.lse_far[qrow + s.pos] = lse2 * kLn2;
+          row_tok[r] = s.valid ? s.zq * a.m + s.pos : a.B * a.H * a.m + r;
+          if (write) a.lse_far[static_cast<size_t>(s.zq) * a.m + s.pos] = lse2 * kLn2;
         }
         fence_proxy_async_smem();
         warp_arrive(ost_full, lane);
@@ -690,8 +691,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       st.pos = -1;
       if (MODE == kModeGroup) {
         if (st.valid) {
-          const size_t sidx = static_cast<size_t>(U.prob) * a.n + U.row0 + r;
-          st.pos = a.perm[sidx];
+          const size_t sidx = static_cast<size_t>(U.prob) * a.m + U.row0 + r;
+          st.pos = a.perm[sidx];       // the row's item: O_far row within the head
           lo = 0;
           hi = a.farlen_slot[sidx] - 1;
         }
@@ -819,24 +820,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// K_s[b, kv, s, :] = K[b, kv, perm_a[s], :] (and V), a = assignment of kv.
+// K_s[b, kv, s, :] = K[b, kv, perm_a[s] >> kshift, :] (and V), a = assignment
+// of kv; s runs over the m sorted items, K has n rows per head.
 __global__ void __launch_bounds__(256) permute_kv_kernel(const uint4* __restrict__ K,
                                                          const uint4* __restrict__ V,
                                                          uint4* __restrict__ Ks,
                                                          uint4* __restrict__ Vs,
                                                          const int32_t* __restrict__ perm, int H_kv,
-                                                         int n, int vec_per_row, int A,
-                                                         long long total) {
+                                                         int n, int m, int kshift, int vec_per_row,
+                                                         int A, long long total) {
   for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < total;
        e += static_cast<long long>(gridDim.x) * blockDim.x) {
     const long long row = e / vec_per_row;
     const int u = static_cast<int>(e % vec_per_row);
-    const int s = static_cast<int>(row % n);
-    const long long bk = row / n;             // b * H_kv + kv
+    const int s = static_cast<int>(row % m);
+    const long long bk = row / m;             // b * H_kv + kv
     const int kvh = static_cast<int>(bk % H_kv);
     const long long bb = bk / H_kv;
     const long long p = bb * A + (A == 1 ? 0 : kvh);
-    const int src = __ldg(perm + p * n + s);
+    const int src = __ldg(perm + p * m + s) >> kshift;
     const long long si = (bk * n + src) * vec_per_row + u;
     Ks[e] = __ldg(K + si);
     Vs[e] = __ldg(V + si);
@@ -880,16 +882,16 @@ cudaError_t set_smem() {
 }  // namespace
 
 cudaError_t launch_permute_kv_bf16(const void* K, const void* V, void* Ks, void* Vs,
-                                   const int32_t* perm, int B, int H_kv, int n, int d, int A,
-                                   cudaStream_t st) {
+                                   const int32_t* perm, int B, int H_kv, int n, int m, int kshift,
+                                   int d, int A, cudaStream_t st) {
   const int vpr = d / 8;
-  const long long total = static_cast<long long>(B) * H_kv * n * vpr;
+  const long long total = static_cast<long long>(B) * H_kv * m * vpr;
   if (total == 0) return cudaSuccess;
   const long long want = (total + 255) / 256;
   const int grid = static_cast<int>(want < 152LL * 16 ? want : 152LL * 16);
   permute_kv_kernel<<<grid, 256, 0, st>>>(static_cast<const uint4*>(K), static_cast<const uint4*>(V),
                                           static_cast<uint4*>(Ks), static_cast<uint4*>(Vs), perm,
-                                          H_kv, n, vpr, A, total);
+                                          H_kv, n, m, kshift, vpr, A, total);
   return cudaGetLastError();
 }
 

@@ -14,6 +14,10 @@
 //            rank (position -> slot); warp match + popc     grid (nseg, P)
 //   farlen   per slot: same-group tokens at or before
 //            position - w (binary search in the group run)  grid (n/256, P)
+// For top-k membership the sorted items are the n_tok * k entries (token i's
+// c-th group at e = i * k + c); a group never holds two entries of one token,
+// so its run is still in increasing token position, and farlen compares token
+// positions e >> kshift.
 //   items    work list in canonical order, compacted, and
 //            a longest-first schedule (stable counting sort) grid (1)
 // P = B * A independent problems.
@@ -205,7 +209,7 @@ __global__ void __launch_bounds__(256) index_scatter_kernel(const int32_t* __res
   }
 }
 
-__global__ void __launch_bounds__(256) index_farlen_kernel(int n, int K, int w_eff,
+__global__ void __launch_bounds__(256) index_farlen_kernel(int n, int K, int w_eff, int kshift,
                                                            const int32_t* __restrict__ offsets,
                                                            const int32_t* __restrict__ perm,
                                                            int32_t* __restrict__ farlen_tok,
@@ -218,7 +222,8 @@ __global__ void __launch_bounds__(256) index_farlen_kernel(int n, int K, int w_e
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= n) return;
   const int32_t* pp = perm + static_cast<size_t>(p) * n;
-  const int pos = pp[s];
+  const int item = pp[s];
+  const int pos = item >> kshift;
   const int g = upper_bound_minus1(offs, K, s);
   // members of g at slots [offs[g], s) have positions < pos; count those
   // with position <= pos - w_eff, i.e. < target
@@ -226,11 +231,11 @@ __global__ void __launch_bounds__(256) index_farlen_kernel(int n, int K, int w_e
   int lo = offs[g], hi = s;   // first slot in [lo, hi) whose position >= target
   while (lo < hi) {
     int mid = (lo + hi) >> 1;
-    if (__ldg(pp + mid) < target) lo = mid + 1; else hi = mid;
+    if ((__ldg(pp + mid) >> kshift) < target) lo = mid + 1; else hi = mid;
   }
   const int fl = lo - offs[g];
   farlen_slot[static_cast<size_t>(p) * n + s] = fl;
-  farlen_tok[static_cast<size_t>(p) * n + pos] = fl;
+  farlen_tok[static_cast<size_t>(p) * n + item] = fl;
 }
 
 __global__ void __launch_bounds__(1024) index_items_kernel(
@@ -343,7 +348,7 @@ cudaError_t launch_build_index(const IndexLaunch& L, cudaStream_t st) {
                                                                 L.perm, L.rank, L.err);
   const size_t sm_far = static_cast<size_t>(L.K + 1) * sizeof(int);
   index_farlen_kernel<<<dim3((L.n + 255) / 256, P), 256, sm_far, st>>>(
-      L.n, L.K, L.w_eff, L.offsets, L.perm, L.farlen_tok, L.farlen_slot);
+      L.n, L.K, L.w_eff, L.kshift, L.offsets, L.perm, L.farlen_tok, L.farlen_slot);
   const int nb = (L.n + kTileN - 1) / kTileN + 1;
   const size_t sm_items = static_cast<size_t>(P + 1 + nb) * sizeof(int);
   index_items_kernel<<<1, 1024, sm_items, st>>>(P, L.A, L.n, L.K, L.counts, L.offsets,

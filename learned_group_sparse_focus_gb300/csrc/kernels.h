@@ -21,9 +21,13 @@ enum : int {
   kErrInternal = 4,   // an index or item failed a consistency check
 };
 
+// n counts the sorted items: tokens, or for top-k membership the n_tok * k
+// entries (entry e = i * k + c, token i = e >> kshift); positions compared
+// against the window are token positions.
 struct IndexLaunch {
   const int32_t* gid;
   int P, A, n, K, w_eff;
+  int kshift;           // 0: items are tokens; log2(k): items are entries
   int32_t* segcnt;      // [P][nseg][K]
   int32_t* counts;      // [P][K]
   int32_t* offsets;     // [P][K+1]
@@ -44,8 +48,9 @@ struct AssignLaunch {
   const void* h;   // [B*n, D]
   const void* W;   // [A*d_g, D]
   const void* C;   // [A, K, d_g]
-  int32_t* gid;    // [B, A, n]
+  int32_t* gid;    // [B, A, n, topk]
   int B, n, D, d_g, K, A;
+  int topk;        // 1 or 2 ids per token, best first
   int* err;
 };
 
@@ -65,6 +70,10 @@ struct AttnArgs {
   const int32_t* order;
   const int32_t* n_items;
   int B, H, H_kv, n, A, w;   // w: effective window (>= 1)
+  // group pass only: sorted items per problem (perm, farlen_slot and the
+  // O_far / lse_far rows are indexed by item) and the item -> token shift.
+  // m = n, kshift = 0 for one group per token; m = n * k for top-k entries.
+  int m, kshift;
   float scale_log2;          // scale * log2(e)
   int* err;
 };
@@ -85,9 +94,11 @@ cudaError_t launch_attn_simt_f32(const AttnArgs& a, int d, int mode, int max_ite
                                  cudaStream_t st);
 
 // attn_tc.cu (bf16 storage, tcgen05 tensor cores, fp32 softmax)
+// Ks[b, kv, s] = K[b, kv, perm[s] >> kshift] for the m sorted items s of kv's
+// assignment (and V); K/V have n rows per head, Ks/Vs have m.
 cudaError_t launch_permute_kv_bf16(const void* K, const void* V, void* Ks, void* Vs,
-                                   const int32_t* perm, int B, int H_kv, int n, int d, int A,
-                                   cudaStream_t st);
+                                   const int32_t* perm, int B, int H_kv, int n, int m, int kshift,
+                                   int d, int A, cudaStream_t st);
 // tm_o / tm_of: O and the group partial O_far as {d, n, B*H} tiles (local and
 // dense passes store O, and the local pass loads O_far, through them).
 cudaError_t launch_attn_tc_bf16(const AttnArgs& a, const CUtensorMap* tm_q,
@@ -95,5 +106,28 @@ cudaError_t launch_attn_tc_bf16(const AttnArgs& a, const CUtensorMap* tm_q,
                                 const CUtensorMap* tm_o, const CUtensorMap* tm_of, int d, int mode,
                                 int max_items, int num_sms, cudaStream_t st);
 cudaError_t setup_attn_kernels();
+
+// topk.cu (top-2 membership)
+// pair_gid[p, i] = id of token i's two groups {a, b} (a < b) among the
+// K (K - 1) / 2 pairs; equal or out-of-range ids raise kErrBadGroup.
+cudaError_t launch_pair_ids(const int32_t* gid2, int P, int n, int K, int32_t* pair_gid, int* err,
+                            cudaStream_t st);
+// far_any[p, i] = 1 if either entry of token i has far keys, else 0.
+cudaError_t launch_far_any(const int32_t* farlen_entry, int P, int n, int32_t* far_any,
+                           cudaStream_t st);
+// Per query row: the two entry partials minus the pair partial, combined by
+// log-sum-exp into one far partial per token (O_far, lse_far).
+struct MergeLaunch {
+  const void* O_e;              // [B*H*2n (+ spare), d]  entry partials
+  const float* lse_e;           // [B*H*2n]
+  const void* O_p;              // [B*H*n (+ spare), d]   pair partials
+  const float* lse_p;           // [B*H*n]
+  const int32_t* farlen_entry;  // [B*A][2n]
+  const int32_t* farlen_pair;   // [B*A][n]
+  void* O_far;                  // [B*H*n (+ spare), d]
+  float* lse_far;               // [B*H*n]
+  int B, H, H_kv, A, n, d;
+};
+cudaError_t launch_topk_merge(const MergeLaunch& L, int dtype, cudaStream_t st);
 
 }  // namespace focus

@@ -46,6 +46,11 @@ class Index(ctypes.Structure):
                 ("max_items", ctypes.c_int32), ("w_eff", ctypes.c_int32)]
 
 
+class IndexTopk(ctypes.Structure):
+    _fields_ = [("entry", Index), ("pair", Index), ("pair_gid", ctypes.c_void_p),
+                ("far_tok", ctypes.c_void_p), ("k", ctypes.c_int32), ("pad", ctypes.c_int32)]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"libfocus.so not built ({LIB_PATH}); run __graft_entry__.build()")
@@ -66,6 +71,15 @@ def _load():
         "focus_layer_fwd_host": ([P] + [vp] * 7 + [vp] * 8 + [vp, ctypes.c_size_t, vp], ctypes.c_int),
         "focus_check_errors": ([vp, vp], ctypes.c_int),
         "focus_build_index_static": ([P, vp, ctypes.POINTER(Index), vp, vp], ctypes.c_int),
+        "focus_workspace_bytes_topk": ([P, ctypes.c_int32], ctypes.c_size_t),
+        "focus_assign_topk": ([P, ctypes.c_int32, vp, vp, vp, vp, vp, ctypes.c_size_t, vp], ctypes.c_int),
+        "focus_build_index_topk": ([P, ctypes.c_int32, vp, ctypes.POINTER(IndexTopk), vp, ctypes.c_size_t,
+                                    vp], ctypes.c_int),
+        "focus_attention_topk_fwd": ([P, vp, vp, vp, ctypes.POINTER(IndexTopk), vp, vp, vp, ctypes.c_size_t,
+                                      vp], ctypes.c_int),
+        "focus_attention_topk_fwd_timed": ([P, vp, vp, vp, ctypes.POINTER(IndexTopk), vp, vp, vp,
+                                            ctypes.c_size_t, vp, ctypes.POINTER(ctypes.c_void_p)],
+                                           ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -79,7 +93,8 @@ _lib = _load()
 EXPORTED = ("focus_abi_version", "focus_status_string", "focus_workspace_bytes",
             "focus_workspace_init", "focus_assign", "focus_build_index", "focus_attention_fwd",
             "focus_attention_fwd_timed", "focus_dense_causal_fwd", "focus_layer_fwd_host", "focus_check_errors",
-            "focus_build_index_static")
+            "focus_build_index_static", "focus_workspace_bytes_topk", "focus_assign_topk",
+            "focus_build_index_topk", "focus_attention_topk_fwd", "focus_attention_topk_fwd_timed")
 
 
 def lib():
@@ -211,12 +226,74 @@ def focus_build_index_static(p: Params, gid, bufs: dict, stream=None) -> Index:
     return idx
 
 
+# ------------------------------------------------------- top-k membership ---
+
+def focus_workspace_bytes_topk(p: Params, k: int) -> int:
+    return int(_lib.focus_workspace_bytes_topk(ctypes.byref(p), int(k)))
+
+
+def alloc_workspace_topk(p: Params, k: int, device="cuda", stream=None) -> torch.Tensor:
+    """Caller-owned workspace for the top-k calls, error word cleared."""
+    nbytes = focus_workspace_bytes_topk(p, k)
+    if nbytes == 0:
+        raise FocusError("focus_workspace_bytes_topk", 1)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    focus_workspace_init(ws, stream)
+    return ws
+
+
+def focus_assign_topk(p: Params, k: int, h, W, C, gid, ws, stream=None):
+    """gid: [B, A, n, k] int32 device tensor (best first)."""
+    _check("focus_assign_topk", _lib.focus_assign_topk(ctypes.byref(p), int(k), _ptr(h), _ptr(W), _ptr(C),
+                                                       _ptr(gid), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def focus_build_index_topk(p: Params, k: int, gid, ws, stream=None) -> IndexTopk:
+    idx = IndexTopk()
+    _check("focus_build_index_topk",
+           _lib.focus_build_index_topk(ctypes.byref(p), int(k), _ptr(gid), ctypes.byref(idx), _ptr(ws),
+                                       ws.numel(), _stream(stream)))
+    return idx
+
+
+def focus_attention_topk_fwd(p: Params, Q, K, V, idx: IndexTopk, O, lse, ws, stream=None):
+    _check("focus_attention_topk_fwd",
+           _lib.focus_attention_topk_fwd(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), ctypes.byref(idx),
+                                         _ptr(O), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def focus_attention_topk_fwd_timed(p: Params, Q, K, V, idx: IndexTopk, O, lse, ws, events, stream=None):
+    """events: five torch.cuda.Event objects (see include/focus.h)."""
+    arr = (ctypes.c_void_p * 5)(*[e.cuda_event for e in events])
+    _check("focus_attention_topk_fwd_timed",
+           _lib.focus_attention_topk_fwd_timed(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), ctypes.byref(idx),
+                                               _ptr(O), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream),
+                                               arr))
+
+
+def run_layer_topk(p: Params, k: int, h, W, C, Q, K, V, ws, stream=None, want_lse=False):
+    """assign (top-k) -> index -> attention; returns (O, gid, idx, lse)."""
+    dev = Q.device
+    gid = torch.empty((p.B, p.A, p.n, k), dtype=torch.int32, device=dev)
+    focus_assign_topk(p, k, h, W, C, gid, ws, stream)
+    idx = focus_build_index_topk(p, k, gid, ws, stream)
+    O = torch.empty_like(Q)
+    lse = torch.empty((p.B, p.H, p.n), dtype=torch.float32, device=dev) if want_lse else None
+    focus_attention_topk_fwd(p, Q, K, V, idx, O, lse, ws, stream)
+    return O, gid, idx, lse
+
+
 # ------------------------------------------------------------ index views ---
 
-def index_views(p: Params, idx: Index, ws: torch.Tensor) -> dict:
-    """Torch views (no copy) of the index arrays living inside the workspace."""
+def index_views(p: Params, idx: Index, ws: torch.Tensor, n: int | None = None,
+                K: int | None = None) -> dict:
+    """Torch views (no copy) of the index arrays living inside the workspace.
+    n: sorted items per (b, a) (p.n; n * k for a top-k entry index); K: groups
+    (p.K; K (K - 1) / 2 for a top-2 pair index)."""
     base = ws.data_ptr()
-    P, n, K = p.B * p.A, p.n, p.K
+    P = p.B * p.A
+    n = p.n if n is None else n
+    K = p.K if K is None else K
 
     def view(ptr, count, dtype=torch.int32, shape=None):
         off = ptr - base

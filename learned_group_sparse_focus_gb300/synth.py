@@ -35,11 +35,11 @@ import numpy as np
 
 __all__ = [
     "Workload", "WORKLOADS", "workload", "draw", "redraw_hidden",
-    "round_bf16", "bf16_bits", "draw_group_ids",
+    "round_bf16", "bf16_bits", "draw_group_ids", "draw_group_ids_topk",
 ]
 
 _TAGS = {"h": 1, "W": 2, "C": 3, "Q": 4, "K": 5, "V": 6, "target": 7,
-         "perm": 8, "redraw": 9, "gid": 10}
+         "perm": 8, "redraw": 9, "gid": 10, "gid-topk": 11}
 
 
 @dataclass(frozen=True)
@@ -212,6 +212,45 @@ def draw_group_ids(seed: int, B: int, A: int, n: int, K: int, kind: str = "unifo
     elif kind == "blocks":
         run = max(1, n // max(1, K))
         g = np.minimum(np.arange(n) // run, K - 1)[None, None, :].repeat(B, 0).repeat(A, 1)
+    else:
+        raise ValueError(kind)
+    return np.ascontiguousarray(g, dtype=np.int32)
+
+
+def draw_group_ids_topk(seed: int, B: int, A: int, n: int, K: int, k: int,
+                        kind: str = "uniform") -> np.ndarray:
+    """k distinct group ids per token, [B, A, n, k] (for tests and benchmarks
+    that inject a top-k assignment).
+
+    kind: "uniform" (each ordered k-subset equally likely), "zipf" (ids drawn
+          from truncated Zipf(1.1), repeats redrawn), "both" (every token in
+          groups 0 and 1, in a random order; needs k = 2).
+    """
+    if not 1 <= k <= K:
+        raise ValueError("need 1 <= k <= K")
+    rng = _rng(seed, "gid-topk")
+    shape = (B, A, n)
+    if kind == "both":
+        if k != 2:
+            raise ValueError("'both' is a k = 2 pattern")
+        first = rng.integers(0, 2, size=shape)
+        g = np.stack([first, 1 - first], axis=-1)
+    elif kind in ("uniform", "zipf"):
+        p = None
+        if kind == "zipf":
+            p = np.arange(1, K + 1, dtype=np.float64) ** -1.1
+            p /= p.sum()
+        g = np.empty(shape + (k,), dtype=np.int64)
+        for c in range(k):
+            col = rng.choice(K, size=shape, p=p)
+            while True:
+                clash = np.zeros(shape, dtype=bool)
+                for c2 in range(c):
+                    clash |= col == g[..., c2]
+                if not clash.any():
+                    break
+                col[clash] = rng.choice(K, size=int(clash.sum()), p=p)
+            g[..., c] = col
     else:
         raise ValueError(kind)
     return np.ascontiguousarray(g, dtype=np.int32)

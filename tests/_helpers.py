@@ -52,6 +52,27 @@ def margin_filtered(wl, parts=("assign", "attn"), max_rounds=30):
     return x
 
 
+def margin_filtered_topk(wl, k, parts=("assign", "attn"), max_rounds=40):
+    """margin_filtered for top-k selection: every gap that decides a token's k
+    best centroids and their order (ranks 1..k+1) is at least MARGIN."""
+    x = synth.draw(wl, parts)
+    gid, mg = ref.assign_topk(x["h"], x["W"], x["C"], k)
+    for attempt in range(1, max_rounds + 1):
+        bad = np.argwhere((mg < MARGIN).any(axis=1))
+        if len(bad) == 0:
+            break
+        synth.redraw_hidden(wl, x, bad, attempt)
+        hb = x["h"][bad[:, 0], bad[:, 1]][None]
+        g2, m2 = ref.assign_topk(hb, x["W"], x["C"], k)
+        gid[bad[:, 0], :, bad[:, 1]] = g2[0].transpose(1, 0, 2)
+        mg[bad[:, 0], :, bad[:, 1]] = m2[0].T
+    else:
+        raise RuntimeError("margin filter did not converge")
+    x["gid_ref"] = gid
+    x["margin"] = mg
+    return x
+
+
 def assert_close(got, want, dtype, what=""):
     got = np.asarray(got, np.float64)
     want = np.asarray(want, np.float64)

@@ -34,13 +34,14 @@ def test_every_declared_symbol_is_exported(fz):
     for name in _declared():
         assert hasattr(lib, name), name
     assert set(fz.EXPORTED) == set(_declared())
-    assert lib.focus_abi_version() == 1
+    assert lib.focus_abi_version() == 2
 
 
 def test_struct_layouts_match_header(fz):
     assert ctypes.sizeof(fz.Params) == 12 * 4
     assert ctypes.sizeof(fz.Item) == 8 * 4
     assert ctypes.sizeof(fz.Index) == 9 * 8 + 2 * 4
+    assert ctypes.sizeof(fz.IndexTopk) == 2 * ctypes.sizeof(fz.Index) + 2 * 8 + 2 * 4
 
 
 def test_status_strings(fz):
@@ -94,3 +95,47 @@ def test_null_misaligned_and_small_workspace(fz):
     assert lib.focus_dense_causal_fwd(ctypes.byref(p), ok, ok, ok, ok, None, ok, need, None) == 2
     assert lib.focus_workspace_init(mis, None) == 1
     del idx
+
+
+# ------------------------------------------------------- top-k membership ---
+
+def test_topk_workspace_sizes(fz):
+    p = fz.make_params(B=1, H=32, H_kv=8, n=32768, d=128, D=4096, d_g=64, K=4, A=1, w=512)
+    one, two = fz.focus_workspace_bytes_topk(p, 1), fz.focus_workspace_bytes_topk(p, 2)
+    assert one >= fz.focus_workspace_bytes(p) - 256 and one % 256 == 0
+    # entry partials (2n rows), pair and merged partials (n rows each), bf16
+    assert two >= 4 * 32 * 32768 * 128 * 2 and two > one
+    assert fz.focus_workspace_bytes_topk(p, 0) == 0
+    assert fz.focus_workspace_bytes_topk(p, 3) == 0
+    p.K = 91                                    # 4095 group pairs: the largest K for k = 2
+    assert fz.focus_workspace_bytes_topk(p, 2) > 0
+    p.K = 92
+    assert fz.focus_workspace_bytes_topk(p, 2) == 0
+    assert fz.focus_workspace_bytes_topk(p, 1) > 0
+    p.K = 1                                     # two distinct groups need K >= 2
+    assert fz.focus_workspace_bytes_topk(p, 2) == 0
+
+
+def test_topk_argument_checks(fz):
+    lib = fz.lib()
+    p = fz.make_params(B=1, H=4, H_kv=2, n=64, d=64, D=64, d_g=32, K=4, A=1, w=8)
+    ok = ctypes.c_void_p(1 << 20)
+    mis = ctypes.c_void_p((1 << 20) + 8)
+    need = fz.focus_workspace_bytes_topk(p, 2)
+    assert lib.focus_assign_topk(ctypes.byref(p), 3, ok, ok, ok, ok, ok, need, None) == 1
+    assert lib.focus_assign_topk(ctypes.byref(p), 2, mis, ok, ok, ok, ok, need, None) == 1
+    assert lib.focus_assign_topk(ctypes.byref(p), 2, ok, ok, ok, ok, ok, need - 256, None) == 3
+    idx = fz.IndexTopk()
+    assert lib.focus_build_index_topk(ctypes.byref(p), 2, ok, None, ok, need, None) == 1
+    assert lib.focus_build_index_topk(ctypes.byref(p), 2, mis, ctypes.byref(idx), ok, need, None) == 1
+    assert lib.focus_build_index_topk(ctypes.byref(p), 2, ok, ctypes.byref(idx), ok, need - 256, None) == 3
+    q = fz.make_params(B=1, H=4, H_kv=2, n=64, d=64, D=64, d_g=32, K=100, A=1, w=8)
+    assert lib.focus_build_index_topk(ctypes.byref(q), 2, ok, ctypes.byref(idx), ok, 1 << 40, None) == 2
+    # attention: an index that is not one (k outside {1, 2}, null arrays) is refused
+    assert lib.focus_attention_topk_fwd(ctypes.byref(p), ok, ok, ok, None, ok, None, ok, need, None) == 1
+    idx.k = 3
+    assert lib.focus_attention_topk_fwd(ctypes.byref(p), ok, ok, ok, ctypes.byref(idx), ok, None, ok, need,
+                                        None) == 1
+    idx.k = 2
+    assert lib.focus_attention_topk_fwd(ctypes.byref(p), ok, ok, ok, ctypes.byref(idx), ok, None, ok, need,
+                                        None) == 1
