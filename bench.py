@@ -16,6 +16,9 @@ roofline     the dominant attention kernel's achieved TFLOP/s (its algorithmic
              FLOPs per launch over its CUDA-event duration) against the measured
              sustained bf16 tensor peak.
 cpu_baseline the fp64 oracle timed on the host cores on a bounded row sample.
+comparators  plain causal attention (ms_dense_causal) and the pages' own
+             two-call strategy with a separate combine (ms_two_call_attention)
+             on the same inputs and index.
 
 --topk 2 runs the top-2 membership layer instead (focus_assign_topk ->
 focus_build_index_topk -> focus_attention_topk_fwd; each token in its two
@@ -355,6 +358,18 @@ def run_ours(args, wl, world, rank, local):
     torch.cuda.synchronize()
     t_dense = statistics.mean(a0.elapsed_time(a1) for a0, a1 in dev_ev)
 
+    # two-call comparator (group call, window call, separate combine) on the same index
+    for _ in range(3):
+        fz.focus_attention_two_call_fwd(p, d["Q"], d["K"], d["V"], idx, O, None, ws)
+    tc_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(dn)]
+    for a0, a1 in tc_ev:
+        flush.zero_()
+        a0.record()
+        fz.focus_attention_two_call_fwd(p, d["Q"], d["K"], d["V"], idx, O, None, ws)
+        a1.record()
+    torch.cuda.synchronize()
+    t_two = statistics.mean(a0.elapsed_time(a1) for a0, a1 in tc_ev)
+
     # end to end through the host-buffer entry point
     host = {k: d[k].cpu().pin_memory() for k in ("h", "W", "C", "Q", "K", "V")}
     host["O"] = torch.empty(O.shape, dtype=O.dtype).pin_memory()
@@ -385,9 +400,9 @@ def run_ours(args, wl, world, rank, local):
             raise RuntimeError("host-buffer path and device path disagree")
 
     names = list(t)
-    red = max_over_ranks([t_step, t_attn, t_dense, t_e2e] + [t[k] for k in names], dist, "cuda")
-    t_step, t_attn, t_dense, t_e2e = red[:4]
-    t = dict(zip(names, red[4:]))
+    red = max_over_ranks([t_step, t_attn, t_dense, t_e2e, t_two] + [t[k] for k in names], dist, "cuda")
+    t_step, t_attn, t_dense, t_e2e, t_two = red[:5]
+    t = dict(zip(names, red[5:]))
 
     peaks, peak_kind = load_peaks()
     peak_tc = float(peaks["bf16_tflops_sustained"])
@@ -412,6 +427,7 @@ def run_ours(args, wl, world, rank, local):
         "attention_tflops": f_attn / (t_attn * 1e-3) / 1e12,
         "ms_breakdown": t, "ms_attention": t_attn, "ms_dense_causal": t_dense,
         "speedup_vs_dense": t_dense / t_step, "speedup_vs_dense_attention_only": t_dense / t_attn,
+        "ms_two_call_attention": t_two, "fused_vs_two_call": t_two / t_attn,
         "roofline": {"bound": "tensor", "kernel": "attn_tc_" + dom, "achieved": achieved, "peak": peak_tc,
                      "unit": "TFLOP/s", "frac": achieved / peak_tc,
                      "traffic": tr["bytes_per_launch"] if tr else None,

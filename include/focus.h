@@ -212,6 +212,21 @@ FOCUS_API focus_status_t focus_dense_causal_fwd(const focus_params_t* p, const v
                                       const void* V, void* O, float* lse_opt, void* ws,
                                       size_t ws_bytes, void* stream);
 
+/* The two-call comparator: the same operation and tensors as
+ * focus_attention_fwd, run the way the pages run it ("Why Attend to
+ * Everything? Focus is the Key" 2.3; "Focus: Learning Which Attention Pairs
+ * Matter" 3.3): an in-group causal call (the group pass, writing its partial
+ * to ws), a standalone sliding-window attention call writing O and its LSE,
+ * and a separate log-sum-exp combine that updates O in place.
+ * focus_attention_fwd instead merges inside the local pass; this call exists
+ * to measure that fusion.  idx, ws, errors and lse_opt as focus_attention_fwd
+ * (lse_opt must not alias ws). */
+FOCUS_API focus_status_t focus_attention_two_call_fwd(const focus_params_t* p, const void* Q,
+                                                      const void* K, const void* V,
+                                                      const focus_index_t* idx, void* O,
+                                                      float* lse_opt, void* ws, size_t ws_bytes,
+                                                      void* stream);
+
 /* The whole layer from HOST buffers: copies h, W, C, Q, K, V from host memory
  * (pinned, for the copies to overlap) into the caller's device buffers, runs
  * assign -> index -> attention on `stream`, and copies O back to host memory.

@@ -24,7 +24,7 @@ size_t elt_size(int dtype) { return dtype == FOCUS_BF16 ? 2 : 4; }
 // Byte offsets of every region inside the workspace.
 struct Layout {
   size_t err, segcnt, counts, offsets, tile_base, perm, rank, far_tok, far_slot, items, cost,
-      order, n_items, Ks, Vs, O_far, lse_far, total;
+      order, n_items, Ks, Vs, O_far, lse_far, lse_loc, total;
   int nseg, max_items;
 };
 
@@ -75,6 +75,8 @@ Layout layout_of(const focus_params_t* p) {
   // item's end to (never read)
   L.O_far = take((static_cast<size_t>(p->B) * p->H * n + kTileM) * p->d * es);
   L.lse_far = take(static_cast<size_t>(p->B) * p->H * n * 4);
+  // the two-call comparator's window-call LSE
+  L.lse_loc = take(static_cast<size_t>(p->B) * p->H * n * 4);
   L.total = o;
   return L;
 }
@@ -542,6 +544,58 @@ focus_status_t focus_dense_causal_fwd(const focus_params_t* p, const void* Q, co
       !make_map(&to, O, p->d, p->n, qplanes, 128, 3))
     return FOCUS_ERR_CUDA;
   return cuda_status(launch_attn_tc_bf16(a, &tq, &tk, &tv, &to, &to, p->d, kModeDense, 0, sm_count(), st));
+}
+
+focus_status_t focus_attention_two_call_fwd(const focus_params_t* p, const void* Q, const void* K,
+                                            const void* V, const focus_index_t* idx, void* O,
+                                            float* lse_opt, void* ws, size_t ws_bytes, void* stream) {
+  if (!idx || !idx->perm || !idx->farlen_tok || !idx->farlen_slot || !idx->items || !idx->order ||
+      !idx->n_items)
+    return FOCUS_ERR_INVALID_ARG;
+  if (params_ok(p) && (idx->max_items != layout_of(p).max_items || idx->w_eff != (p->w > 1 ? p->w : 1)))
+    return FOCUS_ERR_INVALID_ARG;
+  if (focus_status_t s = attention_common(p, Q, K, V, O, lse_opt, ws, ws_bytes)) return s;
+  const Layout L = layout_of(p);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  AttnArgs a = attn_args(p, Q, K, V, O, lse_opt, ws, L);
+  a.perm = idx->perm;
+  a.farlen_tok = idx->farlen_tok;
+  a.farlen_slot = idx->farlen_slot;
+  a.items = idx->items;
+  a.order = idx->order;
+  a.n_items = idx->n_items;
+  // call 2 of the pair: a plain sliding-window attention (the dense mode with
+  // the Focus window) writing O and its own LSE
+  AttnArgs win = a;
+  win.lse = at<float>(ws, L.lse_loc);
+  CombineLaunch cl{O, win.lse, a.O_far, a.lse_far, idx->farlen_tok, lse_opt,
+                   p->B, p->H, p->H_kv, p->A, p->n, p->d};
+  cudaError_t e;
+  if (p->dtype == FOCUS_F32) {
+    e = launch_attn_simt_f32(a, p->d, kModeGroup, L.max_items, st);
+    if (e == cudaSuccess) e = launch_attn_simt_f32(win, p->d, kModeDense, 0, st);
+    if (e == cudaSuccess) e = launch_lse_combine(cl, p->dtype, st);
+    return cuda_status(e);
+  }
+  void* Ks = at<void>(ws, L.Ks);
+  void* Vs = at<void>(ws, L.Vs);
+  e = launch_permute_kv_bf16(K, V, Ks, Vs, idx->perm, p->B, p->H_kv, p->n, p->n, 0, p->d, p->A, st);
+  if (e != cudaSuccess) return FOCUS_ERR_CUDA;
+  CUtensorMap tq, tk, tv, tks, tvs, to, tqg, tofs;
+  const uint64_t planes = static_cast<uint64_t>(p->B) * p->H_kv;
+  const uint64_t qplanes = static_cast<uint64_t>(p->B) * p->H;
+  if (!make_map(&tq, Q, p->d, p->n, qplanes, 128, 3) ||
+      !make_map(&tk, K, p->d, p->n, planes, 128, 3) || !make_map(&tv, V, p->d, p->n, planes, 128, 3) ||
+      !make_map(&tks, Ks, p->d, p->n, planes, 128, 3) || !make_map(&tvs, Vs, p->d, p->n, planes, 128, 3) ||
+      !make_map(&to, O, p->d, p->n, qplanes, 128, 3) ||
+      !make_map(&tqg, Q, p->d, qplanes * p->n, 1, 1, 2) ||
+      !make_map(&tofs, a.O_far, p->d, qplanes * p->n + kTileM, 1, 1, 2))
+    return FOCUS_ERR_CUDA;
+  const int sms = sm_count();
+  e = launch_attn_tc_bf16(a, &tqg, &tks, &tvs, &tofs, &tofs, p->d, kModeGroup, L.max_items, sms, st);
+  if (e == cudaSuccess) e = launch_attn_tc_bf16(win, &tq, &tk, &tv, &to, &to, p->d, kModeDense, 0, sms, st);
+  if (e == cudaSuccess) e = launch_lse_combine(cl, p->dtype, st);
+  return cuda_status(e);
 }
 
 focus_status_t focus_layer_fwd_host(const focus_params_t* p, const void* host_h,

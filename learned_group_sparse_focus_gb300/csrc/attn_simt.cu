@@ -10,8 +10,9 @@
 //               entry i * k + c of token i).
 //   local pass  natural-order rows, keys j in [i - w + 1, i]; merges the
 //               group partial (when the row has far keys) by log-sum-exp and
-//               writes O.  The dense comparator is the local pass with every
-//               j <= i kept and no partial.
+//               writes O.  The dense mode is the local pass with no partial:
+//               with w = n every j <= i is kept (the comparator), with the
+//               Focus window it is a standalone sliding-window call.
 // A CTA holds 32 query rows, four threads per row (each owns d/4 of q and of
 // the accumulator); keys stream through shared memory 32 at a time.
 #include "common.cuh"
@@ -95,10 +96,10 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
     const int i0 = qt * kRows;
     const int i = i0 + r;
     key_end = min(a.n, i0 + kRows);
-    key_begin = MODE == kModeDense ? 0 : max(0, i0 - a.w + 1);
+    key_begin = max(0, i0 - a.w + 1);
     if (i < a.n) {
       row_pos = i;
-      lo = MODE == kModeDense ? 0 : i - a.w + 1;
+      lo = i - a.w + 1;
       hi = i;
     } else {
       row_pos = -1;

@@ -16,7 +16,9 @@
 //          i * k + c, whose query is token i).
 //   local  128 consecutive tokens, keys j in [i - w + 1, i]; merges the group
 //          partial by log-sum-exp when the row has far keys; writes O.
-//   dense  128 consecutive tokens, every j <= i (the comparator).
+//   dense  128 consecutive tokens, keys j in [i - w + 1, i] and no partial:
+//          plain causal attention with w = n (the comparator), a standalone
+//          sliding-window call with the Focus window.
 //
 // S = Q K^T reads Q and K from shared memory; O += P V reads P from TMEM and
 // V from shared memory.  TMEM (512 columns for d = 128): S double buffer
@@ -180,7 +182,7 @@ __device__ __forceinline__ void decode_unit(const AttnArgs& a, int u, Unit& U) {
     asg = a.A == 1 ? 0 : kv;
     U.row0 = qt * kBM;
     U.nrows = min(kBM, a.n - U.row0);
-    U.t0 = MODE == kModeDense ? 0 : max(0, U.row0 - a.w + 1) / kBN;
+    U.t0 = max(0, U.row0 - a.w + 1) / kBN;
     U.t1 = (U.row0 + U.nrows - 1) / kBN;
     U.ybase = 0;
   }
@@ -698,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else if (st.valid) {
         st.pos = U.row0 + r;
-        lo = MODE == kModeDense ? 0 : st.pos - a.w + 1;
+        lo = st.pos - a.w + 1;
         hi = st.pos;
         if (MODE == kModeLocal) {
           // this row's group partial: flag and LSE now, O row into L2

@@ -130,4 +130,17 @@ struct MergeLaunch {
 };
 cudaError_t launch_topk_merge(const MergeLaunch& L, int dtype, cudaStream_t st);
 
+// two_call.cu: the two-call comparator's separate log-sum-exp combine of the
+// window call's output (in place in O) with the group partial.
+struct CombineLaunch {
+  void* O;                      // [B*H*n, d] in: window-call output, out: merged
+  const float* lse_loc;         // [B*H*n]    window-call LSE
+  const void* O_far;            // [B*H*n (+ spare), d] group partial
+  const float* lse_far;         // [B*H*n]
+  const int32_t* farlen_tok;    // [B*A][n]   > 0: the row has far keys
+  float* lse_out;               // [B*H*n] merged LSE, or null (must not alias lse_loc)
+  int B, H, H_kv, A, n, d;
+};
+cudaError_t launch_lse_combine(const CombineLaunch& L, int dtype, cudaStream_t st);
+
 }  // namespace focus

@@ -68,6 +68,8 @@ def _load():
         "focus_attention_fwd_timed": ([P, vp, vp, vp, ctypes.POINTER(Index), vp, vp, vp, ctypes.c_size_t,
                                        vp, ctypes.POINTER(ctypes.c_void_p)], ctypes.c_int),
         "focus_dense_causal_fwd": ([P, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp], ctypes.c_int),
+        "focus_attention_two_call_fwd": ([P, vp, vp, vp, ctypes.POINTER(Index), vp, vp, vp, ctypes.c_size_t,
+                                          vp], ctypes.c_int),
         "focus_layer_fwd_host": ([P] + [vp] * 7 + [vp] * 8 + [vp, ctypes.c_size_t, vp], ctypes.c_int),
         "focus_check_errors": ([vp, vp], ctypes.c_int),
         "focus_build_index_static": ([P, vp, ctypes.POINTER(Index), vp, vp], ctypes.c_int),
@@ -94,7 +96,8 @@ EXPORTED = ("focus_abi_version", "focus_status_string", "focus_workspace_bytes",
             "focus_workspace_init", "focus_assign", "focus_build_index", "focus_attention_fwd",
             "focus_attention_fwd_timed", "focus_dense_causal_fwd", "focus_layer_fwd_host", "focus_check_errors",
             "focus_build_index_static", "focus_workspace_bytes_topk", "focus_assign_topk",
-            "focus_build_index_topk", "focus_attention_topk_fwd", "focus_attention_topk_fwd_timed")
+            "focus_build_index_topk", "focus_attention_topk_fwd", "focus_attention_topk_fwd_timed",
+            "focus_attention_two_call_fwd")
 
 
 def lib():
@@ -178,6 +181,13 @@ def focus_attention_fwd_timed(p: Params, Q, K, V, idx: Index, O, lse, ws, events
     _check("focus_attention_fwd_timed",
            _lib.focus_attention_fwd_timed(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), ctypes.byref(idx),
                                           _ptr(O), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream), arr))
+
+
+def focus_attention_two_call_fwd(p: Params, Q, K, V, idx: Index, O, lse, ws, stream=None):
+    """The two-call comparator (group call, window call, separate combine)."""
+    _check("focus_attention_two_call_fwd",
+           _lib.focus_attention_two_call_fwd(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), ctypes.byref(idx),
+                                             _ptr(O), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def focus_dense_causal_fwd(p: Params, Q, K, V, O, lse, ws, stream=None):
