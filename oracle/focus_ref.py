@@ -33,13 +33,22 @@ What the oracle computes (fp64 throughout, no blocking or fusion):
                build_index_topk (memberships sorted by (group, position)),
                keep_mask_rows_topk and attention_rows_topk are the same
                definitions written for k memberships.
+  sinkhorn     the training-time soft assignment ([FocusJA] 2.1, 2.3;
+               [FocusKO] 2.2): the matrix exp(S / tau) of token-to-centroid
+               scores is scaled to be doubly stochastic with every token's
+               row summing to 1 and every group's column to n / K (equal
+               group sizes), by T rounds of Sinkhorn-Knopp scaling (columns,
+               then rows).  scores() gives S = (h W_a^T) C_a^T.
 
 Readings where the pages are silent (each listed in the design notes):
   similarity = dot product; no projection bias; window strictly i - j < w;
   scale = 1/sqrt(d) by default; GQA head map kv = floor(h * H_kv / H);
   each kept pair counted once (union of the local and the group rule);
   top-k: the k best fp32 scores, lower index first among equal scores, and a
-  pair whose tokens share several groups is still one kept pair.
+  pair whose tokens share several groups is still one kept pair;
+  Sinkhorn: temperature tau and round count T are parameters (the pages give
+  neither), each round normalises columns first and rows last, and the
+  marginals are 1 per token and n / K per group.
 
 Parity pins: every function here is checked by tests/test_oracle_pins.py
 against closed forms, brute force, special cases and invariants.
@@ -56,7 +65,7 @@ __all__ = [
     "dense_causal", "lse_merge", "attention_bruteforce", "attention_weights_rows",
     "kv_head", "assignment_of_head",
     "assign_topk", "build_index_topk", "keep_mask_rows_topk", "attention_rows_topk",
-    "attention_bruteforce_topk",
+    "attention_bruteforce_topk", "scores", "sinkhorn",
 ]
 
 
@@ -469,3 +478,42 @@ def attention_bruteforce_topk(q, k, v, G, w: int, scale: float):
             O[i, t] = math.fsum(e[r] * float(v[kept[r], t]) for r in range(len(kept))) / tot
         L[i] = mx + math.log(tot)
     return O, L
+
+
+# --------------------------------------------------------------- sinkhorn ---
+
+def scores(h, W, C):
+    """S[b, a, i, k] = p . c_k with p = W_a h_i (fp64, no bias).  [FocusJA] 2.1."""
+    h = _f64(h)
+    W = _f64(W)
+    C = _f64(C)
+    B, n, _ = h.shape
+    A = W.shape[0]
+    K = C.shape[1]
+    out = np.empty((B, A, n, K))
+    for b in range(B):
+        for a in range(A):
+            out[b, a] = (h[b] @ W[a].T) @ C[a].T
+    return out
+
+
+def sinkhorn(S, T: int, tau: float = 1.0):
+    """Sinkhorn-Knopp scaling of exp(S / tau) for every leading index.
+    [FocusJA] 2.3 and [FocusKO] 2.2: the forward assignment matrix is forced
+    to be doubly stochastic so that every group receives an equal share of
+    the tokens.
+
+    S [..., n, K] -> G [..., n, K] (fp64).  Each of the T >= 1 rounds scales
+    the columns to sum n / K, then the rows to sum 1, in the plain probability
+    domain.  exp is taken after subtracting the matrix's largest S / tau: a
+    constant factor, which the first column step removes exactly.
+    """
+    assert T >= 1 and tau > 0
+    S = _f64(S)
+    n, K = S.shape[-2], S.shape[-1]
+    X = S / tau
+    M = np.exp(X - X.max(axis=(-2, -1), keepdims=True))
+    for _ in range(T):
+        M = M * ((n / K) / M.sum(axis=-2, keepdims=True))
+        M = M / M.sum(axis=-1, keepdims=True)
+    return M

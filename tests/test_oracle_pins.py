@@ -525,6 +525,110 @@ def test_topk_pins_catch_planted_mistakes():
         assert any(list(np.nonzero(M[i])[0]) != gd["kept"][i] for i in range(n)), bad.__name__
 
 
+# --------------------------------------------------------------- sinkhorn ---
+
+def test_scores_closed_form():
+    # W picks coordinates, C are signed basis rows: S is a signed coordinate of h
+    h = np.array([[[3.0, -1.0, 2.0], [0.5, 4.0, -2.0]]])
+    W = np.array([[[1.0, 0.0, 0.0], [0.0, 0.0, 1.0]]])         # p = (h0, h2)
+    C = np.array([[[1.0, 0.0], [0.0, -1.0], [2.0, 1.0]]])
+    S = ref.scores(h, W, C)
+    assert S[0, 0].tolist() == [[3.0, -2.0, 8.0], [0.5, 2.0, -1.0]]
+
+
+def test_sinkhorn_marginals_converge():
+    # Sinkhorn's theorem: a positive matrix scales to the prescribed marginals
+    rng = np.random.default_rng(31)
+    for n, K in ((64, 4), (300, 16), (33, 33)):
+        S = rng.standard_normal((n, K)) * 2
+        G = ref.sinkhorn(S, 200)
+        np.testing.assert_allclose(G.sum(axis=1), 1.0, atol=1e-12)
+        np.testing.assert_allclose(G.sum(axis=0), n / K, atol=1e-8)
+        assert np.all(G > 0)
+
+
+def test_sinkhorn_rank_one_is_uniform_after_one_round():
+    # exp(a_i + b_k) is rank one: one column and one row step give 1/K
+    rng = np.random.default_rng(32)
+    a, b = rng.standard_normal(50), rng.standard_normal(7)
+    G = ref.sinkhorn(a[:, None] + b[None, :], 1, tau=0.7)
+    np.testing.assert_allclose(G, 1.0 / 7, atol=1e-14)
+
+
+def test_sinkhorn_doubly_stochastic_input_is_a_fixed_point():
+    # n = K: a convex combination of permutation matrices (Birkhoff) has unit
+    # row and column sums already, so every round returns it unchanged
+    rng = np.random.default_rng(33)
+    n = 6
+    wts = rng.dirichlet(np.ones(4))
+    P = sum(wv * np.eye(n)[rng.permutation(n)] for wv in wts)
+    P = 0.9 * P + 0.1 / n                       # strictly positive, still doubly stochastic
+    for T in (1, 3):
+        np.testing.assert_allclose(ref.sinkhorn(np.log(P), T), P, atol=1e-14)
+
+
+def test_sinkhorn_column_shift_invariance_and_row_shift_at_convergence():
+    rng = np.random.default_rng(34)
+    S = rng.standard_normal((40, 5))
+    b = rng.standard_normal(5) * 3
+    a = rng.standard_normal(40) * 3
+    for T in (1, 2, 5):   # the first step is a column scaling: exact for any T
+        np.testing.assert_allclose(ref.sinkhorn(S + b[None, :], T), ref.sinkhorn(S, T), atol=1e-13)
+    # a per-row shift changes finite rounds but not the limit
+    assert not np.allclose(ref.sinkhorn(S + a[:, None], 1), ref.sinkhorn(S, 1), atol=1e-6)
+    np.testing.assert_allclose(ref.sinkhorn(S + a[:, None], 400), ref.sinkhorn(S, 400), atol=1e-9)
+
+
+def test_sinkhorn_equivariance_and_special_cases():
+    rng = np.random.default_rng(35)
+    S = rng.standard_normal((2, 30, 6))
+    G = ref.sinkhorn(S, 4, tau=1.5)
+    pr, pc = rng.permutation(30), rng.permutation(6)
+    np.testing.assert_allclose(ref.sinkhorn(S[:, pr][:, :, pc], 4, tau=1.5), G[:, pr][:, :, pc], atol=1e-14)
+    np.testing.assert_allclose(ref.sinkhorn(S[:, :, :1], 3), 1.0, atol=0)        # K = 1
+    np.testing.assert_allclose(ref.sinkhorn(np.zeros((9, 3)), 2), 1.0 / 3, atol=1e-15)
+    # tau scales the scores: sinkhorn(S, tau) == sinkhorn(S / tau, 1)
+    np.testing.assert_allclose(ref.sinkhorn(S, 3, tau=0.25), ref.sinkhorn(S * 4, 3), atol=1e-13)
+
+
+def test_sinkhorn_one_round_by_hand():
+    # 2 x 2, T = 1, worked by hand: exp(S) = [[1, 2], [3, 4]]; n / K = 1.
+    # columns: [[1/4, 2/6], [3/4, 4/6]]; rows: [[3/7, 4/7], [9/17, 8/17]]
+    S = np.log(np.array([[1.0, 2.0], [3.0, 4.0]]))
+    np.testing.assert_allclose(ref.sinkhorn(S, 1), [[3 / 7, 4 / 7], [9 / 17, 8 / 17]], atol=1e-15)
+
+
+def test_sinkhorn_pins_catch_planted_mistakes():
+    S = np.log(np.array([[1.0, 2.0], [3.0, 4.0]]))
+    want = np.array([[3 / 7, 4 / 7], [9 / 17, 8 / 17]])
+
+    def rows_first(SS, T):             # order of the two steps swapped
+        M = np.exp(SS)
+        for _ in range(T):
+            M = M / M.sum(axis=-1, keepdims=True)
+            M = M * ((SS.shape[-2] / SS.shape[-1]) / M.sum(axis=-2, keepdims=True))
+        return M
+
+    def softmax_only(SS, T):           # the column step dropped: a row softmax
+        M = np.exp(SS)
+        return M / M.sum(axis=-1, keepdims=True)
+
+    def scores_not_exponentiated(SS, T):
+        M = SS - SS.min() + 1.0
+        for _ in range(T):
+            M = M * ((SS.shape[-2] / SS.shape[-1]) / M.sum(axis=-2, keepdims=True))
+            M = M / M.sum(axis=-1, keepdims=True)
+        return M
+
+    for bad in (rows_first, softmax_only, scores_not_exponentiated):
+        assert not np.allclose(bad(S, 1), want, atol=1e-6), bad.__name__
+    # (the column target's value alone is not a slip: with equal targets the
+    # row step removes any common factor, so columns reach n / K at the limit)
+    S3 = np.log(np.array([[1.0, 2.0], [3.0, 4.0], [5.0, 1.0]]))
+    np.testing.assert_allclose(ref.sinkhorn(S3, 300).sum(axis=0), 1.5, atol=1e-9)
+    assert not np.allclose(softmax_only(S3, 300).sum(axis=0), 1.5, atol=1e-3)
+
+
 # ------------------------------------------------ planted oracle mistakes ---
 
 def test_pins_catch_planted_mistakes(monkeypatch):
