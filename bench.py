@@ -25,6 +25,11 @@ focus_build_index_topk -> focus_attention_topk_fwd; each token in its two
 best groups, a far pair kept when the tokens' group sets meet), by default
 with the pages' K = 4 (--K).  Kept pairs are counted once.
 
+--sinkhorn T times the training-time soft assignment instead: scores
+(focus_assign_scores) and T Sinkhorn rounds (focus_sinkhorn_fwd) on the
+workload's assignment shape; value = algorithmic GB/s of the Sinkhorn rounds
+(each round streams S twice, the last also writes G).
+
 --impl reference times the oracle alone (the comparison arm of this build).
 Under torchrun (N > 1) every rank runs its own replica of the workload (weak
 scaling); there is no data-path collective.
@@ -631,6 +636,66 @@ def run_ours_topk(args, wl, world, rank, local):
         dist.destroy_process_group()
 
 
+def run_ours_sinkhorn(args, wl, world, rank, local):
+    import torch
+    from learned_group_sparse_focus_gb300 import synth
+    from learned_group_sparse_focus_gb300 import focus as fz
+
+    T = args.sinkhorn
+    torch.cuda.set_device(local)
+    x = synth.draw(wl, parts=("assign",))
+
+    def dev(a):
+        if wl.dtype == "bf16":
+            return torch.from_numpy(synth.bf16_bits(a)).view(torch.bfloat16).cuda()
+        return torch.from_numpy(a).cuda()
+
+    h, W, C = (dev(x[k]) for k in ("h", "W", "C"))
+    p = fz.params_from_workload(wl)
+    ws = fz.alloc_workspace_sinkhorn(p)
+    S = torch.empty((wl.B, wl.A, wl.n, wl.K), dtype=torch.float32, device="cuda")
+    G = torch.empty_like(S)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup):
+        fz.focus_assign_scores(p, h, W, C, S, ws)
+        fz.focus_sinkhorn_fwd(p, T, 1.0, S, G, ws)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    with ClockSampler(int(os.environ.get("FOCUS_NVSMI_INDEX", local))) as clk:
+        for e in ev:
+            flush.zero_()
+            e[0].record()
+            fz.focus_assign_scores(p, h, W, C, S, ws)
+            e[1].record()
+            fz.focus_sinkhorn_fwd(p, T, 1.0, S, G, ws)
+            e[2].record()
+        torch.cuda.synchronize()
+    if fz.focus_check_errors(ws) != 0:
+        raise RuntimeError("device error")
+    t_sc = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    t_sk = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    sbytes = S.numel() * 4
+    alg = (2 * T + 1) * sbytes + 4 * wl.B * wl.A * wl.n * T        # S twice per round, G once, u per round
+    peaks, peak_kind = load_peaks()
+    gbs = alg / (t_sk * 1e-3) / 1e9
+    line = {
+        "metric": "Sinkhorn forward algorithmic GB/s", "value": gbs, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_sc + t_sk, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "rounds": T, "tau": 1.0,
+                   **{k: getattr(wl, k) for k in ("B", "n", "D", "d_g", "K", "A")},
+                   "S_bytes": sbytes, "l2": "flushed (256 MB write) before every timed step"},
+        "ms_breakdown": {"scores": t_sc, "sinkhorn": t_sk, "per_round": t_sk / T},
+        "roofline": {"bound": "hbm", "kernel": "sinkhorn rounds", "achieved": gbs,
+                     "peak": float(peaks["hbm_gbs"]), "unit": "GB/s", "frac": gbs / float(peaks["hbm_gbs"]),
+                     "traffic": None, "peak_source": f"{peak_kind} hbm_gbs",
+                     "note": "S is L2-resident when smaller than ~100 MB, so frac can exceed 1"},
+        "gpu_launches": (1 + 3 * T) * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -644,6 +709,7 @@ def main():
     ap.add_argument("--topk", type=int, default=1, choices=[1, 2],
                     help="groups per token; 2 runs the top-2 membership layer")
     ap.add_argument("--K", type=int, default=None, help="centroids (default: 4 with --topk 2)")
+    ap.add_argument("--sinkhorn", type=int, default=0, help="time T Sinkhorn rounds instead")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -653,6 +719,8 @@ def main():
     world, rank, local = dist_env()
     if args.impl == "reference":
         run_reference(args, wl, world, rank)
+    elif args.sinkhorn > 0:
+        run_ours_sinkhorn(args, wl, world, rank, local)
     elif args.topk > 1:
         run_ours_topk(args, wl, world, rank, local)
     else:

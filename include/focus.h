@@ -328,6 +328,36 @@ FOCUS_API focus_status_t focus_attention_topk_fwd_timed(const focus_params_t* p,
                                                         float* lse_opt, void* ws, size_t ws_bytes,
                                                         void* stream, void* const* events);
 
+/* --------------------------------------------- Sinkhorn soft assignment ---
+ * The training-time assignment ("Focus: Learning Which Attention Pairs
+ * Matter" 2.1, 2.3; "Why Attend to Everything? Focus is the Key" 2.2): tokens
+ * are assigned softly to the K groups and Sinkhorn normalisation makes the
+ * n x K assignment matrix doubly stochastic, so every group gets an equal
+ * share of the tokens.  The pages give neither the temperature nor the number
+ * of rounds: both are arguments.  For each (b, a), with X = S / tau,
+ *   G = diag(e^u) exp(X) diag(e^v): every row of G sums to 1 and every column
+ *   to n / K in the limit; T rounds of Sinkhorn-Knopp scaling, each round
+ *   first the columns (to n / K) then the rows (to 1), from u = 0.
+ * Both calls take a Sinkhorn workspace of focus_sinkhorn_workspace_bytes(p)
+ * (256-byte aligned; error word first, as for the other calls). */
+FOCUS_API size_t focus_sinkhorn_workspace_bytes(const focus_params_t* p);
+
+/* All token-to-centroid scores: S[b,a,i,k] = (W[a] h[b,i]) . C[a,k], fp32
+ * accumulate, as focus_assign computes them before its argmax.
+ *   h, W, C as focus_assign; S [B, A, n, K] fp32 device output.
+ * Shapes and errors as focus_assign. */
+FOCUS_API focus_status_t focus_assign_scores(const focus_params_t* p, const void* h,
+                                             const void* W, const void* C, float* S, void* ws,
+                                             size_t ws_bytes, void* stream);
+
+/* Sinkhorn forward: S [B, A, n, K] fp32 scores -> G [B, A, n, K] fp32 soft
+ * assignment (G may be S: updated in place).  iters = T in [1, 10000],
+ * tau > 0 finite, else FOCUS_ERR_INVALID_ARG.  Log-domain arithmetic in fp32;
+ * 3 launches per round. */
+FOCUS_API focus_status_t focus_sinkhorn_fwd(const focus_params_t* p, int32_t iters, float tau,
+                                            const float* S, float* G, void* ws, size_t ws_bytes,
+                                            void* stream);
+
 /* Synchronises `stream`, reads and clears the device error word in ws.
  * Returns FOCUS_OK, FOCUS_ERR_BAD_GROUP_ID, FOCUS_ERR_TIMEOUT or FOCUS_ERR_CUDA. */
 FOCUS_API focus_status_t focus_check_errors(void* ws, void* stream);

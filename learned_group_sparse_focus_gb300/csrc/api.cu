@@ -829,6 +829,67 @@ focus_status_t focus_attention_topk_fwd(const focus_params_t* p, const void* Q, 
   return focus_attention_topk_fwd_timed(p, Q, K, V, idx, O, lse_opt, ws, ws_bytes, stream, nullptr);
 }
 
+// ------------------------------------------------ Sinkhorn soft assignment ---
+
+static size_t sinkhorn_layout(const focus_params_t* p, size_t* u, size_t* v, size_t* part) {
+  const size_t P = static_cast<size_t>(p->B) * p->A;
+  const int rpc = sinkhorn_rows_per_chunk(p->n);
+  const size_t chunks = (static_cast<size_t>(p->n) + rpc - 1) / rpc;
+  size_t o = align_up(kAlign);                       // error word
+  *u = o;
+  o = align_up(o + P * p->n * 4);
+  *v = o;
+  o = align_up(o + P * p->K * 4);
+  *part = o;
+  o = align_up(o + P * chunks * p->K * 8);
+  return o;
+}
+
+size_t focus_sinkhorn_workspace_bytes(const focus_params_t* p) {
+  if (!params_ok(p)) return 0;
+  size_t u, v, part;
+  return sinkhorn_layout(p, &u, &v, &part);
+}
+
+focus_status_t focus_assign_scores(const focus_params_t* p, const void* h, const void* W,
+                                   const void* C, float* S, void* ws, size_t ws_bytes,
+                                   void* stream) {
+  if (!params_ok(p)) return FOCUS_ERR_INVALID_ARG;
+  if (!h || !W || !C || !S || !aligned16(h) || !aligned16(W) || !aligned16(C) || !aligned16(S))
+    return FOCUS_ERR_INVALID_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return FOCUS_ERR_INVALID_ARG;
+  if (ws_bytes < focus_sinkhorn_workspace_bytes(p)) return FOCUS_ERR_WORKSPACE;
+  if (focus_status_t s = ensure_setup()) return s;
+  AssignLaunch al{h, W, C, nullptr, p->B, p->n, p->D, p->d_g, p->K, p->A, 1, at<int>(ws, 0), S};
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (p->dtype == FOCUS_F32) {
+    if (!(p->d_g == 16 || p->d_g == 32 || p->d_g == 64 || p->d_g == 128)) return FOCUS_ERR_UNSUPPORTED;
+    return cuda_status(launch_assign_f32(al, st));
+  }
+  if (!(p->d_g == 32 || p->d_g == 64 || p->d_g == 128)) return FOCUS_ERR_UNSUPPORTED;
+  if (p->A * p->d_g > 512 || p->D % 8 != 0) return FOCUS_ERR_UNSUPPORTED;
+  const int ncol = p->A * p->d_g;
+  CUtensorMap tm_h, tm_w;
+  if (!make_map(&tm_h, h, p->D, static_cast<uint64_t>(p->B) * p->n, 1, 128, 2) ||
+      !make_map(&tm_w, W, p->D, ncol, 1, ncol < 256 ? ncol : 256, 2))
+    return FOCUS_ERR_CUDA;
+  return cuda_status(launch_assign_bf16(al, &tm_h, &tm_w, st));
+}
+
+focus_status_t focus_sinkhorn_fwd(const focus_params_t* p, int32_t iters, float tau, const float* S,
+                                  float* G, void* ws, size_t ws_bytes, void* stream) {
+  if (!params_ok(p)) return FOCUS_ERR_INVALID_ARG;
+  if (iters < 1 || iters > 10000 || !(std::isfinite(tau) && tau > 0.f)) return FOCUS_ERR_INVALID_ARG;
+  if (!S || !G || !aligned16(S) || !aligned16(G)) return FOCUS_ERR_INVALID_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return FOCUS_ERR_INVALID_ARG;
+  size_t u, v, part;
+  if (ws_bytes < sinkhorn_layout(p, &u, &v, &part)) return FOCUS_ERR_WORKSPACE;
+  if (focus_status_t s = ensure_setup()) return s;
+  SinkhornLaunch L{S, G, at<float>(ws, u), at<float>(ws, v), at<float2>(ws, part), p->B * p->A, p->n,
+                   p->K, 1.f / tau};
+  return cuda_status(launch_sinkhorn(L, iters, static_cast<cudaStream_t>(stream)));
+}
+
 focus_status_t focus_check_errors(void* ws, void* stream) {
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return FOCUS_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -13,6 +13,8 @@
 // TMEM); the epilogue reads each token's row of p from TMEM and scores the
 // centroids with fp32 FMAs, so p is never rounded below fp32.
 // fp32: one thread per token on the CUDA cores.
+// With kScores the kernels write every score s_k (fp32, [B, A, n, K]) instead
+// of the top-k ids: the input of the Sinkhorn soft assignment.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -39,11 +41,12 @@ struct Top2 {
 };
 
 // ------------------------------------------------------------------ fp32 ---
-template <int DG>
+template <int DG, bool kScores>
 __global__ void __launch_bounds__(128) assign_f32_kernel(const float* __restrict__ h,
                                                          const float* __restrict__ W,
                                                          const float* __restrict__ C,
-                                                         int32_t* __restrict__ gid, int B, int n,
+                                                         int32_t* __restrict__ gid,
+                                                         float* __restrict__ scores, int B, int n,
                                                          int D, int K, int A, int topk) {
   const int tok = blockIdx.x * blockDim.x + threadIdx.x;
   if (tok >= B * n) return;
@@ -61,12 +64,15 @@ __global__ void __launch_bounds__(128) assign_f32_kernel(const float* __restrict
     }
     const float* Ca = C + static_cast<size_t>(a) * K * DG;
     Top2 t;
+    float* srow = kScores ? scores + ((static_cast<size_t>(b) * A + a) * n + i) * K : nullptr;
     for (int k = 0; k < K; ++k) {
       float s = 0.f;
 #pragma unroll
       for (int r = 0; r < DG; ++r) s = fmaf(p[r], __ldg(Ca + static_cast<size_t>(k) * DG + r), s);
-      t.push(k, s);
+      if (kScores) srow[k] = s;
+      else t.push(k, s);
     }
+    if (kScores) continue;
     int32_t* out = gid + ((static_cast<size_t>(b) * A + a) * n + i) * topk;
     out[0] = t.b1;
     if (topk == 2) out[1] = t.b2;
@@ -89,11 +95,11 @@ struct AssignCfg {
   static constexpr int kMinBlocks = kSmem <= 112 * 1024 ? 2 : 1;
 };
 
-template <int NALLOC>
+template <int NALLOC, bool kScores>
 __global__ void __launch_bounds__(128, AssignCfg<NALLOC>::kMinBlocks) assign_tc_kernel(
     const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
-    const __nv_bfloat16* __restrict__ C, int32_t* __restrict__ gid, int B, int n, int D, int d_g,
-    int K, int A, int topk, int* err) {
+    const __nv_bfloat16* __restrict__ C, int32_t* __restrict__ gid, float* __restrict__ scores,
+    int B, int n, int D, int d_g, int K, int A, int topk, int* err) {
   using Cfg = AssignCfg<NALLOC>;
   constexpr int S = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -197,6 +203,10 @@ __global__ void __launch_bounds__(128, AssignCfg<NALLOC>::kMinBlocks) assign_tc_
       }
     }
     Top2 t;
+    const bool keep = got && !*abort && tok < B * n;
+    float* srow = kScores && keep
+                      ? scores + ((static_cast<size_t>(tok / n) * A + a) * n + tok % n) * K
+                      : nullptr;
     for (int k0 = 0; k0 < K; k0 += kc) {
       const int kn = min(kc, K - k0);
       __syncthreads();
@@ -222,7 +232,13 @@ __global__ void __launch_bounds__(128, AssignCfg<NALLOC>::kMinBlocks) assign_tc_
           }
         }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) t.push(k0 + k + q, sc[q]);
+        for (int q = 0; q < 4; ++q) {
+          if (kScores) {
+            if (srow) srow[k0 + k + q] = sc[q];
+          } else {
+            t.push(k0 + k + q, sc[q]);
+          }
+        }
       }
       for (; k < kn; ++k) {
         const float* ck = Cs + k * d_g;
@@ -230,10 +246,14 @@ __global__ void __launch_bounds__(128, AssignCfg<NALLOC>::kMinBlocks) assign_tc_
 #pragma unroll
         for (int j = 0; j < 128; ++j)
           if (j < d_g) s = fmaf(p[j], ck[j], s);
-        t.push(k0 + k, s);
+        if (kScores) {
+          if (srow) srow[k0 + k] = s;
+        } else {
+          t.push(k0 + k, s);
+        }
       }
     }
-    if (got && !*abort && tok < B * n) {
+    if (!kScores && keep) {
       const int b = tok / n, i = tok % n;
       int32_t* out = gid + ((static_cast<size_t>(b) * A + a) * n + i) * topk;
       out[0] = t.b1;
@@ -252,9 +272,14 @@ template <int NALLOC>
 cudaError_t launch_tc(const AssignLaunch& L, const CUtensorMap* tm_h, const CUtensorMap* tm_w,
                       cudaStream_t st) {
   const int grid = (L.B * L.n + kBM - 1) / kBM;
-  assign_tc_kernel<NALLOC><<<grid, 128, AssignCfg<NALLOC>::kSmem, st>>>(
-      *tm_h, *tm_w, static_cast<const __nv_bfloat16*>(L.C), L.gid, L.B, L.n, L.D, L.d_g, L.K,
-      L.A, L.topk, L.err);
+  if (L.scores)
+    assign_tc_kernel<NALLOC, true><<<grid, 128, AssignCfg<NALLOC>::kSmem, st>>>(
+        *tm_h, *tm_w, static_cast<const __nv_bfloat16*>(L.C), L.gid, L.scores, L.B, L.n, L.D,
+        L.d_g, L.K, L.A, L.topk, L.err);
+  else
+    assign_tc_kernel<NALLOC, false><<<grid, 128, AssignCfg<NALLOC>::kSmem, st>>>(
+        *tm_h, *tm_w, static_cast<const __nv_bfloat16*>(L.C), L.gid, L.scores, L.B, L.n, L.D,
+        L.d_g, L.K, L.A, L.topk, L.err);
   return cudaGetLastError();
 }
 
@@ -266,10 +291,22 @@ cudaError_t launch_assign_f32(const AssignLaunch& L, cudaStream_t st) {
   const float* W = static_cast<const float*>(L.W);
   const float* C = static_cast<const float*>(L.C);
   switch (L.d_g) {
-    case 16: assign_f32_kernel<16><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.B, L.n, L.D, L.K, L.A, L.topk); break;
-    case 32: assign_f32_kernel<32><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.B, L.n, L.D, L.K, L.A, L.topk); break;
-    case 64: assign_f32_kernel<64><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.B, L.n, L.D, L.K, L.A, L.topk); break;
-    case 128: assign_f32_kernel<128><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.B, L.n, L.D, L.K, L.A, L.topk); break;
+    case 16:
+      if (L.scores) assign_f32_kernel<16, true><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk);
+      else assign_f32_kernel<16, false><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk);
+      break;
+    case 32:
+      if (L.scores) assign_f32_kernel<32, true><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk);
+      else assign_f32_kernel<32, false><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk);
+      break;
+    case 64:
+      if (L.scores) assign_f32_kernel<64, true><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk);
+      else assign_f32_kernel<64, false><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk);
+      break;
+    case 128:
+      if (L.scores) assign_f32_kernel<128, true><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk);
+      else assign_f32_kernel<128, false><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk);
+      break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -288,9 +325,12 @@ cudaError_t launch_assign_bf16(const AssignLaunch& L, const CUtensorMap* tm_h,
 
 cudaError_t setup_assign_kernels() {
   cudaError_t e;
-#define FOCUS_SET_SMEM(N)                                                                   \
-  e = cudaFuncSetAttribute(assign_tc_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                           AssignCfg<N>::kSmem);                                            \
+#define FOCUS_SET_SMEM(N)                                                                          \
+  e = cudaFuncSetAttribute(assign_tc_kernel<N, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                           AssignCfg<N>::kSmem);                                                   \
+  if (e != cudaSuccess) return e;                                                                  \
+  e = cudaFuncSetAttribute(assign_tc_kernel<N, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,  \
+                           AssignCfg<N>::kSmem);                                                   \
   if (e != cudaSuccess) return e;
   FOCUS_SET_SMEM(32)
   FOCUS_SET_SMEM(64)

@@ -52,6 +52,7 @@ struct AssignLaunch {
   int B, n, D, d_g, K, A;
   int topk;        // 1 or 2 ids per token, best first
   int* err;
+  float* scores;   // non-null: write every score [B, A, n, K] (fp32) instead of ids
 };
 
 // Everything the attention kernels read besides the K/V tensor maps.
@@ -142,5 +143,18 @@ struct CombineLaunch {
   int B, H, H_kv, A, n, d;
 };
 cudaError_t launch_lse_combine(const CombineLaunch& L, int dtype, cudaStream_t st);
+
+// sinkhorn.cu: Sinkhorn soft assignment over S [P, n, K] (fp32).
+struct SinkhornLaunch {
+  const float* S;    // [P, n, K] scores
+  float* G;          // [P, n, K] output (may alias S)
+  float* u;          // [P, n] row potentials
+  float* v;          // [P, K] column potentials
+  float2* part;      // [P, chunks, K] per-chunk column (max, sum)
+  int P, n, K;
+  float inv_tau;
+};
+int sinkhorn_rows_per_chunk(int n);
+cudaError_t launch_sinkhorn(const SinkhornLaunch& L, int iters, cudaStream_t st);
 
 }  // namespace focus

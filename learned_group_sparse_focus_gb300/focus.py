@@ -68,6 +68,10 @@ def _load():
         "focus_attention_fwd_timed": ([P, vp, vp, vp, ctypes.POINTER(Index), vp, vp, vp, ctypes.c_size_t,
                                        vp, ctypes.POINTER(ctypes.c_void_p)], ctypes.c_int),
         "focus_dense_causal_fwd": ([P, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp], ctypes.c_int),
+        "focus_sinkhorn_workspace_bytes": ([P], ctypes.c_size_t),
+        "focus_assign_scores": ([P, vp, vp, vp, vp, vp, ctypes.c_size_t, vp], ctypes.c_int),
+        "focus_sinkhorn_fwd": ([P, ctypes.c_int32, ctypes.c_float, vp, vp, vp, ctypes.c_size_t, vp],
+                               ctypes.c_int),
         "focus_attention_two_call_fwd": ([P, vp, vp, vp, ctypes.POINTER(Index), vp, vp, vp, ctypes.c_size_t,
                                           vp], ctypes.c_int),
         "focus_layer_fwd_host": ([P] + [vp] * 7 + [vp] * 8 + [vp, ctypes.c_size_t, vp], ctypes.c_int),
@@ -97,7 +101,8 @@ EXPORTED = ("focus_abi_version", "focus_status_string", "focus_workspace_bytes",
             "focus_attention_fwd_timed", "focus_dense_causal_fwd", "focus_layer_fwd_host", "focus_check_errors",
             "focus_build_index_static", "focus_workspace_bytes_topk", "focus_assign_topk",
             "focus_build_index_topk", "focus_attention_topk_fwd", "focus_attention_topk_fwd_timed",
-            "focus_attention_two_call_fwd")
+            "focus_attention_two_call_fwd", "focus_sinkhorn_workspace_bytes", "focus_assign_scores",
+            "focus_sinkhorn_fwd")
 
 
 def lib():
@@ -291,6 +296,29 @@ def run_layer_topk(p: Params, k: int, h, W, C, Q, K, V, ws, stream=None, want_ls
     lse = torch.empty((p.B, p.H, p.n), dtype=torch.float32, device=dev) if want_lse else None
     focus_attention_topk_fwd(p, Q, K, V, idx, O, lse, ws, stream)
     return O, gid, idx, lse
+
+
+# ------------------------------------------------ Sinkhorn soft assignment ---
+
+def alloc_workspace_sinkhorn(p: Params, device="cuda", stream=None) -> torch.Tensor:
+    nbytes = int(_lib.focus_sinkhorn_workspace_bytes(ctypes.byref(p)))
+    if nbytes == 0:
+        raise FocusError("focus_sinkhorn_workspace_bytes", 1)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    focus_workspace_init(ws, stream)
+    return ws
+
+
+def focus_assign_scores(p: Params, h, W, C, S, ws, stream=None):
+    """S: [B, A, n, K] fp32 device tensor."""
+    _check("focus_assign_scores", _lib.focus_assign_scores(ctypes.byref(p), _ptr(h), _ptr(W), _ptr(C), _ptr(S),
+                                                           _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def focus_sinkhorn_fwd(p: Params, iters: int, tau: float, S, G, ws, stream=None):
+    """G (may be S): [B, A, n, K] fp32 soft assignment after `iters` rounds."""
+    _check("focus_sinkhorn_fwd", _lib.focus_sinkhorn_fwd(ctypes.byref(p), int(iters), float(tau), _ptr(S),
+                                                         _ptr(G), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 # ------------------------------------------------------------ index views ---

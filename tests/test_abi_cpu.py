@@ -141,3 +141,22 @@ def test_topk_argument_checks(fz):
     idx.k = 2
     assert lib.focus_attention_topk_fwd(ctypes.byref(p), ok, ok, ok, ctypes.byref(idx), ok, None, ok, need,
                                         None) == 1
+
+
+def test_sinkhorn_argument_checks(fz):
+    lib = fz.lib()
+    p = fz.make_params(B=1, H=2, H_kv=2, n=1000, d=64, D=64, d_g=32, K=16, A=2, w=8)
+    need = lib.focus_sinkhorn_workspace_bytes(ctypes.byref(p))
+    # error word + u [2, 1000] + v [2, 16] + chunk partials [2, 8, 16] float2, each 256-aligned
+    assert need == 256 + 8192 + 256 + 2048
+    ok = ctypes.c_void_p(1 << 20)
+    mis = ctypes.c_void_p((1 << 20) + 8)
+    f = lib.focus_sinkhorn_fwd
+    assert f(ctypes.byref(p), 0, 1.0, ok, ok, ok, need, None) == 1           # no rounds
+    assert f(ctypes.byref(p), 10001, 1.0, ok, ok, ok, need, None) == 1
+    assert f(ctypes.byref(p), 3, 0.0, ok, ok, ok, need, None) == 1           # tau
+    assert f(ctypes.byref(p), 3, float("inf"), ok, ok, ok, need, None) == 1
+    assert f(ctypes.byref(p), 3, 1.0, mis, ok, ok, need, None) == 1
+    assert f(ctypes.byref(p), 3, 1.0, ok, ok, ok, need - 256, None) == 3
+    assert lib.focus_assign_scores(ctypes.byref(p), ok, ok, ok, None, ok, need, None) == 1
+    assert lib.focus_assign_scores(ctypes.byref(p), ok, ok, ok, ok, ok, need - 256, None) == 3
