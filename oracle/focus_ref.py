@@ -39,6 +39,12 @@ What the oracle computes (fp64 throughout, no blocking or fusion):
                row summing to 1 and every group's column to n / K (equal
                group sizes), by T rounds of Sinkhorn-Knopp scaling (columns,
                then rows).  scores() gives S = (h W_a^T) C_a^T.
+  backward     gradients of the attention output over the kept pairs
+               (training or fine-tuning a retrofit, [FocusKO] 2.1 and
+               [FocusJA] 3.1): with P the kept-pair softmax and a fixed
+               upstream dO, dV = P^T dO, dS = P * (dO V^T - rowsum(dO * O)),
+               dQ = scale dS K, dK = scale dS^T Q, dK and dV summed over the
+               query heads that share a key/value head.
 
 Readings where the pages are silent (each listed in the design notes):
   similarity = dot product; no projection bias; window strictly i - j < w;
@@ -65,7 +71,7 @@ __all__ = [
     "dense_causal", "lse_merge", "attention_bruteforce", "attention_weights_rows",
     "kv_head", "assignment_of_head",
     "assign_topk", "build_index_topk", "keep_mask_rows_topk", "attention_rows_topk",
-    "attention_bruteforce_topk", "scores", "sinkhorn",
+    "attention_bruteforce_topk", "scores", "sinkhorn", "attention_backward",
 ]
 
 
@@ -517,3 +523,38 @@ def sinkhorn(S, T: int, tau: float = 1.0):
         M = M * ((n / K) / M.sum(axis=-2, keepdims=True))
         M = M / M.sum(axis=-1, keepdims=True)
     return M
+
+
+# --------------------------------------------------------------- backward ---
+
+def attention_backward(Q, K, V, gid, w: int, scale: float, A: int, dO):
+    """Gradients of O = attention(Q, K, V) (the top-1 keep rule) for a fixed
+    upstream gradient dO.  Q, dO [B, H, n, d]; K, V [B, H_kv, n, d];
+    gid [B, A, n].  Returns dQ [B, H, n, d], dK, dV [B, H_kv, n, d] (fp64).
+
+    Per (b, h), with M the keep mask and P = softmax over kept keys of
+    S = scale Q K^T (exact, zero off the mask):
+      O = P V,  dV += P^T dO,  dP = dO V^T,  D_i = sum_j P_ij dP_ij,
+      dS = P * (dP - D),  dQ = scale dS K,  dK += scale dS^T Q.
+    (D_i equals dO_i . O_i because the rows of P sum to 1.)
+    """
+    B, H, n, d = Q.shape
+    H_kv = K.shape[1]
+    dQ = np.zeros((B, H, n, d))
+    dK = np.zeros((B, H_kv, n, d))
+    dV = np.zeros((B, H_kv, n, d))
+    rows = np.arange(n)
+    for b in range(B):
+        for hq in range(H):
+            kv = kv_head(hq, H, H_kv)
+            a = assignment_of_head(hq, H, H_kv, A)
+            q, k, v, do = _f64(Q[b, hq]), _f64(K[b, kv]), _f64(V[b, kv]), _f64(dO[b, hq])
+            M = keep_mask_rows(gid[b, a], w, rows)
+            P = attention_weights_rows(q, k, M, rows, scale)
+            dP = do @ v.T
+            Dv = np.sum(P * dP, axis=1, keepdims=True)
+            dS = P * (dP - Dv)
+            dQ[b, hq] = scale * (dS @ k)
+            dK[b, kv] += scale * (dS.T @ q)
+            dV[b, kv] += P.T @ do
+    return dQ, dK, dV

@@ -629,6 +629,99 @@ def test_sinkhorn_pins_catch_planted_mistakes():
     assert not np.allclose(softmax_only(S3, 300).sum(axis=0), 1.5, atol=1e-3)
 
 
+# --------------------------------------------------------------- backward ---
+
+def _loss(Q, K, V, g, w, scale, A, dO):
+    O, _ = ref.attention(Q, K, V, g, w, scale, A)
+    return float(np.sum(O * dO))
+
+
+def test_backward_matches_central_differences():
+    # L = sum(O * dO) has gradient (dQ, dK, dV) for the fixed dO
+    rng = np.random.default_rng(41)
+    B, H, Hkv, n, d, w = 1, 2, 1, 12, 3, 3
+    Q = rng.standard_normal((B, H, n, d))
+    K = rng.standard_normal((B, Hkv, n, d))
+    V = rng.standard_normal((B, Hkv, n, d))
+    dO = rng.standard_normal((B, H, n, d))
+    g = synth.draw_group_ids(6, B, 1, n, 3, "uniform")
+    dQ, dK, dV = ref.attention_backward(Q, K, V, g, w, 0.6, 1, dO)
+    eps = 1e-6
+    for X, dX in ((Q, dQ), (K, dK), (V, dV)):
+        for idx in [(0, 0, 0, 0), (0, 0, 5, 2), (0, X.shape[1] - 1, n - 1, 1), (0, 0, 7, 0)]:
+            Xp, Xm = X.copy(), X.copy()
+            Xp[idx] += eps
+            Xm[idx] -= eps
+            args = lambda Z: (Z if X is Q else Q, Z if X is K else K, Z if X is V else V)
+            num = (_loss(*args(Xp), g, w, 0.6, 1, dO) - _loss(*args(Xm), g, w, 0.6, 1, dO)) / (2 * eps)
+            assert abs(num - dX[idx]) < 1e-7, (idx, num, dX[idx])
+
+
+def test_backward_dense_case_matches_torch_autograd():
+    # K = 1 keeps every causal pair: the gradients of causal SDPA (torch, fp64)
+    rng = np.random.default_rng(42)
+    B, H, Hkv, n, d = 2, 4, 2, 37, 8
+    Q = rng.standard_normal((B, H, n, d))
+    K = rng.standard_normal((B, Hkv, n, d))
+    V = rng.standard_normal((B, Hkv, n, d))
+    dO = rng.standard_normal((B, H, n, d))
+    g = np.zeros((B, 1, n), np.int32)
+    dQ, dK, dV = ref.attention_backward(Q, K, V, g, 5, 0.3, 1, dO)
+    Qt = torch.from_numpy(Q).requires_grad_()
+    Kt = torch.from_numpy(K).requires_grad_()
+    Vt = torch.from_numpy(V).requires_grad_()
+    rep = H // Hkv
+    O = torch.nn.functional.scaled_dot_product_attention(
+        Qt, Kt.repeat_interleave(rep, dim=1), Vt.repeat_interleave(rep, dim=1), is_causal=True, scale=0.3)
+    O.backward(torch.from_numpy(dO))
+    np.testing.assert_allclose(dQ, Qt.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dK, Kt.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dV, Vt.grad.numpy(), atol=1e-12)
+
+
+def test_backward_invariants():
+    # rows of P sum to 1: sum_j dV_j = sum_i dO_i; rows of dS sum to 0: a
+    # common shift of all keys leaves the loss unchanged, so sum_j dK_j = 0
+    rng = np.random.default_rng(43)
+    B, H, Hkv, n, d = 1, 3, 1, 90, 5
+    Q, dO = (rng.standard_normal((B, H, n, d)) for _ in range(2))
+    K, V = (rng.standard_normal((B, Hkv, n, d)) for _ in range(2))
+    g = synth.draw_group_ids(44, B, 1, n, 4, "zipf")
+    dQ, dK, dV = ref.attention_backward(Q, K, V, g, 7, 0.4, 1, dO)
+    np.testing.assert_allclose(dV.sum(axis=2)[0, 0], dO.sum(axis=(1, 2))[0], atol=1e-11)
+    np.testing.assert_allclose(dK.sum(axis=2), 0.0, atol=1e-11)
+    # a key no query keeps gets no gradient: with one group per token and
+    # w = 1 only j = i is kept, so every key feeds one query
+    gd = synth.draw_group_ids(45, 1, 1, 20, 20, "distinct")
+    q1, k1, v1, o1 = (rng.standard_normal((1, 1, 20, 4)) for _ in range(4))
+    _, dK1, dV1 = ref.attention_backward(q1, k1, v1, gd, 1, 0.5, 1, o1)
+    np.testing.assert_allclose(dV1, o1, atol=1e-14)       # P = I
+    np.testing.assert_allclose(dK1, 0.0, atol=1e-14)      # softmax of one key is flat
+
+
+def test_backward_planted_mistake_is_caught():
+    # the finite-difference pin rejects a backward that drops the D term
+    # (dS = P * dP): the planted version's dQ misses the numerical gradient
+    rng = np.random.default_rng(46)
+    n, d, w, sc = 10, 3, 2, 0.5
+    Q, K, V, dO = (rng.standard_normal((1, 1, n, d)) for _ in range(4))
+    g = synth.draw_group_ids(7, 1, 1, n, 2, "uniform")
+    rows = np.arange(n)
+    M = ref.keep_mask_rows(g[0, 0], w, rows)
+    P = ref.attention_weights_rows(Q[0, 0], K[0, 0], M, rows, sc)
+    bad_dQ = sc * ((P * (dO[0, 0] @ V[0, 0].T)) @ K[0, 0])
+    eps = 1e-6
+    worst = 0.0
+    for i in range(n):
+        for c in range(d):
+            Qp, Qm = Q.copy(), Q.copy()
+            Qp[0, 0, i, c] += eps
+            Qm[0, 0, i, c] -= eps
+            num = (_loss(Qp, K, V, g, w, sc, 1, dO) - _loss(Qm, K, V, g, w, sc, 1, dO)) / (2 * eps)
+            worst = max(worst, abs(num - bad_dQ[i, c]))
+    assert worst > 1e-3
+
+
 # ------------------------------------------------ planted oracle mistakes ---
 
 def test_pins_catch_planted_mistakes(monkeypatch):
