@@ -30,6 +30,12 @@ with the pages' K = 4 (--K).  Kept pairs are counted once.
 workload's assignment shape; value = algorithmic GB/s of the Sinkhorn rounds
 (each round streams S twice, the last also writes G).
 
+--backward times focus_attention_bwd (dQ, dK, dV over the kept pairs, after
+one untimed forward for O and LSE); value = 10*d FLOPs per kept pair per head
+(five d-long products: the recomputed score, dO.v, and the dQ, dK, dV
+updates) over the device time, against the fp32 CUDA-core peak derived from
+the SM count and clock (152 SMs x 128 FMA lanes x 2 x 2.07 GHz).
+
 --impl reference times the oracle alone (the comparison arm of this build).
 Under torchrun (N > 1) every rank runs its own replica of the workload (weak
 scaling); there is no data-path collective.
@@ -696,6 +702,71 @@ def run_ours_sinkhorn(args, wl, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12     # CUDA-core fp32 FMA peak
+
+
+def run_ours_backward(args, wl, world, rank, local):
+    import torch
+    from learned_group_sparse_focus_gb300 import synth
+    from learned_group_sparse_focus_gb300 import focus as fz
+
+    torch.cuda.set_device(local)
+    x = synth.draw(wl, parts=("attn",))
+    rng = np.random.default_rng(wl.seed + 17)
+    dO_np = synth.round_bf16(rng.standard_normal(x["Q"].shape).astype(np.float32)) if wl.dtype == "bf16" \
+        else rng.standard_normal(x["Q"].shape).astype(np.float32)
+
+    def dev(a):
+        if wl.dtype == "bf16":
+            return torch.from_numpy(synth.bf16_bits(a)).view(torch.bfloat16).cuda()
+        return torch.from_numpy(a).cuda()
+
+    Q, K, V, dO = dev(x["Q"]), dev(x["K"]), dev(x["V"]), dev(dO_np)
+    g = torch.from_numpy(synth.draw_group_ids(wl.seed, wl.B, wl.A, wl.n, wl.K, wl.groups)).cuda()
+    p = fz.params_from_workload(wl)
+    ws = fz.alloc_workspace(p)
+    wsb = fz.alloc_workspace_backward(p)
+    idx = fz.focus_build_index(p, g, ws)
+    O = torch.empty_like(Q)
+    lse = torch.empty((wl.B, wl.H, wl.n), dtype=torch.float32, device="cuda")
+    fz.focus_attention_fwd(p, Q, K, V, idx, O, lse, ws)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    far = fz.index_views(p, idx, ws)["farlen_tok"].to(torch.int64).cpu().numpy()
+    win = int(np.minimum(np.arange(wl.n) + 1, max(wl.w, 1)).sum()) * wl.B * wl.H
+    far_pairs = sum(int(far[:, 0 if wl.A == 1 else (h * wl.H_kv) // wl.H, :].sum()) for h in range(wl.H))
+    kept = win + far_pairs
+    flops = 10 * wl.d * kept
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup):
+        fz.focus_attention_bwd(p, Q, K, V, O, dO, lse, idx, dQ, dK, dV, wsb)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    with ClockSampler(int(os.environ.get("FOCUS_NVSMI_INDEX", local))) as clk:
+        for a0, a1 in ev:
+            flush.zero_()
+            a0.record()
+            fz.focus_attention_bwd(p, Q, K, V, O, dO, lse, idx, dQ, dK, dV, wsb)
+            a1.record()
+        torch.cuda.synchronize()
+    if fz.focus_check_errors(ws) != 0 or fz.focus_check_errors(wsb) != 0:
+        raise RuntimeError("device error")
+    t = statistics.mean(a0.elapsed_time(a1) for a0, a1 in ev)
+    tf = flops / (t * 1e-3) / 1e12
+    line = {
+        "metric": "backward kept-pair TFLOP/s (10*d FLOP per kept pair per head)", "value": tf,
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": wl.name, **{k: getattr(wl, k) for k in ("B", "H", "H_kv", "n", "d", "K", "w", "A")},
+                   "kept_pairs": kept, "l2": "flushed (256 MB write) before every timed step"},
+        "roofline": {"bound": "alu", "kernel": "backward (fp32 CUDA cores)", "achieved": tf,
+                     "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s", "frac": tf / FP32_ALU_TFLOPS, "traffic": None,
+                     "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz"},
+        "gpu_launches": 5 * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -710,6 +781,7 @@ def main():
                     help="groups per token; 2 runs the top-2 membership layer")
     ap.add_argument("--K", type=int, default=None, help="centroids (default: 4 with --topk 2)")
     ap.add_argument("--sinkhorn", type=int, default=0, help="time T Sinkhorn rounds instead")
+    ap.add_argument("--backward", action="store_true", help="time the backward pass instead")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -719,6 +791,8 @@ def main():
     world, rank, local = dist_env()
     if args.impl == "reference":
         run_reference(args, wl, world, rank)
+    elif args.backward:
+        run_ours_backward(args, wl, world, rank, local)
     elif args.sinkhorn > 0:
         run_ours_sinkhorn(args, wl, world, rank, local)
     elif args.topk > 1:

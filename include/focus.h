@@ -358,6 +358,29 @@ FOCUS_API focus_status_t focus_sinkhorn_fwd(const focus_params_t* p, int32_t ite
                                             const float* S, float* G, void* ws, size_t ws_bytes,
                                             void* stream);
 
+/* ------------------------------------------------------------- backward ---
+ * Gradients of focus_attention_fwd over the kept pairs, for training or
+ * fine-tuning a retrofitted model ("Why Attend to Everything? Focus is the
+ * Key" 2.1: exact softmax over the kept pairs; "Focus: Learning Which
+ * Attention Pairs Matter" 3.1).  With P_ij = exp(scale q_i.k_j - lse_i) on
+ * kept pairs and Delta_i = dO_i . O_i:
+ *   dV_j = sum_i P_ij dO_i,  dS_ij = P_ij (dO_i . v_j - Delta_i),
+ *   dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_i dS_ij q_i,
+ * dK, dV summed over the query heads of each key/value head.
+ *   Q, O, dO, dQ [B, H, n, d]; K, V, dK, dV [B, H_kv, n, d]: dtype of p,
+ *   16-byte aligned; lse [B, H, n] fp32 from the forward call (lse_opt);
+ *   idx from focus_build_index with the same p (in the forward workspace).
+ * ws: a backward workspace of focus_backward_workspace_bytes(p) (error word
+ * first; fp32 partials).  fp32 arithmetic on the CUDA cores for both dtypes;
+ * d in {64, 128}.  Errors as focus_attention_fwd. */
+FOCUS_API size_t focus_backward_workspace_bytes(const focus_params_t* p);
+
+FOCUS_API focus_status_t focus_attention_bwd(const focus_params_t* p, const void* Q, const void* K,
+                                             const void* V, const void* O, const void* dO,
+                                             const float* lse, const focus_index_t* idx, void* dQ,
+                                             void* dK, void* dV, void* ws, size_t ws_bytes,
+                                             void* stream);
+
 /* Synchronises `stream`, reads and clears the device error word in ws.
  * Returns FOCUS_OK, FOCUS_ERR_BAD_GROUP_ID, FOCUS_ERR_TIMEOUT or FOCUS_ERR_CUDA. */
 FOCUS_API focus_status_t focus_check_errors(void* ws, void* stream);

@@ -890,6 +890,82 @@ focus_status_t focus_sinkhorn_fwd(const focus_params_t* p, int32_t iters, float 
   return cuda_status(launch_sinkhorn(L, iters, static_cast<cudaStream_t>(stream)));
 }
 
+// ------------------------------------------------------------- backward ---
+
+static size_t backward_layout(const focus_params_t* p, size_t* delta, size_t* dq, size_t* dk,
+                              size_t* dv) {
+  const size_t qrows = static_cast<size_t>(p->B) * p->H * p->n;
+  const size_t krows = static_cast<size_t>(p->B) * p->H_kv * p->n;
+  size_t o = align_up(kAlign);                       // error word
+  *delta = o;
+  o = align_up(o + qrows * 4);
+  *dq = o;
+  o = align_up(o + qrows * p->d * 4);
+  *dk = o;
+  o = align_up(o + krows * p->d * 4);
+  *dv = o;
+  o = align_up(o + krows * p->d * 4);
+  return o;
+}
+
+size_t focus_backward_workspace_bytes(const focus_params_t* p) {
+  if (!params_ok(p)) return 0;
+  size_t a, b, c, d;
+  return backward_layout(p, &a, &b, &c, &d);
+}
+
+focus_status_t focus_attention_bwd(const focus_params_t* p, const void* Q, const void* K,
+                                   const void* V, const void* O, const void* dO, const float* lse,
+                                   const focus_index_t* idx, void* dQ, void* dK, void* dV, void* ws,
+                                   size_t ws_bytes, void* stream) {
+  if (!params_ok(p)) return FOCUS_ERR_INVALID_ARG;
+  if (!idx || !idx->perm || !idx->farlen_tok || !idx->farlen_slot || !idx->offsets || !idx->items ||
+      !idx->order || !idx->n_items)
+    return FOCUS_ERR_INVALID_ARG;
+  if (idx->max_items != layout_of(p).max_items || idx->w_eff != (p->w > 1 ? p->w : 1))
+    return FOCUS_ERR_INVALID_ARG;
+  const void* ptrs[] = {Q, K, V, O, dO, lse, dQ, dK, dV};
+  for (const void* q : ptrs)
+    if (!q || !aligned16(q)) return FOCUS_ERR_INVALID_ARG;
+  if (!(p->d == 64 || p->d == 128)) return FOCUS_ERR_UNSUPPORTED;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return FOCUS_ERR_INVALID_ARG;
+  size_t o_delta, o_dq, o_dk, o_dv;
+  if (ws_bytes < backward_layout(p, &o_delta, &o_dq, &o_dk, &o_dv)) return FOCUS_ERR_WORKSPACE;
+  if (focus_status_t s = ensure_setup()) return s;
+  BwdArgs a{};
+  a.Q = Q;
+  a.K = K;
+  a.V = V;
+  a.O = O;
+  a.dO = dO;
+  a.lse = lse;
+  a.delta = at<float>(ws, o_delta);
+  a.dq_far = at<float>(ws, o_dq);
+  a.dk_far = at<float>(ws, o_dk);
+  a.dv_far = at<float>(ws, o_dv);
+  a.dQ = dQ;
+  a.dK = dK;
+  a.dV = dV;
+  a.perm = idx->perm;
+  a.farlen_tok = idx->farlen_tok;
+  a.farlen_slot = idx->farlen_slot;
+  a.offsets = idx->offsets;
+  a.items = idx->items;
+  a.order = idx->order;
+  a.n_items = idx->n_items;
+  a.B = p->B;
+  a.H = p->H;
+  a.H_kv = p->H_kv;
+  a.n = p->n;
+  a.d = p->d;
+  a.A = p->A;
+  a.groups = p->K;
+  a.w = idx->w_eff;
+  a.scale = p->scale;
+  a.scale_log2 = p->scale * 1.4426950408889634f;
+  return cuda_status(launch_attn_bwd(a, p->dtype, idx->max_items, static_cast<cudaStream_t>(stream)));
+}
+
 focus_status_t focus_check_errors(void* ws, void* stream) {
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return FOCUS_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -155,6 +155,23 @@ struct SinkhornLaunch {
   float inv_tau;
 };
 int sinkhorn_rows_per_chunk(int n);
+
+// attn_bwd.cu: backward over the kept pairs (fp32 arithmetic on the CUDA cores).
+struct BwdArgs {
+  const void *Q, *K, *V, *O, *dO;   // forward tensors and the upstream gradient
+  const float* lse;                 // [B, H, n] forward LSE (natural log)
+  float* delta;                     // [B, H, n] dO . O
+  float* dq_far;                    // [B*H*n, d]    far-key part of dQ
+  float *dk_far, *dv_far;           // [B*H_kv*n, d] far-query parts of dK, dV
+  void *dQ, *dK, *dV;               // outputs (dtype of Q)
+  const int32_t *perm, *farlen_tok, *farlen_slot, *offsets;
+  const focus_item_t* items;
+  const int32_t* order;
+  const int32_t* n_items;
+  int B, H, H_kv, n, d, A, groups, w;   // groups: K, the number of centroids
+  float scale, scale_log2;
+};
+cudaError_t launch_attn_bwd(const BwdArgs& a, int dtype, int max_items, cudaStream_t st);
 cudaError_t launch_sinkhorn(const SinkhornLaunch& L, int iters, cudaStream_t st);
 
 }  // namespace focus

@@ -72,6 +72,9 @@ def _load():
         "focus_assign_scores": ([P, vp, vp, vp, vp, vp, ctypes.c_size_t, vp], ctypes.c_int),
         "focus_sinkhorn_fwd": ([P, ctypes.c_int32, ctypes.c_float, vp, vp, vp, ctypes.c_size_t, vp],
                                ctypes.c_int),
+        "focus_backward_workspace_bytes": ([P], ctypes.c_size_t),
+        "focus_attention_bwd": ([P, vp, vp, vp, vp, vp, vp, ctypes.POINTER(Index), vp, vp, vp, vp,
+                                 ctypes.c_size_t, vp], ctypes.c_int),
         "focus_attention_two_call_fwd": ([P, vp, vp, vp, ctypes.POINTER(Index), vp, vp, vp, ctypes.c_size_t,
                                           vp], ctypes.c_int),
         "focus_layer_fwd_host": ([P] + [vp] * 7 + [vp] * 8 + [vp, ctypes.c_size_t, vp], ctypes.c_int),
@@ -102,7 +105,7 @@ EXPORTED = ("focus_abi_version", "focus_status_string", "focus_workspace_bytes",
             "focus_build_index_static", "focus_workspace_bytes_topk", "focus_assign_topk",
             "focus_build_index_topk", "focus_attention_topk_fwd", "focus_attention_topk_fwd_timed",
             "focus_attention_two_call_fwd", "focus_sinkhorn_workspace_bytes", "focus_assign_scores",
-            "focus_sinkhorn_fwd")
+            "focus_sinkhorn_fwd", "focus_backward_workspace_bytes", "focus_attention_bwd")
 
 
 def lib():
@@ -296,6 +299,26 @@ def run_layer_topk(p: Params, k: int, h, W, C, Q, K, V, ws, stream=None, want_ls
     lse = torch.empty((p.B, p.H, p.n), dtype=torch.float32, device=dev) if want_lse else None
     focus_attention_topk_fwd(p, Q, K, V, idx, O, lse, ws, stream)
     return O, gid, idx, lse
+
+
+# ---------------------------------------------------------------- backward ---
+
+def alloc_workspace_backward(p: Params, device="cuda", stream=None) -> torch.Tensor:
+    nbytes = int(_lib.focus_backward_workspace_bytes(ctypes.byref(p)))
+    if nbytes == 0:
+        raise FocusError("focus_backward_workspace_bytes", 1)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    focus_workspace_init(ws, stream)
+    return ws
+
+
+def focus_attention_bwd(p: Params, Q, K, V, O, dO, lse, idx: Index, dQ, dK, dV, ws, stream=None):
+    """Gradients over the kept pairs; lse from the forward call, idx from
+    focus_build_index (forward workspace), ws a backward workspace."""
+    _check("focus_attention_bwd",
+           _lib.focus_attention_bwd(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(lse),
+                                    ctypes.byref(idx), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(ws), ws.numel(),
+                                    _stream(stream)))
 
 
 # ------------------------------------------------ Sinkhorn soft assignment ---

@@ -72,6 +72,7 @@ __all__ = [
     "kv_head", "assignment_of_head",
     "assign_topk", "build_index_topk", "keep_mask_rows_topk", "attention_rows_topk",
     "attention_bruteforce_topk", "scores", "sinkhorn", "attention_backward",
+    "attention_backward_dq_rows",
 ]
 
 
@@ -558,3 +559,25 @@ def attention_backward(Q, K, V, gid, w: int, scale: float, A: int, dO):
             dK[b, kv] += scale * (dS.T @ q)
             dV[b, kv] += P.T @ do
     return dQ, dK, dV
+
+
+def attention_backward_dq_rows(Q, K, V, gid, w: int, scale: float, A: int, dO, rows):
+    """dQ of attention_backward for selected query rows only (each row's dQ
+    needs only its own kept keys): dQ_i = scale sum_j P_ij (dO_i . v_j - D_i) k_j.
+    Returns [B, H, R, d]."""
+    B, H, n, d = Q.shape
+    H_kv = K.shape[1]
+    rows = np.asarray(rows, dtype=np.int64)
+    out = np.empty((B, H, len(rows), d))
+    for b in range(B):
+        for hq in range(H):
+            kv = kv_head(hq, H, H_kv)
+            a = assignment_of_head(hq, H, H_kv, A)
+            k, v = _f64(K[b, kv]), _f64(V[b, kv])
+            M = keep_mask_rows(gid[b, a], w, rows)
+            P = attention_weights_rows(_f64(Q[b, hq]), k, M, rows, scale)
+            do = _f64(dO[b, hq])[rows]
+            dP = do @ v.T
+            dS = P * (dP - np.sum(P * dP, axis=1, keepdims=True))
+            out[b, hq] = scale * (dS @ k)
+    return out

@@ -160,3 +160,24 @@ def test_sinkhorn_argument_checks(fz):
     assert f(ctypes.byref(p), 3, 1.0, ok, ok, ok, need - 256, None) == 3
     assert lib.focus_assign_scores(ctypes.byref(p), ok, ok, ok, None, ok, need, None) == 1
     assert lib.focus_assign_scores(ctypes.byref(p), ok, ok, ok, ok, ok, need - 256, None) == 3
+
+
+def test_backward_argument_checks(fz):
+    lib = fz.lib()
+    p = fz.make_params(B=1, H=4, H_kv=2, n=64, d=64, D=64, d_g=32, K=4, A=1, w=8)
+    need = lib.focus_backward_workspace_bytes(ctypes.byref(p))
+    # error word + Delta [4*64] + dQ part [4*64*64] + dK, dV parts [2*64*64] fp32
+    assert need == 256 + 1024 + 65536 + 2 * 32768
+    ok = ctypes.c_void_p(1 << 20)
+    mis = ctypes.c_void_p((1 << 20) + 8)
+    f = lib.focus_attention_bwd
+    assert f(ctypes.byref(p), ok, ok, ok, ok, ok, ok, None, ok, ok, ok, ok, need, None) == 1
+    idx = fz.Index()
+    for name in ("counts", "offsets", "perm", "rank", "farlen_tok", "farlen_slot", "items", "order", "n_items"):
+        setattr(idx, name, 1 << 21)
+    idx.max_items = 1 + 4          # ceil(64/128) + min(K, n) for one problem
+    idx.w_eff = 8
+    assert f(ctypes.byref(p), mis, ok, ok, ok, ok, ok, ctypes.byref(idx), ok, ok, ok, ok, need, None) == 1
+    assert f(ctypes.byref(p), ok, ok, ok, ok, ok, ok, ctypes.byref(idx), ok, ok, ok, ok, need - 256, None) == 3
+    idx.w_eff = 9                  # an index built for another window
+    assert f(ctypes.byref(p), ok, ok, ok, ok, ok, ok, ctypes.byref(idx), ok, ok, ok, ok, need, None) == 1

@@ -1,0 +1,109 @@
+"""GPU parity for the backward pass (focus_attention_bwd) against the fp64
+oracle's gradients on the same inputs and the same upstream gradient dO.
+
+The GPU runs the forward first (its O and LSE feed the backward, as in
+training).  Tolerances, relative to M = max(largest reference gradient entry, 0.1):
+fp32 max |error| <= 1e-4 M (exp2 of the recomputed scores is good to about
+2^-22 times |score - LSE| <= ~20, then sums of up to n products in fp32);
+bf16 max |error| <= 2e-2 M and mean <= 2e-3 M (the forward O that enters
+Delta = dO . O and the stored gradients are bf16, 2^-9 relative each).
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle.focus_ref as ref
+from learned_group_sparse_focus_gb300 import synth
+
+from _helpers import to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fz():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from learned_group_sparse_focus_gb300 import _build
+    if not os.path.exists(_build.LIB):
+        _build.build()
+    from learned_group_sparse_focus_gb300 import focus
+    return focus
+
+
+def _close(got, want, dtype, what):
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    assert np.all(np.isfinite(got)), what
+    # floor 0.1: where the exact gradient is zero (one kept key per row) the
+    # GPU returns rounding noise of the scale of its O(1) terms; the floor
+    # makes the fp32 bar 1e-5 absolute there, the forward's own
+    M = max(np.abs(want).max(), 0.1)
+    diff = np.abs(got - want)
+    if dtype == "bf16":
+        assert diff.max() <= 2e-2 * M, f"{what}: max {diff.max() / M:.3e} of max|ref|"
+        assert diff.mean() <= 2e-3 * M, f"{what}: mean {diff.mean() / M:.3e} of max|ref|"
+    else:
+        assert diff.max() <= 1e-4 * M, f"{what}: max {diff.max() / M:.3e} of max|ref|"
+
+
+def _run(fz, dtype, B, H, H_kv, A, n, d, K, w, kind, seed):
+    import torch
+    rng = np.random.default_rng(seed)
+    store = (lambda a: synth.round_bf16(a)) if dtype == "bf16" else (lambda a: a)
+    Q = store(rng.standard_normal((B, H, n, d)).astype(np.float32))
+    Kt = store(rng.standard_normal((B, H_kv, n, d)).astype(np.float32))
+    V = store(rng.standard_normal((B, H_kv, n, d)).astype(np.float32))
+    dO = store(rng.standard_normal((B, H, n, d)).astype(np.float32))
+    g = synth.draw_group_ids(seed, B, A, n, K, kind)
+    p = fz.make_params(B=B, H=H, H_kv=H_kv, n=n, d=d, D=64, d_g=32, K=K, A=A, w=w, dtype=dtype)
+    ws = fz.alloc_workspace(p)
+    wsb = fz.alloc_workspace_backward(p)
+    Qd, Kd, Vd, dOd = (to_dev(x, dtype) for x in (Q, Kt, V, dO))
+    idx = fz.focus_build_index(p, torch.from_numpy(g).cuda(), ws)
+    O = torch.empty_like(Qd)
+    lse = torch.empty((B, H, n), dtype=torch.float32, device="cuda")
+    fz.focus_attention_fwd(p, Qd, Kd, Vd, idx, O, lse, ws)
+    dQ = torch.full_like(Qd, float("nan"))
+    dK = torch.full_like(Kd, float("nan"))
+    dV = torch.full_like(Vd, float("nan"))
+    fz.focus_attention_bwd(p, Qd, Kd, Vd, O, dOd, lse, idx, dQ, dK, dV, wsb)
+    assert fz.focus_check_errors(ws) == 0 and fz.focus_check_errors(wsb) == 0
+    return (Q, Kt, V, dO, g, p), (to_host(dQ), to_host(dK), to_host(dV))
+
+
+@pytest.mark.parametrize("dtype,B,H,H_kv,A,n,d,K,w,kind", [
+    ("f32", 1, 2, 2, 1, 256, 64, 4, 32, "uniform"),
+    ("f32", 1, 4, 2, 2, 333, 128, 5, 20, "zipf"),
+    ("f32", 2, 2, 1, 1, 100, 64, 1, 7, "one"),              # K = 1: dense causal
+    ("f32", 1, 2, 2, 1, 130, 128, 130, 1, "distinct"),      # self pairs only
+    ("bf16", 1, 2, 2, 1, 300, 128, 4, 32, "uniform"),
+    ("bf16", 1, 4, 2, 1, 513, 64, 8, 100, "zipf"),
+    ("bf16", 1, 8, 2, 2, 700, 128, 6, 64, "uniform"),       # per-KV-head ids, 4 query heads per KV head
+    ("bf16", 1, 2, 2, 1, 1, 128, 3, 5, "uniform"),          # one token
+    ("bf16", 1, 2, 1, 1, 400, 64, 5, 1000, "uniform"),      # w > n
+    ("bf16", 2, 2, 2, 1, 257, 128, 3, 0, "blocks"),         # w = 0
+])
+def test_backward_all_rows(fz, dtype, B, H, H_kv, A, n, d, K, w, kind):
+    (Q, Kt, V, dO, g, p), (dQ, dK, dV) = _run(fz, dtype, B, H, H_kv, A, n, d, K, w, kind, seed=n + K + w + 3)
+    wQ, wK, wV = ref.attention_backward(Q, Kt, V, g, max(w, 1), p.scale, A, dO)
+    _close(dQ, wQ, dtype, "dQ")
+    _close(dK, wK, dtype, "dK")
+    _close(dV, wV, dtype, "dV")
+
+
+def test_backward_at_a_long_length_sampled_and_invariants(fz):
+    """n = 8192, 8 query / 2 KV heads, d = 128, Zipf groups: sampled dQ rows
+    against the oracle, and at every size sum_j dV_j = sum_i dO_i and
+    sum_j dK_j = 0 per KV head (rows of P sum to 1, rows of dS to 0)."""
+    (Q, Kt, V, dO, g, p), (dQ, dK, dV) = _run(fz, "bf16", 1, 8, 2, 1, 8192, 128, 16, 256, "zipf", seed=99)
+    rows = np.unique(np.concatenate([np.arange(260), [8191], np.random.default_rng(5).integers(0, 8192, 40)]))
+    want = ref.attention_backward_dq_rows(Q, Kt, V, g, 256, p.scale, 1, dO, rows)
+    _close(dQ[:, :, rows], want, "bf16", "dQ rows")
+    for kv in range(2):
+        heads = [h for h in range(8) if ref.kv_head(h, 8, 2) == kv]
+        sdo = dO[0, heads].astype(np.float64).sum(axis=(0, 1))
+        M = np.abs(sdo).max()
+        assert np.abs(dV[0, kv].sum(axis=0) - sdo).max() <= 2e-2 * M
+        assert np.abs(dK[0, kv].sum(axis=0)).max() <= 2e-2 * np.abs(dK[0, kv]).sum(axis=0).max()

@@ -699,6 +699,18 @@ def test_backward_invariants():
     np.testing.assert_allclose(dK1, 0.0, atol=1e-14)      # softmax of one key is flat
 
 
+def test_backward_dq_rows_equal_full_backward_rows():
+    rng = np.random.default_rng(47)
+    B, H, Hkv, n, d = 1, 4, 2, 70, 6
+    Q, dO = (rng.standard_normal((B, H, n, d)) for _ in range(2))
+    K, V = (rng.standard_normal((B, Hkv, n, d)) for _ in range(2))
+    g = synth.draw_group_ids(48, B, 2, n, 5, "uniform")
+    dQ, _, _ = ref.attention_backward(Q, K, V, g, 6, 0.35, 2, dO)
+    rows = np.array([0, 3, 17, 50, 69])
+    np.testing.assert_allclose(ref.attention_backward_dq_rows(Q, K, V, g, 6, 0.35, 2, dO, rows),
+                               dQ[:, :, rows], atol=1e-13)
+
+
 def test_backward_planted_mistake_is_caught():
     # the finite-difference pin rejects a backward that drops the D term
     # (dS = P * dP): the planted version's dQ misses the numerical gradient
