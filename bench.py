@@ -33,8 +33,10 @@ workload's assignment shape; value = algorithmic GB/s of the Sinkhorn rounds
 --backward times focus_attention_bwd (dQ, dK, dV over the kept pairs, after
 one untimed forward for O and LSE); value = 10*d FLOPs per kept pair per head
 (five d-long products: the recomputed score, dO.v, and the dQ, dK, dV
-updates) over the device time, against the fp32 CUDA-core peak derived from
-the SM count and clock (152 SMs x 128 FMA lanes x 2 x 2.07 GHz).
+updates) over the device time; bf16 runs on the tensor cores (roofline against
+the measured sustained bf16 peak; the dQ and dK/dV kernels each recompute the
+score and dO.v, 14*d FLOPs executed per pair), fp32 on the CUDA cores (against
+the fp32 peak derived from the SM count and clock: 152 x 128 x 2 x 2.07 GHz).
 
 --impl reference times the oracle alone (the comparison arm of this build).
 Under torchrun (N > 1) every rank runs its own replica of the workload (weak
@@ -699,6 +701,17 @@ def run_ours_sinkhorn(args, wl, world, rank, local):
         "gpu_launches": (1 + 3 * T) * args.steps,
         "clocks": clk.summary(),
     }
+    if not args.no_cpu_baseline:
+        import oracle.focus_ref as ref
+        rows = min(wl.n, 8192)
+        t0 = time.perf_counter()
+        Sref = ref.scores(x["h"][:, :rows], x["W"], x["C"])
+        ref.sinkhorn(Sref, T, 1.0)
+        sec = time.perf_counter() - t0
+        ab = (2 * T + 1) * Sref.size * 4 + 4 * Sref.shape[0] * Sref.shape[1] * rows * T
+        line["cpu_baseline"] = {"value": ab / sec / 1e9, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+                                "sample": f"oracle fp64 scores + {T} Sinkhorn rounds on the first {rows} tokens "
+                                          f"(the same bytes-per-round accounting)", "seconds": sec}
     print(json.dumps(line), flush=True)
 
 
@@ -758,12 +771,37 @@ def run_ours_backward(args, wl, world, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
         "config": {"workload": wl.name, **{k: getattr(wl, k) for k in ("B", "H", "H_kv", "n", "d", "K", "w", "A")},
                    "kept_pairs": kept, "l2": "flushed (256 MB write) before every timed step"},
-        "roofline": {"bound": "alu", "kernel": "backward (fp32 CUDA cores)", "achieved": tf,
-                     "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s", "frac": tf / FP32_ALU_TFLOPS, "traffic": None,
-                     "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz"},
+        "roofline": ({"bound": "tensor", "kernel": "backward (tcgen05 dQ and dK/dV kernels)", "achieved": tf,
+                      "peak": float(load_peaks()[0]["bf16_tflops_sustained"]), "unit": "TFLOP/s",
+                      "frac": tf / float(load_peaks()[0]["bf16_tflops_sustained"]), "traffic": None,
+                      "peak_source": f"{load_peaks()[1]} bf16_tflops_sustained"}
+                     if wl.dtype == "bf16" else
+                     {"bound": "alu", "kernel": "backward (fp32 CUDA cores)", "achieved": tf,
+                      "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s", "frac": tf / FP32_ALU_TFLOPS, "traffic": None,
+                      "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz"}),
         "gpu_launches": 5 * args.steps,
         "clocks": clk.summary(),
+        "ms_note": "bf16: delta + 4 tcgen05 kernels (dQ far, dQ window, dK/dV far, dK/dV window)",
     }
+    if not args.no_cpu_baseline:
+        import oracle.focus_ref as ref
+        nb = min(wl.n, 1024)
+        Hs = min(wl.H, 2 * (wl.H // wl.H_kv))
+        Hkv_s = max(1, Hs * wl.H_kv // wl.H)
+        gs = synth.draw_group_ids(wl.seed, wl.B, wl.A, wl.n, wl.K, wl.groups)[:, :, :nb]
+        t0 = time.perf_counter()
+        ref.attention_backward(x["Q"][:, :Hs, :nb], x["K"][:, :Hkv_s, :nb], x["V"][:, :Hkv_s, :nb], gs[:, :min(wl.A, Hkv_s)],
+                               max(wl.w, 1), wl.scale, min(wl.A, Hkv_s), dO_np[:, :Hs, :nb])
+        sec = time.perf_counter() - t0
+        kept_s = 0
+        for b in range(wl.B):
+            for h in range(Hs):
+                a = 0 if wl.A == 1 else ref.kv_head(h, Hs, Hkv_s)
+                kept_s += int(ref.keep_mask_rows(gs[b, a], max(wl.w, 1), np.arange(nb)).sum())
+        line["cpu_baseline"] = {"value": 10 * wl.d * kept_s / sec / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(),
+                                "kind": "oracle",
+                                "sample": f"oracle fp64 backward on the first {nb} tokens of {Hs} query heads",
+                                "seconds": sec}
     print(json.dumps(line), flush=True)
 
 

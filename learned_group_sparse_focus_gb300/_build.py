@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libfocus.so")
 SOURCES = ["api.cu", "assign.cu", "index.cu", "index_static.cu", "attn_simt.cu", "attn_tc.cu", "topk.cu",
-           "two_call.cu", "sinkhorn.cu", "attn_bwd.cu"]
+           "two_call.cu", "sinkhorn.cu", "attn_bwd.cu", "attn_bwd_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

@@ -112,6 +112,7 @@ focus_status_t ensure_setup() {
     if (setup_index_kernels() != cudaSuccess) return FOCUS_ERR_CUDA;
     if (setup_assign_kernels() != cudaSuccess) return FOCUS_ERR_CUDA;
     if (setup_attn_kernels() != cudaSuccess) return FOCUS_ERR_CUDA;
+    if (setup_bwd_tc_kernels() != cudaSuccess) return FOCUS_ERR_CUDA;
     g_ready[dev] = true;
   }
   return FOCUS_OK;
@@ -943,6 +944,7 @@ focus_status_t focus_attention_bwd(const focus_params_t* p, const void* Q, const
   a.dq_far = at<float>(ws, o_dq);
   a.dk_far = at<float>(ws, o_dk);
   a.dv_far = at<float>(ws, o_dv);
+  a.err = at<int>(ws, 0);
   a.dQ = dQ;
   a.dK = dK;
   a.dV = dV;
@@ -963,7 +965,21 @@ focus_status_t focus_attention_bwd(const focus_params_t* p, const void* Q, const
   a.w = idx->w_eff;
   a.scale = p->scale;
   a.scale_log2 = p->scale * 1.4426950408889634f;
-  return cuda_status(launch_attn_bwd(a, p->dtype, idx->max_items, static_cast<cudaStream_t>(stream)));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (p->dtype == FOCUS_F32) return cuda_status(launch_attn_bwd(a, p->dtype, idx->max_items, st));
+  // bf16: tensor cores
+  const uint64_t qplanes = static_cast<uint64_t>(p->B) * p->H;
+  const uint64_t planes = static_cast<uint64_t>(p->B) * p->H_kv;
+  if (static_cast<long long>(qplanes) * p->n >= (1LL << 31)) return FOCUS_ERR_UNSUPPORTED;
+  CUtensorMap q2, do2, k2, v2, q3, do3, k3, v3;
+  if (!make_map(&q2, Q, p->d, qplanes * p->n, 1, 1, 2) || !make_map(&do2, dO, p->d, qplanes * p->n, 1, 1, 2) ||
+      !make_map(&k2, K, p->d, planes * p->n, 1, 1, 2) || !make_map(&v2, V, p->d, planes * p->n, 1, 1, 2) ||
+      !make_map(&q3, Q, p->d, p->n, qplanes, 128, 3) || !make_map(&do3, dO, p->d, p->n, qplanes, 128, 3) ||
+      !make_map(&k3, K, p->d, p->n, planes, 128, 3) || !make_map(&v3, V, p->d, p->n, planes, 128, 3))
+    return FOCUS_ERR_CUDA;
+  cudaError_t e = launch_bwd_delta(a, p->dtype, st);
+  if (e == cudaSuccess) e = launch_attn_bwd_tc(a, &q2, &do2, &k2, &v2, &q3, &do3, &k3, &v3, idx->max_items, st);
+  return cuda_status(e);
 }
 
 focus_status_t focus_check_errors(void* ws, void* stream) {

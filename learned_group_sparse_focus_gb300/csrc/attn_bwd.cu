@@ -362,6 +362,16 @@ cudaError_t launch_bwd_d(const BwdArgs& a, int max_items, cudaStream_t st) {
 
 }  // namespace
 
+cudaError_t launch_bwd_delta(const BwdArgs& a, int dtype, cudaStream_t st) {
+  const long long rows = static_cast<long long>(a.B) * a.H * a.n;
+  const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
+  if (dtype == FOCUS_BF16)
+    bwd_delta_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(a, rows);
+  else
+    bwd_delta_kernel<float><<<grid, 256, 0, st>>>(a, rows);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_attn_bwd(const BwdArgs& a, int dtype, int max_items, cudaStream_t st) {
   if (dtype == FOCUS_BF16) {
     if (a.d == 64) return launch_bwd_d<64, __nv_bfloat16>(a, max_items, st);

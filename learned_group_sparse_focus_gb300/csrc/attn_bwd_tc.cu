@@ -1,0 +1,554 @@
+// Backward of Focus attention on the tcgen05 tensor cores (bf16 tensors, fp32
+// accumulate): the same gradients as attn_bwd.cu ("Why Attend to Everything?
+// Focus is the Key", section 2.1; "Focus: Learning Which Attention Pairs
+// Matter", section 3.1), with every d-long product an MMA.
+//
+// Two kernels, each in a group form (far pairs, rows and keys in the index's
+// sorted order, reached by TMA row gathers) and a window form (natural order,
+// TMA tiles); one CTA per 128-row unit:
+//   dQ   rows = 128 queries, streamed = 128-key tiles of the kept keys:
+//          S = Q K^T, dP = dO V^T               (SS, TMEM fp32)
+//          dS = P (dP - Delta), P = exp(S scale - LSE)   (CUDA cores -> TMEM bf16)
+//          dQ += dS K                           (TS, K as the MN-major operand)
+//   dKV  rows = 128 keys, streamed = 128-query tiles of the queries that keep
+//        them, for every query head of the key/value head:
+//          S^T = K Q^T, dP^T = V dO^T           (SS)
+//          P^T, dS^T                            (CUDA cores -> TMEM bf16)
+//          dV += P^T dO, dK += dS^T Q           (TS)
+// TMEM (512 columns): S at 0, dP at 128 (the bf16 P^T / dS^T overwrite their
+// first 64 columns once read), accumulators at 256 (and 256 + d).  One tile is
+// in flight at a time; the next tile's operands stream in through a 2-slot TMA
+// ring meanwhile.  Warps 0-3 do the elementwise work on their TMEM lane
+// quadrant, warp 4 loads, warp 5 owns TMEM and issues the MMAs.  Every wait is
+// bounded; on a timeout the CTA raises the error bit, drains and exits.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace focus {
+namespace {
+
+constexpr int kT = 128;
+constexpr int kWarpLd = 4;
+constexpr int kWarpMma = 5;
+constexpr int kThreads = 192;
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum : int { kDqGroup = 0, kDqLocal = 1, kDkvGroup = 2, kDkvLocal = 3 };
+
+template <int D>
+struct BCfg {
+  static constexpr int kChunk = 128 * 128;   // 128 rows x 64 bf16, one swizzle slab
+  static constexpr int kTile = 128 * D * 2;
+  static constexpr int kF0 = 0;              // fixed operands of the unit
+  static constexpr int kF1 = kTile;
+  static constexpr int kR = 2 * kTile;       // ring: 2 slots x (R0, R1)
+  static constexpr int kCol = kR + 4 * kTile;              // [2 slots][lse2, delta][128] fp32
+  static constexpr int kBar = kCol + 2 * 2 * 128 * 4;
+  static constexpr int kMisc = kBar + 256;
+  static constexpr int kBytes = kMisc + 64;
+  static constexpr int kSmem = kBytes + 1024;             // + slack to align the base to 1024
+  static constexpr uint32_t kS = 0, kDP = 128, kA0 = 256, kA1 = 256 + D;
+};
+static_assert(BCfg<128>::kSmem <= 227 * 1024, "backward shared memory above 227 KB");
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          int* err) {
+  const bool ok = mbar_wait(bar, parity, abort, err);
+  return __all_sync(0xffffffffu, ok);
+}
+
+struct BUnit {
+  bool valid;
+  int b, kv, h, prob, zq, zkv;
+  int row0, nrows;      // the unit's rows: query (dQ) or key (dKV) slots / tokens
+  int key0, nkeys;      // dQ group: key slots [key0, key0 + nkeys); dQ local: first key token
+  int ntile;            // streamed tiles per query head
+  int heads;            // query heads walked (dKV: H / H_kv; dQ: 1)
+};
+
+template <int KIND>
+__device__ __forceinline__ BUnit decode(const BwdArgs& a) {
+  BUnit U{};
+  U.valid = true;
+  U.heads = 1;
+  const int u = blockIdx.x;
+  if (KIND == kDqGroup) {
+    const int hpa = a.A == 1 ? a.H : a.H / a.H_kv;
+    const int y = u % hpa, io = u / hpa;
+    if (io >= *a.n_items) {
+      U.valid = false;
+      return U;
+    }
+    const focus_item_t it = a.items[a.order[io]];
+    U.b = it.b;
+    U.h = a.A == 1 ? y : it.a * (a.H / a.H_kv) + y;
+    U.kv = (U.h * a.H_kv) / a.H;
+    U.prob = it.b * a.A + it.a;
+    U.row0 = it.row0;
+    U.nrows = it.rows;
+    U.key0 = it.key0;
+    U.nkeys = it.keys;
+    U.ntile = (it.keys + kT - 1) / kT;
+  } else if (KIND == kDqLocal) {
+    U.h = u % a.H;
+    const int r = u / a.H;
+    const int nqt = (a.n + kT - 1) / kT;
+    const int qt = nqt - 1 - (r % nqt);
+    U.b = r / nqt;
+    U.kv = (U.h * a.H_kv) / a.H;
+    U.prob = U.b * a.A + (a.A == 1 ? 0 : U.kv);
+    U.row0 = qt * kT;
+    U.nrows = min(kT, a.n - U.row0);
+    const int kt0 = max(0, U.row0 - a.w + 1) / kT;
+    U.key0 = kt0 * kT;
+    U.ntile = (U.row0 + U.nrows - 1) / kT - kt0 + 1;
+  } else {
+    const int nkt = (a.n + kT - 1) / kT;
+    const int kt = u % nkt, r = u / nkt;
+    U.kv = r % a.H_kv;
+    U.b = r / a.H_kv;
+    U.h = U.kv * (a.H / a.H_kv);
+    U.prob = U.b * a.A + (a.A == 1 ? 0 : U.kv);
+    U.row0 = kt * kT;
+    U.nrows = min(kT, a.n - U.row0);
+    U.heads = a.H / a.H_kv;
+  }
+  U.zq = U.b * a.H + U.h;
+  U.zkv = U.b * a.H_kv + U.kv;
+  return U;
+}
+
+template <int D, int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const BwdArgs a) {
+  using Cfg = BCfg<D>;
+  constexpr int kChunks = D / 64;
+  constexpr bool kDq = KIND == kDqGroup || KIND == kDqLocal;
+  constexpr bool kGroup = KIND == kDqGroup || KIND == kDkvGroup;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBar);
+  uint64_t* fixed_full = bars + 0;
+  uint64_t* ring_full = bars + 1;     // [2]
+  uint64_t* ring_empty = bars + 3;    // [2]
+  uint64_t* sp_full = bars + 5;
+  uint64_t* ew_done = bars + 6;
+  uint64_t* acc_done = bars + 7;
+  uint64_t* mma_done = bars + 8;
+  uint64_t* col_full = bars + 9;      // [2] dKV: the slot's query LSE / Delta are in shared memory
+  int* misc = reinterpret_cast<int*>(smem + Cfg::kMisc);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 0);
+  volatile int* abort = misc + 1;
+  int* range = misc + 2;              // dKV: walked query range [range[0], range[1]]
+  float* colbuf = reinterpret_cast<float*>(smem + Cfg::kCol);
+
+  const int warp = warp_id(), lane = lane_id();
+  const BUnit U = decode<KIND>(a);
+  if (!U.valid) return;
+  const size_t pn = static_cast<size_t>(U.prob) * a.n;
+
+  if (threadIdx.x == 0) {
+    mbar_init(fixed_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&ring_full[s], 1);
+      mbar_init(&ring_empty[s], 1);
+    }
+    mbar_init(sp_full, 1);
+    mbar_init(ew_done, 4);
+    mbar_init(acc_done, 1);
+    mbar_init(mma_done, 1);
+    mbar_init(&col_full[0], 32);
+    mbar_init(&col_full[1], 32);
+    *abort = 0;
+    range[0] = 0x7fffffff;
+    range[1] = -1;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) tmem_alloc(tmem_slot, 512);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // ---- per-row bookkeeping of the elementwise threads (row = TMEM lane) ----
+  const int r = (warp & 3) * 32 + lane;
+  const bool row_ok = warp < 4 && r < U.nrows;
+  int rpos = -1;        // token of the row
+  int klo = 1, khi = 0; // kept streamed indices of the row (inclusive), in the walked order
+  if (warp < 4 && row_ok) {
+    if (KIND == kDqGroup) {
+      rpos = a.perm[pn + U.row0 + r];
+      klo = 0;
+      khi = a.farlen_slot[pn + U.row0 + r] - 1;           // prefix index
+    } else if (KIND == kDqLocal) {
+      rpos = U.row0 + r;
+      klo = rpos - a.w + 1;
+      khi = rpos;                                         // key tokens
+    } else if (KIND == kDkvGroup) {
+      const int u = U.row0 + r;
+      rpos = a.perm[pn + u];
+      const int32_t* off = a.offsets + static_cast<size_t>(U.prob) * (a.groups + 1);
+      int glo = 0, ghi = a.groups;
+      while (ghi - glo > 1) {
+        const int mid = (glo + ghi) >> 1;
+        if (off[mid] <= u) glo = mid; else ghi = mid;
+      }
+      const int gend = off[glo + 1];
+      const int target = rpos + a.w;
+      int s0 = u + 1, s1 = gend;
+      while (s0 < s1) {
+        const int mid = (s0 + s1) >> 1;
+        if (a.perm[pn + mid] < target) s0 = mid + 1; else s1 = mid;
+      }
+      klo = s0;
+      khi = gend - 1;                                     // query slots
+    } else {
+      rpos = U.row0 + r;
+      klo = rpos;
+      khi = min(a.n - 1, rpos + a.w - 1);                 // query tokens
+    }
+  }
+  if (!kDq) {
+    if (row_ok && klo <= khi) {
+      atomicMin(&range[0], klo);
+      atomicMax(&range[1], khi);
+    }
+    __syncthreads();
+  }
+  int wlo = 0, ntile = U.ntile;
+  if (!kDq) {
+    wlo = range[0];
+    const int whi = range[1];
+    ntile = whi >= wlo ? (whi - wlo) / kT + 1 : 0;
+  }
+  const int ntot = ntile * U.heads;
+
+  if (warp == kWarpLd) {
+    // ------------------------------------------------------------ loads ---
+    bool ok = true;
+    int issued = 0;
+    if (ntot > 0) {
+      // fixed operands: dQ -> (Q, dO) rows of the unit; dKV -> (K, V) rows
+      if (kGroup) {
+        if (lane == 0) mbar_expect_tx(fixed_full, 2 * Cfg::kTile);
+        __syncwarp();
+        const int first = a.perm[pn + U.row0];
+        int rows[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int rr = 4 * lane + j;
+          const int pos = rr < U.nrows ? a.perm[pn + U.row0 + rr] : first;
+          rows[j] = (kDq ? U.zq : U.zkv) * a.n + pos;
+        }
+#pragma unroll
+        for (int ch = 0; ch < kChunks; ++ch) {
+          tma_gather4(smem + Cfg::kF0 + ch * Cfg::kChunk + 4 * lane * 128, kDq ? &tm_q : &tm_k, fixed_full,
+                      ch * 64, rows[0], rows[1], rows[2], rows[3]);
+          tma_gather4(smem + Cfg::kF1 + ch * Cfg::kChunk + 4 * lane * 128, kDq ? &tm_do : &tm_v, fixed_full,
+                      ch * 64, rows[0], rows[1], rows[2], rows[3]);
+        }
+      } else if (lane == 0) {
+        mbar_expect_tx(fixed_full, 2 * Cfg::kTile);
+#pragma unroll
+        for (int ch = 0; ch < kChunks; ++ch) {
+          tma_load_3d(smem + Cfg::kF0 + ch * Cfg::kChunk, kDq ? &tm_q : &tm_k, fixed_full, ch * 64, U.row0,
+                      kDq ? U.zq : U.zkv);
+          tma_load_3d(smem + Cfg::kF1 + ch * Cfg::kChunk, kDq ? &tm_do : &tm_v, fixed_full, ch * 64, U.row0,
+                      kDq ? U.zq : U.zkv);
+        }
+      }
+      for (int it = 0; it < ntot && ok; ++it) {
+        const int sl = it & 1, use = it >> 1;
+        if (use > 0 && !mbar_wait_nap(&ring_empty[sl], (use - 1) & 1, abort, a.err)) ok = false;
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        const int t = it % ntile, hh = it / ntile;
+        const int zq = U.b * a.H + U.h + hh;
+        uint8_t* r0 = smem + Cfg::kR + sl * 2 * Cfg::kTile;
+        uint8_t* r1 = r0 + Cfg::kTile;
+        if (kGroup) {
+          // dQ: key slots key0 + t*128 + rr of the prefix; dKV: query slots wlo + t*128 + rr
+          if (lane == 0) mbar_expect_tx(&ring_full[sl], 2 * Cfg::kTile);
+          __syncwarp();
+          const int base = kDq ? U.key0 : wlo;
+          const int lim = kDq ? U.key0 + U.nkeys : a.n;
+          const int first = a.perm[pn + base];
+          int rows[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int s = base + t * kT + 4 * lane + j;
+            const int pos = s < lim ? a.perm[pn + s] : first;
+            rows[j] = (kDq ? U.zkv : zq) * a.n + pos;
+          }
+#pragma unroll
+          for (int ch = 0; ch < kChunks; ++ch) {
+            tma_gather4(r0 + ch * Cfg::kChunk + 4 * lane * 128, kDq ? &tm_k : &tm_q, &ring_full[sl], ch * 64,
+                        rows[0], rows[1], rows[2], rows[3]);
+            tma_gather4(r1 + ch * Cfg::kChunk + 4 * lane * 128, kDq ? &tm_v : &tm_do, &ring_full[sl], ch * 64,
+                        rows[0], rows[1], rows[2], rows[3]);
+          }
+        } else if (lane == 0) {
+          mbar_expect_tx(&ring_full[sl], 2 * Cfg::kTile);
+          const int y = (kDq ? U.key0 : wlo) + t * kT;
+#pragma unroll
+          for (int ch = 0; ch < kChunks; ++ch) {
+            tma_load_3d(r0 + ch * Cfg::kChunk, kDq ? &tm_k : &tm_q, &ring_full[sl], ch * 64, y, kDq ? U.zkv : zq);
+            tma_load_3d(r1 + ch * Cfg::kChunk, kDq ? &tm_v : &tm_do, &ring_full[sl], ch * 64, y, kDq ? U.zkv : zq);
+          }
+        }
+        if (!kDq) {
+          // the tile's query columns: LSE (log2 units) and Delta for head h + hh;
+          // the slot is free (ring_empty above), and each lane's arrival
+          // publishes its four entries
+          float* cb = colbuf + sl * 256;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int c = 4 * lane + j;
+            const int q = wlo + t * kT + c;
+            float l2 = 0.f, dl = 0.f;
+            if (q < a.n) {
+              const int pos = kGroup ? a.perm[pn + q] : q;
+              const size_t qi = static_cast<size_t>(zq) * a.n + pos;
+              l2 = a.lse[qi] * kLog2e;
+              dl = a.delta[qi];
+            }
+            cb[c] = l2;
+            cb[128 + c] = dl;
+          }
+          mbar_arrive(&col_full[sl]);
+        }
+        ++issued;
+      }
+      if ((*abort || !ok) && lane == 0) {
+        // copies already issued must land before the CTA exits
+        const unsigned long long t0 = global_ns();
+        while (!mbar_try_wait(fixed_full, 0) && global_ns() - t0 < kWaitTimeoutNs) {}
+        for (int it = max(0, issued - 2); it < issued; ++it) {
+          const unsigned long long t1 = global_ns();
+          while (!mbar_try_wait(&ring_full[it & 1], (it >> 1) & 1) && global_ns() - t1 < kWaitTimeoutNs) {}
+        }
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------- MMAs ---
+    if (lane == 0 && ntot > 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(128, kT, false, false);
+      constexpr uint32_t idAcc = idesc_bf16_f32(128, D, false, true);
+      constexpr uint32_t dhi = sw128_desc_hi();
+      const uint32_t f0 = sw128_desc_lo(smem_u32(smem + Cfg::kF0), 16);
+      const uint32_t f1 = sw128_desc_lo(smem_u32(smem + Cfg::kF1), 16);
+      bool ok = mbar_wait_nap(fixed_full, 0, abort, a.err);
+      for (int it = 0; it < ntot && ok; ++it) {
+        const int sl = it & 1;
+        if (!mbar_wait_nap(&ring_full[sl], (it >> 1) & 1, abort, a.err)) { ok = false; break; }
+        if (it > 0 && !mbar_wait_nap(acc_done, (it - 1) & 1, abort, a.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t rb = smem_u32(smem + Cfg::kR + sl * 2 * Cfg::kTile);
+        const uint32_t r0k = sw128_desc_lo(rb, 16), r1k = sw128_desc_lo(rb + Cfg::kTile, 16);
+        // S = F0 R0^T, dP = F1 R1^T (both operands K-major over d)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * Cfg::kChunk + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + Cfg::kS, desc_join(f0 + off, dhi), desc_join(r0k + off, dhi), idS, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * Cfg::kChunk + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + Cfg::kDP, desc_join(f1 + off, dhi), desc_join(r1k + off, dhi), idS, kk > 0);
+        }
+        mma_commit(sp_full);
+        if (!mbar_wait_nap(ew_done, it & 1, abort, a.err)) { ok = false; break; }
+        tc_fence_after();
+        // accumulators: the streamed tiles as MN-major operands (reduction over the tile's rows)
+        const uint32_t r0m = sw128_desc_lo(rb, Cfg::kChunk), r1m = sw128_desc_lo(rb + Cfg::kTile, Cfg::kChunk);
+        if (kDq) {
+#pragma unroll
+          for (int kk = 0; kk < kT / 16; ++kk)
+            mma_ts(tmem + Cfg::kA0, tmem + Cfg::kDP + kk * 8, desc_join(r0m + kk * ((16 * 128) >> 4), dhi), idAcc,
+                   it > 0 || kk > 0);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < kT / 16; ++kk)
+            mma_ts(tmem + Cfg::kA0, tmem + Cfg::kS + kk * 8, desc_join(r1m + kk * ((16 * 128) >> 4), dhi), idAcc,
+                   it > 0 || kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < kT / 16; ++kk)
+            mma_ts(tmem + Cfg::kA1, tmem + Cfg::kDP + kk * 8, desc_join(r0m + kk * ((16 * 128) >> 4), dhi), idAcc,
+                   it > 0 || kk > 0);
+        }
+        mma_commit(acc_done);
+        mma_commit(&ring_empty[sl]);
+      }
+      // every MMA issued above has finished before TMEM is released
+      mma_commit(mma_done);
+      const unsigned long long t0 = global_ns();
+      while (!mbar_try_wait(mma_done, 0) && global_ns() - t0 < kWaitTimeoutNs) {}
+    }
+  } else {
+    // ------------------------------------------------------ elementwise ---
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const float sl2 = a.scale_log2;
+    float lse2 = 0.f, dlt = 0.f;
+    if (kDq && row_ok) {
+      const size_t qi = static_cast<size_t>(U.zq) * a.n + rpos;
+      lse2 = a.lse[qi] * kLog2e;
+      dlt = a.delta[qi];
+    }
+    bool ok = true;
+    for (int it = 0; it < ntot && ok; ++it) {
+      const int t = it % ntile;
+      const float* cb = colbuf + (it & 1) * 256;  // [lse2 x128, delta x128] of this tile's queries
+      if (!kDq && !warp_wait(&col_full[it & 1], (it >> 1) & 1, abort, a.err)) { ok = false; break; }
+      if (!warp_wait(sp_full, it & 1, abort, a.err)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < kT / 32; ++c) {
+        uint32_t sv[32], dv[32];
+        tmem_ld32(tmem + lane_base + Cfg::kS + c * 32, sv);
+        tmem_ld32(tmem + lane_base + Cfg::kDP + c * 32, dv);
+        tmem_wait_ld();
+        uint32_t pp[16], dd[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float p2[2], d2[2];
+#pragma unroll
+          for (int q2 = 0; q2 < 2; ++q2) {
+            const int col = c * 32 + e + q2;
+            const int idx = (kDq ? (KIND == kDqGroup ? 0 : U.key0) : wlo) + t * kT + col;
+            const bool keep = row_ok && idx >= klo && idx <= khi;
+            const float l2 = kDq ? lse2 : cb[col];
+            const float dl = kDq ? dlt : cb[128 + col];
+            const float p = keep ? ex2f(__uint_as_float(sv[e + q2]) * sl2 - l2) : 0.f;
+            p2[q2] = p;
+            d2[q2] = p * (__uint_as_float(dv[e + q2]) - dl);
+          }
+          pp[e / 2] = pack_bf16x2(p2[0], p2[1]);
+          dd[e / 2] = pack_bf16x2(d2[0], d2[1]);
+        }
+        // chunk c's bf16 pairs take columns 16c..16c+15, inside the fp32
+        // columns 0..32c+31 already read
+        tmem_st16(tmem + lane_base + Cfg::kDP + c * 16, dd);
+        if (!kDq) tmem_st16(tmem + lane_base + Cfg::kS + c * 16, pp);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      warp_arrive(ew_done, lane);
+    }
+    // epilogue: the accumulators once the last tile's MMAs are done
+    const bool have = ok && ntot > 0;
+    if (have && !warp_wait(acc_done, (ntot - 1) & 1, abort, a.err)) ok = false;
+    if (ok) {
+      tc_fence_after();
+      const size_t orow = static_cast<size_t>(kDq ? U.zq : U.zkv) * a.n + (rpos >= 0 ? rpos : 0);
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t x0[32], x1[32];
+        if (have) {
+          tmem_ld32(tmem + lane_base + Cfg::kA0 + c * 32, x0);
+          if (!kDq) tmem_ld32(tmem + lane_base + Cfg::kA1 + c * 32, x1);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x0[e] = x1[e] = 0u;
+        }
+        if (!row_ok) continue;
+        const size_t o = orow * D + c * 32;
+        if (KIND == kDqGroup) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) a.dq_far[o + e] = __uint_as_float(x0[e]) * a.scale;
+        } else if (KIND == kDqLocal) {
+          const bool far = a.farlen_tok[pn + rpos] > 0;
+          __nv_bfloat16* dq = static_cast<__nv_bfloat16*>(a.dQ);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            float v = __uint_as_float(x0[e]) * a.scale;
+            if (far) v += a.dq_far[o + e];
+            dq[o + e] = __float2bfloat16_rn(v);
+          }
+        } else if (KIND == kDkvGroup) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            a.dv_far[o + e] = __uint_as_float(x0[e]);
+            a.dk_far[o + e] = __uint_as_float(x1[e]) * a.scale;
+          }
+        } else {
+          __nv_bfloat16* dk = static_cast<__nv_bfloat16*>(a.dK);
+          __nv_bfloat16* dvv = static_cast<__nv_bfloat16*>(a.dV);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            dvv[o + e] = __float2bfloat16_rn(__uint_as_float(x0[e]) + a.dv_far[o + e]);
+            dk[o + e] = __float2bfloat16_rn(__uint_as_float(x1[e]) * a.scale + a.dk_far[o + e]);
+          }
+        }
+      }
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const BwdArgs& a, const CUtensorMap* q2, const CUtensorMap* do2, const CUtensorMap* k2,
+                     const CUtensorMap* v2, const CUtensorMap* q3, const CUtensorMap* do3, const CUtensorMap* k3,
+                     const CUtensorMap* v3, int max_items, cudaStream_t st) {
+  using Cfg = BCfg<D>;
+  const int hpa = a.A == 1 ? a.H : a.H / a.H_kv;
+  const long long g_units = static_cast<long long>(max_items) * hpa;
+  const long long q_units = static_cast<long long>(a.B) * a.H * ((a.n + kT - 1) / kT);
+  const long long k_units = static_cast<long long>(a.B) * a.H_kv * ((a.n + kT - 1) / kT);
+  if (g_units > 0)
+    bwd_tc_kernel<D, kDqGroup><<<static_cast<unsigned>(g_units), kThreads, Cfg::kSmem, st>>>(*q2, *do2, *k2, *v2, a);
+  bwd_tc_kernel<D, kDqLocal><<<static_cast<unsigned>(q_units), kThreads, Cfg::kSmem, st>>>(*q3, *do3, *k3, *v3, a);
+  bwd_tc_kernel<D, kDkvGroup><<<static_cast<unsigned>(k_units), kThreads, Cfg::kSmem, st>>>(*q2, *do2, *k2, *v2, a);
+  bwd_tc_kernel<D, kDkvLocal><<<static_cast<unsigned>(k_units), kThreads, Cfg::kSmem, st>>>(*q3, *do3, *k3, *v3, a);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t set_smem_d() {
+  using Cfg = BCfg<D>;
+  cudaError_t e;
+  e = cudaFuncSetAttribute(bwd_tc_kernel<D, kDqGroup>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(bwd_tc_kernel<D, kDqLocal>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(bwd_tc_kernel<D, kDkvGroup>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(bwd_tc_kernel<D, kDkvLocal>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd_tc(const BwdArgs& a, const CUtensorMap* q2, const CUtensorMap* do2,
+                               const CUtensorMap* k2, const CUtensorMap* v2, const CUtensorMap* q3,
+                               const CUtensorMap* do3, const CUtensorMap* k3, const CUtensorMap* v3,
+                               int max_items, cudaStream_t st) {
+  if (a.d == 64) return launch_d<64>(a, q2, do2, k2, v2, q3, do3, k3, v3, max_items, st);
+  if (a.d == 128) return launch_d<128>(a, q2, do2, k2, v2, q3, do3, k3, v3, max_items, st);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t setup_bwd_tc_kernels() {
+  cudaError_t e = set_smem_d<64>();
+  if (e != cudaSuccess) return e;
+  return set_smem_d<128>();
+}
+
+}  // namespace focus

@@ -170,8 +170,19 @@ struct BwdArgs {
   const int32_t* n_items;
   int B, H, H_kv, n, d, A, groups, w;   // groups: K, the number of centroids
   float scale, scale_log2;
+  int* err;                         // device error word (bounded waits)
 };
 cudaError_t launch_attn_bwd(const BwdArgs& a, int dtype, int max_items, cudaStream_t st);
+cudaError_t launch_bwd_delta(const BwdArgs& a, int dtype, cudaStream_t st);
+
+// attn_bwd_tc.cu: the same backward for bf16 on the tcgen05 tensor cores (after
+// launch_bwd_delta).  *2: {d, planes*n} one-row-box maps for row gathers; *3:
+// {d, n, planes} 128-row tile maps.
+cudaError_t launch_attn_bwd_tc(const BwdArgs& a, const CUtensorMap* q2, const CUtensorMap* do2,
+                               const CUtensorMap* k2, const CUtensorMap* v2, const CUtensorMap* q3,
+                               const CUtensorMap* do3, const CUtensorMap* k3, const CUtensorMap* v3,
+                               int max_items, cudaStream_t st);
+cudaError_t setup_bwd_tc_kernels();
 cudaError_t launch_sinkhorn(const SinkhornLaunch& L, int iters, cudaStream_t st);
 
 }  // namespace focus

@@ -17,9 +17,10 @@
 //            consecutive columns of a row)
 //   colfin   per column: combine the chunk partials -> v
 //            (grid: K/32 x P; 32 columns x 32 chunk lanes per block)
-//   row      one warp per row: LSE over the K columns with v from shared
-//            memory -> u; the last round also writes G (may alias S: each lane
-//            reads its elements before writing them, and rows are disjoint)
+//   row      LR lanes per row (8 for K <= 128, else the whole warp): LSE
+//            over the K columns with v from shared memory -> u; the last
+//            round also writes G (may alias S: each lane reads its elements
+//            before writing them, and rows are disjoint)
 // Memory-bound: each round streams S twice.
 #include "common.cuh"
 #include "kernels.h"
@@ -126,30 +127,35 @@ __global__ void __launch_bounds__(1024) sinkhorn_colfin_kernel(SinkhornLaunch L,
   }
 }
 
+template <int LR>
 __global__ void __launch_bounds__(256) sinkhorn_row_kernel(SinkhornLaunch L, int write_g) {
   extern __shared__ float vs[];        // [K]
+  constexpr int kRowsPerBlock = 256 / LR;
   const int p = blockIdx.y;
   const int K = L.K;
   for (int k = threadIdx.x; k < K; k += blockDim.x) vs[k] = L.v[static_cast<size_t>(p) * K + k];
   __syncthreads();
-  const int lane = lane_id();
-  const int i = blockIdx.x * (blockDim.x / 32) + warp_id();
-  if (i >= L.n) return;
-  const size_t row = (static_cast<size_t>(p) * L.n + i) * K;
+  const int lr = threadIdx.x % LR;
+  const int i = blockIdx.x * kRowsPerBlock + threadIdx.x / LR;
+  // rows past n still join the shuffles (LR < 32 shares a warp between rows)
+  const bool valid = i < L.n;
+  const size_t row = (static_cast<size_t>(p) * L.n + (valid ? i : 0)) * K;
   const float* S = L.S + row;
   float m = -INFINITY, s = 0.f;
-  for (int k = lane; k < K; k += 32) lse_push(m, s, S[k] * L.inv_tau + vs[k]);
+  if (valid)
+    for (int k = lr; k < K; k += LR) lse_push(m, s, S[k] * L.inv_tau + vs[k]);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
+  for (int o = LR / 2; o > 0; o >>= 1) {
     const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
     const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
     lse_join(m, s, m2, s2);
   }
+  if (!valid) return;
   const float ui = s > 0.f ? -(m + logf(s)) : 0.f;
-  if (lane == 0) L.u[static_cast<size_t>(p) * L.n + i] = ui;
+  if (lr == 0) L.u[static_cast<size_t>(p) * L.n + i] = ui;
   if (write_g) {
     float* G = L.G + row;
-    for (int k = lane; k < K; k += 32) G[k] = expf(S[k] * L.inv_tau + ui + vs[k]);
+    for (int k = lr; k < K; k += LR) G[k] = expf(S[k] * L.inv_tau + ui + vs[k]);
   }
 }
 
@@ -172,7 +178,10 @@ cudaError_t launch_sinkhorn(const SinkhornLaunch& L, int iters, cudaStream_t st)
   for (int t = 0; t < iters && e == cudaSuccess; ++t) {
     sinkhorn_colpart_kernel<<<dim3(chunks, L.P), 256, sm_part, st>>>(L, rpc);
     sinkhorn_colfin_kernel<<<dim3((L.K + 31) / 32, L.P), dim3(32, 32), 0, st>>>(L, chunks);
-    sinkhorn_row_kernel<<<dim3((L.n + 7) / 8, L.P), 256, sm_row, st>>>(L, t == iters - 1);
+    if (L.K <= 128)
+      sinkhorn_row_kernel<8><<<dim3((L.n + 31) / 32, L.P), 256, sm_row, st>>>(L, t == iters - 1);
+    else
+      sinkhorn_row_kernel<32><<<dim3((L.n + 7) / 8, L.P), 256, sm_row, st>>>(L, t == iters - 1);
     e = cudaGetLastError();
   }
   return e;

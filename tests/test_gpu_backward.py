@@ -1,5 +1,6 @@
-"""GPU parity for the backward pass (focus_attention_bwd) against the fp64
-oracle's gradients on the same inputs and the same upstream gradient dO.
+"""GPU parity for the backward pass (focus_attention_bwd: tcgen05 tensor cores
+for bf16, CUDA cores for fp32) against the fp64 oracle's gradients on the same
+inputs and the same upstream gradient dO.
 
 The GPU runs the forward first (its O and LSE feed the backward, as in
 training).  Tolerances, relative to M = max(largest reference gradient entry, 0.1):
@@ -84,6 +85,8 @@ def _run(fz, dtype, B, H, H_kv, A, n, d, K, w, kind, seed):
     ("bf16", 1, 2, 2, 1, 1, 128, 3, 5, "uniform"),          # one token
     ("bf16", 1, 2, 1, 1, 400, 64, 5, 1000, "uniform"),      # w > n
     ("bf16", 2, 2, 2, 1, 257, 128, 3, 0, "blocks"),         # w = 0
+    ("bf16", 1, 4, 2, 1, 2048, 128, 8, 128, "zipf"),        # many key and query tiles per group
+    ("bf16", 1, 2, 2, 2, 1500, 64, 1, 200, "one"),          # one group: dense-like far part, d = 64
 ])
 def test_backward_all_rows(fz, dtype, B, H, H_kv, A, n, d, K, w, kind):
     (Q, Kt, V, dO, g, p), (dQ, dK, dV) = _run(fz, dtype, B, H, H_kv, A, n, d, K, w, kind, seed=n + K + w + 3)
