@@ -18,9 +18,12 @@
 // TMEM (512 columns): S at 0, dP at 128 (the bf16 P^T / dS^T overwrite their
 // first 64 columns once read), accumulators at 256 (and 256 + d).  One tile is
 // in flight at a time; the next tile's operands stream in through a 2-slot TMA
-// ring meanwhile.  Warps 0-3 do the elementwise work on their TMEM lane
-// quadrant, warp 4 loads, warp 5 owns TMEM and issues the MMAs.  Every wait is
-// bounded; on a timeout the CTA raises the error bit, drains and exits.
+// ring meanwhile.  Warps 0-7 do the elementwise work, two per TMEM lane
+// quadrant, each on half of the row's columns: both halves read their fp32
+// columns, meet at an mbarrier, and only then write the bf16 pairs over the
+// first half of the fp32 columns.  Warp 8 loads, warp 9 owns TMEM and issues
+// the MMAs.  Every wait is bounded; on a timeout the CTA raises the error bit,
+// drains and exits.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -28,9 +31,10 @@ namespace focus {
 namespace {
 
 constexpr int kT = 128;
-constexpr int kWarpLd = 4;
-constexpr int kWarpMma = 5;
-constexpr int kThreads = 192;
+constexpr int kEwWarps = 8;
+constexpr int kWarpLd = 8;
+constexpr int kWarpMma = 9;
+constexpr int kThreads = 320;
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum : int { kDqGroup = 0, kDqLocal = 1, kDkvGroup = 2, kDkvLocal = 3 };
@@ -149,6 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_done = bars + 7;
   uint64_t* mma_done = bars + 8;
   uint64_t* col_full = bars + 9;      // [2] dKV: the slot's query LSE / Delta are in shared memory
+  uint64_t* read_done = bars + 11;    // every elementwise warp has read this tile's fp32 S and dP
   int* misc = reinterpret_cast<int*>(smem + Cfg::kMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 0);
   volatile int* abort = misc + 1;
@@ -167,7 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ring_empty[s], 1);
     }
     mbar_init(sp_full, 1);
-    mbar_init(ew_done, 4);
+    mbar_init(ew_done, kEwWarps);
+    mbar_init(read_done, kEwWarps);
     mbar_init(acc_done, 1);
     mbar_init(mma_done, 1);
     mbar_init(&col_full[0], 32);
@@ -184,10 +190,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- per-row bookkeeping of the elementwise threads (row = TMEM lane) ----
   const int r = (warp & 3) * 32 + lane;
-  const bool row_ok = warp < 4 && r < U.nrows;
+  const int half = (warp >> 2) & 1;   // elementwise: which half of the columns
+  const bool row_ok = warp < kEwWarps && r < U.nrows;
   int rpos = -1;        // token of the row
   int klo = 1, khi = 0; // kept streamed indices of the row (inclusive), in the walked order
-  if (warp < 4 && row_ok) {
+  if (warp < kEwWarps && row_ok) {
     if (KIND == kDqGroup) {
       rpos = a.perm[pn + U.row0 + r];
       klo = 0;
@@ -413,35 +420,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!kDq && !warp_wait(&col_full[it & 1], (it >> 1) & 1, abort, a.err)) { ok = false; break; }
       if (!warp_wait(sp_full, it & 1, abort, a.err)) { ok = false; break; }
       tc_fence_after();
-#pragma unroll 1
-      for (int c = 0; c < kT / 32; ++c) {
-        uint32_t sv[32], dv[32];
-        tmem_ld32(tmem + lane_base + Cfg::kS + c * 32, sv);
-        tmem_ld32(tmem + lane_base + Cfg::kDP + c * 32, dv);
-        tmem_wait_ld();
-        uint32_t pp[16], dd[16];
+      // this half's 64 columns of S and dP, all read before anyone writes
+      uint32_t sv[64], dv[64];
+      tmem_ld32(tmem + lane_base + Cfg::kS + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+      tmem_ld32(tmem + lane_base + Cfg::kS + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+      tmem_ld32(tmem + lane_base + Cfg::kDP + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&dv[0]));
+      tmem_ld32(tmem + lane_base + Cfg::kDP + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&dv[32]));
+      tmem_wait_ld();
+      tc_fence_before();
+      warp_arrive(read_done, lane);
+      if (!warp_wait(read_done, it & 1, abort, a.err)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t pp[32], dd[32];
+      const int base_idx = (kDq ? (KIND == kDqGroup ? 0 : U.key0) : wlo) + t * kT + half * 64;
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float p2[2], d2[2];
+      for (int e = 0; e < 64; e += 2) {
+        float p2[2], d2[2];
 #pragma unroll
-          for (int q2 = 0; q2 < 2; ++q2) {
-            const int col = c * 32 + e + q2;
-            const int idx = (kDq ? (KIND == kDqGroup ? 0 : U.key0) : wlo) + t * kT + col;
-            const bool keep = row_ok && idx >= klo && idx <= khi;
-            const float l2 = kDq ? lse2 : cb[col];
-            const float dl = kDq ? dlt : cb[128 + col];
-            const float p = keep ? ex2f(__uint_as_float(sv[e + q2]) * sl2 - l2) : 0.f;
-            p2[q2] = p;
-            d2[q2] = p * (__uint_as_float(dv[e + q2]) - dl);
-          }
-          pp[e / 2] = pack_bf16x2(p2[0], p2[1]);
-          dd[e / 2] = pack_bf16x2(d2[0], d2[1]);
+        for (int q2 = 0; q2 < 2; ++q2) {
+          const int col = half * 64 + e + q2;
+          const int idx = base_idx + e + q2;
+          const bool keep = row_ok && idx >= klo && idx <= khi;
+          const float l2 = kDq ? lse2 : cb[col];
+          const float dl = kDq ? dlt : cb[128 + col];
+          const float p = keep ? ex2f(__uint_as_float(sv[e + q2]) * sl2 - l2) : 0.f;
+          p2[q2] = p;
+          d2[q2] = p * (__uint_as_float(dv[e + q2]) - dl);
         }
-        // chunk c's bf16 pairs take columns 16c..16c+15, inside the fp32
-        // columns 0..32c+31 already read
-        tmem_st16(tmem + lane_base + Cfg::kDP + c * 16, dd);
-        if (!kDq) tmem_st16(tmem + lane_base + Cfg::kS + c * 16, pp);
+        pp[e / 2] = pack_bf16x2(p2[0], p2[1]);
+        dd[e / 2] = pack_bf16x2(d2[0], d2[1]);
       }
+      // the half's 64 bf16 values take packed columns 32*half .. 32*half + 31
+      tmem_st32(tmem + lane_base + Cfg::kDP + half * 32, dd);
+      if (!kDq) tmem_st32(tmem + lane_base + Cfg::kS + half * 32, pp);
       tmem_wait_st();
       tc_fence_before();
       warp_arrive(ew_done, lane);
@@ -452,8 +463,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       tc_fence_after();
       const size_t orow = static_cast<size_t>(kDq ? U.zq : U.zkv) * a.n + (rpos >= 0 ? rpos : 0);
+      // this half's accumulator columns: [half * D/2, (half + 1) * D/2)
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
         uint32_t x0[32], x1[32];
         if (have) {
           tmem_ld32(tmem + lane_base + Cfg::kA0 + c * 32, x0);
@@ -466,30 +478,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!row_ok) continue;
         const size_t o = orow * D + c * 32;
         if (KIND == kDqGroup) {
+          float4* dst = reinterpret_cast<float4*>(a.dq_far + o);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) a.dq_far[o + e] = __uint_as_float(x0[e]) * a.scale;
+          for (int v = 0; v < 8; ++v)
+            dst[v] = make_float4(__uint_as_float(x0[4 * v]) * a.scale, __uint_as_float(x0[4 * v + 1]) * a.scale,
+                                 __uint_as_float(x0[4 * v + 2]) * a.scale, __uint_as_float(x0[4 * v + 3]) * a.scale);
         } else if (KIND == kDqLocal) {
           const bool far = a.farlen_tok[pn + rpos] > 0;
-          __nv_bfloat16* dq = static_cast<__nv_bfloat16*>(a.dQ);
+          const float4* fq = reinterpret_cast<const float4*>(a.dq_far + o);
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dQ) + o);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            float v = __uint_as_float(x0[e]) * a.scale;
-            if (far) v += a.dq_far[o + e];
-            dq[o + e] = __float2bfloat16_rn(v);
+          for (int v = 0; v < 4; ++v) {
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(x0[8 * v + e]) * a.scale;
+            if (far) {
+              const float4 g0 = fq[2 * v], g1 = fq[2 * v + 1];
+              f[0] += g0.x; f[1] += g0.y; f[2] += g0.z; f[3] += g0.w;
+              f[4] += g1.x; f[5] += g1.y; f[6] += g1.z; f[7] += g1.w;
+            }
+            dst[v] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                                pack_bf16x2(f[6], f[7]));
           }
         } else if (KIND == kDkvGroup) {
+          float4* dvd = reinterpret_cast<float4*>(a.dv_far + o);
+          float4* dkd = reinterpret_cast<float4*>(a.dk_far + o);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            a.dv_far[o + e] = __uint_as_float(x0[e]);
-            a.dk_far[o + e] = __uint_as_float(x1[e]) * a.scale;
+          for (int v = 0; v < 8; ++v) {
+            dvd[v] = make_float4(__uint_as_float(x0[4 * v]), __uint_as_float(x0[4 * v + 1]),
+                                 __uint_as_float(x0[4 * v + 2]), __uint_as_float(x0[4 * v + 3]));
+            dkd[v] = make_float4(__uint_as_float(x1[4 * v]) * a.scale, __uint_as_float(x1[4 * v + 1]) * a.scale,
+                                 __uint_as_float(x1[4 * v + 2]) * a.scale, __uint_as_float(x1[4 * v + 3]) * a.scale);
           }
         } else {
-          __nv_bfloat16* dk = static_cast<__nv_bfloat16*>(a.dK);
-          __nv_bfloat16* dvv = static_cast<__nv_bfloat16*>(a.dV);
+          const float4* fv = reinterpret_cast<const float4*>(a.dv_far + o);
+          const float4* fk = reinterpret_cast<const float4*>(a.dk_far + o);
+          uint4* dvd = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dV) + o);
+          uint4* dkd = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dK) + o);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            dvv[o + e] = __float2bfloat16_rn(__uint_as_float(x0[e]) + a.dv_far[o + e]);
-            dk[o + e] = __float2bfloat16_rn(__uint_as_float(x1[e]) * a.scale + a.dk_far[o + e]);
+          for (int v = 0; v < 4; ++v) {
+            const float4 v0 = fv[2 * v], v1 = fv[2 * v + 1], k0 = fk[2 * v], k1 = fk[2 * v + 1];
+            const float gv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+            const float gk[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+            float fvv[8], fkk[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              fvv[e] = __uint_as_float(x0[8 * v + e]) + gv[e];
+              fkk[e] = __uint_as_float(x1[8 * v + e]) * a.scale + gk[e];
+            }
+            dvd[v] = make_uint4(pack_bf16x2(fvv[0], fvv[1]), pack_bf16x2(fvv[2], fvv[3]),
+                                pack_bf16x2(fvv[4], fvv[5]), pack_bf16x2(fvv[6], fvv[7]));
+            dkd[v] = make_uint4(pack_bf16x2(fkk[0], fkk[1]), pack_bf16x2(fkk[2], fkk[3]),
+                                pack_bf16x2(fkk[4], fkk[5]), pack_bf16x2(fkk[6], fkk[7]));
           }
         }
       }
