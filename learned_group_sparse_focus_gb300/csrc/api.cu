@@ -893,26 +893,40 @@ focus_status_t focus_sinkhorn_fwd(const focus_params_t* p, int32_t iters, float 
 
 // ------------------------------------------------------------- backward ---
 
-static size_t backward_layout(const focus_params_t* p, size_t* delta, size_t* dq, size_t* dk,
-                              size_t* dv) {
+struct BwdLayout {
+  size_t delta, dq, dk, dv, qs, dos, ks, vs, lse_s, delta_s, total;
+};
+
+static BwdLayout backward_layout(const focus_params_t* p) {
+  BwdLayout L{};
   const size_t qrows = static_cast<size_t>(p->B) * p->H * p->n;
   const size_t krows = static_cast<size_t>(p->B) * p->H_kv * p->n;
   size_t o = align_up(kAlign);                       // error word
-  *delta = o;
-  o = align_up(o + qrows * 4);
-  *dq = o;
-  o = align_up(o + qrows * p->d * 4);
-  *dk = o;
-  o = align_up(o + krows * p->d * 4);
-  *dv = o;
-  o = align_up(o + krows * p->d * 4);
-  return o;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes);
+    return at;
+  };
+  L.delta = take(qrows * 4);
+  L.dq = take(qrows * p->d * 4);
+  L.dk = take(krows * p->d * 4);
+  L.dv = take(krows * p->d * 4);
+  if (p->dtype == FOCUS_BF16) {
+    // the group kernels' operands in index order
+    L.qs = take(qrows * p->d * 2);
+    L.dos = take(qrows * p->d * 2);
+    L.ks = take(krows * p->d * 2);
+    L.vs = take(krows * p->d * 2);
+    L.lse_s = take(qrows * 4);
+    L.delta_s = take(qrows * 4);
+  }
+  L.total = o;
+  return L;
 }
 
 size_t focus_backward_workspace_bytes(const focus_params_t* p) {
   if (!params_ok(p)) return 0;
-  size_t a, b, c, d;
-  return backward_layout(p, &a, &b, &c, &d);
+  return backward_layout(p).total;
 }
 
 focus_status_t focus_attention_bwd(const focus_params_t* p, const void* Q, const void* K,
@@ -930,8 +944,8 @@ focus_status_t focus_attention_bwd(const focus_params_t* p, const void* Q, const
     if (!q || !aligned16(q)) return FOCUS_ERR_INVALID_ARG;
   if (!(p->d == 64 || p->d == 128)) return FOCUS_ERR_UNSUPPORTED;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return FOCUS_ERR_INVALID_ARG;
-  size_t o_delta, o_dq, o_dk, o_dv;
-  if (ws_bytes < backward_layout(p, &o_delta, &o_dq, &o_dk, &o_dv)) return FOCUS_ERR_WORKSPACE;
+  const BwdLayout BL = backward_layout(p);
+  if (ws_bytes < BL.total) return FOCUS_ERR_WORKSPACE;
   if (focus_status_t s = ensure_setup()) return s;
   BwdArgs a{};
   a.Q = Q;
@@ -940,10 +954,10 @@ focus_status_t focus_attention_bwd(const focus_params_t* p, const void* Q, const
   a.O = O;
   a.dO = dO;
   a.lse = lse;
-  a.delta = at<float>(ws, o_delta);
-  a.dq_far = at<float>(ws, o_dq);
-  a.dk_far = at<float>(ws, o_dk);
-  a.dv_far = at<float>(ws, o_dv);
+  a.delta = at<float>(ws, BL.delta);
+  a.dq_far = at<float>(ws, BL.dq);
+  a.dk_far = at<float>(ws, BL.dk);
+  a.dv_far = at<float>(ws, BL.dv);
   a.err = at<int>(ws, 0);
   a.dQ = dQ;
   a.dK = dK;
@@ -971,14 +985,24 @@ focus_status_t focus_attention_bwd(const focus_params_t* p, const void* Q, const
   const uint64_t qplanes = static_cast<uint64_t>(p->B) * p->H;
   const uint64_t planes = static_cast<uint64_t>(p->B) * p->H_kv;
   if (static_cast<long long>(qplanes) * p->n >= (1LL << 31)) return FOCUS_ERR_UNSUPPORTED;
-  CUtensorMap q2, do2, k2, v2, q3, do3, k3, v3;
-  if (!make_map(&q2, Q, p->d, qplanes * p->n, 1, 1, 2) || !make_map(&do2, dO, p->d, qplanes * p->n, 1, 1, 2) ||
-      !make_map(&k2, K, p->d, planes * p->n, 1, 1, 2) || !make_map(&v2, V, p->d, planes * p->n, 1, 1, 2) ||
+  void* Qs = at<void>(ws, BL.qs);
+  void* dOs = at<void>(ws, BL.dos);
+  void* Ks = at<void>(ws, BL.ks);
+  void* Vs = at<void>(ws, BL.vs);
+  a.lse_sorted = at<float>(ws, BL.lse_s);
+  a.delta_sorted = at<float>(ws, BL.delta_s);
+  // tile maps over the sorted copies (group kernels) and the inputs (window kernels)
+  CUtensorMap qs3, dos3, ks3, vs3, q3, do3, k3, v3;
+  if (!make_map(&qs3, Qs, p->d, p->n, qplanes, 128, 3) || !make_map(&dos3, dOs, p->d, p->n, qplanes, 128, 3) ||
+      !make_map(&ks3, Ks, p->d, p->n, planes, 128, 3) || !make_map(&vs3, Vs, p->d, p->n, planes, 128, 3) ||
       !make_map(&q3, Q, p->d, p->n, qplanes, 128, 3) || !make_map(&do3, dO, p->d, p->n, qplanes, 128, 3) ||
       !make_map(&k3, K, p->d, p->n, planes, 128, 3) || !make_map(&v3, V, p->d, p->n, planes, 128, 3))
     return FOCUS_ERR_CUDA;
   cudaError_t e = launch_bwd_delta(a, p->dtype, st);
-  if (e == cudaSuccess) e = launch_attn_bwd_tc(a, &q2, &do2, &k2, &v2, &q3, &do3, &k3, &v3, idx->max_items, st);
+  if (e == cudaSuccess) e = launch_bwd_permute_q(a, Qs, dOs, at<float>(ws, BL.lse_s), at<float>(ws, BL.delta_s), st);
+  if (e == cudaSuccess)
+    e = launch_permute_kv_bf16(K, V, Ks, Vs, idx->perm, p->B, p->H_kv, p->n, p->n, 0, p->d, p->A, st);
+  if (e == cudaSuccess) e = launch_attn_bwd_tc(a, &qs3, &dos3, &ks3, &vs3, &q3, &do3, &k3, &v3, idx->max_items, st);
   return cuda_status(e);
 }
 

@@ -4,8 +4,9 @@
 // Matter", section 3.1), with every d-long product an MMA.
 //
 // Two kernels, each in a group form (far pairs, rows and keys in the index's
-// sorted order, reached by TMA row gathers) and a window form (natural order,
-// TMA tiles); one CTA per 128-row unit:
+// sorted order, read as TMA tiles from copies of Q, dO, K, V (and LSE, Delta)
+// sorted by the index once per call) and a window form (natural order, TMA
+// tiles); one CTA per 128-row unit:
 //   dQ   rows = 128 queries, streamed = 128-key tiles of the kept keys:
 //          S = Q K^T, dP = dO V^T               (SS, TMEM fp32)
 //          dS = P (dP - Delta), P = exp(S scale - LSE)   (CUDA cores -> TMEM bf16)
@@ -248,25 +249,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int issued = 0;
     if (ntot > 0) {
       // fixed operands: dQ -> (Q, dO) rows of the unit; dKV -> (K, V) rows
-      if (kGroup) {
-        if (lane == 0) mbar_expect_tx(fixed_full, 2 * Cfg::kTile);
-        __syncwarp();
-        const int first = a.perm[pn + U.row0];
-        int rows[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int rr = 4 * lane + j;
-          const int pos = rr < U.nrows ? a.perm[pn + U.row0 + rr] : first;
-          rows[j] = (kDq ? U.zq : U.zkv) * a.n + pos;
-        }
-#pragma unroll
-        for (int ch = 0; ch < kChunks; ++ch) {
-          tma_gather4(smem + Cfg::kF0 + ch * Cfg::kChunk + 4 * lane * 128, kDq ? &tm_q : &tm_k, fixed_full,
-                      ch * 64, rows[0], rows[1], rows[2], rows[3]);
-          tma_gather4(smem + Cfg::kF1 + ch * Cfg::kChunk + 4 * lane * 128, kDq ? &tm_do : &tm_v, fixed_full,
-                      ch * 64, rows[0], rows[1], rows[2], rows[3]);
-        }
-      } else if (lane == 0) {
+      // (group kinds: rows of the sorted copies, so one tile either way)
+      if (lane == 0) {
         mbar_expect_tx(fixed_full, 2 * Cfg::kTile);
 #pragma unroll
         for (int ch = 0; ch < kChunks; ++ch) {
@@ -285,28 +269,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int zq = U.b * a.H + U.h + hh;
         uint8_t* r0 = smem + Cfg::kR + sl * 2 * Cfg::kTile;
         uint8_t* r1 = r0 + Cfg::kTile;
-        if (kGroup) {
-          // dQ: key slots key0 + t*128 + rr of the prefix; dKV: query slots wlo + t*128 + rr
-          if (lane == 0) mbar_expect_tx(&ring_full[sl], 2 * Cfg::kTile);
-          __syncwarp();
-          const int base = kDq ? U.key0 : wlo;
-          const int lim = kDq ? U.key0 + U.nkeys : a.n;
-          const int first = a.perm[pn + base];
-          int rows[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int s = base + t * kT + 4 * lane + j;
-            const int pos = s < lim ? a.perm[pn + s] : first;
-            rows[j] = (kDq ? U.zkv : zq) * a.n + pos;
-          }
-#pragma unroll
-          for (int ch = 0; ch < kChunks; ++ch) {
-            tma_gather4(r0 + ch * Cfg::kChunk + 4 * lane * 128, kDq ? &tm_k : &tm_q, &ring_full[sl], ch * 64,
-                        rows[0], rows[1], rows[2], rows[3]);
-            tma_gather4(r1 + ch * Cfg::kChunk + 4 * lane * 128, kDq ? &tm_v : &tm_do, &ring_full[sl], ch * 64,
-                        rows[0], rows[1], rows[2], rows[3]);
-          }
-        } else if (lane == 0) {
+        // dQ: key slots (group) or tokens from key0 + t*128; dKV: query slots or
+        // tokens from wlo + t*128 (rows past a group's run are masked out)
+        if (lane == 0) {
           mbar_expect_tx(&ring_full[sl], 2 * Cfg::kTile);
           const int y = (kDq ? U.key0 : wlo) + t * kT;
 #pragma unroll
@@ -326,10 +291,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int q = wlo + t * kT + c;
             float l2 = 0.f, dl = 0.f;
             if (q < a.n) {
-              const int pos = kGroup ? a.perm[pn + q] : q;
-              const size_t qi = static_cast<size_t>(zq) * a.n + pos;
-              l2 = a.lse[qi] * kLog2e;
-              dl = a.delta[qi];
+              // group: the sorted copies are indexed by slot
+              const size_t qi = static_cast<size_t>(zq) * a.n + q;
+              l2 = (kGroup ? a.lse_sorted : a.lse)[qi] * kLog2e;
+              dl = (kGroup ? a.delta_sorted : a.delta)[qi];
             }
             cb[c] = l2;
             cb[128 + c] = dl;
@@ -544,6 +509,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Q, dO rows and the LSE, Delta of every query head in the order of its
+// assignment's index: dst[zq, s] = src[zq, perm_a[s]], a = the head's assignment.
+__global__ void __launch_bounds__(256) permute_q_kernel(BwdArgs a, __nv_bfloat16* Qs, __nv_bfloat16* dOs,
+                                                        float* lse_s, float* delta_s, long long total) {
+  const int vpr = a.d / 8;
+  for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < total;
+       e += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long row = e / vpr;
+    const int u = static_cast<int>(e % vpr);
+    const int s = static_cast<int>(row % a.n);
+    const long long zq = row / a.n;
+    const int h = static_cast<int>(zq % a.H);
+    const long long b = zq / a.H;
+    const long long p = b * a.A + (a.A == 1 ? 0 : (h * a.H_kv) / a.H);
+    const long long src = zq * a.n + __ldg(a.perm + p * a.n + s);
+    reinterpret_cast<uint4*>(Qs)[e] = __ldg(reinterpret_cast<const uint4*>(a.Q) + src * vpr + u);
+    reinterpret_cast<uint4*>(dOs)[e] = __ldg(reinterpret_cast<const uint4*>(a.dO) + src * vpr + u);
+    if (u == 0) {
+      lse_s[row] = a.lse[src];
+      delta_s[row] = a.delta[src];
+    }
+  }
+}
+
 template <int D>
 cudaError_t launch_d(const BwdArgs& a, const CUtensorMap* q2, const CUtensorMap* do2, const CUtensorMap* k2,
                      const CUtensorMap* v2, const CUtensorMap* q3, const CUtensorMap* do3, const CUtensorMap* k3,
@@ -583,6 +572,16 @@ cudaError_t launch_attn_bwd_tc(const BwdArgs& a, const CUtensorMap* q2, const CU
   if (a.d == 64) return launch_d<64>(a, q2, do2, k2, v2, q3, do3, k3, v3, max_items, st);
   if (a.d == 128) return launch_d<128>(a, q2, do2, k2, v2, q3, do3, k3, v3, max_items, st);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_bwd_permute_q(const BwdArgs& a, void* Qs, void* dOs, float* lse_s, float* delta_s,
+                                 cudaStream_t st) {
+  const long long total = static_cast<long long>(a.B) * a.H * a.n * (a.d / 8);
+  const long long want = (total + 255) / 256;
+  const int grid = static_cast<int>(want < 152LL * 16 ? want : 152LL * 16);
+  permute_q_kernel<<<grid, 256, 0, st>>>(a, static_cast<__nv_bfloat16*>(Qs), static_cast<__nv_bfloat16*>(dOs),
+                                         lse_s, delta_s, total);
+  return cudaGetLastError();
 }
 
 cudaError_t setup_bwd_tc_kernels() {

@@ -171,6 +171,7 @@ struct BwdArgs {
   int B, H, H_kv, n, d, A, groups, w;   // groups: K, the number of centroids
   float scale, scale_log2;
   int* err;                         // device error word (bounded waits)
+  const float *lse_sorted, *delta_sorted;  // bf16 path: LSE and Delta in each head's index order
 };
 cudaError_t launch_attn_bwd(const BwdArgs& a, int dtype, int max_items, cudaStream_t st);
 cudaError_t launch_bwd_delta(const BwdArgs& a, int dtype, cudaStream_t st);
@@ -183,6 +184,10 @@ cudaError_t launch_attn_bwd_tc(const BwdArgs& a, const CUtensorMap* q2, const CU
                                const CUtensorMap* do3, const CUtensorMap* k3, const CUtensorMap* v3,
                                int max_items, cudaStream_t st);
 cudaError_t setup_bwd_tc_kernels();
+// Q, dO rows and LSE, Delta of every query head sorted by its assignment's
+// index (for the group kernels' tile loads).
+cudaError_t launch_bwd_permute_q(const BwdArgs& a, void* Qs, void* dOs, float* lse_s, float* delta_s,
+                                 cudaStream_t st);
 cudaError_t launch_sinkhorn(const SinkhornLaunch& L, int iters, cudaStream_t st);
 
 }  // namespace focus
