@@ -17,6 +17,12 @@
  *   focus_assign        hidden states -> group id per token (top-1 centroid)
  *   focus_build_index   group ids -> (group, position) sorted index + work list
  *   focus_attention_fwd Q, K, V, index -> O over the kept pairs only
+ * Around it: focus_dense_causal_fwd (the dense comparator),
+ * focus_attention_two_call_fwd (the pages' two-call strategy, a comparator),
+ * focus_layer_fwd_host (the layer from host buffers), the top-k membership
+ * calls (*_topk, k = 2), the Sinkhorn soft assignment (focus_assign_scores,
+ * focus_sinkhorn_fwd), the backward (focus_attention_bwd) and
+ * focus_build_index_static (the index without a workspace).
  *
  * Conventions shared by every call
  *   - All tensor pointers are DEVICE pointers to row-major contiguous arrays,
