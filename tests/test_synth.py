@@ -1,4 +1,5 @@
 """Seeded input generators: determinism, dtype grid, shapes."""
+import pytest
 import numpy as np
 import torch
 
@@ -45,3 +46,32 @@ def test_redraw_changes_only_chosen_tokens():
     synth.redraw_hidden(wl, x, np.array([[0, 3], [0, 77]]), attempt=1)
     changed = np.any(x["h"] != h0, axis=2)
     assert changed[0, 3] and changed[0, 77] and changed.sum() == 2
+
+
+def test_topk_group_ids_are_distinct_seeded_and_shaped():
+    for kind in ("uniform", "zipf"):
+        g = synth.draw_group_ids_topk(5, 2, 3, 500, 6, 2, kind)
+        assert g.shape == (2, 3, 500, 2) and g.dtype == np.int32
+        assert np.all(g[..., 0] != g[..., 1])
+        assert g.min() >= 0 and g.max() < 6
+        assert np.array_equal(g, synth.draw_group_ids_topk(5, 2, 3, 500, 6, 2, kind))
+        assert not np.array_equal(g, synth.draw_group_ids_topk(6, 2, 3, 500, 6, 2, kind))
+    g3 = synth.draw_group_ids_topk(1, 1, 1, 200, 5, 3, "uniform")
+    assert all(len(set(r.tolist())) == 3 for r in g3[0, 0])
+
+
+def test_topk_group_id_kinds():
+    u = synth.draw_group_ids_topk(2, 1, 1, 60000, 4, 2, "uniform")
+    counts = np.bincount(u.ravel(), minlength=4)
+    assert np.all(np.abs(counts / counts.sum() - 0.25) < 0.01)          # balanced memberships
+    pairs = np.bincount((np.minimum(u[..., 0], u[..., 1]) * 4 + np.maximum(u[..., 0], u[..., 1])).ravel())
+    assert np.count_nonzero(pairs) == 6                                  # every pair of groups occurs
+    z = synth.draw_group_ids_topk(2, 1, 1, 60000, 8, 2, "zipf")
+    zc = np.bincount(z.ravel(), minlength=8)
+    assert zc[0] > zc[3] > zc[7]                                         # skewed toward low ids
+    b = synth.draw_group_ids_topk(3, 1, 2, 100, 5, 2, "both")
+    assert np.array_equal(np.sort(b, axis=-1), np.broadcast_to([0, 1], b.shape))
+    with pytest.raises(ValueError):
+        synth.draw_group_ids_topk(3, 1, 1, 10, 5, 3, "both")
+    with pytest.raises(ValueError):
+        synth.draw_group_ids_topk(3, 1, 1, 10, 2, 3, "uniform")
