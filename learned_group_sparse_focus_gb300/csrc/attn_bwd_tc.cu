@@ -534,8 +534,8 @@ __global__ void __launch_bounds__(256) permute_q_kernel(BwdArgs a, __nv_bfloat16
 }
 
 template <int D>
-cudaError_t launch_d(const BwdArgs& a, const CUtensorMap* q2, const CUtensorMap* do2, const CUtensorMap* k2,
-                     const CUtensorMap* v2, const CUtensorMap* q3, const CUtensorMap* do3, const CUtensorMap* k3,
+cudaError_t launch_d(const BwdArgs& a, const CUtensorMap* qs, const CUtensorMap* dos, const CUtensorMap* ks,
+                     const CUtensorMap* vs, const CUtensorMap* q3, const CUtensorMap* do3, const CUtensorMap* k3,
                      const CUtensorMap* v3, int max_items, cudaStream_t st) {
   using Cfg = BCfg<D>;
   const int hpa = a.A == 1 ? a.H : a.H / a.H_kv;
@@ -543,9 +543,9 @@ cudaError_t launch_d(const BwdArgs& a, const CUtensorMap* q2, const CUtensorMap*
   const long long q_units = static_cast<long long>(a.B) * a.H * ((a.n + kT - 1) / kT);
   const long long k_units = static_cast<long long>(a.B) * a.H_kv * ((a.n + kT - 1) / kT);
   if (g_units > 0)
-    bwd_tc_kernel<D, kDqGroup><<<static_cast<unsigned>(g_units), kThreads, Cfg::kSmem, st>>>(*q2, *do2, *k2, *v2, a);
+    bwd_tc_kernel<D, kDqGroup><<<static_cast<unsigned>(g_units), kThreads, Cfg::kSmem, st>>>(*qs, *dos, *ks, *vs, a);
   bwd_tc_kernel<D, kDqLocal><<<static_cast<unsigned>(q_units), kThreads, Cfg::kSmem, st>>>(*q3, *do3, *k3, *v3, a);
-  bwd_tc_kernel<D, kDkvGroup><<<static_cast<unsigned>(k_units), kThreads, Cfg::kSmem, st>>>(*q2, *do2, *k2, *v2, a);
+  bwd_tc_kernel<D, kDkvGroup><<<static_cast<unsigned>(k_units), kThreads, Cfg::kSmem, st>>>(*qs, *dos, *ks, *vs, a);
   bwd_tc_kernel<D, kDkvLocal><<<static_cast<unsigned>(k_units), kThreads, Cfg::kSmem, st>>>(*q3, *do3, *k3, *v3, a);
   return cudaGetLastError();
 }
@@ -565,12 +565,12 @@ cudaError_t set_smem_d() {
 
 }  // namespace
 
-cudaError_t launch_attn_bwd_tc(const BwdArgs& a, const CUtensorMap* q2, const CUtensorMap* do2,
-                               const CUtensorMap* k2, const CUtensorMap* v2, const CUtensorMap* q3,
+cudaError_t launch_attn_bwd_tc(const BwdArgs& a, const CUtensorMap* qs, const CUtensorMap* dos,
+                               const CUtensorMap* ks, const CUtensorMap* vs, const CUtensorMap* q3,
                                const CUtensorMap* do3, const CUtensorMap* k3, const CUtensorMap* v3,
                                int max_items, cudaStream_t st) {
-  if (a.d == 64) return launch_d<64>(a, q2, do2, k2, v2, q3, do3, k3, v3, max_items, st);
-  if (a.d == 128) return launch_d<128>(a, q2, do2, k2, v2, q3, do3, k3, v3, max_items, st);
+  if (a.d == 64) return launch_d<64>(a, qs, dos, ks, vs, q3, do3, k3, v3, max_items, st);
+  if (a.d == 128) return launch_d<128>(a, qs, dos, ks, vs, q3, do3, k3, v3, max_items, st);
   return cudaErrorInvalidValue;
 }
 

@@ -177,10 +177,11 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, int dtype, int max_items, cudaStre
 cudaError_t launch_bwd_delta(const BwdArgs& a, int dtype, cudaStream_t st);
 
 // attn_bwd_tc.cu: the same backward for bf16 on the tcgen05 tensor cores (after
-// launch_bwd_delta).  *2: {d, planes*n} one-row-box maps for row gathers; *3:
-// {d, n, planes} 128-row tile maps.
-cudaError_t launch_attn_bwd_tc(const BwdArgs& a, const CUtensorMap* q2, const CUtensorMap* do2,
-                               const CUtensorMap* k2, const CUtensorMap* v2, const CUtensorMap* q3,
+// launch_bwd_delta and the index-order copies).  All maps {d, n, planes} with
+// 128-row boxes: *s over the index-ordered copies (group kernels), *3 over the
+// inputs (window kernels).
+cudaError_t launch_attn_bwd_tc(const BwdArgs& a, const CUtensorMap* qs, const CUtensorMap* dos,
+                               const CUtensorMap* ks, const CUtensorMap* vs, const CUtensorMap* q3,
                                const CUtensorMap* do3, const CUtensorMap* k3, const CUtensorMap* v3,
                                int max_items, cudaStream_t st);
 cudaError_t setup_bwd_tc_kernels();
