@@ -701,7 +701,7 @@ def run_ours_sinkhorn(args, wl, world, rank, local):
         "gpu_launches": (1 + 3 * T) * args.steps,
         "clocks": clk.summary(),
     }
-    if not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline:
         import oracle.focus_ref as ref
         rows = min(wl.n, 8192)
         t0 = time.perf_counter()
@@ -712,7 +712,8 @@ def run_ours_sinkhorn(args, wl, world, rank, local):
         line["cpu_baseline"] = {"value": ab / sec / 1e9, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
                                 "sample": f"oracle fp64 scores + {T} Sinkhorn rounds on the first {rows} tokens "
                                           f"(the same bytes-per-round accounting)", "seconds": sec}
-    print(json.dumps(line), flush=True)
+    if rank == 0:       # one replica per process; rank 0 reports its own
+        print(json.dumps(line), flush=True)
 
 
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12     # CUDA-core fp32 FMA peak
@@ -783,7 +784,7 @@ def run_ours_backward(args, wl, world, rank, local):
         "clocks": clk.summary(),
         "ms_note": "bf16: delta + 4 tcgen05 kernels (dQ far, dQ window, dK/dV far, dK/dV window)",
     }
-    if not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline:
         import oracle.focus_ref as ref
         nb = min(wl.n, 1024)
         Hs = min(wl.H, 2 * (wl.H // wl.H_kv))
@@ -802,7 +803,8 @@ def run_ours_backward(args, wl, world, rank, local):
                                 "kind": "oracle",
                                 "sample": f"oracle fp64 backward on the first {nb} tokens of {Hs} query heads",
                                 "seconds": sec}
-    print(json.dumps(line), flush=True)
+    if rank == 0:       # one replica per process; rank 0 reports its own
+        print(json.dumps(line), flush=True)
 
 
 def main():
