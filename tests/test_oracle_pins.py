@@ -496,6 +496,43 @@ def test_topk_bruteforce_small(n, w, K):
     np.testing.assert_allclose(L[0, 0], Lb, atol=1e-12)
 
 
+def test_topk_inclusion_exclusion_merge_equals_union():
+    # The far keys of token i with groups {a, b}: far members of a, of b, and
+    # of the pair {a, b} (in both).  With w = exp(LSE - M):
+    #   O = (w_a O_a + w_b O_b - w_ab O_ab) / (w_a + w_b - w_ab)
+    # equals the softmax over the union of the far keys (the GPU merge).
+    rng = np.random.default_rng(49)
+    n, d, w, K = 160, 6, 5, 4
+    Q, Kt, V = (rng.standard_normal((n, d)) for _ in range(3))
+    G = np.stack([rng.permutation(K)[:2] for _ in range(n)]).astype(np.int32)
+    rows = np.arange(n)
+    i = rows[:, None]
+    j = rows[None, :]
+    far = j <= i - w
+    in_a = (G[:, 0][:, None] == G[None, :, 0]) | (G[:, 0][:, None] == G[None, :, 1])
+    in_b = (G[:, 1][:, None] == G[None, :, 0]) | (G[:, 1][:, None] == G[None, :, 1])
+    Oa, La = ref.attention_masked_rows(Q, Kt, V, far & in_a, rows, 0.4)
+    Ob, Lb = ref.attention_masked_rows(Q, Kt, V, far & in_b, rows, 0.4)
+    Oab, Lab = ref.attention_masked_rows(Q, Kt, V, far & in_a & in_b, rows, 0.4)
+    Ou, Lu = ref.attention_masked_rows(Q, Kt, V, far & (in_a | in_b), rows, 0.4)
+    has = np.isfinite(Lu)
+    assert has.sum() > n // 2
+    M = np.maximum.reduce([La, Lb, np.where(np.isfinite(Lab), Lab, -np.inf)])
+    with np.errstate(invalid="ignore", divide="ignore"):      # rows with no far key: excluded below
+        wa, wb = np.exp(La - M), np.exp(Lb - M)
+        wab = np.where(np.isfinite(Lab), np.exp(Lab - M), 0.0)
+        den = wa + wb - wab
+        Om = (wa[:, None] * np.nan_to_num(Oa) + wb[:, None] * np.nan_to_num(Ob)
+              - wab[:, None] * np.nan_to_num(Oab)) / den[:, None]
+    np.testing.assert_allclose(Om[has], Ou[has], atol=1e-12)
+    np.testing.assert_allclose(M[has] + np.log(den[has]), Lu[has], atol=1e-12)
+    # the denominator never cancels: it is at least the larger entry weight
+    assert np.all(den[has] >= np.maximum(wa, wb)[has] - 1e-15)
+    # and the union is the top-2 keep rule's far part
+    Mk = ref.keep_mask_rows_topk(G, w, rows)
+    assert np.array_equal(Mk & far, far & (in_a | in_b))
+
+
 def test_topk_pins_catch_planted_mistakes():
     """Plausible slips in the top-k rule each break the hand-worked example."""
     gd, G = _golden_top2()
