@@ -151,16 +151,16 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def traffic_record(kernel: str):
-    """DRAM bytes per launch from a committed ncu summary, if the kernel source
-    is unchanged since it was captured; else None."""
+def traffic_record(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was captured
+    on this workload and the kernel source is unchanged since; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f).get(kernel)
     except (OSError, ValueError):
         return None
-    if not rec:
+    if not rec or rec.get("workload") != workload:
         return None
     src = os.path.join(ROOT, "learned_group_sparse_focus_gb300", "csrc", rec["source"])
     try:
@@ -423,7 +423,7 @@ def run_ours(args, wl, world, rank, local):
     dom = "group_pass" if t["group_pass"] >= t["local_pass"] else "local_pass"
     dom_flops = f_group if dom == "group_pass" else f_local
     achieved = dom_flops / (t[dom] * 1e-3) / 1e12
-    tr = traffic_record("attn_tc_" + dom)
+    tr = traffic_record("attn_tc_" + dom, wl.name)
     value = job_tflops(world, f_attn, t_step)
     es = 2 if wl.dtype == "bf16" else 4
     assign_bytes = (wl.B * wl.n * wl.D + wl.A * wl.d_g * wl.D + wl.A * wl.K * wl.d_g) * es + wl.B * wl.A * wl.n * 4

@@ -48,3 +48,12 @@ def test_topk_oracle_sample_counts_kept_pairs():
     rows = np.sort(np.random.default_rng(3).choice(wl.n, size=10, replace=False))
     kept = int(ref.keep_mask_rows_topk(gid[0, 0], wl.w, rows).sum())
     assert flops == 4 * wl.d * kept
+
+
+def test_traffic_record_only_for_its_workload_and_source():
+    sys.path.insert(0, ROOT)
+    import bench
+    rec = bench.traffic_record("attn_tc_group_pass", "gqa_32k")
+    assert rec is not None and rec["bytes_per_launch"] > 0
+    assert bench.traffic_record("attn_tc_group_pass", "llama7b_8k") is None
+    assert bench.traffic_record("no_such_kernel", "gqa_32k") is None
