@@ -434,7 +434,9 @@ def build_index_topk(gid, K: int, w: int):
 
 def keep_mask_rows_topk(G, w: int, rows):
     """Top-k keep rule for query rows `rows`: j <= i and (i - j < w or the
-    group sets of i and j intersect).  G [n, k]."""
+    group sets of i and j intersect).  G [n, k].  [FocusJA] 2.2 (a far pair
+    is computed only when the tokens share a group; with top-k membership a
+    token is in k groups) and 3.3; [FocusKO] 2.3."""
     G = np.asarray(G)
     rows = np.asarray(rows, dtype=np.int64)
     n, k = G.shape
@@ -449,7 +451,9 @@ def keep_mask_rows_topk(G, w: int, rows):
 
 def attention_rows_topk(Q, K, V, gid, w: int, scale: float, rows, A: int, row_block: int = 256):
     """Top-k Focus attention for selected query rows of every (b, h):
-    Q [B,H,n,d], K/V [B,H_kv,n,d], gid [B,A,n,k].  O [B,H,R,d], LSE [B,H,R]."""
+    Q [B,H,n,d], K/V [B,H_kv,n,d], gid [B,A,n,k].  O [B,H,R,d], LSE [B,H,R].
+    Exact softmax over the top-k keep rule's pairs, each pair once ([FocusKO]
+    2.1, 2.3; [FocusJA] 2.2)."""
     B, H, n, d = Q.shape
     H_kv = K.shape[1]
     rows = np.asarray(rows, dtype=np.int64)
@@ -470,7 +474,9 @@ def attention_rows_topk(Q, K, V, gid, w: int, scale: float, rows, A: int, row_bl
 
 def attention_bruteforce_topk(q, k, v, G, w: int, scale: float):
     """Scalar loops for one head: kept set per row from the window and set
-    intersection, math.fsum softmax.  q, k, v [n, d], G [n, kk] -> O, LSE."""
+    intersection, math.fsum softmax.  q, k, v [n, d], G [n, kk] -> O, LSE.
+    The same rule as keep_mask_rows_topk built a different way (lists, not a
+    mask), for the brute-force pin ([FocusJA] 2.2; [FocusKO] 2.1)."""
     n, d = q.shape
     O = np.zeros((n, d))
     L = np.zeros(n)
@@ -530,7 +536,8 @@ def sinkhorn(S, T: int, tau: float = 1.0):
 
 def attention_backward(Q, K, V, gid, w: int, scale: float, A: int, dO):
     """Gradients of O = attention(Q, K, V) (the top-1 keep rule) for a fixed
-    upstream gradient dO.  Q, dO [B, H, n, d]; K, V [B, H_kv, n, d];
+    upstream gradient dO: the exact softmax over the kept pairs ([FocusKO]
+    2.1) is what a retrofitted model is fine-tuned through ([FocusJA] 3.1).  Q, dO [B, H, n, d]; K, V [B, H_kv, n, d];
     gid [B, A, n].  Returns dQ [B, H, n, d], dK, dV [B, H_kv, n, d] (fp64).
 
     Per (b, h), with M the keep mask and P = softmax over kept keys of
@@ -564,7 +571,8 @@ def attention_backward(Q, K, V, gid, w: int, scale: float, A: int, dO):
 def attention_backward_dq_rows(Q, K, V, gid, w: int, scale: float, A: int, dO, rows):
     """dQ of attention_backward for selected query rows only (each row's dQ
     needs only its own kept keys): dQ_i = scale sum_j P_ij (dO_i . v_j - D_i) k_j.
-    Returns [B, H, R, d]."""
+    Returns [B, H, R, d].  The same definition as attention_backward
+    ([FocusKO] 2.1), restricted to rows."""
     B, H, n, d = Q.shape
     H_kv = K.shape[1]
     rows = np.asarray(rows, dtype=np.int64)
