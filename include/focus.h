@@ -161,7 +161,7 @@ FOCUS_API focus_status_t focus_build_index(const focus_params_t* p, const int32_
  * allocate device memory when they build the index (a process whose device
  * footprint is fixed at start-up, or one that wants the index without the
  * attention workspace).  Same operation and bit-identical outputs as
- * focus_build_index ("Focus: Learning Which Attention Pairs Matter" 2.2).
+ * focus_build_index.
  *   gid  [B, A, n] int32 device input, 16-byte aligned.
  *   idx  host struct, in/out.  On entry counts, offsets, perm, rank,
  *        farlen_tok, farlen_slot, items, order and n_items are caller-owned

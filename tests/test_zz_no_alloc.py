@@ -1,9 +1,11 @@
 """focus_build_index_static: the index built with no workspace and no
-allocation, against focus_build_index on the same inputs.
+allocation, against the CPU oracle's index and against focus_build_index on
+the same inputs.
 
 Every output is integer work, so the comparison is bit for bit (tolerance 0).
 The GPU cases make two calls in a row (different group ids, then the first
-ones again) so that leftovers in the shared fixed scratch would show.  The
+ones again) so that leftovers in the shared fixed scratch would show; one case
+needs 99% of the fixed scratch, so its far end is written and read too.  The
 size and argument checks run before anything touches the device and are
 tested on the CPU.
 """
@@ -13,6 +15,7 @@ import os
 import numpy as np
 import pytest
 
+import oracle.focus_ref as ref
 from learned_group_sparse_focus_gb300 import synth
 
 FOCUS_ERR_INVALID_ARG = 1
@@ -113,6 +116,25 @@ def _same(a, b):
         np.testing.assert_array_equal(a[k], b[k], err_msg=k)
 
 
+def _oracle(fz, gid, K, w):
+    """The CPU oracle's index, work list and longest-first order for gid."""
+    want = ref.build_index(gid, K, max(w, 1))
+    items = ref.work_items(want, fz.TILE_M)
+    out = {k: want[k] for k in ("counts", "offsets", "perm", "rank", "farlen_tok", "farlen_slot")}
+    out["items"] = items
+    out["order"] = ref.lpt_order(items, fz.TILE_N)
+    out["n_items"] = len(items)
+    return out
+
+
+def _same_as_oracle(got, want):
+    assert got["n_items"] == want["n_items"]
+    for k in ("counts", "offsets", "perm", "rank", "farlen_tok", "farlen_slot"):
+        np.testing.assert_array_equal(got[k].reshape(want[k].shape), want[k], err_msg=k)
+    np.testing.assert_array_equal(got["items"][:, :7], want["items"], err_msg="items")
+    np.testing.assert_array_equal(got["order"], want["order"], err_msg="order")
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("wl_name,kind", [("llama7b_8k", "zipf"), ("llama70b_64k", "uniform"),
                                           ("gpt2_small_1k", "blocks")])
@@ -126,11 +148,40 @@ def test_static_index_matches_workspace_index_twice(fz, wl_name, kind):
     g2 = torch.from_numpy(synth.draw_group_ids(wl.seed + 7, wl.B, wl.A, wl.n, wl.K, "uniform")).cuda()
     _, _, want1 = _regular(fz, p, g1)
     _, _, want2 = _regular(fz, p, g2)
-    for gid, want in ((g1, want1), (g2, want2), (g1, want1)):
+    ora1 = _oracle(fz, g1.cpu().numpy(), wl.K, wl.w)
+    ora2 = _oracle(fz, g2.cpu().numpy(), wl.K, wl.w)
+    for gid, want, ora in ((g1, want1, ora1), (g2, want2, ora2), (g1, want1, ora1)):
         idx, got = _static(fz, p, gid, bufs)
         _same(got, want)
+        _same_as_oracle(got, ora)
         assert idx.max_items == bufs["order"].numel()
         assert idx.w_eff == max(wl.w, 1)
+
+
+def test_static_index_near_limit_case_fits(fz):
+    # the GPU case below needs 99% of the fixed scratch; ten more groups do not fit
+    p = fz.make_params(B=1, H=1, H_kv=1, n=1 << 18, d=64, D=64, d_g=32, K=1000, A=1, w=64)
+    q = fz.make_params(B=1, H=1, H_kv=1, n=1 << 18, d=64, D=64, d_g=32, K=1010, A=1, w=64)
+    assert 0.99 * SCRATCH_BYTES <= _needed(p)[0] <= SCRATCH_BYTES < _needed(q)[0]
+    assert _call_raw(fz, q, _fake_index(fz, _needed(q)[1])) == FOCUS_ERR_WORKSPACE
+
+
+@pytest.mark.gpu
+def test_static_index_near_the_scratch_limit_twice(fz):
+    """n = 2^18 tokens in K = 1000 groups: the histograms, tile bases and item
+    costs fill 1,040,384 of the 1,048,576 scratch bytes."""
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    n, K, w = 1 << 18, 1000, 64
+    p = fz.make_params(B=1, H=1, H_kv=1, n=n, d=64, D=64, d_g=32, K=K, A=1, w=w)
+    assert _needed(p)[0] >= 0.99 * SCRATCH_BYTES
+    bufs = fz.index_buffers(p)
+    g1 = synth.draw_group_ids(41, 1, 1, n, K, "uniform")
+    g2 = synth.draw_group_ids(42, 1, 1, n, K, "zipf")
+    ora1, ora2 = _oracle(fz, g1, K, w), _oracle(fz, g2, K, w)
+    for g, ora in ((g1, ora1), (g2, ora2), (g1, ora1)):
+        _, got = _static(fz, p, torch.from_numpy(g).cuda(), bufs)
+        _same_as_oracle(got, ora)
 
 
 @pytest.mark.gpu
