@@ -378,7 +378,7 @@ focus_status_t focus_workspace_init(void* ws, void* stream) {
 static focus_status_t assign_impl(const focus_params_t* p, int k, const void* h, const void* W,
                                   const void* C, int32_t* gid, int* err, void* stream) {
   if (focus_status_t s = ensure_setup()) return s;
-  AssignLaunch al{h, W, C, gid, p->B, p->n, p->D, p->d_g, p->K, p->A, k, err};
+  AssignLaunch al{h, W, C, gid, p->B, p->n, p->D, p->d_g, p->K, p->A, k, err, nullptr, sm_count()};
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (p->dtype == FOCUS_F32) {
     if (!(p->d_g == 16 || p->d_g == 32 || p->d_g == 64 || p->d_g == 128)) return FOCUS_ERR_UNSUPPORTED;
@@ -861,7 +861,7 @@ focus_status_t focus_assign_scores(const focus_params_t* p, const void* h, const
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return FOCUS_ERR_INVALID_ARG;
   if (ws_bytes < focus_sinkhorn_workspace_bytes(p)) return FOCUS_ERR_WORKSPACE;
   if (focus_status_t s = ensure_setup()) return s;
-  AssignLaunch al{h, W, C, nullptr, p->B, p->n, p->D, p->d_g, p->K, p->A, 1, at<int>(ws, 0), S};
+  AssignLaunch al{h, W, C, nullptr, p->B, p->n, p->D, p->d_g, p->K, p->A, 1, at<int>(ws, 0), S, sm_count()};
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (p->dtype == FOCUS_F32) {
     if (!(p->d_g == 16 || p->d_g == 32 || p->d_g == 64 || p->d_g == 128)) return FOCUS_ERR_UNSUPPORTED;

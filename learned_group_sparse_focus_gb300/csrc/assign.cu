@@ -9,9 +9,13 @@
 //   g = the k largest s_k, best first, the lower k first among equal scores.
 //
 // bf16: the projection is a [128 tokens x A*d_g] tile of h W^T on the
-// tcgen05 tensor cores (TMA-fed 4..6-stage pipeline, fp32 accumulator in
-// TMEM); the epilogue reads each token's row of p from TMEM and scores the
-// centroids with fp32 FMAs, so p is never rounded below fp32.
+// tcgen05 tensor cores (TMA-fed pipeline, fp32 accumulator in TMEM); the
+// epilogue reads each token's row of p from TMEM and scores the centroids with
+// fp32 FMAs, so p is never rounded below fp32.  Up to 256 projection columns
+// the kernel is persistent: one CTA per SM streams its 128-token tiles of h
+// through an 8-stage TMA ring into double-buffered TMEM accumulators while
+// four epilogue warps score the previous tile; 512 columns (eight 64-wide
+// assignments) use one CTA per tile.
 // fp32: one thread per token on the CUDA cores.
 // With kScores the kernels write every score s_k (fp32, [B, A, n, K]) instead
 // of the top-k ids: the input of the Sinkhorn soft assignment.
@@ -268,6 +272,237 @@ __global__ void __launch_bounds__(128, AssignCfg<NALLOC>::kMinBlocks) assign_tc_
   }
 }
 
+// ------------------------------------------------ bf16 tcgen05, persistent ---
+// One CTA per SM walks tiles blockIdx.x, blockIdx.x + gridDim.x, ...  Warp 0
+// issues the TMA loads of every (tile, k-step) into a kStages ring, warp 1 the
+// MMAs into TMEM buffer (tile index & 1), and warps 2-5 (one per TMEM lane
+// quadrant) score a tile once its accumulator is complete, releasing the
+// buffer as soon as they have read it.  The centroids are read from global
+// memory by every lane at the same address (L1 broadcasts).
+constexpr int kStreamThreads = 192;
+
+template <int NALLOC>
+struct StreamCfg {
+  static constexpr int kStageA = kBM * kBK * 2;            // 16 KB of h
+  static constexpr int kStageB = NALLOC * kBK * 2;         // <= 32 KB of W
+  static constexpr int kStage = kStageA + kStageB;
+  static constexpr int kStages = (200 * 1024 / kStage) < 8 ? (200 * 1024 / kStage) : 8;
+  static constexpr int kSmem = kStages * kStage + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int kTmemCols = 2 * NALLOC;              // two accumulators
+};
+
+// s += p[0..DG) . c (bf16 centroid row, 16-byte aligned), in order j = 0, 1, ...
+template <int DG>
+__device__ __forceinline__ void score4(const float (&p)[128], const __nv_bfloat16* c0, int stride, float (&sc)[4]) {
+#pragma unroll
+  for (int j = 0; j < DG; j += 8) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(c0 + q * stride + j));
+      const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        sc[q] = fmaf(p[j + 2 * e], __uint_as_float(u[e] << 16), sc[q]);
+        sc[q] = fmaf(p[j + 2 * e + 1], __uint_as_float(u[e] & 0xffff0000u), sc[q]);
+      }
+    }
+  }
+}
+
+template <int DG>
+__device__ __forceinline__ float score1(const float (&p)[128], const __nv_bfloat16* c) {
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < DG; j += 8) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(c + j));
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      s = fmaf(p[j + 2 * e], __uint_as_float(u[e] << 16), s);
+      s = fmaf(p[j + 2 * e + 1], __uint_as_float(u[e] & 0xffff0000u), s);
+    }
+  }
+  return s;
+}
+
+template <int NALLOC, int DG, bool kScores>
+__global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
+    const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
+    const __nv_bfloat16* __restrict__ C, int32_t* __restrict__ gid, float* __restrict__ scores,
+    int B, int n, int D, int K, int A, int topk, int* err) {
+  using Cfg = StreamCfg<NALLOC>;
+  constexpr int S = Cfg::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * Cfg::kStage);
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;      // [2] accumulator complete
+  uint64_t* tfree = tfull + 2;      // [2] accumulator read out (4 epilogue warps)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfree + 2);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = warp_id(), lane = lane_id();
+  const int ncol = A * DG;
+  const int ntiles = (B * n + kBM - 1) / kBM;
+  const int nk = (D + kBK - 1) / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tfree[b], 4);
+    }
+    *abort = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tm_h);
+    prefetch_tmap(&tm_w);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, Cfg::kTmemCols);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint32_t bytes = Cfg::kStageA + ncol * kBK * 2;
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % S, u = it / S;
+          if (u > 0 && !mbar_wait_nap(&empty[s], (u - 1) & 1, abort, err)) { ok = false; break; }
+          uint8_t* sa = smem + s * Cfg::kStage;
+          mbar_expect_tx(&full[s], bytes);
+          tma_load_2d(sa, &tm_h, &full[s], kb * kBK, tile * kBM);
+          tma_load_2d(sa + Cfg::kStageA, &tm_w, &full[s], kb * kBK, 0);
+        }
+      }
+      if (*abort || !ok) {
+        // let copies already in flight land before the CTA exits
+        for (int j = max(0, it - S); j < it; ++j) {
+          const unsigned long long t0 = global_ns();
+          while (!mbar_try_wait(&full[j % S], (j / S) & 1) && global_ns() - t0 < kWaitTimeoutNs) {}
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idn = idesc_bf16_f32(128, NALLOC, false, false);
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x, i = 0; tile < ntiles && ok; tile += gridDim.x, ++i) {
+        const int buf = i & 1;
+        if (i >= 2 && !mbar_wait_nap(&tfree[buf], ((i >> 1) - 1) & 1, abort, err)) break;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % S, u = it / S;
+          if (!mbar_wait_nap(&full[s], u & 1, abort, err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + s * Cfg::kStage);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            mma_ss(tmem + buf * NALLOC, sw128_desc(sa + kk * 32, 16, 1024),
+                   sw128_desc(sa + Cfg::kStageA + kk * 32, 16, 1024), idn, (kb | kk) != 0);
+          mma_commit(&empty[s]);
+        }
+        if (ok) mma_commit(&tfull[buf]);
+      }
+    }
+  } else {
+    // epilogue: warps 2-5 read TMEM lane quadrants 2, 3, 0, 1
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    for (int tile = blockIdx.x, i = 0; tile < ntiles; tile += gridDim.x, ++i) {
+      const int buf = i & 1;
+      if (!mbar_wait(&tfull[buf], (i >> 1) & 1, abort, err)) break;
+      tc_fence_after();
+      const int tok = tile * kBM + row;
+      const bool keep = tok < B * n;
+      const int b = keep ? tok / n : 0, ti = keep ? tok % n : 0;
+      for (int a = 0; a < A; ++a) {
+        float p[128];
+#pragma unroll
+        for (int c = 0; c < DG; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_base + buf * NALLOC + a * DG + c, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) p[c + j] = __uint_as_float(r[j]);
+        }
+        if (a == A - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tfree[buf]);   // the accumulator may take tile i + 2
+        }
+        const __nv_bfloat16* Ca = C + static_cast<size_t>(a) * K * DG;
+        float* srow = kScores && keep ? scores + ((static_cast<size_t>(b) * A + a) * n + ti) * K : nullptr;
+        Top2 t;
+        int k = 0;
+        for (; k + 4 <= K; k += 4) {
+          float sc[4] = {0.f, 0.f, 0.f, 0.f};
+          score4<DG>(p, Ca + static_cast<size_t>(k) * DG, DG, sc);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (kScores) {
+              if (srow) srow[k + q] = sc[q];
+            } else {
+              t.push(k + q, sc[q]);
+            }
+          }
+        }
+        for (; k < K; ++k) {
+          const float sk = score1<DG>(p, Ca + static_cast<size_t>(k) * DG);
+          if (kScores) {
+            if (srow) srow[k] = sk;
+          } else {
+            t.push(k, sk);
+          }
+        }
+        if (!kScores && keep) {
+          int32_t* out = gid + ((static_cast<size_t>(b) * A + a) * n + ti) * topk;
+          out[0] = t.b1;
+          if (topk == 2) out[1] = t.b2;
+        }
+      }
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Cfg::kTmemCols);
+  }
+}
+
+template <int NALLOC, int DG>
+cudaError_t launch_stream(const AssignLaunch& L, const CUtensorMap* tm_h, const CUtensorMap* tm_w,
+                          cudaStream_t st) {
+  using Cfg = StreamCfg<NALLOC>;
+  const int ntiles = (L.B * L.n + kBM - 1) / kBM;
+  const int grid = ntiles < L.num_sms ? ntiles : L.num_sms;
+  const __nv_bfloat16* C = static_cast<const __nv_bfloat16*>(L.C);
+  if (L.scores)
+    assign_stream_kernel<NALLOC, DG, true><<<grid, kStreamThreads, Cfg::kSmem, st>>>(
+        *tm_h, *tm_w, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk, L.err);
+  else
+    assign_stream_kernel<NALLOC, DG, false><<<grid, kStreamThreads, Cfg::kSmem, st>>>(
+        *tm_h, *tm_w, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk, L.err);
+  return cudaGetLastError();
+}
+
+template <int NALLOC>
+cudaError_t launch_stream_dg(const AssignLaunch& L, const CUtensorMap* tm_h, const CUtensorMap* tm_w,
+                             cudaStream_t st) {
+  if (L.d_g == 32) return launch_stream<NALLOC, 32>(L, tm_h, tm_w, st);
+  if (L.d_g == 64) return launch_stream<NALLOC, 64>(L, tm_h, tm_w, st);
+  if (L.d_g == 128) return launch_stream<NALLOC, 128>(L, tm_h, tm_w, st);
+  return cudaErrorInvalidValue;
+}
+
 template <int NALLOC>
 cudaError_t launch_tc(const AssignLaunch& L, const CUtensorMap* tm_h, const CUtensorMap* tm_w,
                       cudaStream_t st) {
@@ -314,7 +549,12 @@ cudaError_t launch_assign_f32(const AssignLaunch& L, cudaStream_t st) {
 
 cudaError_t launch_assign_bf16(const AssignLaunch& L, const CUtensorMap* tm_h,
                                const CUtensorMap* tm_w, cudaStream_t st) {
+  // the persistent kernel loads W in one box per stage: ncol is its exact width
   const int ncol = L.A * L.d_g;
+  if (ncol == 32) return launch_stream_dg<32>(L, tm_h, tm_w, st);
+  if (ncol == 64) return launch_stream_dg<64>(L, tm_h, tm_w, st);
+  if (ncol == 128) return launch_stream_dg<128>(L, tm_h, tm_w, st);
+  if (ncol == 256) return launch_stream_dg<256>(L, tm_h, tm_w, st);
   if (ncol <= 32) return launch_tc<32>(L, tm_h, tm_w, st);
   if (ncol <= 64) return launch_tc<64>(L, tm_h, tm_w, st);
   if (ncol <= 128) return launch_tc<128>(L, tm_h, tm_w, st);
@@ -338,6 +578,23 @@ cudaError_t setup_assign_kernels() {
   FOCUS_SET_SMEM(256)
   FOCUS_SET_SMEM(512)
 #undef FOCUS_SET_SMEM
+#define FOCUS_SET_SMEM2(N, G)                                                                       \
+  e = cudaFuncSetAttribute(assign_stream_kernel<N, G, false>,                                       \
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, StreamCfg<N>::kSmem);       \
+  if (e != cudaSuccess) return e;                                                                  \
+  e = cudaFuncSetAttribute(assign_stream_kernel<N, G, true>,                                        \
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, StreamCfg<N>::kSmem);       \
+  if (e != cudaSuccess) return e;
+  FOCUS_SET_SMEM2(32, 32)
+  FOCUS_SET_SMEM2(64, 32)
+  FOCUS_SET_SMEM2(64, 64)
+  FOCUS_SET_SMEM2(128, 32)
+  FOCUS_SET_SMEM2(128, 64)
+  FOCUS_SET_SMEM2(128, 128)
+  FOCUS_SET_SMEM2(256, 32)
+  FOCUS_SET_SMEM2(256, 64)
+  FOCUS_SET_SMEM2(256, 128)
+#undef FOCUS_SET_SMEM2
   return cudaSuccess;
 }
 

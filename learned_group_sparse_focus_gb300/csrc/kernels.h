@@ -53,6 +53,7 @@ struct AssignLaunch {
   int topk;        // 1 or 2 ids per token, best first
   int* err;
   float* scores;   // non-null: write every score [B, A, n, K] (fp32) instead of ids
+  int num_sms;     // SMs of the device (persistent grid)
 };
 
 // Everything the attention kernels read besides the K/V tensor maps.
