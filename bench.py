@@ -164,10 +164,10 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def traffic_record(kernel: str, workload: str):
+def traffic_record(kernel: str, workload: str, path: str | None = None):
     """DRAM bytes per launch from a committed ncu summary, if it was captured
     on this workload and the kernel source is unchanged since; else None."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    path = path or os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f).get(kernel)

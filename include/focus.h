@@ -218,6 +218,18 @@ FOCUS_API focus_status_t focus_dense_causal_fwd(const focus_params_t* p, const v
                                       const void* V, void* O, float* lse_opt, void* ws,
                                       size_t ws_bytes, void* stream);
 
+/* Test hook for the device-side failure path; not part of the method.  Runs
+ * the bf16 dense causal kernel of focus_dense_causal_fwd with every bounded
+ * wait limited to wait_ns nanoseconds (1 <= wait_ns <= 10^9) and with its Q
+ * load warp withholding the first Q tile, so the first S product's wait runs
+ * out: the kernel raises its abort flag, lets the copies it issued land, frees
+ * TMEM and exits.  focus_check_errors(ws) then reports FOCUS_ERR_TIMEOUT (and
+ * clears it); O holds no result.  Arguments, layouts and the workspace as
+ * focus_dense_causal_fwd; bf16 only (FOCUS_ERR_UNSUPPORTED otherwise). */
+FOCUS_API focus_status_t focus_test_attention_wait_limit(const focus_params_t* p, const void* Q,
+                                                 const void* K, const void* V, void* O, void* ws,
+                                                 size_t ws_bytes, uint64_t wait_ns, void* stream);
+
 /* The two-call comparator: the same operation and tensors as
  * focus_attention_fwd, run the way the pages run it ("Why Attend to
  * Everything? Focus is the Key" 2.3; "Focus: Learning Which Attention Pairs

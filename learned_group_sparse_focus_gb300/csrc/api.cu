@@ -170,6 +170,8 @@ AttnArgs attn_args(const focus_params_t* p, const void* Q, const void* K, const 
   a.kshift = 0;
   a.scale_log2 = p->scale * 1.4426950408889634f;
   a.err = at<int>(ws, L.err);
+  a.wait_ns = kWaitLimitNs;
+  a.hold_first_q = 0;
   return a;
 }
 
@@ -537,6 +539,28 @@ focus_status_t focus_dense_causal_fwd(const focus_params_t* p, const void* Q, co
   AttnArgs a = attn_args(p, Q, K, V, O, lse_opt, ws, L);
   a.w = p->n;
   if (p->dtype == FOCUS_F32) return cuda_status(launch_attn_simt_f32(a, p->d, kModeDense, 0, st));
+  CUtensorMap tq, tk, tv, to;
+  const uint64_t planes = static_cast<uint64_t>(p->B) * p->H_kv;
+  const uint64_t qplanes = static_cast<uint64_t>(p->B) * p->H;
+  if (!make_map(&tq, Q, p->d, p->n, qplanes, 128, 3) ||
+      !make_map(&tk, K, p->d, p->n, planes, 128, 3) || !make_map(&tv, V, p->d, p->n, planes, 128, 3) ||
+      !make_map(&to, O, p->d, p->n, qplanes, 128, 3))
+    return FOCUS_ERR_CUDA;
+  return cuda_status(launch_attn_tc_bf16(a, &tq, &tk, &tv, &to, &to, p->d, kModeDense, 0, sm_count(), st));
+}
+
+focus_status_t focus_test_attention_wait_limit(const focus_params_t* p, const void* Q, const void* K,
+                                               const void* V, void* O, void* ws, size_t ws_bytes,
+                                               uint64_t wait_ns, void* stream) {
+  if (!params_ok(p) || wait_ns == 0 || wait_ns > kWaitLimitNs) return FOCUS_ERR_INVALID_ARG;
+  if (p->dtype != FOCUS_BF16) return FOCUS_ERR_UNSUPPORTED;
+  if (focus_status_t s = attention_common(p, Q, K, V, O, nullptr, ws, ws_bytes)) return s;
+  const Layout L = layout_of(p);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  AttnArgs a = attn_args(p, Q, K, V, O, nullptr, ws, L);
+  a.w = p->n;
+  a.wait_ns = wait_ns;
+  a.hold_first_q = 1;
   CUtensorMap tq, tk, tv, to;
   const uint64_t planes = static_cast<uint64_t>(p->B) * p->H_kv;
   const uint64_t qplanes = static_cast<uint64_t>(p->B) * p->H;

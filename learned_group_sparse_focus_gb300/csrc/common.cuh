@@ -13,8 +13,7 @@ namespace focus {
 
 // ------------------------------------------------------------ error word ---
 
-// One second: no wait in these kernels legitimately lasts this long.
-constexpr unsigned long long kWaitTimeoutNs = 1000000000ull;
+constexpr unsigned long long kWaitTimeoutNs = kWaitLimitNs;
 // Longest a single mbarrier try_wait may sleep before the loop checks again.
 constexpr uint32_t kWaitSleepNs = 2000;
 // Sleep between probes of a polling issuer thread.
@@ -79,18 +78,19 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for phase `parity` of `bar` to complete, giving up after
-// kWaitTimeoutNs or as soon as another role of the CTA raised `abort`.
+// Wait for phase `parity` of `bar` to complete, giving up after limit_ns
+// (kWaitTimeoutNs unless the caller shortens it) or as soon as another role of
+// the CTA raised `abort`.
 // On giving up it raises `abort`, sets the timeout bit and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          int* err) {
+                                          int* err, unsigned long long limit_ns = kWaitTimeoutNs) {
   if (mbar_test_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
     if ((it & 63u) == 0) {
       if (*abort) return false;
-      if (global_ns() - t0 > kWaitTimeoutNs) {
+      if (global_ns() - t0 > limit_ns) {
         *abort = 1;
         atomicOr(err, kErrTimeout);
         return false;
@@ -103,7 +103,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 // polls with a short sleep between probes, so while it waits it leaves the
 // issue slots of its SM sub-partition to the compute warps there.
 __device__ __forceinline__ bool mbar_wait_nap(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                              int* err) {
+                                              int* err, unsigned long long limit_ns = kWaitTimeoutNs) {
   if (mbar_test_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
@@ -111,7 +111,7 @@ __device__ __forceinline__ bool mbar_wait_nap(uint64_t* bar, uint32_t parity, vo
     if (mbar_test_wait(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (*abort) return false;
-      if (global_ns() - t0 > kWaitTimeoutNs) {
+      if (global_ns() - t0 > limit_ns) {
         *abort = 1;
         atomicOr(err, kErrTimeout);
         return false;

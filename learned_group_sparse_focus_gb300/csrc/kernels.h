@@ -13,6 +13,8 @@ constexpr int kTileM = FOCUS_TILE_M;   // query rows per group-pass work item
 constexpr int kTileN = FOCUS_TILE_N;   // keys per attention tile
 constexpr int kMaxK = FOCUS_MAX_K;
 constexpr int kIndexSeg = 1024;        // tokens per counting-sort segment
+// One second: no wait in these kernels legitimately lasts this long.
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
 // Bits of the device error word (first int of the workspace).
 enum : int {
@@ -78,6 +80,11 @@ struct AttnArgs {
   int m, kshift;
   float scale_log2;          // scale * log2(e)
   int* err;
+  // Bounded waits give up after wait_ns.  Test hook: with hold_first_q set the
+  // Q load warp never issues its first Q tile, so the first S product's wait
+  // runs out and the kernel takes its abort path.
+  unsigned long long wait_ns;
+  int hold_first_q;
 };
 
 // index.cu

@@ -68,6 +68,8 @@ def _load():
         "focus_attention_fwd_timed": ([P, vp, vp, vp, ctypes.POINTER(Index), vp, vp, vp, ctypes.c_size_t,
                                        vp, ctypes.POINTER(ctypes.c_void_p)], ctypes.c_int),
         "focus_dense_causal_fwd": ([P, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp], ctypes.c_int),
+        "focus_test_attention_wait_limit": ([P, vp, vp, vp, vp, vp, ctypes.c_size_t, ctypes.c_uint64, vp],
+                                            ctypes.c_int),
         "focus_sinkhorn_workspace_bytes": ([P], ctypes.c_size_t),
         "focus_assign_scores": ([P, vp, vp, vp, vp, vp, ctypes.c_size_t, vp], ctypes.c_int),
         "focus_sinkhorn_fwd": ([P, ctypes.c_int32, ctypes.c_float, vp, vp, vp, ctypes.c_size_t, vp],
@@ -105,7 +107,8 @@ EXPORTED = ("focus_abi_version", "focus_status_string", "focus_workspace_bytes",
             "focus_build_index_static", "focus_workspace_bytes_topk", "focus_assign_topk",
             "focus_build_index_topk", "focus_attention_topk_fwd", "focus_attention_topk_fwd_timed",
             "focus_attention_two_call_fwd", "focus_sinkhorn_workspace_bytes", "focus_assign_scores",
-            "focus_sinkhorn_fwd", "focus_backward_workspace_bytes", "focus_attention_bwd")
+            "focus_sinkhorn_fwd", "focus_backward_workspace_bytes", "focus_attention_bwd",
+            "focus_test_attention_wait_limit")
 
 
 def lib():
@@ -202,6 +205,15 @@ def focus_dense_causal_fwd(p: Params, Q, K, V, O, lse, ws, stream=None):
     _check("focus_dense_causal_fwd",
            _lib.focus_dense_causal_fwd(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(lse),
                                        _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def focus_test_attention_wait_limit(p: Params, Q, K, V, O, ws, wait_ns: int, stream=None):
+    """Test hook: the dense kernel with its first Q tile withheld and every
+    device wait limited to wait_ns; the device error word then holds the
+    timeout bit (read it with focus_check_errors)."""
+    _check("focus_test_attention_wait_limit",
+           _lib.focus_test_attention_wait_limit(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(ws),
+                                                ws.numel(), int(wait_ns), _stream(stream)))
 
 
 def focus_layer_fwd_host(p: Params, host: dict, dev: dict, ws, stream=None):

@@ -50,10 +50,19 @@ def test_topk_oracle_sample_counts_kept_pairs():
     assert flops == 4 * wl.d * kept
 
 
-def test_traffic_record_only_for_its_workload_and_source():
+def test_traffic_record_only_for_its_workload_and_source(tmp_path):
     sys.path.insert(0, ROOT)
+    import hashlib
+    import json
     import bench
-    rec = bench.traffic_record("attn_tc_group_pass", "gqa_32k")
-    assert rec is not None and rec["bytes_per_launch"] > 0
-    assert bench.traffic_record("attn_tc_group_pass", "llama7b_8k") is None
-    assert bench.traffic_record("no_such_kernel", "gqa_32k") is None
+    src = os.path.join(ROOT, "learned_group_sparse_focus_gb300", "csrc", "attn_tc.cu")
+    sha = hashlib.sha1(open(src, "rb").read()).hexdigest()
+    rec = {"bytes_per_launch": 123, "workload": "gqa_32k", "source": "attn_tc.cu", "source_sha1": sha}
+    path = tmp_path / "traffic.json"
+    path.write_text(json.dumps({"attn_tc_group_pass": rec,
+                                "attn_tc_local_pass": dict(rec, source_sha1="0" * 40)}))
+    got = bench.traffic_record("attn_tc_group_pass", "gqa_32k", str(path))
+    assert got is not None and got["bytes_per_launch"] == 123
+    assert bench.traffic_record("attn_tc_group_pass", "llama7b_8k", str(path)) is None   # other workload
+    assert bench.traffic_record("attn_tc_local_pass", "gqa_32k", str(path)) is None      # source changed
+    assert bench.traffic_record("no_such_kernel", "gqa_32k", str(path)) is None
