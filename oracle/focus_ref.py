@@ -568,6 +568,41 @@ def attention_backward(Q, K, V, gid, w: int, scale: float, A: int, dO):
     return dQ, dK, dV
 
 
+def attention_backward_dkv_rows(Q, K, V, gid, w: int, scale: float, A: int, dO, krows):
+    """dK and dV of attention_backward for selected key rows only.  Key j
+    receives gradient from every query i that keeps it (i >= j and i - j < w,
+    or g_i = g_j), through that query's full softmax row:
+      dV_j = sum_h sum_i P_ij dO_i,   dK_j = scale sum_h sum_i dS_ij q_i,
+    h over the query heads of j's KV head.  The query rows are gathered from
+    the keep rule column by column, their softmax rows computed in full
+    ([FocusKO] 2.1), and only the columns krows kept.  Returns dK, dV
+    [B, H_kv, R, d] (fp64)."""
+    B, H, n, d = Q.shape
+    H_kv = K.shape[1]
+    krows = np.asarray(krows, dtype=np.int64)
+    dK = np.zeros((B, H_kv, len(krows), d))
+    dV = np.zeros((B, H_kv, len(krows), d))
+    for b in range(B):
+        for hq in range(H):
+            kv = kv_head(hq, H, H_kv)
+            a = assignment_of_head(hq, H, H_kv, A)
+            g = np.asarray(gid[b, a])
+            # the queries that keep at least one of the selected keys
+            need = np.zeros(n, dtype=bool)
+            for j in krows:
+                i = np.arange(j, n)
+                need[i[((i - j) < w) | (g[i] == g[j])]] = True
+            rows = np.nonzero(need)[0]
+            q, k, v, do = _f64(Q[b, hq])[rows], _f64(K[b, kv]), _f64(V[b, kv]), _f64(dO[b, hq])[rows]
+            M = keep_mask_rows(g, w, rows)
+            P = attention_weights_rows(_f64(Q[b, hq]), k, M, rows, scale)
+            dP = do @ v.T
+            dS = P * (dP - np.sum(P * dP, axis=1, keepdims=True))
+            dK[b, kv] += scale * (dS[:, krows].T @ q)
+            dV[b, kv] += P[:, krows].T @ do
+    return dK, dV
+
+
 def attention_backward_dq_rows(Q, K, V, gid, w: int, scale: float, A: int, dO, rows):
     """dQ of attention_backward for selected query rows only (each row's dQ
     needs only its own kept keys): dQ_i = scale sum_j P_ij (dO_i . v_j - D_i) k_j.

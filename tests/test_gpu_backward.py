@@ -96,17 +96,55 @@ def test_backward_all_rows(fz, dtype, B, H, H_kv, A, n, d, K, w, kind):
     _close(dV, wV, dtype, "dV")
 
 
+def _key_rows(n, seed):
+    """Sampled key rows: the first keys, both tile edges at 128 and 256, the
+    last keys, and random keys in the second half (late keys are kept by few
+    queries, which keeps the oracle's cost down)."""
+    r = np.random.default_rng(seed).integers(n // 2, n, 8)
+    return np.unique(np.concatenate([[0, 1, 127, 128, 255, 256, n // 2, n - 129, n - 2, n - 1], r]))
+
+
 def test_backward_at_a_long_length_sampled_and_invariants(fz):
     """n = 8192, 8 query / 2 KV heads, d = 128, Zipf groups: sampled dQ rows
-    against the oracle, and at every size sum_j dV_j = sum_i dO_i and
-    sum_j dK_j = 0 per KV head (rows of P sum to 1, rows of dS to 0)."""
+    and sampled dK, dV rows against the oracle element by element, and
+    sum_j dV_j = sum_i dO_i, sum_j dK_j = 0 per KV head (rows of P sum to 1,
+    rows of dS to 0)."""
     (Q, Kt, V, dO, g, p), (dQ, dK, dV) = _run(fz, "bf16", 1, 8, 2, 1, 8192, 128, 16, 256, "zipf", seed=99)
     rows = np.unique(np.concatenate([np.arange(260), [8191], np.random.default_rng(5).integers(0, 8192, 40)]))
     want = ref.attention_backward_dq_rows(Q, Kt, V, g, 256, p.scale, 1, dO, rows)
     _close(dQ[:, :, rows], want, "bf16", "dQ rows")
+    krows = _key_rows(8192, 6)
+    wK, wV = ref.attention_backward_dkv_rows(Q, Kt, V, g, 256, p.scale, 1, dO, krows)
+    _close(dK[:, :, krows], wK, "bf16", "dK rows")
+    _close(dV[:, :, krows], wV, "bf16", "dV rows")
     for kv in range(2):
         heads = [h for h in range(8) if ref.kv_head(h, 8, 2) == kv]
         sdo = dO[0, heads].astype(np.float64).sum(axis=(0, 1))
         M = np.abs(sdo).max()
         assert np.abs(dV[0, kv].sum(axis=0) - sdo).max() <= 2e-2 * M
         assert np.abs(dK[0, kv].sum(axis=0)).max() <= 2e-2 * np.abs(dK[0, kv]).sum(axis=0).max()
+
+
+def test_backward_at_the_32k_gqa_workload_sampled(fz):
+    """The 32K GQA benchmark shape (32 query / 8 KV heads, n = 32768, d = 128,
+    w = 512, K = 64 Zipf groups) at full size: sampled dQ rows of two query
+    heads and sampled dK, dV rows of two KV heads against the oracle."""
+    wl = synth.WORKLOADS["gqa_32k"]
+    (Q, Kt, V, dO, g, p), (dQ, dK, dV) = _run(fz, "bf16", 1, wl.H, wl.H_kv, 1, wl.n, wl.d, wl.K, wl.w, "zipf",
+                                              seed=1004)
+    hpk = wl.H // wl.H_kv
+    rows = np.unique(np.concatenate([[0, 1, 511, 512, 513, wl.n - 1],
+                                     np.random.default_rng(8).integers(0, wl.n, 30)]))
+    for h in (0, wl.H - 1):
+        want = ref.attention_backward_dq_rows(Q[:, h:h + 1], Kt[:, h // hpk:h // hpk + 1],
+                                              V[:, h // hpk:h // hpk + 1], g, wl.w, p.scale, 1,
+                                              dO[:, h:h + 1], rows)
+        _close(dQ[:, h:h + 1, rows], want, "bf16", f"dQ rows, head {h}")
+    krows = np.unique(np.concatenate([[wl.n - 1, wl.n - 2, wl.n - 600],
+                                      np.random.default_rng(9).integers(wl.n - 2048, wl.n, 5)]))
+    for kv in (0, wl.H_kv - 1):
+        hs = slice(kv * hpk, (kv + 1) * hpk)
+        wK, wV = ref.attention_backward_dkv_rows(Q[:, hs], Kt[:, kv:kv + 1], V[:, kv:kv + 1], g, wl.w, p.scale,
+                                                 1, dO[:, hs], krows)
+        _close(dK[:, kv:kv + 1, krows], wK, "bf16", f"dK rows, KV head {kv}")
+        _close(dV[:, kv:kv + 1, krows], wV, "bf16", f"dV rows, KV head {kv}")

@@ -748,6 +748,43 @@ def test_backward_dq_rows_equal_full_backward_rows():
                                dQ[:, :, rows], atol=1e-13)
 
 
+def test_backward_dkv_rows_equal_full_backward_rows():
+    # key rows gathered column by column (the queries that keep each key) give
+    # the full backward's dK, dV rows: GQA with per-KV-head ids and Zipf groups
+    rng = np.random.default_rng(49)
+    for B, H, Hkv, A, n, d, w, K, kind in ((1, 4, 2, 2, 70, 6, 6, 5, "uniform"),
+                                          (2, 2, 1, 1, 64, 4, 3, 3, "zipf"),
+                                          (1, 2, 2, 1, 40, 5, 50, 2, "uniform")):   # w > n: dense
+        Q, dO = (rng.standard_normal((B, H, n, d)) for _ in range(2))
+        Kt, V = (rng.standard_normal((B, Hkv, n, d)) for _ in range(2))
+        g = synth.draw_group_ids(50 + n, B, A, n, K, kind)
+        _, dK, dV = ref.attention_backward(Q, Kt, V, g, w, 0.35, A, dO)
+        krows = np.array([0, 1, n // 2, n - 2, n - 1])
+        gK, gV = ref.attention_backward_dkv_rows(Q, Kt, V, g, w, 0.35, A, dO, krows)
+        np.testing.assert_allclose(gK, dK[:, :, krows], atol=1e-12)
+        np.testing.assert_allclose(gV, dV[:, :, krows], atol=1e-12)
+
+
+def test_backward_dkv_rows_match_central_differences():
+    rng = np.random.default_rng(51)
+    B, H, Hkv, n, d, w = 1, 2, 1, 12, 3, 3
+    Q, dO = (rng.standard_normal((B, H, n, d)) for _ in range(2))
+    K, V = (rng.standard_normal((B, Hkv, n, d)) for _ in range(2))
+    g = synth.draw_group_ids(52, B, 1, n, 3, "uniform")
+    krows = np.array([2, 7, 11])
+    gK, gV = ref.attention_backward_dkv_rows(Q, K, V, g, w, 0.6, 1, dO, krows)
+    eps = 1e-6
+    for X, G in ((K, gK), (V, gV)):
+        for r, j in enumerate(krows):
+            for c in range(d):
+                Xp, Xm = X.copy(), X.copy()
+                Xp[0, 0, j, c] += eps
+                Xm[0, 0, j, c] -= eps
+                args = lambda Z: (Q, Z if X is K else K, Z if X is V else V)
+                num = (_loss(*args(Xp), g, w, 0.6, 1, dO) - _loss(*args(Xm), g, w, 0.6, 1, dO)) / (2 * eps)
+                assert abs(num - G[0, 0, r, c]) < 1e-7, (j, c, num, G[0, 0, r, c])
+
+
 def test_backward_planted_mistake_is_caught():
     # the finite-difference pin rejects a backward that drops the D term
     # (dS = P * dP): the planted version's dQ misses the numerical gradient
