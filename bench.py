@@ -440,6 +440,8 @@ def run_ours(args, wl, world, rank, local):
     es = 2 if wl.dtype == "bf16" else 4
     assign_bytes = (wl.B * wl.n * wl.D + wl.A * wl.d_g * wl.D + wl.A * wl.K * wl.d_g) * es + wl.B * wl.A * wl.n * 4
     kv_bytes = 2 * wl.B * wl.H_kv * wl.n * wl.d * es
+    # index: gid read once, perm, rank, farlen per token and per slot written (int32)
+    index_bytes = wl.B * wl.A * wl.n * 4 * 5
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True, "scaling": "weak",
@@ -460,7 +462,8 @@ def run_ours(args, wl, world, rank, local):
             "permute_kv": {"ms": t["permute_kv"], "GB/s": 2 * kv_bytes / (t["permute_kv"] * 1e-3) / 1e9},
             "group_pass": {"ms": t["group_pass"], "TFLOP/s": f_group / (t["group_pass"] * 1e-3) / 1e12},
             "local_pass": {"ms": t["local_pass"], "TFLOP/s": f_local / (t["local_pass"] * 1e-3) / 1e12},
-            "index": {"ms": t["index"]},
+            "index": {"ms": t["index"], "GB/s": index_bytes / (t["index"] * 1e-3) / 1e9,
+                      "hbm_frac": index_bytes / (t["index"] * 1e-3) / 1e9 / peak_hbm},
         },
         "e2e": {"value": job_tflops(world, f_attn, t_e2e), "unit": UNIT, "ms_per_step": t_e2e,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
