@@ -157,12 +157,11 @@ __device__ __forceinline__ int unit_count(const AttnArgs& a) {
 }
 
 template <int MODE>
-__device__ __forceinline__ void decode_unit(const AttnArgs& a, int u, Unit& U) {
+__device__ __forceinline__ void decode_unit(const AttnArgs& a, int u, const focus_item_t& it, Unit& U) {
   int kv, asg;
   if (MODE == kModeGroup) {
     const int hpa = a.A == 1 ? a.H : a.H / a.H_kv;
     const int y = u % hpa;
-    const focus_item_t it = a.items[a.order[u / hpa]];
     U.b = it.b;
     asg = it.a;
     U.h = a.A == 1 ? y : it.a * (a.H / a.H_kv) + y;
@@ -200,6 +199,42 @@ __device__ __forceinline__ int snake_unit(int k, int n_units) {
   const int u = base + ((k & 1) ? G - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x));
   return u < n_units ? u : -2;
 }
+
+// Every role walks the same units.  In the group pass a unit is named by two
+// dependent loads (its order entry, then its item); the walk keeps the next
+// round's item and the order entry of the round after it in flight while the
+// current unit runs, so neither load sits on a role's path at a unit boundary.
+template <int MODE>
+struct UnitWalk {
+  focus_item_t nxt;   // item of round k + 1's unit
+  int ord;            // order entry of round k + 2's unit
+  int hpa, n_units;
+
+  __device__ __forceinline__ void begin(const AttnArgs& a, int n) {
+    n_units = n;
+    hpa = a.A == 1 ? a.H : a.H / a.H_kv;
+    if (MODE == kModeGroup) {
+      const int u0 = snake_unit(0, n), u1 = snake_unit(1, n);
+      if (u0 >= 0) nxt = a.items[a.order[u0 / hpa]];
+      ord = u1 >= 0 ? a.order[u1 / hpa] : 0;
+    }
+  }
+  // Round k's unit (as snake_unit: -1 past the end, -2 none this round),
+  // decoded into U when there is one.
+  __device__ __forceinline__ int step(const AttnArgs& a, int k, Unit& U) {
+    const int u = snake_unit(k, n_units);
+    if (MODE == kModeGroup) {
+      const focus_item_t it = nxt;
+      if (snake_unit(k + 1, n_units) >= 0) nxt = a.items[ord];
+      const int u2 = snake_unit(k + 2, n_units);
+      if (u2 >= 0) ord = a.order[u2 / hpa];
+      if (u >= 0) decode_unit<MODE>(a, u, it, U);
+    } else if (u >= 0) {
+      decode_unit<MODE>(a, u, nxt, U);
+    }
+    return u;
+  }
+};
 
 // What the epilogue of a unit needs once its tile loop is over.  In the local
 // pass the row's far flag and group LSE are read when the unit starts (and its
@@ -302,12 +337,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       int qn = 0;                // Q tiles issued
       int ck = 0;                // K tiles issued
       bool ok = true;
+      UnitWalk<MODE> walk;
+      walk.begin(a, n_units);
       for (int k = 0; ok; ++k) {
-        const int u = snake_unit(k, n_units);
+        Unit U;
+        const int u = walk.step(a, k, U);
         if (u == -1) break;
         if (u < 0) continue;
-        Unit U;
-        decode_unit<MODE>(a, u, U);
         {
           // the unit's Q tile
           const int sl = qn % kQSlots, use = qn / kQSlots;
@@ -402,12 +438,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (MODE != kModeLocal) mbar_arrive(ost_free);
           return true;
         };
+        UnitWalk<MODE> walk;
+        walk.begin(a, n_units);
         for (int k = 0; ok; ++k) {
-          const int u = snake_unit(k, n_units);
+          Unit U;
+          const int u = walk.step(a, k, U);
           if (u == -1) break;
           if (u < 0) continue;
-          Unit U;
-          decode_unit<MODE>(a, u, U);
           for (int t = U.t0, i = 0; t <= U.t1; ++t, ++cv, ++i) {
             const int sl = cv % kVSlots, use = cv / kVSlots;
             if (use > 0 && !mbar_wait_nap(&v_empty[sl], (use - 1) & 1, abort, a.err, a.wait_ns)) { ok = false; break; }
@@ -468,12 +505,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         int cv = 0;       // V ring entries walked
         int un = 0;       // units walked
         bool ok = true;
+        UnitWalk<MODE> walk;
+        walk.begin(a, n_units);
         for (int k = 0; ok; ++k) {
-          const int u = snake_unit(k, n_units);
+          Unit U;
+          const int u = walk.step(a, k, U);
           if (u == -1) break;
           if (u < 0) continue;
-          Unit U;
-          decode_unit<MODE>(a, u, U);
           const int nt = U.t1 - U.t0 + 1;
           if (warp == kWarpS) {
             // S(gg) = Q K^T into S buffer gg&1 once the softmax has read S(gg-2),
@@ -673,18 +711,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
 
+    UnitWalk<MODE> walk;
+    walk.begin(a, n_units);
     for (int k = 0; ok; ++k) {
-      const int u = snake_unit(k, n_units);
+      Unit U;
+      const int u = walk.step(a, k, U);
       if (u == -1) break;
       if (u < 0) continue;
-      Unit U;
-      decode_unit<MODE>(a, u, U);
-      // 1. the previous unit's epilogue overlaps this unit's first S products
-      if (have_prev) {
-        if (!epilogue(prev, un - 1)) { ok = false; break; }
-        have_prev = false;
-      }
-      // 2. this unit's key tiles
+      // 1. this unit's rows: their loads are issued before the previous
+      // unit's epilogue, which hides their latency
       RowState st{};
       st.valid = r < U.nrows;
       st.prob = U.prob;
@@ -715,6 +750,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      // 2. the previous unit's epilogue overlaps this unit's first S products
+      if (have_prev) {
+        if (!epilogue(prev, un - 1)) { ok = false; break; }
+        have_prev = false;
+      }
+      // 3. this unit's key tiles
       float m_run = -INFINITY, l = 0.f;
       const int nt = U.t1 - U.t0 + 1;
       for (int i = 0; i < nt; ++i) {
