@@ -389,8 +389,9 @@ static focus_status_t assign_impl(const focus_params_t* p, int k, const void* h,
   if (!(p->d_g == 32 || p->d_g == 64 || p->d_g == 128)) return FOCUS_ERR_UNSUPPORTED;
   if (p->A * p->d_g > 512 || p->D % 8 != 0) return FOCUS_ERR_UNSUPPORTED;
   const int ncol = p->A * p->d_g;
+  al.tile_rows = assign_tile_rows(p->B * p->n, ncol, al.num_sms);
   CUtensorMap tm_h, tm_w;
-  if (!make_map(&tm_h, h, p->D, static_cast<uint64_t>(p->B) * p->n, 1, 128, 2) ||
+  if (!make_map(&tm_h, h, p->D, static_cast<uint64_t>(p->B) * p->n, 1, al.tile_rows, 2) ||
       !make_map(&tm_w, W, p->D, ncol, 1, ncol < 256 ? ncol : 256, 2))
     return FOCUS_ERR_CUDA;
   return cuda_status(launch_assign_bf16(al, &tm_h, &tm_w, st));
@@ -894,8 +895,9 @@ focus_status_t focus_assign_scores(const focus_params_t* p, const void* h, const
   if (!(p->d_g == 32 || p->d_g == 64 || p->d_g == 128)) return FOCUS_ERR_UNSUPPORTED;
   if (p->A * p->d_g > 512 || p->D % 8 != 0) return FOCUS_ERR_UNSUPPORTED;
   const int ncol = p->A * p->d_g;
+  al.tile_rows = assign_tile_rows(p->B * p->n, ncol, al.num_sms);
   CUtensorMap tm_h, tm_w;
-  if (!make_map(&tm_h, h, p->D, static_cast<uint64_t>(p->B) * p->n, 1, 128, 2) ||
+  if (!make_map(&tm_h, h, p->D, static_cast<uint64_t>(p->B) * p->n, 1, al.tile_rows, 2) ||
       !make_map(&tm_w, W, p->D, ncol, 1, ncol < 256 ? ncol : 256, 2))
     return FOCUS_ERR_CUDA;
   return cuda_status(launch_assign_bf16(al, &tm_h, &tm_w, st));

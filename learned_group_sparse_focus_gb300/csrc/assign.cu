@@ -329,7 +329,7 @@ template <int NALLOC, int DG, bool kScores>
 __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
     const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
     const __nv_bfloat16* __restrict__ C, int32_t* __restrict__ gid, float* __restrict__ scores,
-    int B, int n, int D, int K, int A, int topk, int* err) {
+    int B, int n, int D, int K, int A, int topk, int R, int* err) {
   using Cfg = StreamCfg<NALLOC>;
   constexpr int S = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
 
   const int warp = warp_id(), lane = lane_id();
   const int ncol = A * DG;
-  const int ntiles = (B * n + kBM - 1) / kBM;
+  const int ntiles = (B * n + R - 1) / R;   // tiles of R <= 128 tokens
   const int nk = (D + kBK - 1) / kBK;
 
   if (threadIdx.x == 0) {
@@ -367,7 +367,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
 
   if (warp == 0) {
     if (lane == 0) {
-      const uint32_t bytes = Cfg::kStageA + ncol * kBK * 2;
+      // a tile's R rows of h fill the first R rows of the stage; the MMAs read
+      // all 128, and the accumulator rows past R are never read out
+      const uint32_t bytes = R * kBK * 2 + ncol * kBK * 2;
       int it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
@@ -376,7 +378,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
           if (u > 0 && !mbar_wait_nap(&empty[s], (u - 1) & 1, abort, err)) { ok = false; break; }
           uint8_t* sa = smem + s * Cfg::kStage;
           mbar_expect_tx(&full[s], bytes);
-          tma_load_2d(sa, &tm_h, &full[s], kb * kBK, tile * kBM);
+          tma_load_2d(sa, &tm_h, &full[s], kb * kBK, tile * R);
           tma_load_2d(sa + Cfg::kStageA, &tm_w, &full[s], kb * kBK, 0);
         }
       }
@@ -419,8 +421,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
       const int buf = i & 1;
       if (!mbar_wait(&tfull[buf], (i >> 1) & 1, abort, err)) break;
       tc_fence_after();
-      const int tok = tile * kBM + row;
-      const bool keep = tok < B * n;
+      const int tok = tile * R + row;
+      const bool keep = row < R && tok < B * n;
       const int b = keep ? tok / n : 0, ti = keep ? tok % n : 0;
       for (int a = 0; a < A; ++a) {
         float p[128];
@@ -482,15 +484,17 @@ template <int NALLOC, int DG>
 cudaError_t launch_stream(const AssignLaunch& L, const CUtensorMap* tm_h, const CUtensorMap* tm_w,
                           cudaStream_t st) {
   using Cfg = StreamCfg<NALLOC>;
-  const int ntiles = (L.B * L.n + kBM - 1) / kBM;
+  const int R = L.tile_rows;
+  if (R < 1 || R > kBM) return cudaErrorInvalidValue;
+  const int ntiles = (L.B * L.n + R - 1) / R;
   const int grid = ntiles < L.num_sms ? ntiles : L.num_sms;
   const __nv_bfloat16* C = static_cast<const __nv_bfloat16*>(L.C);
   if (L.scores)
     assign_stream_kernel<NALLOC, DG, true><<<grid, kStreamThreads, Cfg::kSmem, st>>>(
-        *tm_h, *tm_w, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk, L.err);
+        *tm_h, *tm_w, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk, R, L.err);
   else
     assign_stream_kernel<NALLOC, DG, false><<<grid, kStreamThreads, Cfg::kSmem, st>>>(
-        *tm_h, *tm_w, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk, L.err);
+        *tm_h, *tm_w, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk, R, L.err);
   return cudaGetLastError();
 }
 
@@ -506,6 +510,7 @@ cudaError_t launch_stream_dg(const AssignLaunch& L, const CUtensorMap* tm_h, con
 template <int NALLOC>
 cudaError_t launch_tc(const AssignLaunch& L, const CUtensorMap* tm_h, const CUtensorMap* tm_w,
                       cudaStream_t st) {
+  if (L.tile_rows != kBM) return cudaErrorInvalidValue;
   const int grid = (L.B * L.n + kBM - 1) / kBM;
   if (L.scores)
     assign_tc_kernel<NALLOC, true><<<grid, 128, AssignCfg<NALLOC>::kSmem, st>>>(
@@ -545,6 +550,20 @@ cudaError_t launch_assign_f32(const AssignLaunch& L, cudaStream_t st) {
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
+}
+
+static bool stream_width(int ncol) { return ncol == 32 || ncol == 64 || ncol == 128 || ncol == 256; }
+
+int assign_tile_rows(int tokens, int ncol, int num_sms) {
+  // With t tiles per SM the last wave is full when every tile has the same
+  // share of the tokens: R = ceil(tokens / (SMs * t)), which lies in (64, 128]
+  // for t >= 2.  One tile per SM or less keeps 128-token tiles.
+  if (!stream_width(ncol) || num_sms < 1) return kBM;
+  const long long per_wave = static_cast<long long>(num_sms) * kBM;
+  if (tokens <= per_wave) return kBM;
+  const long long t = (tokens + per_wave - 1) / per_wave;
+  const long long span = static_cast<long long>(num_sms) * t;
+  return static_cast<int>((tokens + span - 1) / span);
 }
 
 cudaError_t launch_assign_bf16(const AssignLaunch& L, const CUtensorMap* tm_h,

@@ -56,6 +56,7 @@ struct AssignLaunch {
   int* err;
   float* scores;   // non-null: write every score [B, A, n, K] (fp32) instead of ids
   int num_sms;     // SMs of the device (persistent grid)
+  int tile_rows;   // tokens per tile = rows of tm_h's box (assign_tile_rows)
 };
 
 // Everything the attention kernels read besides the K/V tensor maps.
@@ -96,6 +97,10 @@ cudaError_t launch_assign_f32(const AssignLaunch& L, cudaStream_t st);
 cudaError_t launch_assign_bf16(const AssignLaunch& L, const CUtensorMap* tm_h,
                                const CUtensorMap* tm_w, cudaStream_t st);
 cudaError_t setup_assign_kernels();
+// Tokens per tile of the bf16 assign kernel for `tokens` tokens and ncol = A * d_g
+// projection columns: 128, or (persistent kernel, more than one tile per SM) the
+// smallest count that gives every SM the same number of tiles.
+int assign_tile_rows(int tokens, int ncol, int num_sms);
 
 // attn_simt.cu (fp32 storage, fp32 arithmetic on the CUDA cores)
 enum AttnMode : int { kModeLocal = 0, kModeGroup = 1, kModeDense = 2 };

@@ -63,6 +63,9 @@ def _check_index(got, want_idx, want_items, want_order):
     ("bf16", 3, 129, 128, 64, 1, 1, 1),
     ("bf16", 1, 200, 64, 64, 64, 8, 8),      # A * d_g = 512 columns
     ("bf16", 1, 64, 1024, 32, 300, 1, 1),    # centroids in several shared-memory chunks
+    # more tokens than 128 per SM: tiles shrink so every SM gets the same count
+    ("bf16", 1, 20000, 256, 64, 16, 1, 1),   # 66-token tiles
+    ("bf16", 2, 16500, 128, 32, 8, 2, 2),    # 109-token tiles across the batch boundary
     ("f32", 2, 300, 128, 64, 4, 1, 1),
     ("f32", 1, 77, 96, 16, 9, 2, 2),
 ])

@@ -58,6 +58,7 @@ def _np_index(fz, p, x, ws, n_items_len, K):
     ("bf16", 1, 200, 64, 64, 64, 8, 8),
     ("bf16", 1, 64, 1024, 128, 91, 1, 1),         # largest K for k = 2
     ("bf16", 1, 130, 128, 64, 2, 1, 1),           # K = 2: both groups, order decided
+    ("bf16", 1, 21000, 128, 32, 4, 2, 2),         # tiles of fewer than 128 tokens
     ("f32", 2, 300, 128, 64, 4, 1, 1),
     ("f32", 1, 77, 96, 16, 9, 2, 2),
 ])
