@@ -30,7 +30,8 @@ with the pages' K = 4 (--K).  Kept pairs are counted once.
 --sinkhorn T times the training-time soft assignment instead: scores
 (focus_assign_scores) and T Sinkhorn rounds (focus_sinkhorn_fwd) on the
 workload's assignment shape; value = algorithmic GB/s of the Sinkhorn rounds
-(each round streams S twice, the last also writes G).
+(for K <= 256, K % 4 == 0: S read once up front and once per round, G
+written once).
 
 --backward times focus_attention_bwd (dQ, dK, dV over the kept pairs, after
 one untimed forward for O and LSE); value = 10*d FLOPs per kept pair per head
@@ -691,7 +692,10 @@ def run_ours_sinkhorn(args, wl, world, rank, local):
     t_sc = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     t_sk = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     sbytes = S.numel() * 4
-    alg = (2 * T + 1) * sbytes + 4 * wl.B * wl.A * wl.n * T        # S twice per round, G once, u per round
+    # K <= 256: S once up front and once per round, G once; larger K: S twice
+    # per round, G once, u per round
+    fused = wl.K <= 256 and wl.K % 4 == 0
+    alg = (T + 2) * sbytes if fused else (2 * T + 1) * sbytes + 4 * wl.B * wl.A * wl.n * T
     peaks, peak_kind = load_peaks()
     gbs = alg / (t_sk * 1e-3) / 1e9
     line = {
@@ -706,7 +710,7 @@ def run_ours_sinkhorn(args, wl, world, rank, local):
                      "peak": float(peaks["hbm_gbs"]), "unit": "GB/s", "frac": gbs / float(peaks["hbm_gbs"]),
                      "traffic": None, "peak_source": f"{peak_kind} hbm_gbs",
                      "note": "S is L2-resident when smaller than ~100 MB, so frac can exceed 1"},
-        "gpu_launches": (1 + 3 * T) * args.steps,
+        "gpu_launches": ((2 + T) if fused else (1 + 3 * T)) * args.steps,
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -716,7 +720,8 @@ def run_ours_sinkhorn(args, wl, world, rank, local):
         Sref = ref.scores(x["h"][:, :rows], x["W"], x["C"])
         ref.sinkhorn(Sref, T, 1.0)
         sec = time.perf_counter() - t0
-        ab = (2 * T + 1) * Sref.size * 4 + 4 * Sref.shape[0] * Sref.shape[1] * rows * T
+        ab = ((T + 2) * Sref.size * 4 if fused
+              else (2 * T + 1) * Sref.size * 4 + 4 * Sref.shape[0] * Sref.shape[1] * rows * T)
         line["cpu_baseline"] = {"value": ab / sec / 1e9, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
                                 "sample": f"oracle fp64 scores + {T} Sinkhorn rounds on the first {rows} tokens "
                                           f"(the same bytes-per-round accounting)", "seconds": sec}

@@ -370,8 +370,10 @@ FOCUS_API focus_status_t focus_assign_scores(const focus_params_t* p, const void
 
 /* Sinkhorn forward: S [B, A, n, K] fp32 scores -> G [B, A, n, K] fp32 soft
  * assignment (G may be S: updated in place).  iters = T in [1, 10000],
- * tau > 0 finite, else FOCUS_ERR_INVALID_ARG.  Log-domain arithmetic in fp32;
- * 3 launches per round. */
+ * tau > 0 finite, else FOCUS_ERR_INVALID_ARG.  Log-domain arithmetic in fp32.
+ * For K <= 256 with K % 4 == 0 a round is one launch and one pass over S (the
+ * row step fused with the next round's column step), plus one column pass up
+ * front; other K take two passes and three launches per round. */
 FOCUS_API focus_status_t focus_sinkhorn_fwd(const focus_params_t* p, int32_t iters, float tau,
                                             const float* S, float* G, void* ws, size_t ws_bytes,
                                             void* stream);

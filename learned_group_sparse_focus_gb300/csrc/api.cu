@@ -113,6 +113,7 @@ focus_status_t ensure_setup() {
     if (setup_assign_kernels() != cudaSuccess) return FOCUS_ERR_CUDA;
     if (setup_attn_kernels() != cudaSuccess) return FOCUS_ERR_CUDA;
     if (setup_bwd_tc_kernels() != cudaSuccess) return FOCUS_ERR_CUDA;
+    if (setup_sinkhorn_kernels() != cudaSuccess) return FOCUS_ERR_CUDA;
     g_ready[dev] = true;
   }
   return FOCUS_OK;
@@ -857,7 +858,8 @@ focus_status_t focus_attention_topk_fwd(const focus_params_t* p, const void* Q, 
 
 // ------------------------------------------------ Sinkhorn soft assignment ---
 
-static size_t sinkhorn_layout(const focus_params_t* p, size_t* u, size_t* v, size_t* part) {
+static size_t sinkhorn_layout(const focus_params_t* p, size_t* u, size_t* v, size_t* part,
+                              size_t* ticket) {
   const size_t P = static_cast<size_t>(p->B) * p->A;
   const int rpc = sinkhorn_rows_per_chunk(p->n);
   const size_t chunks = (static_cast<size_t>(p->n) + rpc - 1) / rpc;
@@ -868,13 +870,15 @@ static size_t sinkhorn_layout(const focus_params_t* p, size_t* u, size_t* v, siz
   o = align_up(o + P * p->K * 4);
   *part = o;
   o = align_up(o + P * chunks * p->K * 8);
+  *ticket = o;
+  o = align_up(o + P * 4);
   return o;
 }
 
 size_t focus_sinkhorn_workspace_bytes(const focus_params_t* p) {
   if (!params_ok(p)) return 0;
-  size_t u, v, part;
-  return sinkhorn_layout(p, &u, &v, &part);
+  size_t u, v, part, ticket;
+  return sinkhorn_layout(p, &u, &v, &part, &ticket);
 }
 
 focus_status_t focus_assign_scores(const focus_params_t* p, const void* h, const void* W,
@@ -909,11 +913,11 @@ focus_status_t focus_sinkhorn_fwd(const focus_params_t* p, int32_t iters, float 
   if (iters < 1 || iters > 10000 || !(std::isfinite(tau) && tau > 0.f)) return FOCUS_ERR_INVALID_ARG;
   if (!S || !G || !aligned16(S) || !aligned16(G)) return FOCUS_ERR_INVALID_ARG;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return FOCUS_ERR_INVALID_ARG;
-  size_t u, v, part;
-  if (ws_bytes < sinkhorn_layout(p, &u, &v, &part)) return FOCUS_ERR_WORKSPACE;
+  size_t u, v, part, ticket;
+  if (ws_bytes < sinkhorn_layout(p, &u, &v, &part, &ticket)) return FOCUS_ERR_WORKSPACE;
   if (focus_status_t s = ensure_setup()) return s;
-  SinkhornLaunch L{S, G, at<float>(ws, u), at<float>(ws, v), at<float2>(ws, part), p->B * p->A, p->n,
-                   p->K, 1.f / tau};
+  SinkhornLaunch L{S, G, at<float>(ws, u), at<float>(ws, v), at<float2>(ws, part), at<int>(ws, ticket),
+                   p->B * p->A, p->n, p->K, 1.f / tau, at<int>(ws, 0), sm_count()};
   return cuda_status(launch_sinkhorn(L, iters, static_cast<cudaStream_t>(stream)));
 }
 

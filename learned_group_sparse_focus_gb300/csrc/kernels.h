@@ -164,10 +164,14 @@ struct SinkhornLaunch {
   float* u;          // [P, n] row potentials
   float* v;          // [P, K] column potentials
   float2* part;      // [P, chunks, K] per-chunk column (max, sum)
+  int* ticket;       // [P] blocks of the current pass done (0 between launches)
   int P, n, K;
   float inv_tau;
+  int* err;          // device error word (bounded waits)
+  int num_sms;
 };
 int sinkhorn_rows_per_chunk(int n);
+cudaError_t setup_sinkhorn_kernels();
 
 // attn_bwd.cu: backward over the kept pairs (fp32 arithmetic on the CUDA cores).
 struct BwdArgs {

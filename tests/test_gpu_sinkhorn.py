@@ -74,6 +74,10 @@ def test_scores_match_oracle(fz, dtype, B, n, D, d_g, K, A, H_kv):
     (1, 1, 3000, 300, 7, 1.0),       # K > 256: columns in two passes
     (1, 1, 1, 5, 3, 1.0),            # one token
     (1, 1, 300000, 8, 3, 1.0),       # more than 2048 row chunks of 128
+    (1, 1, 777, 33, 6, 0.7),         # K % 4 != 0: two reads of S per round
+    (1, 1, 777, 36, 6, 0.7),         # one pass per round, second float4 slot mostly empty
+    (1, 2, 1000, 132, 5, 1.0),       # eight float4 slots per lane, most empty
+    (1, 1, 2000, 64, 5, 0.2),        # peaked rows: X up to about 45
 ])
 def test_sinkhorn_matches_oracle(fz, B, A, n, K, T, tau):
     import torch
