@@ -147,8 +147,9 @@ def test_sinkhorn_argument_checks(fz):
     lib = fz.lib()
     p = fz.make_params(B=1, H=2, H_kv=2, n=1000, d=64, D=64, d_g=32, K=16, A=2, w=8)
     need = lib.focus_sinkhorn_workspace_bytes(ctypes.byref(p))
-    # error word + u [2, 1000] + v [2, 16] + chunk partials [2, 8, 16] float2, each 256-aligned
-    assert need == 256 + 8192 + 256 + 2048
+    # error word + u [2, 1000] + v [2, 16] + chunk partials [2, 8, 16] float2 + a
+    # ticket per problem, each 256-aligned
+    assert need == 256 + 8192 + 256 + 2048 + 256
     ok = ctypes.c_void_p(1 << 20)
     mis = ctypes.c_void_p((1 << 20) + 8)
     f = lib.focus_sinkhorn_fwd
