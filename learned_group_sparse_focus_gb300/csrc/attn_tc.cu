@@ -84,6 +84,11 @@ constexpr int kRegsHigh = 208;
 constexpr int kQSlots = 2;
 constexpr int kKSlots = 2;
 constexpr int kVSlots = 2;
+// S buffers in TMEM.  The softmax writes P(g) as bf16 pairs over the S(g) it
+// has just read (each half-row warp into the first 32 columns of its own 64),
+// so a buffer is free again once O += P(g) V(g) is done, and no P buffer of its
+// own has to be waited for before the write.
+constexpr int kSBuf = 3;
 
 template <int D>
 struct AttnCfg {
@@ -97,13 +102,13 @@ struct AttnCfg {
   static constexpr int kXch = kBar + 256;                   // row max / sum exchange: [2][2][128] fp32
   static constexpr int kRowTok = kXch + 2 * 2 * 128 * 4;    // group pass: O_far row of each tile row
   static constexpr int kSmem = kRowTok + 128 * 4;
-  static constexpr uint32_t kS = 0;          // two S buffers of 128 columns
-  static constexpr uint32_t kO = 256;        // O: d columns
-  static constexpr uint32_t kP = 384;        // P double buffer: 2 x 64 columns of bf16 pairs
+  static constexpr uint32_t kS = 0;          // kSBuf S buffers of 128 columns (P over S)
+  static constexpr uint32_t kO = kSBuf * 128;  // O: d columns
   static constexpr uint32_t kTmemCols = 512;
 };
 
 static_assert(AttnCfg<128>::kSmem <= 227 * 1024, "attention shared memory above the 227 KB per CTA");
+static_assert(AttnCfg<128>::kO + 128 <= AttnCfg<128>::kTmemCols, "S buffers and O exceed TMEM");
 static_assert(kBN / 2 % 16 == 0, "the half-row max walks 16 columns per step");
 
 // max(a, b, c) in one instruction
@@ -268,16 +273,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sV = smem + Cfg::kV;
   uint8_t* sO = smem + Cfg::kOst;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBar);
-  uint64_t* pv_done = bars + 0;       // [2] per P buffer: O += P V of that buffer done
-  uint64_t* o_final = bars + 2;       // one phase per unit: its last PV landed
-  uint64_t* o_free = bars + 3;        // one phase per unit: O read out (softmax warps)
-  uint64_t* s_full = bars + 4;        // [2] per S buffer
-  uint64_t* p_ready = bars + 6;       // [2] per S buffer (softmax warps)
-  uint64_t* s_free = bars + 8;        // [2] per S buffer: the softmax has read it
-  uint64_t* ofar_full = bars + 10;    // local: the unit's group-partial tile is staged
-  uint64_t* ost_free = bars + 11;     // group, dense: the O stage was stored out (1 arrival)
-  uint64_t* ost_full = bars + 12;     // local/dense: the O stage is written (softmax warps)
-  uint64_t* q_full = bars + 13;       // [kQSlots]
+  uint64_t* pv_done = bars + 0;       // [kSBuf] per S buffer: O += P V from it done
+  uint64_t* o_final = pv_done + kSBuf;  // one phase per unit: its last PV landed
+  uint64_t* o_free = o_final + 1;     // one phase per unit: O read out (softmax warps)
+  uint64_t* s_full = o_free + 1;      // [kSBuf] per S buffer
+  uint64_t* p_ready = s_full + kSBuf; // [kSBuf] per S buffer: P written over S (softmax warps)
+  uint64_t* ofar_full = p_ready + kSBuf;  // local: the unit's group-partial tile is staged
+  uint64_t* ost_free = ofar_full + 1; // group, dense: the O stage was stored out (1 arrival)
+  uint64_t* ost_full = ost_free + 1;  // local/dense: the O stage is written (softmax warps)
+  uint64_t* q_full = ost_full + 1;    // [kQSlots]
   uint64_t* q_empty = q_full + kQSlots;
   uint64_t* k_full = q_empty + kQSlots;   // [kKSlots]
   uint64_t* k_empty = k_full + kKSlots;
@@ -291,17 +295,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = warp_id(), lane = lane_id();
   const int n_units = unit_count<MODE>(a);
   if (threadIdx.x == 0) {
-    mbar_init(&pv_done[0], 1);
-    mbar_init(&pv_done[1], 1);
     mbar_init(o_final, 1);
     mbar_init(o_free, kSoftmaxWarps);
     mbar_init(ofar_full, 1);
     mbar_init(ost_free, 1);
     mbar_init(ost_full, kSoftmaxWarps);
-    for (int x = 0; x < 2; ++x) {
+    for (int x = 0; x < kSBuf; ++x) {
+      mbar_init(&pv_done[x], 1);
       mbar_init(&s_full[x], 1);
       mbar_init(&p_ready[x], kSoftmaxWarps);
-      mbar_init(&s_free[x], kSoftmaxWarps);
     }
     for (int k = 0; k < kQSlots; ++k) {
       mbar_init(&q_full[k], 1);
@@ -514,15 +516,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (u < 0) continue;
           const int nt = U.t1 - U.t0 + 1;
           if (warp == kWarpS) {
-            // S(gg) = Q K^T into S buffer gg&1 once the softmax has read S(gg-2),
-            // the previous content of that buffer; the unit's Q slot is released
-            // after its last S product
+            // S(gg) = Q K^T into S buffer gg % kSBuf once O += P(gg-kSBuf) V is
+            // done (P lies over the buffer's previous S); the unit's Q slot is
+            // released after its last S product
             const int qsl = un % kQSlots;
             if (!mbar_wait_nap(&q_full[qsl], (un / kQSlots) & 1, abort, a.err, a.wait_ns)) break;
             const uint32_t q0 = sw128_desc_lo(smem_u32(sQ + qsl * Cfg::kTile), 16);
             for (int i = 0; i < nt; ++i, ++ck) {
               const int gg = g + i;
-              if (gg >= 2 && !mbar_wait_nap(&s_free[gg & 1], ((gg - 2) >> 1) & 1, abort, a.err, a.wait_ns)) { ok = false; break; }
+              const int sb = gg % kSBuf;
+              if (gg >= kSBuf && !mbar_wait_nap(&pv_done[sb], (gg / kSBuf - 1) & 1, abort, a.err, a.wait_ns)) { ok = false; break; }
               const int sl = ck % kKSlots;
               if (!mbar_wait_nap(&k_full[sl], (ck / kKSlots) & 1, abort, a.err, a.wait_ns)) { ok = false; break; }
               tc_fence_after();
@@ -530,10 +533,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = ((kk >> 2) * Cfg::kChunk + (kk & 3) * 32) >> 4;
-                mma_ss(tmem + Cfg::kS + 128 * (gg & 1), desc_join(q0 + off, dhi), desc_join(b0 + off, dhi),
+                mma_ss(tmem + Cfg::kS + 128 * sb, desc_join(q0 + off, dhi), desc_join(b0 + off, dhi),
                        idS, kk > 0);
               }
-              mma_commit(&s_full[gg & 1]);
+              mma_commit(&s_full[sb]);
               mma_commit(&k_empty[sl]);
             }
             if (!ok) break;
@@ -545,14 +548,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int sl = cv % kVSlots;
               if (!mbar_wait_nap(&v_full[sl], (cv / kVSlots) & 1, abort, a.err, a.wait_ns)) { ok = false; break; }
               if (i == 0 && un > 0 && !mbar_wait_nap(o_free, (un - 1) & 1, abort, a.err, a.wait_ns)) { ok = false; break; }
-              if (!mbar_wait_nap(&p_ready[gg & 1], (gg >> 1) & 1, abort, a.err, a.wait_ns)) { ok = false; break; }
+              const int sb = gg % kSBuf;
+              if (!mbar_wait_nap(&p_ready[sb], (gg / kSBuf) & 1, abort, a.err, a.wait_ns)) { ok = false; break; }
               tc_fence_after();
               const uint32_t vb = vlo + sl * (Cfg::kTile >> 4);
 #pragma unroll
               for (int kk = 0; kk < kBN / 16; ++kk)
-                mma_ts(tmem + Cfg::kO, tmem + Cfg::kP + 64 * (gg & 1) + kk * 8,
+                // keys 16kk..16kk+15 of P(gg): half kk / 4 of the row, packed
+                // into the first 32 columns of that half's 64
+                mma_ts(tmem + Cfg::kO, tmem + Cfg::kS + 128 * sb + 64 * (kk / 4) + 8 * (kk % 4),
                        desc_join(vb + kk * ((16 * 128) >> 4), dhi), idPV, i > 0 || kk > 0);
-              mma_commit(&pv_done[gg & 1]);
+              mma_commit(&pv_done[sb]);
               mma_commit(&v_empty[sl]);
               if (i == nt - 1) mma_commit(o_final);
             }
@@ -761,16 +767,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < nt; ++i) {
         const int gg = g + i;
         const int j0 = (U.t0 + i) * kBN + hf * kHalfS;    // first key of this half
-        const uint32_t tS = tmem + lane_base + Cfg::kS + 128 * (gg & 1) + hf * kHalfS;
-        if (!warp_wait(&s_full[gg & 1], (gg >> 1) & 1, abort, a.err, a.wait_ns)) { ok = false; break; }
+        const int sb = gg % kSBuf;
+        const uint32_t tS = tmem + lane_base + Cfg::kS + 128 * sb + hf * kHalfS;
+        if (!warp_wait(&s_full[sb], (gg / kSBuf) & 1, abort, a.err, a.wait_ns)) { ok = false; break; }
         tc_fence_after();
         // this half of the S row: two 32-column loads in flight, one wait
         uint32_t su[kHalfS];
         tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&su[0]));
         tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&su[32]));
         tmem_wait_ld();
-        tc_fence_before();
-        warp_arrive(&s_free[gg & 1], lane);     // S(gg+2) may now overwrite this buffer
         const bool full = j0 >= lo && j0 + kHalfS - 1 <= hi;
         if (!full) {
 #pragma unroll
@@ -794,12 +799,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float m_new = fmaxf(m_run, mt * sl2);
         const bool need = m_run != -INFINITY && m_new > m_run + kRescaleThreshold;
         if (m_run == -INFINITY) m_run = m_new;      // nothing accumulated yet for this row
-        // O may be rescaled once PV(gg-1) is done.  P buffer b holds P(gg) for
-        // gg = b, b+2, ...; this thread waited for PV(gg-3) before writing
-        // P(gg-1), so pv_done[(gg-1)&1] is at most one phase behind.
+        // O may be rescaled once PV(gg-1) is done.  pv_done[b] completes one
+        // phase per PV from buffer b (gg = b, b + kSBuf, ...); S(gg-1), which
+        // this thread has read, was issued after PV(gg-1-kSBuf), so the
+        // barrier of buffer (gg-1) % kSBuf is at most one phase behind.
         const bool pv_prev = i > 0;
         if (pv_prev && __any_sync(0xffffffffu, need)) {
-          if (!warp_wait(&pv_done[(gg - 1) & 1], ((gg - 1) >> 1) & 1, abort, a.err, a.wait_ns)) { ok = false; break; }
+          const int pb = (gg - 1) % kSBuf;
+          if (!warp_wait(&pv_done[pb], ((gg - 1) / kSBuf) & 1, abort, a.err, a.wait_ns)) { ok = false; break; }
           tc_fence_after();
           const float alpha = need ? ex2f(m_run - m_new) : 1.f;
           uint32_t rr[32];
@@ -818,8 +825,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float mu = m_run == -INFINITY ? 0.f : m_run;
         // p = 2^(s*scale*log2e - m): scale-and-shift in packed pairs, exp2 per
-        // element, four packed partial sums; P is written as bf16 pairs into
-        // this half of P buffer gg&1 once PV(gg-2) has finished reading it
+        // element, four packed partial sums; P is written as bf16 pairs over
+        // the first 32 of this half's 64 S columns, already read above
         const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(-mu, -mu);
         uint64_t acc[4] = {0, 0, 0, 0};
         uint32_t pk[kHalfS / 2];
@@ -831,9 +838,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc[(cc >> 1) & 3] = f2_add(acc[(cc >> 1) & 3], f2_pack(p0, p1));
           pk[cc / 2] = pack_bf16x2(p0, p1);
         }
-        if (gg >= 2 && !warp_wait(&pv_done[gg & 1], ((gg - 2) >> 1) & 1, abort, a.err, a.wait_ns)) { ok = false; break; }
-        tc_fence_after();
-        tmem_st32(tmem + lane_base + Cfg::kP + 64 * (gg & 1) + hf * (kHalfS / 2), pk);
+        tmem_st32(tS, pk);
         {
           const uint64_t s2 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
           float s0, s1;
@@ -842,7 +847,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
         tc_fence_before();
-        warp_arrive(&p_ready[gg & 1], lane);
+        warp_arrive(&p_ready[sb], lane);
       }
       if (!ok) break;
       g += nt;
