@@ -283,8 +283,13 @@ constexpr int kStreamThreads = 192;
 
 template <int NALLOC>
 struct StreamCfg {
-  static constexpr int kStageA = kBM * kBK * 2;            // 16 KB of h
-  static constexpr int kStageB = NALLOC * kBK * 2;         // <= 32 KB of W
+  // 64-column k-slabs per stage: two for narrow projections, so each stage
+  // asks for 256 contiguous bytes of every h row at once
+  static constexpr int kSlabs = NALLOC <= 64 ? 2 : 1;
+  static constexpr int kSlabA = kBM * kBK * 2;             // 16 KB of h per slab
+  static constexpr int kSlabB = NALLOC * kBK * 2;          // <= 32 KB of W per slab
+  static constexpr int kStageA = kSlabs * kSlabA;
+  static constexpr int kStageB = kSlabs * kSlabB;
   static constexpr int kStage = kStageA + kStageB;
   static constexpr int kStages = (200 * 1024 / kStage) < 8 ? (200 * 1024 / kStage) : 8;
   static constexpr int kSmem = kStages * kStage + 1024 /*align*/ + 256 /*barriers*/;
@@ -367,19 +372,24 @@ __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
 
   if (warp == 0) {
     if (lane == 0) {
-      // a tile's R rows of h fill the first R rows of the stage; the MMAs read
+      // a tile's R rows of h fill the first R rows of each slab; the MMAs read
       // all 128, and the accumulator rows past R are never read out
-      const uint32_t bytes = R * kBK * 2 + ncol * kBK * 2;
+      const uint32_t slab_bytes = R * kBK * 2 + ncol * kBK * 2;
+      const int ns = (nk + Cfg::kSlabs - 1) / Cfg::kSlabs;   // stages per tile
       int it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-        for (int kb = 0; kb < nk; ++kb, ++it) {
+        for (int ks = 0; ks < ns; ++ks, ++it) {
           const int s = it % S, u = it / S;
           if (u > 0 && !mbar_wait_nap(&empty[s], (u - 1) & 1, abort, err)) { ok = false; break; }
           uint8_t* sa = smem + s * Cfg::kStage;
-          mbar_expect_tx(&full[s], bytes);
-          tma_load_2d(sa, &tm_h, &full[s], kb * kBK, tile * R);
-          tma_load_2d(sa + Cfg::kStageA, &tm_w, &full[s], kb * kBK, 0);
+          const int nsl = min(Cfg::kSlabs, nk - ks * Cfg::kSlabs);
+          mbar_expect_tx(&full[s], slab_bytes * nsl);
+          for (int j = 0; j < nsl; ++j) {
+            const int kb = ks * Cfg::kSlabs + j;
+            tma_load_2d(sa + j * Cfg::kSlabA, &tm_h, &full[s], kb * kBK, tile * R);
+            tma_load_2d(sa + Cfg::kStageA + j * Cfg::kSlabB, &tm_w, &full[s], kb * kBK, 0);
+          }
         }
       }
       if (*abort || !ok) {
@@ -398,15 +408,20 @@ __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
       for (int tile = blockIdx.x, i = 0; tile < ntiles && ok; tile += gridDim.x, ++i) {
         const int buf = i & 1;
         if (i >= 2 && !mbar_wait_nap(&tfree[buf], ((i >> 1) - 1) & 1, abort, err)) break;
-        for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int ns = (nk + Cfg::kSlabs - 1) / Cfg::kSlabs;
+        for (int ks = 0; ks < ns; ++ks, ++it) {
           const int s = it % S, u = it / S;
           if (!mbar_wait_nap(&full[s], u & 1, abort, err)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + s * Cfg::kStage);
+          const int nsl = min(Cfg::kSlabs, nk - ks * Cfg::kSlabs);
+          for (int j = 0; j < nsl; ++j) {
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            mma_ss(tmem + buf * NALLOC, sw128_desc(sa + kk * 32, 16, 1024),
-                   sw128_desc(sa + Cfg::kStageA + kk * 32, 16, 1024), idn, (kb | kk) != 0);
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              mma_ss(tmem + buf * NALLOC, sw128_desc(sa + j * Cfg::kSlabA + kk * 32, 16, 1024),
+                     sw128_desc(sa + Cfg::kStageA + j * Cfg::kSlabB + kk * 32, 16, 1024), idn,
+                     (ks | j | kk) != 0);
+          }
           mma_commit(&empty[s]);
         }
         if (ok) mma_commit(&tfull[buf]);
