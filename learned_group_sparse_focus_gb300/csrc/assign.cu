@@ -334,7 +334,8 @@ template <int NALLOC, int DG, bool kScores>
 __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
     const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
     const __nv_bfloat16* __restrict__ C, int32_t* __restrict__ gid, float* __restrict__ scores,
-    int B, int n, int D, int K, int A, int topk, int R, int* err) {
+    int B, int n, int D, int K, int A, int topk, int R, int a0, int A_all, int* err) {
+  // this launch covers assignments a0 .. a0 + A - 1 of A_all (W rows from a0 * DG)
   using Cfg = StreamCfg<NALLOC>;
   constexpr int S = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -388,7 +389,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
           for (int j = 0; j < nsl; ++j) {
             const int kb = ks * Cfg::kSlabs + j;
             tma_load_2d(sa + j * Cfg::kSlabA, &tm_h, &full[s], kb * kBK, tile * R);
-            tma_load_2d(sa + Cfg::kStageA + j * Cfg::kSlabB, &tm_w, &full[s], kb * kBK, 0);
+            tma_load_2d(sa + Cfg::kStageA + j * Cfg::kSlabB, &tm_w, &full[s], kb * kBK, a0 * DG);
           }
         }
       }
@@ -454,8 +455,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
           __syncwarp();
           if (lane == 0) mbar_arrive(&tfree[buf]);   // the accumulator may take tile i + 2
         }
-        const __nv_bfloat16* Ca = C + static_cast<size_t>(a) * K * DG;
-        float* srow = kScores && keep ? scores + ((static_cast<size_t>(b) * A + a) * n + ti) * K : nullptr;
+        const __nv_bfloat16* Ca = C + static_cast<size_t>(a0 + a) * K * DG;
+        float* srow = kScores && keep ? scores + ((static_cast<size_t>(b) * A_all + a0 + a) * n + ti) * K : nullptr;
         Top2 t;
         int k = 0;
         for (; k + 4 <= K; k += 4) {
@@ -479,7 +480,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
           }
         }
         if (!kScores && keep) {
-          int32_t* out = gid + ((static_cast<size_t>(b) * A + a) * n + ti) * topk;
+          int32_t* out = gid + ((static_cast<size_t>(b) * A_all + a0 + a) * n + ti) * topk;
           out[0] = t.b1;
           if (topk == 2) out[1] = t.b2;
         }
@@ -497,7 +498,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
 
 template <int NALLOC, int DG>
 cudaError_t launch_stream(const AssignLaunch& L, const CUtensorMap* tm_h, const CUtensorMap* tm_w,
-                          cudaStream_t st) {
+                          int a0, int A_pass, cudaStream_t st) {
   using Cfg = StreamCfg<NALLOC>;
   const int R = L.tile_rows;
   if (R < 1 || R > kBM) return cudaErrorInvalidValue;
@@ -506,19 +507,19 @@ cudaError_t launch_stream(const AssignLaunch& L, const CUtensorMap* tm_h, const 
   const __nv_bfloat16* C = static_cast<const __nv_bfloat16*>(L.C);
   if (L.scores)
     assign_stream_kernel<NALLOC, DG, true><<<grid, kStreamThreads, Cfg::kSmem, st>>>(
-        *tm_h, *tm_w, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk, R, L.err);
+        *tm_h, *tm_w, C, L.gid, L.scores, L.B, L.n, L.D, L.K, A_pass, L.topk, R, a0, L.A, L.err);
   else
     assign_stream_kernel<NALLOC, DG, false><<<grid, kStreamThreads, Cfg::kSmem, st>>>(
-        *tm_h, *tm_w, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk, R, L.err);
+        *tm_h, *tm_w, C, L.gid, L.scores, L.B, L.n, L.D, L.K, A_pass, L.topk, R, a0, L.A, L.err);
   return cudaGetLastError();
 }
 
 template <int NALLOC>
 cudaError_t launch_stream_dg(const AssignLaunch& L, const CUtensorMap* tm_h, const CUtensorMap* tm_w,
-                             cudaStream_t st) {
-  if (L.d_g == 32) return launch_stream<NALLOC, 32>(L, tm_h, tm_w, st);
-  if (L.d_g == 64) return launch_stream<NALLOC, 64>(L, tm_h, tm_w, st);
-  if (L.d_g == 128) return launch_stream<NALLOC, 128>(L, tm_h, tm_w, st);
+                             int a0, int A_pass, cudaStream_t st) {
+  if (L.d_g == 32) return launch_stream<NALLOC, 32>(L, tm_h, tm_w, a0, A_pass, st);
+  if (L.d_g == 64) return launch_stream<NALLOC, 64>(L, tm_h, tm_w, a0, A_pass, st);
+  if (L.d_g == 128) return launch_stream<NALLOC, 128>(L, tm_h, tm_w, a0, A_pass, st);
   return cudaErrorInvalidValue;
 }
 
@@ -568,12 +569,14 @@ cudaError_t launch_assign_f32(const AssignLaunch& L, cudaStream_t st) {
 }
 
 static bool stream_width(int ncol) { return ncol == 32 || ncol == 64 || ncol == 128 || ncol == 256; }
+// wider projections run as passes of 256 columns (whole assignments each)
+static bool stream_passes(int ncol) { return ncol > 256 && ncol % 256 == 0; }
 
 int assign_tile_rows(int tokens, int ncol, int num_sms) {
   // With t tiles per SM the last wave is full when every tile has the same
   // share of the tokens: R = ceil(tokens / (SMs * t)), which lies in (64, 128]
   // for t >= 2.  One tile per SM or less keeps 128-token tiles.
-  if (!stream_width(ncol) || num_sms < 1) return kBM;
+  if (!(stream_width(ncol) || stream_passes(ncol)) || num_sms < 1) return kBM;
   const long long per_wave = static_cast<long long>(num_sms) * kBM;
   if (tokens <= per_wave) return kBM;
   const long long t = (tokens + per_wave - 1) / per_wave;
@@ -585,10 +588,20 @@ cudaError_t launch_assign_bf16(const AssignLaunch& L, const CUtensorMap* tm_h,
                                const CUtensorMap* tm_w, cudaStream_t st) {
   // the persistent kernel loads W in one box per stage: ncol is its exact width
   const int ncol = L.A * L.d_g;
-  if (ncol == 32) return launch_stream_dg<32>(L, tm_h, tm_w, st);
-  if (ncol == 64) return launch_stream_dg<64>(L, tm_h, tm_w, st);
-  if (ncol == 128) return launch_stream_dg<128>(L, tm_h, tm_w, st);
-  if (ncol == 256) return launch_stream_dg<256>(L, tm_h, tm_w, st);
+  if (ncol == 32) return launch_stream_dg<32>(L, tm_h, tm_w, 0, L.A, st);
+  if (ncol == 64) return launch_stream_dg<64>(L, tm_h, tm_w, 0, L.A, st);
+  if (ncol == 128) return launch_stream_dg<128>(L, tm_h, tm_w, 0, L.A, st);
+  if (ncol == 256) return launch_stream_dg<256>(L, tm_h, tm_w, 0, L.A, st);
+  if (stream_passes(ncol)) {
+    // 256 columns (256 / d_g assignments) per pass: h is read once per pass,
+    // and each pass keeps the two-accumulator pipeline of the 256-wide kernel
+    const int per = 256 / L.d_g;
+    for (int a0 = 0; a0 < L.A; a0 += per) {
+      const cudaError_t e = launch_stream_dg<256>(L, tm_h, tm_w, a0, per, st);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
   if (ncol <= 32) return launch_tc<32>(L, tm_h, tm_w, st);
   if (ncol <= 64) return launch_tc<64>(L, tm_h, tm_w, st);
   if (ncol <= 128) return launch_tc<128>(L, tm_h, tm_w, st);

@@ -66,6 +66,7 @@ def _check_index(got, want_idx, want_items, want_order):
     # more tokens than 128 per SM: tiles shrink so every SM gets the same count
     ("bf16", 1, 20000, 256, 64, 16, 1, 1),   # 66-token tiles
     ("bf16", 2, 16500, 128, 32, 8, 2, 2),    # 109-token tiles across the batch boundary
+    ("bf16", 1, 20000, 256, 64, 16, 8, 8),   # 512 columns: two passes of four assignments
     ("f32", 2, 300, 128, 64, 4, 1, 1),
     ("f32", 1, 77, 96, 16, 9, 2, 2),
 ])
