@@ -70,7 +70,8 @@ __all__ = [
     "kept_counts", "attention", "attention_rows", "attention_masked_rows",
     "dense_causal", "lse_merge", "attention_bruteforce", "attention_weights_rows",
     "kv_head", "assignment_of_head",
-    "assign_topk", "build_index_topk", "keep_mask_rows_topk", "attention_rows_topk",
+    "assign_topk", "build_index_topk", "build_index_top2_split", "work_items_top2_split",
+    "keep_mask_rows_topk", "attention_rows_topk",
     "attention_bruteforce_topk", "scores", "sinkhorn", "attention_backward",
     "attention_backward_dq_rows",
 ]
@@ -430,6 +431,99 @@ def build_index_topk(gid, K: int, w: int):
                 other[b, a] = ge[p ^ 1]                       # the token's other membership
     return dict(counts=counts, offsets=offsets, perm=perm, rank=rank,
                 farlen_entry=far_e, farlen_slot=far_s, other=other)
+
+
+def build_index_top2_split(gid, K: int, w: int):
+    """Membership index for top-2 groups that visits every far pair once.
+
+    [FocusJA] 2.2, 3.3: token i sits in both of its groups, and a far pair is
+    kept when the two tokens share a group; a pair whose tokens share both
+    groups is still one kept pair ([FocusKO] 2.3).  Here each kept far pair is
+    counted in the pass of the smaller group the two tokens share (this
+    build's reading of "once").  Memberships (entry e = 2 i + c, group
+    g = gid[i, c], other group o = gid[i, 1 - c]) are sorted by the virtual
+    group v = g * K + o, then by position, so group g's members form K - 1
+    sub-runs (g, o').  For the slot s of an entry with groups (g, o) and each
+    other group o' != g (column j = o' if o' < g else o' - 1):
+      farlen_sub[s, j] = members of sub-run (g, o') at positions <= i - w,
+    except 0 when o' == o and o < g (those tokens share both groups with i,
+    and the pair is counted in group o's pass).
+
+    gid [B, A, n, 2].  Returns arrays with leading dims [B, A]: counts [K*K],
+    offsets [K*K + 1], perm [2n] (slot -> entry), rank [2n], farlen_sub
+    [2n, K - 1] (by slot), farlen_entry [2n] (far keys of each entry over all
+    its sub-runs).
+    """
+    gid = np.asarray(gid)
+    B, A, n, k = gid.shape
+    assert k == 2, "two groups per token"
+    m = 2 * n
+    Kv = K * K
+    counts = np.zeros((B, A, Kv), np.int32)
+    offsets = np.zeros((B, A, Kv + 1), np.int32)
+    perm = np.zeros((B, A, m), np.int32)
+    rank = np.zeros((B, A, m), np.int32)
+    fsub = np.zeros((B, A, m, max(K - 1, 1)), np.int32)
+    fent = np.zeros((B, A, m), np.int32)
+    for b in range(B):
+        for a in range(A):
+            G = gid[b, a].astype(np.int64)
+            assert G.min() >= 0 and G.max() < K, "group id out of range"
+            assert np.all(G[:, 0] != G[:, 1]), "a token's two groups must differ"
+            g_e = G.reshape(m)                        # own group of entry 2i + c
+            o_e = G[:, ::-1].reshape(m)               # the other group
+            v_e = g_e * K + o_e
+            counts[b, a] = np.bincount(v_e, minlength=Kv)
+            offsets[b, a, 1:] = np.cumsum(counts[b, a])
+            p = np.argsort(v_e, kind="stable")        # by (g, o), then entry = position order
+            perm[b, a] = p
+            rank[b, a, p] = np.arange(m)
+            pos_slot = p // 2
+            for s in range(m):
+                e = p[s]
+                g, o, i = int(g_e[e]), int(o_e[e]), int(e // 2)
+                for o2 in range(K):
+                    if o2 == g:
+                        continue
+                    j = o2 if o2 < g else o2 - 1
+                    if o2 == o and o < g:
+                        continue                      # counted in group o's pass
+                    v2 = g * K + o2
+                    lo, hi = offsets[b, a, v2], offsets[b, a, v2 + 1]
+                    fsub[b, a, s, j] = int(np.searchsorted(pos_slot[lo:hi], i - w + 1, side="left"))
+            fent[b, a, p] = fsub[b, a].sum(axis=1)
+    return dict(counts=counts, offsets=offsets, perm=perm, rank=rank,
+                farlen_sub=fsub, farlen_entry=fent)
+
+
+def work_items_top2_split(index: dict, BM: int):
+    """Group-pass work list over the split index, canonical order
+    (b, a, v, row0, j): one candidate per BM slots of each virtual group v and
+    each other-group column j; emitted when the tile's last row has far keys
+    in that sub-run (farlen_sub is non-decreasing inside a sub-run).  Each item
+    is (b, a, v, row0, rows, keys, key0, j): keys = that row's farlen_sub[., j],
+    key0 = the first slot of sub-run (g, o') with o' the j-th group other
+    than g = v // K.
+    """
+    counts, offsets, fs = index["counts"], index["offsets"], index["farlen_sub"]
+    B, A, Kv = counts.shape
+    K = int(round(math.sqrt(Kv)))
+    out = []
+    for b in range(B):
+        for a in range(A):
+            for v in range(Kv):
+                c = int(counts[b, a, v])
+                o = int(offsets[b, a, v])
+                g = v // K
+                for t in range(0, c, BM):
+                    rows = min(BM, c - t)
+                    last = o + t + rows - 1
+                    for j in range(K - 1):
+                        keys = int(fs[b, a, last, j])
+                        if keys > 0:
+                            o2 = j if j < g else j + 1
+                            out.append((b, a, v, o + t, rows, keys, int(offsets[b, a, g * K + o2]), j))
+    return np.array(out, dtype=np.int32).reshape(-1, 8)
 
 
 def keep_mask_rows_topk(G, w: int, rows):

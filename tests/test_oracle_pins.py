@@ -461,6 +461,41 @@ def test_topk_far_count_once_per_pair(K, n, w):
     assert dedup == far_kept
 
 
+@pytest.mark.parametrize("K,n,w", [(2, 50, 3), (3, 120, 5), (4, 200, 7), (5, 150, 1), (4, 100, 1000)])
+def test_top2_split_index_visits_every_far_pair_once(K, n, w):
+    # Brute force over the work list: the (row, key) token pairs that the
+    # items cover, each row taking the first farlen_sub keys of the item's
+    # sub-run, are exactly the far pairs of the top-2 keep mask, once each;
+    # and each token's two entries together hold its far-key count.
+    rng = np.random.default_rng(K * 1000 + n + w)
+    G = np.stack([rng.permutation(K)[:2] for _ in range(n)]).astype(np.int32)[None, None]
+    idx = ref.build_index_top2_split(G, K, w)
+    items = ref.work_items_top2_split(idx, 16)
+    perm, fs = idx["perm"][0, 0], idx["farlen_sub"][0, 0]
+    seen = {}
+    for b, a, v, row0, rows, keys, key0, j in items:
+        assert keys == fs[row0 + rows - 1, j] and keys > 0
+        for s in range(row0, row0 + rows):
+            assert fs[s, j] <= keys
+            for t in range(key0, key0 + fs[s, j]):
+                pr = (int(perm[s]) // 2, int(perm[t]) // 2)
+                seen[pr] = seen.get(pr, 0) + 1
+    M = ref.keep_mask_rows_topk(G[0, 0], w, np.arange(n))
+    ii, jj = np.nonzero(M)
+    want = {(int(i), int(j)) for i, j in zip(ii, jj) if i - j >= w}
+    assert set(seen) == want
+    assert all(c == 1 for c in seen.values())
+    per_tok = idx["farlen_entry"][0, 0].reshape(n, 2).sum(axis=1)
+    assert np.array_equal(per_tok, np.bincount(ii[ii - jj >= w], minlength=n))
+    # the sort: virtual group v = g * K + o, then position
+    ge = G[0, 0].reshape(-1)
+    oe = G[0, 0][:, ::-1].reshape(-1)
+    vs = (ge * K + oe)[perm]
+    assert np.all(np.diff(vs) >= 0)
+    same = np.diff(vs) == 0
+    assert np.all(np.diff(perm // 2)[same] > 0)
+
+
 def test_topk_reduces_to_dense_and_to_top1():
     rng = np.random.default_rng(22)
     B, H, Hkv, n, d = 1, 4, 2, 83, 8
