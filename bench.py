@@ -519,10 +519,11 @@ def run_ours_topk(args, wl, world, rank, local):
     if st != 0:
         raise RuntimeError(f"device error status {st}")
     # far pairs per assignment: entry far keys (a key sharing both groups
-    # counted twice) minus pair far keys (those keys once more)
-    ent = fz.index_views(p, idx.entry, ws, n=wl.n * k)
+    # counted twice) minus pair far keys (those keys once more); the split
+    # index (K <= 8) counts every far pair once and has no pair index
+    ent = fz.index_views(p, idx.entry, ws, n=wl.n * k, K=wl.K * wl.K if idx.split else wl.K)
     far_e = ent["farlen_tok"].to(torch.int64).sum(dim=2).cpu().numpy()       # [B, A]
-    if k == 2:
+    if k == 2 and not idx.split:
         pv = fz.index_views(p, idx.pair, ws, K=wl.K * (wl.K - 1) // 2)
         far_p = pv["farlen_tok"].to(torch.int64).sum(dim=2).cpu().numpy()
     else:
@@ -632,6 +633,7 @@ def run_ours_topk(args, wl, world, rank, local):
                    **{kk: getattr(wl, kk) for kk in ("B", "H", "H_kv", "n", "d", "D", "d_g", "K", "w", "A")},
                    "kept_pairs": kept, "kept_density_vs_causal": kept / (wl.B * wl.H * wl.n * (wl.n + 1) / 2),
                    "far_pairs_entry_pass": ent_pairs, "far_pairs_pair_pass": pair_pairs,
+                   "topk_index": "split (each far pair once)" if idx.split else "entry + pair",
                    "l2": "flushed (256 MB write) before every timed step; flush not timed",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "ms_breakdown": t, "ms_dense_causal": t_dense, "speedup_vs_dense": t_dense / t_step,

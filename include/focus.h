@@ -59,7 +59,7 @@
 extern "C" {
 #endif
 
-#define FOCUS_ABI_VERSION 2   /* 2: adds the top-k membership calls */
+#define FOCUS_ABI_VERSION 3   /* 2: adds the top-k membership calls; 3: the split top-2 index layout */
 
 #if defined(__GNUC__)
 #define FOCUS_API __attribute__((visibility("default")))
@@ -289,14 +289,26 @@ FOCUS_API focus_status_t focus_layer_fwd_host(const focus_params_t* p,
  *   pair_gid   k = 2: [B*A][n] pair id per token.
  *   far_tok    [B*A][n] 1 if token i has any far key, else 0.
  * k = 2 needs K (K - 1) / 2 <= FOCUS_MAX_K (K <= 91), else
- * FOCUS_ERR_UNSUPPORTED. */
+ * FOCUS_ERR_UNSUPPORTED.
+ *
+ * Split layout (k = 2, K <= 8 and bf16 tensors; split = 1): no pair index.  The entry index
+ * sorts the entries by virtual group v = g * K + o (g the entry's group, o the
+ * token's other group), then by position, so counts/offsets have K * K (+1)
+ * entries and each group g splits into K - 1 sub-runs (g, o').  farlen_sub
+ * [B*A][2n][K-1] (by slot, column j = o' - (o' > g)) holds the slot's far
+ * members in sub-run (g, o'), 0 for o' = o when o < g: a pair of tokens that
+ * share both groups is visited once, in the smaller group's pass.  farlen_tok
+ * and farlen_slot hold each entry's / slot's total over its sub-runs, and the
+ * work list has one item per (row tile, sub-run): item.g = v, item.pad = j,
+ * key0 = the sub-run's first slot. */
 typedef struct {
   focus_index_t entry;
   focus_index_t pair;
   int32_t* pair_gid;
   int32_t* far_tok;
   int32_t k;
-  int32_t pad;
+  int32_t split;         /* 1: split layout (see above), 0: entry + pair */
+  int32_t* farlen_sub;   /* split layout only, else NULL */
 } focus_index_topk_t;
 
 /* Bytes of device workspace the top-k calls need for problem p and k (0 if p
@@ -314,7 +326,8 @@ FOCUS_API focus_status_t focus_assign_topk(const focus_params_t* p, int32_t k, c
 
 /* Top-k index: the entry index (stable counting sort of the n*k entries by
  * (group, entry), i.e. by (group, position)), farlen per entry and slot and
- * the work list; for k = 2 also the pair ids, the pair index and far_tok.
+ * the work list; for k = 2 also the pair ids, the pair index and far_tok, or
+ * for K <= 8 with bf16 tensors the split layout above.
  * gid [B, A, n, k] int32 device input; a token's k ids must differ.  A gid
  * outside [0, K), or two equal ids of one token, is clamped or refiled for
  * safety and flagged as FOCUS_ERR_BAD_GROUP_ID in the device error word.
@@ -328,8 +341,9 @@ FOCUS_API focus_status_t focus_build_index_topk(const focus_params_t* p, int32_t
  * as focus_attention_fwd; idx from focus_build_index_topk with the same p and
  * ws.  Runs: the group pass over entries (one partial per entry), for k = 2 a
  * group pass over pair ids and a merge that combines each token's two entry
- * partials minus its pair partial by log-sum-exp, then the local pass that
- * merges the far partial with the window keys. */
+ * partials minus its pair partial by log-sum-exp (split layout: no pair pass,
+ * the merge adds the two entry partials), then the local pass that merges the
+ * far partial with the window keys. */
 FOCUS_API focus_status_t focus_attention_topk_fwd(const focus_params_t* p, const void* Q,
                                                   const void* K, const void* V,
                                                   const focus_index_topk_t* idx, void* O,

@@ -186,11 +186,24 @@ struct IndexRegions {
 
 struct LayoutTopk {
   size_t err, pair_gid, far_any, Ks, Vs, O_e, lse_e, O_p, lse_p, O_far, lse_far, total;
+  size_t vgid, far_sub;   // split index: virtual group ids, far prefix per (slot, sub-run)
   IndexRegions ent, pair;
   int k, m, Kp;
+  bool split;
 };
 
 int pair_count(int K) { return K * (K - 1) / 2; }
+
+// Top-2 with few groups and bf16 tensors uses the split index (memberships
+// sorted by (group, other group, position)): it visits every far pair once,
+// where the entry and pair indices visit pairs that share both groups twice
+// and subtract them once.  A row tile walks the K - 1 sub-runs of its group,
+// so the split pays for small K, where shared pairs are common (1 in 6 at
+// K = 4).  The fp32 path keeps the entry and pair indices.
+constexpr int kSplitMaxK = 8;
+bool split_topk(const focus_params_t* p, int k) {
+  return k == 2 && p->K <= kSplitMaxK && p->dtype == FOCUS_BF16;
+}
 
 bool topk_ok(const focus_params_t* p, int k) {
   if (!params_ok(p) || !(k == 1 || k == 2)) return false;
@@ -204,16 +217,18 @@ LayoutTopk layout_topk(const focus_params_t* p, int k) {
   const size_t n = p->n;
   L.k = k;
   L.m = p->n * k;
-  L.Kp = k == 2 ? pair_count(p->K) : 0;
+  L.split = split_topk(p, k);
+  L.Kp = k == 2 && !L.split ? pair_count(p->K) : 0;
   size_t o = 0;
   auto take = [&](size_t bytes) {
     size_t at = o;
     o = align_up(o + bytes);
     return at;
   };
-  auto take_index = [&](IndexRegions& R, size_t m, size_t K) {
+  // mult: work items per row tile (the split index: one per key sub-run)
+  auto take_index = [&](IndexRegions& R, size_t m, size_t K, size_t mult) {
     R.nseg = static_cast<int>((m + kIndexSeg - 1) / kIndexSeg);
-    R.max_items = static_cast<int>(P * ((m + kTileM - 1) / kTileM + (K < m ? K : m)));
+    R.max_items = static_cast<int>(P * ((m + kTileM - 1) / kTileM + (K < m ? K : m)) * mult);
     R.segcnt = take(P * R.nseg * K * 4);
     R.counts = take(P * K * 4);
     R.offsets = take(P * (K + 1) * 4);
@@ -228,11 +243,19 @@ LayoutTopk layout_topk(const focus_params_t* p, int k) {
     R.n_items = take(4);
   };
   L.err = take(kAlign);
-  take_index(L.ent, static_cast<size_t>(L.m), p->K);
-  if (k == 2) {
-    take_index(L.pair, n, L.Kp);
-    L.pair_gid = take(P * n * 4);
+  if (L.split) {
+    const size_t K = p->K;
+    take_index(L.ent, static_cast<size_t>(L.m), K * K, 1);
+    L.vgid = take(P * L.m * 4);
+    L.far_sub = take(P * L.m * (K - 1) * 4);
     L.far_any = take(P * n * 4);
+  } else {
+    take_index(L.ent, static_cast<size_t>(L.m), p->K, 1);
+    if (k == 2) {
+      take_index(L.pair, n, L.Kp, 1);
+      L.pair_gid = take(P * n * 4);
+      L.far_any = take(P * n * 4);
+    }
   }
   const size_t es = elt_size(p->dtype);
   const size_t qplanes = static_cast<size_t>(p->B) * p->H;
@@ -244,8 +267,10 @@ LayoutTopk layout_topk(const focus_params_t* p, int k) {
     // scatter sends rows past an item's end to
     L.O_e = take((qplanes * L.m + kTileM) * p->d * es);
     L.lse_e = take(qplanes * L.m * 4);
-    L.O_p = take((qplanes * n + kTileM) * p->d * es);
-    L.lse_p = take(qplanes * n * 4);
+    if (!L.split) {
+      L.O_p = take((qplanes * n + kTileM) * p->d * es);
+      L.lse_p = take(qplanes * n * 4);
+    }
   }
   L.O_far = take((qplanes * n + kTileM) * p->d * es);
   L.lse_far = take(qplanes * n * 4);
@@ -728,11 +753,26 @@ focus_status_t focus_build_index_topk(const focus_params_t* p, int32_t k, const 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int P = p->B * p->A, w_eff = p->w > 1 ? p->w : 1;
   int* err = at<int>(ws, L.err);
+  focus_index_topk_t out{};
+  out.k = k;
+  if (L.split) {
+    int32_t* vg = at<int32_t>(ws, L.vgid);
+    int32_t* fsub = at<int32_t>(ws, L.far_sub);
+    int32_t* fa = at<int32_t>(ws, L.far_any);
+    if (launch_split_ids(gid, P, p->n, p->K, vg, err, st) != cudaSuccess) return FOCUS_ERR_CUDA;
+    const IndexLaunch ie = index_launch(ws, L.ent, vg, P, p->A, L.m, p->K * p->K, w_eff, 1, err);
+    if (launch_build_index_split(ie, p->K, fsub, st) != cudaSuccess) return FOCUS_ERR_CUDA;
+    if (launch_far_any(ie.farlen_tok, P, p->n, fa, st) != cudaSuccess) return FOCUS_ERR_CUDA;
+    index_out(ie, &out.entry);
+    out.split = 1;
+    out.farlen_sub = fsub;
+    out.far_tok = fa;
+    *idx_out = out;
+    return FOCUS_OK;
+  }
   const IndexLaunch ie = index_launch(ws, L.ent, gid, P, p->A, L.m, p->K, w_eff, k == 2 ? 1 : 0, err);
   if (launch_build_index(ie, st) != cudaSuccess) return FOCUS_ERR_CUDA;
-  focus_index_topk_t out{};
   index_out(ie, &out.entry);
-  out.k = k;
   if (k == 2) {
     int32_t* pg = at<int32_t>(ws, L.pair_gid);
     int32_t* fa = at<int32_t>(ws, L.far_any);
@@ -762,7 +802,9 @@ focus_status_t focus_attention_topk_fwd_timed(const focus_params_t* p, const voi
   if (!index_ok(idx->entry) || !idx->far_tok || idx->entry.max_items != L.ent.max_items ||
       idx->entry.w_eff != w_eff)
     return FOCUS_ERR_INVALID_ARG;
-  if (k == 2 && (!index_ok(idx->pair) || idx->pair.max_items != L.pair.max_items || idx->pair.w_eff != w_eff))
+  if ((idx->split != 0) != L.split || (L.split && !idx->farlen_sub)) return FOCUS_ERR_INVALID_ARG;
+  if (k == 2 && !L.split &&
+      (!index_ok(idx->pair) || idx->pair.max_items != L.pair.max_items || idx->pair.w_eff != w_eff))
     return FOCUS_ERR_INVALID_ARG;
   if (!Q || !K || !V || !O || !aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) ||
       (lse_opt && !aligned16(lse_opt)))
@@ -791,21 +833,28 @@ focus_status_t focus_attention_topk_fwd_timed(const focus_params_t* p, const voi
   float* lse_p = at<float>(ws, L.lse_p);
   AttnArgs ge = base;
   group_args(ge, idx->entry, L.m, k == 2 ? 1 : 0, O_e, lse_e);
+  if (L.split) {
+    ge.farlen_sub = idx->farlen_sub;
+    ge.nsub = p->K - 1;
+    ge.offsets = idx->entry.offsets;
+  }
+  // the pair pass subtracts the pairs the entry pass visits twice; the split
+  // index visits none twice
+  const bool pair_pass = k == 2 && !L.split;
   AttnArgs gp = base;
-  if (k == 2) group_args(gp, idx->pair, p->n, 0, O_p, lse_p);
+  if (pair_pass) group_args(gp, idx->pair, p->n, 0, O_p, lse_p);
   AttnArgs lo = base;
   lo.farlen_tok = idx->far_tok;
-  MergeLaunch ml{O_e, lse_e, O_p, lse_p, idx->entry.farlen_tok, idx->pair.farlen_tok, O_far, lse_far,
+  MergeLaunch ml{O_e, lse_e, pair_pass ? O_p : nullptr, pair_pass ? lse_p : nullptr, idx->entry.farlen_tok,
+                 pair_pass ? idx->pair.farlen_tok : nullptr, O_far, lse_far,
                  p->B, p->H, p->H_kv, p->A, p->n, p->d};
   cudaError_t e = mark(0);
   if (p->dtype == FOCUS_F32) {
     if (e == cudaSuccess) e = mark(1);
     if (e == cudaSuccess) e = launch_attn_simt_f32(ge, p->d, kModeGroup, L.ent.max_items, st);
     if (e == cudaSuccess) e = mark(2);
-    if (k == 2) {
-      if (e == cudaSuccess) e = launch_attn_simt_f32(gp, p->d, kModeGroup, L.pair.max_items, st);
-      if (e == cudaSuccess) e = launch_topk_merge(ml, p->dtype, st);
-    }
+    if (pair_pass && e == cudaSuccess) e = launch_attn_simt_f32(gp, p->d, kModeGroup, L.pair.max_items, st);
+    if (k == 2 && e == cudaSuccess) e = launch_topk_merge(ml, p->dtype, st);
     if (e == cudaSuccess) e = mark(3);
     if (e == cudaSuccess) e = launch_attn_simt_f32(lo, p->d, kModeLocal, 0, st);
     if (e == cudaSuccess) e = mark(4);
@@ -824,9 +873,11 @@ focus_status_t focus_attention_topk_fwd_timed(const focus_params_t* p, const voi
       !make_map(&tks, Ks, p->d, L.m, planes, 128, 3) || !make_map(&tvs, Vs, p->d, L.m, planes, 128, 3) ||
       !make_map(&tofs, O_e, p->d, qplanes * L.m + kTileM, 1, 1, 2))
     return FOCUS_ERR_CUDA;
-  e = launch_attn_tc_bf16(ge, &tqg, &tks, &tvs, &tofs, &tofs, p->d, kModeGroup, L.ent.max_items, sms, st);
+  e = launch_attn_tc_bf16(ge, &tqg, &tks, &tvs, &tofs, &tofs, p->d, L.split ? kModeGroupSplit : kModeGroup,
+                          L.ent.max_items, sms, st);
   if (e == cudaSuccess) e = mark(2);
-  if (e == cudaSuccess && k == 2) {
+  if (e == cudaSuccess && k == 2 && !pair_pass) e = launch_topk_merge(ml, p->dtype, st);
+  if (e == cudaSuccess && pair_pass) {
     // pair pass over the same K/V buffers, re-sorted by pair (the entry pass
     // is done with them: same stream)
     CUtensorMap pks, pvs, pofs;

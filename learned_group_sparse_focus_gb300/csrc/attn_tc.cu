@@ -150,11 +150,45 @@ struct Unit {
   int b, h, prob, zkv, zq, ybase;
   int row0, nrows;
   int t0, t1;   // inclusive key-tile range
+  int sub;      // group pass over a split top-2 index: the key sub-run's column
+  int grp;      // split index: the rows' group g (virtual group v = g * K + o)
+};
+
+// Split top-2 index: a unit's keys are the sub-runs (g, o') of its group in
+// increasing o' (column j = o' - (o' > g)), each up to the far prefix of the
+// unit's last row; empty ones are skipped.  The walk gives, tile by tile, the
+// column, the tile within it and the sub-run's first slot.
+struct SegWalk {
+  int j, tt, nt, key0;
+  __device__ __forceinline__ void next_col(const AttnArgs& a, const Unit& U) {
+    const int K = a.nsub + 1;
+    const int32_t* last = a.farlen_sub + (static_cast<size_t>(U.prob) * a.m + U.row0 + U.nrows - 1) * a.nsub;
+    for (++j; j < a.nsub; ++j) {
+      const int keys = last[j];
+      if (keys > 0) {
+        const int o2 = j < U.grp ? j : j + 1;
+        nt = (keys + kBN - 1) / kBN;
+        tt = 0;
+        key0 = a.offsets[static_cast<size_t>(U.prob) * (K * K + 1) + U.grp * K + o2];
+        return;
+      }
+    }
+  }
+  __device__ __forceinline__ void begin(const AttnArgs& a, const Unit& U) {
+    j = -1;
+    next_col(a, U);
+  }
+  // true when the next tile starts a new column
+  __device__ __forceinline__ bool step(const AttnArgs& a, const Unit& U) {
+    if (++tt < nt) return false;
+    next_col(a, U);
+    return true;
+  }
 };
 
 template <int MODE>
 __device__ __forceinline__ int unit_count(const AttnArgs& a) {
-  if (MODE == kModeGroup) {
+  if (is_group_mode(MODE)) {
     const int hpa = a.A == 1 ? a.H : a.H / a.H_kv;
     return *a.n_items * hpa;
   }
@@ -164,7 +198,7 @@ __device__ __forceinline__ int unit_count(const AttnArgs& a) {
 template <int MODE>
 __device__ __forceinline__ void decode_unit(const AttnArgs& a, int u, const focus_item_t& it, Unit& U) {
   int kv, asg;
-  if (MODE == kModeGroup) {
+  if (is_group_mode(MODE)) {
     const int hpa = a.A == 1 ? a.H : a.H / a.H_kv;
     const int y = u % hpa;
     U.b = it.b;
@@ -176,6 +210,18 @@ __device__ __forceinline__ void decode_unit(const AttnArgs& a, int u, const focu
     U.t0 = 0;
     U.t1 = (it.keys + kBN - 1) / kBN - 1;
     U.ybase = it.key0;
+    U.sub = it.pad;
+    U.grp = 0;
+    if (MODE == kModeGroupSplit) {
+      // tiles = the sub-runs' tiles, each rounded up on its own
+      const int K = a.nsub + 1;
+      U.grp = it.g / K;
+      const int32_t* last = a.farlen_sub +
+                            (static_cast<size_t>(it.b * a.A + it.a) * a.m + it.row0 + it.rows - 1) * a.nsub;
+      int nt = 0;
+      for (int j = 0; j < a.nsub; ++j) nt += (last[j] + kBN - 1) / kBN;
+      U.t1 = nt - 1;
+    }
   } else {
     U.h = u % a.H;
     const int r = u / a.H;
@@ -189,6 +235,8 @@ __device__ __forceinline__ void decode_unit(const AttnArgs& a, int u, const focu
     U.t0 = max(0, U.row0 - a.w + 1) / kBN;
     U.t1 = (U.row0 + U.nrows - 1) / kBN;
     U.ybase = 0;
+    U.sub = 0;
+    U.grp = 0;
   }
   U.prob = U.b * a.A + asg;
   U.zkv = U.b * a.H_kv + kv;
@@ -218,7 +266,7 @@ struct UnitWalk {
   __device__ __forceinline__ void begin(const AttnArgs& a, int n) {
     n_units = n;
     hpa = a.A == 1 ? a.H : a.H / a.H_kv;
-    if (MODE == kModeGroup) {
+    if (is_group_mode(MODE)) {
       const int u0 = snake_unit(0, n), u1 = snake_unit(1, n);
       if (u0 >= 0) nxt = a.items[a.order[u0 / hpa]];
       ord = u1 >= 0 ? a.order[u1 / hpa] : 0;
@@ -228,7 +276,7 @@ struct UnitWalk {
   // decoded into U when there is one.
   __device__ __forceinline__ int step(const AttnArgs& a, int k, Unit& U) {
     const int u = snake_unit(k, n_units);
-    if (MODE == kModeGroup) {
+    if (is_group_mode(MODE)) {
       const focus_item_t it = nxt;
       if (snake_unit(k + 1, n_units) >= 0) nxt = a.items[ord];
       const int u2 = snake_unit(k + 2, n_units);
@@ -353,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* dst = sQ + sl * Cfg::kTile;
           if (a.hold_first_q && qn == 0) {
             // test hook: this tile is never requested, so its wait runs out
-          } else if (MODE == kModeGroup) {
+          } else if (is_group_mode(MODE)) {
             // TMA row gather through perm: lane l fetches tile rows 4l..4l+3 of every
             // 64-column slab (tm_q is a 2-D {d, B*H*n} view with one-row boxes);
             // rows past the item repeat its first row, whose scores are all masked
@@ -380,14 +428,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++qn;
         }
         if (lane == 0) {
+          SegWalk sw;
+          if (MODE == kModeGroupSplit) sw.begin(a, U);
           for (int t = U.t0; t <= U.t1; ++t, ++ck) {
             const int sl = ck % kKSlots, use = ck / kKSlots;
             if (use > 0 && !mbar_wait_nap(&k_empty[sl], (use - 1) & 1, abort, a.err, a.wait_ns)) { ok = false; break; }
+            const int krow = MODE == kModeGroupSplit ? sw.key0 + sw.tt * kBN : U.ybase + t * kBN;
             mbar_expect_tx(&k_full[sl], Cfg::kTile);
 #pragma unroll
             for (int ch = 0; ch < kChunks; ++ch)
-              tma_load_3d(sK + sl * Cfg::kTile + ch * Cfg::kChunk, &tm_k, &k_full[sl], ch * 64,
-                          U.ybase + t * kBN, U.zkv);
+              tma_load_3d(sK + sl * Cfg::kTile + ch * Cfg::kChunk, &tm_k, &k_full[sl], ch * 64, krow, U.zkv);
+            if (MODE == kModeGroupSplit) sw.step(a, U);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort;
@@ -421,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int prow0 = 0, pzq = 0;  // the previous unit's tile
         auto store_prev = [&]() -> bool {
           if (!mbar_wait_nap(ost_full, (un - 1) & 1, abort, a.err, a.wait_ns)) return false;
-          if (MODE == kModeGroup) {
+          if (is_group_mode(MODE)) {
             // four rows per scatter, one 64-column slab at a time
 #pragma unroll 4
             for (int q4 = 0; q4 < 32; ++q4) {
@@ -447,14 +498,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int u = walk.step(a, k, U);
           if (u == -1) break;
           if (u < 0) continue;
+          SegWalk sw;
+          if (MODE == kModeGroupSplit) sw.begin(a, U);
           for (int t = U.t0, i = 0; t <= U.t1; ++t, ++cv, ++i) {
             const int sl = cv % kVSlots, use = cv / kVSlots;
             if (use > 0 && !mbar_wait_nap(&v_empty[sl], (use - 1) & 1, abort, a.err, a.wait_ns)) { ok = false; break; }
+            const int vrow = MODE == kModeGroupSplit ? sw.key0 + sw.tt * kBN : U.ybase + t * kBN;
             mbar_expect_tx(&v_full[sl], Cfg::kTile);
 #pragma unroll
             for (int ch = 0; ch < kChunks; ++ch)
-              tma_load_3d(sV + sl * Cfg::kTile + ch * Cfg::kChunk, &tm_v, &v_full[sl], ch * 64,
-                          U.ybase + t * kBN, U.zkv);
+              tma_load_3d(sV + sl * Cfg::kTile + ch * Cfg::kChunk, &tm_v, &v_full[sl], ch * 64, vrow, U.zkv);
+            if (MODE == kModeGroupSplit) sw.step(a, U);
             // after this unit's first V tiles: the previous unit's O, whose
             // epilogue runs at the start of this unit, then this unit's partial
             if (i == min(1, U.t1 - U.t0)) {
@@ -630,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         c2 = e2 / den;
         lse2 = mm + log2f(den);
       }
-      if (MODE == kModeGroup) {
+      if (is_group_mode(MODE)) {
         // rows are scattered by perm: the tile is staged in shared memory with
         // each row's O_far row index (rows past the item go to the spare rows
         // after the last plane), and the V load warp scatters it with TMA once
@@ -734,12 +788,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       st.far = false;
       int lo = 1, hi = 0;
       st.pos = -1;
-      if (MODE == kModeGroup) {
+      if (is_group_mode(MODE)) {
         if (st.valid) {
           const size_t sidx = static_cast<size_t>(U.prob) * a.m + U.row0 + r;
           st.pos = a.perm[sidx];       // the row's item: O_far row within the head
           lo = 0;
-          hi = a.farlen_slot[sidx] - 1;
+          // split top-2 index: the row's far prefix per key sub-run, read as
+          // the tile loop enters each sub-run
+          if (MODE == kModeGroup) hi = (a.farlen_sub ? a.farlen_sub[sidx * a.nsub + U.sub] : a.farlen_slot[sidx]) - 1;
         }
       } else if (st.valid) {
         st.pos = U.row0 + r;
@@ -764,9 +820,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 3. this unit's key tiles
       float m_run = -INFINITY, l = 0.f;
       const int nt = U.t1 - U.t0 + 1;
+      SegWalk sw;
+      bool new_col = true;
+      if (MODE == kModeGroupSplit) sw.begin(a, U);
       for (int i = 0; i < nt; ++i) {
         const int gg = g + i;
-        const int j0 = (U.t0 + i) * kBN + hf * kHalfS;    // first key of this half
+        if (MODE == kModeGroupSplit && new_col) {
+          // entering a sub-run: this row's far prefix in it
+          hi = st.valid ? a.farlen_sub[(static_cast<size_t>(U.prob) * a.m + U.row0 + r) * a.nsub + sw.j] - 1 : -1;
+        }
+        // first key of this half (split index: within the current sub-run)
+        const int j0 = (MODE == kModeGroupSplit ? sw.tt : U.t0 + i) * kBN + hf * kHalfS;
+        if (MODE == kModeGroupSplit) new_col = sw.step(a, U);
         const int sb = gg % kSBuf;
         const uint32_t tS = tmem + lane_base + Cfg::kS + 128 * sb + hf * kHalfS;
         if (!warp_wait(&s_full[sb], (gg / kSBuf) & 1, abort, a.err, a.wait_ns)) { ok = false; break; }
@@ -901,7 +966,7 @@ cudaError_t launch_d(const AttnArgs& a, const CUtensorMap* tm_q, const CUtensorM
                      int max_items, int num_sms, cudaStream_t st) {
   using Cfg = AttnCfg<D>;
   long long units;
-  if (mode == kModeGroup) {
+  if (is_group_mode(mode)) {
     const int hpa = a.A == 1 ? a.H : a.H / a.H_kv;
     units = static_cast<long long>(max_items) * hpa;
   } else {
@@ -911,6 +976,8 @@ cudaError_t launch_d(const AttnArgs& a, const CUtensorMap* tm_q, const CUtensorM
   const unsigned grid = static_cast<unsigned>(units < num_sms ? units : num_sms);
   if (mode == kModeGroup)
     attn_tc_kernel<D, kModeGroup><<<grid, kThreads, Cfg::kSmem, st>>>(*tm_q, *tm_k, *tm_v, *tm_o, *tm_of, a);
+  else if (mode == kModeGroupSplit)
+    attn_tc_kernel<D, kModeGroupSplit><<<grid, kThreads, Cfg::kSmem, st>>>(*tm_q, *tm_k, *tm_v, *tm_o, *tm_of, a);
   else if (mode == kModeLocal)
     attn_tc_kernel<D, kModeLocal><<<grid, kThreads, Cfg::kSmem, st>>>(*tm_q, *tm_k, *tm_v, *tm_o, *tm_of, a);
   else
@@ -923,6 +990,8 @@ cudaError_t set_smem() {
   using Cfg = AttnCfg<D>;
   cudaError_t e;
   e = cudaFuncSetAttribute(attn_tc_kernel<D, kModeGroup>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(attn_tc_kernel<D, kModeGroupSplit>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(attn_tc_kernel<D, kModeLocal>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
   if (e != cudaSuccess) return e;

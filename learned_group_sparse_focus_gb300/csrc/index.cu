@@ -333,7 +333,181 @@ __global__ void __launch_bounds__(1024) index_items_kernel(
   }
 }
 
+// Split top-2 index, far prefixes: for sorted slot s of entry e (token
+// i = e >> 1) in virtual group v = g * K + o, and each other group o' != g
+// (column j = o' - (o' > g)), the members of sub-run (g, o') at positions
+// <= i - w, or 0 when o' == o and o < g (that pair's pass is group o's).
+// m = 2n slots per problem; Kv = K * K virtual groups.
+__global__ void __launch_bounds__(256) index_farlen_split_kernel(int m, int K, int w_eff,
+                                                                 const int32_t* __restrict__ offsets,
+                                                                 const int32_t* __restrict__ perm,
+                                                                 int32_t* __restrict__ farlen_sub,
+                                                                 int32_t* __restrict__ farlen_tok,
+                                                                 int32_t* __restrict__ farlen_slot) {
+  extern __shared__ int offs[];  // K * K + 1
+  const int p = blockIdx.y;
+  const int Kv = K * K;
+  const int32_t* op = offsets + static_cast<size_t>(p) * (Kv + 1);
+  for (int v = threadIdx.x; v <= Kv; v += blockDim.x) offs[v] = op[v];
+  __syncthreads();
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= m) return;
+  const int32_t* pp = perm + static_cast<size_t>(p) * m;
+  const int e = pp[s];
+  const int pos = e >> 1;
+  const int v = upper_bound_minus1(offs, Kv, s);
+  const int g = v / K, o = v - g * K;
+  const int target = pos - w_eff + 1;   // count members with position < target
+  int32_t* fs = farlen_sub + (static_cast<size_t>(p) * m + s) * (K - 1);
+  int total = 0;
+  for (int o2 = 0; o2 < K; ++o2) {
+    if (o2 == g) continue;
+    const int j = o2 < g ? o2 : o2 - 1;
+    int fl = 0;
+    if (!(o2 == o && o < g)) {
+      const int v2 = g * K + o2;
+      int lo = offs[v2], hi = offs[v2 + 1];    // first slot whose position >= target
+      const int base = lo;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if ((__ldg(pp + mid) >> 1) < target) lo = mid + 1; else hi = mid;
+      }
+      fl = lo - base;
+    }
+    fs[j] = fl;
+    total += fl;
+  }
+  farlen_slot[static_cast<size_t>(p) * m + s] = total;
+  farlen_tok[static_cast<size_t>(p) * m + e] = total;
+}
+
+// Split work list: candidates (problem, row tile of a virtual group) in
+// canonical order; an item when the tile's last row has far keys in any of
+// its group's sub-runs (keys = their total, key0 = the group's first slot;
+// the attention kernel walks the sub-runs from offsets and farlen_sub); then
+// the same compaction and longest-first schedule as index_items_kernel.
+// item.g = virtual group.
+__global__ void __launch_bounds__(1024) index_items_split_kernel(
+    int P, int A, int m, int K, const int32_t* __restrict__ counts,
+    const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_base,
+    const int32_t* __restrict__ farlen_sub, focus_item_t* __restrict__ items,
+    int32_t* __restrict__ cost, int32_t* __restrict__ order, int32_t* __restrict__ n_items,
+    int max_items, int* err) {
+  extern __shared__ int sm[];
+  int* pbase = sm;                 // P + 1
+  int* hist = sm + P + 1;          // nb + 1
+  __shared__ int warp_sums[32];
+  const int Kv = K * K, nsub = K - 1;
+  // cost buckets 0..nb-1: a tile's keys over its sub-runs stay below m + K * kTileN
+  const int nb = (m + kTileN - 1) / kTileN + K + 1;
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int p = 0; p < P; ++p) {
+      pbase[p] = run;
+      run += tile_base[static_cast<size_t>(p) * (Kv + 1) + Kv];
+    }
+    pbase[P] = run;
+  }
+  for (int c = threadIdx.x; c < nb; c += blockDim.x) hist[c] = 0;
+  __syncthreads();
+  const int total = pbase[P];
+  int out = 0;
+  for (int c0 = 0; c0 < total; c0 += blockDim.x) {
+    const int c = c0 + threadIdx.x;
+    int flag = 0;
+    focus_item_t it{};
+    if (c < total) {
+      const int p = upper_bound_minus1(pbase, P, c);
+      const int t = c - pbase[p];
+      const int32_t* tb = tile_base + static_cast<size_t>(p) * (Kv + 1);
+      int lo = 0, hi = Kv;        // virtual group of tile t: largest v with tb[v] <= t
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(tb + mid) <= t) lo = mid; else hi = mid;
+      }
+      const int v = lo, g = v / K;
+      const int tt = t - tb[v];
+      const int32_t* op = offsets + static_cast<size_t>(p) * (Kv + 1);
+      const int off = op[v];
+      const int cnt = counts[static_cast<size_t>(p) * Kv + v];
+      it.b = p / A;
+      it.a = p % A;
+      it.g = v;
+      it.row0 = off + tt * kTileM;
+      it.rows = min(kTileM, cnt - tt * kTileM);
+      it.key0 = op[g * K];
+      it.pad = 0;
+      if (it.rows <= 0) {
+        atomicOr(err, kErrInternal);
+      } else {
+        const int32_t* fl = farlen_sub + (static_cast<size_t>(p) * m + it.row0 + it.rows - 1) * nsub;
+        int keys = 0;
+        for (int j = 0; j < nsub; ++j) keys += fl[j];
+        it.keys = keys;
+        flag = keys > 0;
+      }
+    }
+    int tot;
+    const int pos = block_excl_scan(flag, warp_sums, &tot);
+    if (flag && out + pos < max_items) {
+      items[out + pos] = it;
+      const int cb = (it.keys + kTileN - 1) / kTileN;
+      cost[out + pos] = cb;
+      atomicAdd(&hist[cb], 1);
+    }
+    out += tot;
+  }
+  if (out > max_items) {
+    if (threadIdx.x == 0) atomicOr(err, kErrInternal);
+    out = max_items;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int cb = nb - 1; cb >= 0; --cb) {
+      int v = hist[cb];
+      hist[cb] = run;
+      run += v;
+    }
+    *n_items = out;
+  }
+  __syncthreads();
+  if (warp_id() == 0) {
+    const int lane = lane_id();
+    const unsigned lt = (1u << lane) - 1u;
+    for (int c0 = 0; c0 < out; c0 += 32) {
+      const int c = c0 + lane;
+      const int cb = c < out ? cost[c] : -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, cb);
+      if (c < out) order[hist[cb] + __popc(peers & lt)] = c;
+      __syncwarp();
+      if (c < out && lane == __ffs(peers) - 1) hist[cb] += __popc(peers);
+      __syncwarp();
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_build_index_split(const IndexLaunch& L, int K, int32_t* farlen_sub, cudaStream_t st) {
+  const int P = L.P;
+  const int Kv = L.K;            // K * K virtual groups
+  if (K < 2 || Kv != K * K || L.kshift != 1) return cudaErrorInvalidValue;
+  const int nseg = (L.n + kIndexSeg - 1) / kIndexSeg;
+  index_count_kernel<<<dim3(nseg, P), 256, static_cast<size_t>(Kv) * sizeof(int), st>>>(
+      L.gid, L.n, Kv, nseg, L.segcnt, L.err);
+  index_scan_kernel<<<P, 1024, 2 * static_cast<size_t>(Kv) * sizeof(int), st>>>(
+      L.n, Kv, nseg, L.segcnt, L.counts, L.offsets, L.tile_base);
+  index_scatter_kernel<<<dim3(nseg, P), 256, static_cast<size_t>(Kv) * sizeof(int) + 8 * static_cast<size_t>(Kv) * 2,
+                         st>>>(L.gid, L.n, Kv, nseg, L.segcnt, L.perm, L.rank, L.err);
+  index_farlen_split_kernel<<<dim3((L.n + 255) / 256, P), 256, static_cast<size_t>(Kv + 1) * sizeof(int), st>>>(
+      L.n, K, L.w_eff, L.offsets, L.perm, farlen_sub, L.farlen_tok, L.farlen_slot);
+  const int nb = (L.n + kTileN - 1) / kTileN + K + 1;
+  index_items_split_kernel<<<1, 1024, static_cast<size_t>(P + 1 + nb) * sizeof(int), st>>>(
+      P, L.A, L.n, K, L.counts, L.offsets, L.tile_base, farlen_sub, L.items, L.cost, L.order, L.n_items,
+      L.max_items, L.err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_build_index(const IndexLaunch& L, cudaStream_t st) {
   const int P = L.P;
@@ -364,6 +538,9 @@ cudaError_t setup_index_kernels() {
                                        kMaxK * 4 + 8 * kMaxK * 2);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(index_items_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           160 * 1024);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(index_items_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            160 * 1024);
   return e;
 }

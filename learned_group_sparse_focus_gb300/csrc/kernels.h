@@ -86,10 +86,23 @@ struct AttnArgs {
   // runs out and the kernel takes its abort path.
   unsigned long long wait_ns;
   int hold_first_q;
+  // group pass over a top-2 split index: per-row bounds from farlen_sub
+  // [m][nsub] (column = the item's pad) instead of farlen_slot; else null
+  const int32_t* farlen_sub;
+  int nsub;
+  const int32_t* offsets;    // split index: [B*A][K*K + 1] sub-run starts
 };
 
 // index.cu
 cudaError_t launch_build_index(const IndexLaunch& L, cudaStream_t st);
+// Top-2 split index: L describes the 2n entries with their virtual group
+// ids v = g * K + o (L.gid, L.K = K * K, L.kshift = 1); farlen_sub
+// [P][2n][K - 1] receives each slot's far prefix in every sub-run (g, o') of its
+// group, L.farlen_tok / L.farlen_slot the entry's / slot's total, and the work
+// list holds one item per (row tile, sub-run) with item.pad = the sub-run's
+// column.  Each far pair is visited once: in the pass of the smaller group the
+// two tokens share.
+cudaError_t launch_build_index_split(const IndexLaunch& L, int K, int32_t* farlen_sub, cudaStream_t st);
 cudaError_t setup_index_kernels();
 
 // assign.cu
@@ -103,7 +116,10 @@ cudaError_t setup_assign_kernels();
 int assign_tile_rows(int tokens, int ncol, int num_sms);
 
 // attn_simt.cu (fp32 storage, fp32 arithmetic on the CUDA cores)
-enum AttnMode : int { kModeLocal = 0, kModeGroup = 1, kModeDense = 2 };
+// kModeGroupSplit: the group pass over a split top-2 index (each unit walks
+// its row tile's key sub-runs one after another; see launch_build_index_split)
+enum AttnMode : int { kModeLocal = 0, kModeGroup = 1, kModeDense = 2, kModeGroupSplit = 3 };
+__host__ __device__ constexpr bool is_group_mode(int mode) { return mode == kModeGroup || mode == kModeGroupSplit; }
 cudaError_t launch_attn_simt_f32(const AttnArgs& a, int d, int mode, int max_items,
                                  cudaStream_t st);
 
@@ -122,6 +138,9 @@ cudaError_t launch_attn_tc_bf16(const AttnArgs& a, const CUtensorMap* tm_q,
 cudaError_t setup_attn_kernels();
 
 // topk.cu (top-2 membership)
+// vg[p, 2i + c] = g_c * K + g_(1-c) for token i's groups g_0, g_1 (the split
+// index's virtual group ids); equal or out-of-range ids raise kErrBadGroup.
+cudaError_t launch_split_ids(const int32_t* gid2, int P, int n, int K, int32_t* vg, int* err, cudaStream_t st);
 // pair_gid[p, i] = id of token i's two groups {a, b} (a < b) among the
 // K (K - 1) / 2 pairs; equal or out-of-range ids raise kErrBadGroup.
 cudaError_t launch_pair_ids(const int32_t* gid2, int P, int n, int K, int32_t* pair_gid, int* err,

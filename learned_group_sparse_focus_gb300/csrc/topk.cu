@@ -18,6 +18,12 @@
 // The pair keys are a subset of each group's keys, so w_ab <= min(w_a, w_b)
 // and the denominator is at least max(w_a, w_b): it never cancels, and the
 // result's error is at most three roundings of the stored partials.
+//
+// For small K the index can be split instead (memberships sorted by group,
+// then the token's other group, then position): the entry of the larger of
+// two shared groups skips the sub-run of the other one, so every far pair is
+// visited once, there is no pair partial, and the merge is the plain
+// log-sum-exp of the two entry partials.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -40,6 +46,23 @@ __global__ void __launch_bounds__(256) pair_ids_kernel(const int2* __restrict__ 
     }
     // pairs {lo, hi} numbered row by row: (0,1), (0,2), ..., (0,K-1), (1,2), ...
     pair_gid[t] = lo * K - lo * (lo + 1) / 2 + (hi - lo - 1);
+  }
+}
+
+// Virtual group ids of the split index: entry 2i + c of token i with groups
+// (g_0, g_1) gets g_c * K + g_(1-c).
+__global__ void __launch_bounds__(256) split_ids_kernel(const int2* __restrict__ gid2, long long total,
+                                                        int K, int2* __restrict__ vg, int* err) {
+  for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < total;
+       t += static_cast<long long>(gridDim.x) * blockDim.x) {
+    int2 g = __ldg(gid2 + t);
+    if (g.x < 0 || g.x >= K || g.y < 0 || g.y >= K || g.x == g.y) {
+      // not two distinct groups in [0, K): flag it and file the token under
+      // groups 0 and 1 so every later index stays in bounds
+      atomicOr(err, kErrBadGroup);
+      g = make_int2(0, 1);
+    }
+    vg[t] = make_int2(g.x * K + g.y, g.y * K + g.x);
   }
 }
 
@@ -115,8 +138,9 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(MergeLaunch L, long lon
     const bool fa = __ldg(L.farlen_entry + p * m + 2 * i) > 0;
     const bool fb = __ldg(L.farlen_entry + p * m + 2 * i + 1) > 0;
     if (!fa && !fb) continue;            // no far keys: the local pass reads nothing here
-    // a consistent index has pair far keys only where both groups have some
-    const bool fp = fa && fb && __ldg(L.farlen_pair + p * L.n + i) > 0;
+    // a consistent index has pair far keys only where both groups have some;
+    // the split index visits every far pair once and has no pair partial
+    const bool fp = L.farlen_pair != nullptr && fa && fb && __ldg(L.farlen_pair + p * L.n + i) > 0;
     const size_t ea = static_cast<size_t>(zq) * m + 2 * i;
     const size_t tp = static_cast<size_t>(zq) * L.n + i;
     const float la = fa ? __ldg(L.lse_e + ea) : -INFINITY;
@@ -161,6 +185,13 @@ cudaError_t launch_pair_ids(const int32_t* gid2, int P, int n, int K, int32_t* p
   const long long total = static_cast<long long>(P) * n;
   pair_ids_kernel<<<grid_for(total), 256, 0, st>>>(reinterpret_cast<const int2*>(gid2), total, K,
                                                    pair_gid, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_ids(const int32_t* gid2, int P, int n, int K, int32_t* vg, int* err, cudaStream_t st) {
+  const long long total = static_cast<long long>(P) * n;
+  split_ids_kernel<<<grid_for(total), 256, 0, st>>>(reinterpret_cast<const int2*>(gid2), total, K,
+                                                    reinterpret_cast<int2*>(vg), err);
   return cudaGetLastError();
 }
 

@@ -48,7 +48,8 @@ class Index(ctypes.Structure):
 
 class IndexTopk(ctypes.Structure):
     _fields_ = [("entry", Index), ("pair", Index), ("pair_gid", ctypes.c_void_p),
-                ("far_tok", ctypes.c_void_p), ("k", ctypes.c_int32), ("pad", ctypes.c_int32)]
+                ("far_tok", ctypes.c_void_p), ("k", ctypes.c_int32), ("split", ctypes.c_int32),
+                ("farlen_sub", ctypes.c_void_p)]
 
 
 def _load():

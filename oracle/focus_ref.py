@@ -71,6 +71,7 @@ __all__ = [
     "dense_causal", "lse_merge", "attention_bruteforce", "attention_weights_rows",
     "kv_head", "assignment_of_head",
     "assign_topk", "build_index_topk", "build_index_top2_split", "work_items_top2_split",
+    "segments_top2_split",
     "keep_mask_rows_topk", "attention_rows_topk",
     "attention_bruteforce_topk", "scores", "sinkhorn", "attention_backward",
     "attention_backward_dq_rows",
@@ -498,12 +499,14 @@ def build_index_top2_split(gid, K: int, w: int):
 
 def work_items_top2_split(index: dict, BM: int):
     """Group-pass work list over the split index, canonical order
-    (b, a, v, row0, j): one candidate per BM slots of each virtual group v and
-    each other-group column j; emitted when the tile's last row has far keys
-    in that sub-run (farlen_sub is non-decreasing inside a sub-run).  Each item
-    is (b, a, v, row0, rows, keys, key0, j): keys = that row's farlen_sub[., j],
-    key0 = the first slot of sub-run (g, o') with o' the j-th group other
-    than g = v // K.
+    (b, a, v, row0): one candidate per BM slots of each virtual group
+    v = g * K + o.  Its keys are the K - 1 sub-runs (g, o') in increasing o',
+    each up to the far prefix of the tile's last row (farlen_sub is
+    non-decreasing inside a sub-run), the rows' own sub-run left out when
+    o < g; a candidate is emitted when the total is positive.  Each item is
+    (b, a, v, row0, rows, keys, key0, 0): keys = the total over the sub-runs,
+    key0 = the first slot of group g.  segments(index, item) gives the
+    sub-runs' (first slot, length).
     """
     counts, offsets, fs = index["counts"], index["offsets"], index["farlen_sub"]
     B, A, Kv = counts.shape
@@ -517,13 +520,26 @@ def work_items_top2_split(index: dict, BM: int):
                 g = v // K
                 for t in range(0, c, BM):
                     rows = min(BM, c - t)
-                    last = o + t + rows - 1
-                    for j in range(K - 1):
-                        keys = int(fs[b, a, last, j])
-                        if keys > 0:
-                            o2 = j if j < g else j + 1
-                            out.append((b, a, v, o + t, rows, keys, int(offsets[b, a, g * K + o2]), j))
+                    keys = int(fs[b, a, o + t + rows - 1].sum())
+                    if keys > 0:
+                        out.append((b, a, v, o + t, rows, keys, int(offsets[b, a, g * K]), 0))
     return np.array(out, dtype=np.int32).reshape(-1, 8)
+
+
+def segments_top2_split(index: dict, item):
+    """The key sub-runs of a split work item: [(first slot, length, column j)]
+    for j = 0 .. K - 2 in order; length = the far prefix of the item's last
+    row in sub-run (g, o'), o' = j + (j >= g)."""
+    b, a, v, row0, rows = (int(x) for x in item[:5])
+    Kv = index["counts"].shape[-1]
+    K = int(round(math.sqrt(Kv)))
+    g = v // K
+    last = index["farlen_sub"][b, a, row0 + rows - 1]
+    out = []
+    for j in range(K - 1):
+        o2 = j if j < g else j + 1
+        out.append((int(index["offsets"][b, a, g * K + o2]), int(last[j]), j))
+    return out
 
 
 def keep_mask_rows_topk(G, w: int, rows):

@@ -34,14 +34,14 @@ def test_every_declared_symbol_is_exported(fz):
     for name in _declared():
         assert hasattr(lib, name), name
     assert set(fz.EXPORTED) == set(_declared())
-    assert lib.focus_abi_version() == 2
+    assert lib.focus_abi_version() == 3
 
 
 def test_struct_layouts_match_header(fz):
     assert ctypes.sizeof(fz.Params) == 12 * 4
     assert ctypes.sizeof(fz.Item) == 8 * 4
     assert ctypes.sizeof(fz.Index) == 9 * 8 + 2 * 4
-    assert ctypes.sizeof(fz.IndexTopk) == 2 * ctypes.sizeof(fz.Index) + 2 * 8 + 2 * 4
+    assert ctypes.sizeof(fz.IndexTopk) == 2 * ctypes.sizeof(fz.Index) + 2 * 8 + 2 * 4 + 8
 
 
 def test_status_strings(fz):

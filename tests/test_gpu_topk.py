@@ -135,6 +135,10 @@ def test_index_top2_bit_exact(fz, B, A, n, K, w, kind):
     idx = fz.focus_build_index_topk(p, 2, torch.from_numpy(G).cuda(), ws)
     assert fz.focus_check_errors(ws) == 0
     we = max(w, 1)
+    if K <= 8:          # bf16 params (the make_params default): the split layout
+        _check_split_index(fz, p, idx, ws, G, n, K, we)
+        return
+    assert idx.split == 0
     # entries
     got = _np_index(fz, p, idx.entry, ws, 2 * n, K)
     want = ref.build_index_topk(G, K, we)
@@ -161,6 +165,32 @@ def test_index_top2_bit_exact(fz, B, A, n, K, w, kind):
     far = ws[idx.far_tok - ws_base:idx.far_tok - ws_base + P * n * 4].view(torch.int32).cpu().numpy()
     fe = want["farlen_entry"].reshape(B, A, n, 2)
     assert np.array_equal(far.reshape(B, A, n), (fe.max(axis=-1) > 0).astype(np.int32))
+
+
+def _check_split_index(fz, p, idx, ws, G, n, K, we):
+    """Split layout (K <= 8): entries sorted by (group, other group, position),
+    far prefixes per sub-run, one work item per (row tile, sub-run)."""
+    import torch
+    assert idx.split == 1 and idx.farlen_sub
+    got = _np_index(fz, p, idx.entry, ws, 2 * n, K * K)
+    want = ref.build_index_top2_split(G, K, we)
+    for k_got, k_want in (("counts", "counts"), ("offsets", "offsets"), ("perm", "perm"), ("rank", "rank"),
+                          ("farlen_tok", "farlen_entry")):
+        assert np.array_equal(got[k_got], want[k_want]), k_got
+    P = p.B * p.A
+    base = ws.data_ptr()
+    off = idx.farlen_sub - base
+    fs = ws[off:off + P * 2 * n * (K - 1) * 4].view(torch.int32).cpu().numpy()
+    assert np.array_equal(fs.reshape(p.B, p.A, 2 * n, K - 1), want["farlen_sub"])
+    v = fz.index_views(p, idx.entry, ws, n=2 * n, K=K * K)
+    m = int(v["n_items"][0])
+    items = v["items"][:m].cpu().numpy()
+    witems = ref.work_items_top2_split(want, fz.TILE_M)
+    assert np.array_equal(items, witems)
+    assert np.array_equal(v["order"][:m].cpu().numpy(), ref.lpt_order(witems, fz.TILE_N))
+    far = ws[idx.far_tok - base:idx.far_tok - base + P * n * 4].view(torch.int32).cpu().numpy()
+    fe = want["farlen_entry"].reshape(p.B, p.A, n, 2)
+    assert np.array_equal(far.reshape(p.B, p.A, n), (fe.max(axis=-1) > 0).astype(np.int32))
 
 
 def test_index_top2_repeated_id_is_reported(fz):

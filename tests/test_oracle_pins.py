@@ -473,13 +473,16 @@ def test_top2_split_index_visits_every_far_pair_once(K, n, w):
     items = ref.work_items_top2_split(idx, 16)
     perm, fs = idx["perm"][0, 0], idx["farlen_sub"][0, 0]
     seen = {}
-    for b, a, v, row0, rows, keys, key0, j in items:
-        assert keys == fs[row0 + rows - 1, j] and keys > 0
-        for s in range(row0, row0 + rows):
-            assert fs[s, j] <= keys
-            for t in range(key0, key0 + fs[s, j]):
-                pr = (int(perm[s]) // 2, int(perm[t]) // 2)
-                seen[pr] = seen.get(pr, 0) + 1
+    for it in items:
+        row0, rows, keys = int(it[3]), int(it[4]), int(it[5])
+        segs = ref.segments_top2_split(idx, it)
+        assert keys == sum(ln for _, ln, _ in segs) and keys > 0
+        for start, ln, j in segs:
+            for s in range(row0, row0 + rows):
+                assert fs[s, j] <= ln
+                for t in range(start, start + fs[s, j]):
+                    pr = (int(perm[s]) // 2, int(perm[t]) // 2)
+                    seen[pr] = seen.get(pr, 0) + 1
     M = ref.keep_mask_rows_topk(G[0, 0], w, np.arange(n))
     ii, jj = np.nonzero(M)
     want = {(int(i), int(j)) for i, j in zip(ii, jj) if i - j >= w}
