@@ -158,6 +158,17 @@ struct Unit {
 // increasing o' (column j = o' - (o' > g)), each up to the far prefix of the
 // unit's last row; empty ones are skipped.  The walk gives, tile by tile, the
 // column, the tile within it and the sub-run's first slot.
+// sub-run columns per split unit (K <= 8)
+constexpr int kMaxSub = 7;
+
+// a[j] for a runtime j < kMaxSub, without local memory
+__device__ __forceinline__ int pick(const int (&a)[kMaxSub], int j) {
+  int v = a[0];
+#pragma unroll
+  for (int q = 1; q < kMaxSub; ++q) v = q == j ? a[q] : v;
+  return v;
+}
+
 struct SegWalk {
   int j, tt, nt, key0;
   __device__ __forceinline__ void next_col(const AttnArgs& a, const Unit& U) {
@@ -788,6 +799,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       st.far = false;
       int lo = 1, hi = 0;
       st.pos = -1;
+      // split index: the row's and the unit's last row's far prefix in every
+      // sub-run, loaded here with the rest of the row state so the tile loop
+      // never waits on them
+      int rowb[kMaxSub], lastb[kMaxSub];
+      if (MODE == kModeGroupSplit) {
+        const int32_t* lf = a.farlen_sub + (static_cast<size_t>(U.prob) * a.m + U.row0 + U.nrows - 1) * a.nsub;
+        const int32_t* rf = a.farlen_sub + (static_cast<size_t>(U.prob) * a.m + U.row0 + min(r, U.nrows - 1)) * a.nsub;
+#pragma unroll
+        for (int q = 0; q < kMaxSub; ++q) {
+          lastb[q] = q < a.nsub ? lf[q] : 0;
+          rowb[q] = q < a.nsub && st.valid ? rf[q] : 0;
+        }
+      }
       if (is_group_mode(MODE)) {
         if (st.valid) {
           const size_t sidx = static_cast<size_t>(U.prob) * a.m + U.row0 + r;
@@ -820,18 +844,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 3. this unit's key tiles
       float m_run = -INFINITY, l = 0.f;
       const int nt = U.t1 - U.t0 + 1;
-      SegWalk sw;
-      bool new_col = true;
-      if (MODE == kModeGroupSplit) sw.begin(a, U);
+      // split index: current sub-run column, tile within it, and its tiles
+      int sj = -1, stt = 0, snt = 0;
+      auto next_sub = [&]() {
+        for (++sj; sj < a.nsub; ++sj) {
+          const int keys = pick(lastb, sj);
+          if (keys > 0) {
+            snt = (keys + kBN - 1) / kBN;
+            stt = 0;
+            hi = st.valid ? pick(rowb, sj) - 1 : -1;
+            return;
+          }
+        }
+      };
+      if (MODE == kModeGroupSplit) next_sub();
       for (int i = 0; i < nt; ++i) {
         const int gg = g + i;
-        if (MODE == kModeGroupSplit && new_col) {
-          // entering a sub-run: this row's far prefix in it
-          hi = st.valid ? a.farlen_sub[(static_cast<size_t>(U.prob) * a.m + U.row0 + r) * a.nsub + sw.j] - 1 : -1;
-        }
         // first key of this half (split index: within the current sub-run)
-        const int j0 = (MODE == kModeGroupSplit ? sw.tt : U.t0 + i) * kBN + hf * kHalfS;
-        if (MODE == kModeGroupSplit) new_col = sw.step(a, U);
+        const int j0 = (MODE == kModeGroupSplit ? stt : U.t0 + i) * kBN + hf * kHalfS;
         const int sb = gg % kSBuf;
         const uint32_t tS = tmem + lane_base + Cfg::kS + 128 * sb + hf * kHalfS;
         if (!warp_wait(&s_full[sb], (gg / kSBuf) & 1, abort, a.err, a.wait_ns)) { ok = false; break; }
@@ -913,6 +943,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         warp_arrive(&p_ready[sb], lane);
+        if (MODE == kModeGroupSplit && ++stt == snt) next_sub();   // the next tile's sub-run
       }
       if (!ok) break;
       g += nt;
