@@ -25,6 +25,8 @@
 // first half of the fp32 columns.  Warp 8 loads, warp 9 owns TMEM and issues
 // the MMAs.  Every wait is bounded; on a timeout the CTA raises the error bit,
 // drains and exits.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -83,11 +85,10 @@ struct BUnit {
 };
 
 template <int KIND>
-__device__ __forceinline__ BUnit decode(const BwdArgs& a) {
+__device__ __forceinline__ BUnit decode(const BwdArgs& a, int u) {
   BUnit U{};
   U.valid = true;
   U.heads = 1;
-  const int u = blockIdx.x;
   if (KIND == kDqGroup) {
     const int hpa = a.A == 1 ? a.H : a.H / a.H_kv;
     const int y = u % hpa, io = u / hpa;
@@ -162,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* colbuf = reinterpret_cast<float*>(smem + Cfg::kCol);
 
   const int warp = warp_id(), lane = lane_id();
-  const BUnit U = decode<KIND>(a);
+  const BUnit U = decode<KIND>(a, static_cast<int>(blockIdx.x));
   if (!U.valid) return;
   const size_t pn = static_cast<size_t>(U.prob) * a.n;
 
@@ -509,6 +510,349 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// dQ kernels, persistent: one CTA per SM walks the units in snake order (a
+// longest-first list for the group kind) and keeps two tiles in flight.  dS
+// goes to its own TMEM double buffer (columns 384 + 64 * (tile & 1)), so the
+// next tile's S and dP products run as soon as the elementwise warps have
+// read this tile's fp32 S and dP, and the tensor pipe issues, per tile,
+//   S(g), dP(g)  then  dQ += dS(g - 1) K(g - 1)
+// K tiles sit in a 3-slot ring (freed by the dQ product two steps later), V
+// tiles in a 2-slot ring (freed by the dP product), the unit's Q and dO rows
+// in one fixed pair of tiles that the next unit's rows replace once the last
+// S and dP products of the unit are done.
+template <int D>
+struct DqCfg {
+  static constexpr int kChunk = 128 * 128;   // 128 rows x 64 bf16, one swizzle slab
+  static constexpr int kTile = 128 * D * 2;
+  static constexpr int kKSlots = 3, kVSlots = 2;
+  static constexpr int kF0 = 0;              // Q rows of the unit
+  static constexpr int kF1 = kTile;          // dO rows of the unit
+  static constexpr int kK = 2 * kTile;
+  static constexpr int kV = kK + kKSlots * kTile;
+  static constexpr int kBar = kV + kVSlots * kTile;
+  static constexpr int kMisc = kBar + 256;
+  static constexpr int kBytes = kMisc + 64;
+  static constexpr int kSmem = kBytes + 1024;
+  static constexpr uint32_t kS = 0, kDP = 128, kA = 256, kDS = 384;
+};
+static_assert(DqCfg<128>::kSmem <= 227 * 1024, "dQ shared memory above 227 KB");
+
+// Unit k of this CTA in snake order over n_units (-1: past the end, -2: none this round).
+__device__ __forceinline__ int bwd_snake(int k, int n_units) {
+  const int G = gridDim.x, base = k * G;
+  if (base >= n_units) return -1;
+  const int u = base + ((k & 1) ? G - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x));
+  return u < n_units ? u : -2;
+}
+
+template <int D, int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const BwdArgs a) {
+  using Cfg = DqCfg<D>;
+  constexpr int kChunks = D / 64;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBar);
+  uint64_t* fixed_full = bars + 0;
+  uint64_t* fixed_empty = bars + 1;
+  uint64_t* k_full = bars + 2;        // [3]
+  uint64_t* k_empty = bars + 5;       // [3]
+  uint64_t* v_full = bars + 8;        // [2]
+  uint64_t* v_empty = bars + 10;      // [2]
+  uint64_t* sp_full = bars + 12;
+  uint64_t* read_done = bars + 13;    // every elementwise warp has read the tile's S and dP
+  uint64_t* ew_done = bars + 14;      // [2] the tile's dS is in TMEM
+  uint64_t* acc_full = bars + 16;     // the unit's dQ is complete
+  uint64_t* mma_done = bars + 17;
+  int* misc = reinterpret_cast<int*>(smem + Cfg::kMisc);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 0);
+  volatile int* abort = misc + 1;
+
+  const int warp = warp_id(), lane = lane_id();
+  const int n_units = KIND == kDqGroup ? *a.n_items * (a.A == 1 ? a.H : a.H / a.H_kv)
+                                       : a.B * a.H * ((a.n + kT - 1) / kT);
+
+  if (threadIdx.x == 0) {
+    mbar_init(fixed_full, 1);
+    mbar_init(fixed_empty, 1);
+    for (int s = 0; s < Cfg::kKSlots; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < Cfg::kVSlots; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    mbar_init(sp_full, 1);
+    mbar_init(read_done, kEwWarps);
+    mbar_init(&ew_done[0], kEwWarps);
+    mbar_init(&ew_done[1], kEwWarps);
+    mbar_init(acc_full, 1);
+    mbar_init(mma_done, 1);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) tmem_alloc(tmem_slot, 512);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kWarpLd) {
+    // ------------------------------------------------------------ loads ---
+    bool ok = true;
+    int g = 0, uf = 0;
+    for (int k = 0; ok; ++k) {
+      const int u = bwd_snake(k, n_units);
+      if (u == -1) break;
+      if (u < 0) continue;
+      const BUnit U = decode<KIND>(a, u);
+      if (!U.valid || U.ntile == 0) continue;
+      for (int t = 0; t < U.ntile; ++t, ++g) {
+        const int ks = g % Cfg::kKSlots, vs = g % Cfg::kVSlots;
+        if (g >= Cfg::kKSlots && !mbar_wait_nap(&k_empty[ks], (g / Cfg::kKSlots - 1) & 1, abort, a.err)) ok = false;
+        if (ok && g >= Cfg::kVSlots && !mbar_wait_nap(&v_empty[vs], (g / Cfg::kVSlots - 1) & 1, abort, a.err))
+          ok = false;
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        // key slots (group) or key tokens (window) from key0 + t * 128
+        const int y = U.key0 + t * kT;
+        if (lane == 0) {
+          uint8_t* dk = smem + Cfg::kK + ks * Cfg::kTile;
+          uint8_t* dv = smem + Cfg::kV + vs * Cfg::kTile;
+          mbar_expect_tx(&k_full[ks], Cfg::kTile);
+#pragma unroll
+          for (int ch = 0; ch < kChunks; ++ch) tma_load_3d(dk + ch * Cfg::kChunk, &tm_k, &k_full[ks], ch * 64, y, U.zkv);
+          mbar_expect_tx(&v_full[vs], Cfg::kTile);
+#pragma unroll
+          for (int ch = 0; ch < kChunks; ++ch) tma_load_3d(dv + ch * Cfg::kChunk, &tm_v, &v_full[vs], ch * 64, y, U.zkv);
+        }
+        if (t == 0) {
+          // the unit's Q and dO rows, once the previous unit's last S and dP are done
+          if (uf > 0 && !mbar_wait_nap(fixed_empty, (uf - 1) & 1, abort, a.err)) ok = false;
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) {
+            ++g;
+            break;
+          }
+          if (lane == 0) {
+            mbar_expect_tx(fixed_full, 2 * Cfg::kTile);
+#pragma unroll
+            for (int ch = 0; ch < kChunks; ++ch) {
+              tma_load_3d(smem + Cfg::kF0 + ch * Cfg::kChunk, &tm_q, fixed_full, ch * 64, U.row0, U.zq);
+              tma_load_3d(smem + Cfg::kF1 + ch * Cfg::kChunk, &tm_do, fixed_full, ch * 64, U.row0, U.zq);
+            }
+          }
+          ++uf;
+        }
+      }
+    }
+    if ((*abort || !ok) && lane == 0) {
+      // copies already issued must land before the CTA exits
+      if (uf > 0) {
+        const unsigned long long t0 = global_ns();
+        while (!mbar_try_wait(fixed_full, (uf - 1) & 1) && global_ns() - t0 < kWaitTimeoutNs) {}
+      }
+      for (int x = max(0, g - Cfg::kKSlots); x < g; ++x) {
+        const unsigned long long t1 = global_ns();
+        while (!mbar_try_wait(&k_full[x % Cfg::kKSlots], (x / Cfg::kKSlots) & 1) && global_ns() - t1 < kWaitTimeoutNs) {}
+      }
+      for (int x = max(0, g - Cfg::kVSlots); x < g; ++x) {
+        const unsigned long long t1 = global_ns();
+        while (!mbar_try_wait(&v_full[x % Cfg::kVSlots], (x / Cfg::kVSlots) & 1) && global_ns() - t1 < kWaitTimeoutNs) {}
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------- MMAs ---
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(128, kT, false, false);
+      constexpr uint32_t idAcc = idesc_bf16_f32(128, D, false, true);
+      constexpr uint32_t dhi = sw128_desc_hi();
+      const uint32_t f0 = sw128_desc_lo(smem_u32(smem + Cfg::kF0), 16);
+      const uint32_t f1 = sw128_desc_lo(smem_u32(smem + Cfg::kF1), 16);
+      // dQ += dS(x) K(x): the tile's K rows as the MN-major operand
+      auto dq_product = [&](int x, bool first, bool last) -> bool {
+        if (!mbar_wait_nap(&ew_done[x & 1], (x >> 1) & 1, abort, a.err)) return false;
+        tc_fence_after();
+        const uint32_t km = sw128_desc_lo(smem_u32(smem + Cfg::kK + (x % Cfg::kKSlots) * Cfg::kTile), Cfg::kChunk);
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk)
+          mma_ts(tmem + Cfg::kA, tmem + Cfg::kDS + 64 * (x & 1) + kk * 8,
+                 desc_join(km + kk * ((16 * 128) >> 4), dhi), idAcc, !first || kk > 0);
+        mma_commit(&k_empty[x % Cfg::kKSlots]);
+        if (last) mma_commit(acc_full);
+        return true;
+      };
+      bool ok = true;
+      int g = 0, uf = 0;
+      for (int k = 0; ok; ++k) {
+        const int u = bwd_snake(k, n_units);
+        if (u == -1) break;
+        if (u < 0) continue;
+        const BUnit U = decode<KIND>(a, u);
+        if (!U.valid || U.ntile == 0) continue;
+        if (!mbar_wait_nap(fixed_full, uf & 1, abort, a.err)) { ok = false; break; }
+        ++uf;
+        for (int t = 0; t < U.ntile; ++t, ++g) {
+          const int ks = g % Cfg::kKSlots, vs = g % Cfg::kVSlots;
+          if (!mbar_wait_nap(&k_full[ks], (g / Cfg::kKSlots) & 1, abort, a.err) ||
+              !mbar_wait_nap(&v_full[vs], (g / Cfg::kVSlots) & 1, abort, a.err) ||
+              (g > 0 && !mbar_wait_nap(read_done, (g - 1) & 1, abort, a.err))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // S = Q K^T, dP = dO V^T (both operands K-major over d)
+          const uint32_t kb = sw128_desc_lo(smem_u32(smem + Cfg::kK + ks * Cfg::kTile), 16);
+          const uint32_t vb = sw128_desc_lo(smem_u32(smem + Cfg::kV + vs * Cfg::kTile), 16);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * Cfg::kChunk + (kk & 3) * 32) >> 4;
+            mma_ss(tmem + Cfg::kS, desc_join(f0 + off, dhi), desc_join(kb + off, dhi), idS, kk > 0);
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * Cfg::kChunk + (kk & 3) * 32) >> 4;
+            mma_ss(tmem + Cfg::kDP, desc_join(f1 + off, dhi), desc_join(vb + off, dhi), idS, kk > 0);
+          }
+          mma_commit(sp_full);
+          mma_commit(&v_empty[vs]);
+          if (t == U.ntile - 1) mma_commit(fixed_empty);
+          // the previous tile's product, now that this tile's S and dP are queued
+          if (t > 0 && !dq_product(g - 1, t == 1, false)) { ok = false; break; }
+        }
+        if (!ok) break;
+        if (!dq_product(g - 1, U.ntile == 1, true)) { ok = false; break; }
+      }
+      // every MMA issued above has finished before TMEM is released
+      mma_commit(mma_done);
+      const unsigned long long t0 = global_ns();
+      while (!mbar_try_wait(mma_done, 0) && global_ns() - t0 < kWaitTimeoutNs) {}
+    }
+  } else if (warp < kEwWarps) {
+    // ------------------------------------------------------ elementwise ---
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int r = (warp & 3) * 32 + lane;
+    const int half = (warp >> 2) & 1;   // which half of the columns
+    const float sl2 = a.scale_log2;
+    bool ok = true;
+    int g = 0, uf = 0;
+    for (int k = 0; ok; ++k) {
+      const int u = bwd_snake(k, n_units);
+      if (u == -1) break;
+      if (u < 0) continue;
+      const BUnit U = decode<KIND>(a, u);
+      if (!U.valid) continue;
+      const size_t pn = static_cast<size_t>(U.prob) * a.n;
+      const bool row_ok = r < U.nrows;
+      int rpos = -1, klo = 1, khi = 0;
+      float lse2 = 0.f, dlt = 0.f;
+      if (row_ok) {
+        if (KIND == kDqGroup) {
+          rpos = a.perm[pn + U.row0 + r];
+          klo = 0;
+          khi = a.farlen_slot[pn + U.row0 + r] - 1;       // prefix index
+        } else {
+          rpos = U.row0 + r;
+          klo = rpos - a.w + 1;
+          khi = rpos;                                     // key tokens
+        }
+        const size_t qi = static_cast<size_t>(U.zq) * a.n + rpos;
+        lse2 = a.lse[qi] * kLog2e;
+        dlt = a.delta[qi];
+      }
+      for (int t = 0; t < U.ntile; ++t, ++g) {
+        if (!warp_wait(sp_full, g & 1, abort, a.err)) { ok = false; break; }
+        tc_fence_after();
+        // this half's 64 columns of S and dP
+        uint32_t sv[64], dv[64];
+        tmem_ld32(tmem + lane_base + Cfg::kS + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+        tmem_ld32(tmem + lane_base + Cfg::kS + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+        tmem_ld32(tmem + lane_base + Cfg::kDP + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&dv[0]));
+        tmem_ld32(tmem + lane_base + Cfg::kDP + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&dv[32]));
+        tmem_wait_ld();
+        tc_fence_before();
+        warp_arrive(read_done, lane);
+        uint32_t dd[32];
+        const int base_idx = (KIND == kDqGroup ? 0 : U.key0) + t * kT + half * 64;
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) {
+          float d2[2];
+#pragma unroll
+          for (int q2 = 0; q2 < 2; ++q2) {
+            const int idx = base_idx + e + q2;
+            const bool keep = row_ok && idx >= klo && idx <= khi;
+            const float p = keep ? ex2f(__uint_as_float(sv[e + q2]) * sl2 - lse2) : 0.f;
+            d2[q2] = p * (__uint_as_float(dv[e + q2]) - dlt);
+          }
+          dd[e / 2] = pack_bf16x2(d2[0], d2[1]);
+        }
+        // the half's 64 bf16 values take packed columns 32*half .. 32*half + 31 of dS(g)
+        tmem_st32(tmem + lane_base + Cfg::kDS + 64 * (g & 1) + half * 32, dd);
+        tmem_wait_st();
+        tc_fence_before();
+        warp_arrive(&ew_done[g & 1], lane);
+      }
+      if (!ok) break;
+      // epilogue: this half's dQ columns [half * D/2, (half + 1) * D/2) once the unit's products are done
+      const bool have = U.ntile > 0;
+      if (have) {
+        if (!warp_wait(acc_full, uf & 1, abort, a.err)) { ok = false; break; }
+        ++uf;
+        tc_fence_after();
+      }
+      const size_t orow = static_cast<size_t>(U.zq) * a.n + (rpos >= 0 ? rpos : 0);
+#pragma unroll 1
+      for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
+        uint32_t x0[32];
+        if (have) {
+          tmem_ld32(tmem + lane_base + Cfg::kA + c * 32, x0);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x0[e] = 0u;
+        }
+        if (!row_ok) continue;
+        const size_t o = orow * D + c * 32;
+        if (KIND == kDqGroup) {
+          float4* dst = reinterpret_cast<float4*>(a.dq_far + o);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            dst[v] = make_float4(__uint_as_float(x0[4 * v]) * a.scale, __uint_as_float(x0[4 * v + 1]) * a.scale,
+                                 __uint_as_float(x0[4 * v + 2]) * a.scale, __uint_as_float(x0[4 * v + 3]) * a.scale);
+        } else {
+          const bool far = a.farlen_tok[pn + rpos] > 0;
+          const float4* fq = reinterpret_cast<const float4*>(a.dq_far + o);
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dQ) + o);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(x0[8 * v + e]) * a.scale;
+            if (far) {
+              const float4 g0 = fq[2 * v], g1 = fq[2 * v + 1];
+              f[0] += g0.x; f[1] += g0.y; f[2] += g0.z; f[3] += g0.w;
+              f[4] += g1.x; f[5] += g1.y; f[6] += g1.z; f[7] += g1.w;
+            }
+            dst[v] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                                pack_bf16x2(f[6], f[7]));
+          }
+        }
+      }
+      tc_fence_before();
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 // Q, dO rows and the LSE, Delta of every query head in the order of its
 // assignment's index: dst[zq, s] = src[zq, perm_a[s]], a = the head's assignment.
 __global__ void __launch_bounds__(256) permute_q_kernel(BwdArgs a, __nv_bfloat16* Qs, __nv_bfloat16* dOs,
@@ -536,15 +880,18 @@ __global__ void __launch_bounds__(256) permute_q_kernel(BwdArgs a, __nv_bfloat16
 template <int D>
 cudaError_t launch_d(const BwdArgs& a, const CUtensorMap* qs, const CUtensorMap* dos, const CUtensorMap* ks,
                      const CUtensorMap* vs, const CUtensorMap* q3, const CUtensorMap* do3, const CUtensorMap* k3,
-                     const CUtensorMap* v3, int max_items, cudaStream_t st) {
+                     const CUtensorMap* v3, int max_items, int num_sms, cudaStream_t st) {
   using Cfg = BCfg<D>;
   const int hpa = a.A == 1 ? a.H : a.H / a.H_kv;
   const long long g_units = static_cast<long long>(max_items) * hpa;
   const long long q_units = static_cast<long long>(a.B) * a.H * ((a.n + kT - 1) / kT);
   const long long k_units = static_cast<long long>(a.B) * a.H_kv * ((a.n + kT - 1) / kT);
+  const long long sms = num_sms > 0 ? num_sms : 1;
   if (g_units > 0)
-    bwd_tc_kernel<D, kDqGroup><<<static_cast<unsigned>(g_units), kThreads, Cfg::kSmem, st>>>(*qs, *dos, *ks, *vs, a);
-  bwd_tc_kernel<D, kDqLocal><<<static_cast<unsigned>(q_units), kThreads, Cfg::kSmem, st>>>(*q3, *do3, *k3, *v3, a);
+    bwd_dq_kernel<D, kDqGroup><<<static_cast<unsigned>(std::min(g_units, sms)), kThreads, DqCfg<D>::kSmem, st>>>(
+        *qs, *dos, *ks, *vs, a);
+  bwd_dq_kernel<D, kDqLocal><<<static_cast<unsigned>(std::min(q_units, sms)), kThreads, DqCfg<D>::kSmem, st>>>(
+      *q3, *do3, *k3, *v3, a);
   bwd_tc_kernel<D, kDkvGroup><<<static_cast<unsigned>(k_units), kThreads, Cfg::kSmem, st>>>(*qs, *dos, *ks, *vs, a);
   bwd_tc_kernel<D, kDkvLocal><<<static_cast<unsigned>(k_units), kThreads, Cfg::kSmem, st>>>(*q3, *do3, *k3, *v3, a);
   return cudaGetLastError();
@@ -554,9 +901,9 @@ template <int D>
 cudaError_t set_smem_d() {
   using Cfg = BCfg<D>;
   cudaError_t e;
-  e = cudaFuncSetAttribute(bwd_tc_kernel<D, kDqGroup>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+  e = cudaFuncSetAttribute(bwd_dq_kernel<D, kDqGroup>, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kSmem);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(bwd_tc_kernel<D, kDqLocal>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+  e = cudaFuncSetAttribute(bwd_dq_kernel<D, kDqLocal>, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kSmem);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(bwd_tc_kernel<D, kDkvGroup>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
   if (e != cudaSuccess) return e;
@@ -568,9 +915,9 @@ cudaError_t set_smem_d() {
 cudaError_t launch_attn_bwd_tc(const BwdArgs& a, const CUtensorMap* qs, const CUtensorMap* dos,
                                const CUtensorMap* ks, const CUtensorMap* vs, const CUtensorMap* q3,
                                const CUtensorMap* do3, const CUtensorMap* k3, const CUtensorMap* v3,
-                               int max_items, cudaStream_t st) {
-  if (a.d == 64) return launch_d<64>(a, qs, dos, ks, vs, q3, do3, k3, v3, max_items, st);
-  if (a.d == 128) return launch_d<128>(a, qs, dos, ks, vs, q3, do3, k3, v3, max_items, st);
+                               int max_items, int num_sms, cudaStream_t st) {
+  if (a.d == 64) return launch_d<64>(a, qs, dos, ks, vs, q3, do3, k3, v3, max_items, num_sms, st);
+  if (a.d == 128) return launch_d<128>(a, qs, dos, ks, vs, q3, do3, k3, v3, max_items, num_sms, st);
   return cudaErrorInvalidValue;
 }
 

@@ -219,7 +219,7 @@ cudaError_t launch_bwd_delta(const BwdArgs& a, int dtype, cudaStream_t st);
 cudaError_t launch_attn_bwd_tc(const BwdArgs& a, const CUtensorMap* qs, const CUtensorMap* dos,
                                const CUtensorMap* ks, const CUtensorMap* vs, const CUtensorMap* q3,
                                const CUtensorMap* do3, const CUtensorMap* k3, const CUtensorMap* v3,
-                               int max_items, cudaStream_t st);
+                               int max_items, int num_sms, cudaStream_t st);
 cudaError_t setup_bwd_tc_kernels();
 // Q, dO rows and LSE, Delta of every query head sorted by its assignment's
 // index (for the group kernels' tile loads).
