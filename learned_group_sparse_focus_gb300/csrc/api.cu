@@ -1072,6 +1072,7 @@ focus_status_t focus_attention_bwd(const focus_params_t* p, const void* Q, const
   void* Vs = at<void>(ws, BL.vs);
   a.lse_sorted = at<float>(ws, BL.lse_s);
   a.delta_sorted = at<float>(ws, BL.delta_s);
+  a.ticket = at<int>(ws, 0) + 1;   // the word after the error word
   // tile maps over the sorted copies (group kernels) and the inputs (window kernels)
   CUtensorMap qs3, dos3, ks3, vs3, q3, do3, k3, v3;
   if (!make_map(&qs3, Qs, p->d, p->n, qplanes, 128, 3) || !make_map(&dos3, dOs, p->d, p->n, qplanes, 128, 3) ||
@@ -1083,6 +1084,7 @@ focus_status_t focus_attention_bwd(const focus_params_t* p, const void* Q, const
   if (e == cudaSuccess) e = launch_bwd_permute_q(a, Qs, dOs, at<float>(ws, BL.lse_s), at<float>(ws, BL.delta_s), st);
   if (e == cudaSuccess)
     e = launch_permute_kv_bf16(K, V, Ks, Vs, idx->perm, p->B, p->H_kv, p->n, p->n, 0, p->d, p->A, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(a.ticket, 0, sizeof(int), st);
   if (e == cudaSuccess) e = launch_attn_bwd_tc(a, &qs3, &dos3, &ks3, &vs3, &q3, &do3, &k3, &v3, idx->max_items, sm_count(), st);
   return cuda_status(e);
 }

@@ -3,10 +3,10 @@
 // Focus is the Key", section 2.1; "Focus: Learning Which Attention Pairs
 // Matter", section 3.1), with every d-long product an MMA.
 //
-// Two kernels, each in a group form (far pairs, rows and keys in the index's
-// sorted order, read as TMA tiles from copies of Q, dO, K, V (and LSE, Delta)
-// sorted by the index once per call) and a window form (natural order, TMA
-// tiles); one CTA per 128-row unit:
+// Two persistent kernels (one CTA per SM looping over 128-row units), each in
+// a group form (far pairs, rows and keys in the index's sorted order, read as
+// TMA tiles from copies of Q, dO, K, V (and LSE, Delta) sorted by the index
+// once per call) and a window form (natural order, TMA tiles):
 //   dQ   rows = 128 queries, streamed = 128-key tiles of the kept keys:
 //          S = Q K^T, dP = dO V^T               (SS, TMEM fp32)
 //          dS = P (dP - Delta), P = exp(S scale - LSE)   (CUDA cores -> TMEM bf16)
@@ -16,15 +16,11 @@
 //          S^T = K Q^T, dP^T = V dO^T           (SS)
 //          P^T, dS^T                            (CUDA cores -> TMEM bf16)
 //          dV += P^T dO, dK += dS^T Q           (TS)
-// TMEM (512 columns): S at 0, dP at 128 (the bf16 P^T / dS^T overwrite their
-// first 64 columns once read), accumulators at 256 (and 256 + d).  One tile is
-// in flight at a time; the next tile's operands stream in through a 2-slot TMA
-// ring meanwhile.  Warps 0-7 do the elementwise work, two per TMEM lane
-// quadrant, each on half of the row's columns: both halves read their fp32
-// columns, meet at an mbarrier, and only then write the bf16 pairs over the
-// first half of the fp32 columns.  Warp 8 loads, warp 9 owns TMEM and issues
-// the MMAs.  Every wait is bounded; on a timeout the CTA raises the error bit,
-// drains and exits.
+// Warps 0-7 do the elementwise work, two per TMEM lane quadrant, each on half
+// of the row's columns; warp 8 loads, warp 9 owns TMEM and issues the MMAs.
+// Each kernel keeps the tensor pipe busy while the elementwise warps work (its
+// own comment says how).  Every wait is bounded; on a timeout the CTA raises
+// the error bit, drains its copies, frees TMEM and exits.
 #include <algorithm>
 
 #include "common.cuh"
@@ -42,21 +38,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 enum : int { kDqGroup = 0, kDqLocal = 1, kDkvGroup = 2, kDkvLocal = 3 };
 
-template <int D>
-struct BCfg {
-  static constexpr int kChunk = 128 * 128;   // 128 rows x 64 bf16, one swizzle slab
-  static constexpr int kTile = 128 * D * 2;
-  static constexpr int kF0 = 0;              // fixed operands of the unit
-  static constexpr int kF1 = kTile;
-  static constexpr int kR = 2 * kTile;       // ring: 2 slots x (R0, R1)
-  static constexpr int kCol = kR + 4 * kTile;              // [2 slots][lse2, delta][128] fp32
-  static constexpr int kBar = kCol + 2 * 2 * 128 * 4;
-  static constexpr int kMisc = kBar + 256;
-  static constexpr int kBytes = kMisc + 64;
-  static constexpr int kSmem = kBytes + 1024;             // + slack to align the base to 1024
-  static constexpr uint32_t kS = 0, kDP = 128, kA0 = 256, kA1 = 256 + D;
-};
-static_assert(BCfg<128>::kSmem <= 227 * 1024, "backward shared memory above 227 KB");
+__device__ __forceinline__ void prefetch_l2(const float* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 
 __device__ __forceinline__ float ex2f(float x) {
   float y;
@@ -133,381 +117,6 @@ __device__ __forceinline__ BUnit decode(const BwdArgs& a, int u) {
   U.zq = U.b * a.H + U.h;
   U.zkv = U.b * a.H_kv + U.kv;
   return U;
-}
-
-template <int D, int KIND>
-__global__ void __launch_bounds__(kThreads, 1)
-    bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
-                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const BwdArgs a) {
-  using Cfg = BCfg<D>;
-  constexpr int kChunks = D / 64;
-  constexpr bool kDq = KIND == kDqGroup || KIND == kDqLocal;
-  constexpr bool kGroup = KIND == kDqGroup || KIND == kDkvGroup;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBar);
-  uint64_t* fixed_full = bars + 0;
-  uint64_t* ring_full = bars + 1;     // [2]
-  uint64_t* ring_empty = bars + 3;    // [2]
-  uint64_t* sp_full = bars + 5;
-  uint64_t* ew_done = bars + 6;
-  uint64_t* acc_done = bars + 7;
-  uint64_t* mma_done = bars + 8;
-  uint64_t* col_full = bars + 9;      // [2] dKV: the slot's query LSE / Delta are in shared memory
-  uint64_t* read_done = bars + 11;    // every elementwise warp has read this tile's fp32 S and dP
-  int* misc = reinterpret_cast<int*>(smem + Cfg::kMisc);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 0);
-  volatile int* abort = misc + 1;
-  int* range = misc + 2;              // dKV: walked query range [range[0], range[1]]
-  float* colbuf = reinterpret_cast<float*>(smem + Cfg::kCol);
-
-  const int warp = warp_id(), lane = lane_id();
-  const BUnit U = decode<KIND>(a, static_cast<int>(blockIdx.x));
-  if (!U.valid) return;
-  const size_t pn = static_cast<size_t>(U.prob) * a.n;
-
-  if (threadIdx.x == 0) {
-    mbar_init(fixed_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&ring_full[s], 1);
-      mbar_init(&ring_empty[s], 1);
-    }
-    mbar_init(sp_full, 1);
-    mbar_init(ew_done, kEwWarps);
-    mbar_init(read_done, kEwWarps);
-    mbar_init(acc_done, 1);
-    mbar_init(mma_done, 1);
-    mbar_init(&col_full[0], 32);
-    mbar_init(&col_full[1], 32);
-    *abort = 0;
-    range[0] = 0x7fffffff;
-    range[1] = -1;
-    fence_mbar_init();
-  }
-  if (warp == kWarpMma) tmem_alloc(tmem_slot, 512);
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  // ---- per-row bookkeeping of the elementwise threads (row = TMEM lane) ----
-  const int r = (warp & 3) * 32 + lane;
-  const int half = (warp >> 2) & 1;   // elementwise: which half of the columns
-  const bool row_ok = warp < kEwWarps && r < U.nrows;
-  int rpos = -1;        // token of the row
-  int klo = 1, khi = 0; // kept streamed indices of the row (inclusive), in the walked order
-  if (warp < kEwWarps && row_ok) {
-    if (KIND == kDqGroup) {
-      rpos = a.perm[pn + U.row0 + r];
-      klo = 0;
-      khi = a.farlen_slot[pn + U.row0 + r] - 1;           // prefix index
-    } else if (KIND == kDqLocal) {
-      rpos = U.row0 + r;
-      klo = rpos - a.w + 1;
-      khi = rpos;                                         // key tokens
-    } else if (KIND == kDkvGroup) {
-      const int u = U.row0 + r;
-      rpos = a.perm[pn + u];
-      const int32_t* off = a.offsets + static_cast<size_t>(U.prob) * (a.groups + 1);
-      int glo = 0, ghi = a.groups;
-      while (ghi - glo > 1) {
-        const int mid = (glo + ghi) >> 1;
-        if (off[mid] <= u) glo = mid; else ghi = mid;
-      }
-      const int gend = off[glo + 1];
-      const int target = rpos + a.w;
-      int s0 = u + 1, s1 = gend;
-      while (s0 < s1) {
-        const int mid = (s0 + s1) >> 1;
-        if (a.perm[pn + mid] < target) s0 = mid + 1; else s1 = mid;
-      }
-      klo = s0;
-      khi = gend - 1;                                     // query slots
-    } else {
-      rpos = U.row0 + r;
-      klo = rpos;
-      khi = min(a.n - 1, rpos + a.w - 1);                 // query tokens
-    }
-  }
-  if (!kDq) {
-    if (row_ok && klo <= khi) {
-      atomicMin(&range[0], klo);
-      atomicMax(&range[1], khi);
-    }
-    __syncthreads();
-  }
-  int wlo = 0, ntile = U.ntile;
-  if (!kDq) {
-    wlo = range[0];
-    const int whi = range[1];
-    ntile = whi >= wlo ? (whi - wlo) / kT + 1 : 0;
-  }
-  const int ntot = ntile * U.heads;
-
-  if (warp == kWarpLd) {
-    // ------------------------------------------------------------ loads ---
-    bool ok = true;
-    int issued = 0;
-    if (ntot > 0) {
-      // fixed operands: dQ -> (Q, dO) rows of the unit; dKV -> (K, V) rows
-      // (group kinds: rows of the sorted copies, so one tile either way)
-      if (lane == 0) {
-        mbar_expect_tx(fixed_full, 2 * Cfg::kTile);
-#pragma unroll
-        for (int ch = 0; ch < kChunks; ++ch) {
-          tma_load_3d(smem + Cfg::kF0 + ch * Cfg::kChunk, kDq ? &tm_q : &tm_k, fixed_full, ch * 64, U.row0,
-                      kDq ? U.zq : U.zkv);
-          tma_load_3d(smem + Cfg::kF1 + ch * Cfg::kChunk, kDq ? &tm_do : &tm_v, fixed_full, ch * 64, U.row0,
-                      kDq ? U.zq : U.zkv);
-        }
-      }
-      for (int it = 0; it < ntot && ok; ++it) {
-        const int sl = it & 1, use = it >> 1;
-        if (use > 0 && !mbar_wait_nap(&ring_empty[sl], (use - 1) & 1, abort, a.err)) ok = false;
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        const int t = it % ntile, hh = it / ntile;
-        const int zq = U.b * a.H + U.h + hh;
-        uint8_t* r0 = smem + Cfg::kR + sl * 2 * Cfg::kTile;
-        uint8_t* r1 = r0 + Cfg::kTile;
-        // dQ: key slots (group) or tokens from key0 + t*128; dKV: query slots or
-        // tokens from wlo + t*128 (rows past a group's run are masked out)
-        if (lane == 0) {
-          mbar_expect_tx(&ring_full[sl], 2 * Cfg::kTile);
-          const int y = (kDq ? U.key0 : wlo) + t * kT;
-#pragma unroll
-          for (int ch = 0; ch < kChunks; ++ch) {
-            tma_load_3d(r0 + ch * Cfg::kChunk, kDq ? &tm_k : &tm_q, &ring_full[sl], ch * 64, y, kDq ? U.zkv : zq);
-            tma_load_3d(r1 + ch * Cfg::kChunk, kDq ? &tm_v : &tm_do, &ring_full[sl], ch * 64, y, kDq ? U.zkv : zq);
-          }
-        }
-        if (!kDq) {
-          // the tile's query columns: LSE (log2 units) and Delta for head h + hh;
-          // the slot is free (ring_empty above), and each lane's arrival
-          // publishes its four entries
-          float* cb = colbuf + sl * 256;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int c = 4 * lane + j;
-            const int q = wlo + t * kT + c;
-            float l2 = 0.f, dl = 0.f;
-            if (q < a.n) {
-              // group: the sorted copies are indexed by slot
-              const size_t qi = static_cast<size_t>(zq) * a.n + q;
-              l2 = (kGroup ? a.lse_sorted : a.lse)[qi] * kLog2e;
-              dl = (kGroup ? a.delta_sorted : a.delta)[qi];
-            }
-            cb[c] = l2;
-            cb[128 + c] = dl;
-          }
-          mbar_arrive(&col_full[sl]);
-        }
-        ++issued;
-      }
-      if ((*abort || !ok) && lane == 0) {
-        // copies already issued must land before the CTA exits
-        const unsigned long long t0 = global_ns();
-        while (!mbar_try_wait(fixed_full, 0) && global_ns() - t0 < kWaitTimeoutNs) {}
-        for (int it = max(0, issued - 2); it < issued; ++it) {
-          const unsigned long long t1 = global_ns();
-          while (!mbar_try_wait(&ring_full[it & 1], (it >> 1) & 1) && global_ns() - t1 < kWaitTimeoutNs) {}
-        }
-      }
-    }
-  } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------- MMAs ---
-    if (lane == 0 && ntot > 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, kT, false, false);
-      constexpr uint32_t idAcc = idesc_bf16_f32(128, D, false, true);
-      constexpr uint32_t dhi = sw128_desc_hi();
-      const uint32_t f0 = sw128_desc_lo(smem_u32(smem + Cfg::kF0), 16);
-      const uint32_t f1 = sw128_desc_lo(smem_u32(smem + Cfg::kF1), 16);
-      bool ok = mbar_wait_nap(fixed_full, 0, abort, a.err);
-      for (int it = 0; it < ntot && ok; ++it) {
-        const int sl = it & 1;
-        if (!mbar_wait_nap(&ring_full[sl], (it >> 1) & 1, abort, a.err)) { ok = false; break; }
-        if (it > 0 && !mbar_wait_nap(acc_done, (it - 1) & 1, abort, a.err)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t rb = smem_u32(smem + Cfg::kR + sl * 2 * Cfg::kTile);
-        const uint32_t r0k = sw128_desc_lo(rb, 16), r1k = sw128_desc_lo(rb + Cfg::kTile, 16);
-        // S = F0 R0^T, dP = F1 R1^T (both operands K-major over d)
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * Cfg::kChunk + (kk & 3) * 32) >> 4;
-          mma_ss(tmem + Cfg::kS, desc_join(f0 + off, dhi), desc_join(r0k + off, dhi), idS, kk > 0);
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * Cfg::kChunk + (kk & 3) * 32) >> 4;
-          mma_ss(tmem + Cfg::kDP, desc_join(f1 + off, dhi), desc_join(r1k + off, dhi), idS, kk > 0);
-        }
-        mma_commit(sp_full);
-        if (!mbar_wait_nap(ew_done, it & 1, abort, a.err)) { ok = false; break; }
-        tc_fence_after();
-        // accumulators: the streamed tiles as MN-major operands (reduction over the tile's rows)
-        const uint32_t r0m = sw128_desc_lo(rb, Cfg::kChunk), r1m = sw128_desc_lo(rb + Cfg::kTile, Cfg::kChunk);
-        if (kDq) {
-#pragma unroll
-          for (int kk = 0; kk < kT / 16; ++kk)
-            mma_ts(tmem + Cfg::kA0, tmem + Cfg::kDP + kk * 8, desc_join(r0m + kk * ((16 * 128) >> 4), dhi), idAcc,
-                   it > 0 || kk > 0);
-        } else {
-#pragma unroll
-          for (int kk = 0; kk < kT / 16; ++kk)
-            mma_ts(tmem + Cfg::kA0, tmem + Cfg::kS + kk * 8, desc_join(r1m + kk * ((16 * 128) >> 4), dhi), idAcc,
-                   it > 0 || kk > 0);
-#pragma unroll
-          for (int kk = 0; kk < kT / 16; ++kk)
-            mma_ts(tmem + Cfg::kA1, tmem + Cfg::kDP + kk * 8, desc_join(r0m + kk * ((16 * 128) >> 4), dhi), idAcc,
-                   it > 0 || kk > 0);
-        }
-        mma_commit(acc_done);
-        mma_commit(&ring_empty[sl]);
-      }
-      // every MMA issued above has finished before TMEM is released
-      mma_commit(mma_done);
-      const unsigned long long t0 = global_ns();
-      while (!mbar_try_wait(mma_done, 0) && global_ns() - t0 < kWaitTimeoutNs) {}
-    }
-  } else {
-    // ------------------------------------------------------ elementwise ---
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const float sl2 = a.scale_log2;
-    float lse2 = 0.f, dlt = 0.f;
-    if (kDq && row_ok) {
-      const size_t qi = static_cast<size_t>(U.zq) * a.n + rpos;
-      lse2 = a.lse[qi] * kLog2e;
-      dlt = a.delta[qi];
-    }
-    bool ok = true;
-    for (int it = 0; it < ntot && ok; ++it) {
-      const int t = it % ntile;
-      const float* cb = colbuf + (it & 1) * 256;  // [lse2 x128, delta x128] of this tile's queries
-      if (!kDq && !warp_wait(&col_full[it & 1], (it >> 1) & 1, abort, a.err)) { ok = false; break; }
-      if (!warp_wait(sp_full, it & 1, abort, a.err)) { ok = false; break; }
-      tc_fence_after();
-      // this half's 64 columns of S and dP, all read before anyone writes
-      uint32_t sv[64], dv[64];
-      tmem_ld32(tmem + lane_base + Cfg::kS + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-      tmem_ld32(tmem + lane_base + Cfg::kS + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-      tmem_ld32(tmem + lane_base + Cfg::kDP + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&dv[0]));
-      tmem_ld32(tmem + lane_base + Cfg::kDP + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&dv[32]));
-      tmem_wait_ld();
-      tc_fence_before();
-      warp_arrive(read_done, lane);
-      if (!warp_wait(read_done, it & 1, abort, a.err)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t pp[32], dd[32];
-      const int base_idx = (kDq ? (KIND == kDqGroup ? 0 : U.key0) : wlo) + t * kT + half * 64;
-#pragma unroll
-      for (int e = 0; e < 64; e += 2) {
-        float p2[2], d2[2];
-#pragma unroll
-        for (int q2 = 0; q2 < 2; ++q2) {
-          const int col = half * 64 + e + q2;
-          const int idx = base_idx + e + q2;
-          const bool keep = row_ok && idx >= klo && idx <= khi;
-          const float l2 = kDq ? lse2 : cb[col];
-          const float dl = kDq ? dlt : cb[128 + col];
-          const float p = keep ? ex2f(__uint_as_float(sv[e + q2]) * sl2 - l2) : 0.f;
-          p2[q2] = p;
-          d2[q2] = p * (__uint_as_float(dv[e + q2]) - dl);
-        }
-        pp[e / 2] = pack_bf16x2(p2[0], p2[1]);
-        dd[e / 2] = pack_bf16x2(d2[0], d2[1]);
-      }
-      // the half's 64 bf16 values take packed columns 32*half .. 32*half + 31
-      tmem_st32(tmem + lane_base + Cfg::kDP + half * 32, dd);
-      if (!kDq) tmem_st32(tmem + lane_base + Cfg::kS + half * 32, pp);
-      tmem_wait_st();
-      tc_fence_before();
-      warp_arrive(ew_done, lane);
-    }
-    // epilogue: the accumulators once the last tile's MMAs are done
-    const bool have = ok && ntot > 0;
-    if (have && !warp_wait(acc_done, (ntot - 1) & 1, abort, a.err)) ok = false;
-    if (ok) {
-      tc_fence_after();
-      const size_t orow = static_cast<size_t>(kDq ? U.zq : U.zkv) * a.n + (rpos >= 0 ? rpos : 0);
-      // this half's accumulator columns: [half * D/2, (half + 1) * D/2)
-#pragma unroll 1
-      for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
-        uint32_t x0[32], x1[32];
-        if (have) {
-          tmem_ld32(tmem + lane_base + Cfg::kA0 + c * 32, x0);
-          if (!kDq) tmem_ld32(tmem + lane_base + Cfg::kA1 + c * 32, x1);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) x0[e] = x1[e] = 0u;
-        }
-        if (!row_ok) continue;
-        const size_t o = orow * D + c * 32;
-        if (KIND == kDqGroup) {
-          float4* dst = reinterpret_cast<float4*>(a.dq_far + o);
-#pragma unroll
-          for (int v = 0; v < 8; ++v)
-            dst[v] = make_float4(__uint_as_float(x0[4 * v]) * a.scale, __uint_as_float(x0[4 * v + 1]) * a.scale,
-                                 __uint_as_float(x0[4 * v + 2]) * a.scale, __uint_as_float(x0[4 * v + 3]) * a.scale);
-        } else if (KIND == kDqLocal) {
-          const bool far = a.farlen_tok[pn + rpos] > 0;
-          const float4* fq = reinterpret_cast<const float4*>(a.dq_far + o);
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dQ) + o);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            float f[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(x0[8 * v + e]) * a.scale;
-            if (far) {
-              const float4 g0 = fq[2 * v], g1 = fq[2 * v + 1];
-              f[0] += g0.x; f[1] += g0.y; f[2] += g0.z; f[3] += g0.w;
-              f[4] += g1.x; f[5] += g1.y; f[6] += g1.z; f[7] += g1.w;
-            }
-            dst[v] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
-                                pack_bf16x2(f[6], f[7]));
-          }
-        } else if (KIND == kDkvGroup) {
-          float4* dvd = reinterpret_cast<float4*>(a.dv_far + o);
-          float4* dkd = reinterpret_cast<float4*>(a.dk_far + o);
-#pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            dvd[v] = make_float4(__uint_as_float(x0[4 * v]), __uint_as_float(x0[4 * v + 1]),
-                                 __uint_as_float(x0[4 * v + 2]), __uint_as_float(x0[4 * v + 3]));
-            dkd[v] = make_float4(__uint_as_float(x1[4 * v]) * a.scale, __uint_as_float(x1[4 * v + 1]) * a.scale,
-                                 __uint_as_float(x1[4 * v + 2]) * a.scale, __uint_as_float(x1[4 * v + 3]) * a.scale);
-          }
-        } else {
-          const float4* fv = reinterpret_cast<const float4*>(a.dv_far + o);
-          const float4* fk = reinterpret_cast<const float4*>(a.dk_far + o);
-          uint4* dvd = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dV) + o);
-          uint4* dkd = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dK) + o);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const float4 v0 = fv[2 * v], v1 = fv[2 * v + 1], k0 = fk[2 * v], k1 = fk[2 * v + 1];
-            const float gv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-            const float gk[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
-            float fvv[8], fkk[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              fvv[e] = __uint_as_float(x0[8 * v + e]) + gv[e];
-              fkk[e] = __uint_as_float(x1[8 * v + e]) * a.scale + gk[e];
-            }
-            dvd[v] = make_uint4(pack_bf16x2(fvv[0], fvv[1]), pack_bf16x2(fvv[2], fvv[3]),
-                                pack_bf16x2(fvv[4], fvv[5]), pack_bf16x2(fvv[6], fvv[7]));
-            dkd[v] = make_uint4(pack_bf16x2(fkk[0], fkk[1]), pack_bf16x2(fkk[2], fkk[3]),
-                                pack_bf16x2(fkk[4], fkk[5]), pack_bf16x2(fkk[6], fkk[7]));
-          }
-        }
-      }
-    }
-  }
-  __syncwarp();
-  tc_fence_before();
-  __syncthreads();
-  if (warp == kWarpMma) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
 }
 
 // ---------------------------------------------------------------------------
@@ -749,6 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_ok = r < U.nrows;
       int rpos = -1, klo = 1, khi = 0;
       float lse2 = 0.f, dlt = 0.f;
+      bool far = false;
       if (row_ok) {
         if (KIND == kDqGroup) {
           rpos = a.perm[pn + U.row0 + r];
@@ -762,8 +372,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const size_t qi = static_cast<size_t>(U.zq) * a.n + rpos;
         lse2 = a.lse[qi] * kLog2e;
         dlt = a.delta[qi];
+        if (KIND == kDqLocal) far = a.farlen_tok[pn + rpos] > 0;   // read by the epilogue
       }
+      const uint64_t sc2 = f2_pack(sl2, sl2), nl2 = f2_pack(-lse2, -lse2), nd2 = f2_pack(-dlt, -dlt);
       for (int t = 0; t < U.ntile; ++t, ++g) {
+        if (KIND == kDqLocal && far && t == max(0, U.ntile - 3)) {
+          // the epilogue's far part, three tiles ahead so that it is in L2 when read
+          const size_t o = (static_cast<size_t>(U.zq) * a.n + rpos) * D + half * (D / 2);
+#pragma unroll
+          for (int q = 0; q < D / 2; q += 32) prefetch_l2(a.dq_far + o + q);
+        }
+        const int c0 = (KIND == kDqGroup ? 0 : U.key0) + t * kT + half * 64;   // key index of column 0
+        // bit e: the row keeps column c0 + e
+        const int lo = max(klo - c0, 0), hi = min(khi - c0, 63);
+        const uint64_t keepm = (row_ok && lo <= hi) ? ((~0ull >> (63 - hi)) & (~0ull << lo)) : 0ull;
+        const bool full = __all_sync(0xffffffffu, keepm == ~0ull);
         if (!warp_wait(sp_full, g & 1, abort, a.err)) { ok = false; break; }
         tc_fence_after();
         // this half's 64 columns of S and dP
@@ -775,19 +398,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         tc_fence_before();
         warp_arrive(read_done, lane);
+        // dS = P (dP - Delta), P = 2^(s scale log2e - lse2), in packed pairs; a
+        // dropped pair gets exp2(-inf) = +0, no branch around the exponential
         uint32_t dd[32];
-        const int base_idx = (KIND == kDqGroup ? 0 : U.key0) + t * kT + half * 64;
+        if (full) {
 #pragma unroll
-        for (int e = 0; e < 64; e += 2) {
-          float d2[2];
-#pragma unroll
-          for (int q2 = 0; q2 < 2; ++q2) {
-            const int idx = base_idx + e + q2;
-            const bool keep = row_ok && idx >= klo && idx <= khi;
-            const float p = keep ? ex2f(__uint_as_float(sv[e + q2]) * sl2 - lse2) : 0.f;
-            d2[q2] = p * (__uint_as_float(dv[e + q2]) - dlt);
+          for (int e = 0; e < 64; e += 2) {
+            float t0, t1, d0, d1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sc2, nl2), t0, t1);
+            const uint64_t q = f2_pack(ex2f(t0), ex2f(t1));
+            f2_unpack(f2_mul(q, f2_add(f2_pack(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])), nd2)), d0, d1);
+            dd[e / 2] = pack_bf16x2(d0, d1);
           }
-          dd[e / 2] = pack_bf16x2(d2[0], d2[1]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; e += 2) {
+            float t0, t1, d0, d1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sc2, nl2), t0, t1);
+            const uint64_t q = f2_pack(ex2f((keepm >> e) & 1 ? t0 : -INFINITY),
+                                       ex2f((keepm >> (e + 1)) & 1 ? t1 : -INFINITY));
+            f2_unpack(f2_mul(q, f2_add(f2_pack(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])), nd2)), d0, d1);
+            dd[e / 2] = pack_bf16x2(d0, d1);
+          }
         }
         // the half's 64 bf16 values take packed columns 32*half .. 32*half + 31 of dS(g)
         tmem_st32(tmem + lane_base + Cfg::kDS + 64 * (g & 1) + half * 32, dd);
@@ -823,7 +455,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             dst[v] = make_float4(__uint_as_float(x0[4 * v]) * a.scale, __uint_as_float(x0[4 * v + 1]) * a.scale,
                                  __uint_as_float(x0[4 * v + 2]) * a.scale, __uint_as_float(x0[4 * v + 3]) * a.scale);
         } else {
-          const bool far = a.farlen_tok[pn + rpos] > 0;
           const float4* fq = reinterpret_cast<const float4*>(a.dq_far + o);
           uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dQ) + o);
 #pragma unroll
@@ -838,6 +469,567 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             dst[v] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
                                 pack_bf16x2(f[6], f[7]));
+          }
+        }
+      }
+      tc_fence_before();
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// dK/dV kernels, persistent: one CTA per SM takes units (128 key rows of one
+// KV head) from a ticket counter (group kind) or in snake order (window
+// kind) and walks, for every query head of the KV head, the query tiles that
+// keep the unit's keys.  The loader warp names each unit, finds its rows'
+// kept query ranges and publishes them through a 2-entry ring in shared
+// memory, so the elementwise warps never search at a unit boundary.  TMEM is
+// S^T | dP^T | dV | dK; per tile the tensor pipe runs
+//   S^T = K Q^T,  dP^T = V dO^T,  dV += P^T dO,  dK += dS^T Q
+// and the elementwise warps work in two steps, P^T (over S^T, in place) as
+// soon as S^T is there and dS^T (over dP^T) once dP^T is.  The next tile's
+// S^T is issued as soon as dV has read P^T, ahead of dK, so it runs while
+// dS^T is computed.
+template <int D>
+struct KvCfg {
+  static constexpr int kChunk = 128 * 128;
+  static constexpr int kTile = 128 * D * 2;
+  static constexpr int kF0 = 0;              // K rows of the unit
+  static constexpr int kF1 = kTile;          // V rows of the unit
+  static constexpr int kR = 2 * kTile;       // ring: 2 slots x (Q, dO)
+  static constexpr int kCol = kR + 4 * kTile;          // [2 slots][-lse2, -delta][128] fp32
+  static constexpr int kRow = kCol + 2 * 2 * 128 * 4;  // [2 units][128] (klo, khi)
+  static constexpr int kInfo = kRow + 2 * 128 * 8;     // [2 units] {unit, wlo, ntile, -}
+  static constexpr int kStage = kInfo + 64;            // [8 warps][32 rows][16] fp32 epilogue slabs
+  static constexpr int kBar = kStage + kEwWarps * 32 * 16 * 4;
+  static constexpr int kMisc = kBar + 256;
+  static constexpr int kBytes = kMisc + 64;
+  static constexpr int kSmem = kBytes + 1024;
+  static constexpr uint32_t kS = 0, kDP = 128, kDV = 256, kDK = 256 + D;
+};
+static_assert(KvCfg<128>::kSmem <= 227 * 1024, "dK/dV shared memory above 227 KB");
+
+template <int D, int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                   const BwdArgs a) {
+  using Cfg = KvCfg<D>;
+  constexpr int kChunks = D / 64;
+  constexpr bool kGroup = KIND == kDkvGroup;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBar);
+  uint64_t* fixed_full = bars + 0;
+  uint64_t* fixed_empty = bars + 1;
+  uint64_t* ring_full = bars + 2;     // [2]
+  uint64_t* ring_empty = bars + 4;    // [2]
+  uint64_t* col_full = bars + 6;      // [2] the slot's query LSE / Delta are in shared memory
+  uint64_t* s_full = bars + 8;
+  uint64_t* dp_full = bars + 9;
+  uint64_t* p_done = bars + 10;       // P^T of the tile is in TMEM
+  uint64_t* ds_done = bars + 11;      // dS^T of the tile is in TMEM
+  uint64_t* v_done = bars + 12;       // dV += P^T dO of the tile is done (S^T columns free)
+  uint64_t* k_done = bars + 13;       // dK += dS^T Q of the tile is done (dP^T columns free)
+  uint64_t* acc_full = bars + 14;     // the unit's dK, dV are complete
+  uint64_t* info_full = bars + 15;    // [2]
+  uint64_t* info_empty = bars + 17;   // [2]
+  uint64_t* mma_done = bars + 19;
+  int* misc = reinterpret_cast<int*>(smem + Cfg::kMisc);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 0);
+  volatile int* abort = misc + 1;
+  float* colbuf = reinterpret_cast<float*>(smem + Cfg::kCol);
+  int2* rowinfo = reinterpret_cast<int2*>(smem + Cfg::kRow);
+  int4* info = reinterpret_cast<int4*>(smem + Cfg::kInfo);
+  float* stage = reinterpret_cast<float*>(smem + Cfg::kStage);
+
+  const int warp = warp_id(), lane = lane_id();
+  const int nkt = (a.n + kT - 1) / kT;
+  const int n_units = a.B * a.H_kv * nkt;
+  const int heads = a.H / a.H_kv;
+
+  if (threadIdx.x == 0) {
+    mbar_init(fixed_full, 1);
+    mbar_init(fixed_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&ring_full[s], 1);
+      mbar_init(&ring_empty[s], 1);
+      mbar_init(&col_full[s], 32);
+      mbar_init(&info_full[s], 1);
+      mbar_init(&info_empty[s], kEwWarps + 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(p_done, kEwWarps);
+    mbar_init(ds_done, kEwWarps);
+    mbar_init(v_done, 1);
+    mbar_init(k_done, 1);
+    mbar_init(acc_full, 1);
+    mbar_init(mma_done, 1);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) tmem_alloc(tmem_slot, 512);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kWarpLd) {
+    // ------------------------------------------- unit names, ranges, loads ---
+    bool ok = true;
+    int g = 0, uf = 0, snake = 0;
+    // Names unit k, finds every row's kept query range [klo, khi] (slots in the
+    // group kind, tokens in the window kind) and publishes both; runs one unit
+    // ahead of the loads, so the searches overlap the previous unit's tiles.
+    auto name_unit = [&](int k, int& u, BUnit& U, int& wlo, int& ntile) -> bool {
+      u = -1;
+      if (kGroup) {
+        if (lane == 0) u = atomicAdd(a.ticket, 1);
+        u = __shfl_sync(0xffffffffu, u, 0);
+        if (u >= n_units) u = -1;
+      } else {
+        for (;;) {
+          u = bwd_snake(snake++, n_units);
+          if (u != -2) break;
+        }
+      }
+      bool fine = !(k >= 2 && !mbar_wait_nap(&info_empty[k & 1], ((k >> 1) - 1) & 1, abort, a.err));
+      if (!__all_sync(0xffffffffu, fine)) return false;
+      wlo = 0;
+      ntile = 0;
+      int lo = 0x7fffffff, hi = -1;
+      if (u >= 0) {
+        U = decode<KIND>(a, u);
+        const size_t pn = static_cast<size_t>(U.prob) * a.n;
+        int klo[4], khi[4];
+        if (kGroup) {
+          // four rows per lane, their binary searches interleaved
+          const int32_t* off = a.offsets + static_cast<size_t>(U.prob) * (a.groups + 1);
+          int us[4], tg[4], gl[4], gh[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int rr = lane + 32 * j;
+            us[j] = U.row0 + rr;
+            const bool v = rr < U.nrows;
+            tg[j] = v ? a.perm[pn + us[j]] + a.w : 0;
+            gl[j] = 0;
+            gh[j] = v ? a.groups : 1;
+          }
+          for (;;) {   // the slot's group: off[gl] <= slot < off[gl + 1]
+            bool more = false;
+            int val[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) val[j] = gh[j] - gl[j] > 1 ? off[(gl[j] + gh[j]) >> 1] : 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (gh[j] - gl[j] > 1) {
+                const int mid = (gl[j] + gh[j]) >> 1;
+                if (val[j] <= us[j]) gl[j] = mid; else gh[j] = mid;
+                more = more || gh[j] - gl[j] > 1;
+              }
+            if (!more) break;
+          }
+          int s0[4], s1[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const bool v = lane + 32 * j < U.nrows;
+            s1[j] = v ? off[gl[j] + 1] : 0;
+            s0[j] = v ? us[j] + 1 : 0;
+            khi[j] = v ? s1[j] - 1 : 0;
+            if (!v) {
+              s0[j] = 1;
+              s1[j] = 1;
+            }
+          }
+          for (;;) {   // first later slot of the group at or past position + w
+            bool more = false;
+            int val[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) val[j] = s0[j] < s1[j] ? a.perm[pn + ((s0[j] + s1[j]) >> 1)] : 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (s0[j] < s1[j]) {
+                const int mid = (s0[j] + s1[j]) >> 1;
+                if (val[j] < tg[j]) s0[j] = mid + 1; else s1[j] = mid;
+                more = more || s0[j] < s1[j];
+              }
+            if (!more) break;
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) klo[j] = s0[j];
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int rp = U.row0 + lane + 32 * j;
+            klo[j] = rp;
+            khi[j] = min(a.n - 1, rp + a.w - 1);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int rr = lane + 32 * j;
+          if (rr >= U.nrows) {
+            klo[j] = 1;
+            khi[j] = 0;
+          }
+          rowinfo[(k & 1) * 128 + rr] = make_int2(klo[j], khi[j]);
+          if (klo[j] <= khi[j]) {
+            lo = min(lo, klo[j]);
+            hi = max(hi, khi[j]);
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+          hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+        }
+        if (hi >= lo) {
+          wlo = lo;
+          ntile = (hi - lo) / kT + 1;
+        }
+      }
+      if (lane == 0) info[k & 1] = make_int4(u, wlo, ntile, 0);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&info_full[k & 1]);
+      return true;
+    };
+    int u = -1, wlo = 0, ntile = 0;
+    BUnit U{};
+    ok = name_unit(0, u, U, wlo, ntile);
+    for (int k = 0; ok && u >= 0; ++k) {
+      int u1 = -1, wlo1 = 0, ntile1 = 0;
+      BUnit U1{};
+      if (!name_unit(k + 1, u1, U1, wlo1, ntile1)) {
+        ok = false;
+        break;
+      }
+      const int ntot = ntile * heads;
+      for (int i = 0; i < ntot; ++i, ++g) {
+        const int sl = g & 1;
+        if (g >= 2 && !mbar_wait_nap(&ring_empty[sl], ((g >> 1) - 1) & 1, abort, a.err)) ok = false;
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        const int t = i % ntile, hh = i / ntile;
+        const int zq = U.b * a.H + U.h + hh;
+        const int y = wlo + t * kT;
+        uint8_t* r0 = smem + Cfg::kR + sl * 2 * Cfg::kTile;
+        if (lane == 0) {
+          mbar_expect_tx(&ring_full[sl], 2 * Cfg::kTile);
+#pragma unroll
+          for (int ch = 0; ch < kChunks; ++ch) {
+            tma_load_3d(r0 + ch * Cfg::kChunk, &tm_q, &ring_full[sl], ch * 64, y, zq);
+            tma_load_3d(r0 + Cfg::kTile + ch * Cfg::kChunk, &tm_do, &ring_full[sl], ch * 64, y, zq);
+          }
+        }
+        // the tile's query columns: -LSE (log2 units) and -Delta of head h + hh
+        float* cb = colbuf + sl * 256;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int c = 4 * lane + j;
+          const int q = y + c;
+          float l2 = 0.f, dl = 0.f;
+          if (q < a.n) {
+            const size_t qi = static_cast<size_t>(zq) * a.n + q;
+            l2 = (kGroup ? a.lse_sorted : a.lse)[qi] * kLog2e;
+            dl = (kGroup ? a.delta_sorted : a.delta)[qi];
+          }
+          cb[c] = -l2;
+          cb[128 + c] = -dl;
+        }
+        mbar_arrive(&col_full[sl]);
+        if (i == 0) {
+          // the unit's K and V rows, once the previous unit's last S^T and dP^T are done
+          if (uf > 0 && !mbar_wait_nap(fixed_empty, (uf - 1) & 1, abort, a.err)) ok = false;
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) {
+            ++g;
+            break;
+          }
+          if (lane == 0) {
+            mbar_expect_tx(fixed_full, 2 * Cfg::kTile);
+#pragma unroll
+            for (int ch = 0; ch < kChunks; ++ch) {
+              tma_load_3d(smem + Cfg::kF0 + ch * Cfg::kChunk, &tm_k, fixed_full, ch * 64, U.row0, U.zkv);
+              tma_load_3d(smem + Cfg::kF1 + ch * Cfg::kChunk, &tm_v, fixed_full, ch * 64, U.row0, U.zkv);
+            }
+          }
+          ++uf;
+        }
+      }
+      u = u1;
+      U = U1;
+      wlo = wlo1;
+      ntile = ntile1;
+    }
+    if ((*abort || !ok) && lane == 0) {
+      // copies already issued must land before the CTA exits
+      if (uf > 0) {
+        const unsigned long long t0 = global_ns();
+        while (!mbar_try_wait(fixed_full, (uf - 1) & 1) && global_ns() - t0 < kWaitTimeoutNs) {}
+      }
+      for (int x = max(0, g - 2); x < g; ++x) {
+        const unsigned long long t1 = global_ns();
+        while (!mbar_try_wait(&ring_full[x & 1], (x >> 1) & 1) && global_ns() - t1 < kWaitTimeoutNs) {}
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------- MMAs ---
+    bool ok = true;
+    int g = 0, uf = 0;
+    constexpr uint32_t idS = idesc_bf16_f32(128, kT, false, false);
+    constexpr uint32_t idAcc = idesc_bf16_f32(128, D, false, true);
+    constexpr uint32_t dhi = sw128_desc_hi();
+    const uint32_t f0 = sw128_desc_lo(smem_u32(smem + Cfg::kF0), 16);
+    const uint32_t f1 = sw128_desc_lo(smem_u32(smem + Cfg::kF1), 16);
+    for (int k = 0; ok; ++k) {
+      if (!warp_wait(&info_full[k & 1], (k >> 1) & 1, abort, a.err)) { ok = false; break; }
+      const int4 in = info[k & 1];
+      warp_arrive(&info_empty[k & 1], lane);
+      if (in.x < 0) break;
+      const int ntot = in.z * heads;
+      if (ntot == 0) continue;
+      if (lane == 0) {
+        // S^T = K Q^T of tile x into TMEM columns 0..127, once dV of tile x - 1 has read its P^T
+        auto issue_s = [&](int x) -> bool {
+          if (!mbar_wait_nap(&ring_full[x & 1], (x >> 1) & 1, abort, a.err) ||
+              (x > 0 && !mbar_wait_nap(v_done, (x - 1) & 1, abort, a.err)))
+            return false;
+          tc_fence_after();
+          const uint32_t r0k = sw128_desc_lo(smem_u32(smem + Cfg::kR + (x & 1) * 2 * Cfg::kTile), 16);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * Cfg::kChunk + (kk & 3) * 32) >> 4;
+            mma_ss(tmem + Cfg::kS, desc_join(f0 + off, dhi), desc_join(r0k + off, dhi), idS, kk > 0);
+          }
+          mma_commit(s_full);
+          return true;
+        };
+        // Per tile the pipe runs dP^T(g), dV(g), S^T(g + 1), dK(g): the next
+        // tile's S^T goes ahead of dK, which waits for the elementwise dS^T.
+        ok = mbar_wait_nap(fixed_full, uf & 1, abort, a.err) && issue_s(g);
+        for (int i = 0; i < ntot && ok; ++i, ++g) {
+          const int sl = g & 1;
+          const uint32_t rb = smem_u32(smem + Cfg::kR + sl * 2 * Cfg::kTile);
+          const uint32_t r1k = sw128_desc_lo(rb + Cfg::kTile, 16);
+          if (g > 0 && !mbar_wait_nap(k_done, (g - 1) & 1, abort, a.err)) { ok = false; break; }
+          tc_fence_after();
+          // dP^T = V dO^T
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * Cfg::kChunk + (kk & 3) * 32) >> 4;
+            mma_ss(tmem + Cfg::kDP, desc_join(f1 + off, dhi), desc_join(r1k + off, dhi), idS, kk > 0);
+          }
+          mma_commit(dp_full);
+          if (i == ntot - 1) mma_commit(fixed_empty);
+          // dV += P^T dO (P^T packed over S^T: queries 64h.. at columns 64h..64h+31)
+          const uint32_t r0m = sw128_desc_lo(rb, Cfg::kChunk), r1m = sw128_desc_lo(rb + Cfg::kTile, Cfg::kChunk);
+          if (!mbar_wait_nap(p_done, g & 1, abort, a.err)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kT / 16; ++kk)
+            mma_ts(tmem + Cfg::kDV, tmem + Cfg::kS + 64 * (kk >> 2) + 8 * (kk & 3),
+                   desc_join(r1m + kk * ((16 * 128) >> 4), dhi), idAcc, i > 0 || kk > 0);
+          mma_commit(v_done);
+          if (i + 1 < ntot && !issue_s(g + 1)) { ok = false; break; }
+          // dK += dS^T Q (dS^T packed over dP^T the same way)
+          if (!mbar_wait_nap(ds_done, g & 1, abort, a.err)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kT / 16; ++kk)
+            mma_ts(tmem + Cfg::kDK, tmem + Cfg::kDP + 64 * (kk >> 2) + 8 * (kk & 3),
+                   desc_join(r0m + kk * ((16 * 128) >> 4), dhi), idAcc, i > 0 || kk > 0);
+          mma_commit(k_done);
+          mma_commit(&ring_empty[sl]);
+          if (i == ntot - 1) mma_commit(acc_full);
+        }
+        ++uf;
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      g = __shfl_sync(0xffffffffu, g, 0);
+    }
+    if (lane == 0) {
+      // every MMA issued above has finished before TMEM is released
+      mma_commit(mma_done);
+      const unsigned long long t0 = global_ns();
+      while (!mbar_try_wait(mma_done, 0) && global_ns() - t0 < kWaitTimeoutNs) {}
+    }
+  } else if (warp < kEwWarps) {
+    // ------------------------------------------------------ elementwise ---
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int r = (warp & 3) * 32 + lane;
+    const int half = (warp >> 2) & 1;   // which half of the query columns
+    const float sl2 = a.scale_log2;
+    bool ok = true;
+    int g = 0, uf = 0;
+    for (int k = 0; ok; ++k) {
+      if (!warp_wait(&info_full[k & 1], (k >> 1) & 1, abort, a.err)) { ok = false; break; }
+      const int4 in = info[k & 1];
+      const int2 kr = rowinfo[(k & 1) * 128 + r];
+      warp_arrive(&info_empty[k & 1], lane);
+      if (in.x < 0) break;
+      const BUnit U = decode<KIND>(a, in.x);
+      const int wlo = in.y, ntile = in.z, ntot = ntile * heads;
+      const size_t pn = static_cast<size_t>(U.prob) * a.n;
+      const bool row_ok = r < U.nrows;
+      const int rpos = row_ok ? (kGroup ? a.perm[pn + U.row0 + r] : U.row0 + r) : 0;
+      const int klo = kr.x, khi = kr.y;
+      const uint64_t sc2 = f2_pack(sl2, sl2);
+      for (int i = 0; i < ntot; ++i, ++g) {
+        if (!kGroup && row_ok && i == max(0, ntot - 3)) {
+          // the epilogue's far parts, three tiles ahead so that they are in L2 when read
+          const size_t o = (static_cast<size_t>(U.zkv) * a.n + rpos) * D + half * (D / 2);
+#pragma unroll
+          for (int q = 0; q < D / 2; q += 32) {
+            prefetch_l2(a.dv_far + o + q);
+            prefetch_l2(a.dk_far + o + q);
+          }
+        }
+        const int t = i % ntile;
+        const float* cb = colbuf + (g & 1) * 256;   // [-lse2 x128, -delta x128] of this tile's queries
+        const int c0 = wlo + t * kT + half * 64;    // query index of this half's first column
+        // bit e: the row keeps column c0 + e
+        const int lo = max(klo - c0, 0), hi = min(khi - c0, 63);
+        const uint64_t keepm = (row_ok && lo <= hi) ? ((~0ull >> (63 - hi)) & (~0ull << lo)) : 0ull;
+        const bool full = __all_sync(0xffffffffu, keepm == ~0ull);
+        if (!warp_wait(&col_full[g & 1], (g >> 1) & 1, abort, a.err)) { ok = false; break; }
+        if (!warp_wait(s_full, g & 1, abort, a.err)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t sv[64];
+        tmem_ld32(tmem + lane_base + Cfg::kS + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+        tmem_ld32(tmem + lane_base + Cfg::kS + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+        tmem_wait_ld();
+        // P = 2^(s scale log2e - lse2) in packed pairs; a dropped pair gets
+        // exp2(-inf) = +0, no branch around the exponential
+        const uint64_t* nl = reinterpret_cast<const uint64_t*>(cb + half * 64);
+        uint64_t p2[32];
+        uint32_t pk[32];
+        if (full) {
+#pragma unroll
+          for (int e = 0; e < 64; e += 2) {
+            float t0, t1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sc2, nl[e / 2]), t0, t1);
+            const float q0 = ex2f(t0), q1 = ex2f(t1);
+            p2[e / 2] = f2_pack(q0, q1);
+            pk[e / 2] = pack_bf16x2(q0, q1);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; e += 2) {
+            float t0, t1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sc2, nl[e / 2]), t0, t1);
+            const float q0 = ex2f((keepm >> e) & 1 ? t0 : -INFINITY);
+            const float q1 = ex2f((keepm >> (e + 1)) & 1 ? t1 : -INFINITY);
+            p2[e / 2] = f2_pack(q0, q1);
+            pk[e / 2] = pack_bf16x2(q0, q1);
+          }
+        }
+        // P^T over the first 32 of this half's 64 S^T columns
+        tmem_st32(tmem + lane_base + Cfg::kS + half * 64, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        warp_arrive(p_done, lane);
+        if (!warp_wait(dp_full, g & 1, abort, a.err)) { ok = false; break; }
+        tc_fence_after();
+        // dS = P (dP - Delta) in packed pairs, 32 columns of dP^T at a time
+        const uint64_t* nd = reinterpret_cast<const uint64_t*>(cb + 128 + half * 64);
+#pragma unroll
+        for (int hq = 0; hq < 2; ++hq) {
+          uint32_t dv[32];
+          tmem_ld32(tmem + lane_base + Cfg::kDP + half * 64 + 32 * hq, dv);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const int q = 16 * hq + e / 2;
+            float d0, d1;
+            f2_unpack(f2_mul(p2[q], f2_add(f2_pack(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])), nd[q])), d0, d1);
+            pk[q] = pack_bf16x2(d0, d1);
+          }
+        }
+        // dS^T over the first 32 of this half's 64 dP^T columns
+        tmem_st32(tmem + lane_base + Cfg::kDP + half * 64, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        warp_arrive(ds_done, lane);
+      }
+      if (!ok) break;
+      // epilogue: this half's dV and dK columns [half * D/2, (half + 1) * D/2)
+      const bool have = ntot > 0;
+      if (have) {
+        if (!warp_wait(acc_full, uf & 1, abort, a.err)) { ok = false; break; }
+        ++uf;
+        tc_fence_after();
+      }
+      // Each thread holds its row's values; they go through this warp's 32 x 16
+      // fp32 slab in shared memory (16-byte pieces at slot piece ^ ((row >> 1) & 3),
+      // so neither the row writes nor the column reads conflict) and leave as
+      // 64-byte runs of one row per four lanes.
+      float* stg = stage + warp * 512;
+      const int jr = lane >> 2, kq = lane & 3;
+      const size_t zrow = static_cast<size_t>(U.zkv) * a.n;
+      int rp4[4];          // token of pass row 8i + jr
+      bool ok4[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        rp4[i] = __shfl_sync(0xffffffffu, rpos, 8 * i + jr);
+        ok4[i] = (warp & 3) * 32 + 8 * i + jr < U.nrows;
+      }
+#pragma unroll
+      for (int cm = 0; cm < D / 32; ++cm) {      // (32-column group of this half, dV or dK)
+        const int c = half * (D / 64) + (cm >> 1), m = cm & 1;
+        const float mul = m ? a.scale : 1.f;     // dK carries the softmax scale
+        float* far = m ? a.dk_far : a.dv_far;
+        // window kind: the far parts of the group's eight row pieces, in flight
+        // while the accumulator is read and staged
+        float4 fv[8];
+        if (!kGroup) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int i = q & 3, s16 = q >> 2;
+            fv[q] = ok4[i] ? *reinterpret_cast<const float4*>(far + (zrow + rp4[i]) * D + c * 32 + s16 * 16 + 4 * kq)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+        uint32_t x[32];
+        if (have) {
+          tmem_ld32(tmem + lane_base + (m ? Cfg::kDK : Cfg::kDV) + c * 32, x);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x[e] = 0u;
+        }
+#pragma unroll
+        for (int s16 = 0; s16 < 2; ++s16) {    // 16-column pieces of the 32
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int e = 16 * s16 + 4 * k;
+            *reinterpret_cast<float4*>(stg + lane * 16 + 4 * (k ^ ((lane >> 1) & 3))) =
+                make_float4(__uint_as_float(x[e]) * mul, __uint_as_float(x[e + 1]) * mul,
+                            __uint_as_float(x[e + 2]) * mul, __uint_as_float(x[e + 3]) * mul);
+          }
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int j = 8 * i + jr;            // row of this warp's 32
+            const float4 v = *reinterpret_cast<const float4*>(stg + j * 16 + 4 * (kq ^ ((j >> 1) & 3)));
+            if (ok4[i]) {
+              const size_t o = (zrow + rp4[i]) * D + c * 32 + s16 * 16 + 4 * kq;
+              if (kGroup) {
+                *reinterpret_cast<float4*>(far + o) = v;
+              } else {
+                const float4 f = fv[4 * s16 + i];
+                __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(m ? a.dK : a.dV);
+                *reinterpret_cast<uint2*>(dst + o) =
+                    make_uint2(pack_bf16x2(v.x + f.x, v.y + f.y), pack_bf16x2(v.z + f.z, v.w + f.w));
+              }
+            }
           }
         }
       }
@@ -881,7 +1073,6 @@ template <int D>
 cudaError_t launch_d(const BwdArgs& a, const CUtensorMap* qs, const CUtensorMap* dos, const CUtensorMap* ks,
                      const CUtensorMap* vs, const CUtensorMap* q3, const CUtensorMap* do3, const CUtensorMap* k3,
                      const CUtensorMap* v3, int max_items, int num_sms, cudaStream_t st) {
-  using Cfg = BCfg<D>;
   const int hpa = a.A == 1 ? a.H : a.H / a.H_kv;
   const long long g_units = static_cast<long long>(max_items) * hpa;
   const long long q_units = static_cast<long long>(a.B) * a.H * ((a.n + kT - 1) / kT);
@@ -892,22 +1083,23 @@ cudaError_t launch_d(const BwdArgs& a, const CUtensorMap* qs, const CUtensorMap*
         *qs, *dos, *ks, *vs, a);
   bwd_dq_kernel<D, kDqLocal><<<static_cast<unsigned>(std::min(q_units, sms)), kThreads, DqCfg<D>::kSmem, st>>>(
       *q3, *do3, *k3, *v3, a);
-  bwd_tc_kernel<D, kDkvGroup><<<static_cast<unsigned>(k_units), kThreads, Cfg::kSmem, st>>>(*qs, *dos, *ks, *vs, a);
-  bwd_tc_kernel<D, kDkvLocal><<<static_cast<unsigned>(k_units), kThreads, Cfg::kSmem, st>>>(*q3, *do3, *k3, *v3, a);
+  const unsigned kv_grid = static_cast<unsigned>(std::min(k_units, sms));
+  bwd_dkv_kernel<D, kDkvGroup><<<kv_grid, kThreads, KvCfg<D>::kSmem, st>>>(*qs, *dos, *ks, *vs, a);
+  bwd_dkv_kernel<D, kDkvLocal><<<kv_grid, kThreads, KvCfg<D>::kSmem, st>>>(*q3, *do3, *k3, *v3, a);
   return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t set_smem_d() {
-  using Cfg = BCfg<D>;
   cudaError_t e;
   e = cudaFuncSetAttribute(bwd_dq_kernel<D, kDqGroup>, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kSmem);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(bwd_dq_kernel<D, kDqLocal>, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kSmem);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(bwd_tc_kernel<D, kDkvGroup>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+  e = cudaFuncSetAttribute(bwd_dkv_kernel<D, kDkvGroup>, cudaFuncAttributeMaxDynamicSharedMemorySize, KvCfg<D>::kSmem);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(bwd_tc_kernel<D, kDkvLocal>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+  return cudaFuncSetAttribute(bwd_dkv_kernel<D, kDkvLocal>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              KvCfg<D>::kSmem);
 }
 
 }  // namespace

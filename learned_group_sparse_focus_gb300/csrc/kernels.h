@@ -208,6 +208,7 @@ struct BwdArgs {
   float scale, scale_log2;
   int* err;                         // device error word (bounded waits)
   const float *lse_sorted, *delta_sorted;  // bf16 path: LSE and Delta in each head's index order
+  int* ticket;                      // bf16 path: unit counter of the far dK/dV kernel, zero at launch
 };
 cudaError_t launch_attn_bwd(const BwdArgs& a, int dtype, int max_items, cudaStream_t st);
 cudaError_t launch_bwd_delta(const BwdArgs& a, int dtype, cudaStream_t st);
