@@ -348,6 +348,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = a.scale_log2;
     bool ok = true;
     int g = 0, uf = 0;
+    // window kind: the next unit's LSE, Delta and far flag, loaded one unit ahead
+    int nu = -1;
+    float n_lse = 0.f, n_dlt = 0.f;
+    bool n_far = false;
     for (int k = 0; ok; ++k) {
       const int u = bwd_snake(k, n_units);
       if (u == -1) break;
@@ -359,7 +363,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       int rpos = -1, klo = 1, khi = 0;
       float lse2 = 0.f, dlt = 0.f;
       bool far = false;
-      if (row_ok) {
+      if (KIND == kDqLocal && u == nu) {
+        if (row_ok) {
+          rpos = U.row0 + r;
+          klo = rpos - a.w + 1;
+          khi = rpos;
+          lse2 = n_lse * kLog2e;
+          dlt = n_dlt;
+          far = n_far;
+        }
+      } else if (row_ok) {
         if (KIND == kDqGroup) {
           rpos = a.perm[pn + U.row0 + r];
           klo = 0;
@@ -373,6 +386,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         lse2 = a.lse[qi] * kLog2e;
         dlt = a.delta[qi];
         if (KIND == kDqLocal) far = a.farlen_tok[pn + rpos] > 0;   // read by the epilogue
+      }
+      if (KIND == kDqLocal) {
+        nu = bwd_snake(k + 1, n_units);
+        if (nu >= 0) {
+          const BUnit N = decode<KIND>(a, nu);
+          if (r < N.nrows) {
+            const size_t qi = static_cast<size_t>(N.zq) * a.n + N.row0 + r;
+            n_lse = a.lse[qi];
+            n_dlt = a.delta[qi];
+            n_far = a.farlen_tok[static_cast<size_t>(N.prob) * a.n + N.row0 + r] > 0;
+          }
+        }
       }
       const uint64_t sc2 = f2_pack(sl2, sl2), nl2 = f2_pack(-lse2, -lse2), nd2 = f2_pack(-dlt, -dlt);
       for (int t = 0; t < U.ntile; ++t, ++g) {
@@ -389,36 +414,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool full = __all_sync(0xffffffffu, keepm == ~0ull);
         if (!warp_wait(sp_full, g & 1, abort, a.err)) { ok = false; break; }
         tc_fence_after();
-        // this half's 64 columns of S and dP
-        uint32_t sv[64], dv[64];
-        tmem_ld32(tmem + lane_base + Cfg::kS + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-        tmem_ld32(tmem + lane_base + Cfg::kS + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-        tmem_ld32(tmem + lane_base + Cfg::kDP + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&dv[0]));
-        tmem_ld32(tmem + lane_base + Cfg::kDP + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&dv[32]));
-        tmem_wait_ld();
-        tc_fence_before();
-        warp_arrive(read_done, lane);
-        // dS = P (dP - Delta), P = 2^(s scale log2e - lse2), in packed pairs; a
-        // dropped pair gets exp2(-inf) = +0, no branch around the exponential
+        // this half's 64 columns of S and dP, 32 at a time (the second pair of
+        // reads releases S and dP to the next tile's products); dS = P (dP - Delta)
+        // with P = 2^(s scale log2e - lse2) in packed pairs, a dropped pair
+        // getting exp2(-inf) = +0 with no branch around the exponential
         uint32_t dd[32];
-        if (full) {
 #pragma unroll
-          for (int e = 0; e < 64; e += 2) {
-            float t0, t1, d0, d1;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sc2, nl2), t0, t1);
-            const uint64_t q = f2_pack(ex2f(t0), ex2f(t1));
-            f2_unpack(f2_mul(q, f2_add(f2_pack(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])), nd2)), d0, d1);
-            dd[e / 2] = pack_bf16x2(d0, d1);
+        for (int hq = 0; hq < 2; ++hq) {
+          uint32_t sv[32], dv[32];
+          tmem_ld32(tmem + lane_base + Cfg::kS + half * 64 + 32 * hq, sv);
+          tmem_ld32(tmem + lane_base + Cfg::kDP + half * 64 + 32 * hq, dv);
+          tmem_wait_ld();
+          if (hq == 1) {
+            tc_fence_before();
+            warp_arrive(read_done, lane);
           }
-        } else {
+          if (full) {
 #pragma unroll
-          for (int e = 0; e < 64; e += 2) {
-            float t0, t1, d0, d1;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sc2, nl2), t0, t1);
-            const uint64_t q = f2_pack(ex2f((keepm >> e) & 1 ? t0 : -INFINITY),
-                                       ex2f((keepm >> (e + 1)) & 1 ? t1 : -INFINITY));
-            f2_unpack(f2_mul(q, f2_add(f2_pack(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])), nd2)), d0, d1);
-            dd[e / 2] = pack_bf16x2(d0, d1);
+            for (int e = 0; e < 32; e += 2) {
+              float t0, t1, d0, d1;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sc2, nl2), t0, t1);
+              const uint64_t q = f2_pack(ex2f(t0), ex2f(t1));
+              f2_unpack(f2_mul(q, f2_add(f2_pack(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])), nd2)), d0, d1);
+              dd[16 * hq + e / 2] = pack_bf16x2(d0, d1);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const int b0 = 32 * hq + e;
+              float t0, t1, d0, d1;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sc2, nl2), t0, t1);
+              const uint64_t q = f2_pack(ex2f((keepm >> b0) & 1 ? t0 : -INFINITY),
+                                         ex2f((keepm >> (b0 + 1)) & 1 ? t1 : -INFINITY));
+              f2_unpack(f2_mul(q, f2_add(f2_pack(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])), nd2)), d0, d1);
+              dd[16 * hq + e / 2] = pack_bf16x2(d0, d1);
+            }
           }
         }
         // the half's 64 bf16 values take packed columns 32*half .. 32*half + 31 of dS(g)
@@ -504,8 +534,8 @@ struct KvCfg {
   static constexpr int kF0 = 0;              // K rows of the unit
   static constexpr int kF1 = kTile;          // V rows of the unit
   static constexpr int kR = 2 * kTile;       // ring: 2 slots x (Q, dO)
-  static constexpr int kCol = kR + 4 * kTile;          // [2 slots][-lse2, -delta][128] fp32
-  static constexpr int kRow = kCol + 2 * 2 * 128 * 4;  // [2 units][128] (klo, khi)
+  static constexpr int kCol = kR + 4 * kTile;          // [4 slots][-lse2, -delta][128] fp32
+  static constexpr int kRow = kCol + 4 * 2 * 128 * 4;  // [2 units][128] (klo, khi)
   static constexpr int kInfo = kRow + 2 * 128 * 8;     // [2 units] {unit, wlo, ntile, -}
   static constexpr int kStage = kInfo + 64;            // [8 warps][32 rows][16] fp32 epilogue slabs
   static constexpr int kBar = kStage + kEwWarps * 32 * 16 * 4;
@@ -531,17 +561,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* fixed_empty = bars + 1;
   uint64_t* ring_full = bars + 2;     // [2]
   uint64_t* ring_empty = bars + 4;    // [2]
-  uint64_t* col_full = bars + 6;      // [2] the slot's query LSE / Delta are in shared memory
-  uint64_t* s_full = bars + 8;
-  uint64_t* dp_full = bars + 9;
-  uint64_t* p_done = bars + 10;       // P^T of the tile is in TMEM
-  uint64_t* ds_done = bars + 11;      // dS^T of the tile is in TMEM
-  uint64_t* v_done = bars + 12;       // dV += P^T dO of the tile is done (S^T columns free)
-  uint64_t* k_done = bars + 13;       // dK += dS^T Q of the tile is done (dP^T columns free)
-  uint64_t* acc_full = bars + 14;     // the unit's dK, dV are complete
-  uint64_t* info_full = bars + 15;    // [2]
-  uint64_t* info_empty = bars + 17;   // [2]
-  uint64_t* mma_done = bars + 19;
+  uint64_t* col_full = bars + 6;      // [4] the tile's query LSE / Delta are in shared memory
+  uint64_t* s_full = bars + 10;
+  uint64_t* dp_full = bars + 11;
+  uint64_t* p_done = bars + 12;       // P^T of the tile is in TMEM
+  uint64_t* ds_done = bars + 13;      // dS^T of the tile is in TMEM
+  uint64_t* v_done = bars + 14;       // dV += P^T dO of the tile is done (S^T columns free)
+  uint64_t* k_done = bars + 15;       // dK += dS^T Q of the tile is done (dP^T columns free)
+  uint64_t* acc_full = bars + 16;     // the unit's dK, dV are complete
+  uint64_t* info_full = bars + 17;    // [2]
+  uint64_t* info_empty = bars + 19;   // [2]
+  uint64_t* mma_done = bars + 21;
   int* misc = reinterpret_cast<int*>(smem + Cfg::kMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 0);
   volatile int* abort = misc + 1;
@@ -561,10 +591,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ring_full[s], 1);
       mbar_init(&ring_empty[s], 1);
-      mbar_init(&col_full[s], 32);
       mbar_init(&info_full[s], 1);
       mbar_init(&info_empty[s], kEwWarps + 1);
     }
+    for (int s = 0; s < 4; ++s) mbar_init(&col_full[s], 32);
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
     mbar_init(p_done, kEwWarps);
@@ -711,14 +741,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       const int ntot = ntile * heads;
-      for (int i = 0; i < ntot; ++i, ++g) {
+      for (int i = 0, t = 0, hh = 0; i < ntot; ++i, ++g) {
         const int sl = g & 1;
+        const int zq = U.b * a.H + U.h + hh;
+        const int y = wlo + t * kT;
+        // the tile's query columns: -LSE (log2 units) and -Delta of head h + hh,
+        // read from global memory before the ring wait and stored after it
+        float l2[4], dl[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int q = y + 4 * lane + j;
+          l2[j] = dl[j] = 0.f;
+          if (q < a.n) {
+            const size_t qi = static_cast<size_t>(zq) * a.n + q;
+            l2[j] = (kGroup ? a.lse_sorted : a.lse)[qi];
+            dl[j] = (kGroup ? a.delta_sorted : a.delta)[qi];
+          }
+        }
         if (g >= 2 && !mbar_wait_nap(&ring_empty[sl], ((g >> 1) - 1) & 1, abort, a.err)) ok = false;
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        const int t = i % ntile, hh = i / ntile;
-        const int zq = U.b * a.H + U.h + hh;
-        const int y = wlo + t * kT;
         uint8_t* r0 = smem + Cfg::kR + sl * 2 * Cfg::kTile;
         if (lane == 0) {
           mbar_expect_tx(&ring_full[sl], 2 * Cfg::kTile);
@@ -728,22 +770,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(r0 + Cfg::kTile + ch * Cfg::kChunk, &tm_do, &ring_full[sl], ch * 64, y, zq);
           }
         }
-        // the tile's query columns: -LSE (log2 units) and -Delta of head h + hh
-        float* cb = colbuf + sl * 256;
+        float* cb = colbuf + (g & 3) * 256;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const int c = 4 * lane + j;
-          const int q = y + c;
-          float l2 = 0.f, dl = 0.f;
-          if (q < a.n) {
-            const size_t qi = static_cast<size_t>(zq) * a.n + q;
-            l2 = (kGroup ? a.lse_sorted : a.lse)[qi] * kLog2e;
-            dl = (kGroup ? a.delta_sorted : a.delta)[qi];
-          }
-          cb[c] = -l2;
-          cb[128 + c] = -dl;
+          cb[4 * lane + j] = -l2[j] * kLog2e;
+          cb[128 + 4 * lane + j] = -dl[j];
         }
-        mbar_arrive(&col_full[sl]);
+        mbar_arrive(&col_full[g & 3]);
+        if (++t == ntile) {
+          t = 0;
+          ++hh;
+        }
         if (i == 0) {
           // the unit's K and V rows, once the previous unit's last S^T and dP^T are done
           if (uf > 0 && !mbar_wait_nap(fixed_empty, (uf - 1) & 1, abort, a.err)) ok = false;
@@ -881,7 +918,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int rpos = row_ok ? (kGroup ? a.perm[pn + U.row0 + r] : U.row0 + r) : 0;
       const int klo = kr.x, khi = kr.y;
       const uint64_t sc2 = f2_pack(sl2, sl2);
-      for (int i = 0; i < ntot; ++i, ++g) {
+      for (int i = 0, t = 0; i < ntot; ++i, ++g, t = (t + 1 == ntile ? 0 : t + 1)) {
         if (!kGroup && row_ok && i == max(0, ntot - 3)) {
           // the epilogue's far parts, three tiles ahead so that they are in L2 when read
           const size_t o = (static_cast<size_t>(U.zkv) * a.n + rpos) * D + half * (D / 2);
@@ -891,14 +928,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_l2(a.dk_far + o + q);
           }
         }
-        const int t = i % ntile;
-        const float* cb = colbuf + (g & 1) * 256;   // [-lse2 x128, -delta x128] of this tile's queries
+        const float* cb = colbuf + (g & 3) * 256;   // [-lse2 x128, -delta x128] of this tile's queries
         const int c0 = wlo + t * kT + half * 64;    // query index of this half's first column
         // bit e: the row keeps column c0 + e
         const int lo = max(klo - c0, 0), hi = min(khi - c0, 63);
         const uint64_t keepm = (row_ok && lo <= hi) ? ((~0ull >> (63 - hi)) & (~0ull << lo)) : 0ull;
         const bool full = __all_sync(0xffffffffu, keepm == ~0ull);
-        if (!warp_wait(&col_full[g & 1], (g >> 1) & 1, abort, a.err)) { ok = false; break; }
+        if (!warp_wait(&col_full[g & 3], (g >> 2) & 1, abort, a.err)) { ok = false; break; }
         if (!warp_wait(s_full, g & 1, abort, a.err)) { ok = false; break; }
         tc_fence_after();
         uint32_t sv[64];
