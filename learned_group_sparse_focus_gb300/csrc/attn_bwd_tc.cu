@@ -176,6 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* ew_done = bars + 14;      // [2] the tile's dS is in TMEM
   uint64_t* acc_full = bars + 16;     // the unit's dQ is complete
   uint64_t* mma_done = bars + 17;
+  uint64_t* stage_free = bars + 18;   // [2] by unit parity: the unit's epilogue is done with its slabs
   int* misc = reinterpret_cast<int*>(smem + Cfg::kMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 0);
   volatile int* abort = misc + 1;
@@ -201,6 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ew_done[1], kEwWarps);
     mbar_init(acc_full, 1);
     mbar_init(mma_done, 1);
+    mbar_init(&stage_free[0], kEwWarps);
+    mbar_init(&stage_free[1], kEwWarps);
     *abort = 0;
     fence_mbar_init();
   }
@@ -213,6 +216,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ loads ---
     bool ok = true;
     int g = 0, uf = 0;
+    // A unit's epilogue stages its rows in the V slot of the unit's last tile
+    // L; the V load of tile L + 2, the next into that slot, waits for it.
+    // Pending targets L + 2, oldest first (at most two: every unit has a tile).
+    // The barrier alternates with the unit: the epilogue two units later needs
+    // the V load of a tile past L + 2, so neither runs a phase ahead.
+    int st0 = -1, st1 = -1, sw = 0;
     for (int k = 0; ok; ++k) {
       const int u = bwd_snake(k, n_units);
       if (u == -1) break;
@@ -224,6 +233,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (g >= Cfg::kKSlots && !mbar_wait_nap(&k_empty[ks], (g / Cfg::kKSlots - 1) & 1, abort, a.err)) ok = false;
         if (ok && g >= Cfg::kVSlots && !mbar_wait_nap(&v_empty[vs], (g / Cfg::kVSlots - 1) & 1, abort, a.err))
           ok = false;
+        if (ok && g == st0) {
+          if (!mbar_wait_nap(&stage_free[sw & 1], (sw >> 1) & 1, abort, a.err)) ok = false;
+          ++sw;
+          st0 = st1;
+          st1 = -1;
+        }
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         // key slots (group) or key tokens (window) from key0 + t * 128
@@ -257,6 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++uf;
         }
       }
+      if (!ok) break;
+      if (st0 < 0) st0 = g + 1; else st1 = g + 1;   // this unit's L + 2 (g = L + 1 here)
     }
     if ((*abort || !ok) && lane == 0) {
       // copies already issued must land before the CTA exits
@@ -458,50 +475,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         warp_arrive(&ew_done[g & 1], lane);
       }
       if (!ok) break;
-      // epilogue: this half's dQ columns [half * D/2, (half + 1) * D/2) once the unit's products are done
-      const bool have = U.ntile > 0;
-      if (have) {
-        if (!warp_wait(acc_full, uf & 1, abort, a.err)) { ok = false; break; }
-        ++uf;
-        tc_fence_after();
+      // Epilogue: this half's dQ columns [half * D/2, (half + 1) * D/2) once the
+      // unit's products are done.  A unit with no tiles (group kind) has no
+      // far keys in any row, and the window kernel reads none of its rows.
+      if (U.ntile == 0) continue;
+      if (!warp_wait(acc_full, uf & 1, abort, a.err)) { ok = false; break; }
+      ++uf;
+      tc_fence_after();
+      // Each thread holds its row's values; they go through this warp's 32 x 16
+      // fp32 slab (16-byte pieces at slot piece ^ ((row >> 1) & 3), so neither
+      // the row writes nor the column reads conflict) in the V slot of the
+      // unit's last tile, which its products no longer read and the loader
+      // refills only after stage_free, and leave as 64-byte runs of one row per
+      // four lanes.
+      float* stg = reinterpret_cast<float*>(smem + Cfg::kV + ((g - 1) % Cfg::kVSlots) * Cfg::kTile) + warp * 512;
+      const int jr = lane >> 2, kq = lane & 3;
+      const size_t zrow = static_cast<size_t>(U.zq) * a.n;
+      int rp4[4];          // token of pass row 8i + jr
+      bool ok4[4], far4[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        rp4[i] = __shfl_sync(0xffffffffu, rpos, 8 * i + jr);
+        far4[i] = __shfl_sync(0xffffffffu, far ? 1 : 0, 8 * i + jr) != 0;
+        ok4[i] = (warp & 3) * 32 + 8 * i + jr < U.nrows;
       }
-      const size_t orow = static_cast<size_t>(U.zq) * a.n + (rpos >= 0 ? rpos : 0);
-#pragma unroll 1
-      for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
-        uint32_t x0[32];
-        if (have) {
-          tmem_ld32(tmem + lane_base + Cfg::kA + c * 32, x0);
-          tmem_wait_ld();
-        } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) x0[e] = 0u;
+      for (int cc = 0; cc < D / 64; ++cc) {      // this half's 32-column groups
+        const int c = half * (D / 64) + cc;
+        // window kind: the far part of the group's eight row pieces, in flight
+        // while the accumulator is read and staged
+        float4 fv[8];
+        if (KIND == kDqLocal) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int i = q & 3, s16 = q >> 2;
+            fv[q] = ok4[i] && far4[i]
+                        ? *reinterpret_cast<const float4*>(a.dq_far + (zrow + rp4[i]) * D + c * 32 + s16 * 16 + 4 * kq)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
         }
-        if (!row_ok) continue;
-        const size_t o = orow * D + c * 32;
-        if (KIND == kDqGroup) {
-          float4* dst = reinterpret_cast<float4*>(a.dq_far + o);
+        uint32_t x[32];
+        tmem_ld32(tmem + lane_base + Cfg::kA + c * 32, x);
+        tmem_wait_ld();
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            dst[v] = make_float4(__uint_as_float(x0[4 * v]) * a.scale, __uint_as_float(x0[4 * v + 1]) * a.scale,
-                                 __uint_as_float(x0[4 * v + 2]) * a.scale, __uint_as_float(x0[4 * v + 3]) * a.scale);
-        } else {
-          const float4* fq = reinterpret_cast<const float4*>(a.dq_far + o);
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dQ) + o);
+        for (int s16 = 0; s16 < 2; ++s16) {      // 16-column pieces of the 32
+          __syncwarp();
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            float f[8];
+          for (int k = 0; k < 4; ++k) {
+            const int e = 16 * s16 + 4 * k;
+            *reinterpret_cast<float4*>(stg + lane * 16 + 4 * (k ^ ((lane >> 1) & 3))) =
+                make_float4(__uint_as_float(x[e]) * a.scale, __uint_as_float(x[e + 1]) * a.scale,
+                            __uint_as_float(x[e + 2]) * a.scale, __uint_as_float(x[e + 3]) * a.scale);
+          }
+          __syncwarp();
 #pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(x0[8 * v + e]) * a.scale;
-            if (far) {
-              const float4 g0 = fq[2 * v], g1 = fq[2 * v + 1];
-              f[0] += g0.x; f[1] += g0.y; f[2] += g0.z; f[3] += g0.w;
-              f[4] += g1.x; f[5] += g1.y; f[6] += g1.z; f[7] += g1.w;
+          for (int i = 0; i < 4; ++i) {
+            const int j = 8 * i + jr;              // row of this warp's 32
+            const float4 v = *reinterpret_cast<const float4*>(stg + j * 16 + 4 * (kq ^ ((j >> 1) & 3)));
+            if (ok4[i]) {
+              const size_t o = (zrow + rp4[i]) * D + c * 32 + s16 * 16 + 4 * kq;
+              if (KIND == kDqGroup) {
+                *reinterpret_cast<float4*>(a.dq_far + o) = v;
+              } else {
+                const float4 f = fv[4 * s16 + i];
+                *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.dQ) + o) =
+                    make_uint2(pack_bf16x2(v.x + f.x, v.y + f.y), pack_bf16x2(v.z + f.z, v.w + f.w));
+              }
             }
-            dst[v] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
-                                pack_bf16x2(f[6], f[7]));
           }
         }
       }
+      // the slab's generic accesses before the loader's next copy into the slot
+      fence_proxy_async_smem();
+      warp_arrive(&stage_free[(uf - 1) & 1], lane);
       tc_fence_before();
     }
   }
