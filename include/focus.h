@@ -405,7 +405,8 @@ FOCUS_API focus_status_t focus_sinkhorn_fwd(const focus_params_t* p, int32_t ite
  *   16-byte aligned; lse [B, H, n] fp32 from the forward call (lse_opt);
  *   idx from focus_build_index with the same p (in the forward workspace).
  * ws: a backward workspace of focus_backward_workspace_bytes(p) (error word
- * first; fp32 partials; for bf16 also index-ordered copies of Q, dO, K, V).
+ * first; fp32 partials; for bf16 also index-ordered copies of Q, dO, K, V and
+ * the far dK/dV kernel's work order).
  * bf16 runs on the tcgen05 tensor cores (bf16 products, fp32 accumulate and
  * softmax arithmetic); fp32 runs in fp32 on the CUDA cores.  d in {64, 128}.
  * Errors as focus_attention_fwd. */

@@ -975,7 +975,7 @@ focus_status_t focus_sinkhorn_fwd(const focus_params_t* p, int32_t iters, float 
 // ------------------------------------------------------------- backward ---
 
 struct BwdLayout {
-  size_t delta, dq, dk, dv, qs, dos, ks, vs, lse_s, delta_s, total;
+  size_t delta, dq, dk, dv, qs, dos, ks, vs, lse_s, delta_s, kv_order, total;
 };
 
 static BwdLayout backward_layout(const focus_params_t* p) {
@@ -1000,6 +1000,8 @@ static BwdLayout backward_layout(const focus_params_t* p) {
     L.vs = take(krows * p->d * 2);
     L.lse_s = take(qrows * 4);
     L.delta_s = take(qrows * 4);
+    // the far dK/dV kernel's units (128 key slots of one KV head), longest first
+    L.kv_order = take(static_cast<size_t>(p->B) * p->H_kv * ((p->n + 127) / 128) * 4);
   }
   L.total = o;
   return L;
@@ -1073,6 +1075,7 @@ focus_status_t focus_attention_bwd(const focus_params_t* p, const void* Q, const
   a.lse_sorted = at<float>(ws, BL.lse_s);
   a.delta_sorted = at<float>(ws, BL.delta_s);
   a.ticket = at<int>(ws, 0) + 1;   // the word after the error word
+  a.kv_order = at<int32_t>(ws, BL.kv_order);
   // tile maps over the sorted copies (group kernels) and the inputs (window kernels)
   CUtensorMap qs3, dos3, ks3, vs3, q3, do3, k3, v3;
   if (!make_map(&qs3, Qs, p->d, p->n, qplanes, 128, 3) || !make_map(&dos3, dOs, p->d, p->n, qplanes, 128, 3) ||

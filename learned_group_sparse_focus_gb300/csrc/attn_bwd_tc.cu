@@ -667,9 +667,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto name_unit = [&](int k, int& u, BUnit& U, int& wlo, int& ntile) -> bool {
       u = -1;
       if (kGroup) {
-        if (lane == 0) u = atomicAdd(a.ticket, 1);
+        if (lane == 0) {
+          const int tk = atomicAdd(a.ticket, 1);
+          u = tk < n_units ? a.kv_order[tk] : -1;
+        }
         u = __shfl_sync(0xffffffffu, u, 0);
-        if (u >= n_units) u = -1;
       } else {
         for (;;) {
           u = bwd_snake(snake++, n_units);
@@ -1127,6 +1129,48 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// The far dK/dV kernel's units (u = kt + nkt * (kv + H_kv * b)) longest first.
+// A unit's weight is the number of 128-slot tiles from its first key slot to
+// the end of the group of its last one: the query slots that its keys can
+// meet lie in that stretch.  One CTA: counting sort over the weights (1 ..
+// nkt), units of equal weight in any order (each unit owns its rows, so the
+// order changes no result).  Past 12,287 weights it writes the natural order.
+__global__ void __launch_bounds__(1024) kv_order_kernel(const BwdArgs a, int n_units) {
+  extern __shared__ int cnt[];
+  const int nkt = (a.n + kT - 1) / kT;
+  const int nb = nkt + 1;
+  if (nb > 12287) {
+    for (int u = threadIdx.x; u < n_units; u += blockDim.x) a.kv_order[u] = u;
+    return;
+  }
+  auto weight = [&](int u) {
+    const int kt = u % nkt, r = u / nkt;
+    const int kv = r % a.H_kv, b = r / a.H_kv;
+    const int32_t* off = a.offsets + static_cast<size_t>(b * a.A + (a.A == 1 ? 0 : kv)) * (a.groups + 1);
+    const int row0 = kt * kT, last = min(a.n, row0 + kT) - 1;
+    int lo = 0, hi = a.groups;   // off[lo] <= last < off[lo + 1]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (off[mid] <= last) lo = mid; else hi = mid;
+    }
+    return min(nkt, max(1, (off[lo + 1] - row0 + kT - 1) / kT));
+  };
+  for (int i = threadIdx.x; i < nb; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  for (int u = threadIdx.x; u < n_units; u += blockDim.x) atomicAdd(&cnt[weight(u)], 1);
+  __syncthreads();
+  if (threadIdx.x == 0) {   // first position of each weight, heaviest first
+    int run = 0;
+    for (int w = nb - 1; w >= 0; --w) {
+      const int c = cnt[w];
+      cnt[w] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  for (int u = threadIdx.x; u < n_units; u += blockDim.x) a.kv_order[atomicAdd(&cnt[weight(u)], 1)] = u;
+}
+
 // Q, dO rows and the LSE, Delta of every query head in the order of its
 // assignment's index: dst[zq, s] = src[zq, perm_a[s]], a = the head's assignment.
 __global__ void __launch_bounds__(256) permute_q_kernel(BwdArgs a, __nv_bfloat16* Qs, __nv_bfloat16* dOs,
@@ -1166,6 +1210,8 @@ cudaError_t launch_d(const BwdArgs& a, const CUtensorMap* qs, const CUtensorMap*
   bwd_dq_kernel<D, kDqLocal><<<static_cast<unsigned>(std::min(q_units, sms)), kThreads, DqCfg<D>::kSmem, st>>>(
       *q3, *do3, *k3, *v3, a);
   const unsigned kv_grid = static_cast<unsigned>(std::min(k_units, sms));
+  const int nb = (a.n + kT - 1) / kT + 1;
+  kv_order_kernel<<<1, 1024, nb <= 12287 ? nb * 4 : 0, st>>>(a, static_cast<int>(k_units));
   bwd_dkv_kernel<D, kDkvGroup><<<kv_grid, kThreads, KvCfg<D>::kSmem, st>>>(*qs, *dos, *ks, *vs, a);
   bwd_dkv_kernel<D, kDkvLocal><<<kv_grid, kThreads, KvCfg<D>::kSmem, st>>>(*q3, *do3, *k3, *v3, a);
   return cudaGetLastError();

@@ -209,6 +209,7 @@ struct BwdArgs {
   int* err;                         // device error word (bounded waits)
   const float *lse_sorted, *delta_sorted;  // bf16 path: LSE and Delta in each head's index order
   int* ticket;                      // bf16 path: unit counter of the far dK/dV kernel, zero at launch
+  int32_t* kv_order;                // bf16 path: far dK/dV units, longest first [B * H_kv * ceil(n / 128)]
 };
 cudaError_t launch_attn_bwd(const BwdArgs& a, int dtype, int max_items, cudaStream_t st);
 cudaError_t launch_bwd_delta(const BwdArgs& a, int dtype, cudaStream_t st);

@@ -169,8 +169,9 @@ def test_backward_argument_checks(fz):
     need = lib.focus_backward_workspace_bytes(ctypes.byref(p))
     # error word + Delta [4*64] + dQ part [4*64*64] + dK, dV parts [2*64*64] fp32,
     # and for bf16 the index-ordered copies: Q, dO [4*64*64], K, V [2*64*64] bf16,
-    # LSE and Delta [4*64] fp32
-    assert need == 256 + 1024 + 65536 + 2 * 32768 + 2 * 32768 + 2 * 16384 + 2 * 1024
+    # LSE and Delta [4*64] fp32, and the far dK/dV unit order [2 KV heads x 1 tile]
+    # int32 (one 256-byte block)
+    assert need == 256 + 1024 + 65536 + 2 * 32768 + 2 * 32768 + 2 * 16384 + 2 * 1024 + 256
     q = fz.make_params(B=1, H=4, H_kv=2, n=64, d=64, D=64, d_g=32, K=4, A=1, w=8, dtype="f32")
     assert lib.focus_backward_workspace_bytes(ctypes.byref(q)) == 256 + 1024 + 65536 + 2 * 32768
     ok = ctypes.c_void_p(1 << 20)
