@@ -222,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The barrier alternates with the unit: the epilogue two units later needs
     // the V load of a tile past L + 2, so neither runs a phase ahead.
     int st0 = -1, st1 = -1, sw = 0;
+    int kv_half = 0;   // set when the loop stops with tile g's V issued and its K not
     for (int k = 0; ok; ++k) {
       const int u = bwd_snake(k, n_units);
       if (u == -1) break;
@@ -230,9 +231,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!U.valid || U.ntile == 0) continue;
       for (int t = 0; t < U.ntile; ++t, ++g) {
         const int ks = g % Cfg::kKSlots, vs = g % Cfg::kVSlots;
-        if (g >= Cfg::kKSlots && !mbar_wait_nap(&k_empty[ks], (g / Cfg::kKSlots - 1) & 1, abort, a.err)) ok = false;
-        if (ok && g >= Cfg::kVSlots && !mbar_wait_nap(&v_empty[vs], (g / Cfg::kVSlots - 1) & 1, abort, a.err))
-          ok = false;
+        // key slots (group) or key tokens (window) from key0 + t * 128; V first:
+        // its slot frees when the S and dP products are done, K's only after
+        // the dQ product
+        const int y = U.key0 + t * kT;
+        if (g >= Cfg::kVSlots && !mbar_wait_nap(&v_empty[vs], (g / Cfg::kVSlots - 1) & 1, abort, a.err)) ok = false;
         if (ok && g == st0) {
           if (!mbar_wait_nap(&stage_free[sw & 1], (sw >> 1) & 1, abort, a.err)) ok = false;
           ++sw;
@@ -241,17 +244,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        // key slots (group) or key tokens (window) from key0 + t * 128
-        const int y = U.key0 + t * kT;
         if (lane == 0) {
-          uint8_t* dk = smem + Cfg::kK + ks * Cfg::kTile;
           uint8_t* dv = smem + Cfg::kV + vs * Cfg::kTile;
-          mbar_expect_tx(&k_full[ks], Cfg::kTile);
-#pragma unroll
-          for (int ch = 0; ch < kChunks; ++ch) tma_load_3d(dk + ch * Cfg::kChunk, &tm_k, &k_full[ks], ch * 64, y, U.zkv);
           mbar_expect_tx(&v_full[vs], Cfg::kTile);
 #pragma unroll
           for (int ch = 0; ch < kChunks; ++ch) tma_load_3d(dv + ch * Cfg::kChunk, &tm_v, &v_full[vs], ch * 64, y, U.zkv);
+        }
+        if (g >= Cfg::kKSlots && !mbar_wait_nap(&k_empty[ks], (g / Cfg::kKSlots - 1) & 1, abort, a.err)) ok = false;
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+          kv_half = 1;   // V of tile g is in flight, K is not
+          break;
+        }
+        if (lane == 0) {
+          uint8_t* dk = smem + Cfg::kK + ks * Cfg::kTile;
+          mbar_expect_tx(&k_full[ks], Cfg::kTile);
+#pragma unroll
+          for (int ch = 0; ch < kChunks; ++ch) tma_load_3d(dk + ch * Cfg::kChunk, &tm_k, &k_full[ks], ch * 64, y, U.zkv);
         }
         if (t == 0) {
           // the unit's Q and dO rows, once the previous unit's last S and dP are done
@@ -285,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const unsigned long long t1 = global_ns();
         while (!mbar_try_wait(&k_full[x % Cfg::kKSlots], (x / Cfg::kKSlots) & 1) && global_ns() - t1 < kWaitTimeoutNs) {}
       }
-      for (int x = max(0, g - Cfg::kVSlots); x < g; ++x) {
+      for (int x = max(0, g + kv_half - Cfg::kVSlots); x < g + kv_half; ++x) {
         const unsigned long long t1 = global_ns();
         while (!mbar_try_wait(&v_full[x % Cfg::kVSlots], (x / Cfg::kVSlots) & 1) && global_ns() - t1 < kWaitTimeoutNs) {}
       }
