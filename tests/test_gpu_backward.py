@@ -49,7 +49,7 @@ def _close(got, want, dtype, what):
         assert diff.max() <= 1e-4 * M, f"{what}: max {diff.max() / M:.3e} of max|ref|"
 
 
-def _run(fz, dtype, B, H, H_kv, A, n, d, K, w, kind, seed):
+def _run(fz, dtype, B, H, H_kv, A, n, d, K, w, kind, seed, twice=False):
     import torch
     rng = np.random.default_rng(seed)
     store = (lambda a: synth.round_bf16(a)) if dtype == "bf16" else (lambda a: a)
@@ -71,7 +71,13 @@ def _run(fz, dtype, B, H, H_kv, A, n, d, K, w, kind, seed):
     dV = torch.full_like(Vd, float("nan"))
     fz.focus_attention_bwd(p, Qd, Kd, Vd, O, dOd, lse, idx, dQ, dK, dV, wsb)
     assert fz.focus_check_errors(ws) == 0 and fz.focus_check_errors(wsb) == 0
-    return (Q, Kt, V, dO, g, p), (to_host(dQ), to_host(dK), to_host(dV))
+    out = (to_host(dQ), to_host(dK), to_host(dV))
+    if twice:
+        # the same call again on the same workspaces
+        fz.focus_attention_bwd(p, Qd, Kd, Vd, O, dOd, lse, idx, dQ, dK, dV, wsb)
+        assert fz.focus_check_errors(wsb) == 0
+        return (Q, Kt, V, dO, g, p), out, (to_host(dQ), to_host(dK), to_host(dV))
+    return (Q, Kt, V, dO, g, p), out
 
 
 @pytest.mark.parametrize("dtype,B,H,H_kv,A,n,d,K,w,kind", [
@@ -94,6 +100,26 @@ def test_backward_all_rows(fz, dtype, B, H, H_kv, A, n, d, K, w, kind):
     _close(dQ, wQ, dtype, "dQ")
     _close(dK, wK, dtype, "dK")
     _close(dV, wV, dtype, "dV")
+
+
+@pytest.mark.gpu
+def test_backward_many_units_per_cta_all_rows_and_rerun(fz):
+    """More units than the 152 persistent CTAs in every kernel (B = 2, four
+    KV heads with an assignment each, n = 4096: 256 window and key-tile
+    units), so CTAs cross unit boundaries (fixed-tile reload, accumulator
+    reuse, the dQ epilogue's staging slot, the far dK/dV work order over
+    several problems); every element against the oracle, and a second call on
+    the same workspaces must give the same bits (the unit ticket starts again
+    from zero and the order of units changes no result)."""
+    import torch
+    B, H, H_kv, A, n, d, K, w = 2, 4, 4, 4, 4096, 64, 6, 64
+    (Q, Kt, V, dO, g, p), (dQ, dK, dV), (dQ2, dK2, dV2) = _run(fz, "bf16", B, H, H_kv, A, n, d, K, w, "zipf",
+                                                              seed=4107, twice=True)
+    wQ, wK, wV = ref.attention_backward(Q, Kt, V, g, w, p.scale, A, dO)
+    _close(dQ, wQ, "bf16", "dQ")
+    _close(dK, wK, "bf16", "dK")
+    _close(dV, wV, "bf16", "dV")
+    assert np.array_equal(dQ, dQ2) and np.array_equal(dK, dK2) and np.array_equal(dV, dV2)
 
 
 def _key_rows(n, seed):
