@@ -1083,8 +1083,8 @@ focus_status_t focus_attention_bwd(const focus_params_t* p, const void* Q, const
       !make_map(&q3, Q, p->d, p->n, qplanes, 128, 3) || !make_map(&do3, dO, p->d, p->n, qplanes, 128, 3) ||
       !make_map(&k3, K, p->d, p->n, planes, 128, 3) || !make_map(&v3, V, p->d, p->n, planes, 128, 3))
     return FOCUS_ERR_CUDA;
-  cudaError_t e = launch_bwd_delta(a, p->dtype, st);
-  if (e == cudaSuccess) e = launch_bwd_permute_q(a, Qs, dOs, at<float>(ws, BL.lse_s), at<float>(ws, BL.delta_s), st);
+  // Delta comes with the index-order copy of Q, dO, LSE (one read of dO)
+  cudaError_t e = launch_bwd_permute_q(a, Qs, dOs, at<float>(ws, BL.lse_s), at<float>(ws, BL.delta_s), st);
   if (e == cudaSuccess)
     e = launch_permute_kv_bf16(K, V, Ks, Vs, idx->perm, p->B, p->H_kv, p->n, p->n, 0, p->d, p->A, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(a.ticket, 0, sizeof(int), st);

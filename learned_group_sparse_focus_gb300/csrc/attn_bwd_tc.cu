@@ -1180,26 +1180,50 @@ __global__ void __launch_bounds__(1024) kv_order_kernel(const BwdArgs a, int n_u
   for (int u = threadIdx.x; u < n_units; u += blockDim.x) a.kv_order[atomicAdd(&cnt[weight(u)], 1)] = u;
 }
 
-// Q, dO rows and the LSE, Delta of every query head in the order of its
-// assignment's index: dst[zq, s] = src[zq, perm_a[s]], a = the head's assignment.
+// Q, dO rows and the LSE of every query head in the order of its assignment's
+// index, dst[zq, s] = src[zq, perm_a[s]] (a = the head's assignment), and
+// Delta_i = dO_i . O_i (fp32) of every row in both orders.  d / 8 lanes per
+// row, 16 bytes each; the lanes of a row are an aligned group of the warp and
+// every lane of a warp runs every iteration, so the row's shuffle reduction
+// always sees the whole warp.
 __global__ void __launch_bounds__(256) permute_q_kernel(BwdArgs a, __nv_bfloat16* Qs, __nv_bfloat16* dOs,
                                                         float* lse_s, float* delta_s, long long total) {
   const int vpr = a.d / 8;
-  for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < total;
-       e += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long row = e / vpr;
-    const int u = static_cast<int>(e % vpr);
-    const int s = static_cast<int>(row % a.n);
-    const long long zq = row / a.n;
-    const int h = static_cast<int>(zq % a.H);
-    const long long b = zq / a.H;
-    const long long p = b * a.A + (a.A == 1 ? 0 : (h * a.H_kv) / a.H);
-    const long long src = zq * a.n + __ldg(a.perm + p * a.n + s);
-    reinterpret_cast<uint4*>(Qs)[e] = __ldg(reinterpret_cast<const uint4*>(a.Q) + src * vpr + u);
-    reinterpret_cast<uint4*>(dOs)[e] = __ldg(reinterpret_cast<const uint4*>(a.dO) + src * vpr + u);
-    if (u == 0) {
+  const int lane = lane_id();
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long base = blockIdx.x * static_cast<long long>(blockDim.x) + (threadIdx.x & ~31u); base < total;
+       base += stride) {
+    const long long e = base + lane;
+    const bool act = e < total;
+    float dsum = 0.f;
+    long long row = 0, src = 0;
+    int u = 0;
+    if (act) {
+      row = e / vpr;
+      u = static_cast<int>(e % vpr);
+      const int s = static_cast<int>(row % a.n);
+      const long long zq = row / a.n;
+      const int h = static_cast<int>(zq % a.H);
+      const long long b = zq / a.H;
+      const long long p = b * a.A + (a.A == 1 ? 0 : (h * a.H_kv) / a.H);
+      src = zq * a.n + __ldg(a.perm + p * a.n + s);
+      const uint4 q = __ldg(reinterpret_cast<const uint4*>(a.Q) + src * vpr + u);
+      const uint4 g = __ldg(reinterpret_cast<const uint4*>(a.dO) + src * vpr + u);
+      const uint4 o = __ldg(reinterpret_cast<const uint4*>(a.O) + src * vpr + u);
+      reinterpret_cast<uint4*>(Qs)[e] = q;
+      reinterpret_cast<uint4*>(dOs)[e] = g;
+      const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        dsum = fmaf(__uint_as_float(gw[j] << 16), __uint_as_float(ow[j] << 16), dsum);
+        dsum = fmaf(__uint_as_float(gw[j] & 0xffff0000u), __uint_as_float(ow[j] & 0xffff0000u), dsum);
+      }
+    }
+    for (int off = vpr >> 1; off > 0; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
+    if (act && u == 0) {
       lse_s[row] = a.lse[src];
-      delta_s[row] = a.delta[src];
+      delta_s[row] = dsum;
+      a.delta[src] = dsum;
     }
   }
 }

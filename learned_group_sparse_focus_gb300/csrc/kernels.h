@@ -223,8 +223,9 @@ cudaError_t launch_attn_bwd_tc(const BwdArgs& a, const CUtensorMap* qs, const CU
                                const CUtensorMap* do3, const CUtensorMap* k3, const CUtensorMap* v3,
                                int max_items, int num_sms, cudaStream_t st);
 cudaError_t setup_bwd_tc_kernels();
-// Q, dO rows and LSE, Delta of every query head sorted by its assignment's
-// index (for the group kernels' tile loads).
+// Q, dO rows and LSE of every query head sorted by its assignment's index (for
+// the group kernels' tile loads), and Delta = rowsum(dO * O) in natural and
+// index order.
 cudaError_t launch_bwd_permute_q(const BwdArgs& a, void* Qs, void* dOs, float* lse_s, float* delta_s,
                                  cudaStream_t st);
 cudaError_t launch_sinkhorn(const SinkhornLaunch& L, int iters, cudaStream_t st);
