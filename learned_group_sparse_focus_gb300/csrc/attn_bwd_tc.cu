@@ -68,28 +68,39 @@ struct BUnit {
   int heads;            // query heads walked (dKV: H / H_kv; dQ: 1)
 };
 
+// dQ far unit u (item order[u / hpa], query head u % hpa of its assignment) from its item.
+__device__ __forceinline__ BUnit decode_item(const BwdArgs& a, int u, const focus_item_t& it) {
+  BUnit U{};
+  U.valid = true;
+  U.heads = 1;
+  const int hpa = a.A == 1 ? a.H : a.H / a.H_kv;
+  const int y = u % hpa;
+  U.b = it.b;
+  U.h = a.A == 1 ? y : it.a * (a.H / a.H_kv) + y;
+  U.kv = (U.h * a.H_kv) / a.H;
+  U.prob = it.b * a.A + it.a;
+  U.row0 = it.row0;
+  U.nrows = it.rows;
+  U.key0 = it.key0;
+  U.nkeys = it.keys;
+  U.ntile = (it.keys + kT - 1) / kT;
+  U.zq = U.b * a.H + U.h;
+  U.zkv = U.b * a.H_kv + U.kv;
+  return U;
+}
+
 template <int KIND>
 __device__ __forceinline__ BUnit decode(const BwdArgs& a, int u) {
   BUnit U{};
   U.valid = true;
   U.heads = 1;
   if (KIND == kDqGroup) {
-    const int hpa = a.A == 1 ? a.H : a.H / a.H_kv;
-    const int y = u % hpa, io = u / hpa;
+    const int io = u / (a.A == 1 ? a.H : a.H / a.H_kv);
     if (io >= *a.n_items) {
       U.valid = false;
       return U;
     }
-    const focus_item_t it = a.items[a.order[io]];
-    U.b = it.b;
-    U.h = a.A == 1 ? y : it.a * (a.H / a.H_kv) + y;
-    U.kv = (U.h * a.H_kv) / a.H;
-    U.prob = it.b * a.A + it.a;
-    U.row0 = it.row0;
-    U.nrows = it.rows;
-    U.key0 = it.key0;
-    U.nkeys = it.keys;
-    U.ntile = (it.keys + kT - 1) / kT;
+    return decode_item(a, u, a.items[a.order[io]]);
   } else if (KIND == kDqLocal) {
     U.h = u % a.H;
     const int r = u / a.H;
@@ -378,18 +389,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     int nu = -1;
     float n_lse = 0.f, n_dlt = 0.f;
     bool n_far = false;
+    // group kind: the next unit is named by a chain of dependent loads (order
+    // entry, item, then the row's slot and far length, then its LSE and
+    // Delta); one link is issued per tile of this unit, so the chain is done
+    // by the time the next unit starts
+    int gq_u = -1, gq_stage = 0, gq_ord = 0, gq_rpos = -1, gq_khi = 0;
+    focus_item_t gq_it{};
+    BUnit GU{};
+    float gq_lse = 0.f, gq_dlt = 0.f;
+    auto gq_advance = [&]() {
+      if (gq_stage == 1) {
+        gq_it = a.items[gq_ord];
+      } else if (gq_stage == 2) {
+        GU = decode_item(a, gq_u, gq_it);
+        if (r < GU.nrows) {
+          const size_t at = static_cast<size_t>(GU.prob) * a.n + GU.row0 + r;
+          gq_rpos = a.perm[at];
+          gq_khi = a.farlen_slot[at] - 1;
+        }
+      } else if (gq_stage == 3 && r < GU.nrows) {
+        const size_t qi = static_cast<size_t>(GU.zq) * a.n + gq_rpos;
+        gq_lse = a.lse[qi];
+        gq_dlt = a.delta[qi];
+      }
+      ++gq_stage;
+    };
     for (int k = 0; ok; ++k) {
       const int u = bwd_snake(k, n_units);
       if (u == -1) break;
       if (u < 0) continue;
-      const BUnit U = decode<KIND>(a, u);
+      const bool pre = KIND == kDqGroup && u == gq_u && gq_stage == 4;
+      const BUnit U = pre ? GU : decode<KIND>(a, u);
       if (!U.valid) continue;
       const size_t pn = static_cast<size_t>(U.prob) * a.n;
       const bool row_ok = r < U.nrows;
       int rpos = -1, klo = 1, khi = 0;
       float lse2 = 0.f, dlt = 0.f;
       bool far = false;
-      if (KIND == kDqLocal && u == nu) {
+      if (pre) {
+        if (row_ok) {
+          rpos = gq_rpos;
+          klo = 0;
+          khi = gq_khi;
+          lse2 = gq_lse * kLog2e;
+          dlt = gq_dlt;
+        }
+      } else if (KIND == kDqLocal && u == nu) {
         if (row_ok) {
           rpos = U.row0 + r;
           klo = rpos - a.w + 1;
@@ -412,6 +457,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         lse2 = a.lse[qi] * kLog2e;
         dlt = a.delta[qi];
         if (KIND == kDqLocal) far = a.farlen_tok[pn + rpos] > 0;   // read by the epilogue
+      }
+      if (KIND == kDqGroup) {
+        // start the next unit's chain: its order entry now
+        gq_u = bwd_snake(k + 1, n_units);
+        gq_stage = 0;
+        if (gq_u >= 0) {
+          gq_ord = a.order[gq_u / (a.A == 1 ? a.H : a.H / a.H_kv)];
+          gq_stage = 1;
+        }
       }
       if (KIND == kDqLocal) {
         nu = bwd_snake(k + 1, n_units);
@@ -482,11 +536,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         warp_arrive(&ew_done[g & 1], lane);
+        if (KIND == kDqGroup && gq_stage > 0 && gq_stage < 4) gq_advance();
       }
       if (!ok) break;
       // Epilogue: this half's dQ columns [half * D/2, (half + 1) * D/2) once the
       // unit's products are done.  A unit with no tiles (group kind) has no
       // far keys in any row, and the window kernel reads none of its rows.
+      // one more link of the next unit's chain, its latency under the epilogue
+      if (KIND == kDqGroup && gq_stage > 0 && gq_stage < 4) gq_advance();
       if (U.ntile == 0) continue;
       if (!warp_wait(acc_full, uf & 1, abort, a.err)) { ok = false; break; }
       ++uf;
@@ -558,6 +615,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       warp_arrive(&stage_free[(uf - 1) & 1], lane);
       tc_fence_before();
+      // a short unit leaves links of the chain for here
+      while (KIND == kDqGroup && gq_stage > 0 && gq_stage < 4) gq_advance();
     }
   }
   __syncwarp();
