@@ -395,41 +395,70 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
     if (warp == kWarpLoad) {
       // -------------------------------------------------- Q and K loads ---
-      int qn = 0;                // Q tiles issued
+      int qn = 0;                // Q tiles requested in full
       int ck = 0;                // K tiles issued
       bool ok = true;
       UnitWalk<MODE> walk;
       walk.begin(a, n_units);
+      // Group passes: a unit's Q tile is 128 row gathers through perm (lane l:
+      // rows 4l..4l+3 of every 64-column slab).  The next unit's gathers go
+      // out in four batches (lanes 8j..8j+7) between this unit's K loads, one
+      // batch per K tile once the Q slot is free, so the tile is in place when
+      // the unit's first S product is due and no long run of gathers sits in
+      // front of a K load in the SM's TMA queue.
+      Unit U_nx;
+      int u_nx = -1, nx_b = 0, rows_nx[4] = {0, 0, 0, 0};
+      bool have_nx = false;
+      auto gather_rows = [&](const Unit& V, int (&rows)[4]) {
+        // rows past the item repeat its first row, whose scores are all masked
+        const int32_t* pp = a.perm + static_cast<size_t>(V.prob) * a.m + V.row0;
+        const int first = pp[0] >> a.kshift;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int rr = 4 * lane + j;
+          rows[j] = V.zq * a.n + (rr < V.nrows ? pp[rr] >> a.kshift : first);
+        }
+      };
+      // batch bt of Q tile qn (its slot already free)
+      auto q_batch = [&](const int (&rows)[4], int bt) {
+        const int sl = qn % kQSlots;
+        if (bt == 0) {
+          if (lane == 0) mbar_expect_tx(&q_full[sl], Cfg::kTile);
+          __syncwarp();
+        }
+        if ((lane >> 3) == bt) {
+          uint8_t* dst = sQ + sl * Cfg::kTile;
+#pragma unroll
+          for (int ch = 0; ch < kChunks; ++ch)
+            tma_gather4(dst + ch * Cfg::kChunk + 4 * lane * 128, &tm_q, &q_full[sl], ch * 64, rows[0], rows[1],
+                        rows[2], rows[3]);
+        }
+      };
       for (int k = 0; ok; ++k) {
         Unit U;
-        const int u = walk.step(a, k, U);
+        int u, rows[4] = {0, 0, 0, 0}, done_b = 0;
+        if (have_nx) {
+          have_nx = false;
+          u = u_nx;
+          U = U_nx;
+          done_b = nx_b;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) rows[j] = rows_nx[j];
+        } else {
+          u = walk.step(a, k, U);
+          if (is_group_mode(MODE) && u >= 0) gather_rows(U, rows);
+        }
         if (u == -1) break;
         if (u < 0) continue;
         {
-          // the unit's Q tile
+          // the unit's Q tile (group passes: the batches its predecessor did not issue)
           const int sl = qn % kQSlots, use = qn / kQSlots;
-          if (use > 0 && !warp_wait_nap(&q_empty[sl], (use - 1) & 1, abort, a.err, a.wait_ns)) break;
+          if (done_b == 0 && use > 0 && !warp_wait_nap(&q_empty[sl], (use - 1) & 1, abort, a.err, a.wait_ns)) break;
           uint8_t* dst = sQ + sl * Cfg::kTile;
           if (a.hold_first_q && qn == 0) {
             // test hook: this tile is never requested, so its wait runs out
           } else if (is_group_mode(MODE)) {
-            // TMA row gather through perm: lane l fetches tile rows 4l..4l+3 of every
-            // 64-column slab (tm_q is a 2-D {d, B*H*n} view with one-row boxes);
-            // rows past the item repeat its first row, whose scores are all masked
-            if (lane == 0) mbar_expect_tx(&q_full[sl], Cfg::kTile);
-            __syncwarp();
-            const int32_t* pp = a.perm + static_cast<size_t>(U.prob) * a.m + U.row0;
-            const int first = pp[0] >> a.kshift;
-            int rows[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int rr = 4 * lane + j;
-              rows[j] = U.zq * a.n + (rr < U.nrows ? pp[rr] >> a.kshift : first);
-            }
-#pragma unroll
-            for (int ch = 0; ch < kChunks; ++ch)
-              tma_gather4(dst + ch * Cfg::kChunk + 4 * lane * 128, &tm_q, &q_full[sl], ch * 64, rows[0],
-                          rows[1], rows[2], rows[3]);
+            for (int bt = done_b; bt < 4; ++bt) q_batch(rows, bt);
           } else if (lane == 0) {
             mbar_expect_tx(&q_full[sl], Cfg::kTile);
 #pragma unroll
@@ -438,22 +467,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ++qn;
         }
-        if (lane == 0) {
-          SegWalk sw;
-          if (MODE == kModeGroupSplit) sw.begin(a, U);
-          for (int t = U.t0; t <= U.t1; ++t, ++ck) {
-            const int sl = ck % kKSlots, use = ck / kKSlots;
-            if (use > 0 && !mbar_wait_nap(&k_empty[sl], (use - 1) & 1, abort, a.err, a.wait_ns)) { ok = false; break; }
-            const int krow = MODE == kModeGroupSplit ? sw.key0 + sw.tt * kBN : U.ybase + t * kBN;
+        if (is_group_mode(MODE)) {
+          // the next unit, named one walk round early
+          u_nx = walk.step(a, k + 1, U_nx);
+          have_nx = true;
+          nx_b = 0;
+          if (u_nx >= 0) gather_rows(U_nx, rows_nx);
+        }
+        SegWalk sw;
+        if (MODE == kModeGroupSplit) sw.begin(a, U);
+        for (int t = U.t0; t <= U.t1; ++t, ++ck) {
+          if (is_group_mode(MODE) && u_nx >= 0 && nx_b < 4) {
+            // one batch of the next unit's Q, if its slot is free (lane 0's view)
+            const int qsl = qn % kQSlots, quse = qn / kQSlots;
+            const bool fr = quse == 0 || mbar_test_wait(&q_empty[qsl], (quse - 1) & 1);
+            if (__shfl_sync(0xffffffffu, fr ? 1 : 0, 0)) q_batch(rows_nx, nx_b++);
+          }
+          const int sl = ck % kKSlots, use = ck / kKSlots;
+          if (use > 0 && !warp_wait_nap(&k_empty[sl], (use - 1) & 1, abort, a.err, a.wait_ns)) { ok = false; break; }
+          const int krow = MODE == kModeGroupSplit ? sw.key0 + sw.tt * kBN : U.ybase + t * kBN;
+          if (lane == 0) {
             mbar_expect_tx(&k_full[sl], Cfg::kTile);
 #pragma unroll
             for (int ch = 0; ch < kChunks; ++ch)
               tma_load_3d(sK + sl * Cfg::kTile + ch * Cfg::kChunk, &tm_k, &k_full[sl], ch * 64, krow, U.zkv);
-            if (MODE == kModeGroupSplit) sw.step(a, U);
           }
+          if (MODE == kModeGroupSplit) sw.step(a, U);
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort;
-        ck = __shfl_sync(0xffffffffu, ck, 0);
+        ok = __shfl_sync(0xffffffffu, (ok && !*abort) ? 1 : 0, 0) != 0;   // one view for the warp
+      }
+      if (is_group_mode(MODE) && have_nx && u_nx >= 0 && nx_b > 0) {
+        // stopped with a tile part-requested: request the rest (its slot is
+        // free) so that the whole tile lands and the drain below can wait for it
+        for (int bt = nx_b; bt < 4; ++bt) q_batch(rows_nx, bt);
+        ++qn;
       }
       if (*abort && lane == 0) {
         // drain: TMA copies already issued must land before the CTA exits
