@@ -402,10 +402,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       walk.begin(a, n_units);
       // Group passes: a unit's Q tile is 128 row gathers through perm (lane l:
       // rows 4l..4l+3 of every 64-column slab).  The next unit's gathers go
-      // out in four batches (lanes 8j..8j+7) between this unit's K loads, one
-      // batch per K tile once the Q slot is free, so the tile is in place when
-      // the unit's first S product is due and no long run of gathers sits in
-      // front of a K load in the SM's TMA queue.
+      // out in kQBatches batches (lanes 4j..4j+3, 8 gathers each) between this
+      // unit's K loads, one batch per K tile once the Q slot is free, so the
+      // tile is in place when the unit's first S product is due and no long
+      // run of gathers sits in front of a K load in the SM's TMA queue (4 or
+      // 16 batches measured slower than 8).
+      constexpr int kQBatches = 8;
       Unit U_nx;
       int u_nx = -1, nx_b = 0, rows_nx[4] = {0, 0, 0, 0};
       bool have_nx = false;
@@ -426,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_expect_tx(&q_full[sl], Cfg::kTile);
           __syncwarp();
         }
-        if ((lane >> 3) == bt) {
+        if (lane / (32 / kQBatches) == bt) {
           uint8_t* dst = sQ + sl * Cfg::kTile;
 #pragma unroll
           for (int ch = 0; ch < kChunks; ++ch)
@@ -458,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (a.hold_first_q && qn == 0) {
             // test hook: this tile is never requested, so its wait runs out
           } else if (is_group_mode(MODE)) {
-            for (int bt = done_b; bt < 4; ++bt) q_batch(rows, bt);
+            for (int bt = done_b; bt < kQBatches; ++bt) q_batch(rows, bt);
           } else if (lane == 0) {
             mbar_expect_tx(&q_full[sl], Cfg::kTile);
 #pragma unroll
@@ -477,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         SegWalk sw;
         if (MODE == kModeGroupSplit) sw.begin(a, U);
         for (int t = U.t0; t <= U.t1; ++t, ++ck) {
-          if (is_group_mode(MODE) && u_nx >= 0 && nx_b < 4) {
+          if (is_group_mode(MODE) && u_nx >= 0 && nx_b < kQBatches) {
             // one batch of the next unit's Q, if its slot is free (lane 0's view)
             const int qsl = qn % kQSlots, quse = qn / kQSlots;
             const bool fr = quse == 0 || mbar_test_wait(&q_empty[qsl], (quse - 1) & 1);
@@ -499,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (is_group_mode(MODE) && have_nx && u_nx >= 0 && nx_b > 0) {
         // stopped with a tile part-requested: request the rest (its slot is
         // free) so that the whole tile lands and the drain below can wait for it
-        for (int bt = nx_b; bt < 4; ++bt) q_batch(rows_nx, bt);
+        for (int bt = nx_b; bt < kQBatches; ++bt) q_batch(rows_nx, bt);
         ++qn;
       }
       if (*abort && lane == 0) {
