@@ -630,9 +630,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------------------
 // dK/dV kernels, persistent: one CTA per SM takes units (128 key rows of one
-// KV head) from a ticket counter (group kind) or in snake order (window
-// kind) and walks, for every query head of the KV head, the query tiles that
-// keep the unit's keys.  The loader warp names each unit, finds its rows'
+// KV head) from a ticket counter in the longest-first order kv_order_kernel
+// writes (group kind) or in snake order (window kind) and walks, for every
+// query head of the KV head, the query tiles that keep the unit's keys.  The loader warp names each unit, finds its rows'
 // kept query ranges and publishes them through a 2-entry ring in shared
 // memory, so the elementwise warps never search at a unit boundary.  TMEM is
 // S^T | dP^T | dV | dK; per tile the tensor pipe runs
