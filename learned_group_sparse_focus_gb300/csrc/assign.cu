@@ -334,8 +334,11 @@ template <int NALLOC, int DG, bool kScores>
 __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
     const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
     const __nv_bfloat16* __restrict__ C, int32_t* __restrict__ gid, float* __restrict__ scores,
-    int B, int n, int D, int K, int A, int topk, int R, int a0, int A_all, int* err) {
-  // this launch covers assignments a0 .. a0 + A - 1 of A_all (W rows from a0 * DG)
+    int B, int n, int D, int K, int A, int topk, int R, int a0, int npass, int A_all, int* err) {
+  // this launch covers assignments a0 .. a0 + npass * A - 1 of A_all in npass
+  // passes of A: unit u is token tile u / npass in pass u % npass (W rows from
+  // (a0 + pass * A) * DG), so the passes over one tile run side by side on
+  // neighbouring CTAs and all but the first read its h rows from L2
   using Cfg = StreamCfg<NALLOC>;
   constexpr int S = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -350,6 +353,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
   const int warp = warp_id(), lane = lane_id();
   const int ncol = A * DG;
   const int ntiles = (B * n + R - 1) / R;   // tiles of R <= 128 tokens
+  const int nunits = ntiles * npass;
   const int nk = (D + kBK - 1) / kBK;
 
   if (threadIdx.x == 0) {
@@ -379,7 +383,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
       const int ns = (nk + Cfg::kSlabs - 1) / Cfg::kSlabs;   // stages per tile
       int it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+      for (int unit = blockIdx.x; unit < nunits && ok; unit += gridDim.x) {
+        const int tile = unit / npass, wrow = (a0 + (unit % npass) * A) * DG;
         for (int ks = 0; ks < ns; ++ks, ++it) {
           const int s = it % S, u = it / S;
           if (u > 0 && !mbar_wait_nap(&empty[s], (u - 1) & 1, abort, err)) { ok = false; break; }
@@ -389,7 +394,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
           for (int j = 0; j < nsl; ++j) {
             const int kb = ks * Cfg::kSlabs + j;
             tma_load_2d(sa + j * Cfg::kSlabA, &tm_h, &full[s], kb * kBK, tile * R);
-            tma_load_2d(sa + Cfg::kStageA + j * Cfg::kSlabB, &tm_w, &full[s], kb * kBK, a0 * DG);
+            tma_load_2d(sa + Cfg::kStageA + j * Cfg::kSlabB, &tm_w, &full[s], kb * kBK, wrow);
           }
         }
       }
@@ -406,7 +411,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
       constexpr uint32_t idn = idesc_bf16_f32(128, NALLOC, false, false);
       int it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x, i = 0; tile < ntiles && ok; tile += gridDim.x, ++i) {
+      for (int unit = blockIdx.x, i = 0; unit < nunits && ok; unit += gridDim.x, ++i) {
         const int buf = i & 1;
         if (i >= 2 && !mbar_wait_nap(&tfree[buf], ((i >> 1) - 1) & 1, abort, err)) break;
         const int ns = (nk + Cfg::kSlabs - 1) / Cfg::kSlabs;
@@ -433,10 +438,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    for (int tile = blockIdx.x, i = 0; tile < ntiles; tile += gridDim.x, ++i) {
+    for (int unit = blockIdx.x, i = 0; unit < nunits; unit += gridDim.x, ++i) {
       const int buf = i & 1;
       if (!mbar_wait(&tfull[buf], (i >> 1) & 1, abort, err)) break;
       tc_fence_after();
+      const int tile = unit / npass, pa = a0 + (unit % npass) * A;   // the pass's first assignment
       const int tok = tile * R + row;
       const bool keep = row < R && tok < B * n;
       const int b = keep ? tok / n : 0, ti = keep ? tok % n : 0;
@@ -455,8 +461,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
           __syncwarp();
           if (lane == 0) mbar_arrive(&tfree[buf]);   // the accumulator may take tile i + 2
         }
-        const __nv_bfloat16* Ca = C + static_cast<size_t>(a0 + a) * K * DG;
-        float* srow = kScores && keep ? scores + ((static_cast<size_t>(b) * A_all + a0 + a) * n + ti) * K : nullptr;
+        const __nv_bfloat16* Ca = C + static_cast<size_t>(pa + a) * K * DG;
+        float* srow = kScores && keep ? scores + ((static_cast<size_t>(b) * A_all + pa + a) * n + ti) * K : nullptr;
         Top2 t;
         int k = 0;
         for (; k + 4 <= K; k += 4) {
@@ -480,7 +486,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
           }
         }
         if (!kScores && keep) {
-          int32_t* out = gid + ((static_cast<size_t>(b) * A_all + a0 + a) * n + ti) * topk;
+          int32_t* out = gid + ((static_cast<size_t>(b) * A_all + pa + a) * n + ti) * topk;
           out[0] = t.b1;
           if (topk == 2) out[1] = t.b2;
         }
@@ -498,28 +504,28 @@ __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
 
 template <int NALLOC, int DG>
 cudaError_t launch_stream(const AssignLaunch& L, const CUtensorMap* tm_h, const CUtensorMap* tm_w,
-                          int a0, int A_pass, cudaStream_t st) {
+                          int a0, int A_pass, int npass, cudaStream_t st) {
   using Cfg = StreamCfg<NALLOC>;
   const int R = L.tile_rows;
-  if (R < 1 || R > kBM) return cudaErrorInvalidValue;
-  const int ntiles = (L.B * L.n + R - 1) / R;
-  const int grid = ntiles < L.num_sms ? ntiles : L.num_sms;
+  if (R < 1 || R > kBM || npass < 1) return cudaErrorInvalidValue;
+  const long long units = static_cast<long long>((L.B * L.n + R - 1) / R) * npass;
+  const int grid = static_cast<int>(units < L.num_sms ? units : L.num_sms);
   const __nv_bfloat16* C = static_cast<const __nv_bfloat16*>(L.C);
   if (L.scores)
     assign_stream_kernel<NALLOC, DG, true><<<grid, kStreamThreads, Cfg::kSmem, st>>>(
-        *tm_h, *tm_w, C, L.gid, L.scores, L.B, L.n, L.D, L.K, A_pass, L.topk, R, a0, L.A, L.err);
+        *tm_h, *tm_w, C, L.gid, L.scores, L.B, L.n, L.D, L.K, A_pass, L.topk, R, a0, npass, L.A, L.err);
   else
     assign_stream_kernel<NALLOC, DG, false><<<grid, kStreamThreads, Cfg::kSmem, st>>>(
-        *tm_h, *tm_w, C, L.gid, L.scores, L.B, L.n, L.D, L.K, A_pass, L.topk, R, a0, L.A, L.err);
+        *tm_h, *tm_w, C, L.gid, L.scores, L.B, L.n, L.D, L.K, A_pass, L.topk, R, a0, npass, L.A, L.err);
   return cudaGetLastError();
 }
 
 template <int NALLOC>
 cudaError_t launch_stream_dg(const AssignLaunch& L, const CUtensorMap* tm_h, const CUtensorMap* tm_w,
-                             int a0, int A_pass, cudaStream_t st) {
-  if (L.d_g == 32) return launch_stream<NALLOC, 32>(L, tm_h, tm_w, a0, A_pass, st);
-  if (L.d_g == 64) return launch_stream<NALLOC, 64>(L, tm_h, tm_w, a0, A_pass, st);
-  if (L.d_g == 128) return launch_stream<NALLOC, 128>(L, tm_h, tm_w, a0, A_pass, st);
+                             int a0, int A_pass, int npass, cudaStream_t st) {
+  if (L.d_g == 32) return launch_stream<NALLOC, 32>(L, tm_h, tm_w, a0, A_pass, npass, st);
+  if (L.d_g == 64) return launch_stream<NALLOC, 64>(L, tm_h, tm_w, a0, A_pass, npass, st);
+  if (L.d_g == 128) return launch_stream<NALLOC, 128>(L, tm_h, tm_w, a0, A_pass, npass, st);
   return cudaErrorInvalidValue;
 }
 
@@ -588,19 +594,17 @@ cudaError_t launch_assign_bf16(const AssignLaunch& L, const CUtensorMap* tm_h,
                                const CUtensorMap* tm_w, cudaStream_t st) {
   // the persistent kernel loads W in one box per stage: ncol is its exact width
   const int ncol = L.A * L.d_g;
-  if (ncol == 32) return launch_stream_dg<32>(L, tm_h, tm_w, 0, L.A, st);
-  if (ncol == 64) return launch_stream_dg<64>(L, tm_h, tm_w, 0, L.A, st);
-  if (ncol == 128) return launch_stream_dg<128>(L, tm_h, tm_w, 0, L.A, st);
-  if (ncol == 256) return launch_stream_dg<256>(L, tm_h, tm_w, 0, L.A, st);
+  if (ncol == 32) return launch_stream_dg<32>(L, tm_h, tm_w, 0, L.A, 1, st);
+  if (ncol == 64) return launch_stream_dg<64>(L, tm_h, tm_w, 0, L.A, 1, st);
+  if (ncol == 128) return launch_stream_dg<128>(L, tm_h, tm_w, 0, L.A, 1, st);
+  if (ncol == 256) return launch_stream_dg<256>(L, tm_h, tm_w, 0, L.A, 1, st);
   if (stream_passes(ncol)) {
-    // 256 columns (256 / d_g assignments) per pass: h is read once per pass,
-    // and each pass keeps the two-accumulator pipeline of the 256-wide kernel
+    // 256 columns (256 / d_g assignments) per pass, each pass keeping the
+    // two-accumulator pipeline of the 256-wide kernel; one launch walks (tile,
+    // pass) units with the passes of a tile side by side, so h streams from
+    // HBM about once
     const int per = 256 / L.d_g;
-    for (int a0 = 0; a0 < L.A; a0 += per) {
-      const cudaError_t e = launch_stream_dg<256>(L, tm_h, tm_w, a0, per, st);
-      if (e != cudaSuccess) return e;
-    }
-    return cudaSuccess;
+    return launch_stream_dg<256>(L, tm_h, tm_w, 0, per, L.A / per, st);
   }
   if (ncol <= 32) return launch_tc<32>(L, tm_h, tm_w, st);
   if (ncol <= 64) return launch_tc<64>(L, tm_h, tm_w, st);
