@@ -132,13 +132,6 @@ __device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
   if (lane == 0) mbar_arrive(bar);
 }
 
-// warp-uniform bounded wait for a load warp (sleeping between probes)
-__device__ __forceinline__ bool warp_wait_nap(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                              int* err, unsigned long long limit_ns) {
-  const bool ok = mbar_wait_nap(bar, parity, abort, err, limit_ns);
-  return __all_sync(0xffffffffu, ok);
-}
-
 // warp-uniform bounded wait (every lane waits; the verdict is shared)
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           int* err, unsigned long long limit_ns) {
@@ -455,7 +448,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
           // the unit's Q tile (group passes: the batches its predecessor did not issue)
           const int sl = qn % kQSlots, use = qn / kQSlots;
-          if (done_b == 0 && use > 0 && !warp_wait_nap(&q_empty[sl], (use - 1) & 1, abort, a.err, a.wait_ns)) break;
+          bool qf = true;
+          if (lane == 0 && done_b == 0 && use > 0) qf = mbar_wait_nap(&q_empty[sl], (use - 1) & 1, abort, a.err, a.wait_ns);
+          if (!__shfl_sync(0xffffffffu, qf ? 1 : 0, 0)) break;
           uint8_t* dst = sQ + sl * Cfg::kTile;
           if (a.hold_first_q && qn == 0) {
             // test hook: this tile is never requested, so its wait runs out
@@ -486,7 +481,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (__shfl_sync(0xffffffffu, fr ? 1 : 0, 0)) q_batch(rows_nx, nx_b++);
           }
           const int sl = ck % kKSlots, use = ck / kKSlots;
-          if (use > 0 && !warp_wait_nap(&k_empty[sl], (use - 1) & 1, abort, a.err, a.wait_ns)) { ok = false; break; }
+          // lane 0 polls; the other lanes wait at the shuffle without issuing
+          bool kf = true;
+          if (lane == 0 && use > 0) kf = mbar_wait_nap(&k_empty[sl], (use - 1) & 1, abort, a.err, a.wait_ns);
+          if (!__shfl_sync(0xffffffffu, kf ? 1 : 0, 0)) { ok = false; break; }
           const int krow = MODE == kModeGroupSplit ? sw.key0 + sw.tt * kBN : U.ybase + t * kBN;
           if (lane == 0) {
             mbar_expect_tx(&k_full[sl], Cfg::kTile);
