@@ -65,6 +65,16 @@ METRIC = "kept-pair TFLOP/s (% of bf16 TC peak), ms/layer at n=32K, speedup vs d
 UNIT = "TFLOP/s"
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20      # larger than the 129 MB L2
+L2_NOTE = ("flushed before every timed step: a 256 MB write, then the same 256 MB read back, so the "
+           "flush's own dirty lines are written back before the step; flush not timed")
+
+
+def flush_l2(buf):
+    """Evict the step's data from L2: write a buffer larger than L2, then read
+    it, so that L2 holds clean lines and no write-back of the flush lands on
+    the first timed kernel."""
+    buf.zero_()
+    buf.amax()
 
 
 def load_peaks():
@@ -330,7 +340,7 @@ def run_ours(args, wl, world, rank, local):
     f_attn, f_group, f_local = 4 * wl.d * kept, 4 * wl.d * far_pairs, 4 * wl.d * win_pairs
 
     def step(evs):
-        flush.zero_()
+        flush_l2(flush)
         evs[0].record()
         fz.focus_assign(p, d["h"], d["W"], d["C"], gid, ws)
         evs[1].record()
@@ -378,7 +388,7 @@ def run_ours(args, wl, world, rank, local):
     dn = max(3, min(args.steps, 10))
     dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(dn)]
     for a0, a1 in dev_ev:
-        flush.zero_()
+        flush_l2(flush)
         a0.record()
         fz.focus_dense_causal_fwd(p, d["Q"], d["K"], d["V"], O, None, ws)
         a1.record()
@@ -390,7 +400,7 @@ def run_ours(args, wl, world, rank, local):
         fz.focus_attention_two_call_fwd(p, d["Q"], d["K"], d["V"], idx, O, None, ws)
     tc_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(dn)]
     for a0, a1 in tc_ev:
-        flush.zero_()
+        flush_l2(flush)
         a0.record()
         fz.focus_attention_two_call_fwd(p, d["Q"], d["K"], d["V"], idx, O, None, ws)
         a1.record()
@@ -410,7 +420,7 @@ def run_ours(args, wl, world, rank, local):
     en = max(3, min(args.steps, 10))
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(en)]
     for a0, a1 in e2e_ev:
-        flush.zero_()
+        flush_l2(flush)
         a0.record()
         fz.focus_layer_fwd_host(p, host, dbuf, ws)
         a1.record()
@@ -449,7 +459,7 @@ def run_ours(args, wl, world, rank, local):
         "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded N(0,1) Q/K/V/h, Zipf-planted groups)",
         "config": {"workload": wl.name, **{k: getattr(wl, k) for k in ("B", "H", "H_kv", "n", "d", "D", "d_g", "K", "w", "A")},
                    "kept_pairs": kept, "kept_density_vs_causal": kept / (wl.B * wl.H * wl.n * (wl.n + 1) / 2),
-                   "work_items": n_items, "l2": "flushed (256 MB write) before every timed step; flush not timed",
+                   "work_items": n_items, "l2": L2_NOTE,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "pct_of_bf16_peak": 100.0 * (f_attn / (t_step * 1e-3) / 1e12) / float(peaks["bf16_tflops"]),
         "attention_tflops": f_attn / (t_attn * 1e-3) / 1e12,
@@ -537,7 +547,7 @@ def run_ours_topk(args, wl, world, rank, local):
     f_attn = 4 * wl.d * kept
 
     def step(evs):
-        flush.zero_()
+        flush_l2(flush)
         evs[0].record()
         fz.focus_assign_topk(p, k, d["h"], d["W"], d["C"], gid, ws)
         evs[1].record()
@@ -585,7 +595,7 @@ def run_ours_topk(args, wl, world, rank, local):
         fz.focus_dense_causal_fwd(p, d["Q"], d["K"], d["V"], O, None, dws)
     dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(5)]
     for a0, a1 in dev_ev:
-        flush.zero_()
+        flush_l2(flush)
         a0.record()
         fz.focus_dense_causal_fwd(p, d["Q"], d["K"], d["V"], O, None, dws)
         a1.record()
@@ -611,7 +621,7 @@ def run_ours_topk(args, wl, world, rank, local):
         e2e_step()
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(5)]
     for a0, a1 in e2e_ev:
-        flush.zero_()
+        flush_l2(flush)
         a0.record()
         e2e_step()
         a1.record()
@@ -634,7 +644,7 @@ def run_ours_topk(args, wl, world, rank, local):
                    "kept_pairs": kept, "kept_density_vs_causal": kept / (wl.B * wl.H * wl.n * (wl.n + 1) / 2),
                    "far_pairs_entry_pass": ent_pairs, "far_pairs_pair_pass": pair_pairs,
                    "topk_index": "split (each far pair once)" if idx.split else "entry + pair",
-                   "l2": "flushed (256 MB write) before every timed step; flush not timed",
+                   "l2": L2_NOTE,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "ms_breakdown": t, "ms_dense_causal": t_dense, "speedup_vs_dense": t_dense / t_step,
         "roofline": tensor_roofline("attn_tc_group_pass (entries)", achieved),
@@ -682,7 +692,7 @@ def run_ours_sinkhorn(args, wl, world, rank, local):
     torch.cuda.synchronize()
     with ClockSampler(int(os.environ.get("FOCUS_NVSMI_INDEX", local))) as clk:
         for e in ev:
-            flush.zero_()
+            flush_l2(flush)
             e[0].record()
             fz.focus_assign_scores(p, h, W, C, S, ws)
             e[1].record()
@@ -706,7 +716,7 @@ def run_ours_sinkhorn(args, wl, world, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": wl.name, "rounds": T, "tau": 1.0,
                    **{k: getattr(wl, k) for k in ("B", "n", "D", "d_g", "K", "A")},
-                   "S_bytes": sbytes, "l2": "flushed (256 MB write) before every timed step"},
+                   "S_bytes": sbytes, "l2": L2_NOTE},
         "ms_breakdown": {"scores": t_sc, "sinkhorn": t_sk, "per_round": t_sk / T},
         "roofline": {"bound": "hbm", "kernel": "sinkhorn rounds", "achieved": gbs,
                      "peak": float(peaks["hbm_gbs"]), "unit": "GB/s", "frac": gbs / float(peaks["hbm_gbs"]),
@@ -772,7 +782,7 @@ def run_ours_backward(args, wl, world, rank, local):
     torch.cuda.synchronize()
     with ClockSampler(int(os.environ.get("FOCUS_NVSMI_INDEX", local))) as clk:
         for a0, a1 in ev:
-            flush.zero_()
+            flush_l2(flush)
             a0.record()
             fz.focus_attention_bwd(p, Q, K, V, O, dO, lse, idx, dQ, dK, dV, wsb)
             a1.record()
@@ -786,7 +796,7 @@ def run_ours_backward(args, wl, world, rank, local):
         "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
         "config": {"workload": wl.name, **{k: getattr(wl, k) for k in ("B", "H", "H_kv", "n", "d", "K", "w", "A")},
-                   "kept_pairs": kept, "l2": "flushed (256 MB write) before every timed step"},
+                   "kept_pairs": kept, "l2": L2_NOTE},
         "roofline": (tensor_roofline("backward (tcgen05 dQ and dK/dV kernels)", tf)
                      if wl.dtype == "bf16" else
                      {"bound": "alu", "kernel": "backward (fp32 CUDA cores)", "achieved": tf,

@@ -28,19 +28,17 @@ namespace {
 // Running best and runner-up over centroids scanned in increasing k: a later
 // centroid displaces one only with a strictly larger score, so the lower index
 // wins ties (and a NaN score never displaces anything but the empty start).
+// Written as selects: the lanes of a warp disagree on which case applies.
 struct Top2 {
   int b1 = -1, b2 = -1;
   float s1 = -INFINITY, s2 = -INFINITY;
   __device__ __forceinline__ void push(int k, float s) {
-    if (b1 < 0 || s > s1) {
-      b2 = b1;
-      s2 = s1;
-      b1 = k;
-      s1 = s;
-    } else if (b2 < 0 || s > s2) {
-      b2 = k;
-      s2 = s;
-    }
+    const bool g1 = (b1 < 0) | (s > s1);
+    const bool g2 = !g1 & ((b2 < 0) | (s > s2));
+    s2 = g1 ? s1 : (g2 ? s : s2);
+    b2 = g1 ? b1 : (g2 ? k : b2);
+    s1 = g1 ? s : s1;
+    b1 = g1 ? k : b1;
   }
 };
 
@@ -277,8 +275,10 @@ __global__ void __launch_bounds__(128, AssignCfg<NALLOC>::kMinBlocks) assign_tc_
 // issues the TMA loads of every (tile, k-step) into a kStages ring, warp 1 the
 // MMAs into TMEM buffer (tile index & 1), and warps 2-5 (one per TMEM lane
 // quadrant) score a tile once its accumulator is complete, releasing the
-// buffer as soon as they have read it.  The centroids are read from global
-// memory by every lane at the same address (L1 broadcasts).
+// buffer as soon as they have read it.  The centroids are staged in shared
+// memory as fp32, one chunk [d_g][chunk] at a time (kept while it stays the
+// same), and every lane reads the same address (broadcast) while scoring two
+// centroids per packed FMA.
 constexpr int kStreamThreads = 192;
 
 template <int NALLOC>
@@ -292,42 +292,35 @@ struct StreamCfg {
   static constexpr int kStageB = kSlabs * kSlabB;
   static constexpr int kStage = kStageA + kStageB;
   static constexpr int kStages = (200 * 1024 / kStage) < 8 ? (200 * 1024 / kStage) : 8;
-  static constexpr int kSmem = kStages * kStage + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int kRing = kStages * kStage;
+  // fp32 centroids for the scoring loop, in what the 227 KB opt-in leaves
+  // (24-32 KB): a chunk of centroids [d_g][chunk] per fill
+  static constexpr int kCLeft = 227 * 1024 - kRing - 1024 /*align*/ - 256 /*barriers*/;
+  static constexpr int kCBytes = (kCLeft > 32768 ? 32768 : kCLeft) & ~1023;
+  static constexpr int kSmem = kRing + 1024 + 256 + kCBytes;
   static constexpr int kTmemCols = 2 * NALLOC;              // two accumulators
 };
 
-// s += p[0..DG) . c (bf16 centroid row, 16-byte aligned), in order j = 0, 1, ...
+// Scores of 32 centroids kb .. kb + 31 of a staged chunk (cs[j * kc + k],
+// fp32): acc holds them as pairs (k, k + 1); each score is summed from 0 in
+// order j = 0, 1, ... with one rounding per FMA, as a scalar loop would.
 template <int DG>
-__device__ __forceinline__ void score4(const float (&p)[128], const __nv_bfloat16* c0, int stride, float (&sc)[4]) {
+__device__ __forceinline__ void score32(const float (&p)[128], const float* cs, int kc, int kb,
+                                        uint64_t (&acc)[16]) {
 #pragma unroll
-  for (int j = 0; j < DG; j += 8) {
+  for (int q = 0; q < 16; ++q) acc[q] = 0ull;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 w = __ldg(reinterpret_cast<const uint4*>(c0 + q * stride + j));
-      const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+  for (int j = 0; j < DG; ++j) {
+    const uint64_t pp = f2_pack(p[j], p[j]);
+    const float* row = cs + j * kc + kb;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        sc[q] = fmaf(p[j + 2 * e], __uint_as_float(u[e] << 16), sc[q]);
-        sc[q] = fmaf(p[j + 2 * e + 1], __uint_as_float(u[e] & 0xffff0000u), sc[q]);
-      }
+    for (int q = 0; q < 8; ++q) {
+      uint64_t c0, c1;
+      lds_f2x2(row + 4 * q, c0, c1);
+      acc[2 * q] = f2_fma(pp, c0, acc[2 * q]);
+      acc[2 * q + 1] = f2_fma(pp, c1, acc[2 * q + 1]);
     }
   }
-}
-
-template <int DG>
-__device__ __forceinline__ float score1(const float (&p)[128], const __nv_bfloat16* c) {
-  float s = 0.f;
-#pragma unroll
-  for (int j = 0; j < DG; j += 8) {
-    const uint4 w = __ldg(reinterpret_cast<const uint4*>(c + j));
-    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      s = fmaf(p[j + 2 * e], __uint_as_float(u[e] << 16), s);
-      s = fmaf(p[j + 2 * e + 1], __uint_as_float(u[e] & 0xffff0000u), s);
-    }
-  }
-  return s;
 }
 
 template <int NALLOC, int DG, bool kScores>
@@ -437,10 +430,19 @@ __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
     // epilogue: warps 2-5 read TMEM lane quadrants 2, 3, 0, 1
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
+    const int et = threadIdx.x - 64;   // 0..127 over the epilogue warps
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    // centroids in chunks of kc (a multiple of 32) staged as fp32 [DG][kc];
+    // a chunk stays staged while consecutive tiles use the same one
+    float* cs = reinterpret_cast<float*>(smem + Cfg::kRing + 256);
+    const int kc_max = (Cfg::kCBytes / 4 / DG) & ~31;
+    const int kc = min(kc_max, (K + 31) & ~31);
+    int staged_a = -1, staged_k0 = -1;
     for (int unit = blockIdx.x, i = 0; unit < nunits; unit += gridDim.x, ++i) {
       const int buf = i & 1;
-      if (!mbar_wait(&tfull[buf], (i >> 1) & 1, abort, err)) break;
+      // every epilogue thread leaves the loop together, so the named barriers
+      // below always see all 128
+      if (!named_barrier_and(1, 128, mbar_wait(&tfull[buf], (i >> 1) & 1, abort, err))) break;
       tc_fence_after();
       const int tile = unit / npass, pa = a0 + (unit % npass) * A;   // the pass's first assignment
       const int tok = tile * R + row;
@@ -464,25 +466,60 @@ __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
         const __nv_bfloat16* Ca = C + static_cast<size_t>(pa + a) * K * DG;
         float* srow = kScores && keep ? scores + ((static_cast<size_t>(b) * A_all + pa + a) * n + ti) * K : nullptr;
         Top2 t;
-        int k = 0;
-        for (; k + 4 <= K; k += 4) {
-          float sc[4] = {0.f, 0.f, 0.f, 0.f};
-          score4<DG>(p, Ca + static_cast<size_t>(k) * DG, DG, sc);
+        for (int k0 = 0; k0 < K; k0 += kc) {
+          const int nk = min(kc, K - k0);
+          if (staged_a != pa + a || staged_k0 != k0) {
+            named_barrier(1, 128);   // the previous chunk is no longer read
+            // eight 16-byte loads per thread in flight, then their stores
+            constexpr int kFill = 8;
+            for (int e0 = et; e0 < kc * (DG / 8); e0 += 128 * kFill) {
+              uint4 w[kFill];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            if (kScores) {
-              if (srow) srow[k + q] = sc[q];
-            } else {
-              t.push(k + q, sc[q]);
+              for (int f = 0; f < kFill; ++f) {
+                const int e = e0 + f * 128, kk = e / (DG / 8), j8 = (e % (DG / 8)) * 8;
+                w[f] = make_uint4(0u, 0u, 0u, 0u);
+                if (e < kc * (DG / 8) && kk < nk)
+                  w[f] = __ldg(reinterpret_cast<const uint4*>(Ca + static_cast<size_t>(k0 + kk) * DG + j8));
+              }
+#pragma unroll
+              for (int f = 0; f < kFill; ++f) {
+                const int e = e0 + f * 128, kk = e / (DG / 8), j8 = (e % (DG / 8)) * 8;
+                if (e >= kc * (DG / 8)) break;
+                const uint32_t u[4] = {w[f].x, w[f].y, w[f].z, w[f].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  cs[(j8 + 2 * q) * kc + kk] = __uint_as_float(u[q] << 16);
+                  cs[(j8 + 2 * q + 1) * kc + kk] = __uint_as_float(u[q] & 0xffff0000u);
+                }
+              }
             }
+            named_barrier(1, 128);
+            staged_a = pa + a;
+            staged_k0 = k0;
           }
-        }
-        for (; k < K; ++k) {
-          const float sk = score1<DG>(p, Ca + static_cast<size_t>(k) * DG);
-          if (kScores) {
-            if (srow) srow[k] = sk;
-          } else {
-            t.push(k, sk);
+          for (int kb = 0; kb < nk; kb += 32) {
+            uint64_t acc[16];
+            score32<DG>(p, cs, kc, kb, acc);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              float s0, s1;
+              f2_unpack(acc[q], s0, s1);
+              const int k = k0 + kb + 2 * q;
+              if (kb + 2 * q < nk) {
+                if (kScores) {
+                  if (srow) srow[k] = s0;
+                } else {
+                  t.push(k, s0);
+                }
+              }
+              if (kb + 2 * q + 1 < nk) {
+                if (kScores) {
+                  if (srow) srow[k + 1] = s1;
+                } else {
+                  t.push(k + 1, s1);
+                }
+              }
+            }
           }
         }
         if (!kScores && keep) {
@@ -523,9 +560,13 @@ cudaError_t launch_stream(const AssignLaunch& L, const CUtensorMap* tm_h, const 
 template <int NALLOC>
 cudaError_t launch_stream_dg(const AssignLaunch& L, const CUtensorMap* tm_h, const CUtensorMap* tm_w,
                              int a0, int A_pass, int npass, cudaStream_t st) {
-  if (L.d_g == 32) return launch_stream<NALLOC, 32>(L, tm_h, tm_w, a0, A_pass, npass, st);
-  if (L.d_g == 64) return launch_stream<NALLOC, 64>(L, tm_h, tm_w, a0, A_pass, npass, st);
-  if (L.d_g == 128) return launch_stream<NALLOC, 128>(L, tm_h, tm_w, a0, A_pass, npass, st);
+  // an assignment's d_g columns fit the accumulator (NALLOC >= d_g)
+  if constexpr (NALLOC >= 32)
+    if (L.d_g == 32) return launch_stream<NALLOC, 32>(L, tm_h, tm_w, a0, A_pass, npass, st);
+  if constexpr (NALLOC >= 64)
+    if (L.d_g == 64) return launch_stream<NALLOC, 64>(L, tm_h, tm_w, a0, A_pass, npass, st);
+  if constexpr (NALLOC >= 128)
+    if (L.d_g == 128) return launch_stream<NALLOC, 128>(L, tm_h, tm_w, a0, A_pass, npass, st);
   return cudaErrorInvalidValue;
 }
 

@@ -179,6 +179,24 @@ __device__ __forceinline__ void named_barrier_arrive(int id, int count) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Barrier among `count` threads at named barrier `id` that also returns the
+// AND of every participant's `v`, so all of them take the same branch after.
+__device__ __forceinline__ bool named_barrier_and(int id, int count, bool v) {
+  int r;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.s32 pi, %1, 0;\n bar.red.and.pred po, %2, %3, pi;\n"
+      " selp.s32 %0, 1, 0, po;\n}"
+      : "=r"(r)
+      : "r"(v ? 1 : 0), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
+// Two packed fp32 pairs from 16 aligned bytes of shared memory.
+__device__ __forceinline__ void lds_f2x2(const float* p, uint64_t& a, uint64_t& b) {
+  asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(smem_u32(p)));
+}
+
 // Row gather: four rows (r0..r3) of `box_cols` elements each from a 2-D tensor
 // map whose box is one row high; they land one after another at smem_dst.
 __device__ __forceinline__ void tma_gather4(void* smem_dst, const void* tmap, uint64_t* bar, int col,
