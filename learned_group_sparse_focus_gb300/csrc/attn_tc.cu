@@ -21,12 +21,11 @@
 //          sliding-window call with the Focus window.
 //
 // S = Q K^T reads Q and K from shared memory; O += P V reads P from TMEM and
-// V from shared memory.  TMEM (512 columns for d = 128): S double buffer
-// (2 x 128), O (d columns) and a P double buffer (2 x 64 columns of bf16
-// pairs).  S(t+2) may overwrite S(t) as soon as the softmax has read it, and
-// P(t) goes to its own buffer once O += P(t-2) V is done, so the S product of
-// a later tile runs while the softmax works and the softmax never waits for
-// the PV product of the tile before.
+// V from shared memory.  TMEM (512 columns for d = 128): three S buffers of
+// 128 columns and O (d columns).  The softmax writes P(t) as bf16 pairs over
+// the S(t) it has just read, so a buffer is free again once O += P(t) V(t) is
+// done: the S products of the next two tiles run while the softmax works, and
+// the softmax never waits for the PV product of the tile before.
 //
 // Warp roles (384 threads), one CTA per SM looping over units:
 //   warps 0-7   softmax, two warps per query row (warps w and w + 4 share TMEM

@@ -114,7 +114,10 @@ __global__ void __launch_bounds__(256) index_count_kernel(const int32_t* __restr
   for (int g = threadIdx.x; g < K; g += blockDim.x) out[g] = hist[g];
 }
 
-__global__ void __launch_bounds__(1024) index_scan_kernel(int n, int K, int nseg,
+// With `staged` the [nseg][K] segment counts are first copied into shared
+// memory in one coalesced pass, so the per-group walks over the segments read
+// shared memory instead of issuing nseg dependent global loads each.
+__global__ void __launch_bounds__(1024) index_scan_kernel(int n, int K, int nseg, int staged,
                                                           int32_t* __restrict__ segcnt,
                                                           int32_t* __restrict__ counts,
                                                           int32_t* __restrict__ offsets,
@@ -122,12 +125,18 @@ __global__ void __launch_bounds__(1024) index_scan_kernel(int n, int K, int nseg
   extern __shared__ int sm[];
   int* cnt = sm;              // K
   int* tiles = sm + K;        // K
+  int* segs = sm + 2 * K;     // [nseg][K] when staged
   __shared__ int warp_sums[32];
   const int p = blockIdx.x;
   int32_t* sc = segcnt + static_cast<size_t>(p) * nseg * K;
+  if (staged) {
+    for (int e = threadIdx.x; e < nseg * K; e += blockDim.x) segs[e] = sc[e];
+    __syncthreads();
+  }
+  const int* src = staged ? segs : sc;
   for (int g = threadIdx.x; g < K; g += blockDim.x) {
     int s = 0;
-    for (int seg = 0; seg < nseg; ++seg) s += sc[static_cast<size_t>(seg) * K + g];
+    for (int seg = 0; seg < nseg; ++seg) s += src[static_cast<size_t>(seg) * K + g];
     cnt[g] = s;
     counts[static_cast<size_t>(p) * K + g] = s;
     tiles[g] = (s + kTileM - 1) / kTileM;
@@ -142,9 +151,9 @@ __global__ void __launch_bounds__(1024) index_scan_kernel(int n, int K, int nseg
     tb[g] = tiles[g];
     int run = cnt[g];
     for (int seg = 0; seg < nseg; ++seg) {
-      int32_t* c = sc + static_cast<size_t>(seg) * K + g;
-      int v = *c;
-      *c = run;
+      const size_t e = static_cast<size_t>(seg) * K + g;
+      const int v = src[e];
+      sc[e] = run;
       run += v;
     }
   }
@@ -228,7 +237,10 @@ __global__ void __launch_bounds__(256) index_farlen_kernel(int n, int K, int w_e
   // members of g at slots [offs[g], s) have positions < pos; count those
   // with position <= pos - w_eff, i.e. < target
   const int target = pos - w_eff + 1;
-  int lo = offs[g], hi = s;   // first slot in [lo, hi) whose position >= target
+  // positions rise along the group's slots, so at most w_eff - 1 members
+  // before slot s lie at or after target: the answer is within w_eff - 1
+  // slots of s
+  int lo = max(offs[g], s - w_eff + 1), hi = s;   // first slot in [lo, hi) whose position >= target
   while (lo < hi) {
     int mid = (lo + hi) >> 1;
     if ((__ldg(pp + mid) >> kshift) < target) lo = mid + 1; else hi = mid;
@@ -239,7 +251,7 @@ __global__ void __launch_bounds__(256) index_farlen_kernel(int n, int K, int w_e
 }
 
 __global__ void __launch_bounds__(1024) index_items_kernel(
-    int P, int A, int n, int K, const int32_t* __restrict__ counts,
+    int P, int A, int n, int K, int staged, const int32_t* __restrict__ counts,
     const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_base,
     const int32_t* __restrict__ farlen_slot, focus_item_t* __restrict__ items,
     int32_t* __restrict__ cost, int32_t* __restrict__ order, int32_t* __restrict__ n_items,
@@ -249,6 +261,12 @@ __global__ void __launch_bounds__(1024) index_items_kernel(
   int* hist = sm + P + 1;          // nb + 1
   __shared__ int warp_sums[32];
   const int nb = (n + kTileN - 1) / kTileN + 1;   // cost buckets 0..nb-1
+  // with `staged` every problem's tile bases are copied to shared memory, so
+  // each candidate's search over them reads no global memory
+  int* tbs = hist + nb + 1;        // [P][K + 1] when staged
+  if (staged) {
+    for (int e = threadIdx.x; e < P * (K + 1); e += blockDim.x) tbs[e] = tile_base[e];
+  }
   if (threadIdx.x == 0) {
     int run = 0;
     for (int p = 0; p < P; ++p) {
@@ -268,12 +286,12 @@ __global__ void __launch_bounds__(1024) index_items_kernel(
     if (c < total) {
       const int p = upper_bound_minus1(pbase, P, c);
       const int t = c - pbase[p];
-      const int32_t* tb = tile_base + static_cast<size_t>(p) * (K + 1);
+      const int32_t* tb = (staged ? tbs : tile_base) + static_cast<size_t>(p) * (K + 1);
       // group of candidate tile t: largest g with tb[g] <= t (tb[K] > t)
       int lo = 0, hi = K;
       while (hi - lo > 1) {
         int mid = (lo + hi) >> 1;
-        if (__ldg(tb + mid) <= t) lo = mid; else hi = mid;
+        if (tb[mid] <= t) lo = mid; else hi = mid;
       }
       const int g = lo;
       const int tt = t - tb[g];
@@ -487,6 +505,18 @@ __global__ void __launch_bounds__(1024) index_items_split_kernel(
   }
 }
 
+// Shared-memory staging limits: the scan's [nseg][K] segment counts and the
+// work-list kernel's [P][K + 1] tile bases.
+constexpr int kScanStageInts = 16384;    // 64 KB
+constexpr int kItemsStageInts = 8192;    // 32 KB
+
+int scan_staged(int nseg, int K) {
+  return static_cast<long long>(nseg) * K <= kScanStageInts ? 1 : 0;
+}
+size_t scan_smem(int nseg, int K, int staged) {
+  return (2 * static_cast<size_t>(K) + (staged ? static_cast<size_t>(nseg) * K : 0)) * sizeof(int);
+}
+
 }  // namespace
 
 cudaError_t launch_build_index_split(const IndexLaunch& L, int K, int32_t* farlen_sub, cudaStream_t st) {
@@ -496,8 +526,9 @@ cudaError_t launch_build_index_split(const IndexLaunch& L, int K, int32_t* farle
   const int nseg = (L.n + kIndexSeg - 1) / kIndexSeg;
   index_count_kernel<<<dim3(nseg, P), 256, static_cast<size_t>(Kv) * sizeof(int), st>>>(
       L.gid, L.n, Kv, nseg, L.segcnt, L.err);
-  index_scan_kernel<<<P, 1024, 2 * static_cast<size_t>(Kv) * sizeof(int), st>>>(
-      L.n, Kv, nseg, L.segcnt, L.counts, L.offsets, L.tile_base);
+  const int staged_s = scan_staged(nseg, Kv);
+  index_scan_kernel<<<P, 1024, scan_smem(nseg, Kv, staged_s), st>>>(
+      L.n, Kv, nseg, staged_s, L.segcnt, L.counts, L.offsets, L.tile_base);
   index_scatter_kernel<<<dim3(nseg, P), 256, static_cast<size_t>(Kv) * sizeof(int) + 8 * static_cast<size_t>(Kv) * 2,
                          st>>>(L.gid, L.n, Kv, nseg, L.segcnt, L.perm, L.rank, L.err);
   index_farlen_split_kernel<<<dim3((L.n + 255) / 256, P), 256, static_cast<size_t>(Kv + 1) * sizeof(int), st>>>(
@@ -514,9 +545,9 @@ cudaError_t launch_build_index(const IndexLaunch& L, cudaStream_t st) {
   const int nseg = (L.n + kIndexSeg - 1) / kIndexSeg;
   const size_t sm_count = static_cast<size_t>(L.K) * sizeof(int);
   index_count_kernel<<<dim3(nseg, P), 256, sm_count, st>>>(L.gid, L.n, L.K, nseg, L.segcnt, L.err);
-  const size_t sm_scan = 2 * static_cast<size_t>(L.K) * sizeof(int);
-  index_scan_kernel<<<P, 1024, sm_scan, st>>>(L.n, L.K, nseg, L.segcnt, L.counts, L.offsets,
-                                              L.tile_base);
+  const int staged_s = scan_staged(nseg, L.K);
+  index_scan_kernel<<<P, 1024, scan_smem(nseg, L.K, staged_s), st>>>(
+      L.n, L.K, nseg, staged_s, L.segcnt, L.counts, L.offsets, L.tile_base);
   const size_t sm_scatter = static_cast<size_t>(L.K) * sizeof(int) + 8 * static_cast<size_t>(L.K) * 2;
   index_scatter_kernel<<<dim3(nseg, P), 256, sm_scatter, st>>>(L.gid, L.n, L.K, nseg, L.segcnt,
                                                                 L.perm, L.rank, L.err);
@@ -524,8 +555,10 @@ cudaError_t launch_build_index(const IndexLaunch& L, cudaStream_t st) {
   index_farlen_kernel<<<dim3((L.n + 255) / 256, P), 256, sm_far, st>>>(
       L.n, L.K, L.w_eff, L.kshift, L.offsets, L.perm, L.farlen_tok, L.farlen_slot);
   const int nb = (L.n + kTileN - 1) / kTileN + 1;
-  const size_t sm_items = static_cast<size_t>(P + 1 + nb) * sizeof(int);
-  index_items_kernel<<<1, 1024, sm_items, st>>>(P, L.A, L.n, L.K, L.counts, L.offsets,
+  const long long tb_ints = static_cast<long long>(P) * (L.K + 1);
+  const int staged_i = tb_ints <= kItemsStageInts ? 1 : 0;
+  const size_t sm_items = static_cast<size_t>(P + 1 + nb + (staged_i ? tb_ints : 0)) * sizeof(int);
+  index_items_kernel<<<1, 1024, sm_items, st>>>(P, L.A, L.n, L.K, staged_i, L.counts, L.offsets,
                                                 L.tile_base, L.farlen_slot, L.items, L.cost,
                                                 L.order, L.n_items, L.max_items, L.err);
   return cudaGetLastError();
@@ -537,8 +570,11 @@ cudaError_t setup_index_kernels() {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kMaxK * 4 + 8 * kMaxK * 2);
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(index_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (2 * kMaxK + kScanStageInts) * 4);
+  if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(index_items_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           160 * 1024);
+                           160 * 1024 + kItemsStageInts * 4);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(index_items_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            160 * 1024);
