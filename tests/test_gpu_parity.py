@@ -116,6 +116,7 @@ def test_assign_ties_go_to_lowest_index(fz, dtype):
     (1, 1, 512, 512, 1, "distinct"),
     (1, 1, 300, 700, 10, "uniform"),          # K > n: empty groups
     (1, 1, 5000, 4096, 3, "uniform"),         # largest K
+    (3, 1, 2000, 4096, 17, "uniform"),        # tile bases of three problems read from global memory
     (3, 1, 130, 4, 0, "blocks"),              # w = 0 behaves as w = 1
     (1, 1, 4100, 3, 5000, "uniform"),         # w > n: no far keys at all
 ])
