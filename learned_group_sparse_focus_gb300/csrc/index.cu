@@ -87,6 +87,32 @@ __device__ int block_scan_smem(int* a, int L, int* warp_sums) {
   return total;
 }
 
+// hist[cb] <- the number of entries in buckets above cb (an exclusive scan
+// from the last bucket down), by the whole block in chunks of 4 per thread.
+__device__ void bucket_starts_descending(int* hist, int nb, int* warp_sums) {
+  constexpr int kPer = 4;
+  int carry = 0;
+  for (int base = 0; base < nb; base += kPer * blockDim.x) {
+    int v[kPer];
+    int s = 0;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int r = base + kPer * threadIdx.x + k;   // r-th bucket from the top
+      v[k] = r < nb ? hist[nb - 1 - r] : 0;
+      s += v[k];
+    }
+    int tot;
+    int run = carry + block_excl_scan(s, warp_sums, &tot);
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int r = base + kPer * threadIdx.x + k;
+      if (r < nb) hist[nb - 1 - r] = run;
+      run += v[k];
+    }
+    carry += tot;
+  }
+}
+
 __device__ __forceinline__ int upper_bound_minus1(const int* a, int len, int v) {
   // largest i in [0, len) with a[i] <= v, given a[0] <= v < a[len]
   int lo = 0, hi = len;
@@ -325,16 +351,8 @@ __global__ void __launch_bounds__(1024) index_items_kernel(
     out = max_items;
   }
   __syncthreads();
-  // start of each cost bucket in descending-cost order
-  if (threadIdx.x == 0) {
-    int run = 0;
-    for (int cb = nb - 1; cb >= 0; --cb) {
-      int v = hist[cb];
-      hist[cb] = run;
-      run += v;
-    }
-    *n_items = out;
-  }
+  bucket_starts_descending(hist, nb, warp_sums);   // start of each cost bucket, costliest first
+  if (threadIdx.x == 0) *n_items = out;
   __syncthreads();
   if (warp_id() == 0) {
     const int lane = lane_id();
@@ -480,15 +498,8 @@ __global__ void __launch_bounds__(1024) index_items_split_kernel(
     out = max_items;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int run = 0;
-    for (int cb = nb - 1; cb >= 0; --cb) {
-      int v = hist[cb];
-      hist[cb] = run;
-      run += v;
-    }
-    *n_items = out;
-  }
+  bucket_starts_descending(hist, nb, warp_sums);   // start of each cost bucket, costliest first
+  if (threadIdx.x == 0) *n_items = out;
   __syncthreads();
   if (warp_id() == 0) {
     const int lane = lane_id();
