@@ -11,11 +11,13 @@
 // bf16: the projection is a [128 tokens x A*d_g] tile of h W^T on the
 // tcgen05 tensor cores (TMA-fed pipeline, fp32 accumulator in TMEM); the
 // epilogue reads each token's row of p from TMEM and scores the centroids with
-// fp32 FMAs, so p is never rounded below fp32.  Up to 256 projection columns
-// the kernel is persistent: one CTA per SM streams its 128-token tiles of h
-// through an 8-stage TMA ring into double-buffered TMEM accumulators while
-// four epilogue warps score the previous tile; 512 columns (eight 64-wide
-// assignments) use one CTA per tile.
+// fp32 FMAs, so p is never rounded below fp32.  For 32, 64, 128 or 256
+// projection columns the kernel is persistent: one CTA per SM streams its
+// token tiles of h through a 4-6 stage TMA ring into double-buffered TMEM
+// accumulators while four epilogue warps score the previous tile; wider
+// projections that are a multiple of 256 columns run through the same kernel
+// as passes of 256 (whole assignments each), and other widths up to 512 use
+// one CTA per 128-token tile.
 // fp32: one thread per token on the CUDA cores.
 // With kScores the kernels write every score s_k (fp32, [B, A, n, K]) instead
 // of the top-k ids: the input of the Sinkhorn soft assignment.
