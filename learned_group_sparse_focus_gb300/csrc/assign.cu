@@ -18,7 +18,7 @@
 // projections that are a multiple of 256 columns run through the same kernel
 // as passes of 256 (whole assignments each), and other widths up to 512 use
 // one CTA per 128-token tile.
-// fp32: one thread per token on the CUDA cores.
+// fp32: one warp per token and assignment on the CUDA cores.
 // With kScores the kernels write every score s_k (fp32, [B, A, n, K]) instead
 // of the top-k ids: the input of the Sinkhorn soft assignment.
 #include "common.cuh"
@@ -45,38 +45,77 @@ struct Top2 {
 };
 
 // ------------------------------------------------------------------ fp32 ---
+// One warp per (token, assignment).  Lane l accumulates projection rows
+// r = l, l + 32, ... over the hidden dimension in order c = 0, 1, ... (h read
+// as warp-wide broadcasts, each W row by its own lane).  Centroids then go 32
+// at a time, one per lane: s_k sums p_r * c_kr in order r = 0, 1, ..., with
+// p_r broadcast from its lane, and every lane replays the chunk's scores in k
+// order through the same top-k update.  p and s are the sums a scalar loop
+// over c and r gives, so the results do not depend on the thread layout.
+constexpr int kF32Warps = 8;
+
 template <int DG, bool kScores>
-__global__ void __launch_bounds__(128) assign_f32_kernel(const float* __restrict__ h,
-                                                         const float* __restrict__ W,
-                                                         const float* __restrict__ C,
-                                                         int32_t* __restrict__ gid,
-                                                         float* __restrict__ scores, int B, int n,
-                                                         int D, int K, int A, int topk) {
-  const int tok = blockIdx.x * blockDim.x + threadIdx.x;
-  if (tok >= B * n) return;
+__global__ void __launch_bounds__(32 * kF32Warps) assign_f32_kernel(const float* __restrict__ h,
+                                                                   const float* __restrict__ W,
+                                                                   const float* __restrict__ C,
+                                                                   int32_t* __restrict__ gid,
+                                                                   float* __restrict__ scores, int B, int n,
+                                                                   int D, int K, int A, int topk) {
+  constexpr int kR = (DG + 31) / 32;   // projection rows per lane
+  const int lane = lane_id();
+  const int tok = blockIdx.x * kF32Warps + warp_id();
+  const int a = blockIdx.y;
+  if (tok >= B * n) return;            // the whole warp leaves together
   const int b = tok / n, i = tok % n;
   const float* hr = h + static_cast<size_t>(tok) * D;
-  for (int a = 0; a < A; ++a) {
-    float p[DG];
+  const float* Wa = W + static_cast<size_t>(a) * DG * D;
+  float p[kR];
 #pragma unroll
-    for (int r = 0; r < DG; ++r) p[r] = 0.f;
-    const float* Wa = W + static_cast<size_t>(a) * DG * D;
-    for (int c = 0; c < D; ++c) {
-      const float x = hr[c];
+  for (int q = 0; q < kR; ++q) p[q] = 0.f;
+  const bool vec = (D & 3) == 0 && (reinterpret_cast<uintptr_t>(h) & 15) == 0 &&
+                   (reinterpret_cast<uintptr_t>(W) & 15) == 0;
+  int c = 0;
+  if (vec) {
+    for (; c < D; c += 4) {
+      const float4 x = __ldg(reinterpret_cast<const float4*>(hr + c));
 #pragma unroll
-      for (int r = 0; r < DG; ++r) p[r] = fmaf(__ldg(Wa + static_cast<size_t>(r) * D + c), x, p[r]);
+      for (int q = 0; q < kR; ++q) {
+        const int r = lane + 32 * q;
+        if (r < DG) {
+          const float4 wv = __ldg(reinterpret_cast<const float4*>(Wa + static_cast<size_t>(r) * D + c));
+          p[q] = fmaf(wv.x, x.x, p[q]);
+          p[q] = fmaf(wv.y, x.y, p[q]);
+          p[q] = fmaf(wv.z, x.z, p[q]);
+          p[q] = fmaf(wv.w, x.w, p[q]);
+        }
+      }
     }
-    const float* Ca = C + static_cast<size_t>(a) * K * DG;
-    Top2 t;
-    float* srow = kScores ? scores + ((static_cast<size_t>(b) * A + a) * n + i) * K : nullptr;
-    for (int k = 0; k < K; ++k) {
-      float s = 0.f;
+  }
+  for (; c < D; ++c) {
+    const float x = __ldg(hr + c);
 #pragma unroll
-      for (int r = 0; r < DG; ++r) s = fmaf(p[r], __ldg(Ca + static_cast<size_t>(k) * DG + r), s);
-      if (kScores) srow[k] = s;
-      else t.push(k, s);
+    for (int q = 0; q < kR; ++q) {
+      const int r = lane + 32 * q;
+      if (r < DG) p[q] = fmaf(__ldg(Wa + static_cast<size_t>(r) * D + c), x, p[q]);
     }
-    if (kScores) continue;
+  }
+  const float* Ca = C + static_cast<size_t>(a) * K * DG;
+  float* srow = kScores ? scores + ((static_cast<size_t>(b) * A + a) * n + i) * K : nullptr;
+  Top2 t;
+  for (int k0 = 0; k0 < K; k0 += 32) {
+    const int k = k0 + lane;
+    const float* ck = Ca + static_cast<size_t>(k < K ? k : 0) * DG;
+    float sc = 0.f;
+#pragma unroll
+    for (int r = 0; r < DG; ++r) sc = fmaf(__shfl_sync(0xffffffffu, p[r / 32], r % 32), __ldg(ck + r), sc);
+    if (kScores) {
+      if (k < K) srow[k] = sc;
+    } else {
+      const int nk = min(32, K - k0);
+      for (int j = 0; j < nk; ++j) t.push(k0 + j, __shfl_sync(0xffffffffu, sc, j));
+    }
+  }
+  if (!kScores && lane == 0) {
     int32_t* out = gid + ((static_cast<size_t>(b) * A + a) * n + i) * topk;
     out[0] = t.b1;
     if (topk == 2) out[1] = t.b2;
@@ -591,26 +630,27 @@ cudaError_t launch_tc(const AssignLaunch& L, const CUtensorMap* tm_h, const CUte
 }  // namespace
 
 cudaError_t launch_assign_f32(const AssignLaunch& L, cudaStream_t st) {
-  const int grid = (L.B * L.n + 127) / 128;
+  const dim3 grid((L.B * L.n + kF32Warps - 1) / kF32Warps, L.A);
+  constexpr int kThreadsF32 = 32 * kF32Warps;
   const float* h = static_cast<const float*>(L.h);
   const float* W = static_cast<const float*>(L.W);
   const float* C = static_cast<const float*>(L.C);
   switch (L.d_g) {
     case 16:
-      if (L.scores) assign_f32_kernel<16, true><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk);
-      else assign_f32_kernel<16, false><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk);
+      if (L.scores) assign_f32_kernel<16, true><<<grid, kThreadsF32, 0, st>>>(h, W, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk);
+      else assign_f32_kernel<16, false><<<grid, kThreadsF32, 0, st>>>(h, W, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk);
       break;
     case 32:
-      if (L.scores) assign_f32_kernel<32, true><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk);
-      else assign_f32_kernel<32, false><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk);
+      if (L.scores) assign_f32_kernel<32, true><<<grid, kThreadsF32, 0, st>>>(h, W, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk);
+      else assign_f32_kernel<32, false><<<grid, kThreadsF32, 0, st>>>(h, W, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk);
       break;
     case 64:
-      if (L.scores) assign_f32_kernel<64, true><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk);
-      else assign_f32_kernel<64, false><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk);
+      if (L.scores) assign_f32_kernel<64, true><<<grid, kThreadsF32, 0, st>>>(h, W, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk);
+      else assign_f32_kernel<64, false><<<grid, kThreadsF32, 0, st>>>(h, W, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk);
       break;
     case 128:
-      if (L.scores) assign_f32_kernel<128, true><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk);
-      else assign_f32_kernel<128, false><<<grid, 128, 0, st>>>(h, W, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk);
+      if (L.scores) assign_f32_kernel<128, true><<<grid, kThreadsF32, 0, st>>>(h, W, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk);
+      else assign_f32_kernel<128, false><<<grid, kThreadsF32, 0, st>>>(h, W, C, L.gid, L.scores, L.B, L.n, L.D, L.K, L.A, L.topk);
       break;
     default: return cudaErrorInvalidValue;
   }
