@@ -6,7 +6,9 @@
 // tokens by (group, position) turns each group into a contiguous run of
 // sorted slots, which the group pass then walks as dense tiles.
 //
-// Five small launches per call, all integer work:
+// Five small launches per call (two when a problem has at most 4,096 items
+// and 256 groups: one block per problem does the first four steps in shared
+// memory), all integer work:
 //   count    per (segment, group) histogram of ids          grid (nseg, P)
 //   scan     group counts, offsets, per-segment bases,
 //            per-group tile bases                           grid (P)
@@ -369,6 +371,129 @@ __global__ void __launch_bounds__(1024) index_items_kernel(
   }
 }
 
+// Small problems (n <= kSmallN items, K <= kSmallK groups; one block per
+// problem costs about 2 ns per item, so above a few thousand items the
+// general kernels are faster): count, scan,
+// stable scatter and far lengths of one problem in one block, all in shared
+// memory, so the index is two launches (this and the work list) instead of
+// five.  The results are the same arrays the general kernels write: tokens
+// placed in order of position within each group (chunks of 1,024 in order,
+// warps in order within a chunk, lanes in order within a warp).
+constexpr int kSmallN = 4096;
+constexpr int kSmallK = 256;
+
+__global__ void __launch_bounds__(1024, 1) index_small_kernel(const int32_t* __restrict__ gid, int n, int K,
+                                                           int w_eff, int kshift,
+                                                           int32_t* __restrict__ counts,
+                                                           int32_t* __restrict__ offsets,
+                                                           int32_t* __restrict__ tile_base,
+                                                           int32_t* __restrict__ perm,
+                                                           int32_t* __restrict__ rank,
+                                                           int32_t* __restrict__ farlen_tok,
+                                                           int32_t* __restrict__ farlen_slot, int* err) {
+  extern __shared__ int sm[];
+  int* gs = sm;                 // [n] group of each item
+  int* ps = gs + n;             // [n] perm
+  int* cnt = ps + n;            // [K] counts, then offsets
+  int* tiles = cnt + K;         // [K] tile counts, then tile bases
+  int* run = tiles + K;         // [K + 1] next slot of each group; run[K] = total
+  int* wc = run + K + 1;        // [32][K + 1] per-warp counts of a chunk, then their prefixes
+  const int Kp = K + 1;         // row stride: a group's 32 warp entries fall in 32 banks
+  __shared__ int warp_sums[32];
+  const int p = blockIdx.x;
+  const int lane = lane_id(), warp = warp_id();
+  const unsigned lt = (1u << lane) - 1u;
+  const int32_t* gp = gid + static_cast<size_t>(p) * n;
+  for (int g = threadIdx.x; g < K; g += blockDim.x) cnt[g] = 0;
+  for (int e = threadIdx.x; e < 32 * Kp; e += blockDim.x) wc[e] = 0;
+  __syncthreads();
+  // all of this thread's ids are requested before the first is used
+#pragma unroll 8
+  for (int i = threadIdx.x; i < n; i += blockDim.x) gs[i] = __ldg(gp + i);
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int g = clamp_gid(gs[i], K, err);
+    gs[i] = g;
+    atomicAdd(&cnt[g], 1);
+  }
+  __syncthreads();
+  for (int g = threadIdx.x; g < K; g += blockDim.x) {
+    counts[static_cast<size_t>(p) * K + g] = cnt[g];
+    tiles[g] = (cnt[g] + kTileM - 1) / kTileM;
+  }
+  __syncthreads();
+  const int total = block_scan_smem(cnt, K, warp_sums);    // cnt -> offsets
+  const int ttot = block_scan_smem(tiles, K, warp_sums);   // tiles -> tile bases
+  int32_t* off = offsets + static_cast<size_t>(p) * (K + 1);
+  int32_t* tb = tile_base + static_cast<size_t>(p) * (K + 1);
+  for (int g = threadIdx.x; g < K; g += blockDim.x) {
+    off[g] = cnt[g];
+    tb[g] = tiles[g];
+    run[g] = cnt[g];
+  }
+  if (threadIdx.x == 0) {
+    off[K] = total;
+    tb[K] = ttot;
+    run[K] = total;
+  }
+  __syncthreads();
+  // stable placement, 1,024 items per chunk
+  int32_t* pp = perm + static_cast<size_t>(p) * n;
+  int32_t* rp = rank + static_cast<size_t>(p) * n;
+  for (int c0 = 0; c0 < n; c0 += blockDim.x) {
+    const int i = c0 + threadIdx.x;
+    const bool valid = i < n;
+    const int g = valid ? gs[i] : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, g);
+    if (valid && lane == __ffs(peers) - 1) wc[warp * Kp + g] = __popc(peers);
+    __syncthreads();
+    // per group, a warp scans the 32 warp counts (lane = warp of the chunk)
+    for (int gg = warp; gg < K; gg += 32) {
+      const int v = wc[lane * Kp + gg];
+      int x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      const int base = run[gg];
+      wc[lane * Kp + gg] = base + x - v;
+      __syncwarp();
+      if (lane == 31) run[gg] = base + x;
+    }
+    __syncthreads();
+    if (valid) {
+      const int slot = wc[warp * Kp + g] + __popc(peers & lt);
+      ps[slot] = i;
+      pp[slot] = i;
+      rp[i] = slot;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < 32 * Kp; e += blockDim.x) wc[e] = 0;
+    __syncthreads();
+  }
+  // far lengths: same-group items at positions <= pos - w_eff, searched
+  // within w_eff - 1 slots before s (positions rise along a group's slots)
+  for (int sl = threadIdx.x; sl < n; sl += blockDim.x) {
+    const int item = ps[sl];
+    const int pos = item >> kshift;
+    const int g = gs[item];
+    const int target = pos - w_eff + 1;
+    int lo = max(cnt[g], sl - w_eff + 1), hi = sl;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if ((ps[mid] >> kshift) < target) lo = mid + 1; else hi = mid;
+    }
+    const int fl = lo - cnt[g];
+    farlen_slot[static_cast<size_t>(p) * n + sl] = fl;
+    farlen_tok[static_cast<size_t>(p) * n + item] = fl;
+  }
+}
+
+size_t small_smem(int n, int K) {
+  return (2 * static_cast<size_t>(n) + 3 * static_cast<size_t>(K) + 1 + 32 * (static_cast<size_t>(K) + 1)) * sizeof(int);
+}
+
 // Split top-2 index, far prefixes: for sorted slot s of entry e (token
 // i = e >> 1) in virtual group v = g * K + o, and each other group o' != g
 // (column j = o' - (o' > g)), the members of sub-run (g, o') at positions
@@ -554,17 +679,24 @@ cudaError_t launch_build_index_split(const IndexLaunch& L, int K, int32_t* farle
 cudaError_t launch_build_index(const IndexLaunch& L, cudaStream_t st) {
   const int P = L.P;
   const int nseg = (L.n + kIndexSeg - 1) / kIndexSeg;
-  const size_t sm_count = static_cast<size_t>(L.K) * sizeof(int);
-  index_count_kernel<<<dim3(nseg, P), 256, sm_count, st>>>(L.gid, L.n, L.K, nseg, L.segcnt, L.err);
-  const int staged_s = scan_staged(nseg, L.K);
-  index_scan_kernel<<<P, 1024, scan_smem(nseg, L.K, staged_s), st>>>(
-      L.n, L.K, nseg, staged_s, L.segcnt, L.counts, L.offsets, L.tile_base);
-  const size_t sm_scatter = static_cast<size_t>(L.K) * sizeof(int) + 8 * static_cast<size_t>(L.K) * 2;
-  index_scatter_kernel<<<dim3(nseg, P), 256, sm_scatter, st>>>(L.gid, L.n, L.K, nseg, L.segcnt,
-                                                                L.perm, L.rank, L.err);
-  const size_t sm_far = static_cast<size_t>(L.K + 1) * sizeof(int);
-  index_farlen_kernel<<<dim3((L.n + 255) / 256, P), 256, sm_far, st>>>(
-      L.n, L.K, L.w_eff, L.kshift, L.offsets, L.perm, L.farlen_tok, L.farlen_slot);
+  const bool small = L.n <= kSmallN && L.K <= kSmallK;
+  if (small) {
+    index_small_kernel<<<P, 1024, small_smem(L.n, L.K), st>>>(L.gid, L.n, L.K, L.w_eff, L.kshift, L.counts,
+                                                               L.offsets, L.tile_base, L.perm, L.rank,
+                                                               L.farlen_tok, L.farlen_slot, L.err);
+  } else {
+    const size_t sm_count = static_cast<size_t>(L.K) * sizeof(int);
+    index_count_kernel<<<dim3(nseg, P), 256, sm_count, st>>>(L.gid, L.n, L.K, nseg, L.segcnt, L.err);
+    const int staged_s = scan_staged(nseg, L.K);
+    index_scan_kernel<<<P, 1024, scan_smem(nseg, L.K, staged_s), st>>>(
+        L.n, L.K, nseg, staged_s, L.segcnt, L.counts, L.offsets, L.tile_base);
+    const size_t sm_scatter = static_cast<size_t>(L.K) * sizeof(int) + 8 * static_cast<size_t>(L.K) * 2;
+    index_scatter_kernel<<<dim3(nseg, P), 256, sm_scatter, st>>>(L.gid, L.n, L.K, nseg, L.segcnt,
+                                                                  L.perm, L.rank, L.err);
+    const size_t sm_far = static_cast<size_t>(L.K + 1) * sizeof(int);
+    index_farlen_kernel<<<dim3((L.n + 255) / 256, P), 256, sm_far, st>>>(
+        L.n, L.K, L.w_eff, L.kshift, L.offsets, L.perm, L.farlen_tok, L.farlen_slot);
+  }
   const int nb = (L.n + kTileN - 1) / kTileN + 1;
   const long long tb_ints = static_cast<long long>(P) * (L.K + 1);
   const int staged_i = tb_ints <= kItemsStageInts ? 1 : 0;
@@ -580,6 +712,9 @@ cudaError_t setup_index_kernels() {
   cudaError_t e = cudaFuncSetAttribute(index_scatter_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kMaxK * 4 + 8 * kMaxK * 2);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(index_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(small_smem(kSmallN, kSmallK)));
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(index_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (2 * kMaxK + kScanStageInts) * 4);
