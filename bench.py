@@ -77,6 +77,13 @@ def flush_l2(buf):
     buf.amax()
 
 
+def index_launches(items: int, K: int) -> int:
+    """Kernel launches of one focus_build_index call: two for problems of at
+    most 4,096 items and 256 groups (one block per problem, then the work
+    list), five otherwise."""
+    return 2 if items <= 4096 and K <= 256 else 5
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -479,7 +486,7 @@ def run_ours(args, wl, world, rank, local):
         "e2e": {"value": job_tflops(world, f_attn, t_e2e), "unit": UNIT, "ms_per_step": t_e2e,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "call": "focus_layer_fwd_host (pinned host buffers)"},
-        "gpu_launches": 9 * args.steps,
+        "gpu_launches": (4 + index_launches(wl.n, wl.K)) * args.steps,
         "wall_s_timed_region": wall,
     }
     if rank == 0:
@@ -651,7 +658,7 @@ def run_ours_topk(args, wl, world, rank, local):
         "e2e": {"value": job_tflops(world, f_attn, t_e2e), "unit": UNIT, "ms_per_step": t_e2e,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "call": "pinned host copies + focus_assign_topk, focus_build_index_topk, focus_attention_topk_fwd"},
-        "gpu_launches": (1 + (12 if k == 2 else 5) + (6 if k == 2 else 3)) * args.steps,
+        "gpu_launches": (1 + (12 if k == 2 else index_launches(wl.n * k, wl.K)) + (6 if k == 2 else 3)) * args.steps,
     }
     if rank == 0:
         line["clocks"] = clk.summary()
