@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(256) index_farlen_kernel(int n, int K, int w_e
 }
 
 __global__ void __launch_bounds__(1024) index_items_kernel(
-    int P, int A, int n, int K, int staged, const int32_t* __restrict__ counts,
+    int P, int A, int n, int K, int staged, int cstaged, const int32_t* __restrict__ counts,
     const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_base,
     const int32_t* __restrict__ farlen_slot, focus_item_t* __restrict__ items,
     int32_t* __restrict__ cost, int32_t* __restrict__ order, int32_t* __restrict__ n_items,
@@ -292,6 +292,9 @@ __global__ void __launch_bounds__(1024) index_items_kernel(
   // with `staged` every problem's tile bases are copied to shared memory, so
   // each candidate's search over them reads no global memory
   int* tbs = hist + nb + 1;        // [P][K + 1] when staged
+  // with `cstaged` the items' cost buckets are also kept in shared memory, so
+  // the ordering loop below reads no global memory
+  int* cs = tbs + (staged ? P * (K + 1) : 0);   // [max_items] when cstaged
   if (staged) {
     for (int e = threadIdx.x; e < P * (K + 1); e += blockDim.x) tbs[e] = tile_base[e];
   }
@@ -344,6 +347,7 @@ __global__ void __launch_bounds__(1024) index_items_kernel(
       items[out + pos] = it;
       const int cb = (it.keys + kTileN - 1) / kTileN;
       cost[out + pos] = cb;
+      if (cstaged) cs[out + pos] = cb;
       atomicAdd(&hist[cb], 1);
     }
     out += tot;
@@ -359,9 +363,10 @@ __global__ void __launch_bounds__(1024) index_items_kernel(
   if (warp_id() == 0) {
     const int lane = lane_id();
     const unsigned lt = (1u << lane) - 1u;
+    const int* csrc = cstaged ? cs : cost;
     for (int c0 = 0; c0 < out; c0 += 32) {
       const int c = c0 + lane;
-      const int cb = c < out ? cost[c] : -1;
+      const int cb = c < out ? csrc[c] : -1;
       const unsigned peers = __match_any_sync(0xffffffffu, cb);
       if (c < out) order[hist[cb] + __popc(peers & lt)] = c;
       __syncwarp();
@@ -549,7 +554,7 @@ __global__ void __launch_bounds__(256) index_farlen_split_kernel(int m, int K, i
 // the same compaction and longest-first schedule as index_items_kernel.
 // item.g = virtual group.
 __global__ void __launch_bounds__(1024) index_items_split_kernel(
-    int P, int A, int m, int K, const int32_t* __restrict__ counts,
+    int P, int A, int m, int K, int cstaged, const int32_t* __restrict__ counts,
     const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_base,
     const int32_t* __restrict__ farlen_sub, focus_item_t* __restrict__ items,
     int32_t* __restrict__ cost, int32_t* __restrict__ order, int32_t* __restrict__ n_items,
@@ -561,6 +566,7 @@ __global__ void __launch_bounds__(1024) index_items_split_kernel(
   const int Kv = K * K, nsub = K - 1;
   // cost buckets 0..nb-1: a tile's keys over its sub-runs stay below m + K * kTileN
   const int nb = (m + kTileN - 1) / kTileN + K + 1;
+  int* cs = hist + nb + 1;         // [max_items] cost buckets when cstaged
   if (threadIdx.x == 0) {
     int run = 0;
     for (int p = 0; p < P; ++p) {
@@ -614,6 +620,7 @@ __global__ void __launch_bounds__(1024) index_items_split_kernel(
       items[out + pos] = it;
       const int cb = (it.keys + kTileN - 1) / kTileN;
       cost[out + pos] = cb;
+      if (cstaged) cs[out + pos] = cb;
       atomicAdd(&hist[cb], 1);
     }
     out += tot;
@@ -629,9 +636,10 @@ __global__ void __launch_bounds__(1024) index_items_split_kernel(
   if (warp_id() == 0) {
     const int lane = lane_id();
     const unsigned lt = (1u << lane) - 1u;
+    const int* csrc = cstaged ? cs : cost;
     for (int c0 = 0; c0 < out; c0 += 32) {
       const int c = c0 + lane;
-      const int cb = c < out ? cost[c] : -1;
+      const int cb = c < out ? csrc[c] : -1;
       const unsigned peers = __match_any_sync(0xffffffffu, cb);
       if (c < out) order[hist[cb] + __popc(peers & lt)] = c;
       __syncwarp();
@@ -645,6 +653,7 @@ __global__ void __launch_bounds__(1024) index_items_split_kernel(
 // work-list kernel's [P][K + 1] tile bases.
 constexpr int kScanStageInts = 16384;    // 64 KB
 constexpr int kItemsStageInts = 8192;    // 32 KB
+constexpr int kCostStageInts = 8192;     // 32 KB: the work list's cost buckets
 
 int scan_staged(int nseg, int K) {
   return static_cast<long long>(nseg) * K <= kScanStageInts ? 1 : 0;
@@ -670,8 +679,9 @@ cudaError_t launch_build_index_split(const IndexLaunch& L, int K, int32_t* farle
   index_farlen_split_kernel<<<dim3((L.n + 255) / 256, P), 256, static_cast<size_t>(Kv + 1) * sizeof(int), st>>>(
       L.n, K, L.w_eff, L.offsets, L.perm, farlen_sub, L.farlen_tok, L.farlen_slot);
   const int nb = (L.n + kTileN - 1) / kTileN + K + 1;
-  index_items_split_kernel<<<1, 1024, static_cast<size_t>(P + 1 + nb) * sizeof(int), st>>>(
-      P, L.A, L.n, K, L.counts, L.offsets, L.tile_base, farlen_sub, L.items, L.cost, L.order, L.n_items,
+  const int cst = L.max_items <= kCostStageInts ? 1 : 0;
+  index_items_split_kernel<<<1, 1024, static_cast<size_t>(P + 1 + nb + (cst ? L.max_items : 0)) * sizeof(int), st>>>(
+      P, L.A, L.n, K, cst, L.counts, L.offsets, L.tile_base, farlen_sub, L.items, L.cost, L.order, L.n_items,
       L.max_items, L.err);
   return cudaGetLastError();
 }
@@ -700,8 +710,10 @@ cudaError_t launch_build_index(const IndexLaunch& L, cudaStream_t st) {
   const int nb = (L.n + kTileN - 1) / kTileN + 1;
   const long long tb_ints = static_cast<long long>(P) * (L.K + 1);
   const int staged_i = tb_ints <= kItemsStageInts ? 1 : 0;
-  const size_t sm_items = static_cast<size_t>(P + 1 + nb + (staged_i ? tb_ints : 0)) * sizeof(int);
-  index_items_kernel<<<1, 1024, sm_items, st>>>(P, L.A, L.n, L.K, staged_i, L.counts, L.offsets,
+  const int cst = L.max_items <= kCostStageInts ? 1 : 0;
+  const size_t sm_items =
+      static_cast<size_t>(P + 1 + nb + (staged_i ? tb_ints : 0) + (cst ? L.max_items : 0)) * sizeof(int);
+  index_items_kernel<<<1, 1024, sm_items, st>>>(P, L.A, L.n, L.K, staged_i, cst, L.counts, L.offsets,
                                                 L.tile_base, L.farlen_slot, L.items, L.cost,
                                                 L.order, L.n_items, L.max_items, L.err);
   return cudaGetLastError();
@@ -720,10 +732,10 @@ cudaError_t setup_index_kernels() {
                            (2 * kMaxK + kScanStageInts) * 4);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(index_items_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           160 * 1024 + kItemsStageInts * 4);
+                           160 * 1024 + (kItemsStageInts + kCostStageInts) * 4);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(index_items_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           160 * 1024);
+                           160 * 1024 + kCostStageInts * 4);
   return e;
 }
 
