@@ -10,8 +10,10 @@
 //
 // bf16: the projection is a [128 tokens x A*d_g] tile of h W^T on the
 // tcgen05 tensor cores (TMA-fed pipeline, fp32 accumulator in TMEM); the
-// epilogue reads each token's row of p from TMEM and scores the centroids with
-// fp32 FMAs, so p is never rounded below fp32.  For 32, 64, 128 or 256
+// epilogue reads each token's row of p from TMEM and scores the centroids
+// with fp32 FMAs, or (d_g = 64, K <= 64, persistent kernel) on the tensor
+// cores from p split exactly into three bf16 parts, so p is never rounded
+// below fp32.  For 32, 64, 128 or 256
 // projection columns the kernel is persistent: one CTA per SM streams its
 // token tiles of h through a 4-6 stage TMA ring into double-buffered TMEM
 // accumulators while four epilogue warps score the previous tile; wider
@@ -381,7 +383,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
   uint64_t* empty = full + S;
   uint64_t* tfull = empty + S;      // [2] accumulator complete
   uint64_t* tfree = tfull + 2;      // [2] accumulator read out (4 epilogue warps)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfree + 2);
+  uint64_t* sc_bar = tfree + 2;     // scoring product done (tensor-core scores)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sc_bar + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = warp_id(), lane = lane_id();
@@ -399,6 +402,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
       mbar_init(&tfull[b], 1);
       mbar_init(&tfree[b], 4);
     }
+    mbar_init(sc_bar, 1);
     *abort = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_h);
@@ -479,7 +483,21 @@ __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
     const int kc_max = (Cfg::kCBytes / 4 / DG) & ~31;
     const int kc = min(kc_max, (K + 31) & ~31);
     int staged_a = -1, staged_k0 = -1;
-    for (int unit = blockIdx.x, i = 0; unit < nunits; unit += gridDim.x, ++i) {
+    // d_g = 64 and K <= 64: the scores on the tensor cores instead.  p (fp32)
+    // splits exactly into three bf16 parts, p = hi + mid + lo (each part is
+    // the rounding of what the parts before it leave, and what is left after
+    // two parts has at most 8 significant bits); the three parts go through one
+    // 16 KB operand slab in turn, each multiplied with the centroids (bf16,
+    // exact in the product) into the assignment's own 64 accumulator columns,
+    // which p has been read out of.  Products are exact and accumulate in
+    // fp32, so the scores are fp32 dot products of the fp32 p with the
+    // centroids, summed in the tensor core's order.
+    const bool tc = DG == 64 && K <= 64;
+    uint8_t* As = smem + Cfg::kRing + 1024;   // 128 rows x 128 B, 128-byte swizzle
+    uint8_t* Bs = As + 128 * 128;             // N rows x 128 B: the centroids
+    uint32_t sc_ph = 0;
+    bool fine = true;
+    for (int unit = blockIdx.x, i = 0; unit < nunits && fine; unit += gridDim.x, ++i) {
       const int buf = i & 1;
       // every epilogue thread leaves the loop together, so the named barriers
       // below always see all 128
@@ -499,7 +517,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
 #pragma unroll
           for (int j = 0; j < 32; ++j) p[c + j] = __uint_as_float(r[j]);
         }
-        if (a == A - 1) {
+        if (!tc && a == A - 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&tfree[buf]);   // the accumulator may take tile i + 2
@@ -507,6 +525,90 @@ __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
         const __nv_bfloat16* Ca = C + static_cast<size_t>(pa + a) * K * DG;
         float* srow = kScores && keep ? scores + ((static_cast<size_t>(b) * A_all + pa + a) * n + ti) * K : nullptr;
         Top2 t;
+        if constexpr (DG == 64) {
+          if (tc) {
+            const int N = (K + 15) & ~15;
+            const bool stage_b = staged_a != pa + a;
+            uint4 cw[4];
+            if (stage_b) {
+#pragma unroll
+              for (int f = 0; f < 4; ++f) {
+                const int e = et + 128 * f, k = e >> 3, ch = e & 7;
+                cw[f] = make_uint4(0u, 0u, 0u, 0u);
+                if (k < K) cw[f] = __ldg(reinterpret_cast<const uint4*>(Ca + static_cast<size_t>(k) * 64 + ch * 8));
+              }
+            }
+            for (int part = 0; part < 3 && fine; ++part) {
+              uint32_t w[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const uint32_t v = pack_bf16x2(p[2 * j], p[2 * j + 1]);
+                w[j] = v;
+                p[2 * j] -= __uint_as_float(v << 16);
+                p[2 * j + 1] -= __uint_as_float(v & 0xffff0000u);
+              }
+              if (part == 0 && stage_b) {
+#pragma unroll
+                for (int f = 0; f < 4; ++f) {
+                  const int e = et + 128 * f, k = e >> 3, ch = e & 7;
+                  if (k < N) *reinterpret_cast<uint4*>(Bs + k * 128 + ((ch ^ (k & 7)) << 4)) = cw[f];
+                }
+              }
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4*>(As + row * 128 + ((c ^ (row & 7)) << 4)) =
+                    make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+              fence_proxy_async_smem();
+              tc_fence_before();
+              named_barrier(1, 128);
+              if (et == 0) {
+                tc_fence_after();
+                const uint32_t idn = idesc_bf16_f32(128, N, false, false);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  mma_ss(tmem + buf * NALLOC + a * 64, sw128_desc(smem_u32(As) + kk * 32, 16, 1024),
+                         sw128_desc(smem_u32(Bs) + kk * 32, 16, 1024), idn, (part | kk) != 0);
+                mma_commit(sc_bar);
+              }
+              fine = named_barrier_and(1, 128, mbar_wait(sc_bar, sc_ph & 1, abort, err));
+              ++sc_ph;
+              tc_fence_after();
+            }
+            if (!fine) break;
+            staged_a = pa + a;
+            // the scores: columns k < K of the assignment's accumulator block
+#pragma unroll
+            for (int c = 0; c < 64; c += 32) {
+              if (c < N) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_base + buf * NALLOC + a * 64 + c, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                  const int k = c + j;
+                  if (k < K) {
+                    if (kScores) {
+                      if (srow) srow[k] = __uint_as_float(r[j]);
+                    } else {
+                      t.push(k, __uint_as_float(r[j]));
+                    }
+                  }
+                }
+              }
+            }
+            if (a == A - 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&tfree[buf]);   // the accumulator may take tile i + 2
+            }
+            if (!kScores && keep) {
+              int32_t* out = gid + ((static_cast<size_t>(b) * A_all + pa + a) * n + ti) * topk;
+              out[0] = t.b1;
+              if (topk == 2) out[1] = t.b2;
+            }
+            continue;
+          }
+        }
         for (int k0 = 0; k0 < K; k0 += kc) {
           const int nk = min(kc, K - k0);
           if (staged_a != pa + a || staged_k0 != k0) {
