@@ -570,7 +570,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) assign_stream_kernel(
                          sw128_desc(smem_u32(Bs) + kk * 32, 16, 1024), idn, (part | kk) != 0);
                 mma_commit(sc_bar);
               }
-              fine = named_barrier_and(1, 128, mbar_wait(sc_bar, sc_ph & 1, abort, err));
+              // a short wait: poll with naps (a suspend hint can sleep past the commit)
+              fine = named_barrier_and(1, 128, mbar_wait_nap(sc_bar, sc_ph & 1, abort, err));
               ++sc_ph;
               tc_fence_after();
             }
