@@ -134,9 +134,11 @@ FOCUS_API focus_status_t focus_workspace_init(void* ws, void* stream);
  *   h   [B, n, D]      dtype          W [A, d_g, D] dtype     C [A, K, d_g] dtype
  *   gid [B, A, n]      int32 output
  * bf16 runs the projection on the tensor cores (fp32 accumulate) and needs
- * D % 8 == 0, d_g in {32, 64, 128} and A*d_g <= 512; f32 runs it in fp32 on the
- * CUDA cores and needs d_g in {16, 32, 64, 128}.  Other shapes give
- * FOCUS_ERR_UNSUPPORTED. */
+ * D % 8 == 0, d_g in {32, 64, 128} and A*d_g <= 512; with d_g = 64 and K <= 64
+ * the scores run there too, from p split exactly into three bf16 parts
+ * (exact products, fp32 accumulation in the tensor core's order), otherwise
+ * as fp32 FMAs.  f32 runs everything in fp32 on the CUDA cores and needs d_g
+ * in {16, 32, 64, 128}.  Other shapes give FOCUS_ERR_UNSUPPORTED. */
 FOCUS_API focus_status_t focus_assign(const focus_params_t* p, const void* h, const void* W,
                             const void* C, int32_t* gid, void* ws, size_t ws_bytes,
                             void* stream);
