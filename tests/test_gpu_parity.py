@@ -67,6 +67,8 @@ def _check_index(got, want_idx, want_items, want_order):
     ("bf16", 1, 20000, 256, 64, 16, 1, 1),   # 66-token tiles
     ("bf16", 2, 16500, 128, 32, 8, 2, 2),    # 109-token tiles across the batch boundary
     ("bf16", 1, 20000, 256, 64, 16, 8, 8),   # 512 columns: two passes of four assignments
+    ("bf16", 1, 3000, 256, 64, 37, 1, 1),    # scores on the tensor cores, N = 48 (11 empty centroid rows)
+    ("bf16", 1, 3000, 256, 64, 91, 1, 1),    # d_g = 64 with K > 64: the scores in FMAs
     ("f32", 2, 300, 128, 64, 4, 1, 1),
     ("f32", 1, 77, 96, 16, 9, 2, 2),
 ])
@@ -83,10 +85,12 @@ def test_assign_bit_exact(fz, dtype, B, n, D, d_g, K, A, H_kv):
     assert np.array_equal(gid.cpu().numpy(), x["gid_ref"])
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_assign_ties_go_to_lowest_index(fz, dtype):
+@pytest.mark.parametrize("dtype,d_g", [("bf16", 32), ("f32", 32), ("bf16", 64)])
+def test_assign_ties_go_to_lowest_index(fz, dtype, d_g):
+    # d_g = 64 in bf16 takes the tensor-core scores: identical centroids must
+    # still give identical scores
     import torch
-    wl = synth.Workload("t", B=1, H=1, H_kv=1, n=512, d=64, D=128, d_g=32, K=6, w=4, A=1,
+    wl = synth.Workload("t", B=1, H=1, H_kv=1, n=512, d=64, D=128, d_g=d_g, K=6, w=4, A=1,
                         dtype=dtype, groups="uniform", seed=5)
     x = synth.draw(wl, parts=("assign",))
     C = x["C"].copy()
