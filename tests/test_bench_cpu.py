@@ -66,3 +66,15 @@ def test_traffic_record_only_for_its_workload_and_source(tmp_path):
     assert bench.traffic_record("attn_tc_group_pass", "llama7b_8k", str(path)) is None   # other workload
     assert bench.traffic_record("attn_tc_local_pass", "gqa_32k", str(path)) is None      # source changed
     assert bench.traffic_record("no_such_kernel", "gqa_32k", str(path)) is None
+
+
+def test_layer_launch_count_follows_the_index_form():
+    # the index build is two launches for problems of at most 4,096 items and
+    # 256 groups (one block per problem, then the work list), five otherwise
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.index_launches(256, 4) == 2
+    assert bench.index_launches(4096, 256) == 2
+    assert bench.index_launches(4097, 16) == 5
+    assert bench.index_launches(1024, 257) == 5
+    assert bench.index_launches(32768, 64) == 5
