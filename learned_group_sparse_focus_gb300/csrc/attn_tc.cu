@@ -131,7 +131,7 @@ __device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
   if (lane == 0) mbar_arrive(bar);
 }
 
-// warp-uniform bounded wait (every lane waits; the verdict is shared)
+// warp-uniform bounded wait (every lane waits; the outcome is shared)
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           int* err, unsigned long long limit_ns) {
   const bool ok = mbar_wait(bar, parity, abort, err, limit_ns);

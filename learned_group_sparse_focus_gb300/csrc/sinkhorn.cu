@@ -202,7 +202,7 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
 
-// warp-uniform bounded wait (every lane waits; the verdict is shared)
+// warp-uniform bounded wait (every lane waits; the outcome is shared)
 __device__ __forceinline__ bool all_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err) {
   const bool ok = mbar_wait(bar, parity, abort, err);
   return __all_sync(0xffffffffu, ok);
