@@ -401,8 +401,8 @@ __global__ void __launch_bounds__(1024, 1) index_small_kernel(const int32_t* __r
   int* ps = gs + n;             // [n] perm
   int* cnt = ps + n;            // [K] counts, then offsets
   int* tiles = cnt + K;         // [K] tile counts, then tile bases
-  int* run = tiles + K;         // [K + 1] next slot of each group; run[K] = total
-  int* wc = run + K + 1;        // [32][K + 1] per-warp counts of a chunk, then their prefixes
+  int* run = tiles + K;         // [K] next slot of each group
+  int* wc = run + K;            // [32][K + 1] per-warp counts of a chunk, then their prefixes
   const int Kp = K + 1;         // row stride: a group's 32 warp entries fall in 32 banks
   __shared__ int warp_sums[32];
   const int p = blockIdx.x;
@@ -439,7 +439,6 @@ __global__ void __launch_bounds__(1024, 1) index_small_kernel(const int32_t* __r
   if (threadIdx.x == 0) {
     off[K] = total;
     tb[K] = ttot;
-    run[K] = total;
   }
   __syncthreads();
   // stable placement, 1,024 items per chunk
@@ -496,7 +495,7 @@ __global__ void __launch_bounds__(1024, 1) index_small_kernel(const int32_t* __r
 }
 
 size_t small_smem(int n, int K) {
-  return (2 * static_cast<size_t>(n) + 3 * static_cast<size_t>(K) + 1 + 32 * (static_cast<size_t>(K) + 1)) * sizeof(int);
+  return (2 * static_cast<size_t>(n) + 3 * static_cast<size_t>(K) + 32 * (static_cast<size_t>(K) + 1)) * sizeof(int);
 }
 
 // Split top-2 index, far prefixes: for sorted slot s of entry e (token
